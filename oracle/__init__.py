@@ -1,0 +1,285 @@
+"""CPU oracle for the fused low-precision attention forward pass.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg import this package. The product
+package never imports it, and the C code behind it (``attn_oracle.c``) shares
+nothing with the CUDA library.
+
+The oracle has three parts (see ``attn_oracle.h`` for the page passages):
+
+* O-1 ``attention_fp64``: plain FP64 softmax attention.
+* O-2 ``quantize``: the bit-level rotate-and-quantise emulator (E4M3 token
+  blocks, MXFP8 row/column blocks with E8M0 exponents).
+* O-3 ``attention_emulate``: the running-softmax loop over the quantised
+  operands, tiled by 128 keys as the kernel tiles it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_HDR = os.path.join(_HERE, "attn_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+E4M3_TOKBLOCK, MX_ROW32, MX_COL32 = 0, 1, 2
+MX_RULE_NOSAT, MX_RULE_OCP_FLOOR = 0, 1
+QUANTIZE_P = 1
+
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``oracle/_build/liboracle.so``."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = force or not os.path.exists(_LIB_PATH) or any(
+        os.path.getmtime(p) > os.path.getmtime(_LIB_PATH) for p in (_SRC, _HDR))
+    if stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _QT(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("layout", ctypes.c_int), ("block", ctypes.c_int),
+                ("scales_f32", ctypes.c_void_p), ("scales_u8", ctypes.c_void_p)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            vp, i32, u64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_double
+            L.or_set_threads.argtypes = [i32]
+            L.or_threads.restype = i32
+            L.or_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.or_e4m3_decode.restype = dbl
+            L.or_e4m3_encode.argtypes = [ctypes.c_float]
+            L.or_e4m3_encode.restype = ctypes.c_uint8
+            L.or_e8m0_exponent.argtypes = [ctypes.c_float, i32]
+            L.or_e8m0_exponent.restype = i32
+            L.or_bf16_rne.argtypes = [ctypes.c_float]
+            L.or_bf16_rne.restype = ctypes.c_uint16
+            L.or_e4m3_encode_range.argtypes = [u64, u64, vp]
+            L.or_signs.argtypes = [u64, i32, vp]
+            L.or_fwht_f32.argtypes = [vp, i32]
+            L.or_splitmix64_next.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+            L.or_splitmix64_next.restype = u64
+            L.or_num_blocks.argtypes = [vp, i32, i32, i32]
+            L.or_num_blocks.restype = ctypes.c_long
+            L.or_quantize.argtypes = [vp, i32, i32, i32, vp, i32, i32, i32, i32, u64, i32, vp, vp, vp]
+            L.or_quantize.restype = i32
+            L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
+            L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, i32, vp, i32, vp, vp, vp]
+            L.or_attention_emulate.restype = i32
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _cu(cu_seqlens, T):
+    if cu_seqlens is None:
+        return None, 1
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    assert cu[0] == 0 and cu[-1] == T, "cu_seqlens must run from 0 to T"
+    return cu, len(cu) - 1
+
+
+def set_threads(n: int) -> int:
+    return lib().or_set_threads(int(n))
+
+
+def threads() -> int:
+    return lib().or_threads()
+
+
+# ---- number formats ------------------------------------------------------
+def e4m3_decode_table() -> np.ndarray:
+    L = lib()
+    return np.array([L.or_e4m3_decode(i) for i in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bits = x.view(np.uint32).ravel()
+    out = np.empty(bits.size, dtype=np.uint8)
+    L = lib()
+    for i, b in enumerate(bits):  # scalar path: small arrays only
+        out[i] = L.or_e4m3_encode(ctypes.c_float(np.uint32(b).view(np.float32)))
+    return out.reshape(x.shape)
+
+
+def e4m3_encode_range(start: int, count: int) -> np.ndarray:
+    out = np.empty(count, dtype=np.uint8)
+    lib().or_e4m3_encode_range(start, count, out.ctypes.data)
+    return out
+
+
+def e8m0_exponent(amax: float, rule: int = MX_RULE_NOSAT) -> int:
+    return lib().or_e8m0_exponent(float(amax), rule)
+
+
+def bf16_rne(x: float) -> int:
+    return lib().or_bf16_rne(float(x))
+
+
+def splitmix64_stream(seed: int, n: int) -> list[int]:
+    st = ctypes.c_uint64(seed)
+    return [lib().or_splitmix64_next(ctypes.byref(st)) for _ in range(n)]
+
+
+def signs(seed: int, d: int) -> np.ndarray:
+    s = np.empty(d, dtype=np.float32)
+    lib().or_signs(seed, d, s.ctypes.data)
+    return s
+
+
+def fwht(x) -> np.ndarray:
+    y = np.array(x, dtype=np.float32, copy=True)
+    flat = y.reshape(-1, y.shape[-1])
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        lib().or_fwht_f32(row.ctypes.data, row.size)
+        flat[r] = row
+    return flat.reshape(y.shape)
+
+
+def num_blocks(cu_seqlens, T: int, block: int) -> int:
+    cu, nd = _cu(cu_seqlens, T)
+    return lib().or_num_blocks(_ptr(cu), nd, T, block)
+
+
+# ---- O-2 -------------------------------------------------------------------
+def quantize(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, seed=0,
+             mx_rule=MX_RULE_NOSAT):
+    """Quantise x [T, H, d] (fp32 values). Returns (codes u8 [T,H,d], scales, status).
+
+    scales: E4M3 token blocks -> fp32 [H, NB]; MX row32 -> u8 [T, H, d/32];
+    MX col32 -> u8 [H, NG, d] (NG = document-local 32-token groups).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    T, H, d = x.shape
+    cu, nd = _cu(cu_seqlens, T)
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    sf = su = None
+    if layout == E4M3_TOKBLOCK:
+        sf = np.zeros((H, num_blocks(cu, T, block)), dtype=np.float32)
+    elif layout == MX_ROW32:
+        su = np.zeros((T, H, d // 32), dtype=np.uint8)
+    elif layout == MX_COL32:
+        su = np.zeros((H, num_blocks(cu, T, 32), d), dtype=np.uint8)
+    else:
+        raise ValueError(layout)
+    st = lib().or_quantize(x.ctypes.data, T, H, d, _ptr(cu), nd, layout, block, int(bool(rotate)),
+                           seed & (2**64 - 1), mx_rule, codes.ctypes.data, _ptr(sf), _ptr(su))
+    return codes, (sf if sf is not None else su), st
+
+
+class QTensor:
+    """Quantised operand as the oracle produces it (logical scale layouts)."""
+
+    def __init__(self, codes, scales, layout, block=128, rotated=False, seed=0):
+        self.codes, self.scales, self.layout, self.block = codes, scales, layout, block
+        self.rotated, self.seed = rotated, seed
+
+    def _qt(self):
+        sf = self.scales if self.layout == E4M3_TOKBLOCK else None
+        su = self.scales if self.layout != E4M3_TOKBLOCK else None
+        return _QT(self.codes.ctypes.data, self.layout, self.block, _ptr(sf), _ptr(su))
+
+
+def quantize_tensor(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, seed=0,
+                    mx_rule=MX_RULE_NOSAT) -> QTensor:
+    codes, scales, st = quantize(x, cu_seqlens, layout, block, rotate, seed, mx_rule)
+    if st != 0:
+        raise FloatingPointError(f"oracle quantiser status {st}")
+    return QTensor(codes, scales, layout, block, rotate, seed)
+
+
+def dequantize(qt: QTensor, cu_seqlens=None) -> np.ndarray:
+    """Decoded values code * scale in fp64 (rotation not undone)."""
+    dec = e4m3_decode_table()
+    T, H, d = qt.codes.shape
+    v = dec[qt.codes]
+    cu, nd = _cu(cu_seqlens, T)
+    starts = np.zeros(T, dtype=np.int64)
+    docs = np.zeros(T, dtype=np.int64)
+    bounds = cu if cu is not None else np.array([0, T], dtype=np.int32)
+    for i in range(len(bounds) - 1):
+        docs[bounds[i]:bounds[i + 1]] = i
+        starts[bounds[i]:bounds[i + 1]] = bounds[i]
+    local = np.arange(T) - starts
+    if qt.layout == E4M3_TOKBLOCK:
+        b = qt.block
+        nblk = [(int(bounds[i + 1] - bounds[i]) + b - 1) // b for i in range(len(bounds) - 1)]
+        boff = np.concatenate([[0], np.cumsum(nblk)])[:-1]
+        idx = boff[docs] + local // b                      # [T]
+        sc = qt.scales[:, idx].T                           # [T, H]
+        return v * sc[:, :, None].astype(np.float64)
+    if qt.layout == MX_ROW32:
+        X = qt.scales.astype(np.int64) - 127               # [T, H, d/32]
+        return v * np.ldexp(1.0, np.repeat(X, 32, axis=2))
+    ng = [(int(bounds[i + 1] - bounds[i]) + 31) // 32 for i in range(len(bounds) - 1)]
+    goff = np.concatenate([[0], np.cumsum(ng)])[:-1]
+    gidx = goff[docs] + local // 32                        # [T]
+    X = qt.scales[:, gidx, :].transpose(1, 0, 2).astype(np.int64) - 127   # [T, H, d]
+    return v * np.ldexp(1.0, X)
+
+
+# ---- O-1 -------------------------------------------------------------------
+def attention_fp64(q, k, v, cu_seqlens=None, causal=False, softmax_scale=None, rows=None):
+    """FP64 attention. Returns (o [R, H, d] fp64, lse [H, R] fp64)."""
+    q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
+    T, H, d = q.shape
+    cu, nd = _cu(cu_seqlens, T)
+    scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    R = T if r is None else len(r)
+    o = np.zeros((R, H, d), dtype=np.float64)
+    lse = np.zeros((H, R), dtype=np.float64)
+    lib().or_attention_fp64(q.ctypes.data, k.ctypes.data, v.ctypes.data, T, H, d, _ptr(cu), nd,
+                            int(bool(causal)), scale, _ptr(r), R, o.ctypes.data, lse.ctypes.data)
+    return o, lse
+
+
+# ---- O-3 -------------------------------------------------------------------
+def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causal=False,
+                      exact=False, softmax_scale=None, rows=None, quantize_p=True):
+    """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R])."""
+    T, H, d = q.codes.shape
+    if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
+        raise ValueError("Q and K must carry the same rotation")
+    cu, nd = _cu(cu_seqlens, T)
+    scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    R = T if r is None else len(r)
+    o = np.zeros((R, H, d), dtype=np.float32)
+    ob = np.zeros((R, H, d), dtype=np.uint16)
+    lse = np.zeros((H, R), dtype=np.float32)
+    qq, kk, vv = q._qt(), k._qt(), v._qt()
+    st = lib().or_attention_emulate(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
+                                    _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
+                                    int(bool(q.rotated)), scale, QUANTIZE_P if quantize_p else 0,
+                                    _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data)
+    if st != 0:
+        raise ValueError(f"oracle emulation rejected its arguments (status {st})")
+    return o, ob, lse
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)

@@ -1,0 +1,559 @@
+/*
+ * attn_oracle.c -- CPU oracle for the fused low-precision attention forward pass.
+ *
+ * TEST INFRASTRUCTURE (see attn_oracle.h): plain, slow, obviously correct C.
+ * Compiled with -ffp-contract=off so that every float expression rounds the
+ * way it is written. Shares no code with the CUDA library.
+ *
+ * Readings of the pages where they are silent are stated beside the code that
+ * takes them; each is also listed in the repository's design notes.
+ */
+#define _GNU_SOURCE
+#include "attn_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------- */
+/* threads                                                                   */
+/* ------------------------------------------------------------------------- */
+static int g_threads = 0;
+
+int or_set_threads(int n) { g_threads = n > 0 ? n : 0; return or_threads(); }
+
+int or_threads(void) {
+    if (g_threads > 0) return g_threads;
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    return c > 0 ? (int)c : 1;
+}
+
+typedef void (*unit_fn)(void* ctx, long unit);
+typedef struct { unit_fn fn; void* ctx; long n; long next; } pool_t;
+
+static void* pool_worker(void* arg) {
+    pool_t* p = (pool_t*)arg;
+    for (;;) {
+        long u = __atomic_fetch_add(&p->next, 1, __ATOMIC_RELAXED);
+        if (u >= p->n) break;
+        p->fn(p->ctx, u);
+    }
+    return NULL;
+}
+
+static void parallel_for(long n, unit_fn fn, void* ctx) {
+    int nt = or_threads();
+    if (nt > 256) nt = 256;
+    if (nt > n) nt = (int)n;
+    pool_t p = {fn, ctx, n, 0};
+    if (nt <= 1) { pool_worker(&p); return; }
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 0; i < nt - 1; i++)
+        if (pthread_create(&th[started], NULL, pool_worker, &p) == 0) started++;
+    pool_worker(&p);
+    for (int i = 0; i < started; i++) pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------------------------------- */
+/* E4M3 ("Fused attention kernel", 8-bit forward pass: the e4m3 format).     */
+/* The pages name the format only; the OCP 8-bit floating point definition   */
+/* (E4M3FN) is taken: sign, 4 exponent bits with bias 7, 3 mantissa bits, no */
+/* infinities, S.1111.111 is NaN, largest finite 448, subnormals 2^-9 apart. */
+/* ------------------------------------------------------------------------- */
+double or_e4m3_decode(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9)            /* m/8 * 2^-6        */
+                        : ldexp(8.0 + m, e - 10);         /* (1+m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* round half to even of a non-negative double that is exact */
+static double rne_int(double q) {
+    double n = floor(q);
+    double f = q - n;
+    if (f > 0.5 || (f == 0.5 && fmod(n, 2.0) != 0.0)) n += 1.0;
+    return n;
+}
+
+/* Round to nearest, ties to even; finite values beyond 448 and infinities
+ * saturate to +-448 (reading: the "satfinite" conversion); NaN -> 0x7F. */
+uint8_t or_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < 0.015625) {                         /* below 2^-6: subnormal grid 2^-9 */
+        double n = rne_int(a * 512.0);          /* exact scaling by a power of two */
+        return sign | (uint8_t)n;               /* n == 8 is the smallest normal, 0x08 */
+    }
+    int e;
+    double f = frexp(a, &e);                    /* a = f * 2^e, f in [0.5, 1) */
+    int E = e - 1;                              /* a = (2f) * 2^E, 2f in [1, 2) */
+    double n = rne_int((2.0 * f - 1.0) * 8.0);  /* mantissa in eighths, exact */
+    if (n >= 8.0) { E += 1; n = 0.0; }
+    int code = ((E + 7) << 3) | (int)n;
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+void or_e4m3_encode_range(uint64_t start, uint64_t count, uint8_t* out) {
+    for (uint64_t i = 0; i < count; i++) {
+        uint32_t bits = (uint32_t)(start + i);
+        float x;
+        memcpy(&x, &bits, 4);
+        out[i] = or_e4m3_encode(x);
+    }
+}
+
+/* E8M0 shared exponent of a 32-element MX block (FLAMIA, section 2:
+ * microscaling formats use 32-element blocks with one shared scale).
+ * The pages do not fix the exponent rule. Default reading: the smallest X with
+ * amax <= 448 * 2^X, so that no element saturates; with amax = m * 2^E,
+ * m in [1, 2): X = E - 8 if m <= 1.75 (448 = 1.75 * 2^8) else E - 7.
+ * The OCP MX floor rule X = E - 8 is kept as a switch. amax == 0 -> -127. */
+int or_e8m0_exponent(float amax, int rule) {
+    if (!(amax > 0.0f)) return -127;
+    int e;
+    double f = frexp((double)amax, &e);
+    int E = e - 1;
+    double m = 2.0 * f;
+    int X = (rule == OR_MX_RULE_OCP_FLOOR) ? E - 8 : (m <= 1.75 ? E - 8 : E - 7);
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    return X;
+}
+
+/* fp32 -> bf16, round to nearest even (the output format: BF16) */
+uint16_t or_bf16_rne(float x) {
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Rotation ("Fused attention kernel", 8-bit forward pass: incoherent        */
+/* processing multiplies Q and K by a random sign diagonal and a Hadamard    */
+/* matrix; the product cancels in Q K^T).                                    */
+/* Readings: the signs are the top bits of a SplitMix64 stream (Steele, Lea, */
+/* Flood 2014) started at the seed; the Hadamard matrix is the unnormalised  */
+/* Sylvester one (H H^T = d I), applied as a fast Walsh-Hadamard transform   */
+/* with stages h = 1, 2, 4, ..., d/2 in that order, each butterfly           */
+/* (a, b) -> (a + b, a - b) rounded to fp32. The 1/d is left to the score    */
+/* scale.                                                                    */
+/* ------------------------------------------------------------------------- */
+uint64_t or_splitmix64_next(uint64_t* state) {
+    uint64_t z = (*state += 0x9E3779B97F4A7C15ULL);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+void or_signs(uint64_t seed, int d, float* s) {
+    uint64_t st = seed;
+    for (int j = 0; j < d; j++) s[j] = (or_splitmix64_next(&st) >> 63) ? -1.0f : 1.0f;
+}
+
+void or_fwht_f32(float* x, int d) {
+    for (int h = 1; h < d; h <<= 1)
+        for (int i = 0; i < d; i++)
+            if (!(i & h)) {
+                float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+}
+
+/* ------------------------------------------------------------------------- */
+/* documents (FLAMIA abstract and section 4.1: packed documents, scales kept */
+/* document-local, no repacking). cu_seqlens == NULL means one document.     */
+/* ------------------------------------------------------------------------- */
+static int doc_of(const int32_t* cu, int nd, int t) {
+    int lo = 0, hi = nd - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+long or_num_blocks(const int32_t* cu, int nd, int T, int block) {
+    if (!cu) return (T + block - 1) / block;
+    long n = 0;
+    for (int i = 0; i < nd; i++) n += (cu[i + 1] - cu[i] + block - 1) / block;
+    return n;
+}
+
+typedef struct { int nd; int32_t* cu; } docs_t;
+
+static docs_t docs_make(const int32_t* cu, int nd, int T) {
+    docs_t D;
+    if (!cu) { nd = 1; }
+    D.nd = nd;
+    D.cu = (int32_t*)malloc(sizeof(int32_t) * (nd + 1));
+    if (!cu) { D.cu[0] = 0; D.cu[1] = T; }
+    else memcpy(D.cu, cu, sizeof(int32_t) * (nd + 1));
+    return D;
+}
+
+/* block offset of document `doc` for blocks of `block` tokens */
+static long block_offset(const docs_t* D, int doc, int block) {
+    long n = 0;
+    for (int i = 0; i < doc; i++) n += (D->cu[i + 1] - D->cu[i] + block - 1) / block;
+    return n;
+}
+
+/* ------------------------------------------------------------------------- */
+/* O-2 quantiser                                                             */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const float* x; int T, H, d; docs_t D;
+    int layout, block, rotate, mx_rule;
+    float signs[256];
+    uint8_t* codes; float* sf; uint8_t* su;
+    int err;
+} quant_ctx;
+
+static void rotated_row(const quant_ctx* c, int t, int h, float* y) {
+    const float* src = c->x + ((long)t * c->H + h) * c->d;
+    for (int j = 0; j < c->d; j++) y[j] = c->rotate ? c->signs[j] * src[j] : src[j];
+    if (c->rotate) or_fwht_f32(y, c->d);
+}
+
+/* E4M3 token block (reading: scale = amax / 448 with IEEE division, codes from
+ * y * (448 / amax); blocks start at the document start, the last one may be
+ * partial; amax == 0 gives scale 0 and zero codes; a non-finite amax is an
+ * error). Unit = (document, head). */
+static void quant_tokblock_unit(void* vc, long u) {
+    quant_ctx* c = (quant_ctx*)vc;
+    int doc = (int)(u / c->H), h = (int)(u % c->H);
+    int s = c->D.cu[doc], L = c->D.cu[doc + 1] - s, d = c->d, b = c->block;
+    long boff = block_offset(&c->D, doc, b);
+    long NB = block_offset(&c->D, c->D.nd, b);
+    float* y = (float*)malloc(sizeof(float) * (size_t)b * d);
+    for (int blk = 0; blk * b < L; blk++) {
+        int n = L - blk * b < b ? L - blk * b : b;
+        float amax = 0.0f;
+        for (int r = 0; r < n; r++) {
+            rotated_row(c, s + blk * b + r, h, y + (long)r * d);
+            for (int j = 0; j < d; j++) {
+                float a = fabsf(y[(long)r * d + j]);
+                if (!(a <= amax)) amax = a;        /* NaN propagates */
+            }
+        }
+        float scale, inv;
+        if (!isfinite(amax)) { __atomic_store_n(&c->err, OR_ERR_NONFINITE, __ATOMIC_RELAXED); scale = NAN; inv = 0.0f; }
+        else if (amax == 0.0f) { scale = 0.0f; inv = 0.0f; }
+        else { inv = 448.0f / amax; scale = amax / 448.0f; }
+        c->sf[(long)h * NB + boff + blk] = scale;
+        for (int r = 0; r < n; r++) {
+            uint8_t* dst = c->codes + ((long)(s + blk * b + r) * c->H + h) * d;
+            for (int j = 0; j < d; j++) dst[j] = or_e4m3_encode(y[(long)r * d + j] * inv);
+        }
+    }
+    free(y);
+}
+
+static float pow2f_exact(int k) { return ldexpf(1.0f, k); }
+
+/* MX row32: one E8M0 exponent per (token, head, 32 consecutive channels);
+ * codes = E4M3(y * 2^-X). Unit = token. */
+static void quant_mxrow_unit(void* vc, long t) {
+    quant_ctx* c = (quant_ctx*)vc;
+    int d = c->d;
+    float y[256];
+    for (int h = 0; h < c->H; h++) {
+        rotated_row(c, (int)t, h, y);
+        for (int g = 0; g < d / 32; g++) {
+            float amax = 0.0f;
+            for (int j = 0; j < 32; j++) { float a = fabsf(y[g * 32 + j]); if (!(a <= amax)) amax = a; }
+            if (!isfinite(amax)) __atomic_store_n(&c->err, OR_ERR_NONFINITE, __ATOMIC_RELAXED);
+            int X = or_e8m0_exponent(amax, c->mx_rule);
+            c->su[((long)t * c->H + h) * (d / 32) + g] = (uint8_t)(X + 127);
+            float pw = pow2f_exact(-X);
+            uint8_t* dst = c->codes + ((long)t * c->H + h) * d + g * 32;
+            for (int j = 0; j < 32; j++) dst[j] = or_e4m3_encode(y[g * 32 + j] * pw);
+        }
+    }
+}
+
+/* MX col32 (V): one E8M0 exponent per (32 document-local tokens, head,
+ * channel), the blocks running along the sequence, which is the contraction
+ * axis of P V. Unit = (document, head). */
+static void quant_mxcol_unit(void* vc, long u) {
+    quant_ctx* c = (quant_ctx*)vc;
+    int doc = (int)(u / c->H), h = (int)(u % c->H);
+    int s = c->D.cu[doc], L = c->D.cu[doc + 1] - s, d = c->d;
+    long goff = block_offset(&c->D, doc, 32);
+    long NG = block_offset(&c->D, c->D.nd, 32);
+    float y[32][256];
+    for (int g = 0; g * 32 < L; g++) {
+        int n = L - g * 32 < 32 ? L - g * 32 : 32;
+        for (int r = 0; r < n; r++) rotated_row(c, s + g * 32 + r, h, y[r]);
+        for (int j = 0; j < d; j++) {
+            float amax = 0.0f;
+            for (int r = 0; r < n; r++) { float a = fabsf(y[r][j]); if (!(a <= amax)) amax = a; }
+            if (!isfinite(amax)) __atomic_store_n(&c->err, OR_ERR_NONFINITE, __ATOMIC_RELAXED);
+            int X = or_e8m0_exponent(amax, c->mx_rule);
+            c->su[((long)h * NG + goff + g) * d + j] = (uint8_t)(X + 127);
+            float pw = pow2f_exact(-X);
+            for (int r = 0; r < n; r++)
+                c->codes[((long)(s + g * 32 + r) * c->H + h) * d + j] = or_e4m3_encode(y[r][j] * pw);
+        }
+    }
+}
+
+int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
+                int layout, int block, int rotate, uint64_t seed, int mx_rule,
+                uint8_t* codes, float* scales_f32, uint8_t* scales_u8) {
+    if (d < 1 || d > 256 || (d & (d - 1)) || T < 0 || H < 1) return OR_ERR_ARG;
+    if (layout == OR_E4M3_TOKBLOCK && (block < 1 || !scales_f32)) return OR_ERR_ARG;
+    if ((layout == OR_MX_ROW32 || layout == OR_MX_COL32) && (d % 32 || !scales_u8)) return OR_ERR_ARG;
+    quant_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.x = x; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
+    c.layout = layout; c.block = block; c.rotate = rotate; c.mx_rule = mx_rule;
+    c.codes = codes; c.sf = scales_f32; c.su = scales_u8;
+    or_signs(seed, d, c.signs);
+    if (layout == OR_E4M3_TOKBLOCK) parallel_for((long)c.D.nd * H, quant_tokblock_unit, &c);
+    else if (layout == OR_MX_ROW32) parallel_for(T, quant_mxrow_unit, &c);
+    else if (layout == OR_MX_COL32) parallel_for((long)c.D.nd * H, quant_mxcol_unit, &c);
+    else { free(c.D.cu); return OR_ERR_ARG; }
+    free(c.D.cu);
+    return c.err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* O-1: FP64 softmax attention, the plain definition. Per document and head: */
+/* S = scale * Q K^T; causal masks key j > query i (positions local to the   */
+/* document, top-left aligned); O = softmax(S) V; lse = max + log(sum).       */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const double *q, *k, *v; int T, H, d; docs_t D; int causal; double scale;
+    const int32_t* rows; int nrows; double *o, *lse;
+} fp64_ctx;
+
+static void fp64_unit(void* vc, long u) {
+    fp64_ctx* c = (fp64_ctx*)vc;
+    int ri = (int)(u / c->H), h = (int)(u % c->H), d = c->d, H = c->H;
+    int t = c->rows ? c->rows[ri] : ri;
+    int doc = doc_of(c->D.cu, c->D.nd, t);
+    int s0 = c->D.cu[doc], L = c->D.cu[doc + 1] - s0, i = t - s0;
+    int nk = c->causal ? i + 1 : L;
+    double* sc = (double*)malloc(sizeof(double) * (nk > 0 ? nk : 1));
+    const double* qr = c->q + ((long)t * H + h) * d;
+    double m = -INFINITY;
+    for (int j = 0; j < nk; j++) {
+        const double* kr = c->k + ((long)(s0 + j) * H + h) * d;
+        double acc = 0.0;
+        for (int x = 0; x < d; x++) acc += qr[x] * kr[x];
+        sc[j] = c->scale * acc;
+        if (sc[j] > m) m = sc[j];
+    }
+    double l = 0.0;
+    double* out = c->o + ((long)ri * H + h) * d;
+    for (int x = 0; x < d; x++) out[x] = 0.0;
+    for (int j = 0; j < nk; j++) {
+        double p = exp(sc[j] - m);
+        l += p;
+        const double* vr = c->v + ((long)(s0 + j) * H + h) * d;
+        for (int x = 0; x < d; x++) out[x] += p * vr[x];
+    }
+    for (int x = 0; x < d; x++) out[x] = nk > 0 ? out[x] / l : 0.0;
+    c->lse[(long)h * c->nrows + ri] = nk > 0 ? m + log(l) : -INFINITY;
+    free(sc);
+}
+
+void or_attention_fp64(const double* q, const double* k, const double* v, int T, int H, int d,
+                       const int32_t* cu, int nd, int causal, double scale,
+                       const int32_t* rows, int nrows, double* o, double* lse) {
+    fp64_ctx c = {q, k, v, T, H, d, docs_make(cu, nd, T), causal, scale, rows, rows ? nrows : T, o, lse};
+    parallel_for((long)c.nrows * H, fp64_unit, &c);
+    free(c.D.cu);
+}
+
+/* ------------------------------------------------------------------------- */
+/* O-3: the running-softmax loop over quantised operands, the way the kernel */
+/* tiles it ("Fused attention kernel", Implementation sketch: running max m, */
+/* rescale alpha = exp(m_old - m_new) applied to the old output, every key   */
+/* block scored, one normalisation at the end, lse = m + log l).             */
+/*                                                                           */
+/* Per query row, key tiles of 128 document-local keys in ascending order:   */
+/*   S_t   = fl32(sum_c qhat_c khat_c)      (fp64 sum, one rounding: the     */
+/*           tensor core's fp32 accumulation, up to its summation order)      */
+/*   s'_t  = fl32(S_t * fl32(qs * ks_t * C)), C = softmax_scale*log2(e)/d for  */
+/*           rotated Q, K (H H^T = d I) and softmax_scale*log2(e) otherwise;  */
+/*           E4M3 layouts multiply the block scales here, MX layouts carry    */
+/*           them inside qhat, khat ("folding score scales", FLAMIA 4.3)      */
+/*   masked keys (causal t > i, keys past the document end): s' = -inf        */
+/*   m'    = max(m, max_t s'_t); alpha = fl32(2^(m - m'))                     */
+/*   pt_t  = 2^(s'_t - m' + 8)              (probabilities prescaled by 2^8)  */
+/*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = V block scale / reference   */
+/*                                          (E4M3 layouts), 1 (MX layouts)    */
+/*   l     = fl32(alpha l + fl32(sum_t pt_t))                                 */
+/*   O_c   = fl32(alpha O_c + fl32(sum_t Phat_t vhat_tc))                     */
+/* End: O = fl32(O * fl32(ref / l)), lse = ln2 * (m + log2 l - 8), O -> bf16. */
+/* vhat = V code (E4M3 layouts; its scale enters through r_t and ref) or     */
+/* code * 2^X (MX col32: the block-scaled MMA applies V's exponents).        */
+/* ref = max over the document's V blocks (default), or, in the causal-exact */
+/* mode, max of the V token scales at positions <= i, so that no later token */
+/* reaches row i (FLAMIA 1 and 4.5: exact options remove within-block        */
+/* dependencies).                                                            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const or_qtensor *q, *k, *v; int T, H, d; docs_t D; int causal, exact, rotated; double scale;
+    int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse;
+    double dec[256];
+    long nbq, nbk, nbv, ngv;     /* block counts of the logical scale arrays */
+    int h;                       /* head being evaluated */
+    double *kh, *vh;             /* dequantised K and V of head h, [T][d] */
+} emu_ctx;
+
+/* dequantised element: code value, times 2^X for the MX layouts (the E4M3
+ * layouts return the bare code value; their scale is applied per block) */
+static double hat(const emu_ctx* c, const or_qtensor* x, int t, int h, int j, long ng) {
+    uint8_t code = x->codes[((long)t * c->H + h) * c->d + j];
+    double v = c->dec[code];
+    if (x->layout == OR_MX_ROW32) {
+        int X = (int)x->scales_u8[((long)t * c->H + h) * (c->d / 32) + j / 32] - 127;
+        v = ldexp(v, X);
+    } else if (x->layout == OR_MX_COL32) {
+        int doc = doc_of(c->D.cu, c->D.nd, t);
+        long g = block_offset(&c->D, doc, 32) + (t - c->D.cu[doc]) / 32;
+        int X = (int)x->scales_u8[((long)h * ng + g) * c->d + j] - 127;
+        v = ldexp(v, X);
+    }
+    return v;
+}
+
+static void emu_decode_unit(void* vc, long t) {
+    emu_ctx* c = (emu_ctx*)vc;
+    for (int j = 0; j < c->d; j++) {
+        c->kh[t * c->d + j] = hat(c, c->k, (int)t, c->h, j, 0);
+        c->vh[t * c->d + j] = hat(c, c->v, (int)t, c->h, j, c->ngv);
+    }
+}
+
+static void emu_unit(void* vc, long ri) {
+    emu_ctx* c = (emu_ctx*)vc;
+    int h = c->h, d = c->d;
+    int t = c->rows ? c->rows[ri] : (int)ri;
+    int doc = doc_of(c->D.cu, c->D.nd, t);
+    int s0 = c->D.cu[doc], L = c->D.cu[doc + 1] - s0, i = t - s0;
+    const or_qtensor *Q = c->q, *K = c->k, *V = c->v;
+    int mx = (Q->layout == OR_MX_ROW32);
+    int vmx = (V->layout == OR_MX_COL32);
+    double C = c->scale * 1.4426950408889634 / (c->rotated ? (double)d : 1.0);
+    float C32 = (float)C;
+
+    double qh[256];
+    for (int j = 0; j < d; j++) qh[j] = hat(c, Q, t, h, j, 0);
+    float qs = 1.0f;
+    const float *ks_row = NULL, *vs_row = NULL;
+    int kb = 1, vb = 1;
+    if (!mx) {
+        qs = Q->scales_f32[(long)h * c->nbq + block_offset(&c->D, doc, Q->block) + i / Q->block];
+        ks_row = K->scales_f32 + (long)h * c->nbk + block_offset(&c->D, doc, K->block);
+        kb = K->block;
+    }
+    /* V reference for the E4M3 layouts */
+    float ref = 1.0f;
+    if (!vmx) {
+        vs_row = V->scales_f32 + (long)h * c->nbv + block_offset(&c->D, doc, V->block);
+        vb = V->block;
+        int nblk = (L + vb - 1) / vb;
+        int last = c->exact ? i / vb : nblk - 1;
+        float mxv = 0.0f;
+        for (int b = 0; b <= last; b++) if (vs_row[b] > mxv) mxv = vs_row[b];
+        ref = mxv;
+    }
+
+    float m = -INFINITY, l = 0.0f;
+    float O[256];
+    for (int x = 0; x < d; x++) O[x] = 0.0f;
+    int nkeys = c->causal ? i + 1 : L;
+    int ntiles = (nkeys + 127) / 128;
+    float sp[128];
+    double ph[128];
+    for (int jt = 0; jt < ntiles; jt++) {
+        int k0 = jt * 128, kn = (nkeys - k0) < 128 ? nkeys - k0 : 128;
+        float mt = -INFINITY;
+        for (int a = 0; a < kn; a++) {
+            const double* kr = c->kh + (long)(s0 + k0 + a) * d;
+            double acc = 0.0;
+            for (int j = 0; j < d; j++) acc += qh[j] * kr[j];
+            float S = (float)acc;
+            float sc;
+            if (mx) sc = S * C32;
+            else sc = S * (float)((double)qs * (double)ks_row[(k0 + a) / kb] * C);
+            sp[a] = sc;
+            if (sc > mt) mt = sc;
+        }
+        float mnew = mt > m ? mt : m;
+        float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
+        double rowsum = 0.0;
+        for (int a = 0; a < kn; a++) {
+            double pt = exp2((double)sp[a] - (double)mnew + 8.0);
+            rowsum += pt;
+            double r = 1.0;
+            if (!vmx) {
+                float sv = vs_row[(k0 + a) / vb];
+                r = (sv > 0.0f && ref > 0.0f) ? (double)(sv / ref) : 1.0;
+            }
+            float pr = (float)(pt * r);
+            ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[or_e4m3_encode(pr)] : (double)pr;
+        }
+        l = alpha * l + (float)rowsum;
+        for (int x = 0; x < d; x++) {
+            double acc = 0.0;
+            for (int a = 0; a < kn; a++) acc += ph[a] * c->vh[(long)(s0 + k0 + a) * d + x];
+            O[x] = alpha * O[x] + (float)acc;
+        }
+        m = mnew;
+    }
+    float fin = (l > 0.0f) ? (float)((double)ref / (double)l) : 0.0f;
+    float* out = c->o + ((long)ri * c->H + h) * d;
+    for (int x = 0; x < d; x++) {
+        out[x] = O[x] * fin;
+        if (c->ob) c->ob[((long)ri * c->H + h) * d + x] = or_bf16_rne(out[x]);
+    }
+    c->lse[(long)h * c->nrows + ri] =
+        (l > 0.0f) ? (float)(0.6931471805599453 * ((double)m + log2((double)l) - 8.0)) : -INFINITY;
+}
+
+int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
+                         int T, int H, int d, const int32_t* cu, int nd,
+                         int causal, int exact, int rotated, double scale, int flags,
+                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse) {
+    if (d < 1 || d > 256) return OR_ERR_ARG;
+    int mxq = q->layout == OR_MX_ROW32, mxk = k->layout == OR_MX_ROW32;
+    if (mxq != mxk) return OR_ERR_ARG;
+    if (q->layout == OR_MX_COL32 || k->layout == OR_MX_COL32 || v->layout == OR_MX_ROW32) return OR_ERR_ARG;
+    if (exact && (!causal || v->layout != OR_E4M3_TOKBLOCK || v->block != 1)) return OR_ERR_ARG;
+    emu_ctx c;
+    memset(&c, 0, sizeof(c));
+    c.q = q; c.k = k; c.v = v; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
+    c.causal = causal; c.exact = exact; c.rotated = rotated; c.scale = scale; c.flags = flags;
+    c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse;
+    for (int i = 0; i < 256; i++) c.dec[i] = or_e4m3_decode((uint8_t)i);
+    if (!mxq) { c.nbq = block_offset(&c.D, c.D.nd, q->block); c.nbk = block_offset(&c.D, c.D.nd, k->block); }
+    if (v->layout == OR_E4M3_TOKBLOCK) c.nbv = block_offset(&c.D, c.D.nd, v->block);
+    else c.ngv = block_offset(&c.D, c.D.nd, 32);
+    c.kh = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * d);
+    c.vh = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * d);
+    if (!c.kh || !c.vh) { free(c.kh); free(c.vh); free(c.D.cu); return OR_ERR_ARG; }
+    for (int h = 0; h < H; h++) {
+        c.h = h;
+        parallel_for(T, emu_decode_unit, &c);
+        parallel_for(c.nrows, emu_unit, &c);
+    }
+    free(c.kh); free(c.vh); free(c.D.cu);
+    return OR_OK;
+}
