@@ -1,0 +1,181 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused low-precision attention forward.
+ *
+ * The library computes the one-pass running-softmax attention forward over
+ * 8-bit operands that its own quantiser produces:
+ *
+ *   attn_quantize  rotate (Q, K) and encode Q, K, V as E4M3 with per-block
+ *                  scales or as MXFP8 with 32-element E8M0 scales
+ *   attn_fp8_fwd   S = Q K^T per key block, running row max and row sum,
+ *                  P V accumulation, final normalisation and logsumexp;
+ *                  FP32 softmax statistics, BF16 output
+ *   attn_bf16_fwd  the same loop over BF16 operands (the accuracy comparator)
+ *
+ * Sources of the operations (page title, section):
+ *   "Fused attention kernel" -- Overview (fused one-pass attention), 8-bit
+ *     forward pass (e4m3, block quantisation, incoherent processing with a
+ *     random sign diagonal times a Hadamard matrix), Implementation sketch
+ *     (the running-softmax loop and its two notes).
+ *   "FP8 attention that keeps FlashAttention-3 throughput at BF16-level
+ *     accuracy" -- How it gets verified (E4M3 operands, FP32 softmax
+ *     statistics, BF16 output, head dim 128, sequence 8192, causal and not).
+ *   "FLAMIA: FLAsh MIcroscaling Attention for Fast and Causally Safe Training
+ *     on Blackwell" -- Abstract and section 1 (token-block scaling, exact
+ *     scaling options against causal leakage, document-local scaling of
+ *     packed documents without repacking), section 2 (MX formats: 32-element
+ *     blocks with a shared scale consumed by the block-scaled MMA), section
+ *     4.3 (fused quantisation, longest-first ordering, folding score scales),
+ *     appendix F (scales and work lists stay on the GPU, no host
+ *     synchronisation, CUDA-graph capture, replay bitwise equal to eager).
+ *
+ * Conventions for every call:
+ *   - Pointers are device pointers unless a comment says "host". The caller
+ *     allocates and owns every buffer; the library never allocates or frees
+ *     device memory and never synchronises the stream inside a call, so the
+ *     calls can be captured in a CUDA graph.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Argument errors are returned synchronously and nothing is launched.
+ *     Errors found on the device (non-finite input, malformed cu_seqlens, a
+ *     bounded wait that ran out) are OR-ed into a status word at the start of
+ *     the caller's workspace and read back by attn_read_device_status.
+ *   - Results are deterministic: the same inputs give bitwise the same
+ *     outputs, eager or replayed from a graph.
+ *   - Tensors Q, K, V, O are [total_tokens][heads][head_dim] with head_dim
+ *     contiguous ("BSHD" packed; a batch of B sequences of N tokens is
+ *     B documents of N tokens). Supported head_dim: 64 and 128 (MXFP8: 128).
+ */
+#ifndef PA_GB300_ATTN_H
+#define PA_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,     /* bad pointer, size, stride, alignment or combination */
+    ATTN_ERR_UNSUPPORTED = 2,     /* valid request outside what the kernels implement */
+    ATTN_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 4,  /* a bounded on-device wait ran out (kernel returned early) */
+    ATTN_ERR_NONFINITE = 5,       /* a quantisation block held Inf or NaN */
+    ATTN_ERR_SEED_MISMATCH = 6,   /* Q and K carry different rotations */
+    ATTN_ERR_BAD_SEQLENS = 7,     /* cu_seqlens not 0 = c0 <= c1 <= ... = total_tokens */
+    ATTN_ERR_WORKSPACE = 8        /* workspace NULL, misaligned or smaller than required */
+} attn_status;
+
+typedef enum { ATTN_IN_F32 = 0, ATTN_IN_BF16 = 1 } attn_in_dtype;
+
+/* Scale layouts.
+ * ATTN_E4M3_TOKBLOCK: E4M3 codes, one fp32 scale per (document, head, block of
+ *   `block` consecutive tokens x head_dim); blocks start at the document start,
+ *   the last one may be partial. scale = amax / 448, code = E4M3(x * (448 / amax)).
+ *   block in {1, 32, 64, 128}; block 1 is the per-token scale of the
+ *   causal-exact mode.
+ *   Scales array: fp32 [heads][nb_cap], nb_cap = ceil(T / block) + num_docs;
+ *   the block b of document i sits at column boff_i + b with
+ *   boff_i = sum_{j < i} ceil(L_j / block).
+ * ATTN_MX_ROW32 (Q, K): MXFP8, one E8M0 exponent per (token, head, 32
+ *   consecutive channels); code = E4M3(x * 2^-X).
+ * ATTN_MX_COL32 (V): MXFP8, one E8M0 exponent per (32 document-local tokens,
+ *   head, channel): the 32-element blocks run along the sequence, the
+ *   contraction axis of P V.
+ *   MX scales array: bytes [heads][nt_cap][512], nt_cap = ceil(T/128) + num_docs,
+ *   one 512-byte tile per (head, 128-token tile of a document), tile t of
+ *   document i at index toff_i + t, toff_i = sum_{j < i} ceil(L_j / 128).
+ *   Inside a tile, row r (ROW32: the token 128 t + r of the document; COL32:
+ *   the channel r) and column group g (ROW32: channels 32 g..32 g + 31;
+ *   COL32: tokens 128 t + 32 g..+31) hold the biased exponent X + 127 at byte
+ *   (r % 32) * 16 + (r / 32) * 4 + g. Rows or groups past the document end
+ *   hold 127. This is the order the block-scaled tensor-core MMA reads its
+ *   scale factors in, so the forward copies tiles without reshuffling. */
+typedef enum { ATTN_E4M3_TOKBLOCK = 0, ATTN_MX_ROW32 = 1, ATTN_MX_COL32 = 2 } attn_layout;
+
+/* E8M0 exponent rule: NOSAT = smallest X with amax <= 448 * 2^X (nothing
+ * saturates; default); OCP_FLOOR = floor(log2 amax) - 8 (values above
+ * 448 * 2^X saturate). */
+typedef enum { ATTN_MX_RULE_NOSAT = 0, ATTN_MX_RULE_OCP_FLOOR = 1 } attn_mx_rule;
+
+typedef struct {
+    int32_t total_tokens;          /* T >= 1 */
+    int32_t heads;                 /* H >= 1 */
+    int32_t head_dim;              /* d: 64 or 128 */
+    int32_t num_docs;              /* >= 1; must be 1 when cu_seqlens is NULL */
+    const int32_t* cu_seqlens;     /* device, num_docs + 1 prefix offsets, or NULL = one document */
+} attn_shape;
+
+/* A quantised operand. The caller sets codes, scales (buffers of the sizes
+ * attn_quantize_sizes returns), layout, block and mx_rule before
+ * attn_quantize; attn_quantize sets `rotated` and `hadamard_seed`. */
+typedef struct {
+    void* codes;                   /* device, [T][H][d] E4M3 bytes, 16-byte aligned */
+    void* scales;                  /* device, see attn_layout; 16-byte aligned */
+    int32_t layout;                /* attn_layout */
+    int32_t block;                 /* tokens per scale block (ATTN_E4M3_TOKBLOCK) */
+    int32_t mx_rule;               /* attn_mx_rule (MX layouts) */
+    int32_t rotated;               /* 1 when codes are H_d * diag(signs) * x */
+    uint64_t hadamard_seed;        /* seed of the sign diagonal when rotated */
+} attn_qtensor;
+
+/* Byte sizes of the code and scale buffers for one tensor of this shape.
+ * Host-only; reads nothing on the device. */
+attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t block,
+                                size_t* codes_bytes, size_t* scales_bytes);
+
+/* Workspace bytes that attn_quantize, attn_fp8_fwd and attn_bf16_fwd need for
+ * this shape (one buffer serves all three; 256-byte aligned). Host-only. */
+attn_status attn_workspace_size(const attn_shape* shape, size_t* bytes);
+
+/* Fused rotate-and-quantise, one kernel launch (plus a tiny document-table
+ * launch when cu_seqlens is set).
+ * x: device, bf16 or fp32, element (t, h, c) at x[t * token_stride + h * head_stride + c]
+ *    (strides in elements; channels contiguous; 16-byte aligned rows).
+ * rotate != 0: codes of H_d * diag(s) * x, s_j = -1 if bit 63 of the j-th
+ *    SplitMix64 output from `hadamard_seed` is set, else +1; H_d the
+ *    unnormalised Sylvester Hadamard matrix (Q and K only; V is not rotated).
+ * Writes out->codes and out->scales; sets out->rotated and out->hadamard_seed. */
+attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
+                          const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed,
+                          attn_qtensor* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* FP8 attention forward over quantised operands.
+ * q, k: ATTN_E4M3_TOKBLOCK or ATTN_MX_ROW32 (both the same; both rotated with
+ *    the same seed or both not -> else ATTN_ERR_SEED_MISMATCH).
+ * v: ATTN_E4M3_TOKBLOCK (with E4M3 q, k) or ATTN_MX_COL32 (with MX q, k).
+ * causal: key j > query i masked, positions local to each document.
+ * causal_exact: requires causal and block 1 for q, k and v (E4M3); every
+ *    scale then depends on its own token only, and V's scales are folded
+ *    against a running maximum over positions <= i, so that no later token
+ *    changes row i.
+ * softmax_scale <= 0 selects 1 / sqrt(d).
+ * o: device bf16 [T][H][d]; lse: device fp32 [H][T], natural log of the
+ *    scaled scores (lse_i = log sum_j exp(softmax_scale q_i . k_j)). */
+attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                         const attn_shape* shape, int32_t causal, int32_t causal_exact,
+                         float softmax_scale, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* BF16 attention forward: the same loop with bf16 q, k, v [T][H][d]
+ * (contiguous), P in bf16, fp32 accumulation. Same o and lse as above. */
+attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const attn_shape* shape,
+                          int32_t causal, float softmax_scale, void* o, float* lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the device status word in
+ * `workspace`, and returns the first error it holds (ATTN_OK if none).
+ * flags_out (host, may be NULL) receives the raw bit set (bit e = error e). */
+attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* flags_out);
+
+/* Static description of a status code. */
+const char* attn_status_string(int32_t status);
+
+/* Number of streaming multiprocessors the forward sizes its persistent grid
+ * for on the current device, or -1 on error. */
+int32_t attn_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,236 @@
+"""Python binding of the GB300 fused low-precision attention library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpa_gb300.so`` behind the C ABI of ``include/attn.h``. PyTorch
+provides device memory and streams. There is no fallback: if the library is
+missing or fails to load, every call raises.
+
+The functions keep the C names:
+
+    attn_quantize_sizes, attn_workspace_size, attn_quantize, attn_fp8_fwd,
+    attn_bf16_fwd, attn_read_device_status, attn_status_string,
+    attn_device_sm_count
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_DEVICE_TIMEOUT = 4
+ATTN_ERR_NONFINITE = 5
+ATTN_ERR_SEED_MISMATCH = 6
+ATTN_ERR_BAD_SEQLENS = 7
+ATTN_ERR_WORKSPACE = 8
+
+ATTN_IN_F32, ATTN_IN_BF16 = 0, 1
+ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32 = 0, 1, 2
+ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
+
+EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
+           "attn_read_device_status", "attn_status_string", "attn_device_sm_count")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("num_docs", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p)]
+
+
+class _QT(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("layout", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("mx_rule", ctypes.c_int32), ("rotated", ctypes.c_int32),
+                ("hadamard_seed", ctypes.c_uint64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa_gb300.so (raises when it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with precision_attention_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+            S, Q = ctypes.POINTER(_Shape), ctypes.POINTER(_QT)
+            L.attn_quantize_sizes.argtypes = [S, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            L.attn_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
+            L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
+            L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+            L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+            L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+            L.attn_status_string.argtypes = [i32]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_device_sm_count.argtypes = []
+            for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd",
+                      "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count"):
+                getattr(L, f).restype = ctypes.c_int32
+            _lib = L
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_device_sm_count() -> int:
+    return int(lib().attn_device_sm_count())
+
+
+def _check(st: int, where: str):
+    if st != ATTN_OK:
+        raise AttnError(st, where)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def make_shape(T: int, H: int, d: int, cu_seqlens: torch.Tensor | None) -> _Shape:
+    nd = 1 if cu_seqlens is None else int(cu_seqlens.numel()) - 1
+    ptr = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    return _Shape(T, H, d, nd, ptr)
+
+
+def attn_quantize_sizes(T: int, H: int, d: int, num_docs: int, layout: int, block: int) -> tuple[int, int]:
+    s = _Shape(T, H, d, num_docs, None if num_docs == 1 else 1)
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().attn_quantize_sizes(ctypes.byref(s), layout, block, ctypes.byref(cb), ctypes.byref(sb)),
+           "attn_quantize_sizes")
+    return cb.value, sb.value
+
+
+def attn_workspace_size(T: int, H: int, d: int, num_docs: int) -> int:
+    s = _Shape(T, H, d, num_docs, None if num_docs == 1 else 1)
+    b = ctypes.c_size_t()
+    _check(lib().attn_workspace_size(ctypes.byref(s), ctypes.byref(b)), "attn_workspace_size")
+    return b.value
+
+
+def workspace(T: int, H: int, d: int, num_docs: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace buffer (torch allocates it; the library never does)."""
+    n = attn_workspace_size(T, H, d, num_docs)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+@dataclass
+class QTensor:
+    codes: torch.Tensor        # uint8 [T, H, d]
+    scales: torch.Tensor       # fp32 [H, nb_cap] or uint8 [H, nt_cap, 512]
+    layout: int
+    block: int
+    mx_rule: int = ATTN_MX_RULE_NOSAT
+    rotated: int = 0
+    hadamard_seed: int = 0
+
+    def _c(self) -> _QT:
+        return _QT(self.codes.data_ptr(), self.scales.data_ptr(), self.layout, self.block, self.mx_rule,
+                   self.rotated, self.hadamard_seed)
+
+
+def empty_qtensor(T: int, H: int, d: int, num_docs: int, layout: int, block: int,
+                  mx_rule: int = ATTN_MX_RULE_NOSAT, device="cuda") -> QTensor:
+    cb, sb = attn_quantize_sizes(T, H, d, num_docs, layout, block)
+    codes = torch.empty((T, H, d), dtype=torch.uint8, device=device)
+    if layout == ATTN_E4M3_TOKBLOCK:
+        scales = torch.empty((H, sb // (4 * H)), dtype=torch.float32, device=device)
+    else:
+        scales = torch.empty((H, sb // (512 * H), 512), dtype=torch.uint8, device=device)
+    return QTensor(codes, scales, layout, block, mx_rule)
+
+
+def attn_quantize(x: torch.Tensor, cu_seqlens: torch.Tensor | None, layout: int, block: int = 128,
+                  rotate: bool = False, hadamard_seed: int = 0, mx_rule: int = ATTN_MX_RULE_NOSAT,
+                  ws: torch.Tensor | None = None, out: QTensor | None = None, stream=None) -> QTensor:
+    """Rotate (optionally) and quantise x [T, H, d] (bf16 or fp32, channels contiguous)."""
+    assert x.is_cuda and x.dim() == 3 and x.stride(2) == 1
+    T, H, d = x.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if ws is None:
+        ws = workspace(T, H, d, nd, x.device)
+    if out is None:
+        out = empty_qtensor(T, H, d, nd, layout, block, mx_rule, x.device)
+    dt = ATTN_IN_BF16 if x.dtype == torch.bfloat16 else ATTN_IN_F32
+    assert x.dtype in (torch.bfloat16, torch.float32)
+    shape = make_shape(T, H, d, cu_seqlens)
+    c = out._c()
+    _check(lib().attn_quantize(x.data_ptr(), dt, x.stride(0), x.stride(1), ctypes.byref(shape), int(bool(rotate)),
+                               hadamard_seed & (2 ** 64 - 1), ctypes.byref(c), ws.data_ptr(), ws.numel(),
+                               _stream(stream)), "attn_quantize")
+    out.rotated, out.hadamard_seed = c.rotated, c.hadamard_seed
+    return out
+
+
+def attn_fp8_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None, causal: bool = False,
+                 causal_exact: bool = False, softmax_scale: float = 0.0, ws: torch.Tensor | None = None,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """FP8 attention forward. Returns (o bf16 [T, H, d], lse fp32 [H, T])."""
+    T, H, d = q.codes.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.codes.device
+    if ws is None:
+        ws = workspace(T, H, d, nd, dev)
+    if out is None:
+        out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    shape = make_shape(T, H, d, cu_seqlens)
+    cq, ck, cv = q._c(), k._c(), v._c()
+    _check(lib().attn_fp8_fwd(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                              int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), out.data_ptr(),
+                              lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)), "attn_fp8_fwd")
+    return out, lse
+
+
+def attn_bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
+                  causal: bool = False, softmax_scale: float = 0.0, ws: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """BF16 attention forward over contiguous bf16 [T, H, d] q, k, v."""
+    assert q.dtype == k.dtype == v.dtype == torch.bfloat16
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+    T, H, d = q.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if ws is None:
+        ws = workspace(T, H, d, nd, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    shape = make_shape(T, H, d, cu_seqlens)
+    _check(lib().attn_bf16_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(shape), int(bool(causal)),
+                               float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream(stream)), "attn_bf16_fwd")
+    return out, lse
+
+
+def attn_read_device_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:
+    """Synchronise, read and clear the workspace status word. Returns (status, raw flags)."""
+    flags = ctypes.c_uint32()
+    st = lib().attn_read_device_status(ws.data_ptr(), _stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)
+
+
+def default_softmax_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

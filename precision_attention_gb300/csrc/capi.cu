@@ -1,0 +1,281 @@
+// capi.cu -- the extern "C" boundary declared in include/attn.h: argument
+// validation, workspace layout and the kernel launches. No allocation, no
+// stream synchronisation (except attn_read_device_status, by definition).
+#include <cmath>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "params.h"
+
+using namespace pa;
+
+namespace {
+
+constexpr long long kWaitLimit = 4000000000LL;   // SM cycles (about 2 s) before a wait gives up
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_shape(const attn_shape* s) {
+    if (!s) return ATTN_ERR_INVALID_ARG;
+    if (s->total_tokens < 1 || s->heads < 1 || s->num_docs < 1) return ATTN_ERR_INVALID_ARG;
+    if (s->head_dim != 64 && s->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!s->cu_seqlens && s->num_docs != 1) return ATTN_ERR_INVALID_ARG;
+    if (s->num_docs > MAX_DOCS) return ATTN_ERR_UNSUPPORTED;
+    if (s->num_docs > s->total_tokens) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(s->total_tokens) * s->heads > (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+long long blocks_cap(const attn_shape* s, int block) {
+    return (static_cast<long long>(s->total_tokens) + block - 1) / block + s->num_docs;
+}
+long long tiles_cap(const attn_shape* s) { return blocks_cap(s, 128); }
+
+attn_status check_ws(const attn_shape* s, void* ws, size_t bytes) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return ATTN_ERR_WORKSPACE;
+    if (bytes < ws_layout(s->total_tokens, s->heads, s->num_docs).total) return ATTN_ERR_WORKSPACE;
+    return ATTN_OK;
+}
+
+bool valid_block(int layout, int block) {
+    if (layout == ATTN_E4M3_TOKBLOCK) return block == 1 || block == 32 || block == 64 || block == 128;
+    return layout == ATTN_MX_ROW32 || layout == ATTN_MX_COL32;
+}
+
+attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int32_t s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case ATTN_ERR_NONFINITE: return "non-finite input in a quantisation block";
+        case ATTN_ERR_SEED_MISMATCH: return "Q and K rotations differ";
+        case ATTN_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
+        case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t block, size_t* codes_bytes,
+                                size_t* scales_bytes) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!codes_bytes || !scales_bytes) return ATTN_ERR_INVALID_ARG;
+    if (layout < 0 || layout > 2 || !valid_block(layout, block)) return ATTN_ERR_INVALID_ARG;
+    if (layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const long long T = shape->total_tokens, H = shape->heads, d = shape->head_dim;
+    *codes_bytes = static_cast<size_t>(T * H * d);
+    if (layout == ATTN_E4M3_TOKBLOCK)
+        *scales_bytes = static_cast<size_t>(H * blocks_cap(shape, block)) * sizeof(float);
+    else
+        *scales_bytes = static_cast<size_t>(H * tiles_cap(shape)) * 512;
+    return ATTN_OK;
+}
+
+attn_status attn_workspace_size(const attn_shape* shape, size_t* bytes) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!bytes) return ATTN_ERR_INVALID_ARG;
+    *bytes = ws_layout(shape->total_tokens, shape->heads, shape->num_docs).total;
+    return ATTN_OK;
+}
+
+attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
+                          const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed, attn_qtensor* out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!x || !out || !out->codes || !out->scales) return ATTN_ERR_INVALID_ARG;
+    if (in_dtype != ATTN_IN_F32 && in_dtype != ATTN_IN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 2) return ATTN_ERR_INVALID_ARG;
+    if (out->layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (out->mx_rule != ATTN_MX_RULE_NOSAT && out->mx_rule != ATTN_MX_RULE_OCP_FLOOR) return ATTN_ERR_INVALID_ARG;
+    const int elt = in_dtype == ATTN_IN_BF16 ? 2 : 4;
+    if (!aligned16(x) || !aligned16(out->codes) || !aligned16(out->scales)) return ATTN_ERR_INVALID_ARG;
+    if (token_stride < 1 || head_stride < 1 || (token_stride * elt) % 16 || (head_stride * elt) % 16)
+        return ATTN_ERR_INVALID_ARG;
+    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
+    QuantParams p;
+    p.x = x;
+    p.in_bf16 = in_dtype == ATTN_IN_BF16;
+    p.tstride = token_stride;
+    p.hstride = head_stride;
+    p.T = shape->total_tokens;
+    p.H = shape->heads;
+    p.d = shape->head_dim;
+    p.nd = shape->num_docs;
+    p.cu = shape->cu_seqlens;
+    p.codes = static_cast<uint8_t*>(out->codes);
+    p.scales = out->scales;
+    p.block = out->block;
+    p.scale_cap = out->layout == ATTN_E4M3_TOKBLOCK ? blocks_cap(shape, out->block) : tiles_cap(shape);
+    p.rotate = rotate != 0;
+    p.seed = hadamard_seed;
+    p.mx_rule = out->mx_rule;
+    p.status = &static_cast<WsHeader*>(workspace)->status;
+    st = cuda_status(launch_quantize(p, out->layout, static_cast<cudaStream_t>(stream)));
+    if (st == ATTN_OK) {
+        out->rotated = rotate != 0;
+        out->hadamard_seed = rotate ? hadamard_seed : 0;
+    }
+    return st;
+}
+
+static attn_status forward(int mode, const void* q, const void* k, const void* v, const attn_qtensor* qq,
+                           const attn_qtensor* qk, const attn_qtensor* qv, const attn_shape* shape, int causal,
+                           int exact, float softmax_scale, int rotated, void* o, float* lse, void* workspace,
+                           cudaStream_t stream) {
+    const int T = shape->total_tokens, H = shape->heads, d = shape->head_dim, nd = shape->num_docs;
+    const WsLayout L = ws_layout(T, H, nd);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    DocEntry* docs = reinterpret_cast<DocEntry*>(ws + L.docs_off);
+    WorkItem* items = reinterpret_cast<WorkItem*>(ws + L.items_off);
+    float* vref = reinterpret_cast<float*>(ws + L.vref_off);
+    const bool e4m3 = mode == 1 || mode == 2;
+
+    SchedParams sp;
+    sp.cu = shape->cu_seqlens;
+    sp.nd = nd;
+    sp.T = T;
+    sp.H = H;
+    sp.causal = causal;
+    sp.bq = e4m3 ? qq->block : 1;
+    sp.bk = e4m3 ? qk->block : 1;
+    sp.bv = e4m3 ? qv->block : 1;
+    sp.hdr = hdr;
+    sp.docs = docs;
+    sp.items = items;
+    sp.items_cap = L.items_cap;
+    cudaError_t e = launch_sched(sp, stream);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+
+    FwdParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.docs = docs;
+    fp.items = items;
+    fp.hdr = hdr;
+    fp.o = static_cast<uint16_t*>(o);
+    fp.lse = lse;
+    fp.T = T;
+    fp.H = H;
+    fp.nd = nd;
+    fp.causal = causal;
+    fp.exact = exact;
+    const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt((double)d);
+    fp.C = static_cast<float>(sc * 1.4426950408889634 / (rotated ? static_cast<double>(d) : 1.0));
+    fp.wait_limit = kWaitLimit;
+    fp.bq = fp.bk = fp.bv = 1;
+    if (e4m3) {
+        fp.sq = static_cast<const float*>(qq->scales);
+        fp.sk = static_cast<const float*>(qk->scales);
+        fp.sv = static_cast<const float*>(qv->scales);
+        fp.capq = blocks_cap(shape, qq->block);
+        fp.capk = blocks_cap(shape, qk->block);
+        fp.capv = blocks_cap(shape, qv->block);
+        fp.bq = qq->block;
+        fp.bk = qk->block;
+        fp.bv = qv->block;
+        fp.vref = vref;
+        VrefParams vp;
+        vp.sv = fp.sv;
+        vp.sv_cap = fp.capv;
+        vp.docs = docs;
+        vp.hdr = hdr;
+        vp.vref = vref;
+        vp.H = H;
+        vp.nd = nd;
+        vp.T = T;
+        vp.exact = exact;
+        vp.bv = qv->block;
+        if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    } else if (mode == 3) {
+        fp.mq = static_cast<const uint8_t*>(qq->scales);
+        fp.mk = static_cast<const uint8_t*>(qk->scales);
+        fp.mv = static_cast<const uint8_t*>(qv->scales);
+        fp.ntcap = tiles_cap(shape);
+    }
+    const int grid = attn_device_sm_count();
+    if (grid < 1) return ATTN_ERR_CUDA;
+    e = launch_attn(mode, d, q, k, v, fp, grid, stream);
+    return e == cudaSuccess ? ATTN_OK : (e == cudaErrorInvalidValue ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA);
+}
+
+attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                         const attn_shape* shape, int32_t causal, int32_t causal_exact, float softmax_scale,
+                         void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!q->codes || !k->codes || !v->codes || !q->scales || !k->scales || !v->scales) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q->codes) || !aligned16(k->codes) || !aligned16(v->codes) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(q->scales) || !aligned16(k->scales) || !aligned16(v->scales))
+        return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
+    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
+    const bool mx = q->layout == ATTN_MX_ROW32;
+    if (mx) {
+        if (k->layout != ATTN_MX_ROW32 || v->layout != ATTN_MX_COL32) return ATTN_ERR_INVALID_ARG;
+        if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+        if (causal_exact) return ATTN_ERR_UNSUPPORTED;
+    } else {
+        if (q->layout != ATTN_E4M3_TOKBLOCK || k->layout != ATTN_E4M3_TOKBLOCK || v->layout != ATTN_E4M3_TOKBLOCK)
+            return ATTN_ERR_INVALID_ARG;
+        if (!valid_block(0, q->block) || !valid_block(0, k->block) || !valid_block(0, v->block))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (v->rotated) return ATTN_ERR_INVALID_ARG;
+    if (q->rotated != k->rotated || (q->rotated && q->hadamard_seed != k->hadamard_seed))
+        return ATTN_ERR_SEED_MISMATCH;
+    if (causal_exact && (!causal || q->block != 1 || k->block != 1 || v->block != 1)) return ATTN_ERR_INVALID_ARG;
+    int mode = 3;
+    if (!mx) mode = (q->block == 128 && k->block == 128 && v->block == 128 && !causal_exact) ? 1 : 2;
+    return forward(mode, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
+                   softmax_scale, q->rotated, o, lse, workspace, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const attn_shape* shape, int32_t causal,
+                          float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
+    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
+    return forward(0, q, k, v, nullptr, nullptr, nullptr, shape, causal != 0, 0, softmax_scale, 0, o, lse,
+                   workspace, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* flags_out) {
+    if (!workspace) return ATTN_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof(w)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (flags_out) *flags_out = w;
+    if (w & ST_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
+    if (w & ST_BAD_SEQLENS) return ATTN_ERR_BAD_SEQLENS;
+    if (w & ST_NONFINITE) return ATTN_ERR_NONFINITE;
+    return ATTN_OK;
+}
+
+int32_t attn_device_sm_count(void) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// internal.h -- layouts shared by the host launchers and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace pa {
+
+// Device status word bits (bit e = attn_status e), OR-ed by kernels.
+constexpr uint32_t ST_TIMEOUT = 1u << 4;
+constexpr uint32_t ST_NONFINITE = 1u << 5;
+constexpr uint32_t ST_BAD_SEQLENS = 1u << 7;
+
+// Largest document count the quantiser's in-shared-memory document table holds.
+constexpr int MAX_DOCS = 1024;
+
+// One document of the packed batch, as the forward reads it.
+struct DocEntry {
+    int32_t start;    // first token
+    int32_t len;      // tokens
+    int32_t toff;     // first 128-token tile (prefix of ceil(L / 128))
+    int32_t boff_q;   // first scale block of Q (prefix of ceil(L / block_q))
+    int32_t boff_k;
+    int32_t boff_v;
+    int32_t pad0, pad1;
+};
+
+// One unit of forward work: the 128-row query tile `qtile` of (doc, head).
+struct WorkItem {
+    int32_t doc;
+    int32_t head;
+    int32_t qtile;
+    int32_t ntiles;   // key tiles to visit
+};
+
+// Workspace layout: [header 256 B][docs][items][vref]
+struct WsLayout {
+    size_t docs_off, items_off, vref_off, total;
+    int64_t items_cap, vref_cap;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int64_t T, int64_t H, int64_t nd) {
+    WsLayout w;
+    w.items_cap = H * ((T + 127) / 128 + nd);
+    w.vref_cap = H * (T > nd ? T : nd);
+    w.docs_off = 256;
+    w.items_off = align_up(w.docs_off + sizeof(DocEntry) * static_cast<size_t>(nd), 256);
+    w.vref_off = align_up(w.items_off + sizeof(WorkItem) * static_cast<size_t>(w.items_cap), 256);
+    w.total = align_up(w.vref_off + sizeof(float) * static_cast<size_t>(w.vref_cap), 256);
+    return w;
+}
+
+// Header at the start of the workspace.
+struct WsHeader {
+    uint32_t status;
+    int32_t n_items;
+    int32_t n_tiles;
+    int32_t pad[61];
+};
+
+}  // namespace pa

@@ -1,0 +1,70 @@
+// params.h -- launch parameter blocks shared by the host launchers and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace pa {
+
+struct QuantParams {
+    const void* x;
+    int in_bf16;
+    long long tstride, hstride;   // elements
+    int T, H, d, nd;
+    const int32_t* cu;            // may be null (one document)
+    uint8_t* codes;               // [T][H][d]
+    void* scales;
+    long long scale_cap;          // nb_cap (E4M3) or nt_cap (MX)
+    int block;
+    int rotate;
+    unsigned long long seed;
+    int mx_rule;
+    uint32_t* status;
+};
+
+struct SchedParams {
+    const int32_t* cu;     // may be null
+    int nd, T, H, causal;
+    int bq, bk, bv;        // E4M3 scale blocks (1 when unused)
+    WsHeader* hdr;
+    DocEntry* docs;
+    WorkItem* items;
+    long long items_cap;
+};
+
+struct VrefParams {
+    const float* sv;
+    long long sv_cap;
+    const DocEntry* docs;
+    const WsHeader* hdr;
+    float* vref;
+    int H, nd, T, exact, bv;
+};
+
+struct FwdParams {
+    const DocEntry* docs;
+    const WorkItem* items;
+    WsHeader* hdr;
+    uint16_t* o;          // bf16 [T][H][D]
+    float* lse;           // [H][T]
+    int T, H, nd;
+    int causal, exact;
+    float C;              // softmax_scale * log2(e) (/ d when Q and K are rotated)
+    const float *sq, *sk, *sv;
+    long long capq, capk, capv;
+    int bq, bk, bv;
+    const float* vref;
+    const uint8_t *mq, *mk, *mv;
+    long long ntcap;
+    long long wait_limit;
+};
+
+cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st);
+cudaError_t launch_sched(const SchedParams& p, cudaStream_t st);
+cudaError_t launch_vref(const VrefParams& p, cudaStream_t st);
+// mode: 0 bf16, 1 E4M3 with one scale per tile, 2 E4M3 per-column scales, 3 MXFP8
+cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
+                        cudaStream_t st);
+
+}  // namespace pa

@@ -1,0 +1,106 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function
+include/attn.h declares, and rejects bad arguments before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from precision_attention_gb300 import build
+    build.build()
+    import precision_attention_gb300 as pa
+    pa.lib()
+    return pa
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(pa):
+    decl = declared_functions()
+    assert len(decl) >= 8
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert set(decl) == set(pa.EXPORTS)
+
+
+def test_status_strings(pa):
+    for s in range(9):
+        assert pa.attn_status_string(s) and pa.attn_status_string(s) != "unknown status"
+    assert pa.attn_status_string(99) == "unknown status"
+
+
+def test_sizes(pa):
+    T, H, d = 1000, 4, 128
+    cb, sb = pa.attn_quantize_sizes(T, H, d, 1, pa.ATTN_E4M3_TOKBLOCK, 128)
+    assert cb == T * H * d and sb == H * ((T + 127) // 128 + 1) * 4
+    cb, sb = pa.attn_quantize_sizes(T, H, d, 3, pa.ATTN_MX_ROW32, 32)
+    assert sb == H * ((T + 127) // 128 + 3) * 512
+    cb, sb = pa.attn_quantize_sizes(T, H, 64, 1, pa.ATTN_E4M3_TOKBLOCK, 1)
+    assert sb == H * (T + 1) * 4
+    assert pa.attn_workspace_size(T, H, d, 3) % 256 == 0
+
+
+def test_invalid_arguments_rejected_on_host(pa):
+    L = pa.lib()
+    shape = pa._Shape(100, 2, 96, 1, None)      # head_dim 96 unsupported
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.attn_quantize_sizes(ctypes.byref(shape), 0, 128, ctypes.byref(cb), ctypes.byref(sb)) == \
+        pa.ATTN_ERR_UNSUPPORTED
+    shape = pa._Shape(100, 2, 128, 1, None)
+    assert L.attn_quantize_sizes(ctypes.byref(shape), 0, 100, ctypes.byref(cb), ctypes.byref(sb)) == \
+        pa.ATTN_ERR_INVALID_ARG                  # block 100 not offered
+    assert L.attn_quantize_sizes(ctypes.byref(pa._Shape(100, 2, 64, 1, None)), 1, 32, ctypes.byref(cb),
+                                 ctypes.byref(sb)) == pa.ATTN_ERR_UNSUPPORTED   # MX needs d = 128
+    assert L.attn_quantize_sizes(ctypes.byref(pa._Shape(100, 2, 128, 3, None)), 0, 128, ctypes.byref(cb),
+                                 ctypes.byref(sb)) == pa.ATTN_ERR_INVALID_ARG   # 3 docs need cu_seqlens
+    qt = pa._QT(None, None, 0, 128, 0, 0, 0)
+    # null input / outputs: rejected before any CUDA call
+    assert L.attn_quantize(None, 1, 256, 128, ctypes.byref(shape), 1, 1, ctypes.byref(qt), None, 0, None) == \
+        pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_fp8_fwd(ctypes.byref(qt), ctypes.byref(qt), ctypes.byref(qt), ctypes.byref(shape), 0, 0, 0.0,
+                          None, None, None, 0, None) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_bf16_fwd(None, None, None, ctypes.byref(shape), 0, 0.0, None, None, None, 0, None) == \
+        pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_read_device_status(None, None, None) == pa.ATTN_ERR_WORKSPACE
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses placeholder device pointers; only run where no GPU could be reached")
+def test_seed_mismatch_and_layout_rules_on_host(pa):
+    """Q/K rotation mismatch and exact-mode rules are refused before launch.
+    Placeholder aligned pointers pass the null checks and are never used."""
+    L = pa.lib()
+    fake = 1 << 20
+    shape = pa._Shape(256, 2, 128, 1, None)
+    q = pa._QT(fake, fake, 0, 128, 0, 1, 7)
+    k = pa._QT(fake, fake, 0, 128, 0, 1, 8)
+    v = pa._QT(fake, fake, 0, 128, 0, 0, 0)
+    ws_small = 16
+    # workspace too small is reported before the rotation check
+    assert L.attn_fp8_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shape), 0, 0, 0.0,
+                          fake, fake, fake, ws_small, None) == pa.ATTN_ERR_WORKSPACE
+    big = pa.attn_workspace_size(256, 2, 128, 1)
+    assert L.attn_fp8_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shape), 0, 0, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_SEED_MISMATCH
+    k.hadamard_seed = 7
+    # causal-exact needs causal and block 1 everywhere
+    assert L.attn_fp8_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shape), 0, 1, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_fp8_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shape), 1, 1, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
+    # MX Q/K with an E4M3 V is refused
+    qm = pa._QT(fake, fake, 1, 32, 0, 1, 7)
+    km = pa._QT(fake, fake, 1, 32, 0, 1, 7)
+    assert L.attn_fp8_fwd(ctypes.byref(qm), ctypes.byref(km), ctypes.byref(v), ctypes.byref(shape), 0, 0, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,139 @@
+"""GPU attention parity: the CUDA forward against the oracle's quantised-operand
+emulation (O-3), element by element, on seeded workload recipes at sizes that
+span several tiles with ragged documents; plus determinism, packed ==
+per-document, causal exactness and the BF16 path against FP64 attention.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import compare_outputs, to_device
+
+pa = pytest.importorskip("precision_attention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+E4M3, ROW, COL = 0, 1, 2
+
+
+def run_gpu(inp, mx, block, causal, exact=False, rotate=True, seed=None):
+    seed = (0x5EED0000 + inp.wid) if seed is None else seed
+    q, k, v, cu = to_device(inp)
+    T, H, d = q.shape
+    nd = cu.numel() - 1
+    ws = pa.workspace(T, H, d, nd)
+    if mx:
+        Q = pa.attn_quantize(q, cu, ROW, 32, rotate, seed, ws=ws)
+        K = pa.attn_quantize(k, cu, ROW, 32, rotate, seed, ws=ws)
+        V = pa.attn_quantize(v, cu, COL, 32, False, 0, ws=ws)
+    else:
+        Q = pa.attn_quantize(q, cu, E4M3, block, rotate, seed, ws=ws)
+        K = pa.attn_quantize(k, cu, E4M3, block, rotate, seed, ws=ws)
+        V = pa.attn_quantize(v, cu, E4M3, block, False, 0, ws=ws)
+    o, lse = pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0, ws=ws)
+    st, flags = pa.attn_read_device_status(ws)
+    assert st == 0, (st, flags)
+    return o, lse
+
+
+def run_emu(inp, mx, block, causal, exact=False, rotate=True, seed=None, rows=None):
+    seed = (0x5EED0000 + inp.wid) if seed is None else seed
+    cu = inp.cu_seqlens
+    if mx:
+        Q = oracle.quantize_tensor(inp.q, cu, ROW, 32, rotate, seed)
+        K = oracle.quantize_tensor(inp.k, cu, ROW, 32, rotate, seed)
+        V = oracle.quantize_tensor(inp.v, cu, COL, 32, False, 0)
+    else:
+        Q = oracle.quantize_tensor(inp.q, cu, E4M3, block, rotate, seed)
+        K = oracle.quantize_tensor(inp.k, cu, E4M3, block, rotate, seed)
+        V = oracle.quantize_tensor(inp.v, cu, E4M3, block, False, 0)
+    return oracle.attention_emulate(Q, K, V, cu, causal, exact, None, rows=rows)
+
+
+CASES = [
+    # wid, lengths, heads, mx, block, causal, exact
+    (1, [256], 2, False, 64, False, False),          # tiny workload as given (d = 64, fp32 in)
+    (1, [200, 56, 129], 2, False, 64, True, False),
+    (2, [300, 77, 129], 2, False, 128, False, False),
+    (3, [300, 77, 129], 2, False, 128, True, False),
+    (3, [260, 31], 2, False, 1, True, True),         # causal-exact
+    (2, [384], 2, False, 32, False, False),
+    (4, [300, 77, 129], 2, True, 32, False, False),  # MXFP8
+    (5, [300, 77, 129, 1], 2, True, 32, True, False),
+]
+
+
+@pytest.mark.parametrize("wid,lengths,H,mx,block,causal,exact", CASES)
+def test_fp8_forward_matches_emulation(oracle_mod, wid, lengths, H, mx, block, causal, exact):
+    inp = workloads.make(wid, heads=H, lengths=lengths)
+    o, lse = run_gpu(inp, mx, block, causal, exact)
+    _, ob, le = run_emu(inp, mx, block, causal, exact)
+    res = compare_outputs(o, lse, ob, le)
+    assert res["ok"], res
+
+
+def test_fp8_forward_deterministic():
+    inp = workloads.make(3, heads=2, lengths=[300, 200])
+    o1, l1 = run_gpu(inp, False, 128, True)
+    o2, l2 = run_gpu(inp, False, 128, True)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_packed_equals_per_document(mx):
+    lens = [300, 77, 129]
+    wid = 5 if mx else 3
+    inp = workloads.make(wid, heads=2, lengths=lens)
+    o, lse = run_gpu(inp, mx, 128, True)
+    cu = inp.cu_seqlens
+    for i, L in enumerate(lens):
+        s = int(cu[i])
+        sub = workloads.Inputs(inp.q[s:s + L], inp.k[s:s + L], inp.v[s:s + L],
+                               np.array([0, L], dtype=np.int32), True, wid, inp.in_dtype)
+        os_, ls = run_gpu(sub, mx, 128, True)
+        assert torch.equal(o[s:s + L].view(torch.int16), os_.view(torch.int16))
+        assert torch.equal(lse[:, s:s + L], ls)
+
+
+def test_causal_exact_rows_unchanged_by_later_tokens():
+    inp = workloads.make(3, heads=2, lengths=[400])
+    cut = 150
+    pert = workloads.make(3, heads=2, lengths=[400])
+    pert.k[cut + 1:] = workloads.bf16_round(pert.k[cut + 1:] * 30)
+    pert.v[cut + 1:] = workloads.bf16_round(pert.v[cut + 1:] * 40)
+    a, la = run_gpu(inp, False, 1, True, True)
+    b, lb = run_gpu(pert, False, 1, True, True)
+    assert torch.equal(a[:cut + 1].view(torch.int16), b[:cut + 1].view(torch.int16))
+    assert torch.equal(la[:, :cut + 1], lb[:, :cut + 1])
+    assert not torch.equal(a[cut + 1:].view(torch.int16), b[cut + 1:].view(torch.int16))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_against_fp64(oracle_mod, causal):
+    inp = workloads.make(2, heads=2, lengths=[300, 77, 129])
+    q, k, v, cu = to_device(inp)
+    o, lse = pa.attn_bf16_fwd(q, k, v, cu, causal)
+    o1, l1 = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, causal)
+    og = o.float().cpu().numpy()
+    rel = np.linalg.norm(og - o1) / np.linalg.norm(o1)
+    # BF16 P and BF16 output rounding: a few 2^-9 relative
+    assert rel < 6e-3, rel
+    assert np.abs(lse.cpu().numpy() - l1).max() < 2e-3
+
+
+def test_fp8_rmse_against_fp64_reported(oracle_mod):
+    """RMSE of the FP8 and BF16 paths against FP64 attention on the outlier
+    recipe; the ratio is what the accuracy criterion bounds (recorded, and
+    checked here only for sanity: FP8 error is finite and above BF16's)."""
+    inp = workloads.make(2, heads=2, lengths=[512])
+    o8, _ = run_gpu(inp, False, 128, False)
+    q, k, v, cu = to_device(inp)
+    ob, _ = pa.attn_bf16_fwd(q, k, v, cu, False)
+    o1, _ = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, False)
+    r8 = np.sqrt(np.mean((o8.float().cpu().numpy() - o1) ** 2))
+    rb = np.sqrt(np.mean((ob.float().cpu().numpy() - o1) ** 2))
+    assert np.isfinite(r8) and r8 > rb > 0
