@@ -1,0 +1,391 @@
+"""Benchmark: FP8 attention forward TFLOP/s including quantisation.
+
+One step = the whole hot path over one batch of synthetic input resident in
+HBM: rotate-and-quantise Q, K and V (three launches), then the FP8 forward
+(work-list, V-reference and attention launches). FLOPs = 4 B H N^2 d, halved
+for causal workloads. The default workload is the FlashAttention-3 headline
+shape: batch 2, 32 heads, sequence 8192, head_dim 128, non-causal, 0.1%
+N(0, 10) outliers, E4M3 with 128-token block scales and a 128-point Hadamard
+rotation of Q and K.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torch.distributed.run, one rank per GPU; every rank runs its
+own replica of the workload (weak scaling, no collective on the data path).
+`--impl reference` times the CPU oracle (quantiser + quantised-operand
+emulation) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "FP8 attn fwd TFLOP/s incl. quant (hd128, s8192); RMSE vs FP64 oracle"
+UNIT = "TFLOP/s"
+E4M3, ROW, COL = 0, 1, 2
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def fp8_peak():
+    """Dense FP8 tensor peak: measured bf16 GEMM burst x the nominal fp8/bf16
+    ratio (4.5 / 2.25 PFLOP/s); the recipe's fallback when no measurement."""
+    pk = load_peaks()
+    if pk and pk.get("bf16_tflops"):
+        return 2.0 * float(pk["bf16_tflops"]), "measured bf16 burst x2 (nominal fp8/bf16 ratio)"
+    return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x2"
+
+
+def hbm_peak():
+    pk = load_peaks()
+    if pk and pk.get("hbm_gbs"):
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5], parts[6], parts[7], parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r[0] > 0.5 * r[1]] or rows
+        reasons = []
+        for name, col in (("hw_slowdown", 2), ("hw_thermal_slowdown", 3), ("sw_thermal_slowdown", 4),
+                          ("sw_power_cap", 5)):
+            if any(r[col].lower() == "active" for r in rows):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import precision_attention_gb300 as pa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
+    T, H, d = inp.q.shape
+    cu_np = inp.cu_seqlens
+    nd = len(cu_np) - 1
+    causal = w.causal
+    mx = w.mx
+    seed = w.hadamard_seed
+    flops = workloads.attention_flops(cu_np, H, d, causal)
+    in_dt = torch.float32 if w.in_dtype == "f32" else torch.bfloat16
+
+    q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(a)).to(in_dt).pin_memory() for a in (inp.q, inp.k, inp.v))
+    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
+    cu = torch.from_numpy(cu_np.astype(np.int32)).to(dev)
+    ws = pa.workspace(T, H, d, nd, dev)
+    if mx:
+        lq, lk, lv, blk = ROW, ROW, COL, 32
+    else:
+        lq = lk = lv = E4M3
+        blk = w.block
+    Q = pa.empty_qtensor(T, H, d, nd, lq, blk, device=dev)
+    K = pa.empty_qtensor(T, H, d, nd, lk, blk, device=dev)
+    V = pa.empty_qtensor(T, H, d, nd, lv, blk, device=dev)
+    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    attn_ev = []
+
+    def step(record=False):
+        pa.attn_quantize(q, cu, lq, blk, True, seed, ws=ws, out=Q, stream=stream)
+        pa.attn_quantize(k, cu, lk, blk, True, seed, ws=ws, out=K, stream=stream)
+        pa.attn_quantize(v, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws, out=o, lse=lse, stream=stream)
+        if record:
+            e1.record(stream)
+            attn_ev.append((e0, e1))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, flags = pa.attn_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {pa.attn_status_string(st)} flags {flags:#x}")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    st, flags = pa.attn_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {pa.attn_status_string(st)} flags {flags:#x}")
+
+    # end to end: pinned host inputs in, output and lse back, every step
+    o_h = torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((H, T), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
+    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+
+    # accuracy on sampled rows (outside the timed region): FP8 and BF16 paths vs FP64
+    acc = None
+    if rank == 0 and not args.no_accuracy and not mx and not causal:
+        acc = accuracy_sample(args, inp, q, k, v, cu, o, pa, torch)
+
+    ms_step = ms_total / args.steps
+    if dist:
+        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    return {"ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
+            "h2d": h2d, "d2h": d2h, "clocks": clk, "acc": acc, "T": T, "H": H, "d": d, "nd": nd}
+
+
+def accuracy_sample(args, inp, q, k, v, cu, o_fp8, pa, torch):
+    import oracle
+    rng = np.random.default_rng(123)
+    rows = np.sort(rng.choice(inp.T, size=min(64, inp.T), replace=False)).astype(np.int32)
+    ob, _ = pa.attn_bf16_fwd(q, k, v, cu, False)
+    o1, _ = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, False, None, rows=rows)
+    o8 = o_fp8.float().cpu().numpy()[rows].astype(np.float64)
+    obb = ob.float().cpu().numpy()[rows].astype(np.float64)
+    r8 = float(np.sqrt(np.mean((o8 - o1) ** 2)))
+    rb = float(np.sqrt(np.mean((obb - o1) ** 2)))
+    cos = float(np.sum(o8 * o1) / (np.linalg.norm(o8) * np.linalg.norm(o1)))
+    return {"rows_sampled": int(len(rows)), "rmse_fp8_vs_fp64": r8, "rmse_bf16_vs_fp64": rb,
+            "ratio_fp8_over_bf16": r8 / rb if rb > 0 else None, "cosine_fp8_vs_fp64": cos}
+
+
+# ---------------------------------------------------------------------------
+def cpu_sample(args, budget_s=15.0):
+    """Time the oracle (quantiser + quantised-operand emulation) on whole heads
+    of the workload's first document until about `budget_s` of CPU work."""
+    import oracle
+    oracle.build()
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
+    cu = inp.cu_seqlens
+    L0 = int(cu[1] - cu[0])
+    sel = slice(0, L0)
+    flops = 0.0
+    t_total = 0.0
+    heads_done = 0
+    H = inp.q.shape[1]
+    for h in range(H):
+        q = np.ascontiguousarray(inp.q[sel, h:h + 1])
+        k = np.ascontiguousarray(inp.k[sel, h:h + 1])
+        v = np.ascontiguousarray(inp.v[sel, h:h + 1])
+        c1 = np.array([0, L0], np.int32)
+        t0 = time.perf_counter()
+        if w.mx:
+            Q = oracle.quantize_tensor(q, c1, ROW, 32, True, w.hadamard_seed)
+            K = oracle.quantize_tensor(k, c1, ROW, 32, True, w.hadamard_seed)
+            V = oracle.quantize_tensor(v, c1, COL, 32, False, 0)
+        else:
+            Q = oracle.quantize_tensor(q, c1, E4M3, w.block, True, w.hadamard_seed)
+            K = oracle.quantize_tensor(k, c1, E4M3, w.block, True, w.hadamard_seed)
+            V = oracle.quantize_tensor(v, c1, E4M3, w.block, False, 0)
+        oracle.attention_emulate(Q, K, V, c1, w.causal, False, None)
+        t_total += time.perf_counter() - t0
+        flops += workloads.attention_flops(c1, 1, inp.q.shape[2], w.causal)
+        heads_done += 1
+        if t_total >= budget_s:
+            break
+    return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"document 0 ({L0} tokens), {heads_done} of {H} heads: oracle quantiser (Q, K, V) + "
+                      f"quantised-operand emulation over all rows and keys; {t_total:.1f} s",
+            "seconds": t_total}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    samples = []
+    for _ in range(args.warmup):
+        cpu_sample(args, budget_s=0.0)
+    for _ in range(args.steps):
+        samples.append(cpu_sample(args, budget_s=max(1.0, 60.0 / max(args.steps, 1))))
+    secs = sum(s["seconds"] for s in samples)
+    val = float(np.median([s["value"] for s in samples]))
+    w = workloads.WORKLOADS[args.workload]
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * secs / len(samples), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle emulation of e4m3 / fp32)",
+            "data": "synthetic", "impl": "reference", "config": config_of(args, w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": samples[0]["cores"], "kind": "oracle",
+                             "sample": samples[0]["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(args, w):
+    inp_T = None
+    return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
+            "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
+            "causal": w.causal, "quant": ("MXFP8 (E8M0 per 32)" if w.mx else f"E4M3 blocks of {w.block} tokens") +
+            " + Hadamard rotation of Q, K", "input_dtype": w.in_dtype,
+            "l2": "inputs larger than L2 (bf16 Q, K, V and their codes each exceed 129 MB)" if (
+                args.heads is None and args.seqlen is None) else "reduced size"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--heads", type=int, default=None)
+    ap.add_argument("--seqlen", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-accuracy", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    from precision_attention_gb300 import build as pbuild
+    if rank == 0 or world == 1:
+        pbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    r = gpu_arm(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    w = workloads.WORKLOADS[args.workload]
+    value = world * r["flops"] / (r["ms_step"] * 1e-3) / 1e12
+    e2e = world * r["flops"] / (r["e2e_ms"] * 1e-3) / 1e12
+    peak, peak_basis = fp8_peak()
+    achieved = r["flops"] / (r["attn_ms"] * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3" if not w.mx else "mxfp8 (e4m3 + e8m0)", "data": "synthetic",
+            "config": config_of(args, w),
+            "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": 6 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (FP8 forward call)", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_basis": peak_basis + " (of measured)"},
+            "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"],
+            "clocks": r["clocks"], "accuracy": r["acc"]}
+    if not args.no_cpu_baseline and world >= 1:
+        line["cpu_baseline"] = cpu_sample(args)
+        line["cpu_baseline"].pop("seconds", None)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
