@@ -231,7 +231,7 @@ def gpu_arm(args, rank, world, local_rank):
         t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step, e2e_ms = float(t[0]), float(t[1])
-    return {"ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
+    return {"inp": inp, "ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "acc": acc, "T": T, "H": H, "d": d, "nd": nd}
 
 
@@ -251,25 +251,29 @@ def accuracy_sample(args, inp, q, k, v, cu, o_fp8, pa, torch):
 
 
 # ---------------------------------------------------------------------------
-def cpu_sample(args, budget_s=15.0):
+def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
     """Time the oracle (quantiser + quantised-operand emulation) on whole heads
-    of the workload's first document until about `budget_s` of CPU work."""
+    of the workload's first document until about `budget_s` of CPU work.
+    rows: evaluate only the first `rows` query rows of the document (all keys)."""
     import oracle
     oracle.build()
     w = workloads.WORKLOADS[args.workload]
-    inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
+    if inp is None:
+        inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
     cu = inp.cu_seqlens
     L0 = int(cu[1] - cu[0])
-    sel = slice(0, L0)
+    R = L0 if rows is None else min(rows, L0)
+    row_idx = None if R == L0 else np.arange(R, dtype=np.int32)
     flops = 0.0
     t_total = 0.0
     heads_done = 0
     H = inp.q.shape[1]
+    d = inp.q.shape[2]
+    c1 = np.array([0, L0], np.int32)
     for h in range(H):
-        q = np.ascontiguousarray(inp.q[sel, h:h + 1])
-        k = np.ascontiguousarray(inp.k[sel, h:h + 1])
-        v = np.ascontiguousarray(inp.v[sel, h:h + 1])
-        c1 = np.array([0, L0], np.int32)
+        q = np.ascontiguousarray(inp.q[:L0, h:h + 1])
+        k = np.ascontiguousarray(inp.k[:L0, h:h + 1])
+        v = np.ascontiguousarray(inp.v[:L0, h:h + 1])
         t0 = time.perf_counter()
         if w.mx:
             Q = oracle.quantize_tensor(q, c1, ROW, 32, True, w.hadamard_seed)
@@ -279,29 +283,32 @@ def cpu_sample(args, budget_s=15.0):
             Q = oracle.quantize_tensor(q, c1, E4M3, w.block, True, w.hadamard_seed)
             K = oracle.quantize_tensor(k, c1, E4M3, w.block, True, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, E4M3, w.block, False, 0)
-        oracle.attention_emulate(Q, K, V, c1, w.causal, False, None)
+        oracle.attention_emulate(Q, K, V, c1, w.causal, False, None, rows=row_idx)
         t_total += time.perf_counter() - t0
-        flops += workloads.attention_flops(c1, 1, inp.q.shape[2], w.causal)
+        nkeys = np.arange(1, R + 1) if w.causal else np.full(R, L0)
+        flops += float(4.0 * d * nkeys.sum())
         heads_done += 1
         if t_total >= budget_s:
             break
     return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"document 0 ({L0} tokens), {heads_done} of {H} heads: oracle quantiser (Q, K, V) + "
-                      f"quantised-operand emulation over all rows and keys; {t_total:.1f} s",
+            "sample": f"document 0 ({L0} tokens), {heads_done} of {H} heads, {R} query rows each over all "
+                      f"visible keys: oracle quantiser (Q, K, V of the head) + quantised-operand emulation; "
+                      f"{t_total:.1f} s of host time",
             "seconds": t_total}
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
     samples = []
     for _ in range(args.warmup):
-        cpu_sample(args, budget_s=0.0)
+        cpu_sample(args, inp, budget_s=0.0, rows=64)
     for _ in range(args.steps):
-        samples.append(cpu_sample(args, budget_s=max(1.0, 60.0 / max(args.steps, 1))))
+        samples.append(cpu_sample(args, inp, budget_s=0.0, rows=1024))
     secs = sum(s["seconds"] for s in samples)
     val = float(np.median([s["value"] for s in samples]))
-    w = workloads.WORKLOADS[args.workload]
     line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000.0 * secs / len(samples), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle emulation of e4m3 / fp32)",
@@ -313,7 +320,6 @@ def reference_arm(args, rank, world):
 
 
 def config_of(args, w):
-    inp_T = None
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
             "causal": w.causal, "quant": ("MXFP8 (E8M0 per 32)" if w.mx else f"E4M3 blocks of {w.block} tokens") +
@@ -379,7 +385,7 @@ def main():
             "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"],
             "clocks": r["clocks"], "accuracy": r["acc"]}
     if not args.no_cpu_baseline and world >= 1:
-        line["cpu_baseline"] = cpu_sample(args)
+        line["cpu_baseline"] = cpu_sample(args, r.get("inp"))
         line["cpu_baseline"].pop("seconds", None)
     print(json.dumps(line), flush=True)
     if world > 1:
