@@ -55,6 +55,26 @@ def fp8_peak():
     return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x2"
 
 
+def attn_traffic(args):
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    when the kernel source changed since the capture or the workload differs."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.txt")
+    if args.workload != 2 or args.heads or args.seqlen or args.batch or not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh", "params.h"):
+        h.update(open(os.path.join(ROOT, "precision_attention_gb300", "csrc", f), "rb").read())
+    if h.hexdigest()[:16] != kv.get("source_sha256_prefix"):
+        return None
+    return float(kv["bytes_per_launch"])
+
+
 def hbm_peak():
     pk = load_peaks()
     if pk and pk.get("hbm_gbs"):
@@ -380,7 +400,7 @@ def main():
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": 6 * args.steps,
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (FP8 forward call)", "achieved": achieved,
-                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
                          "peak_basis": peak_basis + " (of measured)"},
             "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"],
             "clocks": r["clocks"], "accuracy": r["acc"]}
