@@ -163,6 +163,24 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
                           int32_t causal, float softmax_scale, void* o, float* lse,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* FP8 forward without a caller workspace (the pages have no counterpart to
+ * this call). For callers that cannot allocate device memory where they run
+ * attention -- a host that owns all device memory and forbids extra
+ * allocations, a plugin inside another runtime's stream-ordered region, a
+ * latency-critical path that must not risk an allocation that synchronises --
+ * the scratch that attn_fp8_fwd keeps in its workspace lives here in one
+ * file-scope device array of 16 MiB per device, held by every GPU that loads
+ * the library until the process exits. Shapes whose attn_workspace_size
+ * exceeds 16 MiB are refused with ATTN_ERR_UNSUPPORTED; nothing is allocated.
+ * The first call on a device (with that device current) looks up the array's
+ * address; make it before any stream capture. All calls share the array:
+ * calls that overlap on the GPU race. Arguments and results are those of
+ * attn_fp8_fwd; `status` (device, may be NULL) receives the call's device
+ * status word (bit e = attn_status e), cleared at the start of the call. */
+attn_status attn_fp8_fwd_noalloc(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                                 const attn_shape* shape, int32_t causal, int32_t causal_exact,
+                                 float softmax_scale, void* o, float* lse, uint32_t* status, void* stream);
+
 /* Synchronises `stream`, reads and clears the device status word in
  * `workspace`, and returns the first error it holds (ATTN_OK if none).
  * flags_out (host, may be NULL) receives the raw bit set (bit e = error e). */

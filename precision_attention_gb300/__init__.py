@@ -39,7 +39,7 @@ ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32 = 0, 1, 2
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
-           "attn_read_device_status", "attn_status_string", "attn_device_sm_count")
+           "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
             L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
             L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+            L.attn_fp8_fwd_noalloc.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, vp]
+            L.attn_fp8_fwd_noalloc.restype = ctypes.c_int32
             L.attn_status_string.argtypes = [i32]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_device_sm_count.argtypes = []
@@ -222,6 +224,30 @@ def attn_bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens:
     _check(lib().attn_bf16_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(shape), int(bool(causal)),
                                float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream(stream)), "attn_bf16_fwd")
+    return out, lse
+
+
+def attn_fp8_fwd_noalloc(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None,
+                         causal: bool = False, causal_exact: bool = False, softmax_scale: float = 0.0,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                         status: torch.Tensor | None = None, stream=None):
+    """attn_fp8_fwd without a workspace: scratch comes from the library's fixed
+    16 MiB device array (for callers that cannot allocate; see include/attn.h).
+    `status`, if given, is a 1-element int32 device tensor that receives the
+    call's device status word. Returns (o, lse)."""
+    T, H, d = q.codes.shape
+    dev = q.codes.device
+    if out is None:
+        out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    shape = make_shape(T, H, d, cu_seqlens)
+    cq, ck, cv = q._c(), k._c(), v._c()
+    _check(lib().attn_fp8_fwd_noalloc(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                                      int(bool(causal)), int(bool(causal_exact)), float(softmax_scale),
+                                      out.data_ptr(), lse.data_ptr(),
+                                      None if status is None else status.data_ptr(), _stream(stream)),
+           "attn_fp8_fwd_noalloc")
     return out, lse
 
 
