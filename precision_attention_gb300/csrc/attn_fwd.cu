@@ -63,6 +63,7 @@ struct Bars {
     uint64_t q_full, q_empty, p_full, o_done;
     uint64_t s_full[2], s_empty[2];
     uint64_t k_full[4], v_full[4], kv_empty[4];
+    float tile_scale[4][2];   // E4M3 tile mode: K and V block scale of the tile in each stage
     uint32_t tmem_base;
     int abort;
 };
@@ -182,6 +183,11 @@ __global__ void __launch_bounds__(192, 1)
                     uint8_t* kt = sm + C::OFF_KV + st * 2 * C::TILE;
                     uint8_t* vt = kt + C::TILE;
                     issued[st] = (g / C::NS) & 1;
+                    if constexpr (MODE == MODE_E4M3_TILE) {
+                        // read by the softmax warps after they observe k_full's phase
+                        B->tile_scale[st][0] = p.sk[w.head * p.capk + d.boff_k + (128 * j) / p.bk];
+                        B->tile_scale[st][1] = p.sv[w.head * p.capv + d.boff_v + (128 * j) / p.bv];
+                    }
                     mbar_arrive_expect_tx(&B->k_full[st], qbytes);
                     for (int a = 0; a < C::ATOMS; a++)
                         tma_load_3d(kt + a * 16384, &tmk, &B->k_full[st], a * C::BOX_ELEMS, w.head, k0);
@@ -322,13 +328,19 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 float s[128];
                 {
-                    uint32_t u[32];
+                    uint32_t u0[32], u1[32], u2[32], u3[32];
+                    const uint32_t ta = tmem + lane_off + b * 128;
+                    tmem_ld32(ta, u0);
+                    tmem_ld32(ta + 32, u1);
+                    tmem_ld32(ta + 64, u2);
+                    tmem_ld32(ta + 96, u3);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        tmem_ld32(tmem + lane_off + b * 128 + c * 32, u);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; i++) s[c * 32 + i] = __uint_as_float(u[i]);
+                    for (int i = 0; i < 32; i++) {
+                        s[i] = __uint_as_float(u0[i]);
+                        s[32 + i] = __uint_as_float(u1[i]);
+                        s[64 + i] = __uint_as_float(u2[i]);
+                        s[96 + i] = __uint_as_float(u3[i]);
                     }
                 }
                 tc_fence_before();
@@ -338,8 +350,15 @@ __global__ void __launch_bounds__(192, 1)
                 float c = p.C;
                 float rj = 1.0f;
                 if constexpr (MODE == MODE_E4M3_TILE) {
-                    const float ks = p.sk[h * p.capk + d.boff_k + k0 / p.bk];
-                    const float sv = p.sv[h * p.capv + d.boff_v + k0 / p.bv];
+                    const int st = gj % C::NS;
+                    // acquire the producer's stores: its arrive on k_full[st] released them, and
+                    // the stage cannot be refilled before this tile's P is handed over
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&B->k_full[st], (gj / C::NS) & 1, abort, lim))) {
+                        ok = false;
+                        break;
+                    }
+                    const float ks = B->tile_scale[st][0];
+                    const float sv = B->tile_scale[st][1];
                     c = qs * ks * p.C;
                     rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
                 }
@@ -360,41 +379,72 @@ __global__ void __launch_bounds__(192, 1)
                     for (int t = 0; t < 128; t++)
                         if (t > lim_k) s[t] = -INFINITY;
                 }
-                float mx = -INFINITY;
+                // a zero block scale would turn masked -inf into NaN: the smallest normal
+                // multiplier keeps -inf and leaves finite scores at about zero instead
+                c = fmaxf(c, 1.17549435e-38f);
+                // row max: eight chains of 3-input max
+                float mx8[8];
 #pragma unroll
-                for (int t = 0; t < 128; t++) mx = fmaxf(mx, s[t]);
-                const float mt = (mx == -INFINITY) ? -INFINITY : mx * c;
+                for (int k8 = 0; k8 < 8; k8++) {
+                    float a = s[16 * k8];
+#pragma unroll
+                    for (int i = 1; i < 15; i += 2) a = fmax3(a, s[16 * k8 + i], s[16 * k8 + i + 1]);
+                    mx8[k8] = fmaxf(a, s[16 * k8 + 15]);
+                }
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                const float mt = mx * c;
                 const float m_new = fmaxf(m, mt);
                 const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
                 const float alpha = (m == -INFINITY) ? 0.0f : ex2(m - m_new);
                 float bias = 8.0f - m_use;
                 if constexpr (MODE == MODE_E4M3_TILE) bias += __log2f(rj);
-                float rowsum = 0.0f;
                 uint32_t pk[ELT == 1 ? 32 : 64];
+                float rowsum;
+                if constexpr (MODE != MODE_E4M3_COL) {
+                    // p = 2^(s * c + bias): pairs through the packed FMA, exp2 on MUFU,
+                    // row sum in four packed accumulators
+                    const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int t = 0; t < 128; t += 4) {
-                    float e[4];
+                    for (int t = 0; t < 128; t += 8) {
+                        float e[8];
 #pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const float x = s[t + u];
-                        e[u] = (x == -INFINITY) ? 0.0f : ex2(fmaf(x, c, bias));
-                        rowsum += e[u];
+                        for (int u = 0; u < 8; u += 2) {
+                            const float2 x = __ffma2_rn(make_float2(s[t + u], s[t + u + 1]), c2, b2);
+                            e[u] = ex2(x.x);
+                            e[u + 1] = ex2(x.y);
+                            acc[u >> 1] = __fadd2_rn(acc[u >> 1], make_float2(e[u], e[u + 1]));
+                        }
+                        if constexpr (ELT == 1) {
+                            pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
+                            pk[t / 4 + 1] = pack_e4m3x4(e[4], e[5], e[6], e[7]);
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 4; u++) pk[t / 2 + u] = pack_bf16x2(e[2 * u], e[2 * u + 1]);
+                        }
                     }
-                    if constexpr (MODE == MODE_E4M3_COL) {
+                    const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+                    const float2 a = __fadd2_rn(a01, a23);
+                    rowsum = a.x + a.y;
+                } else {
+                    float rs8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int t = 0; t < 128; t += 4) {
+                        float e[4];
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
+                            e[u] = ex2(fmaf(s[t + u], c, bias));
+                            rs8[(t + u) & 7] += e[u];
                             const int kl = (k0 + t + u) < L ? k0 + t + u : L - 1;
                             const float sv = p.sv[h * p.capv + d.boff_v + kl / p.bv];
                             const float rt = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
                             e[u] = e[u] * rt;
                         }
-                    }
-                    if constexpr (ELT == 1) {
                         pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
-                    } else {
-                        pk[t / 2] = pack_bf16x2(e[0], e[1]);
-                        pk[t / 2 + 1] = pack_bf16x2(e[2], e[3]);
                     }
+                    rowsum = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 }
                 float ltile = rowsum;
                 if constexpr (MODE == MODE_E4M3_TILE) ltile = rowsum * __fdiv_rn(1.0f, rj);
@@ -414,8 +464,13 @@ __global__ void __launch_bounds__(192, 1)
                             const uint32_t ta = tmem + lane_off + C::T_O + cc * 32;
                             tmem_ld32(ta, u);
                             tmem_wait_ld();
+                            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                            for (int i = 0; i < 32; i++) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 v2 = __fmul2_rn(make_float2(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), a2);
+                                u[i] = __float_as_uint(v2.x);
+                                u[i + 1] = __float_as_uint(v2.y);
+                            }
                             tmem_st32(ta, u);
                         }
                         tmem_wait_st();
@@ -478,36 +533,11 @@ __global__ void __launch_bounds__(192, 1)
 
 // ---------------------------------------------------------------------------
 // host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 // [T][H][D] tensor, box = (box_elems channels, 1 head, 128 tokens)
 static bool make_map(CUtensorMap* m, const void* base, int elt, int T, int H, int D, int box_elems, bool sw128) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)D * elt, (cuuint64_t)H * D * elt};
-    cuuint32_t box[3] = {(cuuint32_t)box_elems, 1, 128};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return make_tensor_map_3d(m, base, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              D, H, T, (uint64_t)D * elt, (uint64_t)H * D * elt, box_elems, 128,
+                              sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 template <int ELT, int D, int MODE>

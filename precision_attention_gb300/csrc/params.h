@@ -1,6 +1,7 @@
 // params.h -- launch parameter blocks shared by the host launchers and the kernels.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -59,6 +60,13 @@ struct FwdParams {
     long long ntcap;
     long long wait_limit;
 };
+
+// host: a 3-D tiled tensor map over [d2][d1][d0] (d0 contiguous), box (box0, 1, box2)
+bool make_tensor_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1,
+                        uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box2,
+                        CUtensorMapSwizzle swizzle);
+// host: multiprocessor count of the current device (cached per device)
+int sm_count();
 
 cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t st);

@@ -202,7 +202,19 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-    return static_cast<uint32_t>(cvt_e4m3x2(a, b)) | (static_cast<uint32_t>(cvt_e4m3x2(c, d)) << 16);
+    uint32_t r;
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;

@@ -1,17 +1,23 @@
-// quant.cu -- fused rotate-and-quantise kernels (one launch per tensor).
+// quant.cu -- fused rotate-and-quantise kernel (one launch per tensor).
 //
 // Sources: "Fused attention kernel", 8-bit forward pass (e4m3 codes, block
 // quantisation, incoherent processing: random sign diagonal times Hadamard,
 // applied to Q and K); FLAMIA section 2 (MX: 32-element blocks, one shared
 // E8M0 scale) and section 4.3 (fused quantisation: one launch instead of many).
 //
-// Thread layout (every kernel): a row = (token, head) of d channels is held by
-// 8 consecutive lanes, EPL = d / 8 channels each (lane sub-index sl holds
-// channels sl*EPL .. sl*EPL+EPL-1); a warp holds 4 rows. The Hadamard
-// transform runs its stages h = 1, 2, 4, ... in that order: in registers while
-// h < EPL, then across the 8 lanes with shuffles (lane ^ 1, ^ 2, ^ 4). Every
-// butterfly is (a, b) -> (a + b, a - b) in fp32 with round-to-nearest, so the
-// result does not depend on how elements are spread over lanes.
+// Work unit: one 128-token tile of one document and one head. The kernel is
+// persistent (two CTAs per SM) and double-buffers units in shared memory: a
+// single TMA copy brings the next tile's 128 rows while the current one is
+// rotated and encoded, so the HBM stream never waits for the arithmetic.
+//
+// Thread layout inside a unit: a row (token, head) of d channels is held by 8
+// consecutive lanes, EPL = d / 8 channels each (lane sub-index sl holds
+// channels sl*EPL .. sl*EPL+EPL-1); a warp holds 4 rows, the 8 warps 32 rows
+// per pass, 4 passes per unit. The Hadamard transform runs its stages
+// h = 1, 2, 4, ... in that order: in registers while h < EPL, then across the
+// 8 lanes with shuffles (lane ^ 1, ^ 2, ^ 4). Every butterfly is
+// (a, b) -> (a + b, a - b) in fp32 round-to-nearest, so the result does not
+// depend on how elements are spread over lanes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,15 +46,16 @@ __device__ __forceinline__ uint32_t sign_mask(const QuantParams& p, int sl) {
     return m;
 }
 
-template <int EPL>
-__device__ __forceinline__ void load_row(const QuantParams& p, int t, int h, int sl, float (&v)[EPL]) {
-    const long long off = (long long)t * p.tstride + (long long)h * p.hstride + sl * EPL;
-    if (p.in_bf16) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x) + off);
+// EPL channels of one row from the shared-memory tile [128 rows][d] (bf16 or fp32)
+template <int EPL, int ELT>
+__device__ __forceinline__ void smem_row(const uint8_t* tile, int row, int sl, float (&v)[EPL]) {
+    constexpr int D = EPL * 8;
+    const uint4* src = reinterpret_cast<const uint4*>(tile + (row * D + sl * EPL) * ELT);
+    if constexpr (ELT == 2) {
 #pragma unroll
         for (int q = 0; q < EPL / 8; q++) {
-            uint4 u = __ldg(src + q);
-            uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const uint4 u = src[q];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 v[q * 8 + 2 * k] = __uint_as_float(w[k] << 16);
@@ -56,14 +63,13 @@ __device__ __forceinline__ void load_row(const QuantParams& p, int t, int h, int
             }
         }
     } else {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + off);
 #pragma unroll
         for (int q = 0; q < EPL / 4; q++) {
-            float4 f = __ldg(src + q);
-            v[q * 4 + 0] = f.x;
-            v[q * 4 + 1] = f.y;
-            v[q * 4 + 2] = f.z;
-            v[q * 4 + 3] = f.w;
+            const uint4 u = src[q];
+            v[q * 4 + 0] = __uint_as_float(u.x);
+            v[q * 4 + 1] = __uint_as_float(u.y);
+            v[q * 4 + 2] = __uint_as_float(u.z);
+            v[q * 4 + 3] = __uint_as_float(u.w);
         }
     }
 }
@@ -98,8 +104,8 @@ __device__ __forceinline__ void rotate_row(float (&v)[EPL], uint32_t smask, int 
 
 __device__ __forceinline__ bool finite_abs(float a) { return a <= 3.402823466e38f; }
 
-// E8M0 exponent X of a block amax (see the header: NOSAT = smallest X with
-// amax <= 448 * 2^X; OCP_FLOOR = floor(log2 amax) - 8), clamped to [-127, 127]
+// E8M0 exponent X of a block amax (NOSAT = smallest X with amax <= 448 * 2^X;
+// OCP_FLOOR = floor(log2 amax) - 8), clamped to [-127, 127]
 __device__ __forceinline__ int e8m0_exponent(float amax, int rule) {
     if (!(amax > 0.0f)) return -127;
     const uint32_t u = __float_as_uint(amax);
@@ -107,7 +113,7 @@ __device__ __forceinline__ int e8m0_exponent(float amax, int rule) {
     if (ef == 0) return -127;                       // subnormal amax: X far below -127
     const int E = ef - 127;
     const uint32_t frac = u & 0x7FFFFFu;
-    int X = (rule == 1) ? E - 8 : (frac <= 0x600000u ? E - 8 : E - 7);   // 1.75 = 1 + 0x600000 / 2^23
+    const int X = (rule == 1) ? E - 8 : (frac <= 0x600000u ? E - 8 : E - 7);   // 1.75 = 1 + 0x600000 / 2^23
     return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 __device__ __forceinline__ float pow2_neg(int X) {   // 2^-X for X in [-127, 126]
@@ -129,344 +135,393 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&y)[EPL],
 }
 
 // ---------------------------------------------------------------------------
-// In-CTA document table: starts and prefix counts of `unit`-token pieces.
-// Returns false (after flagging the status word) when cu_seqlens is malformed.
+// In-CTA document table: starts, prefix counts of 128-token tiles and of
+// scale blocks. Returns false (after flagging the status word) when
+// cu_seqlens is malformed.
 struct DocTable {
     int32_t start[MAX_DOCS + 1];
-    int32_t off[MAX_DOCS + 1];   // exclusive prefix of ceil(L / unit); off[nd] = total
+    int32_t off_tile[MAX_DOCS + 1];   // exclusive prefix of ceil(L / 128); [nd] = total tiles
+    int32_t off_blk[MAX_DOCS + 1];    // exclusive prefix of ceil(L / block)
 };
 
-__device__ bool build_doc_table(const QuantParams& p, int unit, DocTable& tab) {
-    __shared__ int bad;
-    __shared__ int wsum[8];
+__device__ bool build_doc_table(const QuantParams& p, DocTable& tab, int* scratch) {
+    int* bad = scratch;          // [1]
+    int* wsum = scratch + 1;     // [2][8]
     const int tid = threadIdx.x, nd = p.nd;
-    if (tid == 0) bad = 0;
+    if (tid == 0) *bad = 0;
     __syncthreads();
-    // each thread owns up to 4 consecutive documents
-    int cnt[4], acc = 0;
+    int ct[4], cb[4], at = 0, ab = 0;   // each thread owns up to 4 consecutive documents
 #pragma unroll
     for (int k = 0; k < 4; k++) {
         const int i = tid * 4 + k;
-        cnt[k] = 0;
+        ct[k] = cb[k] = 0;
         if (i < nd) {
             const int s = p.cu ? p.cu[i] : 0, e = p.cu ? p.cu[i + 1] : p.T;
             tab.start[i] = s;
-            if (e < s) bad = 1;
-            cnt[k] = (e - s + unit - 1) / unit;
-            if (e < s) cnt[k] = 0;
+            if (e < s) *bad = 1;
+            const int L = e > s ? e - s : 0;
+            ct[k] = (L + 127) / 128;
+            cb[k] = (L + p.block - 1) / p.block;
         }
-        acc += cnt[k];
+        at += ct[k];
+        ab += cb[k];
     }
     if (tid == 0) {
         const int c0 = p.cu ? p.cu[0] : 0, cn = p.cu ? p.cu[nd] : p.T;
-        if (c0 != 0 || cn != p.T) bad = 1;
+        if (c0 != 0 || cn != p.T) *bad = 1;
         tab.start[nd] = cn;
     }
-    // block-wide exclusive scan of acc
     const int lane = tid & 31, warp = tid >> 5;
-    int inc = acc;
+    int it = at, ib = ab;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += v;
+        const int xt = __shfl_up_sync(0xFFFFFFFFu, it, o);
+        const int xb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+        if (lane >= o) { it += xt; ib += xb; }
     }
-    if (lane == 31) wsum[warp] = inc;
+    if (lane == 31) { wsum[warp] = it; wsum[8 + warp] = ib; }
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; w++) base += wsum[w];
-    int run = base + inc - acc;
+    int bt = 0, bb = 0;
+    for (int w = 0; w < warp; w++) { bt += wsum[w]; bb += wsum[8 + w]; }
+    int rt = bt + it - at, rb = bb + ib - ab;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
         const int i = tid * 4 + k;
-        if (i < nd) tab.off[i] = run;
-        run += cnt[k];
+        if (i < nd) { tab.off_tile[i] = rt; tab.off_blk[i] = rb; }
+        rt += ct[k];
+        rb += cb[k];
     }
-    if (tid == blockDim.x - 1) tab.off[nd] = run;
+    if (tid == blockDim.x - 1) { tab.off_tile[nd] = rt; tab.off_blk[nd] = rb; }
     __syncthreads();
-    if (bad) {
+    if (*bad) {
         if (tid == 0) atomicOr(p.status, ST_BAD_SEQLENS);
         return false;
     }
     return true;
 }
 
-__device__ __forceinline__ int find_doc(const DocTable& tab, int nd, int u) {
+__device__ __forceinline__ int find_doc(const int32_t* off, int nd, int u) {
     int lo = 0, hi = nd - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tab.off[mid] <= u) lo = mid; else hi = mid - 1;
+        if (off[mid] <= u) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
 
-// ---------------------------------------------------------------------------
-// E4M3, blocks of BLOCK >= 32 tokens: one CTA (8 warps, 32 rows per pass) per
-// (document-local block, head). scale = amax / 448, code = E4M3(y * (448 / amax)).
-template <int EPL, int PASSES>
-__global__ void __launch_bounds__(256) quant_e4m3_block_kernel(QuantParams p) {
-    __shared__ DocTable tab;
-    __shared__ float red[8];
-    __shared__ int nonfin;
-    if (!build_doc_table(p, p.block, tab)) return;
-    const int H = p.H;
-    const int ub = blockIdx.x / H, h = blockIdx.x % H;
-    if (ub >= tab.off[p.nd]) return;
-    const int doc = find_doc(tab, p.nd, ub);
-    const int s = tab.start[doc], L = tab.start[doc + 1] - s;
-    const int b0 = (ub - tab.off[doc]) * p.block;     // first local token of the block
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sl = lane & 7, rw = lane >> 3;
-    if (threadIdx.x == 0) nonfin = 0;
-    const uint32_t smask = sign_mask<EPL>(p, sl);
+enum { QM_E4M3_BLOCK = 0, QM_E4M3_ROW = 1, QM_MX_ROW = 2, QM_MX_COL = 3 };
 
-    float y[PASSES][EPL];
-    float amax = 0.0f;
-    bool bad = false;
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ps++) {
-        const int lt = b0 + ps * 32 + warp * 4 + rw;   // local token
-        const bool valid = (ps * 32 + warp * 4 + rw) < p.block && lt < L;
-        if (valid) load_row<EPL>(p, s + lt, h, sl, y[ps]);
-        else {
-#pragma unroll
-            for (int i = 0; i < EPL; i++) y[ps][i] = 0.0f;
-        }
-        if (p.rotate) rotate_row<EPL>(y[ps], smask, lane);   // whole warp takes part in the shuffles
-#pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const float a = fabsf(y[ps][i]);
-            if (!finite_abs(a)) bad = true;
-            else amax = fmaxf(amax, a);
-        }
+constexpr int QUANT_THREADS = 256;
+
+// shared memory of the quantise kernel (dynamic; the two input stages first),
+// every offset aligned for what it holds (TMA destinations 128 B, mbarriers 8 B)
+template <int EPL, int ELT>
+struct QuantSmem {
+    static constexpr int STAGE = 128 * EPL * 8 * ELT;   // 128 rows x d elements
+    static constexpr int OFF_TAB = 2 * STAGE;
+    static constexpr int OFF_SCRATCH = (OFF_TAB + (int)sizeof(DocTable) + 127) / 128 * 128;   // 32 ints
+    static constexpr int OFF_RED = OFF_SCRATCH + 32 * 4;                                     // float[8][128]
+    static constexpr int OFF_XS = OFF_RED + 8 * 128 * 4;                                     // int[128]
+    static constexpr int OFF_BAR = OFF_XS + 128 * 4;                                         // uint64[2]
+    static constexpr int OFF_FLAG = OFF_BAR + 2 * 8;                                         // int[2]
+    static constexpr int BYTES = OFF_FLAG + 2 * 4 + 128;                                     // + base alignment
+    static_assert(STAGE % 128 == 0 && OFF_SCRATCH % 128 == 0, "TMA destinations need 128-byte alignment");
+    static_assert(OFF_BAR % 8 == 0, "mbarriers need 8-byte alignment");
+};
+
+// One kernel for every layout. QM_E4M3_BLOCK: blocks of HOLD*32 tokens (32,
+// 64 or 128), amax over the block's rows, scale = amax / 448, codes of
+// y * (448 / amax). QM_E4M3_ROW: the same per (token, head). QM_MX_ROW: E8M0
+// per (token, 32 channels). QM_MX_COL: E8M0 per (32 tokens, channel). MX scale
+// bytes go to the unit's 512-byte tile at (r % 32) * 16 + (r / 32) * 4 + g;
+// rows or groups past the document end get 127.
+template <int EPL, int ELT, int QM, int HOLD>
+__global__ void __launch_bounds__(QUANT_THREADS, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
+    using S = QuantSmem<EPL, ELT>;
+    constexpr int D = EPL * 8;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    DocTable& tab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
+    int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 17 ints
+    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [8][128]
+    int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
+    int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
+    volatile int* abort = flag + 1;
+
+    if (!build_doc_table(p, tab, misc)) return;
+    const int H = p.H, nd = p.nd;
+    const int n_units = tab.off_tile[nd] * H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sl = lane & 7, rw = lane >> 3;
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        flag[0] = 0;
+        flag[1] = 0;
+        fence_mbar_init();
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    __syncthreads();   // nonfin initialised
-    if (bad) nonfin = 1;
-    if (lane == 0) red[warp] = amax;
     __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
-    float inv = 0.0f, scale = 0.0f;
-    if (nonfin) {
-        scale = __int_as_float(0x7FC00000);
-        if (threadIdx.x == 0) atomicOr(p.status, ST_NONFINITE);
-    } else if (amax > 0.0f) {
-        inv = __fdiv_rn(448.0f, amax);
-        scale = __fdiv_rn(amax, 448.0f);
+    int issued[2] = {0, 0};   // loads issued per stage (thread 0 only)
+    auto issue = [&](int u, int st) {
+        issued[st]++;
+        const int g = u / H, h = u % H;
+        const int doc = find_doc(tab.off_tile, nd, g);
+        const int t0 = tab.start[doc] + (g - tab.off_tile[doc]) * 128;
+        mbar_arrive_expect_tx(&full[st], S::STAGE);
+        tma_load_3d(sm + st * S::STAGE, &tmx, &full[st], 0, h, t0);
+    };
+    if (tid == 0) {
+        if (blockIdx.x < n_units) issue(blockIdx.x, 0);
+        if (blockIdx.x + gridDim.x < n_units) issue(blockIdx.x + gridDim.x, 1);
     }
-    if (threadIdx.x == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + ub] = scale;
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ps++) {
-        const int lt = b0 + ps * 32 + warp * 4 + rw;
-        const bool valid = (ps * 32 + warp * 4 + rw) < p.block && lt < L;
-        if (valid) store_codes<EPL>(p.codes + ((long long)(s + lt) * H + h) * p.d + sl * EPL, y[ps], inv);
-    }
-}
-
-// E4M3 with one scale per (token, head) (block 1, the causal-exact layout):
-// 4 rows per warp, amax over the row's 8 lanes. No document table is needed:
-// the block index of token t is t itself.
-template <int EPL>
-__global__ void __launch_bounds__(256) quant_e4m3_row_kernel(QuantParams p) {
-    const int lane = threadIdx.x & 31, sl = lane & 7;
-    const long long row = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);
-    const long long nrows = (long long)p.T * p.H;
-    const bool valid = row < nrows;
-    const int t = valid ? (int)(row / p.H) : 0, h = valid ? (int)(row % p.H) : 0;
     const uint32_t smask = sign_mask<EPL>(p, sl);
-    float y[EPL];
-    if (valid) load_row<EPL>(p, t, h, sl, y);
-    else {
-#pragma unroll
-        for (int i = 0; i < EPL; i++) y[i] = 0.0f;
-    }
-    if (p.rotate) rotate_row<EPL>(y, smask, lane);
-    float amax = 0.0f;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < EPL; i++) {
-        const float a = fabsf(y[i]);
-        if (!finite_abs(a)) bad = true;
-        else amax = fmaxf(amax, a);
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
-    }
-    if (!valid) return;
-    float inv = 0.0f, scale = 0.0f;
-    if (bad) {
-        scale = __int_as_float(0x7FC00000);
-        if (sl == 0) atomicOr(p.status, ST_NONFINITE);
-    } else if (amax > 0.0f) {
-        inv = __fdiv_rn(448.0f, amax);
-        scale = __fdiv_rn(amax, 448.0f);
-    }
-    if (sl == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + t] = scale;
-    store_codes<EPL>(p.codes + ((long long)t * p.H + h) * p.d + sl * EPL, y, inv);
-}
+    bool nonfin = false;
+    int k = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, k++) {
+        const int st = k & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (k >> 1) & 1, abort, 4000000000LL))) break;
+        const uint8_t* tile = sm + st * S::STAGE;
+        const int g = u / H, h = u % H;
+        const int doc = find_doc(tab.off_tile, nd, g);
+        const int s0 = tab.start[doc], L = tab.start[doc + 1] - s0;
+        const int t0 = (g - tab.off_tile[doc]) * 128;      // first local token of the tile
 
-// MX row32 (Q, K; d = 128): one CTA per (document tile of 128 tokens, head),
-// 4 passes of 32 rows. A pair of lanes holds one 32-channel group. The four
-// group exponents of a row go to bytes (r%32)*16 + (r/32)*4 + g of the tile's
-// 512-byte scale block; rows past the document end get 127 (2^0).
-__global__ void __launch_bounds__(256) quant_mx_row_kernel(QuantParams p) {
-    constexpr int EPL = 16;
-    __shared__ DocTable tab;
-    if (!build_doc_table(p, 128, tab)) return;
-    const int H = p.H;
-    const int g = blockIdx.x / H, h = blockIdx.x % H;
-    if (g >= tab.off[p.nd]) return;
-    const int doc = find_doc(tab, p.nd, g);
-    const int s = tab.start[doc], L = tab.start[doc + 1] - s;
-    const int t0 = (g - tab.off[doc]) * 128;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sl = lane & 7, rw = lane >> 3;
-    const uint32_t smask = sign_mask<EPL>(p, sl);
-    uint8_t* tile = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
+        if constexpr (QM == QM_E4M3_BLOCK) {
+            constexpr int NBLK = 4 / HOLD;
 #pragma unroll 1
-    for (int ps = 0; ps < 4; ps++) {
-        const int r = ps * 32 + warp * 4 + rw;
-        const int lt = t0 + r;
-        const bool valid = lt < L;
-        float y[EPL];
-        if (valid) load_row<EPL>(p, s + lt, h, sl, y);
-        else {
+            for (int blk = 0; blk < NBLK; blk++) {
+                if (t0 + blk * HOLD * 32 >= L) break;          // block past the document end (uniform)
+                float y[HOLD][EPL];
+                float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i++) y[i] = 0.0f;
-        }
-        if (p.rotate) rotate_row<EPL>(y, smask, lane);
-        float amax = 0.0f;
-        bool bad = false;
+                for (int hp = 0; hp < HOLD; hp++) {
+                    const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
+                    smem_row<EPL, ELT>(tile, row, sl, y[hp]);
+                    if (t0 + row >= L) {
 #pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const float a = fabsf(y[i]);
-            if (!finite_abs(a)) bad = true;
-            else amax = fmaxf(amax, a);
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
-        if (bad && valid) atomicOr(p.status, ST_NONFINITE);
-        const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
-        // gather the 4 group bytes of the row into lane sl == 0
-        uint32_t byte = (uint32_t)(X + 127);
-        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
-        if (sl == 0) {
-            const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            *reinterpret_cast<uint32_t*>(tile + (r % 32) * 16 + (r / 32) * 4) = word;
-        }
-        if (valid) store_codes<EPL>(p.codes + ((long long)(s + lt) * H + h) * p.d + sl * EPL, y, pow2_neg(X));
-    }
-}
-
-// MX col32 (V; d = 128): one CTA per (32-token group of a document tile, head).
-// Per channel amax over the group's tokens; exponent byte of channel c, group
-// gi of tile g at (c%32)*16 + (c/32)*4 + gi. Groups past the document end get 127.
-__global__ void __launch_bounds__(256) quant_mx_col_kernel(QuantParams p) {
-    constexpr int EPL = 16;
-    __shared__ DocTable tab;
-    __shared__ float red[8][128];
-    __shared__ int xs[128];
-    __shared__ int nonfin;
-    if (!build_doc_table(p, 128, tab)) return;
-    const int H = p.H;
-    const int h = blockIdx.x % H, gg = blockIdx.x / H;
-    const int g = gg >> 2, gi = gg & 3;
-    if (g >= tab.off[p.nd]) return;
-    const int doc = find_doc(tab, p.nd, g);
-    const int s = tab.start[doc], L = tab.start[doc + 1] - s;
-    const int t0 = (g - tab.off[doc]) * 128 + gi * 32;
-    uint8_t* tile = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-    if (threadIdx.x == 0) nonfin = 0;
-    if (t0 >= L) {   // group entirely past the document end
-        if (threadIdx.x < 128) {
-            const int c = threadIdx.x;
-            tile[(c % 32) * 16 + (c / 32) * 4 + gi] = 127;
-        }
-        return;
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, sl = lane & 7, rw = lane >> 3;
-    const int lt = t0 + warp * 4 + rw;
-    const bool valid = lt < L;
-    float y[EPL];
-    if (valid) load_row<EPL>(p, s + lt, h, sl, y);
-    else {
+                        for (int i = 0; i < EPL; i++) y[hp][i] = 0.0f;
+                    }
+                    if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
 #pragma unroll
-        for (int i = 0; i < EPL; i++) y[i] = 0.0f;
-    }
-    if (p.rotate) rotate_row<EPL>(y, sign_mask<EPL>(p, sl), lane);
-    float a[EPL];
-    bool bad = false;
+                    for (int i = 0; i < EPL; i++) {
+                        const float a = fabsf(y[hp][i]);
+                        if (!finite_abs(a)) nonfin = true;
+                        else amax = fmaxf(amax, a);
+                    }
+                }
 #pragma unroll
-    for (int i = 0; i < EPL; i++) {
-        a[i] = fabsf(y[i]);
-        if (!finite_abs(a[i])) { bad = true; a[i] = 0.0f; }
-        a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 8));
-        a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 16));
-    }
-    __syncthreads();
-    if (bad) nonfin = 1;
-    if (rw == 0) {
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
+                if (lane == 0) {
+                    red[warp] = amax;
+                    if (wbad) flag[0] = 1;
+                }
+                __syncthreads();
+                amax = red[0];
 #pragma unroll
-        for (int i = 0; i < EPL; i++) red[warp][sl * EPL + i] = a[i];
-    }
-    __syncthreads();
-    if (threadIdx.x < 128) {
-        const int c = threadIdx.x;
-        float m = red[0][c];
+                for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
+                const bool bad = flag[0] != 0;
+                __syncthreads();                                 // red[] and flag[0] reused by the next block
+                if (tid == 0) flag[0] = 0;
+                float inv = 0.0f, scale = 0.0f;
+                if (bad) scale = __int_as_float(0x7FC00000);
+                else if (amax > 0.0f) {
+                    inv = __fdiv_rn(448.0f, amax);
+                    scale = __fdiv_rn(amax, 448.0f);
+                }
+                if (tid == 0) {
+                    const int b = tab.off_blk[doc] + (t0 + blk * HOLD * 32) / (HOLD * 32);
+                    static_cast<float*>(p.scales)[(long long)h * p.scale_cap + b] = scale;
+                }
 #pragma unroll
-        for (int w = 1; w < 8; w++) m = fmaxf(m, red[w][c]);
-        const int X = e8m0_exponent(m, p.mx_rule);
-        xs[c] = X;
-        tile[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X + 127);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && nonfin) atomicOr(p.status, ST_NONFINITE);
-    if (!valid) return;
-    uint32_t w[EPL / 4];
+                for (int hp = 0; hp < HOLD; hp++) {
+                    const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
+                    if (t0 + row < L)
+                        store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y[hp], inv);
+                }
+            }
+        } else if constexpr (QM == QM_E4M3_ROW) {
+#pragma unroll 1
+            for (int ps = 0; ps < 4; ps++) {
+                const int row = ps * 32 + warp * 4 + rw;
+                const bool valid = t0 + row < L;
+                float y[EPL];
+                smem_row<EPL, ELT>(tile, row, sl, y);
+                if (p.rotate) rotate_row<EPL>(y, smask, lane);
+                float amax = 0.0f;
+                bool bad = false;
 #pragma unroll
-    for (int i = 0; i < EPL / 4; i++) {
-        const int c = sl * EPL + 4 * i;
-        w[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(xs[c])), __fmul_rn(y[4 * i + 1], pow2_neg(xs[c + 1])),
-                           __fmul_rn(y[4 * i + 2], pow2_neg(xs[c + 2])),
-                           __fmul_rn(y[4 * i + 3], pow2_neg(xs[c + 3])));
-    }
-    *reinterpret_cast<uint4*>(p.codes + ((long long)(s + lt) * H + h) * p.d + sl * EPL) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// ---------------------------------------------------------------------------
-// host launcher; returns a cudaError_t
-cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st) {
-    const long long H = p.H;
-    if (layout == 0) {
-        if (p.block == 1) {
-            const long long rows = (long long)p.T * H;
-            const unsigned grid = (unsigned)((rows + 31) / 32);
-            if (p.d == 128) quant_e4m3_row_kernel<16><<<grid, 256, 0, st>>>(p);
-            else quant_e4m3_row_kernel<8><<<grid, 256, 0, st>>>(p);
-        } else {
-            const unsigned grid = (unsigned)(H * p.scale_cap);
-            const int passes = p.block / 32;
-            if (p.d == 128) {
-                if (passes == 1) quant_e4m3_block_kernel<16, 1><<<grid, 256, 0, st>>>(p);
-                else if (passes == 2) quant_e4m3_block_kernel<16, 2><<<grid, 256, 0, st>>>(p);
-                else quant_e4m3_block_kernel<16, 4><<<grid, 256, 0, st>>>(p);
-            } else {
-                if (passes == 1) quant_e4m3_block_kernel<8, 1><<<grid, 256, 0, st>>>(p);
-                else if (passes == 2) quant_e4m3_block_kernel<8, 2><<<grid, 256, 0, st>>>(p);
-                else quant_e4m3_block_kernel<8, 4><<<grid, 256, 0, st>>>(p);
+                for (int i = 0; i < EPL; i++) {
+                    const float a = fabsf(y[i]);
+                    if (!finite_abs(a)) bad = true;
+                    else amax = fmaxf(amax, a);
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
+                }
+                if (valid) {
+                    float inv = 0.0f, scale = 0.0f;
+                    if (bad) {
+                        scale = __int_as_float(0x7FC00000);
+                        nonfin = true;
+                    } else if (amax > 0.0f) {
+                        inv = __fdiv_rn(448.0f, amax);
+                        scale = __fdiv_rn(amax, 448.0f);
+                    }
+                    // block 1: the block index of a token is the token itself
+                    if (sl == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = scale;
+                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, inv);
+                }
+            }
+        } else if constexpr (QM == QM_MX_ROW) {
+            uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
+#pragma unroll 1
+            for (int ps = 0; ps < 4; ps++) {
+                const int r = ps * 32 + warp * 4 + rw;
+                const bool valid = t0 + r < L;
+                float y[EPL];
+                smem_row<EPL, ELT>(tile, r, sl, y);
+                if (p.rotate) rotate_row<EPL>(y, smask, lane);
+                float amax = 0.0f;
+                bool bad = false;
+#pragma unroll
+                for (int i = 0; i < EPL; i++) {
+                    const float a = fabsf(y[i]);
+                    if (!finite_abs(a)) bad = true;
+                    else amax = fmaxf(amax, a);
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
+                if (bad && valid) nonfin = true;
+                const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
+                const uint32_t byte = (uint32_t)(X + 127);
+                const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+                const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+                const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+                if (sl == 0)
+                    *reinterpret_cast<uint32_t*>(sct + (r % 32) * 16 + (r / 32) * 4) =
+                        byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                if (valid)
+                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
+            }
+        } else {   // QM_MX_COL
+            uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
+#pragma unroll 1
+            for (int gi = 0; gi < 4; gi++) {
+                if (t0 + gi * 32 >= L) {                       // group past the document end (uniform)
+                    if (tid < 128) sct[(tid % 32) * 16 + (tid / 32) * 4 + gi] = 127;
+                    continue;
+                }
+                const int row = gi * 32 + warp * 4 + rw;
+                const bool valid = t0 + row < L;
+                float y[EPL];
+                smem_row<EPL, ELT>(tile, row, sl, y);
+                if (!valid) {
+#pragma unroll
+                    for (int i = 0; i < EPL; i++) y[i] = 0.0f;
+                }
+                if (p.rotate) rotate_row<EPL>(y, smask, lane);
+                float a[EPL];
+#pragma unroll
+                for (int i = 0; i < EPL; i++) {
+                    a[i] = fabsf(y[i]);
+                    if (!finite_abs(a[i])) { nonfin = true; a[i] = 0.0f; }
+                    a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 8));
+                    a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 16));
+                }
+                if (rw == 0) {
+#pragma unroll
+                    for (int i = 0; i < EPL; i++) red[warp * 128 + sl * EPL + i] = a[i];
+                }
+                __syncthreads();
+                if (tid < 128) {
+                    float m = red[tid];
+#pragma unroll
+                    for (int w = 1; w < 8; w++) m = fmaxf(m, red[w * 128 + tid]);
+                    const int X = e8m0_exponent(m, p.mx_rule);
+                    xs[tid] = X;
+                    sct[(tid % 32) * 16 + (tid / 32) * 4 + gi] = (uint8_t)(X + 127);
+                }
+                __syncthreads();
+                if (valid) {
+                    uint32_t w4[EPL / 4];
+#pragma unroll
+                    for (int i = 0; i < EPL / 4; i++) {
+                        const int c = sl * EPL + 4 * i;
+                        w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(xs[c])),
+                                            __fmul_rn(y[4 * i + 1], pow2_neg(xs[c + 1])),
+                                            __fmul_rn(y[4 * i + 2], pow2_neg(xs[c + 2])),
+                                            __fmul_rn(y[4 * i + 3], pow2_neg(xs[c + 3])));
+                    }
+                    *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+                __syncthreads();                               // red[] and xs[] reused by the next group
             }
         }
-    } else if (layout == 1) {
-        quant_mx_row_kernel<<<(unsigned)(H * p.scale_cap), 256, 0, st>>>(p);
-    } else {
-        quant_mx_col_kernel<<<(unsigned)(H * p.scale_cap * 4), 256, 0, st>>>(p);
+        __syncthreads();                                       // every read of this stage is done
+        if (tid == 0 && u + 2 * (int)gridDim.x < n_units) issue(u + 2 * gridDim.x, st);
     }
+    if (tid == 0) {
+        // every issued copy must have landed before the CTA's shared memory goes away
+        // (immediate on the normal path, where each issued unit was consumed)
+        for (int st = 0; st < 2; st++)
+            if (issued[st]) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&full[st], (issued[st] - 1) & 1) && clock64() - t0 < 4000000000LL) {
+                }
+            }
+    }
+    if (nonfin) atomicOr(p.status, ST_NONFINITE);
+    if (*abort && tid == 0) atomicOr(p.status, ST_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+template <int EPL, int ELT, int QM, int HOLD>
+static cudaError_t launch_q(const CUtensorMap& m, const QuantParams& p, int grid, cudaStream_t st) {
+    using S = QuantSmem<EPL, ELT>;
+    auto kern = quant_tile_kernel<EPL, ELT, QM, HOLD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, QUANT_THREADS, S::BYTES, st>>>(m, p);
     return cudaGetLastError();
+}
+
+template <int EPL, int ELT>
+static cudaError_t launch_layout(const CUtensorMap& m, const QuantParams& p, int layout, int grid, cudaStream_t st) {
+    if constexpr (EPL == 16) {   // MX layouts: d = 128 only
+        if (layout == 1) return launch_q<EPL, ELT, QM_MX_ROW, 1>(m, p, grid, st);
+        if (layout == 2) return launch_q<EPL, ELT, QM_MX_COL, 1>(m, p, grid, st);
+    } else {
+        if (layout != 0) return cudaErrorInvalidValue;
+    }
+    switch (p.block) {
+        case 1: return launch_q<EPL, ELT, QM_E4M3_ROW, 1>(m, p, grid, st);
+        case 32: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 1>(m, p, grid, st);
+        case 64: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 2>(m, p, grid, st);
+        default: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 4>(m, p, grid, st);
+    }
+}
+
+cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st) {
+    const int elt = p.in_bf16 ? 2 : 4;
+    CUtensorMap m;
+    if (!make_tensor_map_3d(&m, p.x, p.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                            p.d, p.H, p.T, (uint64_t)p.hstride * elt, (uint64_t)p.tstride * elt, p.d, 128,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const long long units = (long long)p.H * (((long long)p.T + 127) / 128 + p.nd);
+    const int sms = sm_count();
+    if (sms < 1) return cudaErrorInvalidDevice;
+    // two CTAs per SM except fp32 rows of 128 channels (128 KB of stages per CTA)
+    const int per_sm = (p.d == 128 && !p.in_bf16) ? 1 : 2;
+    const int grid = (int)(units < (long long)per_sm * sms ? units : (long long)per_sm * sms);
+    if (p.d == 128) return p.in_bf16 ? launch_layout<16, 2>(m, p, layout, grid, st)
+                                     : launch_layout<16, 4>(m, p, layout, grid, st);
+    return p.in_bf16 ? launch_layout<8, 2>(m, p, layout, grid, st) : launch_layout<8, 4>(m, p, layout, grid, st);
 }
 
 }  // namespace pa
