@@ -393,7 +393,10 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 /*           E4M3 layouts multiply the block scales here, MX layouts carry    */
 /*           them inside qhat, khat ("folding score scales", FLAMIA 4.3)      */
 /*   masked keys (causal t > i, keys past the document end): s' = -inf        */
-/*   m'    = max(m, max_t s'_t); alpha = fl32(2^(m - m'))                     */
+/*   m'    = ceil(max_t s'_t) if that max exceeds m (or m is -inf), else m:   */
+/*           an integer frame not below the running max; alpha = 2^(m - m')  */
+/*           (exact; 1 when m' = m): the sketch's rescale, taken only when    */
+/*           the max leaves the frame                                         */
 /*   pt_t  = 2^(s'_t - m' + 8)              (probabilities prescaled by 2^8)  */
 /*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = V block scale / reference   */
 /*                                          (E4M3 layouts), 1 (MX layouts)    */
@@ -496,8 +499,20 @@ static void emu_unit(void* vc, long ri) {
             sp[a] = sc;
             if (sc > mt) mt = sc;
         }
-        float mnew = mt > m ? mt : m;
-        float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
+        /* the running max is kept as an integer frame (log2 units): the smallest
+         * integer not below every score seen so far; it moves (and O, l are
+         * rescaled by the exact power of two 2^(m - m')) only when a tile's max
+         * exceeds it. Probabilities are then at most 2^8, and two computations
+         * that land on different frames differ by an exact power of two in every
+         * probability, which E4M3 rounding preserves. */
+        float mnew, alpha;
+        if (m == -INFINITY || mt > m) {
+            mnew = ceilf(mt);
+            alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
+        } else {
+            mnew = m;
+            alpha = 1.0f;
+        }
         double rowsum = 0.0;
         for (int a = 0; a < kn; a++) {
             double pt = exp2((double)sp[a] - (double)mnew + 8.0);

@@ -35,6 +35,12 @@ namespace pa {
 
 enum { MODE_BF16 = 0, MODE_E4M3_TILE = 1, MODE_E4M3_COL = 2, MODE_MX = 3 };
 
+// 2^k for an integral k <= 0 held in a float (0 below the normal range)
+__device__ __forceinline__ float exp2_int(float k) {
+    const int e = (int)k;
+    return e < -126 ? 0.0f : __int_as_float((127 + e) << 23);
+}
+
 template <int ELT, int D, int MODE>
 struct Cfg {
     static constexpr int RB = D * ELT;                  // bytes per Q/K/V row
@@ -43,29 +49,47 @@ struct Cfg {
     static constexpr int BOX_ELEMS = SW128 ? 128 / ELT : D;
     static constexpr int TILE = 128 * RB;
     static constexpr int PBYTES = 128 * 128 * ELT;
-    static constexpr int NS = ELT == 2 ? 2 : 4;
+    static constexpr int PBUF = ELT == 1 ? 2 : 1;       // P buffers (BF16: one, for shared-memory room)
+    static constexpr int NS = ELT == 2 ? 2 : 5;         // K/V ring depth
     static constexpr int KSTEPS_S = RB / 32;            // 32 bytes of K per MMA
     static constexpr int KSTEPS_PV = 128 * ELT / 32;
     static constexpr int KPER = 32 / ELT;               // keys per P V MMA
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_P = OFF_Q + TILE;
-    static constexpr int OFF_KV = OFF_P + PBYTES;
+    static constexpr int OFF_KV = OFF_P + PBUF * PBYTES;
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
     static constexpr int SF_BYTES = MODE == MODE_MX ? 512 * (2 + 2 * NS) : 0;
-    static constexpr int OFF_BAR = OFF_SF + SF_BYTES;
+    static constexpr int OFF_XCH = OFF_SF + SF_BYTES;       // float [2 parities][2 halves][128 rows] row maxima
+    static constexpr int OFF_XL = OFF_XCH + 2 * 2 * 128 * 4; // float [2 halves][128 rows] row sums
+    static constexpr int OFF_BAR = OFF_XL + 2 * 128 * 4;
     // at least 116 KB so that one CTA (which allocates all 512 TMEM columns) fits per SM
     static constexpr int SMEM = (OFF_BAR + 512 + 1024) > 116 * 1024 ? (OFF_BAR + 512 + 1024) : 116 * 1024;
+    static constexpr int SOFTMAX_WARPS = 8;                  // two warps (column halves) per row quarter
+    static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
+    static constexpr int HC = 64;                            // S columns per softmax thread
+    static constexpr int HD = D / 2;                         // O columns per softmax thread
     // TMEM columns
     static constexpr uint32_t T_O = 256, T_SFQ = 384, T_SFP = 388, T_SFK = 392, T_SFV = 400;
 };
 
 struct Bars {
-    uint64_t q_full, q_empty, p_full, o_done;
+    uint64_t q_full, q_empty;
+    uint64_t p_full[2];       // P of tile g handed over -> p_full[g % PBUF]
+    uint64_t pv_done[2];      // P V of tile g completes -> pv_done[g % PBUF]
     uint64_t s_full[2], s_empty[2];
-    uint64_t k_full[4], v_full[4], kv_empty[4];
-    float tile_scale[4][2];   // E4M3 tile mode: K and V block scale of the tile in each stage
+    uint64_t k_full[8], v_full[8], k_empty[8], v_empty[8];   // K slots free after S, V slots after P V
+    // E4M3 tile mode: score multiplier, log2(r), 1/r of key tile g in slot g % 8. The
+    // producer runs at most NS + 1 tiles ahead of the softmax reading them (it needs
+    // the K slot that S of tile g - NS frees), so eight slots never collide.
+    float tile_scale[8][4];
+    uint64_t sc_full[8];
     uint32_t tmem_base;
     int abort;
+    // the two warps sharing a row quarter exchange row maxima and row sums through
+    // shared memory; ep_max[half][quarter] = 1 + last tile whose maxima are written,
+    // ep_sum[half][quarter] = 1 + last item whose row sums are written
+    int ep_max[2][4];
+    int ep_sum[2][4];
 };
 
 template <int ELT, int D, int MODE>
@@ -96,6 +120,21 @@ __device__ __forceinline__ uint64_t desc_v(uint32_t base, int kk) {
 }
 __device__ __forceinline__ uint64_t desc_sf(uint32_t base) { return sdesc(base, 0, 128, SWZ_NONE); }
 
+// start-address increments (16-byte units) of K step kk for each operand
+template <int ELT, int D, int MODE>
+__device__ __forceinline__ constexpr uint64_t koff(int kk) {
+    using C = Cfg<ELT, D, MODE>;
+    return C::SW128 ? (uint64_t)(((kk * 32) / 128) * (128 * 128) + (kk * 32) % 128) >> 4 : (uint64_t)(kk * 32) >> 4;
+}
+__device__ __forceinline__ constexpr uint64_t poff(int kk) {
+    return (uint64_t)(((kk * 32) / 128) * (128 * 128) + (kk * 32) % 128) >> 4;
+}
+template <int ELT, int D, int MODE>
+__device__ __forceinline__ constexpr uint64_t voff(int kk) {
+    using C = Cfg<ELT, D, MODE>;
+    return C::SW128 ? (uint64_t)(kk * C::KPER * 128) >> 4 : (uint64_t)(kk * C::KPER * 64) >> 4;
+}
+
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
@@ -104,7 +143,7 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long 
 }
 
 template <int ELT, int D, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
     using C = Cfg<ELT, D, MODE>;
@@ -118,16 +157,24 @@ __global__ void __launch_bounds__(192, 1)
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
         mbar_init(&B->q_empty, 1);
-        mbar_init(&B->p_full, 128);
-        mbar_init(&B->o_done, 1);
+        mbar_init(&B->p_full[0], 32 * C::SOFTMAX_WARPS);
+        mbar_init(&B->p_full[1], 32 * C::SOFTMAX_WARPS);
+        for (int i = 0; i < 8; i++) {
+            (&B->ep_max[0][0])[i] = 0;
+            (&B->ep_sum[0][0])[i] = 0;
+        }
+        mbar_init(&B->pv_done[0], 1);
+        mbar_init(&B->pv_done[1], 1);
         for (int i = 0; i < 2; i++) {
             mbar_init(&B->s_full[i], 1);
-            mbar_init(&B->s_empty[i], 128);
+            mbar_init(&B->s_empty[i], 32 * C::SOFTMAX_WARPS);
         }
+        for (int i = 0; i < 8; i++) mbar_init(&B->sc_full[i], 1);
         for (int i = 0; i < C::NS; i++) {
             mbar_init(&B->k_full[i], 1);
             mbar_init(&B->v_full[i], 1);
-            mbar_init(&B->kv_empty[i], 1);
+            mbar_init(&B->k_empty[i], 1);
+            mbar_init(&B->v_empty[i], 1);
         }
         B->abort = 0;
         fence_mbar_init();
@@ -158,165 +205,274 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued[4] = {-1, -1, -1, -1};   // parity of the last load per stage
-            int q_issued = -1;
-            uint32_t g = 0;
-            int qi = 0;
-            for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x, qi++) {
-                const WorkItem w = p.items[it];
-                const DocEntry d = p.docs[w.doc];
-                if (!mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim)) break;
-                const uint32_t qbytes = C::TILE + (MODE == MODE_MX ? 512 : 0);
+        // The whole warp runs the loop: lane 0 issues the copies; in E4M3 tile mode the
+        // lanes first load the block scales of the next 32 key tiles in parallel (one
+        // tile each), so no tile waits on a dependent global load.
+        constexpr unsigned FULL = 0xFFFFFFFFu;
+        int issued[8] = {-1, -1, -1, -1, -1, -1, -1, -1};   // parity of the last load per stage
+        int q_issued = -1;
+        uint32_t g = 0;
+        int qi = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
+            const WorkItem w = p.items[it];
+            const DocEntry d = p.docs[w.doc];
+            float qs = 1.0f, ref = 1.0f;
+            if constexpr (MODE == MODE_E4M3_TILE) {
+                qs = p.sq[w.head * p.capq + d.boff_q + (128 * w.qtile) / p.bq];
+                ref = p.vref[(long long)w.head * p.nd + w.doc];
+            }
+            if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
+            const uint32_t qbytes = C::TILE + (MODE == MODE_MX ? 512 : 0);
+            q_issued = qi & 1;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&B->q_full, qbytes);
-                q_issued = qi & 1;
                 for (int a = 0; a < C::ATOMS; a++)
                     tma_load_3d(sm + C::OFF_Q + a * 16384, &tmq, &B->q_full, a * C::BOX_ELEMS, w.head,
                                 d.start + 128 * w.qtile);
                 if constexpr (MODE == MODE_MX)
                     bulk_load(sm + C::OFF_SF, p.mq + ((long long)w.head * p.ntcap + d.toff + w.qtile) * 512, 512,
                               &B->q_full);
-                for (int j = 0; j < w.ntiles; j++, g++) {
-                    const int st = g % C::NS;
-                    if (!mbar_wait(&B->kv_empty[st], ((g / C::NS) & 1) ^ 1, abort, lim)) break;
+            }
+            float t_c = 0.0f, t_lr = 0.0f, t_ir = 1.0f;   // this lane's tile of the current group of 32
+            for (int j = 0; j < w.ntiles; j++, g++) {
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    if ((j & 31) == 0 && j + lane < w.ntiles) {
+                        // the tile's folded score multiplier and V ratio r = s_v / ref
+                        const int jt = j + lane;
+                        const float ks = p.sk[w.head * p.capk + d.boff_k + (128 * jt) / p.bk];
+                        const float sv = p.sv[w.head * p.capv + d.boff_v + (128 * jt) / p.bv];
+                        const float rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                        t_c = qs * ks * p.C;
+                        t_lr = __log2f(rj);
+                        t_ir = __fdiv_rn(1.0f, rj);
+                    }
+                }
+                const int st = g % C::NS;
+                if (!__all_sync(FULL, mbar_wait(&B->k_empty[st], ((g / C::NS) & 1) ^ 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                issued[st] = (g / C::NS) & 1;
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    const float c = __shfl_sync(FULL, t_c, j & 31);
+                    const float lr = __shfl_sync(FULL, t_lr, j & 31);
+                    const float ir = __shfl_sync(FULL, t_ir, j & 31);
+                    if (lane == 0) {   // released to the softmax warps through sc_full
+                        B->tile_scale[g & 7][0] = c;
+                        B->tile_scale[g & 7][1] = lr;
+                        B->tile_scale[g & 7][2] = ir;
+                        mbar_arrive(&B->sc_full[g & 7]);
+                    }
+                }
+                if (lane == 0) {
                     const int k0 = d.start + 128 * j;
                     uint8_t* kt = sm + C::OFF_KV + st * 2 * C::TILE;
-                    uint8_t* vt = kt + C::TILE;
-                    issued[st] = (g / C::NS) & 1;
-                    if constexpr (MODE == MODE_E4M3_TILE) {
-                        // read by the softmax warps after they observe k_full's phase
-                        B->tile_scale[st][0] = p.sk[w.head * p.capk + d.boff_k + (128 * j) / p.bk];
-                        B->tile_scale[st][1] = p.sv[w.head * p.capv + d.boff_v + (128 * j) / p.bv];
-                    }
                     mbar_arrive_expect_tx(&B->k_full[st], qbytes);
                     for (int a = 0; a < C::ATOMS; a++)
                         tma_load_3d(kt + a * 16384, &tmk, &B->k_full[st], a * C::BOX_ELEMS, w.head, k0);
                     if constexpr (MODE == MODE_MX)
                         bulk_load(sm + C::OFF_SF + 1024 + st * 512,
                                   p.mk + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->k_full[st]);
+                }
+                if (!__all_sync(FULL, mbar_wait(&B->v_empty[st], ((g / C::NS) & 1) ^ 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    uint8_t* vt = sm + C::OFF_KV + st * 2 * C::TILE + C::TILE;
                     mbar_arrive_expect_tx(&B->v_full[st], qbytes);
                     for (int a = 0; a < C::ATOMS; a++)
-                        tma_load_3d(vt + a * 16384, &tmv, &B->v_full[st], a * C::BOX_ELEMS, w.head, k0);
+                        tma_load_3d(vt + a * 16384, &tmv, &B->v_full[st], a * C::BOX_ELEMS, w.head,
+                                    d.start + 128 * j);
                     if constexpr (MODE == MODE_MX)
                         bulk_load(sm + C::OFF_SF + 1024 + C::NS * 512 + st * 512,
                                   p.mv + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->v_full[st]);
                 }
             }
-            if (*abort) {   // let in-flight copies land before shared memory is released
-                if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, lim);
-                for (int s = 0; s < C::NS; s++)
-                    if (issued[s] >= 0) {
-                        wait_drain(&B->k_full[s], (uint32_t)issued[s], lim);
-                        wait_drain(&B->v_full[s], (uint32_t)issued[s], lim);
-                    }
-            }
+        }
+        if (*abort && lane == 0) {   // let in-flight copies land before shared memory is released
+            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, lim);
+            for (int s2 = 0; s2 < C::NS; s2++)
+                if (issued[s2] >= 0) {
+                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], lim);
+                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], lim);
+                }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // One thread. Descriptors are built once: every operand tile sits at a fixed
+        // shared-memory address, so a K step only adds a constant to the start-address
+        // field (addresses stay below 256 KB, the field never carries).
         if (lane == 0) {
-            uint32_t id_s, id_pv;
-            if constexpr (ELT == 2) {
-                id_s = idesc(1, 1, false, false, 128, 128);
-                id_pv = idesc(1, 1, false, true, 128, D);
-            } else {
-                id_s = idesc(0, 0, false, false, 128, 128);
-                id_pv = idesc(0, 0, false, true, 128, D);
-            }
+            constexpr uint32_t id_s = ELT == 2 ? idesc(1, 1, false, false, 128, 128) : idesc(0, 0, false, false, 128, 128);
+            constexpr uint32_t id_pv = ELT == 2 ? idesc(1, 1, false, true, 128, D) : idesc(0, 0, false, true, 128, D);
+            const uint64_t dq = desc_kmajor<ELT, D, MODE>(sQ, 0);
+            const uint64_t dk0 = desc_kmajor<ELT, D, MODE>(sKV, 0);
+            const uint64_t dv0 = desc_v<ELT, D, MODE>(sKV + C::TILE, 0);
+            const uint64_t dp0 = desc_p<ELT>(sP, 0);
+            constexpr uint64_t STAGE16 = (uint64_t)(2 * C::TILE) >> 4;   // descriptor step between stages
+            constexpr uint64_t PBUF16 = (uint64_t)C::PBYTES >> 4;
             if constexpr (MODE == MODE_MX) tc_cp_sf(tmem + C::T_SFP, desc_sf(sSF + 512));
-            uint32_t g = 0, pvc = 0;
-            int qi = 0;
-            auto issue_pv = [&](uint32_t gx, bool first) -> bool {
-                const int st = gx % C::NS;
-                if (!mbar_wait(&B->p_full, pvc & 1, abort, lim)) return false;
-                pvc++;
-                if (!mbar_wait(&B->v_full[st], (gx / C::NS) & 1, abort, lim)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sKV + st * 2 * C::TILE + C::TILE;
-                if constexpr (MODE == MODE_MX) {
-                    const uint32_t sfv = tmem + C::T_SFV + (gx & 1) * 4;
-                    tc_cp_sf(sfv, desc_sf(sSF + 1024 + C::NS * 512 + st * 512));
-#pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                        mma_mxf8(tmem + C::T_O, desc_p<ELT>(sP, kk), desc_v<ELT, D, MODE>(vbase, kk),
-                                 idesc_mx(0, 0, false, true, 128, D, kk, kk), tmem + C::T_SFP, sfv,
-                                 (first && kk == 0) ? 0u : 1u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
-                        if constexpr (ELT == 2)
-                            mma_f16(tmem + C::T_O, desc_p<ELT>(sP, kk), desc_v<ELT, D, MODE>(vbase, kk), id_pv,
-                                    (first && kk == 0) ? 0u : 1u);
-                        else
-                            mma_f8(tmem + C::T_O, desc_p<ELT>(sP, kk), desc_v<ELT, D, MODE>(vbase, kk), id_pv,
-                                   (first && kk == 0) ? 0u : 1u);
-                    }
-                }
-                tc_commit(&B->o_done);
-                tc_commit(&B->kv_empty[st]);
-                return true;
-            };
-            bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
-                const WorkItem w = p.items[it];
-                if (!mbar_wait(&B->q_full, qi & 1, abort, lim)) break;
-                tc_fence_after();
-                if constexpr (MODE == MODE_MX) tc_cp_sf(tmem + C::T_SFQ, desc_sf(sSF));
-                const int nt = w.ntiles;
-                for (int j = 0; j < nt && ok; j++) {
-                    const uint32_t gj = g + j;
-                    const int st = gj % C::NS, b = gj & 1;
-                    if (!mbar_wait(&B->k_full[st], (gj / C::NS) & 1, abort, lim)) { ok = false; break; }
-                    if (!mbar_wait(&B->s_empty[b], ((gj >> 1) & 1) ^ 1, abort, lim)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t kbase = sKV + st * 2 * C::TILE;
-                    const uint32_t dS = tmem + b * 128;
-                    if constexpr (MODE == MODE_MX) {
-                        const uint32_t sfk = tmem + C::T_SFK + (gj & 1) * 4;
-                        tc_cp_sf(sfk, desc_sf(sSF + 1024 + st * 512));
-#pragma unroll
-                        for (int kk = 0; kk < C::KSTEPS_S; kk++)
-                            mma_mxf8(dS, desc_kmajor<ELT, D, MODE>(sQ, kk), desc_kmajor<ELT, D, MODE>(kbase, kk),
-                                     idesc_mx(0, 0, false, false, 128, 128, kk, kk), tmem + C::T_SFQ, sfk,
-                                     kk ? 1u : 0u);
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < C::KSTEPS_S; kk++) {
-                            if constexpr (ELT == 2)
-                                mma_f16(dS, desc_kmajor<ELT, D, MODE>(sQ, kk), desc_kmajor<ELT, D, MODE>(kbase, kk),
-                                        id_s, kk ? 1u : 0u);
-                            else
-                                mma_f8(dS, desc_kmajor<ELT, D, MODE>(sQ, kk), desc_kmajor<ELT, D, MODE>(kbase, kk),
-                                       id_s, kk ? 1u : 0u);
+            // Two streams over the CTA's tiles, items back to back: S = Q K^T of tile g + 2
+            // may start as soon as the softmax has loaded S of tile g (two S buffers), ahead
+            // of O += P V. The thread polls both and issues whichever is ready, so an S never
+            // waits behind a P V whose P is not ready.
+            int itS = blockIdx.x, jS = 0, qiS = 0;     // S stream cursor
+            int itP = blockIdx.x, jP = 0;              // P V stream cursor
+            uint32_t gS = 0, gP = 0;                   // global tile counters
+            WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
+            WorkItem wP = wS;
+            long long t_prog = clock64();
+            while (itP < n_items) {
+                bool progressed = false;
+                if (itS < n_items) {   // the S buffer's s_empty phase is the only limit on running ahead
+                    const int st = gS % C::NS, b = gS & 1;
+                    if ((jS != 0 || mbar_test(&B->q_full, qiS & 1)) && mbar_test(&B->k_full[st], (gS / C::NS) & 1) &&
+                        mbar_test(&B->s_empty[b], ((gS >> 1) & 1) ^ 1)) {
+                        tc_fence_after();
+                        if constexpr (MODE == MODE_MX) {
+                            if (jS == 0) tc_cp_sf(tmem + C::T_SFQ, desc_sf(sSF));
                         }
+                        const uint64_t dk = dk0 + st * STAGE16;
+                        const uint32_t dS = tmem + b * 128;
+                        if constexpr (MODE == MODE_MX) {
+                            const uint32_t sfk = tmem + C::T_SFK + (gS & 1) * 4;
+                            tc_cp_sf(sfk, desc_sf(sSF + 1024 + st * 512));
+#pragma unroll
+                            for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                                mma_mxf8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk),
+                                         idesc_mx(0, 0, false, false, 128, 128, kk, kk), tmem + C::T_SFQ, sfk,
+                                         kk ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < C::KSTEPS_S; kk++) {
+                                if constexpr (ELT == 2)
+                                    mma_f16(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s,
+                                            kk ? 1u : 0u);
+                                else
+                                    mma_f8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s,
+                                           kk ? 1u : 0u);
+                            }
+                        }
+                        tc_commit(&B->s_full[b]);
+                        tc_commit(&B->k_empty[st]);
+                        gS++;
+                        if (++jS == wS.ntiles) {           // last S of the item: Q may be replaced
+                            tc_commit(&B->q_empty);
+                            jS = 0;
+                            qiS++;
+                            itS += gridDim.x;
+                            if (itS < n_items) wS = p.items[itS];
+                        }
+                        progressed = true;
                     }
-                    tc_commit(&B->s_full[b]);
-                    if (j == nt - 1) tc_commit(&B->q_empty);
-                    if (j > 0 && !issue_pv(gj - 1, j == 1)) ok = false;
                 }
-                if (ok && !issue_pv(g + nt - 1, nt == 1)) ok = false;
-                g += nt;
+                if (gP < gS) {
+                    const int st = gP % C::NS;
+                    if (mbar_test(&B->p_full[gP % C::PBUF], (gP / C::PBUF) & 1) &&
+                        mbar_test(&B->v_full[st], (gP / C::NS) & 1)) {
+                        tc_fence_after();
+                        const uint64_t dv = dv0 + st * STAGE16;
+                        const uint64_t dp = dp0 + (gP % C::PBUF) * PBUF16;
+                        const bool first = jP == 0;
+                        if constexpr (MODE == MODE_MX) {
+                            const uint32_t sfv = tmem + C::T_SFV + (gP & 1) * 4;
+                            tc_cp_sf(sfv, desc_sf(sSF + 1024 + C::NS * 512 + st * 512));
+#pragma unroll
+                            for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                                mma_mxf8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk),
+                                         idesc_mx(0, 0, false, true, 128, D, kk, kk), tmem + C::T_SFP, sfv,
+                                         (first && kk == 0) ? 0u : 1u);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
+                                if constexpr (ELT == 2)
+                                    mma_f16(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                                            (first && kk == 0) ? 0u : 1u);
+                                else
+                                    mma_f8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                                           (first && kk == 0) ? 0u : 1u);
+                            }
+                        }
+                        tc_commit(&B->pv_done[gP % C::PBUF]);
+                        tc_commit(&B->v_empty[st]);
+                        gP++;
+                        if (++jP == wP.ntiles) {
+                            jP = 0;
+                            itP += gridDim.x;
+                            if (itP < n_items) wP = p.items[itP];
+                        }
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    t_prog = clock64();
+                } else if (*abort || clock64() - t_prog > lim) {
+                    *abort = 1;
+                    break;
+                }
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;                       // query row within the tile
+        // warps 2..9: the two warps with the same TMEM lane quarter share the
+        // 32 rows of that quarter, each taking one half of the S columns
+        // (and of the O columns); they combine row maxima through shared memory
+        // and a 64-thread named barrier.
+        const int hh = (warp - 2) >> 2;                           // column half
+        const int quarter = warp & 3;                             // TMEM lane quarter
+        const int r = quarter * 32 + lane;                        // query row within the tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        uint32_t g = 0, pvw = 0;
+        int items_done = 0;
+        // publish this warp's values (already stored) as epoch `e` and wait, bounded and
+        // abort-aware, until the partner warp has published the same epoch
+        auto pair_exchange = [&](int* mine, int* theirs, int e) -> bool {
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                *reinterpret_cast<volatile int*>(mine) = e;
+            }
+            bool got = true;
+            if (lane == 0) {
+                const volatile int* t = reinterpret_cast<const volatile int*>(theirs);
+                if (*t < e) {
+                    const long long t0 = clock64();
+                    while (*t < e) {
+                        if (*abort || clock64() - t0 > lim) {
+                            *abort = 1;
+                            got = false;
+                            break;
+                        }
+                    }
+                }
+                __threadfence_block();
+            }
+            return __shfl_sync(0xFFFFFFFFu, (int)got, 0) != 0;
+        };
+        float* xch = reinterpret_cast<float*>(sm + C::OFF_XCH);   // [parity][half][row]
+        float* xl = reinterpret_cast<float*>(sm + C::OFF_XL);     // [half][row]
+        uint32_t g = 0;
         bool ok = true;
+        // P V of global tile gx has completed (its barrier cannot move further before
+        // this thread hands over a later P)
+        auto wait_pv = [&](uint32_t gx) -> bool {
+            return __all_sync(0xFFFFFFFFu, mbar_wait(&B->pv_done[gx % C::PBUF], (gx / C::PBUF) & 1, abort, lim));
+        };
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
             const int h = w.head, L = d.len, nt = w.ntiles;
-            const int rloc = 128 * w.qtile + r;                  // row position in the document
+            const int rloc = 128 * w.qtile + r;                   // row position in the document
             const int rcl = rloc < L ? rloc : L - 1;
             float qs = 1.0f, ref = 1.0f;
-            if constexpr (MODE == MODE_E4M3_TILE) qs = p.sq[h * p.capq + d.boff_q + (128 * w.qtile) / p.bq];
-            if constexpr (MODE == MODE_E4M3_COL) qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
-            if constexpr (MODE == MODE_E4M3_TILE || MODE == MODE_E4M3_COL)
+            if constexpr (MODE == MODE_E4M3_COL) {
+                qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
+            }
+            if constexpr (MODE == MODE_E4M3_TILE) ref = p.vref[(long long)h * p.nd + w.doc];
             float m = -INFINITY, l = 0.0f;
             for (int j = 0; j < nt; j++) {
                 const uint32_t gj = g + j;
@@ -326,80 +482,78 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                float s[128];
+                float s[C::HC];
                 {
-                    uint32_t u0[32], u1[32], u2[32], u3[32];
-                    const uint32_t ta = tmem + lane_off + b * 128;
+                    uint32_t u0[32], u1[32];
+                    const uint32_t ta = tmem + lane_off + b * 128 + hh * C::HC;
                     tmem_ld32(ta, u0);
                     tmem_ld32(ta + 32, u1);
-                    tmem_ld32(ta + 64, u2);
-                    tmem_ld32(ta + 96, u3);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
                         s[i] = __uint_as_float(u0[i]);
                         s[32 + i] = __uint_as_float(u1[i]);
-                        s[64 + i] = __uint_as_float(u2[i]);
-                        s[96 + i] = __uint_as_float(u3[i]);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&B->s_empty[b]);
-                const int k0 = 128 * j;                           // first key position of the tile
-                // score multiplier
-                float c = p.C;
-                float rj = 1.0f;
+                const int k0 = 128 * j + hh * C::HC;                // first key position of this thread's columns
+                float c = p.C, lr = 0.0f, invr = 1.0f;
                 if constexpr (MODE == MODE_E4M3_TILE) {
-                    const int st = gj % C::NS;
-                    // acquire the producer's stores: its arrive on k_full[st] released them, and
-                    // the stage cannot be refilled before this tile's P is handed over
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&B->k_full[st], (gj / C::NS) & 1, abort, lim))) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&B->sc_full[gj & 7], (gj >> 3) & 1, abort, lim))) {
                         ok = false;
                         break;
                     }
-                    const float ks = B->tile_scale[st][0];
-                    const float sv = B->tile_scale[st][1];
-                    c = qs * ks * p.C;
-                    rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                    c = B->tile_scale[gj & 7][0];
+                    lr = B->tile_scale[gj & 7][1];
+                    invr = B->tile_scale[gj & 7][2];
                 }
+                tc_fence_before();
+                mbar_arrive(&B->s_empty[b]);
                 if constexpr (MODE == MODE_E4M3_COL) {
                     const float qc = qs * p.C;
 #pragma unroll 8
-                    for (int t = 0; t < 128; t++) {
+                    for (int t = 0; t < C::HC; t++) {
                         const int kl = (k0 + t) < L ? k0 + t : L - 1;
                         s[t] = s[t] * (p.sk[h * p.capk + d.boff_k + kl / p.bk] * qc);
                     }
                     c = 1.0f;
                 }
                 const bool diag = p.causal && j == w.qtile;
-                const bool tail = !p.causal && (k0 + 128 > L);
+                const bool tail = !p.causal && (128 * j + 128 > L);
                 if (diag || tail) {
-                    const int lim_k = diag ? (rloc - k0) : (L - 1 - k0);   // last visible key offset
+                    const int lim_k = diag ? (rloc - k0) : (L - 1 - k0);   // last visible column offset
 #pragma unroll
-                    for (int t = 0; t < 128; t++)
+                    for (int t = 0; t < C::HC; t++)
                         if (t > lim_k) s[t] = -INFINITY;
                 }
                 // a zero block scale would turn masked -inf into NaN: the smallest normal
                 // multiplier keeps -inf and leaves finite scores at about zero instead
                 c = fmaxf(c, 1.17549435e-38f);
-                // row max: eight chains of 3-input max
-                float mx8[8];
+                // row max of this half: four chains of 3-input max, then the partner's half
+                float mx4[4];
 #pragma unroll
-                for (int k8 = 0; k8 < 8; k8++) {
-                    float a = s[16 * k8];
+                for (int k4 = 0; k4 < 4; k4++) {
+                    float a = s[16 * k4];
 #pragma unroll
-                    for (int i = 1; i < 15; i += 2) a = fmax3(a, s[16 * k8 + i], s[16 * k8 + i + 1]);
-                    mx8[k8] = fmaxf(a, s[16 * k8 + 15]);
+                    for (int i2 = 1; i2 < 15; i2 += 2) a = fmax3(a, s[16 * k4 + i2], s[16 * k4 + i2 + 1]);
+                    mx4[k4] = fmaxf(a, s[16 * k4 + 15]);
                 }
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
+                const float pmax = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+                xch[((gj & 1) * 2 + hh) * 128 + r] = pmax;
+                if (!pair_exchange(&B->ep_max[hh][quarter], &B->ep_max[hh ^ 1][quarter], (int)gj + 1)) {
+                    ok = false;
+                    break;
+                }
+                const float mx = fmaxf(pmax, xch[((gj & 1) * 2 + (hh ^ 1)) * 128 + r]);
+                // integer frame for the running max (log2 units): the smallest integer not
+                // below every score so far. It moves only when a tile's max leaves it; O and
+                // l are then rescaled by the exact power of two 2^(m - m_new), and P <= 2^8.
                 const float mt = mx * c;
-                const float m_new = fmaxf(m, mt);
+                const bool upd = (m == -INFINITY) || (mt > m);
+                const float m_new = upd ? ceilf(mt) : m;
                 const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-                const float alpha = (m == -INFINITY) ? 0.0f : ex2(m - m_new);
-                float bias = 8.0f - m_use;
-                if constexpr (MODE == MODE_E4M3_TILE) bias += __log2f(rj);
-                uint32_t pk[ELT == 1 ? 32 : 64];
+                const float alpha = (m == -INFINITY) ? 0.0f : (upd ? exp2_int(m - m_new) : 1.0f);
+                const float bias = 8.0f - m_use + lr;
+                uint32_t pk[ELT == 1 ? 16 : 32];
                 float rowsum;
                 if constexpr (MODE != MODE_E4M3_COL) {
                     // p = 2^(s * c + bias): pairs through the packed FMA, exp2 on MUFU,
@@ -408,7 +562,7 @@ __global__ void __launch_bounds__(192, 1)
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                      make_float2(0.f, 0.f)};
 #pragma unroll
-                    for (int t = 0; t < 128; t += 8) {
+                    for (int t = 0; t < C::HC; t += 8) {
                         float e[8];
 #pragma unroll
                         for (int u = 0; u < 8; u += 2) {
@@ -429,14 +583,14 @@ __global__ void __launch_bounds__(192, 1)
                     const float2 a = __fadd2_rn(a01, a23);
                     rowsum = a.x + a.y;
                 } else {
-                    float rs8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                    float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int t = 0; t < 128; t += 4) {
+                    for (int t = 0; t < C::HC; t += 4) {
                         float e[4];
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
                             e[u] = ex2(fmaf(s[t + u], c, bias));
-                            rs8[(t + u) & 7] += e[u];
+                            rs4[u] += e[u];
                             const int kl = (k0 + t + u) < L ? k0 + t + u : L - 1;
                             const float sv = p.sv[h * p.capv + d.boff_v + kl / p.bv];
                             const float rt = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
@@ -444,79 +598,95 @@ __global__ void __launch_bounds__(192, 1)
                         }
                         pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
                     }
-                    rowsum = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                    rowsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
                 }
-                float ltile = rowsum;
-                if constexpr (MODE == MODE_E4M3_TILE) ltile = rowsum * __fdiv_rn(1.0f, rj);
-                l = alpha * l + ltile;
+                l = alpha * l + rowsum * invr;
                 m = m_new;
-                if (j > 0) {
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&B->o_done, pvw & 1, abort, lim))) {
+                // O rescale (when any row of the warp moved its max): after P V of the
+                // previous tile, before this tile's P is handed over
+                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    if (!wait_pv(gj - 1)) {
                         ok = false;
                         break;
                     }
-                    pvw++;
                     tc_fence_after();
-                    if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    {
                         uint32_t u[32];
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int cc = 0; cc < D / 32; cc++) {
-                            const uint32_t ta = tmem + lane_off + C::T_O + cc * 32;
+                        for (int cc = 0; cc < C::HD / 32; cc++) {
+                            const uint32_t ta = tmem + lane_off + C::T_O + hh * C::HD + cc * 32;
                             tmem_ld32(ta, u);
                             tmem_wait_ld();
-                            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                const float2 v2 = __fmul2_rn(make_float2(__uint_as_float(u[i]), __uint_as_float(u[i + 1])), a2);
-                                u[i] = __float_as_uint(v2.x);
-                                u[i + 1] = __float_as_uint(v2.y);
+                            for (int i2 = 0; i2 < 32; i2 += 2) {
+                                const float2 v2 =
+                                    __fmul2_rn(make_float2(__uint_as_float(u[i2]), __uint_as_float(u[i2 + 1])), a2);
+                                u[i2] = __float_as_uint(v2.x);
+                                u[i2 + 1] = __float_as_uint(v2.y);
                             }
                             tmem_st32(ta, u);
                         }
                         tmem_wait_st();
                     }
                 }
-                // P row -> shared memory, 128-byte swizzled K-major rows
+                // the P buffer of this tile was last read by P V of tile gj - PBUF
+                if (gj >= (uint32_t)C::PBUF && !wait_pv(gj - C::PBUF)) {
+                    ok = false;
+                    break;
+                }
+                // this half of the P row -> shared memory (128-byte swizzled K-major rows)
+                uint8_t* pbuf = sm + C::OFF_P + (gj % C::PBUF) * C::PBYTES;
 #pragma unroll
-                for (int ch = 0; ch < 8 * ELT; ch++) {
-                    const int atom = ch >> 3, cc = ch & 7;
-                    uint8_t* dst = sm + C::OFF_P + atom * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
+                for (int ch = 0; ch < 4 * ELT; ch++) {
+                    const int gch = hh * 4 * ELT + ch;                 // 16-byte chunk within the row
+                    const int atom = gch >> 3, cc = gch & 7;
+                    uint8_t* dst = pbuf + atom * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&B->p_full);
+                mbar_arrive(&B->p_full[gj % C::PBUF]);
             }
             if (!ok) break;
-            // epilogue: O / l -> bf16, lse
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&B->o_done, pvw & 1, abort, lim))) {
+            // epilogue: row sum of both halves, O / l -> bf16 (this half of the columns), lse
+            xl[hh * 128 + r] = l;
+            if (!pair_exchange(&B->ep_sum[hh][quarter], &B->ep_sum[hh ^ 1][quarter], ++items_done)) {
                 ok = false;
                 break;
             }
-            pvw++;
+            const float lt = l + xl[(hh ^ 1) * 128 + r];
+            if (!wait_pv(g + nt - 1)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const float fin = (l > 0.0f) ? __fdiv_rn(ref, l) : 0.0f;
+            const float fin = (lt > 0.0f) ? __fdiv_rn(ref, lt) : 0.0f;
             const bool store = rloc < L;
-            uint16_t* orow = p.o + ((long long)(d.start + rcl) * p.H + h) * D;
+            uint16_t* orow = p.o + ((long long)(d.start + rcl) * p.H + h) * D + hh * C::HD;
+            const float2 f2 = make_float2(fin, fin);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; cc++) {
+            for (int cc = 0; cc < C::HD / 32; cc++) {
                 uint32_t u[32];
-                tmem_ld32(tmem + lane_off + C::T_O + cc * 32, u);
+                tmem_ld32(tmem + lane_off + C::T_O + hh * C::HD + cc * 32, u);
                 tmem_wait_ld();
                 uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; i++)
-                    packed[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * fin, __uint_as_float(u[2 * i + 1]) * fin);
+                for (int i2 = 0; i2 < 16; i2++) {
+                    const float2 v2 =
+                        __fmul2_rn(make_float2(__uint_as_float(u[2 * i2]), __uint_as_float(u[2 * i2 + 1])), f2);
+                    packed[i2] = pack_bf16x2(v2.x, v2.y);
+                }
                 if (store) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                    for (int i2 = 0; i2 < 4; i2++)
+                        dst[i2] = make_uint4(packed[4 * i2], packed[4 * i2 + 1], packed[4 * i2 + 2], packed[4 * i2 + 3]);
                 }
             }
-            if (store)
+            if (store && hh == 0)
                 p.lse[(long long)h * p.T + d.start + rloc] =
-                    (l > 0.0f) ? 0.69314718055994531f * (m + __log2f(l) - 8.0f) : -INFINITY;
+                    (lt > 0.0f) ? 0.69314718055994531f * (m + __log2f(lt) - 8.0f) : -INFINITY;
             tc_fence_before();
             g += nt;
         }
@@ -552,7 +722,7 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
     auto kern = attn_fwd_kernel<ELT, D, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, C::SMEM, st>>>(mq, mk, mv, p);
+    kern<<<grid, C::THREADS, C::SMEM, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 

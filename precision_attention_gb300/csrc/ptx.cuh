@@ -37,6 +37,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// non-blocking test of the phase with the given parity
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete. Gives up after
 // `limit` SM clock cycles or when *abort becomes non-zero; returns false then
 // (and raises *abort itself on a timeout). No wait in this library is unbounded.
@@ -142,15 +155,13 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
+        "l"(a), "l"(b), "r"(id), "r"(acc));
 }
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
+        "l"(a), "l"(b), "r"(id), "r"(acc));
 }
 __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t sfa,
                                          uint32_t sfb, uint32_t acc) {
@@ -158,13 +169,12 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
+        "l"(a), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc));
 }
 // 32 lanes x 128 bits from shared memory, replicated into the four 32-lane
 // quarters of TMEM (the scale-factor copy of block-scaled MMAs)
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t src_desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc));
 }
 
 // 32 lanes x 32 bits, 32 consecutive columns: thread i of the warp gets lane

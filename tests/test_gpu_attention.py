@@ -76,6 +76,23 @@ def test_fp8_forward_matches_emulation(oracle_mod, wid, lengths, H, mx, block, c
     assert res["ok"], res
 
 
+@pytest.mark.parametrize("wid,mx,causal", [(2, False, False), (3, False, True), (4, True, False), (5, True, True)])
+def test_fp8_forward_many_items_per_cta(oracle_mod, wid, mx, causal):
+    """Long documents and enough (doc, head, tile) items that every CTA runs
+    several items of 32 key tiles back to back; rows are sampled for the
+    oracle (every head, first / last rows of each tile position, random rest)."""
+    lens = [4096, 4096]
+    inp = workloads.make(wid, heads=8, lengths=lens)
+    o, lse = run_gpu(inp, mx, 32 if mx else 128, causal)
+    rng = np.random.default_rng(wid)
+    T = inp.T
+    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(T - 130, T), rng.choice(T, 200, replace=False),
+                                     np.array([4095, 4096, 4097])])).astype(np.int32)
+    _, ob, le = run_emu(inp, mx, 32 if mx else 128, causal, rows=rows)
+    res = compare_outputs(o, lse, ob, le, rows=rows)
+    assert res["ok"], res
+
+
 def test_fp8_forward_deterministic():
     inp = workloads.make(3, heads=2, lengths=[300, 200])
     o1, l1 = run_gpu(inp, False, 128, True)
