@@ -135,6 +135,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the job's
+    time); a no-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(world, flops_per_rank, ms_per_step):
+    """Whole-job TFLOP/s: every rank runs its own replica (weak scaling), so the
+    job does world x flops_per_rank in the slowest rank's step time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import precision_attention_gb300 as pa
@@ -248,9 +267,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     ms_step = ms_total / args.steps
     if dist:
-        t = torch.tensor([ms_step, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms = float(t[0]), float(t[1])
+        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev)
     return {"inp": inp, "ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "acc": acc, "T": T, "H": H, "d": d, "nd": nd}
 
@@ -389,8 +406,8 @@ def main():
             dist.destroy_process_group()
         return
     w = workloads.WORKLOADS[args.workload]
-    value = world * r["flops"] / (r["ms_step"] * 1e-3) / 1e12
-    e2e = world * r["flops"] / (r["e2e_ms"] * 1e-3) / 1e12
+    value = job_throughput(world, r["flops"], r["ms_step"])
+    e2e = job_throughput(world, r["flops"], r["e2e_ms"])
     peak, peak_basis = fp8_peak()
     achieved = r["flops"] / (r["attn_ms"] * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
