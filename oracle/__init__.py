@@ -82,7 +82,7 @@ def lib():
             L.or_quantize.restype = i32
             L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
             L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
-                i32, i32, i32, vp, i32, i32, i32, i32, dbl, i32, vp, i32, vp, vp, vp]
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, i32, vp, i32, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
             _lib = L
     return _lib
@@ -259,8 +259,11 @@ def attention_fp64(q, k, v, cu_seqlens=None, causal=False, softmax_scale=None, r
 
 # ---- O-3 -------------------------------------------------------------------
 def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causal=False,
-                      exact=False, softmax_scale=None, rows=None, quantize_p=True):
-    """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R])."""
+                      exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False):
+    """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R]),
+    and with ties=True a fourth array [R,H,d]: the tie allowance (how far E4M3
+    probability codes that sit within rounding of a code boundary can move each
+    output element)."""
     T, H, d = q.codes.shape
     if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
         raise ValueError("Q and K must carry the same rotation")
@@ -271,14 +274,16 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
     o = np.zeros((R, H, d), dtype=np.float32)
     ob = np.zeros((R, H, d), dtype=np.uint16)
     lse = np.zeros((H, R), dtype=np.float32)
+    amb = np.zeros((R, H, d), dtype=np.float32) if ties else None
     qq, kk, vv = q._qt(), k._qt(), v._qt()
     st = lib().or_attention_emulate(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
                                     _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
                                     int(bool(q.rotated)), scale, QUANTIZE_P if quantize_p else 0,
-                                    _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data)
+                                    _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data,
+                                    None if amb is None else amb.ctypes.data)
     if st != 0:
         raise ValueError(f"oracle emulation rejected its arguments (status {st})")
-    return o, ob, lse
+    return (o, ob, lse, amb) if ties else (o, ob, lse)
 
 
 def bf16_bits_to_f32(b) -> np.ndarray:

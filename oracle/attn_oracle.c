@@ -393,10 +393,7 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 /*           E4M3 layouts multiply the block scales here, MX layouts carry    */
 /*           them inside qhat, khat ("folding score scales", FLAMIA 4.3)      */
 /*   masked keys (causal t > i, keys past the document end): s' = -inf        */
-/*   m'    = ceil(max_t s'_t) if that max exceeds m (or m is -inf), else m:   */
-/*           an integer frame not below the running max; alpha = 2^(m - m')  */
-/*           (exact; 1 when m' = m): the sketch's rescale, taken only when    */
-/*           the max leaves the frame                                         */
+/*   m'    = max(m, max_t s'_t); alpha = fl32(2^(m - m'))                     */
 /*   pt_t  = 2^(s'_t - m' + 8)              (probabilities prescaled by 2^8)  */
 /*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = V block scale / reference   */
 /*                                          (E4M3 layouts), 1 (MX layouts)    */
@@ -409,10 +406,24 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 /* mode, max of the V token scales at positions <= i, so that no later token */
 /* reaches row i (FLAMIA 1 and 4.5: exact options remove within-block        */
 /* dependencies).                                                            */
+/*                                                                           */
+/* Optional second output, amb: where several results are correct. A GPU     */
+/* computes S in fp32 in its own summation order and 2^x with an fp32        */
+/* approximation, so a probability lying within that rounding of an E4M3     */
+/* boundary may take either neighbouring code; both are faithful results.    */
+/* For each such key the emulation adds |code_hi - code_lo| * |vhat_tc| to   */
+/* amb (rescaled and normalised like O), so that a parity check can accept   */
+/* exactly the differences these ties explain. The error model, in log2      */
+/* units of the exponent x = s' - m' + 8:                                    */
+/*   dx = 2^-20 (|cf| A_t + A_m) + 2^-21 (|s'_t| + |m'| + 8),                */
+/*   A_t = sum_c |qhat_c khat_c|; 2^-20 A_t covers an fp32 sum of the d      */
+/*   products in any tree of depth <= 16 (each level rounds by 2^-24 A_t),  */
+/*   A_m = the largest |cf| A of the keys so far (error of the running max),*/
+/*   cf the factor from S to s'; relative band on pt: ln2 dx + 2^-20.        */
 /* ------------------------------------------------------------------------- */
 typedef struct {
     const or_qtensor *q, *k, *v; int T, H, d; docs_t D; int causal, exact, rotated; double scale;
-    int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse;
+    int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse; float* amb;
     double dec[256];
     long nbq, nbk, nbv, ngv;     /* block counts of the logical scale arrays */
     int h;                       /* head being evaluated */
@@ -480,39 +491,40 @@ static void emu_unit(void* vc, long ri) {
 
     float m = -INFINITY, l = 0.0f;
     float O[256];
-    for (int x = 0; x < d; x++) O[x] = 0.0f;
+    double Am[256];
+    for (int x = 0; x < d; x++) O[x] = 0.0f, Am[x] = 0.0;
     int nkeys = c->causal ? i + 1 : L;
     int ntiles = (nkeys + 127) / 128;
     float sp[128];
-    double ph[128];
+    double ph[128], at[128], tie[128];
+    double amax = 0.0;
     for (int jt = 0; jt < ntiles; jt++) {
         int k0 = jt * 128, kn = (nkeys - k0) < 128 ? nkeys - k0 : 128;
         float mt = -INFINITY;
+        double cf = 0.0;
         for (int a = 0; a < kn; a++) {
             const double* kr = c->kh + (long)(s0 + k0 + a) * d;
-            double acc = 0.0;
-            for (int j = 0; j < d; j++) acc += qh[j] * kr[j];
+            double acc = 0.0, aa = 0.0;
+            for (int j = 0; j < d; j++) {
+                acc += qh[j] * kr[j];
+                aa += fabs(qh[j] * kr[j]);
+            }
             float S = (float)acc;
             float sc;
-            if (mx) sc = S * C32;
-            else sc = S * (float)((double)qs * (double)ks_row[(k0 + a) / kb] * C);
+            if (mx) {
+                cf = C32;
+                sc = S * C32;
+            } else {
+                cf = (float)((double)qs * (double)ks_row[(k0 + a) / kb] * C);
+                sc = S * (float)cf;
+            }
             sp[a] = sc;
+            at[a] = fabs(cf) * aa;
+            if (at[a] > amax) amax = at[a];
             if (sc > mt) mt = sc;
         }
-        /* the running max is kept as an integer frame (log2 units): the smallest
-         * integer not below every score seen so far; it moves (and O, l are
-         * rescaled by the exact power of two 2^(m - m')) only when a tile's max
-         * exceeds it. Probabilities are then at most 2^8, and two computations
-         * that land on different frames differ by an exact power of two in every
-         * probability, which E4M3 rounding preserves. */
-        float mnew, alpha;
-        if (m == -INFINITY || mt > m) {
-            mnew = ceilf(mt);
-            alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
-        } else {
-            mnew = m;
-            alpha = 1.0f;
-        }
+        float mnew = mt > m ? mt : m;
+        float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
         double rowsum = 0.0;
         for (int a = 0; a < kn; a++) {
             double pt = exp2((double)sp[a] - (double)mnew + 8.0);
@@ -524,12 +536,26 @@ static void emu_unit(void* vc, long ri) {
             }
             float pr = (float)(pt * r);
             ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[or_e4m3_encode(pr)] : (double)pr;
+            tie[a] = 0.0;
+            if (c->amb && (c->flags & OR_EMU_QUANTIZE_P) && pt > 0.0) {
+                double dx = ldexp(at[a] + amax, -20) +
+                            ldexp(fabs((double)sp[a]) + fabs((double)mnew) + 8.0, -21);
+                double band = 0.6931471805599453 * dx + ldexp(1.0, -20);
+                uint8_t lo = or_e4m3_encode((float)(pr * (1.0 - band)));
+                uint8_t hi = or_e4m3_encode((float)(pr * (1.0 + band)));
+                if (lo != hi) tie[a] = fabs(c->dec[hi] - c->dec[lo]);
+            }
         }
         l = alpha * l + (float)rowsum;
         for (int x = 0; x < d; x++) {
-            double acc = 0.0;
-            for (int a = 0; a < kn; a++) acc += ph[a] * c->vh[(long)(s0 + k0 + a) * d + x];
+            double acc = 0.0, ta = 0.0;
+            for (int a = 0; a < kn; a++) {
+                const double vv = c->vh[(long)(s0 + k0 + a) * d + x];
+                acc += ph[a] * vv;
+                ta += tie[a] * fabs(vv);
+            }
             O[x] = alpha * O[x] + (float)acc;
+            Am[x] = (double)alpha * Am[x] + ta;
         }
         m = mnew;
     }
@@ -538,6 +564,7 @@ static void emu_unit(void* vc, long ri) {
     for (int x = 0; x < d; x++) {
         out[x] = O[x] * fin;
         if (c->ob) c->ob[((long)ri * c->H + h) * d + x] = or_bf16_rne(out[x]);
+        if (c->amb) c->amb[((long)ri * c->H + h) * d + x] = (float)(Am[x] * (double)fin);
     }
     c->lse[(long)h * c->nrows + ri] =
         (l > 0.0f) ? (float)(0.6931471805599453 * ((double)m + log2((double)l) - 8.0)) : -INFINITY;
@@ -546,7 +573,7 @@ static void emu_unit(void* vc, long ri) {
 int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                          int T, int H, int d, const int32_t* cu, int nd,
                          int causal, int exact, int rotated, double scale, int flags,
-                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse) {
+                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb) {
     if (d < 1 || d > 256) return OR_ERR_ARG;
     int mxq = q->layout == OR_MX_ROW32, mxk = k->layout == OR_MX_ROW32;
     if (mxq != mxk) return OR_ERR_ARG;
@@ -556,7 +583,7 @@ int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qten
     memset(&c, 0, sizeof(c));
     c.q = q; c.k = k; c.v = v; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
     c.causal = causal; c.exact = exact; c.rotated = rotated; c.scale = scale; c.flags = flags;
-    c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse;
+    c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse; c.amb = amb;
     for (int i = 0; i < 256; i++) c.dec[i] = or_e4m3_decode((uint8_t)i);
     if (!mxq) { c.nbq = block_offset(&c.D, c.D.nd, q->block); c.nbk = block_offset(&c.D, c.D.nd, k->block); }
     if (v->layout == OR_E4M3_TOKBLOCK) c.nbv = block_offset(&c.D, c.D.nd, v->block);

@@ -90,10 +90,16 @@ typedef struct {
 /* flags */
 enum { OR_EMU_QUANTIZE_P = 1 };
 
+/* rows as for O-1; o, o_bf16: [nrows][H][d]; lse: [H][nrows].
+ * amb (NULL to skip): [nrows][H][d], the part of each output element that
+ * E4M3 probability codes within rounding of a code boundary could move (the
+ * tie allowance described beside the implementation). */
+
 int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                          int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
                          int causal, int exact, int rotated, double softmax_scale, int flags,
-                         const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse);
+                         const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
+                         float* amb);
 
 #ifdef __cplusplus
 }

@@ -35,12 +35,6 @@ namespace pa {
 
 enum { MODE_BF16 = 0, MODE_E4M3_TILE = 1, MODE_E4M3_COL = 2, MODE_MX = 3 };
 
-// 2^k for an integral k <= 0 held in a float (0 below the normal range)
-__device__ __forceinline__ float exp2_int(float k) {
-    const int e = (int)k;
-    return e < -126 ? 0.0f : __int_as_float((127 + e) << 23);
-}
-
 template <int ELT, int D, int MODE>
 struct Cfg {
     static constexpr int RB = D * ELT;                  // bytes per Q/K/V row
@@ -83,6 +77,7 @@ struct Bars {
     // the K slot that S of tile g - NS frees), so eight slots never collide.
     float tile_scale[8][4];
     uint64_t sc_full[8];
+    uint64_t drain;
     uint32_t tmem_base;
     int abort;
     // the two warps sharing a row quarter exchange row maxima and row sums through
@@ -170,6 +165,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
             mbar_init(&B->s_empty[i], 32 * C::SOFTMAX_WARPS);
         }
         for (int i = 0; i < 8; i++) mbar_init(&B->sc_full[i], 1);
+        mbar_init(&B->drain, 1);
         for (int i = 0; i < C::NS; i++) {
             mbar_init(&B->k_full[i], 1);
             mbar_init(&B->v_full[i], 1);
@@ -414,6 +410,9 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                     break;
                 }
             }
+            // every MMA this thread issued has completed before TMEM is released
+            tc_commit(&B->drain);
+            wait_drain(&B->drain, 0, lim);
         }
         __syncwarp();
     } else {
@@ -544,14 +543,11 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                     break;
                 }
                 const float mx = fmaxf(pmax, xch[((gj & 1) * 2 + (hh ^ 1)) * 128 + r]);
-                // integer frame for the running max (log2 units): the smallest integer not
-                // below every score so far. It moves only when a tile's max leaves it; O and
-                // l are then rescaled by the exact power of two 2^(m - m_new), and P <= 2^8.
+                // running max (log2 units) and the rescale factor of the old state
                 const float mt = mx * c;
-                const bool upd = (m == -INFINITY) || (mt > m);
-                const float m_new = upd ? ceilf(mt) : m;
+                const float m_new = fmaxf(m, mt);
                 const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-                const float alpha = (m == -INFINITY) ? 0.0f : (upd ? exp2_int(m - m_new) : 1.0f);
+                const float alpha = (m == -INFINITY) ? 0.0f : (m_new > m ? ex2(m - m_new) : 1.0f);
                 const float bias = 8.0f - m_use + lr;
                 uint32_t pk[ELT == 1 ? 16 : 32];
                 float rowsum;
@@ -702,6 +698,495 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Two query tiles per CTA (E4M3 codes, d = 128).
+//
+// The same loop as attn_fwd_kernel, with the CTA's work item widened to the
+// query tiles 2p and 2p + 1 of a (document, head): both share every K and V
+// tile, and their two dependency chains (S -> softmax -> P -> P V) interleave
+// on the tensor pipe and on the SM sub-partitions, so one tile's softmax runs
+// while the other tile's MMAs execute.
+//   warp 0      producer: both Q tiles once per item, K and V tiles into a
+//               4-stage ring; per-tile score multipliers (E4M3 tile mode)
+//   warp 1      TMEM owner and MMA issuer (one thread): an S stream
+//               (S0_j = Q0 K_j^T, then S1_j) and one P V stream per query tile,
+//               each issued as soon as its inputs are ready
+//   warps 2-5   softmax of query tile 0, warps 6-9 of query tile 1: one thread
+//               per row, all 128 columns
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512). A K slot is
+// released after S1_j, a V slot after the second P V of tile j.
+struct PairCfg {
+    static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
+    static constexpr int NS = 4;                      // K/V ring depth
+    static constexpr int OFF_Q = 0;                   // Q0, Q1
+    static constexpr int OFF_P = 2 * TILE;            // P0, P1
+    static constexpr int OFF_KV = 4 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
+    static constexpr int OFF_BAR = OFF_KV + NS * 2 * TILE;
+    static constexpr int SMEM = OFF_BAR + 1024 + 1024;
+    static constexpr int THREADS = 320;
+    static constexpr uint32_t T_O = 256;              // O_q at T_O + 128 q; S_q at 128 q
+};
+
+struct PairBars {
+    uint64_t q_full, q_empty;
+    uint64_t s_full[2], s_empty[2];     // per query tile
+    uint64_t p_full[2], pv_done[2];     // per query tile (one P buffer each)
+    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
+    uint64_t sc_full[8];
+    uint64_t drain;
+    // E4M3 tile mode, key tile g in slot g % 8: K scale x score constant, log2(r), 1/r.
+    // The producer is at most NS tiles ahead of the slower softmax group (it needs the
+    // K slot that S1 of tile g - NS frees), so eight slots never collide.
+    float tile_scale[8][4];
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+    using PC = PairCfg;
+    using C = Cfg<1, 128, MODE>;   // descriptor helpers of the 128-byte-row E4M3 tiles
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairBars* B = reinterpret_cast<PairBars*>(sm + PC::OFF_BAR);
+    volatile int* abort = &B->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long lim = p.wait_limit;
+    constexpr unsigned FULL = 0xFFFFFFFFu;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&B->q_full, 1);
+        mbar_init(&B->q_empty, 1);
+        for (int q = 0; q < 2; q++) {
+            mbar_init(&B->s_full[q], 1);
+            mbar_init(&B->s_empty[q], 128);
+            mbar_init(&B->p_full[q], 128);
+            mbar_init(&B->pv_done[q], 1);
+        }
+        for (int i = 0; i < PC::NS; i++) {
+            mbar_init(&B->k_full[i], 1);
+            mbar_init(&B->v_full[i], 1);
+            mbar_init(&B->k_empty[i], 1);
+            mbar_init(&B->v_empty[i], 1);
+        }
+        for (int i = 0; i < 8; i++) mbar_init(&B->sc_full[i], 1);
+        mbar_init(&B->drain, 1);
+        B->abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmq);
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&B->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem_base;
+    const int n_items = p.hdr->n_items;
+    const uint32_t sQ = smem_u32(sm + PC::OFF_Q);
+    const uint32_t sP = smem_u32(sm + PC::OFF_P);
+    const uint32_t sKV = smem_u32(sm + PC::OFF_KV);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int issued[4] = {-1, -1, -1, -1};   // parity of the last load per stage
+        int q_issued = -1;
+        uint32_t g = 0;
+        int qi = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
+            const WorkItem w = p.items[it];
+            const DocEntry d = p.docs[w.doc];
+            float ref = 1.0f;
+            if constexpr (MODE == MODE_E4M3_TILE) ref = p.vref[(long long)w.head * p.nd + w.doc];
+            if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
+            q_issued = qi & 1;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&B->q_full, 2 * PC::TILE);
+                tma_load_3d(sm + PC::OFF_Q, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile);
+                tma_load_3d(sm + PC::OFF_Q + PC::TILE, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile + 128);
+            }
+            float t_c = 0.0f, t_lr = 0.0f, t_ir = 1.0f;   // this lane's tile of the current group of 32
+            for (int j = 0; j < w.ntiles; j++, g++) {
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    if ((j & 31) == 0 && j + lane < w.ntiles) {
+                        // K block scale folded with the score constant; V ratio r = s_v / ref
+                        const int jt = j + lane;
+                        const float ks = p.sk[w.head * p.capk + d.boff_k + (128 * jt) / p.bk];
+                        const float sv = p.sv[w.head * p.capv + d.boff_v + (128 * jt) / p.bv];
+                        const float rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                        t_c = ks * p.C;
+                        t_lr = __log2f(rj);
+                        t_ir = __fdiv_rn(1.0f, rj);
+                    }
+                }
+                const int st = g % PC::NS;
+                if (!__all_sync(FULL, mbar_wait(&B->k_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                issued[st] = (g / PC::NS) & 1;
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    const float c = __shfl_sync(FULL, t_c, j & 31);
+                    const float lr = __shfl_sync(FULL, t_lr, j & 31);
+                    const float ir = __shfl_sync(FULL, t_ir, j & 31);
+                    if (lane == 0) {   // released to both softmax groups through sc_full
+                        B->tile_scale[g & 7][0] = c;
+                        B->tile_scale[g & 7][1] = lr;
+                        B->tile_scale[g & 7][2] = ir;
+                        mbar_arrive(&B->sc_full[g & 7]);
+                    }
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&B->k_full[st], PC::TILE);
+                    tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE, &tmk, &B->k_full[st], 0, w.head,
+                                d.start + 128 * j);
+                }
+                if (!__all_sync(FULL, mbar_wait(&B->v_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&B->v_full[st], PC::TILE);
+                    tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE + PC::TILE, &tmv, &B->v_full[st], 0, w.head,
+                                d.start + 128 * j);
+                }
+            }
+        }
+        if (*abort && lane == 0) {   // let in-flight copies land before shared memory is released
+            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, lim);
+            for (int s2 = 0; s2 < PC::NS; s2++)
+                if (issued[s2] >= 0) {
+                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], lim);
+                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], lim);
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc(0, 0, false, false, 128, 128);
+            constexpr uint32_t id_pv = idesc(0, 0, false, true, 128, 128);
+            constexpr uint64_t TILE16 = (uint64_t)PC::TILE >> 4;
+            constexpr uint64_t STAGE16 = (uint64_t)(2 * PC::TILE) >> 4;
+            const uint64_t dq0 = desc_kmajor<1, 128, MODE>(sQ, 0);
+            const uint64_t dk0 = desc_kmajor<1, 128, MODE>(sKV, 0);
+            const uint64_t dv0 = desc_v<1, 128, MODE>(sKV + PC::TILE, 0);
+            const uint64_t dp0 = desc_p<1>(sP, 0);
+            // S stream: S0_j then S1_j for every key tile j, items back to back
+            int itS = blockIdx.x, jS = 0, qiS = 0, qS = 0;
+            uint32_t gS = 0;
+            uint32_t sdone[2] = {0, 0};                // S issued per query tile
+            WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
+            // P V streams, one per query tile
+            int itP[2] = {blockIdx.x, blockIdx.x}, jP[2] = {0, 0};
+            uint32_t gP[2] = {0, 0};
+            WorkItem wP[2] = {wS, wS};
+            long long t_prog = clock64();
+            while (itP[0] < n_items || itP[1] < n_items) {
+                bool progressed = false;
+                if (itS < n_items) {
+                    const int st = gS % PC::NS;
+                    const uint32_t x = sdone[qS];
+                    if ((qS != 0 || jS != 0 || mbar_test(&B->q_full, qiS & 1)) &&
+                        mbar_test(&B->k_full[st], (gS / PC::NS) & 1) && mbar_test(&B->s_empty[qS], (x & 1) ^ 1)) {
+                        tc_fence_after();
+                        const uint64_t dq = dq0 + qS * TILE16;
+                        const uint64_t dk = dk0 + st * STAGE16;
+#pragma unroll
+                        for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                            mma_f8(tmem + qS * 128, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s,
+                                   kk ? 1u : 0u);
+                        tc_commit(&B->s_full[qS]);
+                        sdone[qS]++;
+                        if (qS == 1) {
+                            tc_commit(&B->k_empty[st]);
+                            gS++;
+                            qS = 0;
+                            if (++jS == wS.ntiles) {   // last S of the item: Q may be replaced
+                                tc_commit(&B->q_empty);
+                                jS = 0;
+                                qiS++;
+                                itS += gridDim.x;
+                                if (itS < n_items) wS = p.items[itS];
+                            }
+                        } else {
+                            qS = 1;
+                        }
+                        progressed = true;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    if (itP[q] < n_items && gP[q] < sdone[q]) {
+                        const uint32_t gx = gP[q];
+                        const int st = gx % PC::NS;
+                        if (mbar_test(&B->p_full[q], gx & 1) && mbar_test(&B->v_full[st], (gx / PC::NS) & 1)) {
+                            tc_fence_after();
+                            const uint64_t dv = dv0 + st * STAGE16;
+                            const uint64_t dp = dp0 + q * TILE16;
+                            const bool first = jP[q] == 0;
+#pragma unroll
+                            for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                                mma_f8(tmem + PC::T_O + q * 128, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv,
+                                       (first && kk == 0) ? 0u : 1u);
+                            tc_commit(&B->pv_done[q]);
+                            // the second P V of this key tile frees its V slot
+                            if (gP[q ^ 1] > gx) tc_commit(&B->v_empty[st]);
+                            gP[q]++;
+                            if (++jP[q] == wP[q].ntiles) {
+                                jP[q] = 0;
+                                itP[q] += gridDim.x;
+                                if (itP[q] < n_items) wP[q] = p.items[itP[q]];
+                            }
+                            progressed = true;
+                        }
+                    }
+                }
+                if (progressed) {
+                    t_prog = clock64();
+                } else if (*abort || clock64() - t_prog > lim) {
+                    *abort = 1;
+                    break;
+                }
+            }
+            // every MMA this thread issued has completed before TMEM is released
+            tc_commit(&B->drain);
+            wait_drain(&B->drain, 0, lim);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int q = (warp - 2) >> 2;                            // query tile of this group
+        const int quarter = warp & 3;                             // TMEM lane quarter
+        const int r = quarter * 32 + lane;                        // row within the query tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + q * 128;
+        const uint32_t tO = tmem + lane_off + PC::T_O + q * 128;
+        uint8_t* pbuf = sm + PC::OFF_P + q * PC::TILE;
+        uint32_t g = 0;
+        bool ok = true;
+        auto wait_pv = [&](uint32_t gx) -> bool {
+            return __all_sync(FULL, mbar_wait(&B->pv_done[q], gx & 1, abort, lim));
+        };
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const WorkItem w = p.items[it];
+            const DocEntry d = p.docs[w.doc];
+            const int h = w.head, L = d.len, nt = w.ntiles;
+            const int ntd = (L + 127) / 128;
+            const int qt = 2 * w.qtile + q;                       // query tile within the document
+            const int qtc = qt < ntd ? qt : ntd - 1;
+            const int rloc = 128 * qt + r;                        // row position in the document
+            const int rcl = rloc < L ? rloc : L - 1;
+            float qs = 1.0f, ref = 1.0f;
+            if constexpr (MODE == MODE_E4M3_TILE) {
+                qs = p.sq[h * p.capq + d.boff_q + (128 * qtc) / p.bq];
+                ref = p.vref[(long long)h * p.nd + w.doc];
+            } else {
+                qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
+                ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
+            }
+            float m = -INFINITY, l = 0.0f;
+            for (int j = 0; j < nt; j++) {
+                const uint32_t gj = g + j;
+                if (!__all_sync(FULL, mbar_wait(&B->s_full[q], gj & 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[128];
+                {
+                    uint32_t u0[32], u1[32], u2[32], u3[32];
+                    tmem_ld32(tS, u0);
+                    tmem_ld32(tS + 32, u1);
+                    tmem_ld32(tS + 64, u2);
+                    tmem_ld32(tS + 96, u3);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) {
+                        s[i] = __uint_as_float(u0[i]);
+                        s[32 + i] = __uint_as_float(u1[i]);
+                        s[64 + i] = __uint_as_float(u2[i]);
+                        s[96 + i] = __uint_as_float(u3[i]);
+                    }
+                }
+                float c = p.C, lr = 0.0f, invr = 1.0f;
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    if (!__all_sync(FULL, mbar_wait(&B->sc_full[gj & 7], (gj >> 3) & 1, abort, lim))) {
+                        ok = false;
+                        break;
+                    }
+                    c = qs * B->tile_scale[gj & 7][0];
+                    lr = B->tile_scale[gj & 7][1];
+                    invr = B->tile_scale[gj & 7][2];
+                }
+                tc_fence_before();
+                mbar_arrive(&B->s_empty[q]);
+                const int k0 = 128 * j;                              // first key position of the tile
+                if constexpr (MODE == MODE_E4M3_COL) {
+                    const float qc = qs * p.C;
+#pragma unroll 8
+                    for (int t = 0; t < 128; t++) {
+                        const int kl = (k0 + t) < L ? k0 + t : L - 1;
+                        s[t] = s[t] * (p.sk[h * p.capk + d.boff_k + kl / p.bk] * qc);
+                    }
+                    c = 1.0f;
+                }
+                // causal: key tiles past the query tile are fully masked (the pair's
+                // first tile visits one key tile more than it needs), the diagonal
+                // tile keeps keys <= the row; otherwise keys past the document end
+                const bool mask = p.causal ? (j >= qt) : (k0 + 128 > L);
+                if (mask) {
+                    const int lim_k = p.causal ? (rloc - k0) : (L - 1 - k0);   // last visible column
+#pragma unroll
+                    for (int t = 0; t < 128; t++)
+                        if (t > lim_k) s[t] = -INFINITY;
+                }
+                c = fmaxf(c, 1.17549435e-38f);   // keeps masked -inf when a block scale is 0
+                float mx8[8];
+#pragma unroll
+                for (int k8 = 0; k8 < 8; k8++) {
+                    float a = s[16 * k8];
+#pragma unroll
+                    for (int i2 = 1; i2 < 15; i2 += 2) a = fmax3(a, s[16 * k8 + i2], s[16 * k8 + i2 + 1]);
+                    mx8[k8] = fmaxf(a, s[16 * k8 + 15]);
+                }
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                // running max (log2 units) and the rescale factor of the old state
+                const float mt = mx * c;
+                const float m_new = fmaxf(m, mt);
+                const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+                const float alpha = (m == -INFINITY) ? 0.0f : (m_new > m ? ex2(m - m_new) : 1.0f);
+                const float bias = 8.0f - m_use + lr;
+                uint32_t pk[32];
+                float rowsum;
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int t = 0; t < 128; t += 8) {
+                        float e[8];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            const float2 xx = __ffma2_rn(make_float2(s[t + u], s[t + u + 1]), c2, b2);
+                            e[u] = ex2(xx.x);
+                            e[u + 1] = ex2(xx.y);
+                            acc[u >> 1] = __fadd2_rn(acc[u >> 1], make_float2(e[u], e[u + 1]));
+                        }
+                        pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
+                        pk[t / 4 + 1] = pack_e4m3x4(e[4], e[5], e[6], e[7]);
+                    }
+                    const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                    rowsum = a.x + a.y;
+                } else {
+                    float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+                    for (int t = 0; t < 128; t += 4) {
+                        float e[4];
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            e[u] = ex2(fmaf(s[t + u], c, bias));
+                            rs4[u] += e[u];
+                            const int kl = (k0 + t + u) < L ? k0 + t + u : L - 1;
+                            const float sv = p.sv[h * p.capv + d.boff_v + kl / p.bv];
+                            const float rt = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                            e[u] = e[u] * rt;
+                        }
+                        pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
+                    }
+                    rowsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                }
+                l = alpha * l + rowsum * invr;
+                m = m_new;
+                // the P buffer was last read by P V of the previous tile, which must also be
+                // complete before O is rescaled
+                if (gj > 0 && !wait_pv(gj - 1)) {
+                    ok = false;
+                    break;
+                }
+                if (j > 0 && __any_sync(FULL, alpha != 1.0f)) {
+                    tc_fence_after();
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                    for (int cc = 0; cc < 4; cc++) {
+                        uint32_t u[32];
+                        tmem_ld32(tO + cc * 32, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i2 = 0; i2 < 32; i2 += 2) {
+                            const float2 v2 =
+                                __fmul2_rn(make_float2(__uint_as_float(u[i2]), __uint_as_float(u[i2 + 1])), a2);
+                            u[i2] = __float_as_uint(v2.x);
+                            u[i2 + 1] = __float_as_uint(v2.y);
+                        }
+                        tmem_st32(tO + cc * 32, u);
+                    }
+                    tmem_wait_st();
+                }
+                // the P row -> shared memory (128-byte swizzled K-major rows)
+#pragma unroll
+                for (int ch = 0; ch < 8; ch++) {
+                    uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&B->p_full[q]);
+            }
+            if (!ok) break;
+            // epilogue: O / l -> bf16, lse
+            if (!wait_pv(g + nt - 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float fin = (l > 0.0f) ? __fdiv_rn(ref, l) : 0.0f;
+            const bool store = rloc < L;
+            uint16_t* orow = p.o + ((long long)(d.start + rcl) * p.H + h) * 128;
+            const float2 f2 = make_float2(fin, fin);
+#pragma unroll
+            for (int cc = 0; cc < 4; cc++) {
+                uint32_t u[32];
+                tmem_ld32(tO + cc * 32, u);
+                tmem_wait_ld();
+                uint32_t packed[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; i2++) {
+                    const float2 v2 =
+                        __fmul2_rn(make_float2(__uint_as_float(u[2 * i2]), __uint_as_float(u[2 * i2 + 1])), f2);
+                    packed[i2] = pack_bf16x2(v2.x, v2.y);
+                }
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; i2++)
+                        dst[i2] = make_uint4(packed[4 * i2], packed[4 * i2 + 1], packed[4 * i2 + 2], packed[4 * i2 + 3]);
+                }
+            }
+            if (store)
+                p.lse[(long long)h * p.T + d.start + rloc] =
+                    (l > 0.0f) ? 0.69314718055994531f * (m + __log2f(l) - 8.0f) : -INFINITY;
+            tc_fence_before();
+            g += nt;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && *abort) atomicOr(&p.hdr->status, ST_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // [T][H][D] tensor, box = (box_elems channels, 1 head, 128 tokens)
 static bool make_map(CUtensorMap* m, const void* base, int elt, int T, int H, int D, int box_elems, bool sw128) {
@@ -726,14 +1211,29 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
     return cudaGetLastError();
 }
 
+template <int MODE>
+static cudaError_t launch_pair(const void* q, const void* k, const void* v, const FwdParams& p, int grid,
+                               cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, 1, p.T, p.H, 128, 128, true) || !make_map(&mk, k, 1, p.T, p.H, 128, 128, true) ||
+        !make_map(&mv, v, 1, p.T, p.H, 128, 128, true))
+        return cudaErrorInvalidValue;
+    auto kern = attn_pair_kernel<MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, PairCfg::THREADS, PairCfg::SMEM, st>>>(mq, mk, mv, p);
+    return cudaGetLastError();
+}
+
 // mode: 0 bf16, 1 E4M3 tile scales, 2 E4M3 per-column scales, 3 MX
 cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                         cudaStream_t st) {
     if (mode == MODE_BF16) return D == 128 ? launch_t<2, 128, MODE_BF16>(q, k, v, p, grid, st)
                                            : launch_t<2, 64, MODE_BF16>(q, k, v, p, grid, st);
-    if (mode == MODE_E4M3_TILE) return D == 128 ? launch_t<1, 128, MODE_E4M3_TILE>(q, k, v, p, grid, st)
+    // E4M3 at d = 128: two query tiles per CTA (the work list is built in pair mode)
+    if (mode == MODE_E4M3_TILE) return D == 128 ? launch_pair<MODE_E4M3_TILE>(q, k, v, p, grid, st)
                                                 : launch_t<1, 64, MODE_E4M3_TILE>(q, k, v, p, grid, st);
-    if (mode == MODE_E4M3_COL) return D == 128 ? launch_t<1, 128, MODE_E4M3_COL>(q, k, v, p, grid, st)
+    if (mode == MODE_E4M3_COL) return D == 128 ? launch_pair<MODE_E4M3_COL>(q, k, v, p, grid, st)
                                                : launch_t<1, 64, MODE_E4M3_COL>(q, k, v, p, grid, st);
     if (mode == MODE_MX && D == 128) return launch_t<1, 128, MODE_MX>(q, k, v, p, grid, st);
     return cudaErrorInvalidValue;

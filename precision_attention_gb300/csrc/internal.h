@@ -21,10 +21,12 @@ struct DocEntry {
     int32_t boff_q;   // first scale block of Q (prefix of ceil(L / block_q))
     int32_t boff_k;
     int32_t boff_v;
-    int32_t pad0, pad1;
+    int32_t poff;     // first query-tile pair (prefix of ceil(ceil(L / 128) / 2))
+    int32_t pad1;
 };
 
-// One unit of forward work: the 128-row query tile `qtile` of (doc, head).
+// One unit of forward work: the 128-row query tile `qtile` of (doc, head), or,
+// in pair mode, the query tiles 2 * qtile and 2 * qtile + 1.
 struct WorkItem {
     int32_t doc;
     int32_t head;

@@ -32,6 +32,7 @@ struct SchedParams {
     DocEntry* docs;
     WorkItem* items;
     long long items_cap;
+    int qpair;             // 1: an item covers the query tiles 2p and 2p + 1 of a document
 };
 
 struct VrefParams {

@@ -45,13 +45,13 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
     if (tid == 0) bad = 0;
     __syncthreads();
     // pass 1: document table (4 documents per thread per round)
-    int carry_t = 0, carry_q = 0, carry_k = 0, carry_v = 0;
+    int carry_t = 0, carry_q = 0, carry_k = 0, carry_v = 0, carry_p = 0;
     for (int base = 0; base < nd; base += 4 * blockDim.x) {
-        int nt[4], nq[4], nk[4], nv[4], st[4], ln[4];
+        int nt[4], nq[4], nk[4], nv[4], np[4], st[4], ln[4];
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const int i = base + tid * 4 + k;
-            nt[k] = nq[k] = nk[k] = nv[k] = st[k] = ln[k] = 0;
+            nt[k] = nq[k] = nk[k] = nv[k] = np[k] = st[k] = ln[k] = 0;
             if (i < nd) {
                 const int s = p.cu ? p.cu[i] : 0, e = p.cu ? p.cu[i + 1] : p.T;
                 if (e < s) bad = 1;
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
                 st[k] = s;
                 ln[k] = L;
                 nt[k] = (L + 127) / 128;
+                np[k] = (nt[k] + 1) / 2;
                 nq[k] = (L + p.bq - 1) / p.bq;
                 nk[k] = (L + p.bk - 1) / p.bk;
                 nv[k] = (L + p.bv - 1) / p.bv;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
         const int tq = block_exclusive_scan4(nq, wsum);
         const int tk = block_exclusive_scan4(nk, wsum);
         const int tv = block_exclusive_scan4(nv, wsum);
+        const int tp = block_exclusive_scan4(np, wsum);
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const int i = base + tid * 4 + k;
@@ -79,7 +81,8 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
                 d.boff_q = carry_q + nq[k];
                 d.boff_k = carry_k + nk[k];
                 d.boff_v = carry_v + nv[k];
-                d.pad0 = d.pad1 = 0;
+                d.poff = carry_p + np[k];
+                d.pad1 = 0;
                 p.docs[i] = d;
             }
         }
@@ -87,13 +90,15 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
         carry_q += tq;
         carry_k += tk;
         carry_v += tv;
+        carry_p += tp;
     }
     if (tid == 0) {
         const int c0 = p.cu ? p.cu[0] : 0, cn = p.cu ? p.cu[nd] : p.T;
         if (c0 != 0 || cn != p.T) bad = 1;
     }
     __syncthreads();
-    const long long total = (long long)carry_t * p.H;
+    const int units = p.qpair ? carry_p : carry_t;     // query tiles or query-tile pairs
+    const long long total = (long long)units * p.H;
     if (bad || total > p.items_cap) {
         if (tid == 0) {
             atomicOr(&p.hdr->status, ST_BAD_SEQLENS);
@@ -109,50 +114,56 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
             int lo = 0, hi = nd - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if ((long long)p.docs[mid].toff * p.H <= i) lo = mid; else hi = mid - 1;
+                const int off = p.qpair ? p.docs[mid].poff : p.docs[mid].toff;
+                if ((long long)off * p.H <= i) lo = mid; else hi = mid - 1;
             }
             const DocEntry d = p.docs[lo];
             const int nt = (d.len + 127) / 128;
-            const long long rem = i - (long long)d.toff * p.H;
+            const int nu = p.qpair ? (nt + 1) / 2 : nt;
+            const long long rem = i - (long long)(p.qpair ? d.poff : d.toff) * p.H;
             WorkItem w;
             w.doc = lo;
-            w.head = (int)(rem / nt);
-            w.qtile = (int)(rem % nt);
+            w.head = (int)(rem / nu);
+            w.qtile = (int)(rem % nu);
             w.ntiles = nt;
             p.items[i] = w;
         }
     } else {
         // longest first: query tile qt of a causal document visits qt + 1 key
-        // tiles; order by qt descending, then document, then head
-        for (long long pr = tid; pr < carry_t; pr += blockDim.x) {
+        // tiles (a pair p visits min(2p + 2, tiles)); order by the unit index
+        // descending, then document, then head
+        for (long long pr = tid; pr < units; pr += blockDim.x) {
             int lo = 0, hi = nd - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if (p.docs[mid].toff <= pr) lo = mid; else hi = mid - 1;
+                const int off = p.qpair ? p.docs[mid].poff : p.docs[mid].toff;
+                if (off <= pr) lo = mid; else hi = mid - 1;
             }
             const int doc = lo;
-            const int qt = (int)(pr - p.docs[doc].toff);
-            long long before = 0;   // tiles of every document with a larger qt
-            int rank = 0;           // earlier documents that also have tile qt
+            const int qt = (int)(pr - (p.qpair ? p.docs[doc].poff : p.docs[doc].toff));
+            long long before = 0;   // units of every document with a larger index
+            int rank = 0;           // earlier documents that also have unit qt
             for (int j = 0; j < nd; j++) {
                 const int ntj = (p.docs[j].len + 127) / 128;
-                if (ntj > qt + 1) before += ntj - qt - 1;
-                if (j < doc && ntj > qt) rank++;
+                const int nuj = p.qpair ? (ntj + 1) / 2 : ntj;
+                if (nuj > qt + 1) before += nuj - qt - 1;
+                if (j < doc && nuj > qt) rank++;
             }
+            const int ntd = (p.docs[doc].len + 127) / 128;
             const long long base = (before + rank) * p.H;
             for (int h = 0; h < p.H; h++) {
                 WorkItem w;
                 w.doc = doc;
                 w.head = h;
                 w.qtile = qt;
-                w.ntiles = qt + 1;
+                w.ntiles = p.qpair ? (2 * qt + 2 < ntd ? 2 * qt + 2 : ntd) : qt + 1;
                 p.items[base + h] = w;
             }
         }
     }
     if (tid == 0) {
         p.hdr->n_items = (int)total;
-        p.hdr->n_tiles = carry_t;
+        p.hdr->n_tiles = units;
     }
 }
 

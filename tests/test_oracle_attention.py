@@ -157,6 +157,36 @@ def test_emulation_p_quantisation_error_bound(oracle_mod, mx):
     assert np.linalg.norm(o3 - o3n) > 0          # P quantisation does act
 
 
+@pytest.mark.parametrize("mx", [False, True])
+def test_tie_allowance_explains_score_rounding(oracle_mod, mx):
+    """A relative change of 2^-21 in the score scale (the size of fp32
+    rounding difference) moves some E4M3 probability codes across a boundary;
+    every output change it causes lies within the emulation's tie allowance,
+    and the allowance is zero where P is not quantised."""
+    inp = workloads.make(4 if mx else 2, heads=2, lengths=[1024])
+    cu = inp.cu_seqlens
+    Q, K, V = quant3(oracle_mod, inp, mx, 128)
+    scale = 1 / math.sqrt(128)
+    oa, _, _, amb = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale, ties=True)
+    ob, _, _ = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale * (1 + 2.0 ** -21))
+    diff = np.abs(oa.astype(np.float64) - ob)
+    # the continuous part: p and the rescale alpha move by about ln2 * Dx with
+    # Dx up to two fp32 ulps of s' (6e-5 at the outlier rows' |s'| ~ 400); it
+    # acts on every term P v / l, also where the terms cancel in O, so it is
+    # bounded relative to sum_t P_t |v_t| / l: the emulation run on |V|
+    Va = oracle_mod.QTensor(V.codes & 0x7F, V.scales, V.layout, V.block, V.rotated, V.seed)
+    oabs, _, _ = oracle_mod.attention_emulate(Q, K, Va, cu, False, False, scale)
+    cont = 1e-4 * oabs + 1e-7
+    assert np.all(amb >= 0)
+    assert np.all(diff <= amb + cont)
+    assert np.count_nonzero(amb) > 0                                   # ties exist
+    if not mx:                      # (the MX outlier rows are too peaked for a visible flip here)
+        assert np.count_nonzero(diff > cont) > 0                     # and some codes did flip
+    assert np.mean(amb > 1e-3) < 0.01                                 # ties rarely matter
+    _, _, _, amb0 = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale, quantize_p=False, ties=True)
+    assert not amb0.any()
+
+
 def test_causal_exact_rows_unchanged_by_later_tokens(oracle_mod):
     """Causal-exact mode: row i is bit-for-bit unchanged when keys or values at
     positions after i are perturbed; the default block mode leaks."""
