@@ -311,104 +311,97 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
             constexpr uint64_t STAGE16 = (uint64_t)(2 * C::TILE) >> 4;   // descriptor step between stages
             constexpr uint64_t PBUF16 = (uint64_t)C::PBYTES >> 4;
             if constexpr (MODE == MODE_MX) tc_cp_sf(tmem + C::T_SFP, desc_sf(sSF + 512));
-            // Two streams over the CTA's tiles, items back to back: S = Q K^T of tile g + 2
-            // may start as soon as the softmax has loaded S of tile g (two S buffers), ahead
-            // of O += P V. The thread polls both and issues whichever is ready, so an S never
-            // waits behind a P V whose P is not ready.
+            // Fixed order, S up to two key tiles ahead of P V (two S buffers), across
+            // item boundaries:  S_0 S_1 | P V_0 S_2 | P V_1 S_3 | ...  as  S_{j+2} needs
+            // only that the softmax has loaded S_j, which it does before P_j is ready.
+            // Each step parks on the one barrier it needs (mbarrier.try_wait). Polling
+            // several barriers instead costs a shared-memory instruction per test, and
+            // those queue behind the softmax warps' MUFU and shared-memory traffic.
             int itS = blockIdx.x, jS = 0, qiS = 0;     // S stream cursor
             int itP = blockIdx.x, jP = 0;              // P V stream cursor
             uint32_t gS = 0, gP = 0;                   // global tile counters
             WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
             WorkItem wP = wS;
-            long long t_prog = clock64();
-            while (itP < n_items) {
-                bool progressed = false;
-                if (itS < n_items) {   // the S buffer's s_empty phase is the only limit on running ahead
-                    const int st = gS % C::NS, b = gS & 1;
-                    if ((jS != 0 || mbar_test(&B->q_full, qiS & 1)) && mbar_test(&B->k_full[st], (gS / C::NS) & 1) &&
-                        mbar_test(&B->s_empty[b], ((gS >> 1) & 1) ^ 1)) {
-                        tc_fence_after();
-                        if constexpr (MODE == MODE_MX) {
-                            if (jS == 0) tc_cp_sf(tmem + C::T_SFQ, desc_sf(sSF));
-                        }
-                        const uint64_t dk = dk0 + st * STAGE16;
-                        const uint32_t dS = tmem + b * 128;
-                        if constexpr (MODE == MODE_MX) {
-                            const uint32_t sfk = tmem + C::T_SFK + (gS & 1) * 4;
-                            tc_cp_sf(sfk, desc_sf(sSF + 1024 + st * 512));
+            auto issue_s = [&]() -> bool {
+                const int st = gS % C::NS, b = gS & 1;
+                if (jS == 0 && !mbar_wait(&B->q_full, qiS & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->k_full[st], (gS / C::NS) & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->s_empty[b], ((gS >> 1) & 1) ^ 1, abort, lim)) return false;
+                tc_fence_after();
+                if constexpr (MODE == MODE_MX) {
+                    if (jS == 0) tc_cp_sf(tmem + C::T_SFQ, desc_sf(sSF));
+                }
+                const uint64_t dk = dk0 + st * STAGE16;
+                const uint32_t dS = tmem + b * 128;
+                if constexpr (MODE == MODE_MX) {
+                    const uint32_t sfk = tmem + C::T_SFK + (gS & 1) * 4;
+                    tc_cp_sf(sfk, desc_sf(sSF + 1024 + st * 512));
 #pragma unroll
-                            for (int kk = 0; kk < C::KSTEPS_S; kk++)
-                                mma_mxf8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk),
-                                         idesc_mx(0, 0, false, false, 128, 128, kk, kk), tmem + C::T_SFQ, sfk,
-                                         kk ? 1u : 0u);
-                        } else {
+                    for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                        mma_mxf8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk),
+                                 idesc_mx(0, 0, false, false, 128, 128, kk, kk), tmem + C::T_SFQ, sfk, kk ? 1u : 0u);
+                } else {
 #pragma unroll
-                            for (int kk = 0; kk < C::KSTEPS_S; kk++) {
-                                if constexpr (ELT == 2)
-                                    mma_f16(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s,
-                                            kk ? 1u : 0u);
-                                else
-                                    mma_f8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s,
-                                           kk ? 1u : 0u);
-                            }
-                        }
-                        tc_commit(&B->s_full[b]);
-                        tc_commit(&B->k_empty[st]);
-                        gS++;
-                        if (++jS == wS.ntiles) {           // last S of the item: Q may be replaced
-                            tc_commit(&B->q_empty);
-                            jS = 0;
-                            qiS++;
-                            itS += gridDim.x;
-                            if (itS < n_items) wS = p.items[itS];
-                        }
-                        progressed = true;
+                    for (int kk = 0; kk < C::KSTEPS_S; kk++) {
+                        if constexpr (ELT == 2)
+                            mma_f16(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
+                        else
+                            mma_f8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
                     }
                 }
-                if (gP < gS) {
-                    const int st = gP % C::NS;
-                    if (mbar_test(&B->p_full[gP % C::PBUF], (gP / C::PBUF) & 1) &&
-                        mbar_test(&B->v_full[st], (gP / C::NS) & 1)) {
-                        tc_fence_after();
-                        const uint64_t dv = dv0 + st * STAGE16;
-                        const uint64_t dp = dp0 + (gP % C::PBUF) * PBUF16;
-                        const bool first = jP == 0;
-                        if constexpr (MODE == MODE_MX) {
-                            const uint32_t sfv = tmem + C::T_SFV + (gP & 1) * 4;
-                            tc_cp_sf(sfv, desc_sf(sSF + 1024 + C::NS * 512 + st * 512));
+                tc_commit(&B->s_full[b]);
+                tc_commit(&B->k_empty[st]);
+                gS++;
+                if (++jS == wS.ntiles) {           // last S of the item: Q may be replaced
+                    tc_commit(&B->q_empty);
+                    jS = 0;
+                    qiS++;
+                    itS += gridDim.x;
+                    if (itS < n_items) wS = p.items[itS];
+                }
+                return true;
+            };
+            auto issue_pv = [&]() -> bool {
+                const int st = gP % C::NS;
+                if (!mbar_wait(&B->v_full[st], (gP / C::NS) & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->p_full[gP % C::PBUF], (gP / C::PBUF) & 1, abort, lim)) return false;
+                tc_fence_after();
+                const uint64_t dv = dv0 + st * STAGE16;
+                const uint64_t dp = dp0 + (gP % C::PBUF) * PBUF16;
+                const bool first = jP == 0;
+                if constexpr (MODE == MODE_MX) {
+                    const uint32_t sfv = tmem + C::T_SFV + (gP & 1) * 4;
+                    tc_cp_sf(sfv, desc_sf(sSF + 1024 + C::NS * 512 + st * 512));
 #pragma unroll
-                            for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                                mma_mxf8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk),
-                                         idesc_mx(0, 0, false, true, 128, D, kk, kk), tmem + C::T_SFP, sfv,
-                                         (first && kk == 0) ? 0u : 1u);
-                        } else {
+                    for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                        mma_mxf8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk),
+                                 idesc_mx(0, 0, false, true, 128, D, kk, kk), tmem + C::T_SFP, sfv,
+                                 (first && kk == 0) ? 0u : 1u);
+                } else {
 #pragma unroll
-                            for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
-                                if constexpr (ELT == 2)
-                                    mma_f16(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
-                                            (first && kk == 0) ? 0u : 1u);
-                                else
-                                    mma_f8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
-                                           (first && kk == 0) ? 0u : 1u);
-                            }
-                        }
-                        tc_commit(&B->pv_done[gP % C::PBUF]);
-                        tc_commit(&B->v_empty[st]);
-                        gP++;
-                        if (++jP == wP.ntiles) {
-                            jP = 0;
-                            itP += gridDim.x;
-                            if (itP < n_items) wP = p.items[itP];
-                        }
-                        progressed = true;
+                    for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
+                        if constexpr (ELT == 2)
+                            mma_f16(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                                    (first && kk == 0) ? 0u : 1u);
+                        else
+                            mma_f8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                                   (first && kk == 0) ? 0u : 1u);
                     }
                 }
-                if (progressed) {
-                    t_prog = clock64();
-                } else if (*abort || clock64() - t_prog > lim) {
-                    *abort = 1;
-                    break;
+                tc_commit(&B->pv_done[gP % C::PBUF]);
+                tc_commit(&B->v_empty[st]);
+                gP++;
+                if (++jP == wP.ntiles) {
+                    jP = 0;
+                    itP += gridDim.x;
+                    if (itP < n_items) wP = p.items[itP];
                 }
+                return true;
+            };
+            bool ok = true;
+            while (ok && itP < n_items) {
+                while (ok && itS < n_items && gS < gP + 2) ok = issue_s();
+                if (ok) ok = issue_pv();
             }
             // every MMA this thread issued has completed before TMEM is released
             tc_commit(&B->drain);
@@ -707,32 +700,35 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 // while the other tile's MMAs execute.
 //   warp 0      producer: both Q tiles once per item, K and V tiles into a
 //               4-stage ring; per-tile score multipliers (E4M3 tile mode)
-//   warp 1      TMEM owner and MMA issuer (one thread): an S stream
-//               (S0_j = Q0 K_j^T, then S1_j) and one P V stream per query tile,
-//               each issued as soon as its inputs are ready
+//   warp 1      TMEM owner; its lane 0 issues the MMAs of query tile 0 and
+//   warp 10     lane 0 those of query tile 1, each in a fixed order with S one
+//               key tile ahead: S_q(j+1) = Q_q K_{j+1}^T, then P_q V_j
 //   warps 2-5   softmax of query tile 0, warps 6-9 of query tile 1: one thread
 //               per row, all 128 columns
 // TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512). A K slot is
-// released after S1_j, a V slot after the second P V of tile j.
+// released after both S_0j and S_1j, a V slot after both P V of tile j. P has two
+// shared-memory buffers per query tile: the softmax of tile j writes its P while
+// P V of tile j - 1 may still be reading the other one.
 struct PairCfg {
     static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
     static constexpr int NS = 4;                      // K/V ring depth
     static constexpr int OFF_Q = 0;                   // Q0, Q1
-    static constexpr int OFF_P = 2 * TILE;            // P0, P1
-    static constexpr int OFF_KV = 4 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
+    static constexpr int OFF_P = 2 * TILE;            // P of query tile q, buffer b at (2q + b) TILE
+    static constexpr int OFF_KV = 6 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
     static constexpr int OFF_BAR = OFF_KV + NS * 2 * TILE;
     static constexpr int SMEM = OFF_BAR + 1024 + 1024;
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 352;
     static constexpr uint32_t T_O = 256;              // O_q at T_O + 128 q; S_q at 128 q
 };
+static_assert(PairCfg::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 
 struct PairBars {
     uint64_t q_full, q_empty;
     uint64_t s_full[2], s_empty[2];     // per query tile
-    uint64_t p_full[2], pv_done[2];     // per query tile (one P buffer each)
+    uint64_t p_full[2][2], pv_done[2][2];   // per query tile and P buffer
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
     uint64_t sc_full[8];
-    uint64_t drain;
+    uint64_t drain[2];
     // E4M3 tile mode, key tile g in slot g % 8: K scale x score constant, log2(r), 1/r.
     // The producer is at most NS tiles ahead of the slower softmax group (it needs the
     // K slot that S1 of tile g - NS frees), so eight slots never collide.
@@ -740,6 +736,7 @@ struct PairBars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(PairBars) <= 1024, "pair kernel barrier block exceeds its reserved space");
 
 template <int MODE>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
@@ -757,21 +754,24 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
-        mbar_init(&B->q_empty, 1);
+        mbar_init(&B->q_empty, 2);
         for (int q = 0; q < 2; q++) {
             mbar_init(&B->s_full[q], 1);
             mbar_init(&B->s_empty[q], 128);
-            mbar_init(&B->p_full[q], 128);
-            mbar_init(&B->pv_done[q], 1);
+            for (int b = 0; b < 2; b++) {
+                mbar_init(&B->p_full[q][b], 128);
+                mbar_init(&B->pv_done[q][b], 1);
+            }
         }
         for (int i = 0; i < PC::NS; i++) {
             mbar_init(&B->k_full[i], 1);
             mbar_init(&B->v_full[i], 1);
-            mbar_init(&B->k_empty[i], 1);
-            mbar_init(&B->v_empty[i], 1);
+            mbar_init(&B->k_empty[i], 2);
+            mbar_init(&B->v_empty[i], 2);
         }
         for (int i = 0; i < 8; i++) mbar_init(&B->sc_full[i], 1);
-        mbar_init(&B->drain, 1);
+        mbar_init(&B->drain[0], 1);
+        mbar_init(&B->drain[1], 1);
         B->abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmq);
@@ -866,97 +866,82 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == PC::THREADS / 32 - 1) {
+        // ------------------------------------------------------------ MMA issuers
+        // One thread per query tile (warp 1: tile 0, the last warp: tile 1), so that
+        // neither chain S_q -> softmax_q -> P_q V waits behind the other's. Each issues
+        // in a fixed order with S one key tile ahead of P V (across item boundaries):
+        //   S_0 | S_1 P V_0 | S_2 P V_1 | ...
+        // and parks on the one barrier it needs (mbarrier.try_wait). A K, V or Q slot
+        // is released once both issuers have committed their MMAs that read it.
         if (lane == 0) {
+            const int q = warp == 1 ? 0 : 1;
             constexpr uint32_t id_s = idesc(0, 0, false, false, 128, 128);
             constexpr uint32_t id_pv = idesc(0, 0, false, true, 128, 128);
             constexpr uint64_t TILE16 = (uint64_t)PC::TILE >> 4;
             constexpr uint64_t STAGE16 = (uint64_t)(2 * PC::TILE) >> 4;
-            const uint64_t dq0 = desc_kmajor<1, 128, MODE>(sQ, 0);
+            const uint64_t dq = desc_kmajor<1, 128, MODE>(sQ, 0) + q * TILE16;
             const uint64_t dk0 = desc_kmajor<1, 128, MODE>(sKV, 0);
             const uint64_t dv0 = desc_v<1, 128, MODE>(sKV + PC::TILE, 0);
-            const uint64_t dp0 = desc_p<1>(sP, 0);
-            // S stream: S0_j then S1_j for every key tile j, items back to back
-            int itS = blockIdx.x, jS = 0, qiS = 0, qS = 0;
+            const uint64_t dp0 = desc_p<1>(sP, 0) + 2 * q * TILE16;
+            const uint32_t tS = tmem + q * 128, tO = tmem + PC::T_O + q * 128;
+            int itS = blockIdx.x, jS = 0, qiS = 0;
             uint32_t gS = 0;
-            uint32_t sdone[2] = {0, 0};                // S issued per query tile
             WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
-            // P V streams, one per query tile
-            int itP[2] = {blockIdx.x, blockIdx.x}, jP[2] = {0, 0};
-            uint32_t gP[2] = {0, 0};
-            WorkItem wP[2] = {wS, wS};
-            long long t_prog = clock64();
-            while (itP[0] < n_items || itP[1] < n_items) {
-                bool progressed = false;
-                if (itS < n_items) {
-                    const int st = gS % PC::NS;
-                    const uint32_t x = sdone[qS];
-                    if ((qS != 0 || jS != 0 || mbar_test(&B->q_full, qiS & 1)) &&
-                        mbar_test(&B->k_full[st], (gS / PC::NS) & 1) && mbar_test(&B->s_empty[qS], (x & 1) ^ 1)) {
-                        tc_fence_after();
-                        const uint64_t dq = dq0 + qS * TILE16;
-                        const uint64_t dk = dk0 + st * STAGE16;
+            int itP = blockIdx.x, jP = 0;
+            uint32_t gP = 0;
+            WorkItem wP = wS;
+            auto issue_s = [&]() -> bool {   // S_q of key tile gS
+                const int st = gS % PC::NS;
+                if (jS == 0 && !mbar_wait(&B->q_full, qiS & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->k_full[st], (gS / PC::NS) & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->s_empty[q], (gS & 1) ^ 1, abort, lim)) return false;
+                tc_fence_after();
+                const uint64_t dk = dk0 + st * STAGE16;
 #pragma unroll
-                        for (int kk = 0; kk < C::KSTEPS_S; kk++)
-                            mma_f8(tmem + qS * 128, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s,
-                                   kk ? 1u : 0u);
-                        tc_commit(&B->s_full[qS]);
-                        sdone[qS]++;
-                        if (qS == 1) {
-                            tc_commit(&B->k_empty[st]);
-                            gS++;
-                            qS = 0;
-                            if (++jS == wS.ntiles) {   // last S of the item: Q may be replaced
-                                tc_commit(&B->q_empty);
-                                jS = 0;
-                                qiS++;
-                                itS += gridDim.x;
-                                if (itS < n_items) wS = p.items[itS];
-                            }
-                        } else {
-                            qS = 1;
-                        }
-                        progressed = true;
-                    }
+                for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                    mma_f8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s, kk ? 1u : 0u);
+                tc_commit(&B->s_full[q]);
+                tc_commit(&B->k_empty[st]);
+                gS++;
+                if (++jS == wS.ntiles) {   // last S of the item: Q may be replaced
+                    tc_commit(&B->q_empty);
+                    jS = 0;
+                    qiS++;
+                    itS += gridDim.x;
+                    if (itS < n_items) wS = p.items[itS];
                 }
+                return true;
+            };
+            auto issue_pv = [&]() -> bool {   // P_q V of key tile gP
+                const int st = gP % PC::NS;
+                if (!mbar_wait(&B->v_full[st], (gP / PC::NS) & 1, abort, lim)) return false;
+                if (!mbar_wait(&B->p_full[q][gP & 1], (gP >> 1) & 1, abort, lim)) return false;
+                tc_fence_after();
+                const uint64_t dv = dv0 + st * STAGE16;
+                const uint64_t dp = dp0 + (gP & 1) * TILE16;
+                const bool first = jP == 0;
 #pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    if (itP[q] < n_items && gP[q] < sdone[q]) {
-                        const uint32_t gx = gP[q];
-                        const int st = gx % PC::NS;
-                        if (mbar_test(&B->p_full[q], gx & 1) && mbar_test(&B->v_full[st], (gx / PC::NS) & 1)) {
-                            tc_fence_after();
-                            const uint64_t dv = dv0 + st * STAGE16;
-                            const uint64_t dp = dp0 + q * TILE16;
-                            const bool first = jP[q] == 0;
-#pragma unroll
-                            for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                                mma_f8(tmem + PC::T_O + q * 128, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv,
-                                       (first && kk == 0) ? 0u : 1u);
-                            tc_commit(&B->pv_done[q]);
-                            // the second P V of this key tile frees its V slot
-                            if (gP[q ^ 1] > gx) tc_commit(&B->v_empty[st]);
-                            gP[q]++;
-                            if (++jP[q] == wP[q].ntiles) {
-                                jP[q] = 0;
-                                itP[q] += gridDim.x;
-                                if (itP[q] < n_items) wP[q] = p.items[itP[q]];
-                            }
-                            progressed = true;
-                        }
-                    }
+                for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                    mma_f8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
+                tc_commit(&B->pv_done[q][gP & 1]);
+                tc_commit(&B->v_empty[st]);
+                gP++;
+                if (++jP == wP.ntiles) {
+                    jP = 0;
+                    itP += gridDim.x;
+                    if (itP < n_items) wP = p.items[itP];
                 }
-                if (progressed) {
-                    t_prog = clock64();
-                } else if (*abort || clock64() - t_prog > lim) {
-                    *abort = 1;
-                    break;
-                }
+                return true;
+            };
+            bool ok = itS >= n_items || issue_s();
+            while (ok && itP < n_items) {
+                if (itS < n_items && !issue_s()) break;
+                ok = issue_pv();
             }
             // every MMA this thread issued has completed before TMEM is released
-            tc_commit(&B->drain);
-            wait_drain(&B->drain, 0, lim);
+            tc_commit(&B->drain[q]);
+            wait_drain(&B->drain[q], 0, lim);
         }
         __syncwarp();
     } else {
@@ -967,11 +952,10 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + q * 128;
         const uint32_t tO = tmem + lane_off + PC::T_O + q * 128;
-        uint8_t* pbuf = sm + PC::OFF_P + q * PC::TILE;
         uint32_t g = 0;
         bool ok = true;
         auto wait_pv = [&](uint32_t gx) -> bool {
-            return __all_sync(FULL, mbar_wait(&B->pv_done[q], gx & 1, abort, lim));
+            return __all_sync(FULL, mbar_wait(&B->pv_done[q][gx & 1], (gx >> 1) & 1, abort, lim));
         };
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const WorkItem w = p.items[it];
@@ -999,12 +983,24 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
                 tc_fence_after();
                 float s[128];
+                float c = p.C, lr = 0.0f, invr = 1.0f;
                 {
                     uint32_t u0[32], u1[32], u2[32], u3[32];
                     tmem_ld32(tS, u0);
                     tmem_ld32(tS + 32, u1);
                     tmem_ld32(tS + 64, u2);
                     tmem_ld32(tS + 96, u3);
+                    // the key tile's score multipliers, read while the loads are in flight
+                    if constexpr (MODE == MODE_E4M3_TILE) {
+                        if (!__all_sync(FULL, mbar_wait(&B->sc_full[gj & 7], (gj >> 3) & 1, abort, lim))) {
+                            tmem_wait_ld();
+                            ok = false;
+                            break;
+                        }
+                        c = qs * B->tile_scale[gj & 7][0];
+                        lr = B->tile_scale[gj & 7][1];
+                        invr = B->tile_scale[gj & 7][2];
+                    }
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
@@ -1013,16 +1009,6 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                         s[64 + i] = __uint_as_float(u2[i]);
                         s[96 + i] = __uint_as_float(u3[i]);
                     }
-                }
-                float c = p.C, lr = 0.0f, invr = 1.0f;
-                if constexpr (MODE == MODE_E4M3_TILE) {
-                    if (!__all_sync(FULL, mbar_wait(&B->sc_full[gj & 7], (gj >> 3) & 1, abort, lim))) {
-                        ok = false;
-                        break;
-                    }
-                    c = qs * B->tile_scale[gj & 7][0];
-                    lr = B->tile_scale[gj & 7][1];
-                    invr = B->tile_scale[gj & 7][2];
                 }
                 tc_fence_before();
                 mbar_arrive(&B->s_empty[q]);
@@ -1104,19 +1090,30 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
                 l = alpha * l + rowsum * invr;
                 m = m_new;
-                // the P buffer was last read by P V of the previous tile, which must also be
-                // complete before O is rescaled
-                if (gj > 0 && !wait_pv(gj - 1)) {
+                // P buffer gj & 1 was last read by P V of tile gj - 2. A rescale of O needs
+                // P V of tile gj - 1 complete (and with it every earlier one); without a
+                // rescale, P V of tile gj may queue right behind it on the tensor pipe.
+                const bool rescale = j > 0 && __any_sync(FULL, alpha != 1.0f);
+                if (rescale ? !wait_pv(gj - 1) : (gj >= 2 && !wait_pv(gj - 2))) {
                     ok = false;
                     break;
                 }
-                if (j > 0 && __any_sync(FULL, alpha != 1.0f)) {
+                // the P row -> shared memory (128-byte swizzled K-major rows)
+                uint8_t* pbuf = sm + PC::OFF_P + (2 * q + (gj & 1)) * PC::TILE;
+#pragma unroll
+                for (int ch = 0; ch < 8; ch++) {
+                    uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                if (rescale) {
                     tc_fence_after();
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int cc = 0; cc < 4; cc++) {
-                        uint32_t u[32];
+                    for (int cc = 0; cc < 4; cc += 2) {   // two 32-column loads per round trip
+                        uint32_t u[32], w[32];
                         tmem_ld32(tO + cc * 32, u);
+                        tmem_ld32(tO + cc * 32 + 32, w);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i2 = 0; i2 < 32; i2 += 2) {
@@ -1124,20 +1121,18 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                                 __fmul2_rn(make_float2(__uint_as_float(u[i2]), __uint_as_float(u[i2 + 1])), a2);
                             u[i2] = __float_as_uint(v2.x);
                             u[i2 + 1] = __float_as_uint(v2.y);
+                            const float2 w2 =
+                                __fmul2_rn(make_float2(__uint_as_float(w[i2]), __uint_as_float(w[i2 + 1])), a2);
+                            w[i2] = __float_as_uint(w2.x);
+                            w[i2 + 1] = __float_as_uint(w2.y);
                         }
                         tmem_st32(tO + cc * 32, u);
+                        tmem_st32(tO + cc * 32 + 32, w);
                     }
                     tmem_wait_st();
                 }
-                // the P row -> shared memory (128-byte swizzled K-major rows)
-#pragma unroll
-                for (int ch = 0; ch < 8; ch++) {
-                    uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                }
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&B->p_full[q]);
+                mbar_arrive(&B->p_full[q][gj & 1]);
             }
             if (!ok) break;
             // epilogue: O / l -> bf16, lse
