@@ -416,7 +416,7 @@ def main():
             "config": config_of(args, w),
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": 6 * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (FP8 forward call)", "achieved": achieved,
+            "roofline": {"bound": "tensor", "kernel": "attn_pair_kernel (FP8 forward call)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
                          "peak_basis": peak_basis + " (of measured)"},
             "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"],
