@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 // on the tensor pipe and on the SM sub-partitions, so one tile's softmax runs
 // while the other tile's MMAs execute.
 //   warp 0      producer: both Q tiles once per item, K and V tiles into a
-//               4-stage ring; per-tile score multipliers (E4M3 tile mode)
+//               4-stage ring
 //   warp 1      TMEM owner; its lane 0 issues the MMAs of query tile 0 and
 //   warp 10     lane 0 those of query tile 1, each in a fixed order with S one
 //               key tile ahead: S_q(j+1) = Q_q K_{j+1}^T, then P_q V_j
@@ -727,12 +727,7 @@ struct PairBars {
     uint64_t s_full[2], s_empty[2];     // per query tile
     uint64_t p_full[2][2], pv_done[2][2];   // per query tile and P buffer
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
-    uint64_t sc_full[8];
     uint64_t drain[2];
-    // E4M3 tile mode, key tile g in slot g % 8: K scale x score constant, log2(r), 1/r.
-    // The producer is at most NS tiles ahead of the slower softmax group (it needs the
-    // K slot that S1 of tile g - NS frees), so eight slots never collide.
-    float tile_scale[8][4];
     uint32_t tmem_base;
     int abort;
 };
@@ -769,7 +764,6 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             mbar_init(&B->k_empty[i], 2);
             mbar_init(&B->v_empty[i], 2);
         }
-        for (int i = 0; i < 8; i++) mbar_init(&B->sc_full[i], 1);
         mbar_init(&B->drain[0], 1);
         mbar_init(&B->drain[1], 1);
         B->abort = 0;
@@ -801,8 +795,6 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
-            float ref = 1.0f;
-            if constexpr (MODE == MODE_E4M3_TILE) ref = p.vref[(long long)w.head * p.nd + w.doc];
             if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
             q_issued = qi & 1;
             if (lane == 0) {
@@ -810,37 +802,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 tma_load_3d(sm + PC::OFF_Q, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile);
                 tma_load_3d(sm + PC::OFF_Q + PC::TILE, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile + 128);
             }
-            float t_c = 0.0f, t_lr = 0.0f, t_ir = 1.0f;   // this lane's tile of the current group of 32
             for (int j = 0; j < w.ntiles; j++, g++) {
-                if constexpr (MODE == MODE_E4M3_TILE) {
-                    if ((j & 31) == 0 && j + lane < w.ntiles) {
-                        // K block scale folded with the score constant; V ratio r = s_v / ref
-                        const int jt = j + lane;
-                        const float ks = p.sk[w.head * p.capk + d.boff_k + (128 * jt) / p.bk];
-                        const float sv = p.sv[w.head * p.capv + d.boff_v + (128 * jt) / p.bv];
-                        const float rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
-                        t_c = ks * p.C;
-                        t_lr = __log2f(rj);
-                        t_ir = __fdiv_rn(1.0f, rj);
-                    }
-                }
                 const int st = g % PC::NS;
                 if (!__all_sync(FULL, mbar_wait(&B->k_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
                     ok = false;
                     break;
                 }
                 issued[st] = (g / PC::NS) & 1;
-                if constexpr (MODE == MODE_E4M3_TILE) {
-                    const float c = __shfl_sync(FULL, t_c, j & 31);
-                    const float lr = __shfl_sync(FULL, t_lr, j & 31);
-                    const float ir = __shfl_sync(FULL, t_ir, j & 31);
-                    if (lane == 0) {   // released to both softmax groups through sc_full
-                        B->tile_scale[g & 7][0] = c;
-                        B->tile_scale[g & 7][1] = lr;
-                        B->tile_scale[g & 7][2] = ir;
-                        mbar_arrive(&B->sc_full[g & 7]);
-                    }
-                }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&B->k_full[st], PC::TILE);
                     tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE, &tmk, &B->k_full[st], 0, w.head,
@@ -975,32 +943,32 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
             }
             float m = -INFINITY, l = 0.0f;
+            // E4M3 tile mode: the key tiles' multipliers {K scale x C, log2 r, 1 / r}, one
+            // tile ahead of use (written by the V-reference pass before this launch)
+            const float4* tsc = p.tsc + (long long)h * p.tsc_cap + d.toff;
+            float4 tnext = make_float4(0.0f, 0.0f, 1.0f, 0.0f);
+            if constexpr (MODE == MODE_E4M3_TILE) tnext = tsc[0];
             for (int j = 0; j < nt; j++) {
                 const uint32_t gj = g + j;
+                float c = p.C, lr = 0.0f, invr = 1.0f;
+                if constexpr (MODE == MODE_E4M3_TILE) {
+                    c = qs * tnext.x;
+                    lr = tnext.y;
+                    invr = tnext.z;
+                    if (j + 1 < nt) tnext = tsc[j + 1];
+                }
                 if (!__all_sync(FULL, mbar_wait(&B->s_full[q], gj & 1, abort, lim))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float s[128];
-                float c = p.C, lr = 0.0f, invr = 1.0f;
                 {
                     uint32_t u0[32], u1[32], u2[32], u3[32];
                     tmem_ld32(tS, u0);
                     tmem_ld32(tS + 32, u1);
                     tmem_ld32(tS + 64, u2);
                     tmem_ld32(tS + 96, u3);
-                    // the key tile's score multipliers, read while the loads are in flight
-                    if constexpr (MODE == MODE_E4M3_TILE) {
-                        if (!__all_sync(FULL, mbar_wait(&B->sc_full[gj & 7], (gj >> 3) & 1, abort, lim))) {
-                            tmem_wait_ld();
-                            ok = false;
-                            break;
-                        }
-                        c = qs * B->tile_scale[gj & 7][0];
-                        lr = B->tile_scale[gj & 7][1];
-                        invr = B->tile_scale[gj & 7][2];
-                    }
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; i++) {

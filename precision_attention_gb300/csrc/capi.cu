@@ -141,6 +141,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     DocEntry* docs = reinterpret_cast<DocEntry*>(ws + L.docs_off);
     WorkItem* items = reinterpret_cast<WorkItem*>(ws + L.items_off);
     float* vref = reinterpret_cast<float*>(ws + L.vref_off);
+    float4* tsc = reinterpret_cast<float4*>(ws + L.tsc_off);
     const bool e4m3 = mode == 1 || mode == 2;
 
     SchedParams sp;
@@ -198,6 +199,15 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
         vp.T = T;
         vp.exact = exact;
         vp.bv = qv->block;
+        vp.tiles = (mode == 1 && !exact) ? 1 : 0;
+        vp.bk = qk->block;
+        vp.sk = fp.sk;
+        vp.sk_cap = fp.capk;
+        vp.C = fp.C;
+        vp.tsc = tsc;
+        vp.tsc_cap = L.tsc_cap;
+        fp.tsc = tsc;
+        fp.tsc_cap = L.tsc_cap;
         if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     } else if (mode == 3) {
         fp.mq = static_cast<const uint8_t*>(qq->scales);

@@ -34,10 +34,10 @@ struct WorkItem {
     int32_t ntiles;   // key tiles to visit
 };
 
-// Workspace layout: [header 256 B][docs][items][vref]
+// Workspace layout: [header 256 B][docs][items][vref][tile multipliers]
 struct WsLayout {
-    size_t docs_off, items_off, vref_off, total;
-    int64_t items_cap, vref_cap;
+    size_t docs_off, items_off, vref_off, tsc_off, total;
+    int64_t items_cap, vref_cap, tsc_cap;   // tsc_cap: 128-token tiles per head (bound)
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -49,7 +49,9 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t nd) {
     w.docs_off = 256;
     w.items_off = align_up(w.docs_off + sizeof(DocEntry) * static_cast<size_t>(nd), 256);
     w.vref_off = align_up(w.items_off + sizeof(WorkItem) * static_cast<size_t>(w.items_cap), 256);
-    w.total = align_up(w.vref_off + sizeof(float) * static_cast<size_t>(w.vref_cap), 256);
+    w.tsc_cap = (T + 127) / 128 + nd;
+    w.tsc_off = align_up(w.vref_off + sizeof(float) * static_cast<size_t>(w.vref_cap), 256);
+    w.total = align_up(w.tsc_off + 4 * sizeof(float) * static_cast<size_t>(H * w.tsc_cap), 256);
     return w;
 }
 

@@ -42,6 +42,14 @@ struct VrefParams {
     const WsHeader* hdr;
     float* vref;
     int H, nd, T, exact, bv;
+    // per (head, 128-token key tile) multipliers, written when tiles != 0:
+    // {K scale x C, log2 r, 1 / r, 0} with r = V scale / ref
+    int tiles, bk;
+    const float* sk;
+    long long sk_cap;
+    float C;
+    float4* tsc;
+    long long tsc_cap;
 };
 
 struct FwdParams {
@@ -59,6 +67,8 @@ struct FwdParams {
     const float* vref;
     const uint8_t *mq, *mk, *mv;
     long long ntcap;
+    const float4* tsc;    // per (head, key tile) multipliers (E4M3 tile mode), see VrefParams
+    long long tsc_cap;
     long long wait_limit;
 };
 
