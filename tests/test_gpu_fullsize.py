@@ -1,0 +1,75 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (quantise Q, K, V, then the FP8 forward, one workspace): codes and scales
+of every tensor bit-exact to the oracle's quantiser over the whole tensor, and
+the output on sampled rows (the first, tile-boundary and last rows of every
+document plus seeded random rows, all heads) within the parity bounds against
+the oracle's quantised-operand emulation, with its tie allowance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import compare_outputs, mx_col_tiles_to_logical, mx_row_tiles_to_logical, to_device
+
+pa = pytest.importorskip("precision_attention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+E4M3, ROW, COL = 0, 1, 2
+
+
+def sample_rows(cu, T, seed, n_random=384):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        L = e - s
+        for r in (0, 1, 2, 127, 128, 129, 255, 256, L - 3, L - 2, L - 1):
+            if 0 <= r < L:
+                rows.append(s + r)
+    rows.extend(rng.choice(T, size=min(n_random, T), replace=False).tolist())
+    return np.unique(np.asarray(rows, dtype=np.int32))
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4, 5])
+def test_full_size_codes_and_sampled_rows(oracle_mod, wid):
+    w = workloads.WORKLOADS[wid]
+    inp = workloads.make(wid)
+    T, H, d = inp.q.shape
+    cu = inp.cu_seqlens
+    q, k, v, cu_d = to_device(inp)
+    ws = pa.workspace(T, H, d, len(cu) - 1)
+    seed = w.hadamard_seed
+    if w.mx:
+        lq, lk, lv, blk = ROW, ROW, COL, 32
+    else:
+        lq = lk = lv = E4M3
+        blk = w.block
+    Q = pa.attn_quantize(q, cu_d, lq, blk, True, seed, ws=ws)
+    K = pa.attn_quantize(k, cu_d, lk, blk, True, seed, ws=ws)
+    V = pa.attn_quantize(v, cu_d, lv, blk, False, 0, ws=ws)
+    o, lse = pa.attn_fp8_fwd(Q, K, V, cu_d, w.causal, False, 0.0, ws=ws)
+    st, flags = pa.attn_read_device_status(ws)
+    assert st == 0, (st, flags)
+
+    Qo = oracle.quantize_tensor(inp.q, cu, lq, blk, True, seed)
+    Ko = oracle.quantize_tensor(inp.k, cu, lk, blk, True, seed)
+    Vo = oracle.quantize_tensor(inp.v, cu, lv, blk, False, 0)
+    for name, g, c in (("Q", Q, Qo), ("K", K, Ko), ("V", V, Vo)):
+        gc = g.codes.cpu().numpy()
+        assert np.array_equal(gc, c.codes), f"{name}: {np.count_nonzero(gc != c.codes)} code mismatches"
+        gs = g.scales.cpu().numpy()
+        if not w.mx:
+            nb = c.scales.shape[1]
+            assert np.array_equal(gs[:, :nb].view(np.uint32), c.scales.view(np.uint32)), f"{name} scales"
+        elif name == "V":
+            assert np.array_equal(mx_col_tiles_to_logical(gs, cu, T, H, d), c.scales), f"{name} scales"
+        else:
+            assert np.array_equal(mx_row_tiles_to_logical(gs, cu, T, H), c.scales), f"{name} scales"
+
+    rows = sample_rows(cu, T, seed=wid)
+    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, False, None, rows=rows, ties=True)
+    res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
+    print(f"workload {wid}: {len(rows)} rows x {H} heads:", res)
+    assert res["ok"], res
