@@ -128,14 +128,16 @@ attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t
  * this shape (one buffer serves all three; 256-byte aligned). Host-only. */
 attn_status attn_workspace_size(const attn_shape* shape, size_t* bytes);
 
-/* Fused rotate-and-quantise, one kernel launch (plus a tiny document-table
- * launch when cu_seqlens is set).
+/* Fused rotate-and-quantise, one kernel launch (each CTA builds the document
+ * table it needs from cu_seqlens itself).
  * x: device, bf16 or fp32, element (t, h, c) at x[t * token_stride + h * head_stride + c]
  *    (strides in elements; channels contiguous; 16-byte aligned rows).
  * rotate != 0: codes of H_d * diag(s) * x, s_j = -1 if bit 63 of the j-th
  *    SplitMix64 output from `hadamard_seed` is set, else +1; H_d the
  *    unnormalised Sylvester Hadamard matrix (Q and K only; V is not rotated).
- * Writes out->codes and out->scales; sets out->rotated and out->hadamard_seed. */
+ * Writes out->codes and out->scales; sets out->rotated and out->hadamard_seed.
+ * A scale block holding Inf or NaN raises ATTN_ERR_NONFINITE in the status word;
+ * the codes and scale of such a block are then unspecified. */
 attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
                           const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed,
                           attn_qtensor* out, void* workspace, size_t workspace_bytes, void* stream);

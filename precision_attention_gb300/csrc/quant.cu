@@ -74,32 +74,57 @@ __device__ __forceinline__ void smem_row(const uint8_t* tile, int row, int sl, f
     }
 }
 
-// sign flip then the Walsh-Hadamard stages (see the file comment)
+// sign flip then the Walsh-Hadamard stages (see the file comment). Stage h = 1
+// pairs neighbours held in one register pair; stages 2 .. EPL/2 run two
+// butterflies per packed f32x2 add and fused multiply-add (fma(b, -1, a) is a - b
+// rounded once, so every butterfly is the same IEEE operation as before); the
+// cross-lane stages compute o + s v with s = +-1, i.e. v + o or o - v.
 template <int EPL>
 __device__ __forceinline__ void rotate_row(float (&v)[EPL], uint32_t smask, int lane) {
 #pragma unroll
-    for (int i = 0; i < EPL; i++)
-        if (smask & (1u << i)) v[i] = -v[i];
+    for (int i = 0; i < EPL; i++) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((smask >> i) & 1u) << 31));
 #pragma unroll
-    for (int h = 1; h < EPL; h <<= 1) {
+    for (int i = 0; i < EPL; i += 2) {
+        const float a = v[i], b = v[i + 1];
+        v[i] = __fadd_rn(a, b);
+        v[i + 1] = __fsub_rn(a, b);
+    }
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-        for (int i = 0; i < EPL; i++) {
+    for (int h = 2; h < EPL; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < EPL; i += 2) {
             if (!(i & h)) {
-                const float a = v[i], b = v[i + h];
-                v[i] = __fadd_rn(a, b);
-                v[i + h] = __fsub_rn(a, b);
+                const float2 a = make_float2(v[i], v[i + 1]), b = make_float2(v[i + h], v[i + h + 1]);
+                const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, neg1, a);
+                v[i] = sum.x;
+                v[i + 1] = sum.y;
+                v[i + h] = dif.x;
+                v[i + h + 1] = dif.y;
             }
         }
     }
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+        const float sg = (lane & m) ? -1.0f : 1.0f;
+        const float2 s2 = make_float2(sg, sg);
 #pragma unroll
-        for (int i = 0; i < EPL; i++) {
-            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], m);
-            v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+        for (int i = 0; i < EPL; i += 2) {
+            const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v[i], m);
+            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v[i + 1], m);
+            const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), s2, make_float2(o0, o1));
+            v[i] = r.x;
+            v[i + 1] = r.y;
         }
     }
+}
+
+// max of |a| over values, NaN-propagating (a NaN or infinity anywhere leaves a
+// non-finite result, which the caller reports)
+__device__ __forceinline__ float amax_nan(float m, float a) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(a)));
+    return r;
 }
 
 __device__ __forceinline__ bool finite_abs(float a) { return a <= 3.402823466e38f; }
@@ -123,10 +148,13 @@ __device__ __forceinline__ float pow2_neg(int X) {   // 2^-X for X in [-127, 126
 template <int EPL>
 __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&y)[EPL], float mul) {
     uint32_t w[EPL / 4];
+    const float2 m2 = make_float2(mul, mul);
 #pragma unroll
-    for (int i = 0; i < EPL / 4; i++)
-        w[i] = pack_e4m3x4(__fmul_rn(y[4 * i], mul), __fmul_rn(y[4 * i + 1], mul), __fmul_rn(y[4 * i + 2], mul),
-                           __fmul_rn(y[4 * i + 3], mul));
+    for (int i = 0; i < EPL / 4; i++) {
+        const float2 a = __fmul2_rn(make_float2(y[4 * i], y[4 * i + 1]), m2);
+        const float2 b = __fmul2_rn(make_float2(y[4 * i + 2], y[4 * i + 3]), m2);
+        w[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+    }
     if constexpr (EPL == 16) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
@@ -304,11 +332,11 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                     }
                     if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
 #pragma unroll
-                    for (int i = 0; i < EPL; i++) {
-                        const float a = fabsf(y[hp][i]);
-                        if (!finite_abs(a)) nonfin = true;
-                        else amax = fmaxf(amax, a);
-                    }
+                    for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
+                }
+                if (!finite_abs(amax)) {   // NaN or infinity in this thread's rows
+                    nonfin = true;
+                    amax = 0.0f;
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -350,13 +378,10 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                 smem_row<EPL, ELT>(tile, row, sl, y);
                 if (p.rotate) rotate_row<EPL>(y, smask, lane);
                 float amax = 0.0f;
-                bool bad = false;
 #pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    const float a = fabsf(y[i]);
-                    if (!finite_abs(a)) bad = true;
-                    else amax = fmaxf(amax, a);
-                }
+                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+                bool bad = !finite_abs(amax);
+                if (bad) amax = 0.0f;
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) {
                     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -386,13 +411,10 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                 smem_row<EPL, ELT>(tile, r, sl, y);
                 if (p.rotate) rotate_row<EPL>(y, smask, lane);
                 float amax = 0.0f;
-                bool bad = false;
 #pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    const float a = fabsf(y[i]);
-                    if (!finite_abs(a)) bad = true;
-                    else amax = fmaxf(amax, a);
-                }
+                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+                bool bad = !finite_abs(amax);
+                if (bad) amax = 0.0f;
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
                 bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
                 if (bad && valid) nonfin = true;
