@@ -187,8 +187,13 @@ def gpu_arm(args, rank, world, local_rank):
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     attn_ev = []
+    step_ev = []
 
     def step(record=False):
+        if record:
+            es = torch.cuda.Event(enable_timing=True)
+            es.record(stream)
+            step_ev.append(es)
         pa.attn_quantize(q, cu, lq, blk, True, seed, ws=ws, out=Q, stream=stream)
         pa.attn_quantize(k, cu, lk, blk, True, seed, ws=ws, out=K, stream=stream)
         pa.attn_quantize(v, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
@@ -227,6 +232,8 @@ def gpu_arm(args, rank, world, local_rank):
     clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    ends = step_ev[1:] + [t1]
+    step_ms = [a.elapsed_time(b) for a, b in zip(step_ev, ends)]
     st, flags = pa.attn_read_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {pa.attn_status_string(st)} flags {flags:#x}")
@@ -306,7 +313,10 @@ def gpu_arm(args, rank, world, local_rank):
     ms_step = ms_total / args.steps
     if dist:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev)
+    stats = {name: {"median": float(np.median(x)), "min": float(np.min(x)), "p90": float(np.percentile(x, 90))}
+             for name, x in (("step_ms", step_ms), ("attn_ms", attn_ms))}
     return {"inp": inp, "ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
+            "stats": stats,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "acc": acc, "T": T, "H": H, "d": d, "nd": nd}
 
 
@@ -406,8 +416,8 @@ def config_of(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--heads", type=int, default=None)
@@ -454,10 +464,12 @@ def main():
             "config": config_of(args, w),
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": 6 * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "attn_pair_kernel (FP8 forward call)", "achieved": achieved,
+            "roofline": {"bound": "tensor",
+                         "kernel": ("attn_fwd_kernel" if (w.mx or r["d"] != 128) else "attn_pair_kernel")
+                         + " (FP8 forward call)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
                          "peak_basis": peak_basis + " (of measured)"},
-            "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"],
+            "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"], "timing_stats": r["stats"],
             "clocks": r["clocks"], "accuracy": r["acc"]}
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_sample(args, r.get("inp"))
