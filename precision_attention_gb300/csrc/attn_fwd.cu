@@ -709,18 +709,29 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 // released after both S_0j and S_1j, a V slot after both P V of tile j. P has two
 // shared-memory buffers per query tile: the softmax of tile j writes its P while
 // P V of tile j - 1 may still be reading the other one.
-struct PairCfg {
+template <int MODE>
+struct PairCfgT {
+    static constexpr bool MX = MODE == MODE_MX;
     static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
-    static constexpr int NS = 4;                      // K/V ring depth
+    static constexpr int NS = MX ? 3 : 4;             // K/V ring depth
     static constexpr int OFF_Q = 0;                   // Q0, Q1
     static constexpr int OFF_P = 2 * TILE;            // P of query tile q, buffer b at (2q + b) TILE
     static constexpr int OFF_KV = 6 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
-    static constexpr int OFF_BAR = OFF_KV + NS * 2 * TILE;
+    // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
+    static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
+    static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
+    static constexpr int OFF_BAR = OFF_SF + SF_BYTES;
     static constexpr int SMEM = OFF_BAR + 1024 + 1024;
     static constexpr int THREADS = 352;
-    static constexpr uint32_t T_O = 256;              // O_q at T_O + 128 q; S_q at 128 q
+    static constexpr uint32_t T_O = 256;              // O_q at T_O + 128 q
+    // S_q at 128 q; MX: one S buffer at 0 shared by both query tiles, and the scale
+    // factors in the columns that frees: Q_q at T_SFQ + 4q, P at T_SFP + 4q, K and V
+    // of key tile g at T_SFK / T_SFV + 8q + 4 (g % 2)
+    static constexpr uint32_t T_S1 = MX ? 0 : 128;
+    static constexpr uint32_t T_SFQ = 128, T_SFP = 136, T_SFK = 144, T_SFV = 160;
 };
-static_assert(PairCfg::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
+static_assert(PairCfgT<MODE_E4M3_TILE>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
+static_assert(PairCfgT<MODE_MX>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 
 struct PairBars {
     uint64_t q_full, q_empty;
@@ -734,10 +745,10 @@ struct PairBars {
 static_assert(sizeof(PairBars) <= 1024, "pair kernel barrier block exceeds its reserved space");
 
 template <int MODE>
-__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+__global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
-    using PC = PairCfg;
+    using PC = PairCfgT<MODE>;
     using C = Cfg<1, 128, MODE>;   // descriptor helpers of the 128-byte-row E4M3 tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -772,6 +783,13 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
+    if constexpr (PC::MX) {
+        if (warp == 2) {   // P's block scales: all 2^0 (biased 127)
+            reinterpret_cast<uint4*>(sm + PC::OFF_SF + 1024)[lane] =
+                make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            fence_proxy_async_smem();
+        }
+    }
     if (warp == 1) {
         tmem_alloc(&B->tmem_base, 512);
         tmem_relinquish();
@@ -784,6 +802,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     const uint32_t sQ = smem_u32(sm + PC::OFF_Q);
     const uint32_t sP = smem_u32(sm + PC::OFF_P);
     const uint32_t sKV = smem_u32(sm + PC::OFF_KV);
+    const uint32_t sSF = smem_u32(sm + PC::OFF_SF);
+    (void)sSF;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -797,10 +817,18 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const DocEntry d = p.docs[w.doc];
             if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
             q_issued = qi & 1;
+            // MX: the second query tile's scale tile exists only inside the document
+            const bool q1_in = 2 * w.qtile + 1 < (d.len + 127) / 128;
+            const uint32_t qbytes = 2 * PC::TILE + (PC::MX ? (q1_in ? 1024 : 512) : 0);
             if (lane == 0) {
-                mbar_arrive_expect_tx(&B->q_full, 2 * PC::TILE);
+                mbar_arrive_expect_tx(&B->q_full, qbytes);
                 tma_load_3d(sm + PC::OFF_Q, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile);
                 tma_load_3d(sm + PC::OFF_Q + PC::TILE, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile + 128);
+                if constexpr (PC::MX) {
+                    const long long t0 = (long long)w.head * p.ntcap + d.toff + 2 * w.qtile;
+                    bulk_load(sm + PC::OFF_SF, p.mq + t0 * 512, 512, &B->q_full);
+                    if (q1_in) bulk_load(sm + PC::OFF_SF + 512, p.mq + (t0 + 1) * 512, 512, &B->q_full);
+                }
             }
             for (int j = 0; j < w.ntiles; j++, g++) {
                 const int st = g % PC::NS;
@@ -810,18 +838,24 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 }
                 issued[st] = (g / PC::NS) & 1;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&B->k_full[st], PC::TILE);
+                    mbar_arrive_expect_tx(&B->k_full[st], PC::TILE + (PC::MX ? 512 : 0));
                     tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE, &tmk, &B->k_full[st], 0, w.head,
                                 d.start + 128 * j);
+                    if constexpr (PC::MX)
+                        bulk_load(sm + PC::OFF_SF + 1536 + st * 512,
+                                  p.mk + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->k_full[st]);
                 }
                 if (!__all_sync(FULL, mbar_wait(&B->v_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&B->v_full[st], PC::TILE);
+                    mbar_arrive_expect_tx(&B->v_full[st], PC::TILE + (PC::MX ? 512 : 0));
                     tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE + PC::TILE, &tmv, &B->v_full[st], 0, w.head,
                                 d.start + 128 * j);
+                    if constexpr (PC::MX)
+                        bulk_load(sm + PC::OFF_SF + 1536 + PC::NS * 512 + st * 512,
+                                  p.mv + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->v_full[st]);
                 }
             }
         }
@@ -852,7 +886,11 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const uint64_t dk0 = desc_kmajor<1, 128, MODE>(sKV, 0);
             const uint64_t dv0 = desc_v<1, 128, MODE>(sKV + PC::TILE, 0);
             const uint64_t dp0 = desc_p<1>(sP, 0) + 2 * q * TILE16;
-            const uint32_t tS = tmem + q * 128, tO = tmem + PC::T_O + q * 128;
+            const uint32_t tS = tmem + q * PC::T_S1, tO = tmem + PC::T_O + q * 128;
+            // MX: this query tile's Q, P, K and V scale-factor columns
+            const uint32_t sfq = tmem + PC::T_SFQ + 4 * q, sfp = tmem + PC::T_SFP + 4 * q;
+            const uint32_t sfk0 = tmem + PC::T_SFK + 8 * q, sfv0 = tmem + PC::T_SFV + 8 * q;
+            if constexpr (PC::MX) tc_cp_sf(sfp, desc_sf(sSF + 1024));
             int itS = blockIdx.x, jS = 0, qiS = 0;
             uint32_t gS = 0;
             WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
@@ -863,12 +901,30 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const int st = gS % PC::NS;
                 if (jS == 0 && !mbar_wait(&B->q_full, qiS & 1, abort, lim)) return false;
                 if (!mbar_wait(&B->k_full[st], (gS / PC::NS) & 1, abort, lim)) return false;
-                if (!mbar_wait(&B->s_empty[q], (gS & 1) ^ 1, abort, lim)) return false;
+                if constexpr (PC::MX) {
+                    // one S buffer, written S_0(g), S_1(g), S_0(g + 1), ...: S_0(g) once the
+                    // other group has loaded S_1(g - 1), S_1(g) once this one has loaded S_0(g)
+                    if (q == 0 ? (gS >= 1 && !mbar_wait(&B->s_empty[1], (gS - 1) & 1, abort, lim))
+                               : !mbar_wait(&B->s_empty[0], gS & 1, abort, lim))
+                        return false;
+                } else {
+                    if (!mbar_wait(&B->s_empty[q], (gS & 1) ^ 1, abort, lim)) return false;
+                }
                 tc_fence_after();
                 const uint64_t dk = dk0 + st * STAGE16;
+                if constexpr (PC::MX) {
+                    if (jS == 0) tc_cp_sf(sfq, desc_sf(sSF + 512 * q));
+                    const uint32_t sfk = sfk0 + 4 * (gS & 1);
+                    tc_cp_sf(sfk, desc_sf(sSF + 1536 + st * 512));
 #pragma unroll
-                for (int kk = 0; kk < C::KSTEPS_S; kk++)
-                    mma_f8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s, kk ? 1u : 0u);
+                    for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                        mma_mxf8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk),
+                                 idesc_mx(0, 0, false, false, 128, 128, kk, kk), sfq, sfk, kk ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::KSTEPS_S; kk++)
+                        mma_f8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s, kk ? 1u : 0u);
+                }
                 tc_commit(&B->s_full[q]);
                 tc_commit(&B->k_empty[st]);
                 gS++;
@@ -889,9 +945,18 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const uint64_t dv = dv0 + st * STAGE16;
                 const uint64_t dp = dp0 + (gP & 1) * TILE16;
                 const bool first = jP == 0;
+                if constexpr (PC::MX) {
+                    const uint32_t sfv = sfv0 + 4 * (gP & 1);
+                    tc_cp_sf(sfv, desc_sf(sSF + 1536 + PC::NS * 512 + st * 512));
 #pragma unroll
-                for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                    mma_f8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                        mma_mxf8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk),
+                                 idesc_mx(0, 0, false, true, 128, 128, kk, kk), sfp, sfv, (first && kk == 0) ? 0u : 1u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::KSTEPS_PV; kk++)
+                        mma_f8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
+                }
                 tc_commit(&B->pv_done[q][gP & 1]);
                 tc_commit(&B->v_empty[st]);
                 gP++;
@@ -918,7 +983,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         const int quarter = warp & 3;                             // TMEM lane quarter
         const int r = quarter * 32 + lane;                        // row within the query tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + q * 128;
+        const uint32_t tS = tmem + lane_off + q * PC::T_S1;
         const uint32_t tO = tmem + lane_off + PC::T_O + q * 128;
         uint32_t g = 0;
         bool ok = true;
@@ -934,11 +999,11 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const int qtc = qt < ntd ? qt : ntd - 1;
             const int rloc = 128 * qt + r;                        // row position in the document
             const int rcl = rloc < L ? rloc : L - 1;
-            float qs = 1.0f, ref = 1.0f;
+            float qs = 1.0f, ref = 1.0f;   // MX: the scales are inside the MMAs
             if constexpr (MODE == MODE_E4M3_TILE) {
                 qs = p.sq[h * p.capq + d.boff_q + (128 * qtc) / p.bq];
                 ref = p.vref[(long long)h * p.nd + w.doc];
-            } else {
+            } else if constexpr (MODE == MODE_E4M3_COL) {
                 qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
             }
@@ -1019,7 +1084,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                 const float bias = 8.0f - m_use + lr;
                 uint32_t pk[32];
                 float rowsum;
-                if constexpr (MODE == MODE_E4M3_TILE) {
+                if constexpr (MODE != MODE_E4M3_COL) {
                     const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                      make_float2(0.f, 0.f)};
@@ -1181,10 +1246,11 @@ static cudaError_t launch_pair(const void* q, const void* k, const void* v, cons
     if (!make_map(&mq, q, 1, p.T, p.H, 128, 128, true) || !make_map(&mk, k, 1, p.T, p.H, 128, 128, true) ||
         !make_map(&mv, v, 1, p.T, p.H, 128, 128, true))
         return cudaErrorInvalidValue;
+    using PC = PairCfgT<MODE>;
     auto kern = attn_pair_kernel<MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, PairCfg::THREADS, PairCfg::SMEM, st>>>(mq, mk, mv, p);
+    kern<<<grid, PC::THREADS, PC::SMEM, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 
@@ -1193,12 +1259,12 @@ cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const voi
                         cudaStream_t st) {
     if (mode == MODE_BF16) return D == 128 ? launch_t<2, 128, MODE_BF16>(q, k, v, p, grid, st)
                                            : launch_t<2, 64, MODE_BF16>(q, k, v, p, grid, st);
-    // E4M3 at d = 128: two query tiles per CTA (the work list is built in pair mode)
+    // E4M3 and MX at d = 128: two query tiles per CTA (the work list is built in pair mode)
     if (mode == MODE_E4M3_TILE) return D == 128 ? launch_pair<MODE_E4M3_TILE>(q, k, v, p, grid, st)
                                                 : launch_t<1, 64, MODE_E4M3_TILE>(q, k, v, p, grid, st);
     if (mode == MODE_E4M3_COL) return D == 128 ? launch_pair<MODE_E4M3_COL>(q, k, v, p, grid, st)
                                                : launch_t<1, 64, MODE_E4M3_COL>(q, k, v, p, grid, st);
-    if (mode == MODE_MX && D == 128) return launch_t<1, 128, MODE_MX>(q, k, v, p, grid, st);
+    if (mode == MODE_MX && D == 128) return launch_pair<MODE_MX>(q, k, v, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

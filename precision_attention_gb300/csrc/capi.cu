@@ -157,7 +157,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     sp.docs = docs;
     sp.items = items;
     sp.items_cap = L.items_cap;
-    sp.qpair = (mode == 1 || mode == 2) && d == 128;   // E4M3, d = 128: two query tiles per item
+    sp.qpair = (mode == 1 || mode == 2 || mode == 3) && d == 128;   // FP8, d = 128: two query tiles per item
     cudaError_t e = launch_sched(sp, stream);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
 
