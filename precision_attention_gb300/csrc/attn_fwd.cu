@@ -705,18 +705,25 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 //               key tile ahead: S_q(j+1) = Q_q K_{j+1}^T, then P_q V_j
 //   warps 2-5   softmax of query tile 0, warps 6-9 of query tile 1: one thread
 //               per row, all 128 columns
-// TMEM: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512). A K slot is
-// released after both S_0j and S_1j, a V slot after both P V of tile j. P has two
-// shared-memory buffers per query tile: the softmax of tile j writes its P while
-// P V of tile j - 1 may still be reading the other one.
+// TMEM: one S buffer [0,128) that the two query tiles take in turns (S_0(j), then
+// S_1(j) once group 0 has loaded S_0(j), then S_0(j+1) once group 1 has loaded
+// S_1(j)), O0 [256,384), O1 [384,512); E4M3: P of query tile q, buffer b at
+// 128 + 32 (2q + b) as the A operand of P V; MX: the scale factors of the
+// block-scaled MMAs at [128,176) and P in shared memory. A K slot is released
+// after both S_0j and S_1j, a V slot after both P V of tile j. P has two buffers
+// per query tile: the softmax of tile j writes its P while P V of tile j - 1 may
+// still be reading the other one.
 template <int MODE>
 struct PairCfgT {
     static constexpr bool MX = MODE == MODE_MX;
+    // E4M3: P lives in TMEM (the A operand of P V read from there); MX: in shared
+    // memory, as TMEM holds the scale factors instead
+    static constexpr bool P_TMEM = !MX;
     static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
     static constexpr int NS = MX ? 3 : 4;             // K/V ring depth
     static constexpr int OFF_Q = 0;                   // Q0, Q1
     static constexpr int OFF_P = 2 * TILE;            // P of query tile q, buffer b at (2q + b) TILE
-    static constexpr int OFF_KV = 6 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
+    static constexpr int OFF_KV = P_TMEM ? 2 * TILE : 6 * TILE;   // stage s: K at +2s TILE, V at +(2s + 1) TILE
     // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
     static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
@@ -727,8 +734,10 @@ struct PairCfgT {
     // S_q at 128 q; MX: one S buffer at 0 shared by both query tiles, and the scale
     // factors in the columns that frees: Q_q at T_SFQ + 4q, P at T_SFP + 4q, K and V
     // of key tile g at T_SFK / T_SFV + 8q + 4 (g % 2)
-    static constexpr uint32_t T_S1 = MX ? 0 : 128;
+    static constexpr bool SHARED_S = true;
+    static constexpr uint32_t T_S1 = SHARED_S ? 0 : 128;
     static constexpr uint32_t T_SFQ = 128, T_SFP = 136, T_SFK = 144, T_SFV = 160;
+    static constexpr uint32_t T_P = 128;              // E4M3: P of query tile q, buffer b at T_P + 32 (2q + b)
 };
 static_assert(PairCfgT<MODE_E4M3_TILE>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_MX>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
@@ -901,7 +910,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 const int st = gS % PC::NS;
                 if (jS == 0 && !mbar_wait(&B->q_full, qiS & 1, abort, lim)) return false;
                 if (!mbar_wait(&B->k_full[st], (gS / PC::NS) & 1, abort, lim)) return false;
-                if constexpr (PC::MX) {
+                if constexpr (PC::SHARED_S) {
                     // one S buffer, written S_0(g), S_1(g), S_0(g + 1), ...: S_0(g) once the
                     // other group has loaded S_1(g - 1), S_1(g) once this one has loaded S_0(g)
                     if (q == 0 ? (gS >= 1 && !mbar_wait(&B->s_empty[1], (gS - 1) & 1, abort, lim))
@@ -953,9 +962,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                         mma_mxf8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk),
                                  idesc_mx(0, 0, false, true, 128, 128, kk, kk), sfp, sfv, (first && kk == 0) ? 0u : 1u);
                 } else {
+                    const uint32_t tp = tmem + PC::T_P + 32 * (2 * q + (gP & 1));
 #pragma unroll
                     for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                        mma_f8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
+                        mma_f8_ta(tO, tp + 8 * kk, dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
                 }
                 tc_commit(&B->pv_done[q][gP & 1]);
                 tc_commit(&B->v_empty[st]);
@@ -1131,14 +1141,21 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                // the P row -> shared memory (128-byte swizzled K-major rows)
-                uint8_t* pbuf = sm + PC::OFF_P + (2 * q + (gj & 1)) * PC::TILE;
+                if constexpr (PC::P_TMEM) {
+                    // the P row -> TMEM: word c holds keys 4c .. 4c + 3, as the MMA reads A
+                    tmem_st32(tmem + lane_off + PC::T_P + 32 * (2 * q + (gj & 1)), pk);
+                    tmem_wait_st();
+                } else {
+                    // the P row -> shared memory (128-byte swizzled K-major rows)
+                    uint8_t* pbuf = sm + PC::OFF_P + (2 * q + (gj & 1)) * PC::TILE;
 #pragma unroll
-                for (int ch = 0; ch < 8; ch++) {
-                    uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    for (int ch = 0; ch < 8; ch++) {
+                        uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst) =
+                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 if (rescale) {
                     tc_fence_after();
                     const float2 a2 = make_float2(alpha, alpha);
