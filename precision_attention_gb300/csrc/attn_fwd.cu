@@ -691,15 +691,15 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Two query tiles per CTA (E4M3 codes, d = 128).
+// Two query tiles per CTA (E4M3 and MXFP8 codes, d = 128).
 //
 // The same loop as attn_fwd_kernel, with the CTA's work item widened to the
 // query tiles 2p and 2p + 1 of a (document, head): both share every K and V
 // tile, and their two dependency chains (S -> softmax -> P -> P V) interleave
 // on the tensor pipe and on the SM sub-partitions, so one tile's softmax runs
 // while the other tile's MMAs execute.
-//   warp 0      producer: both Q tiles once per item, K and V tiles into a
-//               4-stage ring
+//   warp 0      producer: both Q tiles once per item, K and V tiles (and MX
+//               scale tiles) into a 4-stage ring (3 for MX)
 //   warp 1      TMEM owner; its lane 0 issues the MMAs of query tile 0 and
 //   warp 10     lane 0 those of query tile 1, each in a fixed order with S one
 //               key tile ahead: S_q(j+1) = Q_q K_{j+1}^T, then P_q V_j
@@ -707,23 +707,21 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 //               per row, all 128 columns
 // TMEM: one S buffer [0,128) that the two query tiles take in turns (S_0(j), then
 // S_1(j) once group 0 has loaded S_0(j), then S_0(j+1) once group 1 has loaded
-// S_1(j)), O0 [256,384), O1 [384,512); E4M3: P of query tile q, buffer b at
-// 128 + 32 (2q + b) as the A operand of P V; MX: the scale factors of the
-// block-scaled MMAs at [128,176) and P in shared memory. A K slot is released
-// after both S_0j and S_1j, a V slot after both P V of tile j. P has two buffers
-// per query tile: the softmax of tile j writes its P while P V of tile j - 1 may
-// still be reading the other one.
+// S_1(j)), O0 [256,384), O1 [384,512); P, the A operand of P V, in TMEM: E4M3 two
+// buffers per query tile at 128 + 32 (2q + b), so the softmax of tile j writes P
+// while P V of tile j - 1 may still read the other one; MX one buffer per query
+// tile at 176 + 32q, beside the block-scaled MMAs' scale factors at [128,176).
+// A K slot is released after both S_0j and S_1j, a V slot after both P V of tile j.
 template <int MODE>
 struct PairCfgT {
     static constexpr bool MX = MODE == MODE_MX;
-    // E4M3: P lives in TMEM (the A operand of P V read from there); MX: in shared
-    // memory, as TMEM holds the scale factors instead
-    static constexpr bool P_TMEM = !MX;
+    // P lives in TMEM, the A operand of P V read from there: two buffers per query
+    // tile, one in MX mode (TMEM also holds the scale factors)
+    static constexpr int PBUF = MX ? 1 : 2;
     static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
     static constexpr int NS = MX ? 3 : 4;             // K/V ring depth
     static constexpr int OFF_Q = 0;                   // Q0, Q1
-    static constexpr int OFF_P = 2 * TILE;            // P of query tile q, buffer b at (2q + b) TILE
-    static constexpr int OFF_KV = P_TMEM ? 2 * TILE : 6 * TILE;   // stage s: K at +2s TILE, V at +(2s + 1) TILE
+    static constexpr int OFF_KV = 2 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
     // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
     static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
@@ -737,16 +735,17 @@ struct PairCfgT {
     static constexpr bool SHARED_S = true;
     static constexpr uint32_t T_S1 = SHARED_S ? 0 : 128;
     static constexpr uint32_t T_SFQ = 128, T_SFP = 136, T_SFK = 144, T_SFV = 160;
-    static constexpr uint32_t T_P = 128;              // E4M3: P of query tile q, buffer b at T_P + 32 (2q + b)
+    static constexpr uint32_t T_P = MX ? 176 : 128;   // P of query tile q, buffer b at T_P + 32 (PBUF q + b)
 };
 static_assert(PairCfgT<MODE_E4M3_TILE>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_MX>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
+static_assert(PairCfgT<MODE_E4M3_TILE>::NS <= 8 && PairCfgT<MODE_MX>::NS <= 8, "K/V ring deeper than its barriers");
 
 struct PairBars {
     uint64_t q_full, q_empty;
     uint64_t s_full[2], s_empty[2];     // per query tile
     uint64_t p_full[2][2], pv_done[2][2];   // per query tile and P buffer
-    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
+    uint64_t k_full[8], v_full[8], k_empty[8], v_empty[8];
     uint64_t drain[2];
     uint32_t tmem_base;
     int abort;
@@ -809,14 +808,13 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     const uint32_t tmem = B->tmem_base;
     const int n_items = p.hdr->n_items;
     const uint32_t sQ = smem_u32(sm + PC::OFF_Q);
-    const uint32_t sP = smem_u32(sm + PC::OFF_P);
     const uint32_t sKV = smem_u32(sm + PC::OFF_KV);
     const uint32_t sSF = smem_u32(sm + PC::OFF_SF);
     (void)sSF;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        int issued[4] = {-1, -1, -1, -1};   // parity of the last load per stage
+        int issued[8] = {-1, -1, -1, -1, -1, -1, -1, -1};   // parity of the last load per stage
         int q_issued = -1;
         uint32_t g = 0;
         int qi = 0;
@@ -894,7 +892,6 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             const uint64_t dq = desc_kmajor<1, 128, MODE>(sQ, 0) + q * TILE16;
             const uint64_t dk0 = desc_kmajor<1, 128, MODE>(sKV, 0);
             const uint64_t dv0 = desc_v<1, 128, MODE>(sKV + PC::TILE, 0);
-            const uint64_t dp0 = desc_p<1>(sP, 0) + 2 * q * TILE16;
             const uint32_t tS = tmem + q * PC::T_S1, tO = tmem + PC::T_O + q * 128;
             // MX: this query tile's Q, P, K and V scale-factor columns
             const uint32_t sfq = tmem + PC::T_SFQ + 4 * q, sfp = tmem + PC::T_SFP + 4 * q;
@@ -952,17 +949,16 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 if (!mbar_wait(&B->p_full[q][gP & 1], (gP >> 1) & 1, abort, lim)) return false;
                 tc_fence_after();
                 const uint64_t dv = dv0 + st * STAGE16;
-                const uint64_t dp = dp0 + (gP & 1) * TILE16;
+                const uint32_t tp = tmem + PC::T_P + 32 * (PC::PBUF * q + gP % PC::PBUF);   // P, A from TMEM
                 const bool first = jP == 0;
                 if constexpr (PC::MX) {
                     const uint32_t sfv = sfv0 + 4 * (gP & 1);
                     tc_cp_sf(sfv, desc_sf(sSF + 1536 + PC::NS * 512 + st * 512));
 #pragma unroll
                     for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                        mma_mxf8(tO, dp + poff(kk), dv + voff<1, 128, MODE>(kk),
-                                 idesc_mx(0, 0, false, true, 128, 128, kk, kk), sfp, sfv, (first && kk == 0) ? 0u : 1u);
+                        mma_mxf8_ta(tO, tp + 8 * kk, dv + voff<1, 128, MODE>(kk),
+                                    idesc_mx(0, 0, false, true, 128, 128, kk, kk), sfp, sfv, (first && kk == 0) ? 0u : 1u);
                 } else {
-                    const uint32_t tp = tmem + PC::T_P + 32 * (2 * q + (gP & 1));
 #pragma unroll
                     for (int kk = 0; kk < C::KSTEPS_PV; kk++)
                         mma_f8_ta(tO, tp + 8 * kk, dv + voff<1, 128, MODE>(kk), id_pv, (first && kk == 0) ? 0u : 1u);
@@ -1137,25 +1133,13 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 // P V of tile gj - 1 complete (and with it every earlier one); without a
                 // rescale, P V of tile gj may queue right behind it on the tensor pipe.
                 const bool rescale = j > 0 && __any_sync(FULL, alpha != 1.0f);
-                if (rescale ? !wait_pv(gj - 1) : (gj >= 2 && !wait_pv(gj - 2))) {
+                if (rescale ? !wait_pv(gj - 1) : (gj >= (uint32_t)PC::PBUF && !wait_pv(gj - PC::PBUF))) {
                     ok = false;
                     break;
                 }
-                if constexpr (PC::P_TMEM) {
-                    // the P row -> TMEM: word c holds keys 4c .. 4c + 3, as the MMA reads A
-                    tmem_st32(tmem + lane_off + PC::T_P + 32 * (2 * q + (gj & 1)), pk);
-                    tmem_wait_st();
-                } else {
-                    // the P row -> shared memory (128-byte swizzled K-major rows)
-                    uint8_t* pbuf = sm + PC::OFF_P + (2 * q + (gj & 1)) * PC::TILE;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ch++) {
-                        uint8_t* dst = pbuf + r * 128 + ((ch ^ (r & 7)) << 4);
-                        *reinterpret_cast<uint4*>(dst) =
-                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                    }
-                    fence_proxy_async_smem();
-                }
+                // the P row -> TMEM: word c holds keys 4c .. 4c + 3, as the MMA reads A
+                tmem_st32(tmem + lane_off + PC::T_P + 32 * (PC::PBUF * q + gj % PC::PBUF), pk);
+                tmem_wait_st();
                 if (rescale) {
                     tc_fence_after();
                     const float2 a2 = make_float2(alpha, alpha);

@@ -178,6 +178,14 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b
             d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc));
 }
+__device__ __forceinline__ void mma_mxf8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t sfa,
+                                            uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc));
+}
 // 32 lanes x 128 bits from shared memory, replicated into the four 32-lane
 // quarters of TMEM (the scale-factor copy of block-scaled MMAs)
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t src_desc) {
