@@ -11,17 +11,21 @@
 // skipped and the diagonal tile is masked; packed documents are addressed in
 // place through the document table (FLAMIA 4.1).
 //
-// One CTA per SM, persistent over work items (query tile of 128 rows of one
-// document and head). Warp roles:
+// Two kernels. attn_pair_kernel (below) runs the FP8 modes at d = 128 (E4M3
+// token-block scales and MXFP8) with two query tiles per CTA. attn_fwd_kernel
+// runs the BF16 comparator path and the E4M3 modes at d = 64, one query tile
+// (128 rows of one document and head) per work item, one CTA per SM,
+// persistent over the work items. Its warp roles:
 //   warp 0      TMA producer: Q tile once per item, K and V tiles of each key
-//               block into an NS-stage ring (plus the MX scale tiles)
+//               block into an NS-stage ring
 //   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
 //               S buffers, then O += P_{j-1} V_{j-1}
-//   warps 2-5   softmax: one thread per query row; S row from TMEM, scale,
-//               mask, running max/sum, exp2, P row to shared memory (E4M3 or
-//               BF16), O rescale in TMEM, final normalisation and stores
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + d), MX scale
-// factors from column 384.
+//   warps 2-9   softmax: two warps per 32-row TMEM lane quarter, each holding
+//               half of the S columns of its rows; S from TMEM, scale, mask,
+//               running max (combined through shared memory) and sum, exp2, P to
+//               shared memory (E4M3 or BF16), O rescale in TMEM, final
+//               normalisation and stores
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256 + d).
 // Every mbarrier wait is bounded; on a timeout the CTA raises a flag, stops,
 // drains its TMA copies, frees TMEM and returns, and the host reads
 // ATTN_ERR_DEVICE_TIMEOUT from the status word.
@@ -51,9 +55,7 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_P = OFF_Q + TILE;
     static constexpr int OFF_KV = OFF_P + PBUF * PBYTES;
-    static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
-    static constexpr int SF_BYTES = MODE == MODE_MX ? 512 * (2 + 2 * NS) : 0;
-    static constexpr int OFF_XCH = OFF_SF + SF_BYTES;       // float [2 parities][2 halves][128 rows] row maxima
+    static constexpr int OFF_XCH = OFF_KV + NS * 2 * TILE;  // float [2 parities][2 halves][128 rows] row maxima
     static constexpr int OFF_XL = OFF_XCH + 2 * 2 * 128 * 4; // float [2 halves][128 rows] row sums
     static constexpr int OFF_BAR = OFF_XL + 2 * 128 * 4;
     // at least 116 KB so that one CTA (which allocates all 512 TMEM columns) fits per SM
@@ -63,7 +65,7 @@ struct Cfg {
     static constexpr int HC = 64;                            // S columns per softmax thread
     static constexpr int HD = D / 2;                         // O columns per softmax thread
     // TMEM columns
-    static constexpr uint32_t T_O = 256, T_SFQ = 384, T_SFP = 388, T_SFK = 392, T_SFV = 400;
+    static constexpr uint32_t T_O = 256;
 };
 
 struct Bars {
@@ -178,12 +180,6 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
-    if constexpr (MODE == MODE_MX) {
-        if (warp == 2) {   // P's block scales: all 2^0 (biased 127)
-            reinterpret_cast<uint4*>(sm + C::OFF_SF + 512)[lane] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            fence_proxy_async_smem();
-        }
-    }
     if (warp == 1) {
         tmem_alloc(&B->tmem_base, 512);
         tmem_relinquish();
@@ -197,7 +193,6 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
     const uint32_t sQ = smem_u32(sm + C::OFF_Q);
     const uint32_t sP = smem_u32(sm + C::OFF_P);
     const uint32_t sKV = smem_u32(sm + C::OFF_KV);
-    const uint32_t sSF = smem_u32(sm + C::OFF_SF);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -219,16 +214,13 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                 ref = p.vref[(long long)w.head * p.nd + w.doc];
             }
             if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
-            const uint32_t qbytes = C::TILE + (MODE == MODE_MX ? 512 : 0);
+            const uint32_t qbytes = C::TILE;
             q_issued = qi & 1;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&B->q_full, qbytes);
                 for (int a = 0; a < C::ATOMS; a++)
                     tma_load_3d(sm + C::OFF_Q + a * 16384, &tmq, &B->q_full, a * C::BOX_ELEMS, w.head,
                                 d.start + 128 * w.qtile);
-                if constexpr (MODE == MODE_MX)
-                    bulk_load(sm + C::OFF_SF, p.mq + ((long long)w.head * p.ntcap + d.toff + w.qtile) * 512, 512,
-                              &B->q_full);
             }
             float t_c = 0.0f, t_lr = 0.0f, t_ir = 1.0f;   // this lane's tile of the current group of 32
             for (int j = 0; j < w.ntiles; j++, g++) {
@@ -267,9 +259,6 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                     mbar_arrive_expect_tx(&B->k_full[st], qbytes);
                     for (int a = 0; a < C::ATOMS; a++)
                         tma_load_3d(kt + a * 16384, &tmk, &B->k_full[st], a * C::BOX_ELEMS, w.head, k0);
-                    if constexpr (MODE == MODE_MX)
-                        bulk_load(sm + C::OFF_SF + 1024 + st * 512,
-                                  p.mk + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->k_full[st]);
                 }
                 if (!__all_sync(FULL, mbar_wait(&B->v_empty[st], ((g / C::NS) & 1) ^ 1, abort, lim))) {
                     ok = false;
@@ -281,9 +270,6 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                     for (int a = 0; a < C::ATOMS; a++)
                         tma_load_3d(vt + a * 16384, &tmv, &B->v_full[st], a * C::BOX_ELEMS, w.head,
                                     d.start + 128 * j);
-                    if constexpr (MODE == MODE_MX)
-                        bulk_load(sm + C::OFF_SF + 1024 + C::NS * 512 + st * 512,
-                                  p.mv + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->v_full[st]);
                 }
             }
         }
@@ -310,7 +296,6 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
             const uint64_t dp0 = desc_p<ELT>(sP, 0);
             constexpr uint64_t STAGE16 = (uint64_t)(2 * C::TILE) >> 4;   // descriptor step between stages
             constexpr uint64_t PBUF16 = (uint64_t)C::PBYTES >> 4;
-            if constexpr (MODE == MODE_MX) tc_cp_sf(tmem + C::T_SFP, desc_sf(sSF + 512));
             // Fixed order, S up to two key tiles ahead of P V (two S buffers), across
             // item boundaries:  S_0 S_1 | P V_0 S_2 | P V_1 S_3 | ...  as  S_{j+2} needs
             // only that the softmax has loaded S_j, which it does before P_j is ready.
@@ -328,26 +313,14 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                 if (!mbar_wait(&B->k_full[st], (gS / C::NS) & 1, abort, lim)) return false;
                 if (!mbar_wait(&B->s_empty[b], ((gS >> 1) & 1) ^ 1, abort, lim)) return false;
                 tc_fence_after();
-                if constexpr (MODE == MODE_MX) {
-                    if (jS == 0) tc_cp_sf(tmem + C::T_SFQ, desc_sf(sSF));
-                }
                 const uint64_t dk = dk0 + st * STAGE16;
                 const uint32_t dS = tmem + b * 128;
-                if constexpr (MODE == MODE_MX) {
-                    const uint32_t sfk = tmem + C::T_SFK + (gS & 1) * 4;
-                    tc_cp_sf(sfk, desc_sf(sSF + 1024 + st * 512));
 #pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_S; kk++)
-                        mma_mxf8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk),
-                                 idesc_mx(0, 0, false, false, 128, 128, kk, kk), tmem + C::T_SFQ, sfk, kk ? 1u : 0u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_S; kk++) {
-                        if constexpr (ELT == 2)
-                            mma_f16(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
-                        else
-                            mma_f8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < C::KSTEPS_S; kk++) {
+                    if constexpr (ELT == 2)
+                        mma_f16(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
+                    else
+                        mma_f8(dS, dq + koff<ELT, D, MODE>(kk), dk + koff<ELT, D, MODE>(kk), id_s, kk ? 1u : 0u);
                 }
                 tc_commit(&B->s_full[b]);
                 tc_commit(&B->k_empty[st]);
@@ -369,24 +342,14 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                 const uint64_t dv = dv0 + st * STAGE16;
                 const uint64_t dp = dp0 + (gP % C::PBUF) * PBUF16;
                 const bool first = jP == 0;
-                if constexpr (MODE == MODE_MX) {
-                    const uint32_t sfv = tmem + C::T_SFV + (gP & 1) * 4;
-                    tc_cp_sf(sfv, desc_sf(sSF + 1024 + C::NS * 512 + st * 512));
 #pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_PV; kk++)
-                        mma_mxf8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk),
-                                 idesc_mx(0, 0, false, true, 128, D, kk, kk), tmem + C::T_SFP, sfv,
-                                 (first && kk == 0) ? 0u : 1u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
-                        if constexpr (ELT == 2)
-                            mma_f16(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
-                                    (first && kk == 0) ? 0u : 1u);
-                        else
-                            mma_f8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
-                                   (first && kk == 0) ? 0u : 1u);
-                    }
+                for (int kk = 0; kk < C::KSTEPS_PV; kk++) {
+                    if constexpr (ELT == 2)
+                        mma_f16(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                                (first && kk == 0) ? 0u : 1u);
+                    else
+                        mma_f8(tmem + C::T_O, dp + poff(kk), dv + voff<ELT, D, MODE>(kk), id_pv,
+                               (first && kk == 0) ? 0u : 1u);
                 }
                 tc_commit(&B->pv_done[gP % C::PBUF]);
                 tc_commit(&B->v_empty[st]);
