@@ -774,6 +774,16 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     const uint32_t sKV = smem_u32(sm + PC::OFF_KV);
     const uint32_t sSF = smem_u32(sm + PC::OFF_SF);
     (void)sSF;
+    // Work item of this CTA in round k. Causal: the CTAs take rounds of gridDim.x
+    // items of the longest-first list in alternating directions, so that long and
+    // short items even out across CTAs. Otherwise (equal items, head-major) the same
+    // direction every round, which keeps each round's heads on the same SMs and
+    // their K/V in the nearer L2 partition. Every role walks the same sequence.
+    const bool snake = p.causal != 0;
+    auto item_of = [&](int k) -> int {
+        const int g = (int)gridDim.x, b = (int)blockIdx.x;
+        return k * g + ((snake && (k & 1)) ? g - 1 - b : b);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -782,7 +792,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         uint32_t g = 0;
         int qi = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
+        for (int k = 0, it = item_of(0); it < n_items && ok; it = item_of(++k), qi++) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
             if (!__all_sync(FULL, mbar_wait(&B->q_empty, (qi & 1) ^ 1, abort, lim))) break;
@@ -860,10 +870,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             const uint32_t sfq = tmem + PC::T_SFQ + 4 * q, sfp = tmem + PC::T_SFP + 4 * q;
             const uint32_t sfk0 = tmem + PC::T_SFK + 8 * q, sfv0 = tmem + PC::T_SFV + 8 * q;
             if constexpr (PC::MX) tc_cp_sf(sfp, desc_sf(sSF + 1024));
-            int itS = blockIdx.x, jS = 0, qiS = 0;
+            int kS = 0, itS = item_of(0), jS = 0, qiS = 0;
             uint32_t gS = 0;
-            WorkItem wS = blockIdx.x < n_items ? p.items[blockIdx.x] : WorkItem{};
-            int itP = blockIdx.x, jP = 0;
+            WorkItem wS = itS < n_items ? p.items[itS] : WorkItem{};
+            int kP = 0, itP = itS, jP = 0;
             uint32_t gP = 0;
             WorkItem wP = wS;
             auto issue_s = [&]() -> bool {   // S_q of key tile gS
@@ -901,7 +911,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     tc_commit(&B->q_empty);
                     jS = 0;
                     qiS++;
-                    itS += gridDim.x;
+                    itS = item_of(++kS);
                     if (itS < n_items) wS = p.items[itS];
                 }
                 return true;
@@ -931,7 +941,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 gP++;
                 if (++jP == wP.ntiles) {
                     jP = 0;
-                    itP += gridDim.x;
+                    itP = item_of(++kP);
                     if (itP < n_items) wP = p.items[itP];
                 }
                 return true;
@@ -959,7 +969,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         auto wait_pv = [&](uint32_t gx) -> bool {
             return __all_sync(FULL, mbar_wait(&B->pv_done[q][gx & 1], (gx >> 1) & 1, abort, lim));
         };
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        for (int k = 0, it = item_of(0); it < n_items && ok; it = item_of(++k)) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
             const int h = w.head, L = d.len, nt = w.ntiles;
