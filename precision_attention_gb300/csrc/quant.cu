@@ -248,9 +248,9 @@ struct QuantSmem {
     static constexpr int STAGE = 128 * EPL * 8 * ELT;   // 128 rows x d elements
     static constexpr int OFF_TAB = 2 * STAGE;
     static constexpr int OFF_SCRATCH = (OFF_TAB + (int)sizeof(DocTable) + 127) / 128 * 128;   // 32 ints
-    static constexpr int OFF_RED = OFF_SCRATCH + 32 * 4;                                     // float[8][128]
-    static constexpr int OFF_XS = OFF_RED + 8 * 128 * 4;                                     // int[128]
-    static constexpr int OFF_BAR = OFF_XS + 128 * 4;                                         // uint64[2]
+    static constexpr int OFF_RED = OFF_SCRATCH + 32 * 4;                                     // float[4][8][128]
+    static constexpr int OFF_XS = OFF_RED + 4 * 8 * 128 * 4;                                 // int[4][128]
+    static constexpr int OFF_BAR = OFF_XS + 4 * 128 * 4;                                     // uint64[2]
     static constexpr int OFF_FLAG = OFF_BAR + 2 * 8;                                         // int[2]
     static constexpr int BYTES = OFF_FLAG + 2 * 4 + 128;                                     // + base alignment
     static_assert(STAGE % 128 == 0 && OFF_SCRATCH % 128 == 0, "TMA destinations need 128-byte alignment");
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     DocTable& tab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
     int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 17 ints
-    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [8][128]
-    int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [128]
+    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [4][8][128]
+    int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
     int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
     volatile int* abort = flag + 1;
@@ -430,58 +430,65 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                     store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
             }
         } else {   // QM_MX_COL
+            // all four 32-row groups of the unit at once: each thread holds its row of
+            // every group, the maxima over a group's rows go through the warp (shuffles
+            // over its four rows) and shared memory (over the eight warps), so the unit
+            // needs two block-wide barriers instead of two per group
             uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-#pragma unroll 1
-            for (int gi = 0; gi < 4; gi++) {
-                if (t0 + gi * 32 >= L) {                       // group past the document end (uniform)
-                    if (tid < 128) sct[(tid % 32) * 16 + (tid / 32) * 4 + gi] = 127;
-                    continue;
-                }
-                const int row = gi * 32 + warp * 4 + rw;
-                const bool valid = t0 + row < L;
-                float y[EPL];
-                smem_row<EPL, ELT>(tile, row, sl, y);
-                if (!valid) {
+            float y[4][EPL];
 #pragma unroll
-                    for (int i = 0; i < EPL; i++) y[i] = 0.0f;
+            for (int gi = 0; gi < 4; gi++) {
+                const int row = gi * 32 + warp * 4 + rw;
+                smem_row<EPL, ELT>(tile, row, sl, y[gi]);
+                if (t0 + row >= L) {
+#pragma unroll
+                    for (int i = 0; i < EPL; i++) y[gi][i] = 0.0f;
                 }
-                if (p.rotate) rotate_row<EPL>(y, smask, lane);
                 float a[EPL];
 #pragma unroll
                 for (int i = 0; i < EPL; i++) {
-                    a[i] = fabsf(y[i]);
+                    a[i] = fabsf(y[gi][i]);
                     if (!finite_abs(a[i])) { nonfin = true; a[i] = 0.0f; }
                     a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 8));
                     a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 16));
                 }
                 if (rw == 0) {
 #pragma unroll
-                    for (int i = 0; i < EPL; i++) red[warp * 128 + sl * EPL + i] = a[i];
+                    for (int i = 0; i < EPL; i += 4)
+                        *reinterpret_cast<float4*>(red + (gi * 8 + warp) * 128 + sl * EPL + i) =
+                            make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
                 }
-                __syncthreads();
-                if (tid < 128) {
-                    float m = red[tid];
+            }
+            __syncthreads();
 #pragma unroll
-                    for (int w = 1; w < 8; w++) m = fmaxf(m, red[w * 128 + tid]);
-                    const int X = e8m0_exponent(m, p.mx_rule);
-                    xs[tid] = X;
-                    sct[(tid % 32) * 16 + (tid / 32) * 4 + gi] = (uint8_t)(X + 127);
-                }
-                __syncthreads();
-                if (valid) {
+            for (int e = tid; e < 512; e += QUANT_THREADS) {    // (group, channel) pairs
+                const int gi = e >> 7, c = e & 127;
+                float m = red[(gi * 8) * 128 + c];
+#pragma unroll
+                for (int w = 1; w < 8; w++) m = fmaxf(m, red[(gi * 8 + w) * 128 + c]);
+                const bool inside = t0 + gi * 32 < L;           // groups past the document end: 127
+                const int X = inside ? e8m0_exponent(m, p.mx_rule) : 0;
+                xs[e] = X;
+                sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X + 127);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int gi = 0; gi < 4; gi++) {
+                const int row = gi * 32 + warp * 4 + rw;
+                if (t0 + row < L) {
                     uint32_t w4[EPL / 4];
 #pragma unroll
                     for (int i = 0; i < EPL / 4; i++) {
                         const int c = sl * EPL + 4 * i;
-                        w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(xs[c])),
-                                            __fmul_rn(y[4 * i + 1], pow2_neg(xs[c + 1])),
-                                            __fmul_rn(y[4 * i + 2], pow2_neg(xs[c + 2])),
-                                            __fmul_rn(y[4 * i + 3], pow2_neg(xs[c + 3])));
+                        const int4 x4 = *reinterpret_cast<const int4*>(xs + gi * 128 + c);
+                        w4[i] = pack_e4m3x4(__fmul_rn(y[gi][4 * i], pow2_neg(x4.x)),
+                                            __fmul_rn(y[gi][4 * i + 1], pow2_neg(x4.y)),
+                                            __fmul_rn(y[gi][4 * i + 2], pow2_neg(x4.z)),
+                                            __fmul_rn(y[gi][4 * i + 3], pow2_neg(x4.w)));
                     }
                     *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
                         make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-                __syncthreads();                               // red[] and xs[] reused by the next group
             }
         }
         __syncthreads();                                       // every read of this stage is done
