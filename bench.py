@@ -168,6 +168,7 @@ def gpu_arm(args, rank, world, local_rank):
     causal = w.causal
     mx = w.mx
     seed = w.hadamard_seed
+    rot = not args.no_rotate
     flops = workloads.attention_flops(cu_np, H, d, causal)
     in_dt = torch.float32 if w.in_dtype == "f32" else torch.bfloat16
 
@@ -194,8 +195,8 @@ def gpu_arm(args, rank, world, local_rank):
             es = torch.cuda.Event(enable_timing=True)
             es.record(stream)
             step_ev.append(es)
-        pa.attn_quantize(q, cu, lq, blk, True, seed, ws=ws, out=Q, stream=stream)
-        pa.attn_quantize(k, cu, lk, blk, True, seed, ws=ws, out=K, stream=stream)
+        pa.attn_quantize(q, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
+        pa.attn_quantize(k, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
         pa.attn_quantize(v, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
         if record:
             e0 = torch.cuda.Event(enable_timing=True)
@@ -276,8 +277,8 @@ def gpu_arm(args, rank, world, local_rank):
                 stream.wait_event(d2h_done[b])      # step i - 2's output has been read back
             qi, ki, vi = sets_in[b]
             oi, li = sets_out[b]
-            pa.attn_quantize(qi, cu, lq, blk, True, seed, ws=ws, out=Q, stream=stream)
-            pa.attn_quantize(ki, cu, lk, blk, True, seed, ws=ws, out=K, stream=stream)
+            pa.attn_quantize(qi, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
+            pa.attn_quantize(ki, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
             pa.attn_quantize(vi, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
             pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws, out=oi, lse=li, stream=stream)
             comp_done[b].record(stream)
@@ -307,7 +308,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     # accuracy on sampled rows (outside the timed region): FP8 and BF16 paths vs FP64
     acc = None
-    if rank == 0 and not args.no_accuracy and not mx and not causal:
+    if rank == 0 and not args.no_accuracy:
         acc = accuracy_sample(args, inp, q, k, v, cu, o, pa, torch)
 
     ms_step = ms_total / args.steps
@@ -324,8 +325,9 @@ def accuracy_sample(args, inp, q, k, v, cu, o_fp8, pa, torch):
     import oracle
     rng = np.random.default_rng(123)
     rows = np.sort(rng.choice(inp.T, size=min(64, inp.T), replace=False)).astype(np.int32)
-    ob, _ = pa.attn_bf16_fwd(q, k, v, cu, False)
-    o1, _ = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, False, None, rows=rows)
+    causal = workloads.WORKLOADS[args.workload].causal
+    ob, _ = pa.attn_bf16_fwd(q, k, v, cu, causal)
+    o1, _ = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, causal, None, rows=rows)
     o8 = o_fp8.float().cpu().numpy()[rows].astype(np.float64)
     obb = ob.float().cpu().numpy()[rows].astype(np.float64)
     r8 = float(np.sqrt(np.mean((o8 - o1) ** 2)))
@@ -361,12 +363,12 @@ def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
         v = np.ascontiguousarray(inp.v[:L0, h:h + 1])
         t0 = time.perf_counter()
         if w.mx:
-            Q = oracle.quantize_tensor(q, c1, ROW, 32, True, w.hadamard_seed)
-            K = oracle.quantize_tensor(k, c1, ROW, 32, True, w.hadamard_seed)
+            Q = oracle.quantize_tensor(q, c1, ROW, 32, not args.no_rotate, w.hadamard_seed)
+            K = oracle.quantize_tensor(k, c1, ROW, 32, not args.no_rotate, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, COL, 32, False, 0)
         else:
-            Q = oracle.quantize_tensor(q, c1, E4M3, w.block, True, w.hadamard_seed)
-            K = oracle.quantize_tensor(k, c1, E4M3, w.block, True, w.hadamard_seed)
+            Q = oracle.quantize_tensor(q, c1, E4M3, w.block, not args.no_rotate, w.hadamard_seed)
+            K = oracle.quantize_tensor(k, c1, E4M3, w.block, not args.no_rotate, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, E4M3, w.block, False, 0)
         oracle.attention_emulate(Q, K, V, c1, w.causal, False, None, rows=row_idx)
         t_total += time.perf_counter() - t0
@@ -408,7 +410,7 @@ def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
             "causal": w.causal, "quant": ("MXFP8 (E8M0 per 32)" if w.mx else f"E4M3 blocks of {w.block} tokens") +
-            " + Hadamard rotation of Q, K", "input_dtype": w.in_dtype,
+            (" + Hadamard rotation of Q, K" if not args.no_rotate else ", no rotation"), "input_dtype": w.in_dtype,
             "l2": "inputs larger than L2 (bf16 Q, K, V and their codes each exceed 129 MB)" if (
                 args.heads is None and args.seqlen is None) else "reduced size"}
 
@@ -425,6 +427,7 @@ def main():
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-accuracy", action="store_true")
+    ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
