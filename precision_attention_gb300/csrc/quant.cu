@@ -430,64 +430,65 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                     store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
             }
         } else {   // QM_MX_COL
-            // all four 32-row groups of the unit at once: each thread holds its row of
-            // every group, the maxima over a group's rows go through the warp (shuffles
-            // over its four rows) and shared memory (over the eight warps), so the unit
-            // needs two block-wide barriers instead of two per group
+            // Column maxima straight from the staged tile: warp w takes group w / 2 and
+            // channel pairs 32 (w % 2) .. + 31, one pair per lane, and scans the group's
+            // 32 rows (one 32-bit bf16 pair or 64-bit fp32 pair per row: consecutive
+            // words across the warp). No shuffles and one barrier; the codes are then
+            // written row-parallel as in the other layouts.
             uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-            float y[4][EPL];
-#pragma unroll
-            for (int gi = 0; gi < 4; gi++) {
-                const int row = gi * 32 + warp * 4 + rw;
-                smem_row<EPL, ELT>(tile, row, sl, y[gi]);
-                if (t0 + row >= L) {
-#pragma unroll
-                    for (int i = 0; i < EPL; i++) y[gi][i] = 0.0f;
+            {
+                const int gi = warp >> 1, c = 2 * (32 * (warp & 1) + lane);   // first channel of the pair
+                const int nrow = min(32, L - t0 - gi * 32);                     // rows inside the document
+                float m0 = 0.0f, m1 = 0.0f;
+                for (int r = 0; r < nrow; r++) {
+                    float v0, v1;
+                    const int row = gi * 32 + r;
+                    if constexpr (ELT == 2) {
+                        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(tile + (row * D + c) * 2);
+                        v0 = __uint_as_float(w2 << 16);
+                        v1 = __uint_as_float(w2 & 0xFFFF0000u);
+                    } else {
+                        const float2 f2 = *reinterpret_cast<const float2*>(tile + (row * D + c) * 4);
+                        v0 = f2.x;
+                        v1 = f2.y;
+                    }
+                    m0 = amax_nan(m0, v0);
+                    m1 = amax_nan(m1, v1);
                 }
-                float a[EPL];
-#pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    a[i] = fabsf(y[gi][i]);
-                    if (!finite_abs(a[i])) { nonfin = true; a[i] = 0.0f; }
-                    a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 8));
-                    a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], 16));
-                }
-                if (rw == 0) {
-#pragma unroll
-                    for (int i = 0; i < EPL; i += 4)
-                        *reinterpret_cast<float4*>(red + (gi * 8 + warp) * 128 + sl * EPL + i) =
-                            make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
-                }
+                if (!finite_abs(m0)) { nonfin = true; m0 = 0.0f; }
+                if (!finite_abs(m1)) { nonfin = true; m1 = 0.0f; }
+                const bool inside = nrow > 0;                    // groups past the document end: 127
+                const int X0 = inside ? e8m0_exponent(m0, p.mx_rule) : 0;
+                const int X1 = inside ? e8m0_exponent(m1, p.mx_rule) : 0;
+                xs[gi * 128 + c] = X0;
+                xs[gi * 128 + c + 1] = X1;
+                sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X0 + 127);
+                sct[((c + 1) % 32) * 16 + ((c + 1) / 32) * 4 + gi] = (uint8_t)(X1 + 127);
             }
             __syncthreads();
-#pragma unroll
-            for (int e = tid; e < 512; e += QUANT_THREADS) {    // (group, channel) pairs
-                const int gi = e >> 7, c = e & 127;
-                float m = red[(gi * 8) * 128 + c];
-#pragma unroll
-                for (int w = 1; w < 8; w++) m = fmaxf(m, red[(gi * 8 + w) * 128 + c]);
-                const bool inside = t0 + gi * 32 < L;           // groups past the document end: 127
-                const int X = inside ? e8m0_exponent(m, p.mx_rule) : 0;
-                xs[e] = X;
-                sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X + 127);
-            }
-            __syncthreads();
-#pragma unroll
+#pragma unroll 1
             for (int gi = 0; gi < 4; gi++) {
                 const int row = gi * 32 + warp * 4 + rw;
                 if (t0 + row < L) {
+                    float y[EPL];
+                    smem_row<EPL, ELT>(tile, row, sl, y);
                     uint32_t w4[EPL / 4];
 #pragma unroll
                     for (int i = 0; i < EPL / 4; i++) {
                         const int c = sl * EPL + 4 * i;
                         const int4 x4 = *reinterpret_cast<const int4*>(xs + gi * 128 + c);
-                        w4[i] = pack_e4m3x4(__fmul_rn(y[gi][4 * i], pow2_neg(x4.x)),
-                                            __fmul_rn(y[gi][4 * i + 1], pow2_neg(x4.y)),
-                                            __fmul_rn(y[gi][4 * i + 2], pow2_neg(x4.z)),
-                                            __fmul_rn(y[gi][4 * i + 3], pow2_neg(x4.w)));
+                        w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(x4.x)),
+                                            __fmul_rn(y[4 * i + 1], pow2_neg(x4.y)),
+                                            __fmul_rn(y[4 * i + 2], pow2_neg(x4.z)),
+                                            __fmul_rn(y[4 * i + 3], pow2_neg(x4.w)));
                     }
-                    *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    if constexpr (EPL == 16) {
+                        *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    } else {
+                        *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
+                            make_uint2(w4[0], w4[1]);
+                    }
                 }
             }
         }
