@@ -169,6 +169,9 @@ def gpu_arm(args, rank, world, local_rank):
     mx = w.mx
     seed = w.hadamard_seed
     rot = not args.no_rotate
+    exact = bool(args.exact)
+    if exact and (mx or not causal):
+        raise SystemExit("--exact needs a causal E4M3 workload")
     flops = workloads.attention_flops(cu_np, H, d, causal)
     in_dt = torch.float32 if w.in_dtype == "f32" else torch.bfloat16
 
@@ -180,7 +183,7 @@ def gpu_arm(args, rank, world, local_rank):
         lq, lk, lv, blk = ROW, ROW, COL, 32
     else:
         lq = lk = lv = E4M3
-        blk = w.block
+        blk = 1 if args.exact else w.block
     Q = pa.empty_qtensor(T, H, d, nd, lq, blk, device=dev)
     K = pa.empty_qtensor(T, H, d, nd, lk, blk, device=dev)
     V = pa.empty_qtensor(T, H, d, nd, lv, blk, device=dev)
@@ -202,7 +205,7 @@ def gpu_arm(args, rank, world, local_rank):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws, out=o, lse=lse, stream=stream)
+        pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0, ws=ws, out=o, lse=lse, stream=stream)
         if record:
             e1.record(stream)
             attn_ev.append((e0, e1))
@@ -280,7 +283,7 @@ def gpu_arm(args, rank, world, local_rank):
             pa.attn_quantize(qi, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
             pa.attn_quantize(ki, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
             pa.attn_quantize(vi, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
-            pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws, out=oi, lse=li, stream=stream)
+            pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0, ws=ws, out=oi, lse=li, stream=stream)
             comp_done[b].record(stream)
             used[b] = True
             d2h_s.wait_event(comp_done[b])
@@ -367,10 +370,11 @@ def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
             K = oracle.quantize_tensor(k, c1, ROW, 32, not args.no_rotate, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, COL, 32, False, 0)
         else:
-            Q = oracle.quantize_tensor(q, c1, E4M3, w.block, not args.no_rotate, w.hadamard_seed)
-            K = oracle.quantize_tensor(k, c1, E4M3, w.block, not args.no_rotate, w.hadamard_seed)
-            V = oracle.quantize_tensor(v, c1, E4M3, w.block, False, 0)
-        oracle.attention_emulate(Q, K, V, c1, w.causal, False, None, rows=row_idx)
+            b = 1 if args.exact else w.block
+            Q = oracle.quantize_tensor(q, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
+            K = oracle.quantize_tensor(k, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
+            V = oracle.quantize_tensor(v, c1, E4M3, b, False, 0)
+        oracle.attention_emulate(Q, K, V, c1, w.causal, bool(args.exact), None, rows=row_idx)
         t_total += time.perf_counter() - t0
         nkeys = np.arange(1, R + 1) if w.causal else np.full(R, L0)
         flops += float(4.0 * d * nkeys.sum())
@@ -409,7 +413,9 @@ def reference_arm(args, rank, world):
 def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
-            "causal": w.causal, "quant": ("MXFP8 (E8M0 per 32)" if w.mx else f"E4M3 blocks of {w.block} tokens") +
+            "causal": w.causal, "causal_exact": bool(args.exact),
+            "quant": ("MXFP8 (E8M0 per 32)" if w.mx else
+                      ("E4M3 one scale per token (causal-exact)" if args.exact else f"E4M3 blocks of {w.block} tokens")) +
             (" + Hadamard rotation of Q, K" if not args.no_rotate else ", no rotation"), "input_dtype": w.in_dtype,
             "l2": "inputs larger than L2 (bf16 Q, K, V and their codes each exceed 129 MB)" if (
                 args.heads is None and args.seqlen is None) else "reduced size"}
@@ -428,6 +434,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
+    ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -395,7 +395,8 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 /*   masked keys (causal t > i, keys past the document end): s' = -inf        */
 /*   m'    = max(m, max_t s'_t); alpha = fl32(2^(m - m'))                     */
 /*   pt_t  = 2^(s'_t - m' + 8)              (probabilities prescaled by 2^8)  */
-/*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = V block scale / reference   */
+/*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = fl32(V block scale x        */
+/*                                          fl32(1 / reference))              */
 /*                                          (E4M3 layouts), 1 (MX layouts)    */
 /*   l     = fl32(alpha l + fl32(sum_t pt_t))                                 */
 /*   O_c   = fl32(alpha O_c + fl32(sum_t Phat_t vhat_tc))                     */
@@ -488,6 +489,7 @@ static void emu_unit(void* vc, long ri) {
         for (int b = 0; b <= last; b++) if (vs_row[b] > mxv) mxv = vs_row[b];
         ref = mxv;
     }
+    const float inv_ref = ref > 0.0f ? 1.0f / ref : 0.0f;   /* rounded once per row */
 
     float m = -INFINITY, l = 0.0f;
     float O[256];
@@ -532,7 +534,7 @@ static void emu_unit(void* vc, long ri) {
             double r = 1.0;
             if (!vmx) {
                 float sv = vs_row[(k0 + a) / vb];
-                r = (sv > 0.0f && ref > 0.0f) ? (double)(sv / ref) : 1.0;
+                r = (sv > 0.0f && ref > 0.0f) ? (double)(sv * inv_ref) : 1.0;
             }
             float pr = (float)(pt * r);
             ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[or_e4m3_encode(pr)] : (double)pr;

@@ -223,14 +223,15 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                                 d.start + 128 * w.qtile);
             }
             float t_c = 0.0f, t_lr = 0.0f, t_ir = 1.0f;   // this lane's tile of the current group of 32
+            const float inv_ref = ref > 0.0f ? __fdiv_rn(1.0f, ref) : 0.0f;
             for (int j = 0; j < w.ntiles; j++, g++) {
                 if constexpr (MODE == MODE_E4M3_TILE) {
                     if ((j & 31) == 0 && j + lane < w.ntiles) {
-                        // the tile's folded score multiplier and V ratio r = s_v / ref
+                        // the tile's folded score multiplier and V ratio r = s_v x (1 / ref)
                         const int jt = j + lane;
                         const float ks = p.sk[w.head * p.capk + d.boff_k + (128 * jt) / p.bk];
                         const float sv = p.sv[w.head * p.capv + d.boff_v + (128 * jt) / p.bv];
-                        const float rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                        const float rj = (sv > 0.0f && ref > 0.0f) ? __fmul_rn(sv, inv_ref) : 1.0f;
                         t_c = qs * ks * p.C;
                         t_lr = __log2f(rj);
                         t_ir = __fdiv_rn(1.0f, rj);
@@ -428,6 +429,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
             }
             if constexpr (MODE == MODE_E4M3_TILE) ref = p.vref[(long long)h * p.nd + w.doc];
+            const float inv_ref = ref > 0.0f ? __fdiv_rn(1.0f, ref) : 0.0f;   // V ratios: s_v x (1 / ref)
             float m = -INFINITY, l = 0.0f;
             for (int j = 0; j < nt; j++) {
                 const uint32_t gj = g + j;
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                             rs4[u] += e[u];
                             const int kl = (k0 + t + u) < L ? k0 + t + u : L - 1;
                             const float sv = p.sv[h * p.capv + d.boff_v + kl / p.bv];
-                            const float rt = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+                            const float rt = (sv > 0.0f && ref > 0.0f) ? __fmul_rn(sv, inv_ref) : 1.0f;
                             e[u] = e[u] * rt;
                         }
                         pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
@@ -688,7 +690,12 @@ struct PairCfgT {
     // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
     static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
-    static constexpr int OFF_BAR = OFF_SF + SF_BYTES;
+    // E4M3 per-column scales (blocks shorter than a tile, causal-exact): each key's K
+    // and V scale of key tile g, staged per stage: float [NS][2][128]
+    static constexpr bool COLS = MODE == MODE_E4M3_COL;
+    static constexpr int OFF_KSC = OFF_SF + SF_BYTES;
+    static constexpr int KSC_BYTES = COLS ? NS * 1024 : 0;
+    static constexpr int OFF_BAR = OFF_KSC + KSC_BYTES;
     static constexpr int SMEM = OFF_BAR + 1024 + 1024;
     static constexpr int THREADS = 352;
     static constexpr uint32_t T_O = 256;              // O_q at T_O + 128 q
@@ -710,6 +717,7 @@ struct PairBars {
     uint64_t p_full[2][2], pv_done[2][2];   // per query tile and P buffer
     uint64_t k_full[8], v_full[8], k_empty[8], v_empty[8];
     uint64_t drain[2];
+    uint64_t ksc_full[8], ksc_empty[8];   // per-column mode: key scales of a stage written / read
     uint32_t tmem_base;
     int abort;
 };
@@ -748,6 +756,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         }
         mbar_init(&B->drain[0], 1);
         mbar_init(&B->drain[1], 1);
+        for (int i = 0; i < PC::NS; i++) {
+            mbar_init(&B->ksc_full[i], 32);    // every producer lane, after its stores
+            mbar_init(&B->ksc_empty[i], 256);  // every softmax thread of both query tiles
+        }
         B->abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmq);
@@ -836,6 +848,25 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     if constexpr (PC::MX)
                         bulk_load(sm + PC::OFF_SF + 1536 + PC::NS * 512 + st * 512,
                                   p.mv + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->v_full[st]);
+                }
+                if constexpr (PC::COLS) {
+                    // each key's K and V scale of this tile (keys past the document end
+                    // repeat the last one; they are masked anyway), four keys per lane
+                    if (!__all_sync(FULL, mbar_wait(&B->ksc_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
+                        ok = false;
+                        break;
+                    }
+                    float* ksc = reinterpret_cast<float*>(sm + PC::OFF_KSC + st * 1024);
+                    float kv[4], vv[4];
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const int kl = min(128 * j + 4 * lane + u, d.len - 1);
+                        kv[u] = p.sk[w.head * p.capk + d.boff_k + kl / p.bk];
+                        vv[u] = p.sv[w.head * p.capv + d.boff_v + kl / p.bv];
+                    }
+                    *reinterpret_cast<float4*>(ksc + 4 * lane) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    *reinterpret_cast<float4*>(ksc + 128 + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                    mbar_arrive(&B->ksc_full[st]);
                 }
             }
         }
@@ -986,6 +1017,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
             }
+            const float inv_ref = ref > 0.0f ? __fdiv_rn(1.0f, ref) : 0.0f;   // V ratios: s_v x (1 / ref)
             float m = -INFINITY, l = 0.0f;
             // E4M3 tile mode: the key tiles' multipliers {K scale x C, log2 r, 1 / r}, one
             // tile ahead of use (written by the V-reference pass before this launch)
@@ -1025,12 +1057,20 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(&B->s_empty[q]);
                 const int k0 = 128 * j;                              // first key position of the tile
-                if constexpr (MODE == MODE_E4M3_COL) {
+                const float* ksc = reinterpret_cast<const float*>(sm + PC::OFF_KSC + (gj % PC::NS) * 1024);
+                if constexpr (PC::COLS) {
+                    if (!__all_sync(FULL, mbar_wait(&B->ksc_full[gj % PC::NS], (gj / PC::NS) & 1, abort, lim))) {
+                        ok = false;
+                        break;
+                    }
                     const float qc = qs * p.C;
-#pragma unroll 8
-                    for (int t = 0; t < 128; t++) {
-                        const int kl = (k0 + t) < L ? k0 + t : L - 1;
-                        s[t] = s[t] * (p.sk[h * p.capk + d.boff_k + kl / p.bk] * qc);
+#pragma unroll
+                    for (int t = 0; t < 128; t += 4) {
+                        const float4 k4 = *reinterpret_cast<const float4*>(ksc + t);
+                        s[t] = s[t] * (k4.x * qc);
+                        s[t + 1] = s[t + 1] * (k4.y * qc);
+                        s[t + 2] = s[t + 2] * (k4.z * qc);
+                        s[t + 3] = s[t + 3] * (k4.w * qc);
                     }
                     c = 1.0f;
                 }
@@ -1083,22 +1123,37 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
                     rowsum = a.x + a.y;
                 } else {
-                    float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-                    for (int t = 0; t < 128; t += 4) {
-                        float e[4];
+                    // p = 2^(s' + bias), row sum of the unquantised p, then each key's V
+                    // ratio r = s_v x (1 / ref) (1 where the key's V scale is 0) folded in
+                    const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
+                    const float2 ir2 = make_float2(inv_ref, inv_ref);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
 #pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            e[u] = ex2(fmaf(s[t + u], c, bias));
-                            rs4[u] += e[u];
-                            const int kl = (k0 + t + u) < L ? k0 + t + u : L - 1;
-                            const float sv = p.sv[h * p.capv + d.boff_v + kl / p.bv];
-                            const float rt = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
-                            e[u] = e[u] * rt;
+                    for (int t = 0; t < 128; t += 8) {
+                        const float4 va = *reinterpret_cast<const float4*>(ksc + 128 + t);
+                        const float4 vb = *reinterpret_cast<const float4*>(ksc + 128 + t + 4);
+                        const float sv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                        float e[8];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            const float2 xx = __ffma2_rn(make_float2(s[t + u], s[t + u + 1]), c2, b2);
+                            const float2 ee = make_float2(ex2(xx.x), ex2(xx.y));
+                            acc[u >> 1] = __fadd2_rn(acc[u >> 1], ee);
+                            const float2 r2 = __fmul2_rn(make_float2(sv[u], sv[u + 1]), ir2);
+                            const float2 rt = make_float2(sv[u] > 0.0f && ref > 0.0f ? r2.x : 1.0f,
+                                                          sv[u + 1] > 0.0f && ref > 0.0f ? r2.y : 1.0f);
+                            const float2 pr = __fmul2_rn(ee, rt);
+                            e[u] = pr.x;
+                            e[u + 1] = pr.y;
                         }
                         pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
+                        pk[t / 4 + 1] = pack_e4m3x4(e[4], e[5], e[6], e[7]);
                     }
-                    rowsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                    const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                    rowsum = a.x + a.y;
+                    tc_fence_before();
+                    mbar_arrive(&B->ksc_empty[gj % PC::NS]);
                 }
                 l = alpha * l + rowsum * invr;
                 m = m_new;

@@ -43,7 +43,7 @@ struct VrefParams {
     float* vref;
     int H, nd, T, exact, bv;
     // per (head, 128-token key tile) multipliers, written when tiles != 0:
-    // {K scale x C, log2 r, 1 / r, 0} with r = V scale / ref
+    // {K scale x C, log2 r, 1 / r, 0} with r = V scale x (1 / ref)
     int tiles, bk;
     const float* sk;
     long long sk_cap;

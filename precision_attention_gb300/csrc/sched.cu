@@ -198,11 +198,12 @@ __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
         __syncthreads();
         // each key tile's score multiplier and V ratio (one scale per 128-token tile)
         const float ref = carry;
+        const float inv_ref = ref > 0.0f ? __fdiv_rn(1.0f, ref) : 0.0f;   // rounded once per document
         const int nt = (d.len + 127) / 128;
         for (int j = threadIdx.x; j < nt; j += 256) {
             const float ks = p.sk[(long long)h * p.sk_cap + d.boff_k + (128 * j) / p.bk];
             const float sv = s[(128 * j) / p.bv];
-            const float rj = (sv > 0.0f && ref > 0.0f) ? __fdiv_rn(sv, ref) : 1.0f;
+            const float rj = (sv > 0.0f && ref > 0.0f) ? __fmul_rn(sv, inv_ref) : 1.0f;
             p.tsc[(long long)h * p.tsc_cap + d.toff + j] = make_float4(ks * p.C, __log2f(rj), __fdiv_rn(1.0f, rj), 0.0f);
         }
         return;

@@ -32,8 +32,10 @@ def sample_rows(cu, T, seed, n_random=384):
     return np.unique(np.asarray(rows, dtype=np.int32))
 
 
-@pytest.mark.parametrize("wid", [2, 3, 4, 5])
-def test_full_size_codes_and_sampled_rows(oracle_mod, wid):
+@pytest.mark.parametrize("wid,exact", [(2, False), (3, False), (3, True), (4, False), (5, False)])
+def test_full_size_codes_and_sampled_rows(oracle_mod, wid, exact):
+    """exact: the causal configuration's causal-exact mode (one E4M3 scale per
+    token, V ratios against the running maximum of earlier tokens' scales)."""
     w = workloads.WORKLOADS[wid]
     inp = workloads.make(wid)
     T, H, d = inp.q.shape
@@ -45,11 +47,11 @@ def test_full_size_codes_and_sampled_rows(oracle_mod, wid):
         lq, lk, lv, blk = ROW, ROW, COL, 32
     else:
         lq = lk = lv = E4M3
-        blk = w.block
+        blk = 1 if exact else w.block
     Q = pa.attn_quantize(q, cu_d, lq, blk, True, seed, ws=ws)
     K = pa.attn_quantize(k, cu_d, lk, blk, True, seed, ws=ws)
     V = pa.attn_quantize(v, cu_d, lv, blk, False, 0, ws=ws)
-    o, lse = pa.attn_fp8_fwd(Q, K, V, cu_d, w.causal, False, 0.0, ws=ws)
+    o, lse = pa.attn_fp8_fwd(Q, K, V, cu_d, w.causal, exact, 0.0, ws=ws)
     st, flags = pa.attn_read_device_status(ws)
     assert st == 0, (st, flags)
 
@@ -69,7 +71,7 @@ def test_full_size_codes_and_sampled_rows(oracle_mod, wid):
             assert np.array_equal(mx_row_tiles_to_logical(gs, cu, T, H), c.scales), f"{name} scales"
 
     rows = sample_rows(cu, T, seed=wid)
-    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, False, None, rows=rows, ties=True)
+    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, exact, None, rows=rows, ties=True)
     res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
-    print(f"workload {wid}: {len(rows)} rows x {H} heads:", res)
+    print(f"workload {wid}{' exact' if exact else ''}: {len(rows)} rows x {H} heads:", res)
     assert res["ok"], res
