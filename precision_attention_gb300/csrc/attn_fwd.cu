@@ -1040,19 +1040,11 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 tc_fence_after();
                 float s[128];
                 {
-                    uint32_t u0[32], u1[32], u2[32], u3[32];
-                    tmem_ld32(tS, u0);
-                    tmem_ld32(tS + 32, u1);
-                    tmem_ld32(tS + 64, u2);
-                    tmem_ld32(tS + 96, u3);
+                    uint32_t u[128];
+                    tmem_ld128(tS, u);   // the whole row in one load
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        s[i] = __uint_as_float(u0[i]);
-                        s[32 + i] = __uint_as_float(u1[i]);
-                        s[64 + i] = __uint_as_float(u2[i]);
-                        s[96 + i] = __uint_as_float(u3[i]);
-                    }
+                    for (int i = 0; i < 128; i++) s[i] = __uint_as_float(u[i]);
                 }
                 tc_fence_before();
                 mbar_arrive(&B->s_empty[q]);
