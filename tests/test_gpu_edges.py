@@ -1,0 +1,72 @@
+"""GPU edge cases of the forward: empty documents inside the packed batch (at
+its start, middle and end), all-zero inputs (every block maximum 0: scale 0,
+zero codes, every score 0) against the closed form, and a single head."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_helpers import compare_outputs
+from test_gpu_attention import run_emu, run_gpu
+
+pa = pytest.importorskip("precision_attention_gb300")
+
+pytestmark = pytest.mark.gpu
+
+EMPTY_DOCS = [0, 150, 0, 0, 257, 1, 0]
+
+
+@pytest.mark.parametrize("wid,mx,block,causal", [
+    (1, False, 64, True),      # d = 64, one-tile kernel
+    (2, False, 128, False),    # E4M3 tile scales
+    (3, False, 32, True),      # E4M3 per-column scales
+    (4, True, 32, False),      # MXFP8
+    (5, True, 32, True),
+])
+def test_zero_length_documents(oracle_mod, wid, mx, block, causal):
+    inp = workloads.make(wid, heads=2, lengths=EMPTY_DOCS)
+    o, lse = run_gpu(inp, mx, block, causal)
+    _, ob, le, amb = run_emu(inp, mx, block, causal)
+    res = compare_outputs(o, lse, ob, le, ties=amb)
+    assert res["ok"], res
+
+
+def visible_keys(cu, causal):
+    """Keys each row sees: its document's length, or its position + 1 (causal)."""
+    n = []
+    for a, b in zip(cu[:-1], cu[1:]):
+        L = int(b - a)
+        n.append(np.arange(1, L + 1) if causal else np.full(L, L))
+    return np.concatenate(n).astype(np.float64)
+
+
+@pytest.mark.parametrize("wid,mx,block,causal", [
+    (1, False, 64, False),
+    (2, False, 128, False),
+    (3, False, 128, True),
+    (3, False, 1, True),       # one scale per token (causal-exact layout)
+    (4, True, 32, False),
+    (5, True, 32, True),
+])
+def test_all_zero_inputs_closed_form(wid, mx, block, causal):
+    """Q = K = V = 0: every score is 0, so each row's probabilities are uniform
+    over the keys it sees, O = 0 exactly and lse = ln(number of visible keys)."""
+    inp = workloads.make(wid, heads=2, lengths=[200, 77, 129])
+    inp.q[:] = 0.0
+    inp.k[:] = 0.0
+    inp.v[:] = 0.0
+    o, lse = run_gpu(inp, mx, block, causal, exact=(block == 1))
+    assert int(torch.count_nonzero(o.float())) == 0
+    want = np.log(visible_keys(inp.cu_seqlens, causal))
+    got = lse.double().cpu().numpy()
+    assert got.shape == (2, inp.T)
+    assert np.abs(got - want[None, :]).max() <= 1e-5 * np.maximum(1.0, want).max()
+
+
+@pytest.mark.parametrize("wid,mx,block,causal", [(2, False, 128, False), (3, False, 128, True), (5, True, 32, True)])
+def test_single_head(oracle_mod, wid, mx, block, causal):
+    inp = workloads.make(wid, heads=1, lengths=[300, 77])
+    o, lse = run_gpu(inp, mx, block, causal)
+    _, ob, le, amb = run_emu(inp, mx, block, causal)
+    res = compare_outputs(o, lse, ob, le, ties=amb)
+    assert res["ok"], res

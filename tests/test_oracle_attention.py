@@ -256,3 +256,25 @@ def test_trend_block_rotation_beats_per_tensor(oracle_mod):
     rb = np.sqrt(np.mean((ob - o1) ** 2))
     rt = np.sqrt(np.mean((ot - o1) ** 2))
     assert rb < rt, (rb, rt)
+
+
+@pytest.mark.parametrize("mx,block,causal,exact", [(False, 128, False, False), (False, 128, True, False),
+                                                   (False, 1, True, True), (True, 32, False, False),
+                                                   (True, 32, True, False)])
+def test_emulation_all_zero_inputs_closed_form(oracle_mod, mx, block, causal, exact):
+    """Q = K = V = 0 with empty documents in the batch: every block maximum is 0
+    (scale 0, zero codes), every score is 0, so each row is uniform over the keys
+    it sees: O = 0 and lse = ln(number of visible keys)."""
+    inp = workloads.make(4 if mx else 2, heads=2, lengths=[0, 200, 0, 77, 1])
+    inp.q[:] = 0.0
+    inp.k[:] = 0.0
+    inp.v[:] = 0.0
+    cu = inp.cu_seqlens
+    Q, K, V = quant3(oracle_mod, inp, mx, block)
+    assert not Q.codes.any() and not K.codes.any() and not V.codes.any()
+    o3, _, l3 = oracle_mod.attention_emulate(Q, K, V, cu, causal, exact, None)
+    assert not np.any(o3)
+    n = np.concatenate([np.arange(1, b - a + 1) if causal else np.full(b - a, b - a)
+                        for a, b in zip(cu[:-1], cu[1:])]).astype(np.float64)
+    # the emulation forms lse in fp32 as the kernels do: a few fp32 ulps of ln n
+    assert np.abs(l3 - np.log(n)[None, :]).max() < 2e-6
