@@ -1055,16 +1055,19 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const float qc = qs * p.C;
+                    // each key's K scale here; the row's factor q_scale x C enters with
+                    // the exponent's FFMA (and the row maximum) below
 #pragma unroll
                     for (int t = 0; t < 128; t += 4) {
                         const float4 k4 = *reinterpret_cast<const float4*>(ksc + t);
-                        s[t] = s[t] * (k4.x * qc);
-                        s[t + 1] = s[t + 1] * (k4.y * qc);
-                        s[t + 2] = s[t + 2] * (k4.z * qc);
-                        s[t + 3] = s[t + 3] * (k4.w * qc);
+                        const float2 a = __fmul2_rn(make_float2(s[t], s[t + 1]), make_float2(k4.x, k4.y));
+                        const float2 b = __fmul2_rn(make_float2(s[t + 2], s[t + 3]), make_float2(k4.z, k4.w));
+                        s[t] = a.x;
+                        s[t + 1] = a.y;
+                        s[t + 2] = b.x;
+                        s[t + 3] = b.y;
                     }
-                    c = 1.0f;
+                    c = qs * p.C;
                 }
                 // causal: key tiles past the query tile are fully masked (the pair's
                 // first tile visits one key tile more than it needs), the diagonal
@@ -1116,7 +1119,8 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     rowsum = a.x + a.y;
                 } else {
                     // p = 2^(s' + bias), row sum of the unquantised p, then each key's V
-                    // ratio r = s_v x (1 / ref) (1 where the key's V scale is 0) folded in
+                    // ratio r = s_v x (1 / ref) folded in. A key whose V scale is 0 has
+                    // all-zero V codes, so its ratio (0 here) changes no output.
                     const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
                     const float2 ir2 = make_float2(inv_ref, inv_ref);
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -1132,10 +1136,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                             const float2 xx = __ffma2_rn(make_float2(s[t + u], s[t + u + 1]), c2, b2);
                             const float2 ee = make_float2(ex2(xx.x), ex2(xx.y));
                             acc[u >> 1] = __fadd2_rn(acc[u >> 1], ee);
-                            const float2 r2 = __fmul2_rn(make_float2(sv[u], sv[u + 1]), ir2);
-                            const float2 rt = make_float2(sv[u] > 0.0f && ref > 0.0f ? r2.x : 1.0f,
-                                                          sv[u + 1] > 0.0f && ref > 0.0f ? r2.y : 1.0f);
-                            const float2 pr = __fmul2_rn(ee, rt);
+                            const float2 pr = __fmul2_rn(ee, __fmul2_rn(make_float2(sv[u], sv[u + 1]), ir2));
                             e[u] = pr.x;
                             e[u + 1] = pr.y;
                         }
