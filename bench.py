@@ -473,9 +473,11 @@ def main():
             "vs_baseline": None, "dtype": "e4m3" if not w.mx else "mxfp8 (e4m3 + e8m0)", "data": "synthetic",
             "config": config_of(args, w),
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": 6 * args.steps,
+            # per step: three quantiser launches, the work list, (E4M3 only) the V
+            # references, the attention kernel
+            "gpu_launches": (5 if w.mx else 6) * args.steps,
             "roofline": {"bound": "tensor",
-                         "kernel": ("attn_fwd_kernel" if (w.mx or r["d"] != 128) else "attn_pair_kernel")
+                         "kernel": ("attn_pair_kernel" if r["d"] == 128 else "attn_fwd_kernel")
                          + " (FP8 forward call)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
                          "peak_basis": peak_basis + " (of measured)"},
