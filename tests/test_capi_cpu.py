@@ -75,6 +75,34 @@ def test_invalid_arguments_rejected_on_host(pa):
     assert L.attn_read_device_status(None, None, None) == pa.ATTN_ERR_WORKSPACE
 
 
+def test_shape_rules_on_host(pa):
+    """The shape checks every call starts with, through the two size queries (pure
+    host functions: there cu_seqlens is only tested for presence, never read)."""
+    L = pa.lib()
+    cb, sb, wb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    placeholder_cu = 1 << 20
+
+    def sizes(shape, layout=0, block=128):
+        return L.attn_quantize_sizes(ctypes.byref(shape), layout, block, ctypes.byref(cb), ctypes.byref(sb))
+
+    def ws(shape):
+        return L.attn_workspace_size(ctypes.byref(shape), ctypes.byref(wb))
+
+    for T, H, nd, cu in [(0, 2, 1, None), (100, 0, 1, None), (100, 2, 0, None),   # empty shapes
+                         (5, 2, 6, placeholder_cu)]:                              # more documents than tokens
+        shape = pa._Shape(T, H, 128, nd, cu)
+        assert sizes(shape) == pa.ATTN_ERR_INVALID_ARG and ws(shape) == pa.ATTN_ERR_INVALID_ARG
+    assert sizes(pa._Shape(5000, 2, 128, 1025, placeholder_cu)) == pa.ATTN_ERR_UNSUPPORTED   # > 1024 documents
+    assert sizes(pa._Shape(1 << 26, 64, 128, 1, None)) == pa.ATTN_ERR_UNSUPPORTED          # T x H beyond int32
+    assert sizes(pa._Shape(1024, 2, 128, 1024, placeholder_cu)) == pa.ATTN_OK              # one token per document
+    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=3, block=32) == pa.ATTN_ERR_INVALID_ARG
+    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=1, block=64) == pa.ATTN_OK   # block: E4M3 layout only
+    shape = pa._Shape(100, 2, 128, 1, None)
+    assert L.attn_quantize_sizes(ctypes.byref(shape), 0, 128, None, None) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_workspace_size(ctypes.byref(shape), None) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_workspace_size(None, ctypes.byref(wb)) == pa.ATTN_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
                     reason="uses placeholder device pointers; only run where no GPU could be reached")
 def test_seed_mismatch_and_layout_rules_on_host(pa):
