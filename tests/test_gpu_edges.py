@@ -70,3 +70,15 @@ def test_single_head(oracle_mod, wid, mx, block, causal):
     _, ob, le, amb = run_emu(inp, mx, block, causal)
     res = compare_outputs(o, lse, ob, le, ties=amb)
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("wid,mx,block,causal", [(3, False, 128, True), (2, False, 32, False), (4, True, 32, False)])
+def test_maximum_document_count(oracle_mod, wid, mx, block, causal):
+    """1024 documents (the most one call takes): the quantiser's and the work
+    list's document tables at capacity, lengths 1 .. 40 drawn from a seed."""
+    lengths = np.random.default_rng(1024 + wid).integers(1, 41, size=1024).tolist()
+    inp = workloads.make(wid, heads=2, lengths=lengths)
+    o, lse = run_gpu(inp, mx, block, causal)
+    _, ob, le, amb = run_emu(inp, mx, block, causal)
+    res = compare_outputs(o, lse, ob, le, ties=amb)
+    assert res["ok"], res
