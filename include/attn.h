@@ -188,6 +188,15 @@ attn_status attn_fp8_fwd_noalloc(const attn_qtensor* q, const attn_qtensor* k, c
  * flags_out (host, may be NULL) receives the raw bit set (bit e = error e). */
 attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* flags_out);
 
+/* Limit, in SM clock cycles, of every bounded on-device wait of the attention
+ * calls made after this one (default about 2 s of SM clock; cycles <= 0
+ * restores it). When a wait runs out the kernel stops its work, lets the copies
+ * and MMAs already in flight finish, frees what it holds and returns; the call's
+ * status word then holds ATTN_ERR_DEVICE_TIMEOUT and O and lse are undefined.
+ * A short limit makes that path testable without a device fault. Process-wide;
+ * host only (never touches the device). Returns ATTN_OK. */
+attn_status attn_set_wait_limit(int64_t cycles);
+
 /* Static description of a status code. */
 const char* attn_status_string(int32_t status);
 

@@ -39,7 +39,8 @@ ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32 = 0, 1, 2
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
-           "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc")
+           "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
+           "attn_set_wait_limit")
 
 
 class AttnError(RuntimeError):
@@ -84,8 +85,9 @@ def lib() -> ctypes.CDLL:
             L.attn_status_string.argtypes = [i32]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_device_sm_count.argtypes = []
+            L.attn_set_wait_limit.argtypes = [i64]
             for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd",
-                      "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count"):
+                      "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count", "attn_set_wait_limit"):
                 getattr(L, f).restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -97,6 +99,12 @@ def attn_status_string(status: int) -> str:
 
 def attn_device_sm_count() -> int:
     return int(lib().attn_device_sm_count())
+
+
+def attn_set_wait_limit(cycles: int) -> None:
+    """Limit (SM cycles) of the attention kernels' bounded waits for later calls;
+    cycles <= 0 restores the default. A short limit exercises the timeout path."""
+    _check(lib().attn_set_wait_limit(int(cycles)), "attn_set_wait_limit")
 
 
 def _check(st: int, where: str):

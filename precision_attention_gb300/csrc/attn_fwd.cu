@@ -132,6 +132,11 @@ __device__ __forceinline__ constexpr uint64_t voff(int kk) {
     return C::SW128 ? (uint64_t)(kk * C::KPER * 128) >> 4 : (uint64_t)(kk * C::KPER * 64) >> 4;
 }
 
+// Limit of the end-of-kernel drains (copies and MMAs already in flight when a wait
+// gave up): those complete by themselves, so the drains keep this long limit
+// whatever the (possibly short) limit of the ordinary waits.
+constexpr long long kDrainLimit = 4000000000LL;
+
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
@@ -275,11 +280,11 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
             }
         }
         if (*abort && lane == 0) {   // let in-flight copies land before shared memory is released
-            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, lim);
+            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, kDrainLimit);
             for (int s2 = 0; s2 < C::NS; s2++)
                 if (issued[s2] >= 0) {
-                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], lim);
-                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], lim);
+                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], kDrainLimit);
+                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], kDrainLimit);
                 }
         }
         __syncwarp();
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
             }
             // every MMA this thread issued has completed before TMEM is released
             tc_commit(&B->drain);
-            wait_drain(&B->drain, 0, lim);
+            wait_drain(&B->drain, 0, kDrainLimit);
         }
         __syncwarp();
     } else {
@@ -871,11 +876,11 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             }
         }
         if (*abort && lane == 0) {   // let in-flight copies land before shared memory is released
-            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, lim);
+            if (q_issued >= 0) wait_drain(&B->q_full, (uint32_t)q_issued, kDrainLimit);
             for (int s2 = 0; s2 < PC::NS; s2++)
                 if (issued[s2] >= 0) {
-                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], lim);
-                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], lim);
+                    wait_drain(&B->k_full[s2], (uint32_t)issued[s2], kDrainLimit);
+                    wait_drain(&B->v_full[s2], (uint32_t)issued[s2], kDrainLimit);
                 }
         }
         __syncwarp();
@@ -984,7 +989,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             }
             // every MMA this thread issued has completed before TMEM is released
             tc_commit(&B->drain[q]);
-            wait_drain(&B->drain[q], 0, lim);
+            wait_drain(&B->drain[q], 0, kDrainLimit);
         }
         __syncwarp();
     } else {

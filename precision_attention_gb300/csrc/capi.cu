@@ -1,6 +1,7 @@
 // capi.cu -- the extern "C" boundary declared in include/attn.h: argument
 // validation, workspace layout and the kernel launches. No allocation, no
 // stream synchronisation (except attn_read_device_status, by definition).
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -14,6 +15,7 @@ using namespace pa;
 namespace {
 
 constexpr long long kWaitLimit = 4000000000LL;   // SM cycles (about 2 s) before a wait gives up
+std::atomic<long long> g_wait_limit{kWaitLimit};   // attn_set_wait_limit
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -175,7 +177,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     fp.exact = exact;
     const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt((double)d);
     fp.C = static_cast<float>(sc * 1.4426950408889634 / (rotated ? static_cast<double>(d) : 1.0));
-    fp.wait_limit = kWaitLimit;
+    fp.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     fp.bq = fp.bk = fp.bv = 1;
     if (e4m3) {
         fp.sq = static_cast<const float*>(qq->scales);
@@ -266,6 +268,11 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
     if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
     return forward(0, q, k, v, nullptr, nullptr, nullptr, shape, causal != 0, 0, softmax_scale, 0, o, lse,
                    workspace, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_set_wait_limit(int64_t cycles) {
+    g_wait_limit.store(cycles > 0 ? static_cast<long long>(cycles) : kWaitLimit, std::memory_order_relaxed);
+    return ATTN_OK;
 }
 
 attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* flags_out) {

@@ -75,6 +75,11 @@ def test_invalid_arguments_rejected_on_host(pa):
     assert L.attn_read_device_status(None, None, None) == pa.ATTN_ERR_WORKSPACE
 
 
+def test_wait_limit_setting_is_host_only(pa):
+    assert pa.lib().attn_set_wait_limit(1000) == pa.ATTN_OK
+    assert pa.lib().attn_set_wait_limit(0) == pa.ATTN_OK     # back to the default
+
+
 def test_shape_rules_on_host(pa):
     """The shape checks every call starts with, through the two size queries (pure
     host functions: there cu_seqlens is only tested for presence, never read)."""
