@@ -1,7 +1,10 @@
 """Failure detection on the GPU without a fault: with a bounded-wait limit far
 shorter than a tile's copy, the forward gives up, lets what is in flight
 finish, frees what it holds and reports ATTN_ERR_DEVICE_TIMEOUT in the status
-word; the context stays usable and the next call is correct."""
+word; the context stays usable and the next call is correct. (The quantiser
+waits only for its own tile copies, each of which lands within one
+mbarrier.try_wait, so no limit makes it time out; its wait is the same bounded
+loop.)"""
 import pytest
 
 import workloads
