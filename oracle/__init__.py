@@ -7,7 +7,8 @@ nothing with the CUDA library.
 
 The oracle has three parts (see ``attn_oracle.h`` for the page passages):
 
-* O-1 ``attention_fp64``: plain FP64 softmax attention.
+* O-1 ``attention_fp64``: plain FP64 softmax attention, and
+  ``attention_fp64_backward``: its gradients (dQ, dK, dV) for an upstream dO.
 * O-2 ``quantize``: the bit-level rotate-and-quantise emulator (E4M3 token
   blocks, MXFP8 row/column blocks with E8M0 exponents).
 * O-3 ``attention_emulate``: the running-softmax loop over the quantised
@@ -81,6 +82,7 @@ def lib():
             L.or_quantize.argtypes = [vp, i32, i32, i32, vp, i32, i32, i32, i32, u64, i32, vp, vp, vp]
             L.or_quantize.restype = i32
             L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
+            L.or_attention_fp64_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, vp, vp]
             L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
                 i32, i32, i32, vp, i32, i32, i32, i32, dbl, i32, vp, i32, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
@@ -255,6 +257,20 @@ def attention_fp64(q, k, v, cu_seqlens=None, causal=False, softmax_scale=None, r
     lib().or_attention_fp64(q.ctypes.data, k.ctypes.data, v.ctypes.data, T, H, d, _ptr(cu), nd,
                             int(bool(causal)), scale, _ptr(r), R, o.ctypes.data, lse.ctypes.data)
     return o, lse
+
+
+def attention_fp64_backward(q, k, v, dout, cu_seqlens=None, causal=False, softmax_scale=None):
+    """Gradients of the FP64 attention for an upstream gradient dout.
+    Returns (dq, dk, dv), each fp64 [T, H, d]."""
+    q, k, v, dout = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, dout))
+    T, H, d = q.shape
+    cu, nd = _cu(cu_seqlens, T)
+    scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    dq, dk, dv = (np.zeros((T, H, d), dtype=np.float64) for _ in range(3))
+    lib().or_attention_fp64_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, T, H, d,
+                                _ptr(cu), nd, int(bool(causal)), scale, dq.ctypes.data, dk.ctypes.data,
+                                dv.ctypes.data)
+    return dq, dk, dv
 
 
 # ---- O-3 -------------------------------------------------------------------

@@ -380,6 +380,84 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 }
 
 /* ------------------------------------------------------------------------- */
+/* O-1 backward: the gradients of the plain definition above for an upstream */
+/* gradient dO (the step after the forward; FLAMIA section 1 lists the       */
+/* backward among its kernels). With P = softmax(S) row-wise, S = scale Q K^T */
+/* (masked as in the forward) and O = P V:                                   */
+/*   dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij  (= dO_i . O_i);       */
+/*   dS = P o (dP - D);  dQ = scale dS K;  dK = scale dS^T Q.                  */
+/* One (document, head) per unit, so a thread owns that unit's dK, dV rows.  */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const double *q, *k, *v, *dout; int T, H, d; docs_t D; int causal; double scale;
+    double *dq, *dk, *dv;
+} bwd_ctx;
+
+static void bwd_unit(void* vc, long u) {
+    bwd_ctx* c = (bwd_ctx*)vc;
+    int doc = (int)(u / c->H), h = (int)(u % c->H), d = c->d, H = c->H;
+    int s0 = c->D.cu[doc], L = c->D.cu[doc + 1] - s0;
+    if (L <= 0) return;
+    double* p = (double*)malloc(sizeof(double) * L);
+    double* dp = (double*)malloc(sizeof(double) * L);
+    for (int j = 0; j < L; j++) {
+        double* dkr = c->dk + ((long)(s0 + j) * H + h) * d;
+        double* dvr = c->dv + ((long)(s0 + j) * H + h) * d;
+        for (int x = 0; x < d; x++) dkr[x] = dvr[x] = 0.0;
+    }
+    for (int i = 0; i < L; i++) {
+        int nk = c->causal ? i + 1 : L;
+        const double* qr = c->q + ((long)(s0 + i) * H + h) * d;
+        const double* gr = c->dout + ((long)(s0 + i) * H + h) * d;
+        double m = -INFINITY;
+        for (int j = 0; j < nk; j++) {
+            const double* kr = c->k + ((long)(s0 + j) * H + h) * d;
+            double acc = 0.0;
+            for (int x = 0; x < d; x++) acc += qr[x] * kr[x];
+            p[j] = c->scale * acc;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (int j = 0; j < nk; j++) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        double D = 0.0;
+        for (int j = 0; j < nk; j++) {
+            p[j] /= l;
+            const double* vr = c->v + ((long)(s0 + j) * H + h) * d;
+            double acc = 0.0;
+            for (int x = 0; x < d; x++) acc += gr[x] * vr[x];
+            dp[j] = acc;
+            D += p[j] * dp[j];
+        }
+        double* dqr = c->dq + ((long)(s0 + i) * H + h) * d;
+        for (int x = 0; x < d; x++) dqr[x] = 0.0;
+        for (int j = 0; j < nk; j++) {
+            const double ds = p[j] * (dp[j] - D);
+            const double* kr = c->k + ((long)(s0 + j) * H + h) * d;
+            double* dkr = c->dk + ((long)(s0 + j) * H + h) * d;
+            double* dvr = c->dv + ((long)(s0 + j) * H + h) * d;
+            for (int x = 0; x < d; x++) {
+                dqr[x] += c->scale * ds * kr[x];
+                dkr[x] += c->scale * ds * qr[x];
+                dvr[x] += p[j] * gr[x];
+            }
+        }
+    }
+    free(p);
+    free(dp);
+}
+
+void or_attention_fp64_bwd(const double* q, const double* k, const double* v, const double* dout, int T, int H,
+                           int d, const int32_t* cu, int nd, int causal, double scale, double* dq, double* dk,
+                           double* dv) {
+    bwd_ctx c = {q, k, v, dout, T, H, d, docs_make(cu, nd, T), causal, scale, dq, dk, dv};
+    parallel_for((long)c.D.nd * H, bwd_unit, &c);
+    free(c.D.cu);
+}
+
+/* ------------------------------------------------------------------------- */
 /* O-3: the running-softmax loop over quantised operands, the way the kernel */
 /* tiles it ("Fused attention kernel", Implementation sketch: running max m, */
 /* rescale alpha = exp(m_old - m_new) applied to the old output, every key   */

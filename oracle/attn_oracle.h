@@ -78,6 +78,13 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
                        const int32_t* cu_seqlens, int num_docs, int causal, double softmax_scale,
                        const int32_t* rows, int nrows, double* o, double* lse);
 
+/* ---- O-1 backward: dQ, dK, dV of the FP64 attention for an upstream dO ----
+ * All arrays [T][H][d] fp64; masking and documents as in or_attention_fp64.
+ */
+void or_attention_fp64_bwd(const double* q, const double* k, const double* v, const double* dout, int T, int H,
+                           int d, const int32_t* cu_seqlens, int num_docs, int causal, double softmax_scale,
+                           double* dq, double* dk, double* dv);
+
 /* ---- O-3 quantised-operand emulation ---- */
 typedef struct {
     const uint8_t* codes;       /* [T][H][d] */
