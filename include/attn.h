@@ -120,16 +120,34 @@ typedef struct {
 } attn_qtensor;
 
 /* Byte sizes of the code and scale buffers for one tensor of this shape.
- * Host-only; reads nothing on the device. */
+ * Host-only; reads nothing on the device.
+ * Source: "Fused attention kernel", 8-bit forward pass (one e4m3 code per
+ * element, one scale per block); FLAMIA section 2 (one E8M0 scale per 32
+ * elements). */
 attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t block,
                                 size_t* codes_bytes, size_t* scales_bytes);
 
 /* Workspace bytes that attn_quantize, attn_fp8_fwd and attn_bf16_fwd need for
- * this shape (one buffer serves all three; 256-byte aligned). Host-only. */
+ * this shape (one buffer serves all three; 256-byte aligned). Host-only.
+ * Source: FLAMIA appendix F (work lists and scales kept on the GPU, so the
+ * caller provides their memory once and no call allocates). */
 attn_status attn_workspace_size(const attn_shape* shape, size_t* bytes);
+
+/* The same size for a forward call of the given causality. The work list holds
+ * one entry per (document, head, query-tile unit) whether or not the call is
+ * causal, so `causal` does not change the result; it is accepted so that a
+ * caller sizes the workspace for exactly the call it makes. Host-only.
+ * Source: as attn_workspace_size. */
+attn_status attn_fwd_workspace_size(const attn_shape* shape, int32_t causal, size_t* bytes);
 
 /* Fused rotate-and-quantise, one kernel launch (each CTA builds the document
  * table it needs from cu_seqlens itself).
+ * Source: "Fused attention kernel", 8-bit forward pass (e4m3 codes, block
+ * quantisation, incoherent processing: a random sign diagonal times a
+ * Hadamard matrix applied to Q and K, cancelling in Q K^T); FLAMIA section 2
+ * (MX: 32-element blocks sharing one E8M0 scale), abstract and section 4.1
+ * (document-local scales of packed documents, no repacking), section 4.3
+ * (quantisation fused into one launch).
  * x: device, bf16 or fp32, element (t, h, c) at x[t * token_stride + h * head_stride + c]
  *    (strides in elements; channels contiguous; 16-byte aligned rows).
  * rotate != 0: codes of H_d * diag(s) * x, s_j = -1 if bit 63 of the j-th
@@ -143,6 +161,16 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
                           attn_qtensor* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* FP8 attention forward over quantised operands.
+ * Source: "Fused attention kernel", Implementation sketch (per key block:
+ * S = Q K^T, new row max, rescale of the old sum and output by
+ * exp(m_old - m_new), P V accumulation; one normalisation at the end and
+ * lse = m + log l) and 8-bit forward pass (e4m3 operands, FP32 accumulation);
+ * "FP8 attention that keeps FlashAttention-3 throughput at BF16-level
+ * accuracy", How it gets verified (E4M3 operands, FP32 softmax statistics,
+ * BF16 output, causal and non-causal); FLAMIA section 2 (block-scaled MMA),
+ * section 4.3 (score scales folded into one multiplier, longest-first causal
+ * work), sections 1 and 4.5 (exact scaling against causal leakage), section
+ * 4.1 (packed documents).
  * q, k: ATTN_E4M3_TOKBLOCK or ATTN_MX_ROW32 (both the same; both rotated with
  *    the same seed or both not -> else ATTN_ERR_SEED_MISMATCH).
  * v: ATTN_E4M3_TOKBLOCK (with E4M3 q, k) or ATTN_MX_COL32 (with MX q, k).
@@ -160,7 +188,11 @@ attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const att
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* BF16 attention forward: the same loop with bf16 q, k, v [T][H][d]
- * (contiguous), P in bf16, fp32 accumulation. Same o and lse as above. */
+ * (contiguous), P in bf16, fp32 accumulation. Same o and lse as above.
+ * Source: "FP8 attention that keeps FlashAttention-3 throughput at BF16-level
+ * accuracy", The problem and How it gets verified (the BF16 attention whose
+ * error the 8-bit path is measured against); "Fused attention kernel",
+ * Implementation sketch (the loop). */
 attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const attn_shape* shape,
                           int32_t causal, float softmax_scale, void* o, float* lse,
                           void* workspace, size_t workspace_bytes, void* stream);
@@ -177,15 +209,21 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
  * The first call on a device (with that device current) looks up the array's
  * address; make it before any stream capture. All calls share the array:
  * calls that overlap on the GPU race. Arguments and results are those of
- * attn_fp8_fwd; `status` (device, may be NULL) receives the call's device
- * status word (bit e = attn_status e), cleared at the start of the call. */
+ * attn_fp8_fwd, and so are its argument checks, made before the array or
+ * `status` is touched. `status` (device, may be NULL) receives the forward's
+ * device status word (bit e = attn_status e), cleared at the start of the
+ * call; it is written only when the call returns ATTN_OK. Errors that the
+ * quantiser found (a non-finite block) stay in the workspace given to
+ * attn_quantize, not here. */
 attn_status attn_fp8_fwd_noalloc(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
                                  const attn_shape* shape, int32_t causal, int32_t causal_exact,
                                  float softmax_scale, void* o, float* lse, uint32_t* status, void* stream);
 
 /* Synchronises `stream`, reads and clears the device status word in
  * `workspace`, and returns the first error it holds (ATTN_OK if none).
- * flags_out (host, may be NULL) receives the raw bit set (bit e = error e). */
+ * flags_out (host, may be NULL) receives the raw bit set (bit e = error e).
+ * Source: FLAMIA appendix F (no host synchronisation inside the calls: the
+ * errors found on the device wait in the workspace until the caller asks). */
 attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* flags_out);
 
 /* Limit, in SM clock cycles, of every bounded on-device wait of the attention
@@ -194,14 +232,15 @@ attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* fla
  * and MMAs already in flight finish, frees what it holds and returns; the call's
  * status word then holds ATTN_ERR_DEVICE_TIMEOUT and O and lse are undefined.
  * A short limit makes that path testable without a device fault. Process-wide;
- * host only (never touches the device). Returns ATTN_OK. */
+ * host only (never touches the device). Returns ATTN_OK. No counterpart on the
+ * pages: the bounded waits are this library's failure detection. */
 attn_status attn_set_wait_limit(int64_t cycles);
 
-/* Static description of a status code. */
+/* Static description of a status code (no counterpart on the pages). */
 const char* attn_status_string(int32_t status);
 
 /* Number of streaming multiprocessors the forward sizes its persistent grid
- * for on the current device, or -1 on error. */
+ * for on the current device, or -1 on error (no counterpart on the pages). */
 int32_t attn_device_sm_count(void);
 
 #ifdef __cplusplus

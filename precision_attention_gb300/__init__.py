@@ -7,7 +7,8 @@ missing or fails to load, every call raises.
 
 The functions keep the C names:
 
-    attn_quantize_sizes, attn_workspace_size, attn_quantize, attn_fp8_fwd,
+    attn_quantize_sizes, attn_workspace_size, attn_fwd_workspace_size,
+    attn_quantize, attn_fp8_fwd,
     attn_bf16_fwd, attn_read_device_status, attn_status_string,
     attn_device_sm_count
 """
@@ -38,7 +39,7 @@ ATTN_IN_F32, ATTN_IN_BF16 = 0, 1
 ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32 = 0, 1, 2
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 
-EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
+EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
            "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
            "attn_set_wait_limit")
 
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
             S, Q = ctypes.POINTER(_Shape), ctypes.POINTER(_QT)
             L.attn_quantize_sizes.argtypes = [S, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
             L.attn_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
+            L.attn_fwd_workspace_size.argtypes = [S, i32, ctypes.POINTER(sz)]
             L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
             L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
             L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
@@ -86,7 +88,8 @@ def lib() -> ctypes.CDLL:
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_device_sm_count.argtypes = []
             L.attn_set_wait_limit.argtypes = [i64]
-            for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_quantize", "attn_fp8_fwd",
+            for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
+                      "attn_fp8_fwd",
                       "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count", "attn_set_wait_limit"):
                 getattr(L, f).restype = ctypes.c_int32
             _lib = L
@@ -136,6 +139,13 @@ def attn_workspace_size(T: int, H: int, d: int, num_docs: int) -> int:
     s = _Shape(T, H, d, num_docs, None if num_docs == 1 else 1)
     b = ctypes.c_size_t()
     _check(lib().attn_workspace_size(ctypes.byref(s), ctypes.byref(b)), "attn_workspace_size")
+    return b.value
+
+
+def attn_fwd_workspace_size(T: int, H: int, d: int, num_docs: int, causal: bool) -> int:
+    s = _Shape(T, H, d, num_docs, None if num_docs == 1 else 1)
+    b = ctypes.c_size_t()
+    _check(lib().attn_fwd_workspace_size(ctypes.byref(s), int(causal), ctypes.byref(b)), "attn_fwd_workspace_size")
     return b.value
 
 

@@ -50,6 +50,47 @@ attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATT
 
 }  // namespace
 
+namespace pa {
+
+// Every synchronous check of attn_fp8_fwd, in its order; the workspace is checked
+// only when check_workspace is set (the no-allocation entry point has none).
+// *mode receives the kernel mode (1 E4M3 one scale per tile, 2 E4M3 per-column
+// scales, 3 MX).
+attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                          const attn_shape* shape, int causal, int causal_exact, float softmax_scale, const void* o,
+                          const float* lse, bool check_workspace, void* workspace, size_t workspace_bytes,
+                          int* mode) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !lse || !mode) return ATTN_ERR_INVALID_ARG;
+    if (!q->codes || !k->codes || !v->codes || !q->scales || !k->scales || !v->scales) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q->codes) || !aligned16(k->codes) || !aligned16(v->codes) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(q->scales) || !aligned16(k->scales) || !aligned16(v->scales))
+        return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
+    if (check_workspace && (st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
+    const bool mx = q->layout == ATTN_MX_ROW32;
+    if (mx) {
+        if (k->layout != ATTN_MX_ROW32 || v->layout != ATTN_MX_COL32) return ATTN_ERR_INVALID_ARG;
+        if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+        if (causal_exact) return ATTN_ERR_UNSUPPORTED;
+    } else {
+        if (q->layout != ATTN_E4M3_TOKBLOCK || k->layout != ATTN_E4M3_TOKBLOCK || v->layout != ATTN_E4M3_TOKBLOCK)
+            return ATTN_ERR_INVALID_ARG;
+        if (!valid_block(0, q->block) || !valid_block(0, k->block) || !valid_block(0, v->block))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    if (v->rotated) return ATTN_ERR_INVALID_ARG;
+    if (q->rotated != k->rotated || (q->rotated && q->hadamard_seed != k->hadamard_seed))
+        return ATTN_ERR_SEED_MISMATCH;
+    if (causal_exact && (!causal || q->block != 1 || k->block != 1 || v->block != 1)) return ATTN_ERR_INVALID_ARG;
+    *mode = 3;
+    if (!mx) *mode = (q->block == 128 && k->block == 128 && v->block == 128 && !causal_exact) ? 1 : 2;
+    return ATTN_OK;
+}
+
+}  // namespace pa
+
 extern "C" {
 
 const char* attn_status_string(int32_t s) {
@@ -89,6 +130,11 @@ attn_status attn_workspace_size(const attn_shape* shape, size_t* bytes) {
     if (!bytes) return ATTN_ERR_INVALID_ARG;
     *bytes = ws_layout(shape->total_tokens, shape->heads, shape->num_docs).total;
     return ATTN_OK;
+}
+
+attn_status attn_fwd_workspace_size(const attn_shape* shape, int32_t causal, size_t* bytes) {
+    (void)causal;   // the work list holds one entry per query-tile unit either way
+    return attn_workspace_size(shape, bytes);
 }
 
 attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
@@ -226,32 +272,10 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
 attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
                          const attn_shape* shape, int32_t causal, int32_t causal_exact, float softmax_scale,
                          void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-    attn_status st = check_shape(shape);
+    int mode = 0;
+    attn_status st = pa::fp8_fwd_check(q, k, v, shape, causal, causal_exact, softmax_scale, o, lse, true, workspace,
+                                       workspace_bytes, &mode);
     if (st != ATTN_OK) return st;
-    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-    if (!q->codes || !k->codes || !v->codes || !q->scales || !k->scales || !v->scales) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q->codes) || !aligned16(k->codes) || !aligned16(v->codes) || !aligned16(o) || !aligned16(lse) ||
-        !aligned16(q->scales) || !aligned16(k->scales) || !aligned16(v->scales))
-        return ATTN_ERR_INVALID_ARG;
-    if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
-    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
-    const bool mx = q->layout == ATTN_MX_ROW32;
-    if (mx) {
-        if (k->layout != ATTN_MX_ROW32 || v->layout != ATTN_MX_COL32) return ATTN_ERR_INVALID_ARG;
-        if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-        if (causal_exact) return ATTN_ERR_UNSUPPORTED;
-    } else {
-        if (q->layout != ATTN_E4M3_TOKBLOCK || k->layout != ATTN_E4M3_TOKBLOCK || v->layout != ATTN_E4M3_TOKBLOCK)
-            return ATTN_ERR_INVALID_ARG;
-        if (!valid_block(0, q->block) || !valid_block(0, k->block) || !valid_block(0, v->block))
-            return ATTN_ERR_INVALID_ARG;
-    }
-    if (v->rotated) return ATTN_ERR_INVALID_ARG;
-    if (q->rotated != k->rotated || (q->rotated && q->hadamard_seed != k->hadamard_seed))
-        return ATTN_ERR_SEED_MISMATCH;
-    if (causal_exact && (!causal || q->block != 1 || k->block != 1 || v->block != 1)) return ATTN_ERR_INVALID_ARG;
-    int mode = 3;
-    if (!mx) mode = (q->block == 128 && k->block == 128 && v->block == 128 && !causal_exact) ? 1 : 2;
     return forward(mode, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
                    softmax_scale, q->rotated, o, lse, workspace, static_cast<cudaStream_t>(stream));
 }

@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
 __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
     __shared__ float wmax[8];
     __shared__ float carry;
-    if (p.hdr->status & ST_BAD_SEQLENS) return;
+    // this call's schedule: the work-list pass wrote no items when its cu_seqlens
+    // were malformed (the status word's bits may be older than this call)
+    if (p.hdr->n_items <= 0) return;
     const int h = blockIdx.x % p.H, doc = blockIdx.x / p.H;
     const DocEntry d = p.docs[doc];
     const float* s = p.sv + (long long)h * p.sv_cap + d.boff_v;

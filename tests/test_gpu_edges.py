@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_helpers import compare_outputs
+from gpu_helpers import compare_outputs, to_device
 from test_gpu_attention import run_emu, run_gpu
 
 pa = pytest.importorskip("precision_attention_gb300")
@@ -82,3 +82,32 @@ def test_maximum_document_count(oracle_mod, wid, mx, block, causal):
     _, ob, le, amb = run_emu(inp, mx, block, causal)
     res = compare_outputs(o, lse, ob, le, ties=amb)
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("block", [128, 1])
+def test_valid_forward_after_bad_seqlens_on_same_workspace(oracle_mod, block):
+    """A quantise call with malformed cu_seqlens leaves ATTN_ERR_BAD_SEQLENS in
+    the workspace's status word; a later, valid forward on the same workspace
+    (the status not read in between) must still compute its own schedule and V
+    references, and match the emulation."""
+    causal = block == 1
+    inp = workloads.make(3, heads=2, lengths=[300, 77, 129])
+    q, k, v, cu = to_device(inp)
+    T, H, d = q.shape
+    ws = pa.workspace(T, H, d, cu.numel() - 1)
+    bad = cu.clone()
+    bad[1], bad[2] = bad[2].clone(), bad[1].clone()            # offsets out of order
+    pa.attn_quantize(q, bad, pa.ATTN_E4M3_TOKBLOCK, block, True, 0x5EED0003, ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) & (1 << pa.ATTN_ERR_BAD_SEQLENS)
+    seed = 0x5EED0003
+    Q = pa.attn_quantize(q, cu, pa.ATTN_E4M3_TOKBLOCK, block, True, seed, ws=ws)
+    K = pa.attn_quantize(k, cu, pa.ATTN_E4M3_TOKBLOCK, block, True, seed, ws=ws)
+    V = pa.attn_quantize(v, cu, pa.ATTN_E4M3_TOKBLOCK, block, False, 0, ws=ws)
+    o, lse = pa.attn_fp8_fwd(Q, K, V, cu, causal, causal, 0.0, ws=ws)
+    torch.cuda.synchronize()
+    _, ob, le, amb = run_emu(inp, False, block, causal, exact=causal)
+    res = compare_outputs(o, lse, ob, le, ties=amb)
+    assert res["ok"], res
+    st, flags = pa.attn_read_device_status(ws)
+    assert st == pa.ATTN_ERR_BAD_SEQLENS and flags == (1 << pa.ATTN_ERR_BAD_SEQLENS)
