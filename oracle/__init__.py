@@ -29,7 +29,7 @@ _HDR = os.path.join(_HERE, "attn_oracle.h")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-E4M3_TOKBLOCK, MX_ROW32, MX_COL32 = 0, 1, 2
+E4M3_TOKBLOCK, MX_ROW32, MX_COL32, MX_TOKEN = 0, 1, 2, 3
 MX_RULE_NOSAT, MX_RULE_OCP_FLOOR = 0, 1
 QUANTIZE_P = 1
 
@@ -84,8 +84,11 @@ def lib():
             L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
             L.or_attention_fp64_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, vp, vp]
             L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
-                i32, i32, i32, vp, i32, i32, i32, i32, dbl, i32, vp, i32, vp, vp, vp, vp]
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
+            L.or_attention_emulate_given_p.argtypes = [ctypes.POINTER(_QT)] * 3 + [
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, vp, i32, vp, vp, vp, vp, ctypes.c_long, vp]
+            L.or_attention_emulate_given_p.restype = i32
             _lib = L
     return _lib
 
@@ -172,7 +175,8 @@ def quantize(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, 
     """Quantise x [T, H, d] (fp32 values). Returns (codes u8 [T,H,d], scales, status).
 
     scales: E4M3 token blocks -> fp32 [H, NB]; MX row32 -> u8 [T, H, d/32];
-    MX col32 -> u8 [H, NG, d] (NG = document-local 32-token groups).
+    MX col32 -> u8 [H, NG, d] (NG = document-local 32-token groups); MX token ->
+    u8 [H, T] (one exponent per token and head over all d).
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     T, H, d = x.shape
@@ -185,6 +189,8 @@ def quantize(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, 
         su = np.zeros((T, H, d // 32), dtype=np.uint8)
     elif layout == MX_COL32:
         su = np.zeros((H, num_blocks(cu, T, 32), d), dtype=np.uint8)
+    elif layout == MX_TOKEN:
+        su = np.zeros((H, T), dtype=np.uint8)
     else:
         raise ValueError(layout)
     st = lib().or_quantize(x.ctypes.data, T, H, d, _ptr(cu), nd, layout, block, int(bool(rotate)),
@@ -236,6 +242,9 @@ def dequantize(qt: QTensor, cu_seqlens=None) -> np.ndarray:
     if qt.layout == MX_ROW32:
         X = qt.scales.astype(np.int64) - 127               # [T, H, d/32]
         return v * np.ldexp(1.0, np.repeat(X, 32, axis=2))
+    if qt.layout == MX_TOKEN:
+        X = qt.scales.T.astype(np.int64) - 127             # [T, H]
+        return v * np.ldexp(1.0, X)[:, :, None]
     ng = [(int(bounds[i + 1] - bounds[i]) + 31) // 32 for i in range(len(bounds) - 1)]
     goff = np.concatenate([[0], np.cumsum(ng)])[:-1]
     gidx = goff[docs] + local // 32                        # [T]
@@ -275,11 +284,12 @@ def attention_fp64_backward(q, k, v, dout, cu_seqlens=None, causal=False, softma
 
 # ---- O-3 -------------------------------------------------------------------
 def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causal=False,
-                      exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False):
+                      exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False, rescale_tau=0.0):
     """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R]),
     and with ties=True a fourth array [R,H,d]: the tie allowance (how far E4M3
     probability codes that sit within rounding of a code boundary can move each
-    output element)."""
+    output element). rescale_tau: a row's reference maximum moves only when a
+    key tile's maximum exceeds it by more than this (log2 units; 0 = exact)."""
     T, H, d = q.codes.shape
     if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
         raise ValueError("Q and K must carry the same rotation")
@@ -294,12 +304,48 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
     qq, kk, vv = q._qt(), k._qt(), v._qt()
     st = lib().or_attention_emulate(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
                                     _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
-                                    int(bool(q.rotated)), scale, QUANTIZE_P if quantize_p else 0,
+                                    int(bool(q.rotated)), scale, float(rescale_tau),
+                                    QUANTIZE_P if quantize_p else 0,
                                     _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data,
                                     None if amb is None else amb.ctypes.data)
     if st != 0:
         raise ValueError(f"oracle emulation rejected its arguments (status {st})")
     return (o, ob, lse, amb) if ties else (o, ob, lse)
+
+
+def attention_emulate_given_p(q: QTensor, k: QTensor, v: QTensor, p_codes: np.ndarray, cu_seqlens=None,
+                              causal=False, exact=False, softmax_scale=None, rows=None, rescale_tau=0.0):
+    """The emulation with a device's E4M3 probability codes checked and used in
+    place of its own. p_codes: uint8 [H, T, stride], the code row t of head h
+    gave document-local key k at [h, t, k] (0 where the row sees no key).
+    Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R], counts) with
+    counts = {same, tie_other, wrong, masked_nonzero}: keys whose device code is
+    the emulation's own, keys whose device code is the other faithful code of a
+    tie, keys with any other code, and unseen keys with a non-zero code."""
+    T, H, d = q.codes.shape
+    if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
+        raise ValueError("Q and K must carry the same rotation")
+    pc = np.ascontiguousarray(p_codes, dtype=np.uint8)
+    if pc.ndim != 3 or pc.shape[0] != H or pc.shape[1] != T:
+        raise ValueError("p_codes must be [H, T, stride]")
+    cu, nd = _cu(cu_seqlens, T)
+    scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    R = T if r is None else len(r)
+    o = np.zeros((R, H, d), dtype=np.float32)
+    ob = np.zeros((R, H, d), dtype=np.uint16)
+    lse = np.zeros((H, R), dtype=np.float32)
+    counts = np.zeros(4, dtype=np.int64)
+    qq, kk, vv = q._qt(), k._qt(), v._qt()
+    st = lib().or_attention_emulate_given_p(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
+                                            _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
+                                            int(bool(q.rotated)), scale, float(rescale_tau), _ptr(r), R, o.ctypes.data,
+                                            ob.ctypes.data, lse.ctypes.data, pc.ctypes.data, pc.shape[2],
+                                            counts.ctypes.data)
+    if st != 0:
+        raise ValueError(f"oracle emulation rejected its arguments (status {st})")
+    names = ("same", "tie_other", "wrong", "masked_nonzero")
+    return o, ob, lse, {n: int(c) for n, c in zip(names, counts)}
 
 
 def bf16_bits_to_f32(b) -> np.ndarray:

@@ -310,12 +310,34 @@ static void quant_mxcol_unit(void* vc, long u) {
     }
 }
 
+/* MX token layout (V of the causal-exact MX mode): one E8M0 exponent per
+ * (token, head) over all d channels, so that every scale depends on its own
+ * token only (FLAMIA sections 1 and 4.5: exact scaling removes within-block
+ * dependencies); codes = E4M3(y * 2^-X). Scales [H][T]. Unit = token. */
+static void quant_mxtok_unit(void* vc, long t) {
+    quant_ctx* c = (quant_ctx*)vc;
+    int d = c->d;
+    float y[256];
+    for (int h = 0; h < c->H; h++) {
+        rotated_row(c, (int)t, h, y);
+        float amax = 0.0f;
+        for (int j = 0; j < d; j++) { float a = fabsf(y[j]); if (!(a <= amax)) amax = a; }
+        if (!isfinite(amax)) __atomic_store_n(&c->err, OR_ERR_NONFINITE, __ATOMIC_RELAXED);
+        int X = or_e8m0_exponent(amax, c->mx_rule);
+        c->su[(long)h * c->T + t] = (uint8_t)(X + 127);
+        float pw = pow2f_exact(-X);
+        uint8_t* dst = c->codes + ((long)t * c->H + h) * d;
+        for (int j = 0; j < d; j++) dst[j] = or_e4m3_encode(y[j] * pw);
+    }
+}
+
 int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
                 int layout, int block, int rotate, uint64_t seed, int mx_rule,
                 uint8_t* codes, float* scales_f32, uint8_t* scales_u8) {
     if (d < 1 || d > 256 || (d & (d - 1)) || T < 0 || H < 1) return OR_ERR_ARG;
     if (layout == OR_E4M3_TOKBLOCK && (block < 1 || !scales_f32)) return OR_ERR_ARG;
     if ((layout == OR_MX_ROW32 || layout == OR_MX_COL32) && (d % 32 || !scales_u8)) return OR_ERR_ARG;
+    if (layout == OR_MX_TOKEN && !scales_u8) return OR_ERR_ARG;
     quant_ctx c;
     memset(&c, 0, sizeof(c));
     c.x = x; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
@@ -325,6 +347,7 @@ int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
     if (layout == OR_E4M3_TOKBLOCK) parallel_for((long)c.D.nd * H, quant_tokblock_unit, &c);
     else if (layout == OR_MX_ROW32) parallel_for(T, quant_mxrow_unit, &c);
     else if (layout == OR_MX_COL32) parallel_for((long)c.D.nd * H, quant_mxcol_unit, &c);
+    else if (layout == OR_MX_TOKEN) parallel_for(T, quant_mxtok_unit, &c);
     else { free(c.D.cu); return OR_ERR_ARG; }
     free(c.D.cu);
     return c.err;
@@ -471,7 +494,9 @@ void or_attention_fp64_bwd(const double* q, const double* k, const double* v, co
 /*           E4M3 layouts multiply the block scales here, MX layouts carry    */
 /*           them inside qhat, khat ("folding score scales", FLAMIA 4.3)      */
 /*   masked keys (causal t > i, keys past the document end): s' = -inf        */
-/*   m'    = max(m, max_t s'_t); alpha = fl32(2^(m - m'))                     */
+/*   m'    = max(m, max_t s'_t) if that exceeds fl32(m + tau), else m:        */
+/*           the reference maximum moves only by more than tau (log2 units;   */
+/*           tau = 0 is the exact running max); alpha = fl32(2^(m - m'))       */
 /*   pt_t  = 2^(s'_t - m' + 8)              (probabilities prescaled by 2^8)  */
 /*   Phat  = E4M3(fl32(pt_t * r_t))         r_t = fl32(V block scale x        */
 /*                                          fl32(1 / reference))              */
@@ -504,9 +529,14 @@ typedef struct {
     const or_qtensor *q, *k, *v; int T, H, d; docs_t D; int causal, exact, rotated; double scale;
     int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse; float* amb;
     double dec[256];
+    float tau;                   /* rescale threshold of the running max, log2 units */
+    const uint8_t* pg;           /* device probability codes [H][T][pstride], or NULL */
+    long pstride;
+    long counts[4];              /* given codes: same, other tie code, violation, masked non-zero */
     long nbq, nbk, nbv, ngv;     /* block counts of the logical scale arrays */
     int h;                       /* head being evaluated */
     double *kh, *vh;             /* dequantised K and V of head h, [T][d] */
+    float* vtok;                 /* MX token layout: V scale 2^X of each token of head h (0 when X = -127) */
 } emu_ctx;
 
 /* dequantised element: code value, times 2^X for the MX layouts (the E4M3
@@ -531,6 +561,10 @@ static void emu_decode_unit(void* vc, long t) {
     for (int j = 0; j < c->d; j++) {
         c->kh[t * c->d + j] = hat(c, c->k, (int)t, c->h, j, 0);
         c->vh[t * c->d + j] = hat(c, c->v, (int)t, c->h, j, c->ngv);
+    }
+    if (c->v->layout == OR_MX_TOKEN) {
+        int b = c->v->scales_u8[(long)c->h * c->T + t];
+        c->vtok[t] = b ? ldexpf(1.0f, b - 127) : 0.0f;
     }
 }
 
@@ -559,8 +593,14 @@ static void emu_unit(void* vc, long ri) {
     /* V reference for the E4M3 layouts */
     float ref = 1.0f;
     if (!vmx) {
-        vs_row = V->scales_f32 + (long)h * c->nbv + block_offset(&c->D, doc, V->block);
-        vb = V->block;
+        /* V's scale per block (E4M3) or per token (MX token layout: 2^X) */
+        if (V->layout == OR_MX_TOKEN) {
+            vs_row = c->vtok + s0;
+            vb = 1;
+        } else {
+            vs_row = V->scales_f32 + (long)h * c->nbv + block_offset(&c->D, doc, V->block);
+            vb = V->block;
+        }
         int nblk = (L + vb - 1) / vb;
         int last = c->exact ? i / vb : nblk - 1;
         float mxv = 0.0f;
@@ -578,6 +618,8 @@ static void emu_unit(void* vc, long ri) {
     float sp[128];
     double ph[128], at[128], tie[128];
     double amax = 0.0;
+    long n_same = 0, n_tie = 0, n_bad = 0, n_mask = 0;
+    const uint8_t* prow = c->pg ? c->pg + ((long)h * c->T + t) * c->pstride : NULL;
     for (int jt = 0; jt < ntiles; jt++) {
         int k0 = jt * 128, kn = (nkeys - k0) < 128 ? nkeys - k0 : 128;
         float mt = -INFINITY;
@@ -603,7 +645,10 @@ static void emu_unit(void* vc, long ri) {
             if (at[a] > amax) amax = at[a];
             if (sc > mt) mt = sc;
         }
-        float mnew = mt > m ? mt : m;
+        /* the reference maximum moves to the new maximum only when that exceeds it
+         * by more than tau (log2 units; tau = 0: whenever it grows) */
+        float mcand = mt > m ? mt : m;
+        float mnew = (m == -INFINITY || mcand > m + c->tau) ? mcand : m;
         float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
         double rowsum = 0.0;
         for (int a = 0; a < kn; a++) {
@@ -615,15 +660,28 @@ static void emu_unit(void* vc, long ri) {
                 r = (sv > 0.0f && ref > 0.0f) ? (double)(sv * inv_ref) : 1.0;
             }
             float pr = (float)(pt * r);
-            ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[or_e4m3_encode(pr)] : (double)pr;
+            uint8_t own = or_e4m3_encode(pr);
+            ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[own] : (double)pr;
             tie[a] = 0.0;
-            if (c->amb && (c->flags & OR_EMU_QUANTIZE_P) && pt > 0.0) {
-                double dx = ldexp(at[a] + amax, -20) +
-                            ldexp(fabs((double)sp[a]) + fabs((double)mnew) + 8.0, -21);
-                double band = 0.6931471805599453 * dx + ldexp(1.0, -20);
-                uint8_t lo = or_e4m3_encode((float)(pr * (1.0 - band)));
-                uint8_t hi = or_e4m3_encode((float)(pr * (1.0 + band)));
-                if (lo != hi) tie[a] = fabs(c->dec[hi] - c->dec[lo]);
+            if ((c->amb || prow) && (c->flags & OR_EMU_QUANTIZE_P)) {
+                uint8_t lo = own, hi = own;
+                if (pt > 0.0) {
+                    double dx = ldexp(at[a] + amax, -20) +
+                                ldexp(fabs((double)sp[a]) + fabs((double)mnew) + 8.0, -21);
+                    double band = 0.6931471805599453 * dx + ldexp(1.0, -20);
+                    lo = or_e4m3_encode((float)(pr * (1.0 - band)));
+                    hi = or_e4m3_encode((float)(pr * (1.0 + band)));
+                }
+                if (prow) {
+                    /* the device's code: the emulation's own, or the other code of a tie */
+                    uint8_t gc = prow[k0 + a];
+                    if (gc == own) n_same++;
+                    else if (lo != hi && (gc == lo || gc == hi)) n_tie++;
+                    else n_bad++;
+                    ph[a] = c->dec[gc];
+                } else if (lo != hi) {
+                    tie[a] = fabs(c->dec[hi] - c->dec[lo]);
+                }
             }
         }
         l = alpha * l + (float)rowsum;
@@ -639,6 +697,15 @@ static void emu_unit(void* vc, long ri) {
         }
         m = mnew;
     }
+    if (prow) {
+        /* keys the row does not see (causal future, past the document end) carry code 0 */
+        for (long kx = nkeys; kx < c->pstride; kx++)
+            if (prow[kx] != 0) n_mask++;
+        __atomic_fetch_add(&c->counts[0], n_same, __ATOMIC_RELAXED);
+        __atomic_fetch_add(&c->counts[1], n_tie, __ATOMIC_RELAXED);
+        __atomic_fetch_add(&c->counts[2], n_bad, __ATOMIC_RELAXED);
+        __atomic_fetch_add(&c->counts[3], n_mask, __ATOMIC_RELAXED);
+    }
     float fin = (l > 0.0f) ? (float)((double)ref / (double)l) : 0.0f;
     float* out = c->o + ((long)ri * c->H + h) * d;
     for (int x = 0; x < d; x++) {
@@ -650,32 +717,69 @@ static void emu_unit(void* vc, long ri) {
         (l > 0.0f) ? (float)(0.6931471805599453 * ((double)m + log2((double)l) - 8.0)) : -INFINITY;
 }
 
-int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
-                         int T, int H, int d, const int32_t* cu, int nd,
-                         int causal, int exact, int rotated, double scale, int flags,
-                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb) {
+static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
+                   int T, int H, int d, const int32_t* cu, int nd,
+                   int causal, int exact, int rotated, double scale, float tau, int flags,
+                   const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb,
+                   const uint8_t* pg, long pstride, long* counts) {
     if (d < 1 || d > 256) return OR_ERR_ARG;
+    if (pg && (!(flags & OR_EMU_QUANTIZE_P) || pstride < 1 || amb)) return OR_ERR_ARG;
+    if (!(tau >= 0.0f && tau < 1.0f)) return OR_ERR_ARG;
     int mxq = q->layout == OR_MX_ROW32, mxk = k->layout == OR_MX_ROW32;
     if (mxq != mxk) return OR_ERR_ARG;
     if (q->layout == OR_MX_COL32 || k->layout == OR_MX_COL32 || v->layout == OR_MX_ROW32) return OR_ERR_ARG;
-    if (exact && (!causal || v->layout != OR_E4M3_TOKBLOCK || v->block != 1)) return OR_ERR_ARG;
+    if (exact && (!causal || !((v->layout == OR_E4M3_TOKBLOCK && v->block == 1) || v->layout == OR_MX_TOKEN)))
+        return OR_ERR_ARG;
+    if (v->layout == OR_MX_TOKEN && !mxq) return OR_ERR_ARG;
     emu_ctx c;
     memset(&c, 0, sizeof(c));
     c.q = q; c.k = k; c.v = v; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
     c.causal = causal; c.exact = exact; c.rotated = rotated; c.scale = scale; c.flags = flags;
     c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse; c.amb = amb;
+    c.pg = pg; c.pstride = pstride; c.tau = tau;
     for (int i = 0; i < 256; i++) c.dec[i] = or_e4m3_decode((uint8_t)i);
     if (!mxq) { c.nbq = block_offset(&c.D, c.D.nd, q->block); c.nbk = block_offset(&c.D, c.D.nd, k->block); }
     if (v->layout == OR_E4M3_TOKBLOCK) c.nbv = block_offset(&c.D, c.D.nd, v->block);
     else c.ngv = block_offset(&c.D, c.D.nd, 32);
+    c.vtok = (float*)malloc(sizeof(float) * (size_t)(T > 0 ? T : 1));
     c.kh = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * d);
     c.vh = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * d);
-    if (!c.kh || !c.vh) { free(c.kh); free(c.vh); free(c.D.cu); return OR_ERR_ARG; }
+    if (!c.kh || !c.vh || !c.vtok) { free(c.kh); free(c.vh); free(c.vtok); free(c.D.cu); return OR_ERR_ARG; }
     for (int h = 0; h < H; h++) {
         c.h = h;
         parallel_for(T, emu_decode_unit, &c);
         parallel_for(c.nrows, emu_unit, &c);
     }
-    free(c.kh); free(c.vh); free(c.D.cu);
+    free(c.kh); free(c.vh); free(c.vtok); free(c.D.cu);
+    if (counts) for (int i = 0; i < 4; i++) counts[i] = c.counts[i];
     return OR_OK;
+}
+
+int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
+                         int T, int H, int d, const int32_t* cu, int nd,
+                         int causal, int exact, int rotated, double scale, float rescale_tau, int flags,
+                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb) {
+    return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, flags, rows, nrows, o, ob,
+                   lse, amb, NULL, 0, NULL);
+}
+
+/* The same emulation with a device's probability codes in place of its own
+ * (where several codes are correct, the device's choice is checked, then
+ * used): p_codes[(h * T + t) * p_stride + k] is the code row t of head h gave
+ * the document-local key k. Every visible key's device code must be the
+ * emulation's own code, or the other code of a tie (the emulation's
+ * probability within its rounding band of an E4M3 boundary: both neighbouring
+ * codes are faithful results); keys the row does not see must carry code 0.
+ * counts: [0] keys with the emulation's code, [1] keys with the other code of
+ * a tie, [2] keys with any other code (errors), [3] unseen keys with a
+ * non-zero code (errors). O and lse are then computed from the device's
+ * codes, so that they can be compared without any tie allowance. */
+int or_attention_emulate_given_p(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
+                                 int T, int H, int d, const int32_t* cu, int nd,
+                                 int causal, int exact, int rotated, double scale, float rescale_tau,
+                                 const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse,
+                                 const uint8_t* p_codes, long p_stride, long* counts) {
+    if (!p_codes || !counts) return OR_ERR_ARG;
+    return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, OR_EMU_QUANTIZE_P, rows,
+                   nrows, o, ob, lse, NULL, p_codes, p_stride, counts);
 }

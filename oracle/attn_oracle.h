@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-enum { OR_E4M3_TOKBLOCK = 0, OR_MX_ROW32 = 1, OR_MX_COL32 = 2 };
+enum { OR_E4M3_TOKBLOCK = 0, OR_MX_ROW32 = 1, OR_MX_COL32 = 2, OR_MX_TOKEN = 3 };
 enum { OR_MX_RULE_NOSAT = 0, OR_MX_RULE_OCP_FLOOR = 1 };
 enum { OR_OK = 0, OR_ERR_ARG = 1, OR_ERR_NONFINITE = 5 };
 
@@ -88,7 +88,7 @@ void or_attention_fp64_bwd(const double* q, const double* k, const double* v, co
 /* ---- O-3 quantised-operand emulation ---- */
 typedef struct {
     const uint8_t* codes;       /* [T][H][d] */
-    int layout;                 /* OR_E4M3_TOKBLOCK / OR_MX_ROW32 / OR_MX_COL32 */
+    int layout;                 /* OR_E4M3_TOKBLOCK / OR_MX_ROW32 / OR_MX_COL32 / OR_MX_TOKEN */
     int block;                  /* token block for OR_E4M3_TOKBLOCK */
     const float* scales_f32;    /* E4M3 layout */
     const uint8_t* scales_u8;   /* MX layouts */
@@ -104,9 +104,20 @@ enum { OR_EMU_QUANTIZE_P = 1 };
 
 int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                          int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
-                         int causal, int exact, int rotated, double softmax_scale, int flags,
+                         int causal, int exact, int rotated, double softmax_scale, float rescale_tau, int flags,
                          const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
                          float* amb);
+
+/* The emulation with a device's E4M3 probability codes checked and substituted
+ * for its own: p_codes[(h * T + t) * p_stride + k] is the code row t of head h
+ * gave document-local key k (0 for keys the row does not see). counts[4]:
+ * keys with the emulation's own code, keys with the other faithful code of a
+ * tie, keys with any other code, unseen keys with a non-zero code. */
+int or_attention_emulate_given_p(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
+                                 int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                                 int causal, int exact, int rotated, double softmax_scale, float rescale_tau,
+                                 const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
+                                 const uint8_t* p_codes, long p_stride, long* counts);
 
 #ifdef __cplusplus
 }

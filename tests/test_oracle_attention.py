@@ -115,7 +115,10 @@ def quant3(oracle_mod, inp, mx, block, rotate=True, seed=0x5EED0009, vblock=None
     if mx:
         Q = oracle_mod.quantize_tensor(q32, cu, ROW, 32, rotate, seed)
         K = oracle_mod.quantize_tensor(k32, cu, ROW, 32, rotate, seed)
-        V = oracle_mod.quantize_tensor(v32, cu, COL, 32, False, 0)
+        if block == 1:   # the causal-exact MX mode: one V exponent per token
+            V = oracle_mod.quantize_tensor(v32, cu, oracle_mod.MX_TOKEN, 1, False, 0)
+        else:
+            V = oracle_mod.quantize_tensor(v32, cu, COL, 32, False, 0)
     else:
         Q = oracle_mod.quantize_tensor(q32, cu, E4M3, block, rotate, seed)
         K = oracle_mod.quantize_tensor(k32, cu, E4M3, block, rotate, seed)
@@ -124,7 +127,7 @@ def quant3(oracle_mod, inp, mx, block, rotate=True, seed=0x5EED0009, vblock=None
 
 
 @pytest.mark.parametrize("mx,block,causal", [(False, 64, False), (False, 128, True), (False, 1, True),
-                                             (True, 32, False), (True, 32, True)])
+                                             (True, 32, False), (True, 32, True), (True, 1, True)])
 def test_emulation_without_p_quantisation_matches_fp64_on_dequantised(oracle_mod, mx, block, causal):
     d = 128 if mx else 64
     inp = workloads.make(2, heads=2, lengths=[300, 77])
@@ -212,6 +215,29 @@ def test_causal_exact_rows_unchanged_by_later_tokens(oracle_mod):
     assert not np.array_equal(ab[:cut + 1], bb[:cut + 1])      # block scales leak
 
 
+def test_mx_causal_exact_rows_unchanged_by_later_tokens(oracle_mod):
+    """The causal-exact MX mode (Q, K one exponent per token and 32 channels, V
+    one per token, V ratios against the running maximum of earlier tokens'
+    exponents): row i is bit-for-bit unchanged when keys or values after i
+    change; the default MX layout (V exponents per 32 tokens) leaks."""
+    inp = workloads.make(5, heads=2, lengths=[400])
+    cu = inp.cu_seqlens
+    cut = 150
+    pert = workloads.make(5, heads=2, lengths=[400])
+    pert.k[cut + 1:] = workloads.bf16_round(pert.k[cut + 1:] * 30)
+    pert.v[cut + 1:] = workloads.bf16_round(pert.v[cut + 1:] * 40)
+    scale = 1 / math.sqrt(128)
+    res = {}
+    for name, block in (("exact", 1), ("default", 32)):
+        res[name] = [oracle_mod.attention_emulate(*quant3(oracle_mod, x, True, block), cu, True, block == 1, scale)
+                     for x in (inp, pert)]
+    (_, ab, al), (_, bb, bl) = res["exact"]
+    assert np.array_equal(ab[:cut + 1], bb[:cut + 1]) and np.array_equal(al[:, :cut + 1], bl[:, :cut + 1])
+    assert not np.array_equal(ab[cut + 1:], bb[cut + 1:])
+    (_, ab, _), (_, bb, _) = res["default"]
+    assert not np.array_equal(ab[:cut + 1], bb[:cut + 1])
+
+
 @pytest.mark.parametrize("mx", [False, True])
 def test_emulation_packed_equals_per_document(oracle_mod, mx):
     lens = [129, 40, 256]
@@ -278,3 +304,52 @@ def test_emulation_all_zero_inputs_closed_form(oracle_mod, mx, block, causal, ex
                         for a, b in zip(cu[:-1], cu[1:])]).astype(np.float64)
     # the emulation forms lse in fp32 as the kernels do: a few fp32 ulps of ln n
     assert np.abs(l3 - np.log(n)[None, :]).max() < 2e-6
+
+
+@pytest.mark.parametrize("mx,block,causal", [(False, 128, False), (False, 128, True), (False, 1, True),
+                                             (True, 32, True)])
+@pytest.mark.parametrize("tau", [0.5, 0.75])
+def test_rescale_threshold_keeps_the_softmax(oracle_mod, mx, block, causal, tau):
+    """A reference maximum that lags the running maximum by at most tau (log2
+    units) changes only the scale P is formed at: with P unquantised the output
+    and lse equal the exact-max emulation's to fp32 rounding, and both equal
+    FP64 attention on the dequantised operands (a wrong rescale factor, row sum
+    or lse term fails one of these)."""
+    inp = workloads.make(3, heads=2, lengths=[700, 77])
+    cu = inp.cu_seqlens
+    Q, K, V = quant3(oracle_mod, inp, mx, block)
+    scale = 1.0 / math.sqrt(128)
+    o0, _, l0 = oracle_mod.attention_emulate(Q, K, V, cu, causal, False, scale, quantize_p=False)
+    ot, _, lt = oracle_mod.attention_emulate(Q, K, V, cu, causal, False, scale, quantize_p=False, rescale_tau=tau)
+    assert np.linalg.norm(ot - o0) / np.linalg.norm(o0) < 2e-6
+    assert np.max(np.abs(lt - l0)) < 2e-5
+    qd, kd, vd = (oracle_mod.dequantize(x, cu) for x in (Q, K, V))
+    o1, l1 = oracle_mod.attention_fp64(qd, kd, vd, cu, causal, scale / 128)
+    assert np.linalg.norm(ot - o1) / np.linalg.norm(o1) < 2e-6
+    assert np.max(np.abs(lt - l1)) < 1e-4
+
+
+def test_rescale_threshold_quantised_p_within_the_e4m3_bound(oracle_mod):
+    """With P quantised, a lagging reference (tau = 0.75) only rescales the
+    probabilities before their E4M3 rounding: the output stays within the
+    rounding bound of the exact-max emulation, differs from it somewhere, and
+    no probability code can saturate -- 2^(8 + tau) = 430.5 rounds to the code
+    416, below E4M3's 448."""
+    assert oracle_mod.e4m3_decode_table()[oracle_mod.e4m3_encode(np.float32(2.0 ** 8.75))[()]] == 416.0
+    inp = workloads.make(2, heads=2, lengths=[1024])
+    cu = inp.cu_seqlens
+    Q, K, V = quant3(oracle_mod, inp, False, 128)
+    scale = 1 / math.sqrt(128)
+    o0, _, _ = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale)
+    ot, _, _ = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale, rescale_tau=0.75)
+    vd = oracle_mod.dequantize(V, cu)
+    bound = 2 * (2.0 ** -4 + 2.0 ** -18 * 1024) * np.abs(vd).max(0)[None]
+    assert np.all(np.abs(ot - o0) <= bound + 1e-6)
+    assert np.linalg.norm(ot - o0) > 0
+
+
+def test_rescale_threshold_out_of_range_rejected(oracle_mod):
+    inp = workloads.make(2, heads=1, lengths=[64])
+    Q, K, V = quant3(oracle_mod, inp, False, 64)
+    with pytest.raises(ValueError):
+        oracle_mod.attention_emulate(Q, K, V, inp.cu_seqlens, False, False, None, rescale_tau=1.5)

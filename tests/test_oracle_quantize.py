@@ -168,3 +168,31 @@ def test_quantise_rotation_uses_same_signs_for_q_and_k(oracle_mod):
     assert not np.array_equal(c1, c2)            # the seed matters
     c3, s3, _ = oracle_mod.quantize(x, None, E4M3, 1, True, 42)
     assert np.array_equal(c1, c3) and np.array_equal(s1, s3)
+
+
+def test_mx_token_rule_error_bound_and_locality(oracle_mod):
+    """MX token layout (V of the causal-exact MX mode): one E8M0 exponent per
+    (token, head) over all channels -- the smallest X with amax <= 448 2^X -- so a
+    token's codes and scale depend on that token alone."""
+    T, H, d = 70, 2, 128
+    x = workloads.draw((T, H, d), "outlier", 31)
+    codes, su, st = oracle_mod.quantize(x, None, oracle_mod.MX_TOKEN, 1, False, 0)
+    assert st == 0 and su.shape == (H, T)
+    X = su.T.astype(np.int64) - 127                          # [T, H]
+    amax = np.abs(x.astype(np.float64)).max(-1)
+    assert np.all(amax <= 448.0 * 2.0 ** X)
+    assert np.all(amax > 448.0 * 2.0 ** (X - 1))
+    deq = oracle_mod.dequantize(oracle_mod.QTensor(codes, su, oracle_mod.MX_TOKEN, 1))
+    unit = np.broadcast_to((2.0 ** X)[:, :, None], x.shape)
+    assert np.all(np.abs(deq - x) <= e4m3_err_bound(x.astype(np.float64), unit))
+    # locality: changing token 40 changes nothing of any other token
+    y = x.copy()
+    y[40] *= 37.0
+    c2, s2, _ = oracle_mod.quantize(y, None, oracle_mod.MX_TOKEN, 1, False, 0)
+    keep = np.arange(T) != 40
+    assert np.array_equal(c2[keep], codes[keep]) and np.array_equal(s2[:, keep], su[:, keep])
+    assert not np.array_equal(s2[:, 40], su[:, 40])
+    # an all-zero token: exponent -127 (byte 0), zero codes
+    z = np.zeros((1, 1, d), dtype=np.float32)
+    c, s, _ = oracle_mod.quantize(z, None, oracle_mod.MX_TOKEN, 1, False, 0)
+    assert s[0, 0] == 0 and not c.any()
