@@ -90,8 +90,12 @@ typedef enum { ATTN_IN_F32 = 0, ATTN_IN_BF16 = 1 } attn_in_dtype;
  *   COL32: tokens 128 t + 32 g..+31) hold the biased exponent X + 127 at byte
  *   (r % 32) * 16 + (r / 32) * 4 + g. Rows or groups past the document end
  *   hold 127. This is the order the block-scaled tensor-core MMA reads its
- *   scale factors in, so the forward copies tiles without reshuffling. */
-typedef enum { ATTN_E4M3_TOKBLOCK = 0, ATTN_MX_ROW32 = 1, ATTN_MX_COL32 = 2 } attn_layout;
+ *   scale factors in, so the forward copies tiles without reshuffling.
+ * ATTN_MX_TOKEN (V of the causal-exact MX mode): MXFP8 codes with one E8M0
+ *   exponent per (token, head) over all head_dim channels, so that no scale
+ *   depends on another token; code = E4M3(x * 2^-X). Scales array: bytes
+ *   [heads][T + num_docs], the token t (global index) at column t. */
+typedef enum { ATTN_E4M3_TOKBLOCK = 0, ATTN_MX_ROW32 = 1, ATTN_MX_COL32 = 2, ATTN_MX_TOKEN = 3 } attn_layout;
 
 /* E8M0 exponent rule: NOSAT = smallest X with amax <= 448 * 2^X (nothing
  * saturates; default); OCP_FLOOR = floor(log2 amax) - 8 (values above
@@ -173,12 +177,15 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
  * 4.1 (packed documents).
  * q, k: ATTN_E4M3_TOKBLOCK or ATTN_MX_ROW32 (both the same; both rotated with
  *    the same seed or both not -> else ATTN_ERR_SEED_MISMATCH).
- * v: ATTN_E4M3_TOKBLOCK (with E4M3 q, k) or ATTN_MX_COL32 (with MX q, k).
+ * v: ATTN_E4M3_TOKBLOCK (with E4M3 q, k), or ATTN_MX_COL32 or ATTN_MX_TOKEN
+ *    (with MX q, k).
  * causal: key j > query i masked, positions local to each document.
- * causal_exact: requires causal and block 1 for q, k and v (E4M3); every
- *    scale then depends on its own token only, and V's scales are folded
- *    against a running maximum over positions <= i, so that no later token
- *    changes row i.
+ * causal_exact: requires causal, and block 1 for q, k and v (E4M3) or a v in
+ *    ATTN_MX_TOKEN (MX: q and k rows are per token already); every scale then
+ *    depends on its own token only, and V's scales are folded against a
+ *    running maximum over positions <= i (for MX a power of two, exactly), so
+ *    that no later token changes row i. An ATTN_MX_TOKEN v without
+ *    causal_exact is folded against its document's largest scale.
  * softmax_scale <= 0 selects 1 / sqrt(d).
  * o: device bf16 [T][H][d]; lse: device fp32 [H][T], natural log of the
  *    scaled scores (lse_i = log sum_j exp(softmax_scale q_i . k_j)). */

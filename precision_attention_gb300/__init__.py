@@ -36,7 +36,7 @@ ATTN_ERR_BAD_SEQLENS = 7
 ATTN_ERR_WORKSPACE = 8
 
 ATTN_IN_F32, ATTN_IN_BF16 = 0, 1
-ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32 = 0, 1, 2
+ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32, ATTN_MX_TOKEN = 0, 1, 2, 3
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
@@ -63,6 +63,35 @@ class _QT(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_pdump = None
+PDUMP_LIB_PATH = os.path.join(_HERE, "libpa_gb300_pdump.so")
+
+
+def _load(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+    S, Q = ctypes.POINTER(_Shape), ctypes.POINTER(_QT)
+    L.attn_quantize_sizes.argtypes = [S, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    L.attn_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
+    L.attn_fwd_workspace_size.argtypes = [S, i32, ctypes.POINTER(sz)]
+    L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
+    L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.attn_fp8_fwd_noalloc.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, vp]
+    L.attn_fp8_fwd_noalloc.restype = ctypes.c_int32
+    L.attn_status_string.argtypes = [i32]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_device_sm_count.argtypes = []
+    L.attn_set_wait_limit.argtypes = [i64]
+    for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
+              "attn_fp8_fwd", "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count",
+              "attn_set_wait_limit"):
+        getattr(L, f).restype = ctypes.c_int32
+    if hasattr(L, "attn_pdump_set"):
+        L.attn_pdump_set.argtypes = [vp, i64]
+        L.attn_pdump_set.restype = ctypes.c_int32
+    return L
 
 
 def lib() -> ctypes.CDLL:
@@ -72,28 +101,21 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with precision_attention_gb300.build.build()")
-            L = ctypes.CDLL(LIB_PATH)
-            vp, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
-            S, Q = ctypes.POINTER(_Shape), ctypes.POINTER(_QT)
-            L.attn_quantize_sizes.argtypes = [S, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
-            L.attn_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
-            L.attn_fwd_workspace_size.argtypes = [S, i32, ctypes.POINTER(sz)]
-            L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
-            L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
-            L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
-            L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
-            L.attn_fp8_fwd_noalloc.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, vp]
-            L.attn_fp8_fwd_noalloc.restype = ctypes.c_int32
-            L.attn_status_string.argtypes = [i32]
-            L.attn_status_string.restype = ctypes.c_char_p
-            L.attn_device_sm_count.argtypes = []
-            L.attn_set_wait_limit.argtypes = [i64]
-            for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
-                      "attn_fp8_fwd",
-                      "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count", "attn_set_wait_limit"):
-                getattr(L, f).restype = ctypes.c_int32
-            _lib = L
+            _lib = _load(LIB_PATH)
     return _lib
+
+
+def pdump_lib() -> ctypes.CDLL:
+    """Load the test build libpa_gb300_pdump.so (include/attn_pdump.h): the same
+    library whose FP8 kernels also report every probability code they hand to
+    the P V product. For parity tests only."""
+    global _pdump
+    with _lock:
+        if _pdump is None:
+            if not os.path.exists(PDUMP_LIB_PATH):
+                raise RuntimeError(f"{PDUMP_LIB_PATH} is missing: build it with build.build(pdump=True)")
+            _pdump = _load(PDUMP_LIB_PATH)
+    return _pdump
 
 
 def attn_status_string(status: int) -> str:
@@ -176,6 +198,8 @@ def empty_qtensor(T: int, H: int, d: int, num_docs: int, layout: int, block: int
     codes = torch.empty((T, H, d), dtype=torch.uint8, device=device)
     if layout == ATTN_E4M3_TOKBLOCK:
         scales = torch.empty((H, sb // (4 * H)), dtype=torch.float32, device=device)
+    elif layout == ATTN_MX_TOKEN:
+        scales = torch.empty((H, sb // H), dtype=torch.uint8, device=device)
     else:
         scales = torch.empty((H, sb // (512 * H), 512), dtype=torch.uint8, device=device)
     return QTensor(codes, scales, layout, block, mx_rule)
@@ -267,6 +291,36 @@ def attn_fp8_fwd_noalloc(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.T
                                       None if status is None else status.data_ptr(), _stream(stream)),
            "attn_fp8_fwd_noalloc")
     return out, lse
+
+
+def attn_fp8_fwd_pdump(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None, key_stride: int,
+                       causal: bool = False, causal_exact: bool = False, softmax_scale: float = 0.0):
+    """attn_fp8_fwd through the test build, which also writes every E4M3
+    probability code it hands to the P V MMA. Returns (o, lse, codes) with
+    codes uint8 [H, T, key_stride]: codes[h, t, k] is what row t of head h gave
+    document-local key k (0 where nothing was written)."""
+    L = pdump_lib()
+    T, H, d = q.codes.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.codes.device
+    ws = workspace(T, H, d, nd, dev)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    codes = torch.zeros((H, T, key_stride), dtype=torch.uint8, device=dev)
+    shape = make_shape(T, H, d, cu_seqlens)
+    cq, ck, cv = q._c(), k._c(), v._c()
+    _check(L.attn_pdump_set(codes.data_ptr(), key_stride), "attn_pdump_set")
+    try:
+        _check(L.attn_fp8_fwd(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                              int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), out.data_ptr(),
+                              lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(None)), "attn_fp8_fwd (test build)")
+        flags = ctypes.c_uint32()
+        st = L.attn_read_device_status(ws.data_ptr(), _stream(None), ctypes.byref(flags))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_fp8_fwd (test build), device status")
+    finally:
+        L.attn_pdump_set(None, 0)
+    return out, lse, codes
 
 
 def attn_read_device_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:

@@ -32,41 +32,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "params.h"
-#include "ptx.cuh"
+#include "attn_common.cuh"
 
 namespace pa {
-
-enum { MODE_BF16 = 0, MODE_E4M3_TILE = 1, MODE_E4M3_COL = 2, MODE_MX = 3 };
-
-template <int ELT, int D, int MODE>
-struct Cfg {
-    static constexpr int RB = D * ELT;                  // bytes per Q/K/V row
-    static constexpr bool SW128 = RB >= 128;
-    static constexpr int ATOMS = SW128 ? RB / 128 : 1;  // 128-byte column blocks per row
-    static constexpr int BOX_ELEMS = SW128 ? 128 / ELT : D;
-    static constexpr int TILE = 128 * RB;
-    static constexpr int PBYTES = 128 * 128 * ELT;
-    static constexpr int PBUF = ELT == 1 ? 2 : 1;       // P buffers (BF16: one, for shared-memory room)
-    static constexpr int NS = ELT == 2 ? 2 : 5;         // K/V ring depth
-    static constexpr int KSTEPS_S = RB / 32;            // 32 bytes of K per MMA
-    static constexpr int KSTEPS_PV = 128 * ELT / 32;
-    static constexpr int KPER = 32 / ELT;               // keys per P V MMA
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_P = OFF_Q + TILE;
-    static constexpr int OFF_KV = OFF_P + PBUF * PBYTES;
-    static constexpr int OFF_XCH = OFF_KV + NS * 2 * TILE;  // float [2 parities][2 halves][128 rows] row maxima
-    static constexpr int OFF_XL = OFF_XCH + 2 * 2 * 128 * 4; // float [2 halves][128 rows] row sums
-    static constexpr int OFF_BAR = OFF_XL + 2 * 128 * 4;
-    // at least 116 KB so that one CTA (which allocates all 512 TMEM columns) fits per SM
-    static constexpr int SMEM = (OFF_BAR + 512 + 1024) > 116 * 1024 ? (OFF_BAR + 512 + 1024) : 116 * 1024;
-    static constexpr int SOFTMAX_WARPS = 8;                  // two warps (column halves) per row quarter
-    static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
-    static constexpr int HC = 64;                            // S columns per softmax thread
-    static constexpr int HD = D / 2;                         // O columns per softmax thread
-    // TMEM columns
-    static constexpr uint32_t T_O = 256;
-};
 
 struct Bars {
     uint64_t q_full, q_empty;
@@ -88,61 +56,6 @@ struct Bars {
     int ep_max[2][4];
     int ep_sum[2][4];
 };
-
-template <int ELT, int D, int MODE>
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
-    using C = Cfg<ELT, D, MODE>;
-    if constexpr (C::SW128) {
-        const uint32_t off = (uint32_t)(kk * 32);
-        return sdesc(base + (off / 128) * (128 * 128) + (off % 128), 16, 1024, SWZ_128B);
-    } else {
-        return sdesc(base + (uint32_t)kk * 32, 16, 512, SWZ_64B);
-    }
-}
-// P: 128 rows x 128 keys, K-major, row = 128 * ELT bytes (always 128-byte swizzle)
-template <int ELT>
-__device__ __forceinline__ uint64_t desc_p(uint32_t base, int kk) {
-    const uint32_t off = (uint32_t)(kk * 32);
-    return sdesc(base + (off / 128) * (128 * 128) + (off % 128), 16, 1024, SWZ_128B);
-}
-// V as the MN-major B operand of P V: rows are keys, channels contiguous
-template <int ELT, int D, int MODE>
-__device__ __forceinline__ uint64_t desc_v(uint32_t base, int kk) {
-    using C = Cfg<ELT, D, MODE>;
-    if constexpr (C::SW128) {
-        return sdesc(base + (uint32_t)(kk * C::KPER * 128), 128 * 128, 1024, SWZ_128B);
-    } else {
-        return sdesc(base + (uint32_t)(kk * C::KPER * 64), 128 * 64, 512, SWZ_64B);
-    }
-}
-__device__ __forceinline__ uint64_t desc_sf(uint32_t base) { return sdesc(base, 0, 128, SWZ_NONE); }
-
-// start-address increments (16-byte units) of K step kk for each operand
-template <int ELT, int D, int MODE>
-__device__ __forceinline__ constexpr uint64_t koff(int kk) {
-    using C = Cfg<ELT, D, MODE>;
-    return C::SW128 ? (uint64_t)(((kk * 32) / 128) * (128 * 128) + (kk * 32) % 128) >> 4 : (uint64_t)(kk * 32) >> 4;
-}
-__device__ __forceinline__ constexpr uint64_t poff(int kk) {
-    return (uint64_t)(((kk * 32) / 128) * (128 * 128) + (kk * 32) % 128) >> 4;
-}
-template <int ELT, int D, int MODE>
-__device__ __forceinline__ constexpr uint64_t voff(int kk) {
-    using C = Cfg<ELT, D, MODE>;
-    return C::SW128 ? (uint64_t)(kk * C::KPER * 128) >> 4 : (uint64_t)(kk * C::KPER * 64) >> 4;
-}
-
-// Limit of the end-of-kernel drains (copies and MMAs already in flight when a wait
-// gave up): those complete by themselves, so the drains keep this long limit
-// whatever the (possibly short) limit of the ordinary waits.
-constexpr long long kDrainLimit = 4000000000LL;
-
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > limit) return false;
-    return true;
-}
 
 template <int ELT, int D, int MODE>
 __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
@@ -559,6 +472,17 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
                     }
                     rowsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
                 }
+#ifdef PA_PDUMP
+                if constexpr (ELT == 1) {
+                    if (p.pdump && rloc < L && k0 + C::HC <= p.pdump_stride) {
+                        uint4* dst =
+                            reinterpret_cast<uint4*>(p.pdump + ((long long)h * p.T + d.start + rloc) * p.pdump_stride + k0);
+#pragma unroll
+                        for (int i = 0; i < C::HC / 16; i++)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+#endif
                 l = alpha * l + rowsum * invr;
                 m = m_new;
                 // O rescale (when any row of the warp moved its max): after P V of the
@@ -684,7 +608,11 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 // A K slot is released after both S_0j and S_1j, a V slot after both P V of tile j.
 template <int MODE>
 struct PairCfgT {
-    static constexpr bool MX = MODE == MODE_MX;
+    // MX: Q K^T block-scaled (scale factors of Q and K in TMEM); MXPV: P V block-scaled
+    // as well (V's 32-token exponents). MODE_MX_EXACT keeps the first and folds V's
+    // per-token exponent into P instead (as the E4M3 per-column mode folds V scales).
+    static constexpr bool MX = MODE == MODE_MX || MODE == MODE_MX_EXACT;
+    static constexpr bool MXPV = MODE == MODE_MX;
     // P lives in TMEM, the A operand of P V read from there: two buffers per query
     // tile, one in MX mode (TMEM also holds the scale factors)
     static constexpr int PBUF = MX ? 1 : 2;
@@ -695,9 +623,11 @@ struct PairCfgT {
     // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
     static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
-    // E4M3 per-column scales (blocks shorter than a tile, causal-exact): each key's K
-    // and V scale of key tile g, staged per stage: float [NS][2][128]
-    static constexpr bool COLS = MODE == MODE_E4M3_COL;
+    // per-key scales of key tile g, staged per stage: float [NS][2][128]. E4M3 per-column
+    // mode (blocks shorter than a tile, causal-exact): K and V scales; MX exact mode: V's
+    // 2^X only (K's exponents are inside the block-scaled MMA)
+    static constexpr bool COLS = MODE == MODE_E4M3_COL || MODE == MODE_MX_EXACT;
+    static constexpr bool KCOLS = MODE == MODE_E4M3_COL;
     static constexpr int OFF_KSC = OFF_SF + SF_BYTES;
     static constexpr int KSC_BYTES = COLS ? NS * 1024 : 0;
     static constexpr int OFF_BAR = OFF_KSC + KSC_BYTES;
@@ -714,6 +644,7 @@ struct PairCfgT {
 };
 static_assert(PairCfgT<MODE_E4M3_TILE>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_MX>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
+static_assert(PairCfgT<MODE_MX_EXACT>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_E4M3_TILE>::NS <= 8 && PairCfgT<MODE_MX>::NS <= 8, "K/V ring deeper than its barriers");
 
 struct PairBars {
@@ -847,10 +778,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&B->v_full[st], PC::TILE + (PC::MX ? 512 : 0));
+                    mbar_arrive_expect_tx(&B->v_full[st], PC::TILE + (PC::MXPV ? 512 : 0));
                     tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE + PC::TILE, &tmv, &B->v_full[st], 0, w.head,
                                 d.start + 128 * j);
-                    if constexpr (PC::MX)
+                    if constexpr (PC::MXPV)
                         bulk_load(sm + PC::OFF_SF + 1536 + PC::NS * 512 + st * 512,
                                   p.mv + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->v_full[st]);
                 }
@@ -866,8 +797,14 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 4; u++) {
                         const int kl = min(128 * j + 4 * lane + u, d.len - 1);
-                        kv[u] = p.sk[w.head * p.capk + d.boff_k + kl / p.bk];
-                        vv[u] = p.sv[w.head * p.capv + d.boff_v + kl / p.bv];
+                        if constexpr (PC::KCOLS) {
+                            kv[u] = p.sk[w.head * p.capk + d.boff_k + kl / p.bk];
+                            vv[u] = p.sv[w.head * p.capv + d.boff_v + kl / p.bv];
+                        } else {   // V exponent byte -> 2^X (0 for X = -127: the token's V codes are 0)
+                            const uint32_t b = p.mv[w.head * p.capv + d.boff_v + kl];
+                            kv[u] = 1.0f;
+                            vv[u] = b ? __uint_as_float(b << 23) : 0.0f;
+                        }
                     }
                     *reinterpret_cast<float4*>(ksc + 4 * lane) = make_float4(kv[0], kv[1], kv[2], kv[3]);
                     *reinterpret_cast<float4*>(ksc + 128 + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
@@ -905,7 +842,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             // MX: this query tile's Q, P, K and V scale-factor columns
             const uint32_t sfq = tmem + PC::T_SFQ + 4 * q, sfp = tmem + PC::T_SFP + 4 * q;
             const uint32_t sfk0 = tmem + PC::T_SFK + 8 * q, sfv0 = tmem + PC::T_SFV + 8 * q;
-            if constexpr (PC::MX) tc_cp_sf(sfp, desc_sf(sSF + 1024));
+            if constexpr (PC::MXPV) tc_cp_sf(sfp, desc_sf(sSF + 1024));
             int kS = 0, itS = item_of(0), jS = 0, qiS = 0;
             uint32_t gS = 0;
             WorkItem wS = itS < n_items ? p.items[itS] : WorkItem{};
@@ -960,7 +897,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 const uint64_t dv = dv0 + st * STAGE16;
                 const uint32_t tp = tmem + PC::T_P + 32 * (PC::PBUF * q + gP % PC::PBUF);   // P, A from TMEM
                 const bool first = jP == 0;
-                if constexpr (PC::MX) {
+                if constexpr (PC::MXPV) {
                     const uint32_t sfv = sfv0 + 4 * (gP & 1);
                     tc_cp_sf(sfv, desc_sf(sSF + 1536 + PC::NS * 512 + st * 512));
 #pragma unroll
@@ -1021,6 +958,8 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             } else if constexpr (MODE == MODE_E4M3_COL) {
                 qs = p.sq[h * p.capq + d.boff_q + rcl / p.bq];
                 ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
+            } else if constexpr (MODE == MODE_MX_EXACT) {   // V's reference exponent, as 2^X
+                ref = p.exact ? p.vref[(long long)h * p.T + d.start + rcl] : p.vref[(long long)h * p.nd + w.doc];
             }
             const float inv_ref = ref > 0.0f ? __fdiv_rn(1.0f, ref) : 0.0f;   // V ratios: s_v x (1 / ref)
             float m = -INFINITY, l = 0.0f;
@@ -1060,17 +999,19 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    // each key's K scale here; the row's factor q_scale x C enters with
-                    // the exponent's FFMA (and the row maximum) below
+                    if constexpr (PC::KCOLS) {
+                        // each key's K scale here; the row's factor q_scale x C enters with
+                        // the exponent's FFMA (and the row maximum) below
 #pragma unroll
-                    for (int t = 0; t < 128; t += 4) {
-                        const float4 k4 = *reinterpret_cast<const float4*>(ksc + t);
-                        const float2 a = __fmul2_rn(make_float2(s[t], s[t + 1]), make_float2(k4.x, k4.y));
-                        const float2 b = __fmul2_rn(make_float2(s[t + 2], s[t + 3]), make_float2(k4.z, k4.w));
-                        s[t] = a.x;
-                        s[t + 1] = a.y;
-                        s[t + 2] = b.x;
-                        s[t + 3] = b.y;
+                        for (int t = 0; t < 128; t += 4) {
+                            const float4 k4 = *reinterpret_cast<const float4*>(ksc + t);
+                            const float2 a = __fmul2_rn(make_float2(s[t], s[t + 1]), make_float2(k4.x, k4.y));
+                            const float2 b = __fmul2_rn(make_float2(s[t + 2], s[t + 3]), make_float2(k4.z, k4.w));
+                            s[t] = a.x;
+                            s[t + 1] = a.y;
+                            s[t + 2] = b.x;
+                            s[t + 3] = b.y;
+                        }
                     }
                     c = qs * p.C;
                 }
@@ -1103,7 +1044,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 const float bias = 8.0f - m_use + lr;
                 uint32_t pk[32];
                 float rowsum;
-                if constexpr (MODE != MODE_E4M3_COL) {
+                if constexpr (!PC::COLS) {
                     const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                      make_float2(0.f, 0.f)};
@@ -1153,6 +1094,13 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     tc_fence_before();
                     mbar_arrive(&B->ksc_empty[gj % PC::NS]);
                 }
+#ifdef PA_PDUMP
+                if (p.pdump && rloc < L && k0 + 128 <= p.pdump_stride) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.pdump + ((long long)h * p.T + d.start + rloc) * p.pdump_stride + k0);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+#endif
                 l = alpha * l + rowsum * invr;
                 m = m_new;
                 // P buffer gj & 1 was last read by P V of tile gj - 2. A rescale of O needs
@@ -1243,12 +1191,6 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
 
 // ---------------------------------------------------------------------------
 // host side
-// [T][H][D] tensor, box = (box_elems channels, 1 head, 128 tokens)
-static bool make_map(CUtensorMap* m, const void* base, int elt, int T, int H, int D, int box_elems, bool sw128) {
-    return make_tensor_map_3d(m, base, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                              D, H, T, (uint64_t)D * elt, (uint64_t)H * D * elt, box_elems, 128,
-                              sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-}
 
 template <int ELT, int D, int MODE>
 static cudaError_t launch_t(const void* q, const void* k, const void* v, const FwdParams& p, int grid,
@@ -1281,7 +1223,7 @@ static cudaError_t launch_pair(const void* q, const void* k, const void* v, cons
     return cudaGetLastError();
 }
 
-// mode: 0 bf16, 1 E4M3 tile scales, 2 E4M3 per-column scales, 3 MX
+// mode: 0 bf16, 1 E4M3 tile scales, 2 E4M3 per-column scales, 3 MX, 4 MX with per-token V (causal-exact)
 cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                         cudaStream_t st) {
     if (mode == MODE_BF16) return D == 128 ? launch_t<2, 128, MODE_BF16>(q, k, v, p, grid, st)
@@ -1292,6 +1234,7 @@ cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const voi
     if (mode == MODE_E4M3_COL) return D == 128 ? launch_pair<MODE_E4M3_COL>(q, k, v, p, grid, st)
                                                : launch_t<1, 64, MODE_E4M3_COL>(q, k, v, p, grid, st);
     if (mode == MODE_MX && D == 128) return launch_pair<MODE_MX>(q, k, v, p, grid, st);
+    if (mode == MODE_MX_EXACT && D == 128) return launch_pair<MODE_MX_EXACT>(q, k, v, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

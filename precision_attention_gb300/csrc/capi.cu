@@ -8,6 +8,9 @@
 #include <cuda_runtime.h>
 
 #include "../../include/attn.h"
+#ifdef PA_PDUMP
+#include "../../include/attn_pdump.h"
+#endif
 #include "params.h"
 
 using namespace pa;
@@ -16,6 +19,10 @@ namespace {
 
 constexpr long long kWaitLimit = 4000000000LL;   // SM cycles (about 2 s) before a wait gives up
 std::atomic<long long> g_wait_limit{kWaitLimit};   // attn_set_wait_limit
+#ifdef PA_PDUMP
+uint8_t* g_pdump = nullptr;                        // attn_pdump_set (test build)
+long long g_pdump_stride = 0;
+#endif
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -43,7 +50,7 @@ attn_status check_ws(const attn_shape* s, void* ws, size_t bytes) {
 
 bool valid_block(int layout, int block) {
     if (layout == ATTN_E4M3_TOKBLOCK) return block == 1 || block == 32 || block == 64 || block == 128;
-    return layout == ATTN_MX_ROW32 || layout == ATTN_MX_COL32;
+    return layout == ATTN_MX_ROW32 || layout == ATTN_MX_COL32 || layout == ATTN_MX_TOKEN;
 }
 
 attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -71,9 +78,12 @@ attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const at
     if (check_workspace && (st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
     const bool mx = q->layout == ATTN_MX_ROW32;
     if (mx) {
-        if (k->layout != ATTN_MX_ROW32 || v->layout != ATTN_MX_COL32) return ATTN_ERR_INVALID_ARG;
+        if (k->layout != ATTN_MX_ROW32 || (v->layout != ATTN_MX_COL32 && v->layout != ATTN_MX_TOKEN))
+            return ATTN_ERR_INVALID_ARG;
         if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-        if (causal_exact) return ATTN_ERR_UNSUPPORTED;
+        // causal-exact MX: V needs one exponent per token (its 32-token column blocks
+        // would let a later token change an earlier row's scale)
+        if (causal_exact && (!causal || v->layout != ATTN_MX_TOKEN)) return ATTN_ERR_INVALID_ARG;
     } else {
         if (q->layout != ATTN_E4M3_TOKBLOCK || k->layout != ATTN_E4M3_TOKBLOCK || v->layout != ATTN_E4M3_TOKBLOCK)
             return ATTN_ERR_INVALID_ARG;
@@ -83,8 +93,9 @@ attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const at
     if (v->rotated) return ATTN_ERR_INVALID_ARG;
     if (q->rotated != k->rotated || (q->rotated && q->hadamard_seed != k->hadamard_seed))
         return ATTN_ERR_SEED_MISMATCH;
-    if (causal_exact && (!causal || q->block != 1 || k->block != 1 || v->block != 1)) return ATTN_ERR_INVALID_ARG;
-    *mode = 3;
+    if (!mx && causal_exact && (!causal || q->block != 1 || k->block != 1 || v->block != 1))
+        return ATTN_ERR_INVALID_ARG;
+    *mode = v->layout == ATTN_MX_TOKEN ? 4 : 3;
     if (!mx) *mode = (q->block == 128 && k->block == 128 && v->block == 128 && !causal_exact) ? 1 : 2;
     return ATTN_OK;
 }
@@ -113,12 +124,14 @@ attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t
     attn_status st = check_shape(shape);
     if (st != ATTN_OK) return st;
     if (!codes_bytes || !scales_bytes) return ATTN_ERR_INVALID_ARG;
-    if (layout < 0 || layout > 2 || !valid_block(layout, block)) return ATTN_ERR_INVALID_ARG;
+    if (layout < 0 || layout > 3 || !valid_block(layout, block)) return ATTN_ERR_INVALID_ARG;
     if (layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     const long long T = shape->total_tokens, H = shape->heads, d = shape->head_dim;
     *codes_bytes = static_cast<size_t>(T * H * d);
     if (layout == ATTN_E4M3_TOKBLOCK)
         *scales_bytes = static_cast<size_t>(H * blocks_cap(shape, block)) * sizeof(float);
+    else if (layout == ATTN_MX_TOKEN)
+        *scales_bytes = static_cast<size_t>(H * blocks_cap(shape, 1));
     else
         *scales_bytes = static_cast<size_t>(H * tiles_cap(shape)) * 512;
     return ATTN_OK;
@@ -144,7 +157,7 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     if (st != ATTN_OK) return st;
     if (!x || !out || !out->codes || !out->scales) return ATTN_ERR_INVALID_ARG;
     if (in_dtype != ATTN_IN_F32 && in_dtype != ATTN_IN_BF16) return ATTN_ERR_INVALID_ARG;
-    if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 2) return ATTN_ERR_INVALID_ARG;
+    if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 3) return ATTN_ERR_INVALID_ARG;
     if (out->layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (out->mx_rule != ATTN_MX_RULE_NOSAT && out->mx_rule != ATTN_MX_RULE_OCP_FLOOR) return ATTN_ERR_INVALID_ARG;
     const int elt = in_dtype == ATTN_IN_BF16 ? 2 : 4;
@@ -164,8 +177,12 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     p.cu = shape->cu_seqlens;
     p.codes = static_cast<uint8_t*>(out->codes);
     p.scales = out->scales;
-    p.block = out->block;
-    p.scale_cap = out->layout == ATTN_E4M3_TOKBLOCK ? blocks_cap(shape, out->block) : tiles_cap(shape);
+    // MX layouts have fixed blocks (32 channels or tokens; one token): the caller's
+    // `block` field does not reach the kernel's block arithmetic for them
+    p.block = out->layout == ATTN_E4M3_TOKBLOCK ? out->block : (out->layout == ATTN_MX_TOKEN ? 1 : 32);
+    p.scale_cap = out->layout == ATTN_E4M3_TOKBLOCK ? blocks_cap(shape, out->block)
+                  : out->layout == ATTN_MX_TOKEN     ? blocks_cap(shape, 1)
+                                                     : tiles_cap(shape);
     p.rotate = rotate != 0;
     p.seed = hadamard_seed;
     p.mx_rule = out->mx_rule;
@@ -205,7 +222,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     sp.docs = docs;
     sp.items = items;
     sp.items_cap = L.items_cap;
-    sp.qpair = (mode == 1 || mode == 2 || mode == 3) && d == 128;   // FP8, d = 128: two query tiles per item
+    sp.qpair = mode >= 1 && d == 128;   // FP8, d = 128: two query tiles per item
     cudaError_t e = launch_sched(sp, stream);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
 
@@ -224,6 +241,10 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt((double)d);
     fp.C = static_cast<float>(sc * 1.4426950408889634 / (rotated ? static_cast<double>(d) : 1.0));
     fp.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+#ifdef PA_PDUMP
+    fp.pdump = g_pdump;
+    fp.pdump_stride = g_pdump_stride;
+#endif
     fp.bq = fp.bk = fp.bv = 1;
     if (e4m3) {
         fp.sq = static_cast<const float*>(qq->scales);
@@ -237,6 +258,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
         fp.bv = qv->block;
         fp.vref = vref;
         VrefParams vp;
+        std::memset(&vp, 0, sizeof(vp));
         vp.sv = fp.sv;
         vp.sv_cap = fp.capv;
         vp.docs = docs;
@@ -257,11 +279,30 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
         fp.tsc = tsc;
         fp.tsc_cap = L.tsc_cap;
         if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-    } else if (mode == 3) {
+    } else if (mode == 3 || mode == 4) {
         fp.mq = static_cast<const uint8_t*>(qq->scales);
         fp.mk = static_cast<const uint8_t*>(qk->scales);
         fp.mv = static_cast<const uint8_t*>(qv->scales);
         fp.ntcap = tiles_cap(shape);
+        if (mode == 4) {
+            // V exponents per token: the V references (running maxima in the exact mode)
+            fp.capv = blocks_cap(shape, 1);
+            fp.bv = 1;
+            fp.vref = vref;
+            VrefParams vp;
+            std::memset(&vp, 0, sizeof(vp));
+            vp.sv_e8 = fp.mv;
+            vp.sv_cap = fp.capv;
+            vp.docs = docs;
+            vp.hdr = hdr;
+            vp.vref = vref;
+            vp.H = H;
+            vp.nd = nd;
+            vp.T = T;
+            vp.exact = exact;
+            vp.bv = 1;
+            if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
     }
     const int grid = attn_device_sm_count();
     if (grid < 1) return ATTN_ERR_CUDA;
@@ -293,6 +334,16 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
     return forward(0, q, k, v, nullptr, nullptr, nullptr, shape, causal != 0, 0, softmax_scale, 0, o, lse,
                    workspace, static_cast<cudaStream_t>(stream));
 }
+
+#ifdef PA_PDUMP
+attn_status attn_pdump_set(void* buf, int64_t key_stride) {
+    if (buf && (key_stride < 128 || key_stride % 128 || (reinterpret_cast<uintptr_t>(buf) & 15u)))
+        return ATTN_ERR_INVALID_ARG;
+    g_pdump = static_cast<uint8_t*>(buf);
+    g_pdump_stride = buf ? key_stride : 0;
+    return ATTN_OK;
+}
+#endif
 
 attn_status attn_set_wait_limit(int64_t cycles) {
     g_wait_limit.store(cycles > 0 ? static_cast<long long>(cycles) : kWaitLimit, std::memory_order_relaxed);

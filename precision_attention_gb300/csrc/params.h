@@ -36,7 +36,8 @@ struct SchedParams {
 };
 
 struct VrefParams {
-    const float* sv;
+    const float* sv;          // V scales (E4M3 layouts), or
+    const uint8_t* sv_e8;     // V exponents X + 127 per token (MX token layout): scale 2^X, 0 for X = -127
     long long sv_cap;
     const DocEntry* docs;
     const WsHeader* hdr;
@@ -70,6 +71,10 @@ struct FwdParams {
     const float4* tsc;    // per (head, key tile) multipliers (E4M3 tile mode), see VrefParams
     long long tsc_cap;
     long long wait_limit;
+    // test build only (PA_PDUMP): every E4M3 probability code handed to the P V MMA,
+    // byte [(h * T + t) * pdump_stride + k] for row t, document-local key k
+    uint8_t* pdump;
+    long long pdump_stride;
 };
 
 // host: a 3-D tiled tensor map over [d2][d1][d0] (d0 contiguous), box (box0, 1, box2)
@@ -82,7 +87,8 @@ int sm_count();
 cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t st);
 cudaError_t launch_vref(const VrefParams& p, cudaStream_t st);
-// mode: 0 bf16, 1 E4M3 with one scale per tile, 2 E4M3 per-column scales, 3 MXFP8
+// mode: 0 bf16, 1 E4M3 with one scale per tile, 2 E4M3 per-column scales, 3 MXFP8,
+// 4 MXFP8 Q and K with one V exponent per token (the causal-exact MX mode)
 cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                         cudaStream_t st);
 

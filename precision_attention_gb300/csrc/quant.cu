@@ -237,7 +237,7 @@ __device__ __forceinline__ int find_doc(const int32_t* off, int nd, int u) {
     return lo;
 }
 
-enum { QM_E4M3_BLOCK = 0, QM_E4M3_ROW = 1, QM_MX_ROW = 2, QM_MX_COL = 3 };
+enum { QM_E4M3_BLOCK = 0, QM_E4M3_ROW = 1, QM_MX_ROW = 2, QM_MX_COL = 3, QM_MX_TOK = 4 };
 
 constexpr int QUANT_THREADS = 256;
 
@@ -262,7 +262,8 @@ struct QuantSmem {
 // y * (448 / amax). QM_E4M3_ROW: the same per (token, head). QM_MX_ROW: E8M0
 // per (token, 32 channels). QM_MX_COL: E8M0 per (32 tokens, channel). MX scale
 // bytes go to the unit's 512-byte tile at (r % 32) * 16 + (r / 32) * 4 + g;
-// rows or groups past the document end get 127.
+// rows or groups past the document end get 127. QM_MX_TOK: E8M0 per (token,
+// head) over all channels, one byte per token.
 template <int EPL, int ELT, int QM, int HOLD>
 __global__ void __launch_bounds__(QUANT_THREADS, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
@@ -401,6 +402,34 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                     store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, inv);
                 }
             }
+        } else if constexpr (QM == QM_MX_TOK) {
+            // one E8M0 exponent per (token, head) over all d channels (the causal-exact
+            // MX mode's V): scale byte at the token's own column
+#pragma unroll 1
+            for (int ps = 0; ps < 4; ps++) {
+                const int row = ps * 32 + warp * 4 + rw;
+                const bool valid = t0 + row < L;
+                float y[EPL];
+                smem_row<EPL, ELT>(tile, row, sl, y);
+                if (p.rotate) rotate_row<EPL>(y, smask, lane);
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+                bool bad = !finite_abs(amax);
+                if (bad) amax = 0.0f;
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
+                }
+                if (valid) {
+                    if (bad) nonfin = true;
+                    const int X = e8m0_exponent(amax, p.mx_rule);
+                    if (sl == 0)
+                        static_cast<uint8_t*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = (uint8_t)(X + 127);
+                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, pow2_neg(X));
+                }
+            }
         } else if constexpr (QM == QM_MX_ROW) {
             uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
 #pragma unroll 1
@@ -525,6 +554,7 @@ static cudaError_t launch_layout(const CUtensorMap& m, const QuantParams& p, int
     if constexpr (EPL == 16) {   // MX layouts: d = 128 only
         if (layout == 1) return launch_q<EPL, ELT, QM_MX_ROW, 1>(m, p, grid, st);
         if (layout == 2) return launch_q<EPL, ELT, QM_MX_COL, 1>(m, p, grid, st);
+        if (layout == 3) return launch_q<EPL, ELT, QM_MX_TOK, 1>(m, p, grid, st);
     } else {
         if (layout != 0) return cudaErrorInvalidValue;
     }

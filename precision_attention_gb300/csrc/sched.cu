@@ -180,12 +180,20 @@ __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
     if (p.hdr->n_items <= 0) return;
     const int h = blockIdx.x % p.H, doc = blockIdx.x / p.H;
     const DocEntry d = p.docs[doc];
-    const float* s = p.sv + (long long)h * p.sv_cap + d.boff_v;
+    const long long base = (long long)h * p.sv_cap + d.boff_v;
+    // block i's V scale: fp32 (E4M3 layouts) or 2^X from the exponent byte (MX token layout)
+    auto sv_at = [&](int i) -> float {
+        if (p.sv_e8) {
+            const uint32_t b = p.sv_e8[base + i];
+            return b ? __uint_as_float(b << 23) : 0.0f;
+        }
+        return p.sv[base + i];
+    };
     const int n = (d.len + p.bv - 1) / p.bv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (!p.exact) {
         float m = 0.0f;
-        for (int i = threadIdx.x; i < n; i += 256) m = fmaxf(m, s[i]);
+        for (int i = threadIdx.x; i < n; i += 256) m = fmaxf(m, sv_at(i));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         if (lane == 0) wmax[warp] = m;
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
         const int nt = (d.len + 127) / 128;
         for (int j = threadIdx.x; j < nt; j += 256) {
             const float ks = p.sk[(long long)h * p.sk_cap + d.boff_k + (128 * j) / p.bk];
-            const float sv = s[(128 * j) / p.bv];
+            const float sv = sv_at((128 * j) / p.bv);
             const float rj = (sv > 0.0f && ref > 0.0f) ? __fmul_rn(sv, inv_ref) : 1.0f;
             p.tsc[(long long)h * p.tsc_cap + d.toff + j] = make_float4(ks * p.C, __log2f(rj), __fdiv_rn(1.0f, rj), 0.0f);
         }
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
     __syncthreads();
     for (int c0 = 0; c0 < n; c0 += 256) {
         const int i = c0 + threadIdx.x;
-        float v = i < n ? s[i] : 0.0f;
+        float v = i < n ? sv_at(i) : 0.0f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float x = __shfl_up_sync(0xFFFFFFFFu, v, o);

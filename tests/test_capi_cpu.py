@@ -100,7 +100,12 @@ def test_shape_rules_on_host(pa):
     assert sizes(pa._Shape(5000, 2, 128, 1025, placeholder_cu)) == pa.ATTN_ERR_UNSUPPORTED   # > 1024 documents
     assert sizes(pa._Shape(1 << 26, 64, 128, 1, None)) == pa.ATTN_ERR_UNSUPPORTED          # T x H beyond int32
     assert sizes(pa._Shape(1024, 2, 128, 1024, placeholder_cu)) == pa.ATTN_OK              # one token per document
-    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=3, block=32) == pa.ATTN_ERR_INVALID_ARG
+    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=4, block=32) == pa.ATTN_ERR_INVALID_ARG   # no such layout
+    assert sizes(pa._Shape(100, 2, 64, 1, None), layout=3, block=1) == pa.ATTN_ERR_UNSUPPORTED     # MX: d = 128
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    shape = pa._Shape(100, 2, 128, 3, placeholder_cu)
+    assert L.attn_quantize_sizes(ctypes.byref(shape), 3, 1, ctypes.byref(cb), ctypes.byref(sb)) == pa.ATTN_OK
+    assert cb.value == 100 * 2 * 128 and sb.value == 2 * (100 + 3)         # one exponent byte per token and head
     assert sizes(pa._Shape(100, 2, 128, 1, None), layout=1, block=64) == pa.ATTN_OK   # block: E4M3 layout only
     shape = pa._Shape(100, 2, 128, 1, None)
     assert L.attn_quantize_sizes(ctypes.byref(shape), 0, 128, None, None) == pa.ATTN_ERR_INVALID_ARG
@@ -137,3 +142,29 @@ def test_seed_mismatch_and_layout_rules_on_host(pa):
     km = pa._QT(fake, fake, 1, 32, 0, 1, 7)
     assert L.attn_fp8_fwd(ctypes.byref(qm), ctypes.byref(km), ctypes.byref(v), ctypes.byref(shape), 0, 0, 0.0,
                           fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
+    # MX causal-exact needs V with one exponent per token, and causal
+    vcol = pa._QT(fake, fake, 2, 32, 0, 0, 0)
+    vtok = pa._QT(fake, fake, 3, 1, 0, 0, 0)
+    assert L.attn_fp8_fwd(ctypes.byref(qm), ctypes.byref(km), ctypes.byref(vcol), ctypes.byref(shape), 1, 1, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_fp8_fwd(ctypes.byref(qm), ctypes.byref(km), ctypes.byref(vtok), ctypes.byref(shape), 0, 1, 0.0,
+                          fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
+
+
+def test_test_build_exports_the_probability_dump_and_the_timed_library_does_not(pa):
+    """libpa_gb300_pdump.so (include/attn_pdump.h) is the parity tests' build: it
+    exports every call of include/attn.h plus attn_pdump_set; the library that
+    is timed exports no such call."""
+    from precision_attention_gb300 import build
+    build.build(pdump=True)
+    src = open(os.path.join(ROOT, "include", "attn_pdump.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    extra = sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)))
+    assert extra == ["attn_pdump_set"]
+    test_lib = ctypes.CDLL(pa.PDUMP_LIB_PATH)
+    for name in declared_functions() + extra:
+        assert hasattr(test_lib, name), name
+    assert not hasattr(ctypes.CDLL(pa.LIB_PATH), "attn_pdump_set")
+    L = pa.pdump_lib()
+    assert L.attn_pdump_set(None, 0) == pa.ATTN_OK
+    assert L.attn_pdump_set(16, 100) == pa.ATTN_ERR_INVALID_ARG      # stride not a multiple of 128

@@ -26,10 +26,10 @@ def run_gpu(inp, mx, block, causal, exact=False, rotate=True, seed=None):
     T, H, d = q.shape
     nd = cu.numel() - 1
     ws = pa.workspace(T, H, d, nd)
-    if mx:
+    if mx:   # block 1: the causal-exact MX mode, one V exponent per token
         Q = pa.attn_quantize(q, cu, ROW, 32, rotate, seed, ws=ws)
         K = pa.attn_quantize(k, cu, ROW, 32, rotate, seed, ws=ws)
-        V = pa.attn_quantize(v, cu, COL, 32, False, 0, ws=ws)
+        V = pa.attn_quantize(v, cu, pa.ATTN_MX_TOKEN if block == 1 else COL, 32, False, 0, ws=ws)
     else:
         Q = pa.attn_quantize(q, cu, E4M3, block, rotate, seed, ws=ws)
         K = pa.attn_quantize(k, cu, E4M3, block, rotate, seed, ws=ws)
@@ -46,7 +46,8 @@ def run_emu(inp, mx, block, causal, exact=False, rotate=True, seed=None, rows=No
     if mx:
         Q = oracle.quantize_tensor(inp.q, cu, ROW, 32, rotate, seed)
         K = oracle.quantize_tensor(inp.k, cu, ROW, 32, rotate, seed)
-        V = oracle.quantize_tensor(inp.v, cu, COL, 32, False, 0)
+        V = oracle.quantize_tensor(inp.v, cu, oracle.MX_TOKEN if block == 1 else COL, 32 if block != 1 else 1,
+                                   False, 0)
     else:
         Q = oracle.quantize_tensor(inp.q, cu, E4M3, block, rotate, seed)
         K = oracle.quantize_tensor(inp.k, cu, E4M3, block, rotate, seed)
@@ -64,6 +65,8 @@ CASES = [
     (2, [384], 2, False, 32, False, False),
     (4, [300, 77, 129], 2, True, 32, False, False),  # MXFP8
     (5, [300, 77, 129, 1], 2, True, 32, True, False),
+    (5, [300, 77, 129, 1], 2, True, 1, True, True),  # MXFP8 causal-exact (V per token)
+    (4, [300, 129], 2, True, 1, False, False),       # MXFP8, V per token, non-causal
 ]
 
 
@@ -124,6 +127,22 @@ def test_causal_exact_rows_unchanged_by_later_tokens():
     pert.v[cut + 1:] = workloads.bf16_round(pert.v[cut + 1:] * 40)
     a, la = run_gpu(inp, False, 1, True, True)
     b, lb = run_gpu(pert, False, 1, True, True)
+    assert torch.equal(a[:cut + 1].view(torch.int16), b[:cut + 1].view(torch.int16))
+    assert torch.equal(la[:, :cut + 1], lb[:, :cut + 1])
+    assert not torch.equal(a[cut + 1:].view(torch.int16), b[cut + 1:].view(torch.int16))
+
+
+def test_mx_causal_exact_rows_unchanged_by_later_tokens():
+    """MXFP8 causal-exact mode on the device: row i is bitwise unchanged when
+    keys or values after i change (Q, K exponents per token and 32 channels, V
+    per token, V ratios against the running maximum of earlier exponents)."""
+    inp = workloads.make(5, heads=2, lengths=[400])
+    cut = 150
+    pert = workloads.make(5, heads=2, lengths=[400])
+    pert.k[cut + 1:] = workloads.bf16_round(pert.k[cut + 1:] * 30)
+    pert.v[cut + 1:] = workloads.bf16_round(pert.v[cut + 1:] * 40)
+    a, la = run_gpu(inp, True, 1, True, True)
+    b, lb = run_gpu(pert, True, 1, True, True)
     assert torch.equal(a[:cut + 1].view(torch.int16), b[:cut + 1].view(torch.int16))
     assert torch.equal(la[:, :cut + 1], lb[:, :cut + 1])
     assert not torch.equal(a[cut + 1:].view(torch.int16), b[cut + 1:].view(torch.int16))

@@ -103,3 +103,17 @@ def test_strided_input_matches_contiguous(oracle_mod):
     codes, scales, _ = oracle_mod.quantize(np.ascontiguousarray(inp.q[:, 1:3, :]), inp.cu_seqlens, E4M3, 128,
                                            True, SEED)
     assert st == 0 and np.array_equal(qt.codes.cpu().numpy(), codes)
+
+
+@pytest.mark.parametrize("lengths,H,rule", [([300, 77, 129], 2, 0), ([130, 1, 255], 3, 1), ([256], 2, 0)])
+def test_mx_token_bit_exact(oracle_mod, lengths, H, rule):
+    """The MX token layout (V of the causal-exact MX mode): codes and the one
+    exponent per (token, head) bit-exact to the oracle, packed documents."""
+    inp = workloads.make(5, heads=H, lengths=lengths)
+    q, k, v, cu = to_device(inp)
+    qt, st = gpu_quant(v, cu, pa.ATTN_MX_TOKEN, 1, False, 0, rule)
+    assert st == 0
+    codes, su, ost = oracle_mod.quantize(inp.v, inp.cu_seqlens, oracle_mod.MX_TOKEN, 1, False, 0, rule)
+    assert ost == 0
+    assert np.array_equal(qt.codes.cpu().numpy(), codes)
+    assert np.array_equal(qt.scales.cpu().numpy()[:, :inp.T], su)
