@@ -154,44 +154,76 @@ def job_throughput(world, flops_per_rank, ms_per_step):
 
 
 # ---------------------------------------------------------------------------
-def gpu_arm(args, rank, world, local_rank):
-    import torch
-    import precision_attention_gb300 as pa
+def quant_bytes(T, H, d, in_elt, mx, block, nd):
+    """Algorithmic HBM bytes of one step's quantisation (Q, K, V): inputs read,
+    codes written, scales written."""
+    n = T * H * d
+    scales = (3 * H * (T + 127) // 128 * 512 / 4) if mx else 3 * H * ((T + block - 1) // block + nd) * 4
+    return 3 * n * (in_elt + 1) + scales
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = workloads.WORKLOADS[args.workload]
-    inp = workloads.make(args.workload, heads=args.heads, seqlen=args.seqlen, batch=args.batch)
+
+def measure_fp8_peak(torch, dev):
+    """Dense E4M3 GEMM throughput of the vendor library (torch._scaled_mm, i.e.
+    cuBLASLt) at 8192^3, best of 10: the measured FP8 tensor peak the attention
+    kernel is compared with (a reference number, not part of the path)."""
+    try:
+        N = 8192
+        a = torch.randn(N, N, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(N, N, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        for _ in range(5):
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * N ** 3 / (best * 1e-3) / 1e12
+    except Exception:   # the library's FP8 GEMM unavailable: report no number
+        return None
+
+
+def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=None, keep=False):
+    """Time `steps` whole steps (quantise Q, K, V, then the FP8 forward) of one
+    workload after `warmup` untimed ones; inputs resident in HBM. Returns the
+    timings (and, with keep, the device tensors for the end-to-end leg)."""
+    w = workloads.WORKLOADS[wid]
+    hd = args.heads if wid == args.workload else None
+    sl = args.seqlen if wid == args.workload else None
+    bt = args.batch if wid == args.workload else None
+    inp = workloads.make(wid, heads=hd, seqlen=sl, batch=bt)
     T, H, d = inp.q.shape
     cu_np = inp.cu_seqlens
     nd = len(cu_np) - 1
-    causal = w.causal
-    mx = w.mx
-    seed = w.hadamard_seed
+    causal, mx, seed = w.causal, w.mx, w.hadamard_seed
     rot = not args.no_rotate
-    exact = bool(args.exact)
-    if exact and (mx or not causal):
-        raise SystemExit("--exact needs a causal E4M3 workload")
+    if exact and not causal:
+        raise SystemExit("--exact needs a causal workload")
     flops = workloads.attention_flops(cu_np, H, d, causal)
     in_dt = torch.float32 if w.in_dtype == "f32" else torch.bfloat16
-
     q_h, k_h, v_h = (torch.from_numpy(np.ascontiguousarray(a)).to(in_dt).pin_memory() for a in (inp.q, inp.k, inp.v))
     q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
     cu = torch.from_numpy(cu_np.astype(np.int32)).to(dev)
     ws = pa.workspace(T, H, d, nd, dev)
-    if mx:
-        lq, lk, lv, blk = ROW, ROW, COL, 32
+    if mx:   # causal-exact: one V exponent per token
+        lq, lk, lv, blk = ROW, ROW, (pa.ATTN_MX_TOKEN if exact else COL), 32
     else:
         lq = lk = lv = E4M3
-        blk = 1 if args.exact else w.block
+        blk = 1 if exact else w.block
     Q = pa.empty_qtensor(T, H, d, nd, lq, blk, device=dev)
     K = pa.empty_qtensor(T, H, d, nd, lk, blk, device=dev)
     V = pa.empty_qtensor(T, H, d, nd, lv, blk, device=dev)
     o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    attn_ev = []
-    step_ev = []
+    attn_ev, step_ev = [], []
 
     def step(record=False):
         if record:
@@ -210,37 +242,69 @@ def gpu_arm(args, rank, world, local_rank):
             e1.record(stream)
             attn_ev.append((e0, e1))
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     st, flags = pa.attn_read_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {pa.attn_status_string(st)} flags {flags:#x}")
-
     dist = None
-    if world > 1:
+    if args.world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
+    sampler = ClockSampler(clocks_idx) if clocks_idx is not None else None
+    if sampler:
+        sampler.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step(record=True)
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    clk = clocks.stop()
+    clk = sampler.stop() if sampler else None
     ms_total = t0.elapsed_time(t1)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms = [a_.elapsed_time(b_) for a_, b_ in attn_ev]
     ends = step_ev[1:] + [t1]
-    step_ms = [a.elapsed_time(b) for a, b in zip(step_ev, ends)]
+    step_ms = [a_.elapsed_time(b_) for a_, b_ in zip(step_ev, ends)]
     st, flags = pa.attn_read_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {pa.attn_status_string(st)} flags {flags:#x}")
+    r = {"inp": inp, "flops": flops, "ms_step": ms_total / steps, "attn_ms": float(np.mean(attn_ms)),
+         "stats": {name: {"median": float(np.median(x)), "min": float(np.min(x)), "p90": float(np.percentile(x, 90))}
+                   for name, x in (("step_ms", step_ms), ("attn_ms", attn_ms))},
+         "clocks": clk, "T": T, "H": H, "d": d, "nd": nd, "mx": mx, "causal": causal, "exact": exact,
+         "quant_bytes": quant_bytes(T, H, d, 4 if w.in_dtype == "f32" else 2, mx, blk, nd)}
+    r["quant_ms"] = r["ms_step"] - r["attn_ms"]
+    if keep:
+        r.update(dict(q=q, k=k, v=v, q_h=q_h, k_h=k_h, v_h=v_h, cu=cu, ws=ws, Q=Q, K=K, V=V, o=o, lse=lse,
+                      lq=lq, lk=lk, lv=lv, blk=blk, rot=rot, seed=seed, stream=stream))
+    else:
+        r["acc"] = None if args.no_accuracy else accuracy_sample(inp, wid, q, k, v, cu, o, pa, torch)
+        del q, k, v, Q, K, V, o, lse, ws
+        torch.cuda.empty_cache()
+    return r
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import precision_attention_gb300 as pa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    args.world = world
+    w = workloads.WORKLOADS[args.workload]
+    r = time_workload(args, pa, torch, dev, args.workload, bool(args.exact), args.steps, args.warmup,
+                      clocks_idx=local_rank, keep=True)
+    T, H, d, nd = r["T"], r["H"], r["d"], r["nd"]
+    q_h, k_h, v_h, cu, ws, Q, K, V = (r[x] for x in ("q_h", "k_h", "v_h", "cu", "ws", "Q", "K", "V"))
+    lq, lk, lv, blk, rot, seed, stream = (r[x] for x in ("lq", "lk", "lv", "blk", "rot", "seed", "stream"))
+    causal, exact = w.causal, bool(args.exact)
+    o, lse = r["o"], r["lse"]
+    q, k, v = r["q"], r["k"], r["v"]
 
     # end to end: every step copies its inputs in from pinned host memory and its
     # output and lse back out. The copies of step i + 1 overlap the compute of step
@@ -297,7 +361,9 @@ def gpu_arm(args, rank, world, local_rank):
     e2e_steps = max(3, min(args.steps, 20))
     run_e2e(2)
     torch.cuda.synchronize()
-    if dist:
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
@@ -309,26 +375,76 @@ def gpu_arm(args, rank, world, local_rank):
     h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
     d2h = o_h.numel() * 2 + lse_h.numel() * 4
 
-    # accuracy on sampled rows (outside the timed region): FP8 and BF16 paths vs FP64
+    # accuracy on sampled rows (outside the timed region): FP8 and BF16 paths vs FP64,
+    # and the BF16 comparator path's own speed on the same inputs
     acc = None
     if rank == 0 and not args.no_accuracy:
-        acc = accuracy_sample(args, inp, q, k, v, cu, o, pa, torch)
+        acc = accuracy_sample(r["inp"], args.workload, q, k, v, cu, o, pa, torch)
+    bf16 = None
+    if rank == 0:
+        bf16 = time_bf16(pa, torch, q, k, v, cu, causal, r["flops"], ws)
+    del sets_in, sets_out, o_h, lse_h
+    for x in ("q", "k", "v", "Q", "K", "V", "o", "lse", "ws"):
+        r.pop(x, None)
+    del q, k, v, Q, K, V, o, lse
+    torch.cuda.empty_cache()
 
-    ms_step = ms_total / args.steps
+    ms_step = r["ms_step"]
     if dist:
         ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dev)
-    stats = {name: {"median": float(np.median(x)), "min": float(np.min(x)), "p90": float(np.percentile(x, 90))}
-             for name, x in (("step_ms", step_ms), ("attn_ms", attn_ms))}
-    return {"inp": inp, "ms_step": ms_step, "flops": flops, "attn_ms": float(np.mean(attn_ms)), "e2e_ms": e2e_ms,
-            "stats": stats,
-            "h2d": h2d, "d2h": d2h, "clocks": clk, "acc": acc, "T": T, "H": H, "d": d, "nd": nd}
+    r.update({"ms_step": ms_step, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "acc": acc, "bf16": bf16})
+    # the other benchmark configurations, timed in this process (rank 0, N = 1 only)
+    r["per_workload"] = None
+    if rank == 0 and world == 1 and not args.no_per_workload and args.heads is None and args.seqlen is None:
+        per = {}
+        for wid, ex in ((2, False), (3, False), (3, True), (4, False), (5, False), (5, True)):
+            if wid == args.workload and ex == bool(args.exact):
+                continue
+            rr = time_workload(args, pa, torch, dev, wid, ex, min(args.steps, 30), 3, clocks_idx=local_rank)
+            per[f"{workloads.WORKLOADS[wid].name}{' causal-exact' if ex else ''}"] = summarize(rr, wid, ex)
+        r["per_workload"] = per
+    r["fp8_peak_measured"] = measure_fp8_peak(torch, dev) if rank == 0 else None
+    return r
 
 
-def accuracy_sample(args, inp, q, k, v, cu, o_fp8, pa, torch):
+def time_bf16(pa, torch, q, k, v, cu, causal, flops, ws, n=10):
+    """The BF16 comparator path's forward time on the workload's bf16 inputs."""
+    if q.dtype != torch.bfloat16:
+        return None
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    for _ in range(2):
+        pa.attn_bf16_fwd(q, k, v, cu, causal, ws=ws, out=o, lse=lse)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        pa.attn_bf16_fwd(q, k, v, cu, causal, ws=ws, out=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"attn_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "kernel": "attn_fwd_kernel (BF16 operands)"}
+
+
+def summarize(rr, wid, exact):
+    peak, _ = fp8_peak()
+    hbm, _ = hbm_peak()
+    val = rr["flops"] / (rr["ms_step"] * 1e-3) / 1e12
+    att = rr["flops"] / (rr["attn_ms"] * 1e-3) / 1e12
+    return {"value": val, "unit": UNIT, "ms_per_step": rr["ms_step"], "attn_ms": rr["attn_ms"],
+            "quant_ms": rr["quant_ms"], "attn_tflops": att, "frac_incl_quant": val / peak, "attn_frac": att / peak,
+            "quant_gbs": rr["quant_bytes"] / (rr["quant_ms"] * 1e-3) / 1e9,
+            "quant_hbm_frac": rr["quant_bytes"] / (rr["quant_ms"] * 1e-3) / 1e9 / hbm,
+            "timing_stats": rr["stats"], "clocks": rr["clocks"], "accuracy": rr.get("acc"),
+            "causal": rr["causal"], "causal_exact": exact, "mx": rr["mx"]}
+
+
+def accuracy_sample(inp, wid, q, k, v, cu, o_fp8, pa, torch):
     import oracle
     rng = np.random.default_rng(123)
     rows = np.sort(rng.choice(inp.T, size=min(64, inp.T), replace=False)).astype(np.int32)
-    causal = workloads.WORKLOADS[args.workload].causal
+    causal = workloads.WORKLOADS[wid].causal
     ob, _ = pa.attn_bf16_fwd(q, k, v, cu, causal)
     o1, _ = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, causal, None, rows=rows)
     o8 = o_fp8.float().cpu().numpy()[rows].astype(np.float64)
@@ -368,7 +484,8 @@ def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
         if w.mx:
             Q = oracle.quantize_tensor(q, c1, ROW, 32, not args.no_rotate, w.hadamard_seed)
             K = oracle.quantize_tensor(k, c1, ROW, 32, not args.no_rotate, w.hadamard_seed)
-            V = oracle.quantize_tensor(v, c1, COL, 32, False, 0)
+            V = (oracle.quantize_tensor(v, c1, oracle.MX_TOKEN, 1, False, 0) if args.exact
+                 else oracle.quantize_tensor(v, c1, COL, 32, False, 0))
         else:
             b = 1 if args.exact else w.block
             Q = oracle.quantize_tensor(q, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
@@ -414,7 +531,8 @@ def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
             "causal": w.causal, "causal_exact": bool(args.exact),
-            "quant": ("MXFP8 (E8M0 per 32)" if w.mx else
+            "quant": (("MXFP8 (E8M0 per 32; V one E8M0 per token, causal-exact)" if args.exact else "MXFP8 (E8M0 per 32)")
+                      if w.mx else
                       ("E4M3 one scale per token (causal-exact)" if args.exact else f"E4M3 blocks of {w.block} tokens")) +
             (" + Hadamard rotation of Q, K" if not args.no_rotate else ", no rotation"), "input_dtype": w.in_dtype,
             "l2": "inputs larger than L2 (bf16 Q, K, V and their codes each exceed 129 MB)" if (
@@ -435,6 +553,8 @@ def main():
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
     ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip timing the other benchmark configurations in the same process")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -467,7 +587,20 @@ def main():
     value = job_throughput(world, r["flops"], r["ms_step"])
     e2e = job_throughput(world, r["flops"], r["e2e_ms"])
     peak, peak_basis = fp8_peak()
+    hbm, hbm_basis = hbm_peak()
     achieved = r["flops"] / (r["attn_ms"] * 1e-3) / 1e12
+    clk = r["clocks"] or {}
+    # the tensor cores' own e4m3 rate at the clock seen (128 x 128 x 32 MMA in 64
+    # cycles: 16,384 FLOP per cycle per SM, measured on this part)
+    mma_rate = None
+    if clk.get("sm_mhz"):
+        import torch
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        mma_rate = 16384.0 * sms * clk["sm_mhz"] * 1e6 / 1e12
+    fp8m = r.get("fp8_peak_measured")
+    kernel = "attn_pair_kernel" if r["d"] == 128 else "attn_fwd_kernel"
+    qbytes = r["quant_bytes"]
+    quant_gbs = qbytes / (r["quant_ms"] * 1e-3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if not w.mx else "mxfp8 (e4m3 + e8m0)", "data": "synthetic",
@@ -476,13 +609,21 @@ def main():
             # per step: three quantiser launches, the work list, (E4M3 only) the V
             # references, the attention kernel
             "gpu_launches": (5 if w.mx else 6) * args.steps,
-            "roofline": {"bound": "tensor",
-                         "kernel": ("attn_pair_kernel" if r["d"] == 128 else "attn_fwd_kernel")
-                         + " (FP8 forward call)", "achieved": achieved,
+            "roofline": {"bound": "tensor", "kernel": kernel + " (FP8 forward call)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
-                         "peak_basis": peak_basis + " (of measured)"},
-            "attn_ms": r["attn_ms"], "quant_ms": r["ms_step"] - r["attn_ms"], "timing_stats": r["stats"],
-            "clocks": r["clocks"], "accuracy": r["acc"]}
+                         "peak_basis": peak_basis + " (of measured)",
+                         "frac_incl_quant": value / world / peak,
+                         "peak_fp8_measured": fp8m, "frac_vs_fp8_measured": (achieved / fp8m) if fp8m else None,
+                         "peak_fp8_measured_basis": "dense e4m3 GEMM of the vendor library (torch._scaled_mm), "
+                                                    "8192^3, best of 10, this process",
+                         "mma_rate_at_clock": mma_rate,
+                         "frac_vs_mma_rate": (achieved / mma_rate) if mma_rate else None},
+            "quant_roofline": {"bound": "hbm", "kernel": "quant_tile_kernel (three launches: Q, K, V)",
+                               "achieved": quant_gbs, "peak": hbm, "unit": "GB/s", "frac": quant_gbs / hbm,
+                               "bytes_per_step": qbytes, "peak_basis": hbm_basis},
+            "attn_ms": r["attn_ms"], "quant_ms": r["quant_ms"], "timing_stats": r["stats"],
+            "clocks": r["clocks"], "accuracy": r["acc"], "bf16_path": r.get("bf16"),
+            "per_workload": r.get("per_workload")}
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_sample(args, r.get("inp"))
         line["cpu_baseline"].pop("seconds", None)
