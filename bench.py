@@ -491,7 +491,8 @@ def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
             Q = oracle.quantize_tensor(q, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
             K = oracle.quantize_tensor(k, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, E4M3, b, False, 0)
-        oracle.attention_emulate(Q, K, V, c1, w.causal, bool(args.exact), None, rows=row_idx)
+        oracle.attention_emulate(Q, K, V, c1, w.causal, bool(args.exact), None, rows=row_idx,
+                                 rescale_tau=0.75 if d == 128 else 0.0)
         t_total += time.perf_counter() - t0
         nkeys = np.arange(1, R + 1) if w.causal else np.full(R, L0)
         flops += float(4.0 * d * nkeys.sum())

@@ -54,6 +54,14 @@
 extern "C" {
 #endif
 
+/* The FP8 forward at head_dim 128 keeps, per query row, a reference maximum that
+ * moves to the row's running maximum only when a key tile raises that by more
+ * than this many log2 units (and always for the row's first key tile); the
+ * probabilities 2^(s - m + 8) then stay below 2^8.75, inside E4M3's range, and
+ * the output is rescaled only when the reference moves. 0 would be the exact
+ * running maximum (the head_dim 64 and BF16 paths use that). */
+#define ATTN_RESCALE_THRESHOLD 0.75f
+
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,     /* bad pointer, size, stride, alignment or combination */

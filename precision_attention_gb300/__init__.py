@@ -38,6 +38,14 @@ ATTN_ERR_WORKSPACE = 8
 ATTN_IN_F32, ATTN_IN_BF16 = 0, 1
 ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32, ATTN_MX_TOKEN = 0, 1, 2, 3
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
+# include/attn.h: the FP8 forward at head_dim 128 moves a row's reference maximum
+# only by more than this (log2 units); the other paths use the exact running max
+ATTN_RESCALE_THRESHOLD = 0.75
+
+
+def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
+    """The reference-maximum threshold the forward uses for this head_dim."""
+    return ATTN_RESCALE_THRESHOLD if (fp8 and head_dim == 128) else 0.0
 
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
            "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",

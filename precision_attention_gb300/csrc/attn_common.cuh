@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/attn.h"
 #include "params.h"
 #include "ptx.cuh"
 

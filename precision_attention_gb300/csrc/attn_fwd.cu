@@ -1036,9 +1036,13 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 }
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7]));
-                // running max (log2 units) and the rescale factor of the old state
+                // reference max (log2 units) and the rescale factor of the old state: the
+                // reference moves to the running max only when that exceeds it by more than
+                // ATTN_RESCALE_THRESHOLD, so that most key tiles leave O as it is; then
+                // 2^(s' - m + 8) <= 2^8.75 < 448 keeps every probability code finite
                 const float mt = mx * c;
-                const float m_new = fmaxf(m, mt);
+                const float m_cand = fmaxf(m, mt);
+                const float m_new = (m == -INFINITY || m_cand > m + ATTN_RESCALE_THRESHOLD) ? m_cand : m;
                 const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
                 const float alpha = (m == -INFINITY) ? 0.0f : (m_new > m ? ex2(m - m_new) : 1.0f);
                 const float bias = 8.0f - m_use + lr;

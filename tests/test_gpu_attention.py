@@ -52,7 +52,8 @@ def run_emu(inp, mx, block, causal, exact=False, rotate=True, seed=None, rows=No
         Q = oracle.quantize_tensor(inp.q, cu, E4M3, block, rotate, seed)
         K = oracle.quantize_tensor(inp.k, cu, E4M3, block, rotate, seed)
         V = oracle.quantize_tensor(inp.v, cu, E4M3, block, False, 0)
-    return oracle.attention_emulate(Q, K, V, cu, causal, exact, None, rows=rows, ties=True)
+    return oracle.attention_emulate(Q, K, V, cu, causal, exact, None, rows=rows, ties=True,
+                                    rescale_tau=pa.rescale_threshold(inp.q.shape[2]))
 
 
 CASES = [

@@ -71,7 +71,8 @@ def test_full_size_codes_and_sampled_rows(oracle_mod, wid, exact):
             assert np.array_equal(mx_row_tiles_to_logical(gs, cu, T, H), c.scales), f"{name} scales"
 
     rows = sample_rows(cu, T, seed=wid)
-    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, exact, None, rows=rows, ties=True)
+    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, exact, None, rows=rows, ties=True,
+                                              rescale_tau=pa.rescale_threshold(inp.q.shape[2]))
     res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
     print(f"workload {wid}{' exact' if exact else ''}: {len(rows)} rows x {H} heads:", res)
     assert res["ok"], res

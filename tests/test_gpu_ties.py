@@ -68,7 +68,8 @@ def check_given_codes(inp, mx, block, causal, exact=False, rows=None):
     # the test build computes the same output bit for bit
     assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(lse, l_ref)
     _, ob, le, counts = oracle.attention_emulate_given_p(Qo, Ko, Vo, codes.cpu().numpy(), inp.cu_seqlens, causal,
-                                                         exact, None, rows=rows)
+                                                         exact, None, rows=rows,
+                                                         rescale_tau=pa.rescale_threshold(inp.q.shape[2]))
     assert counts["wrong"] == 0 and counts["masked_nonzero"] == 0, counts
     res = compare_outputs(o, lse, ob, le, rows=rows)
     assert res["ok"], (res, counts)
