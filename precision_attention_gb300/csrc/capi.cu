@@ -31,7 +31,6 @@ attn_status check_shape(const attn_shape* s) {
     if (s->total_tokens < 1 || s->heads < 1 || s->num_docs < 1) return ATTN_ERR_INVALID_ARG;
     if (s->head_dim != 64 && s->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (!s->cu_seqlens && s->num_docs != 1) return ATTN_ERR_INVALID_ARG;
-    if (s->num_docs > MAX_DOCS) return ATTN_ERR_UNSUPPORTED;
     if (s->num_docs > s->total_tokens) return ATTN_ERR_INVALID_ARG;
     if (static_cast<long long>(s->total_tokens) * s->heads > (1LL << 31) - 1) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
@@ -187,6 +186,10 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     p.seed = hadamard_seed;
     p.mx_rule = out->mx_rule;
     p.status = &static_cast<WsHeader*>(workspace)->status;
+    p.gtab = shape->num_docs > MAX_DOCS
+                 ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                              ws_layout(shape->total_tokens, shape->heads, shape->num_docs).qtab_off)
+                 : nullptr;
     st = cuda_status(launch_quantize(p, out->layout, static_cast<cudaStream_t>(stream)));
     if (st == ATTN_OK) {
         out->rotated = rotate != 0;

@@ -10,7 +10,9 @@ constexpr uint32_t ST_TIMEOUT = 1u << 4;
 constexpr uint32_t ST_NONFINITE = 1u << 5;
 constexpr uint32_t ST_BAD_SEQLENS = 1u << 7;
 
-// Largest document count the quantiser's in-shared-memory document table holds.
+// Largest document count the quantiser keeps its document table for in shared
+// memory (built by every CTA); larger batches get the table in the workspace,
+// written by one extra launch before the quantiser.
 constexpr int MAX_DOCS = 1024;
 
 // One document of the packed batch, as the forward reads it.
@@ -34,9 +36,10 @@ struct WorkItem {
     int32_t ntiles;   // key tiles to visit
 };
 
-// Workspace layout: [header 256 B][docs][items][vref][tile multipliers]
+// Workspace layout: [header 256 B][docs][items][vref][tile multipliers][quantiser
+// document table: start, tile prefix, block prefix, each num_docs + 1 ints]
 struct WsLayout {
-    size_t docs_off, items_off, vref_off, tsc_off, total;
+    size_t docs_off, items_off, vref_off, tsc_off, qtab_off, total;
     int64_t items_cap, vref_cap, tsc_cap;   // tsc_cap: 128-token tiles per head (bound)
 };
 
@@ -51,7 +54,8 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t nd) {
     w.vref_off = align_up(w.items_off + sizeof(WorkItem) * static_cast<size_t>(w.items_cap), 256);
     w.tsc_cap = (T + 127) / 128 + nd;
     w.tsc_off = align_up(w.vref_off + sizeof(float) * static_cast<size_t>(w.vref_cap), 256);
-    w.total = align_up(w.tsc_off + 4 * sizeof(float) * static_cast<size_t>(H * w.tsc_cap), 256);
+    w.qtab_off = align_up(w.tsc_off + 4 * sizeof(float) * static_cast<size_t>(H * w.tsc_cap), 256);
+    w.total = align_up(w.qtab_off + 3 * sizeof(int32_t) * static_cast<size_t>(nd + 1), 256);
     return w;
 }
 

@@ -22,6 +22,9 @@ struct QuantParams {
     unsigned long long seed;
     int mx_rule;
     uint32_t* status;
+    int32_t* gtab;                // device document table [3][nd + 1] (start, tile prefix, block
+                                  // prefix) written by doc_table_kernel, or null: each CTA builds
+                                  // its own in shared memory (nd <= MAX_DOCS)
 };
 
 struct SchedParams {

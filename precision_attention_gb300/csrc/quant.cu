@@ -171,61 +171,90 @@ struct DocTable {
     int32_t off_tile[MAX_DOCS + 1];   // exclusive prefix of ceil(L / 128); [nd] = total tiles
     int32_t off_blk[MAX_DOCS + 1];    // exclusive prefix of ceil(L / block)
 };
+// the table wherever it lives (shared memory, or the workspace for large batches)
+struct DocTablePtrs {
+    int32_t *start, *off_tile, *off_blk;
+};
 
-__device__ bool build_doc_table(const QuantParams& p, DocTable& tab, int* scratch) {
+// Builds the table with the calling CTA (any number of documents, four per thread
+// per round). On malformed cu_seqlens it flags the status word, leaves a table
+// without tiles (off_tile[nd] = 0) and returns false.
+__device__ bool build_doc_table(const QuantParams& p, DocTablePtrs tab, int* scratch) {
     int* bad = scratch;          // [1]
-    int* wsum = scratch + 1;     // [2][8]
-    const int tid = threadIdx.x, nd = p.nd;
+    int* wsum = scratch + 1;     // [2][32]: tile and block totals per warp (up to 32 warps)
+    const int tid = threadIdx.x, nd = p.nd, nw = blockDim.x >> 5;
+    const int lane = tid & 31, warp = tid >> 5;
     if (tid == 0) *bad = 0;
     __syncthreads();
-    int ct[4], cb[4], at = 0, ab = 0;   // each thread owns up to 4 consecutive documents
+    int carry_t = 0, carry_b = 0;
+    for (int base = 0; base < nd; base += 4 * blockDim.x) {   // each thread: 4 consecutive documents
+        int ct[4], cb[4], at = 0, ab = 0;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int i = tid * 4 + k;
-        ct[k] = cb[k] = 0;
-        if (i < nd) {
-            const int s = p.cu ? p.cu[i] : 0, e = p.cu ? p.cu[i + 1] : p.T;
-            tab.start[i] = s;
-            if (e < s) *bad = 1;
-            const int L = e > s ? e - s : 0;
-            ct[k] = (L + 127) / 128;
-            cb[k] = (L + p.block - 1) / p.block;
+        for (int k = 0; k < 4; k++) {
+            const int i = base + tid * 4 + k;
+            ct[k] = cb[k] = 0;
+            if (i < nd) {
+                const int st = p.cu ? p.cu[i] : 0, e = p.cu ? p.cu[i + 1] : p.T;
+                tab.start[i] = st;
+                if (e < st) *bad = 1;
+                const int L = e > st ? e - st : 0;
+                ct[k] = (L + 127) / 128;
+                cb[k] = (L + p.block - 1) / p.block;
+            }
+            at += ct[k];
+            ab += cb[k];
         }
-        at += ct[k];
-        ab += cb[k];
+        int it = at, ib = ab;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int xt = __shfl_up_sync(0xFFFFFFFFu, it, o);
+            const int xb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+            if (lane >= o) { it += xt; ib += xb; }
+        }
+        if (lane == 31) { wsum[warp] = it; wsum[32 + warp] = ib; }
+        __syncthreads();
+        int bt = 0, bb = 0, tt = 0, tb = 0;
+        for (int w = 0; w < nw; w++) {
+            if (w < warp) { bt += wsum[w]; bb += wsum[32 + w]; }
+            tt += wsum[w];
+            tb += wsum[32 + w];
+        }
+        int rt = carry_t + bt + it - at, rb = carry_b + bb + ib - ab;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int i = base + tid * 4 + k;
+            if (i < nd) { tab.off_tile[i] = rt; tab.off_blk[i] = rb; }
+            rt += ct[k];
+            rb += cb[k];
+        }
+        carry_t += tt;
+        carry_b += tb;
+        __syncthreads();   // wsum is reused by the next chunk
     }
     if (tid == 0) {
         const int c0 = p.cu ? p.cu[0] : 0, cn = p.cu ? p.cu[nd] : p.T;
         if (c0 != 0 || cn != p.T) *bad = 1;
         tab.start[nd] = cn;
+        tab.off_tile[nd] = carry_t;
+        tab.off_blk[nd] = carry_b;
     }
-    const int lane = tid & 31, warp = tid >> 5;
-    int it = at, ib = ab;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int xt = __shfl_up_sync(0xFFFFFFFFu, it, o);
-        const int xb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
-        if (lane >= o) { it += xt; ib += xb; }
-    }
-    if (lane == 31) { wsum[warp] = it; wsum[8 + warp] = ib; }
-    __syncthreads();
-    int bt = 0, bb = 0;
-    for (int w = 0; w < warp; w++) { bt += wsum[w]; bb += wsum[8 + w]; }
-    int rt = bt + it - at, rb = bb + ib - ab;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int i = tid * 4 + k;
-        if (i < nd) { tab.off_tile[i] = rt; tab.off_blk[i] = rb; }
-        rt += ct[k];
-        rb += cb[k];
-    }
-    if (tid == blockDim.x - 1) { tab.off_tile[nd] = rt; tab.off_blk[nd] = rb; }
     __syncthreads();
     if (*bad) {
-        if (tid == 0) atomicOr(p.status, ST_BAD_SEQLENS);
+        if (tid == 0) {
+            atomicOr(p.status, ST_BAD_SEQLENS);
+            tab.off_tile[nd] = 0;
+        }
         return false;
     }
     return true;
+}
+
+// The table of a batch with more documents than the quantiser's CTAs keep in
+// shared memory, written once into the workspace ahead of the quantiser.
+__global__ void __launch_bounds__(1024) doc_table_kernel(QuantParams p) {
+    __shared__ int scratch[1 + 64];
+    const DocTablePtrs tab{p.gtab, p.gtab + (p.nd + 1), p.gtab + 2 * (p.nd + 1)};
+    build_doc_table(p, tab, scratch);
 }
 
 __device__ __forceinline__ int find_doc(const int32_t* off, int nd, int u) {
@@ -247,8 +276,8 @@ template <int EPL, int ELT>
 struct QuantSmem {
     static constexpr int STAGE = 128 * EPL * 8 * ELT;   // 128 rows x d elements
     static constexpr int OFF_TAB = 2 * STAGE;
-    static constexpr int OFF_SCRATCH = (OFF_TAB + (int)sizeof(DocTable) + 127) / 128 * 128;   // 32 ints
-    static constexpr int OFF_RED = OFF_SCRATCH + 32 * 4;                                     // float[4][8][128]
+    static constexpr int OFF_SCRATCH = (OFF_TAB + (int)sizeof(DocTable) + 127) / 128 * 128;   // 96 ints
+    static constexpr int OFF_RED = OFF_SCRATCH + 96 * 4;                                     // float[4][8][128]
     static constexpr int OFF_XS = OFF_RED + 4 * 8 * 128 * 4;                                 // int[4][128]
     static constexpr int OFF_BAR = OFF_XS + 4 * 128 * 4;                                     // uint64[2]
     static constexpr int OFF_FLAG = OFF_BAR + 2 * 8;                                         // int[2]
@@ -271,15 +300,20 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     constexpr int D = EPL * 8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    DocTable& tab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
-    int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 17 ints
+    DocTable& stab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
+    int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 65 ints
     float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [4][8][128]
     int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
     int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
     volatile int* abort = flag + 1;
 
-    if (!build_doc_table(p, tab, misc)) return;
+    DocTablePtrs tab{stab.start, stab.off_tile, stab.off_blk};
+    if (p.gtab) {   // written by doc_table_kernel (a malformed batch has no tiles)
+        tab = DocTablePtrs{p.gtab, p.gtab + (p.nd + 1), p.gtab + 2 * (p.nd + 1)};
+    } else if (!build_doc_table(p, tab, misc)) {
+        return;
+    }
     const int H = p.H, nd = p.nd;
     const int n_units = tab.off_tile[nd] * H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sl = lane & 7, rw = lane >> 3;
@@ -567,6 +601,11 @@ static cudaError_t launch_layout(const CUtensorMap& m, const QuantParams& p, int
 }
 
 cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st) {
+    if (p.gtab) {
+        doc_table_kernel<<<1, 1024, 0, st>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int elt = p.in_bf16 ? 2 : 4;
     CUtensorMap m;
     if (!make_tensor_map_3d(&m, p.x, p.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,

@@ -72,14 +72,27 @@ def test_single_head(oracle_mod, wid, mx, block, causal):
     assert res["ok"], res
 
 
-@pytest.mark.parametrize("wid,mx,block,causal", [(3, False, 128, True), (2, False, 32, False), (4, True, 32, False)])
-def test_maximum_document_count(oracle_mod, wid, mx, block, causal):
-    """1024 documents (the most one call takes): the quantiser's and the work
-    list's document tables at capacity, lengths 1 .. 40 drawn from a seed."""
-    lengths = np.random.default_rng(1024 + wid).integers(1, 41, size=1024).tolist()
+@pytest.mark.parametrize("ndocs", [1024, 3000])
+@pytest.mark.parametrize("wid,mx,block,causal", [(3, False, 128, True), (2, False, 32, False), (4, True, 32, False),
+                                                 (3, False, 1, True)])
+def test_many_documents(oracle_mod, ndocs, wid, mx, block, causal):
+    """Many short packed documents, lengths 1 .. 40 drawn from a seed: 1,024
+    (the most the quantiser keeps its document table for in shared memory) and
+    3,000 (the table built in the workspace by one extra launch); codes and
+    scales bit-exact, the forward against the emulation."""
+    lengths = np.random.default_rng(ndocs + wid).integers(1, 41, size=ndocs).tolist()
     inp = workloads.make(wid, heads=2, lengths=lengths)
-    o, lse = run_gpu(inp, mx, block, causal)
-    _, ob, le, amb = run_emu(inp, mx, block, causal)
+    exact = block == 1
+    o, lse = run_gpu(inp, mx, block, causal, exact)
+    q, k, v, cu = to_device(inp)
+    T, H, d = q.shape
+    ws = pa.workspace(T, H, d, cu.numel() - 1)
+    if not mx:   # the quantiser against the oracle's on the same packed batch
+        qt = pa.attn_quantize(q, cu, pa.ATTN_E4M3_TOKBLOCK, block, True, 0x5EED0000 + wid, ws=ws)
+        codes, scales, _ = oracle_mod.quantize(inp.q, inp.cu_seqlens, 0, block, True, 0x5EED0000 + wid)
+        assert np.array_equal(qt.codes.cpu().numpy(), codes)
+        assert np.array_equal(qt.scales.cpu().numpy()[:, :scales.shape[1]].view(np.uint32), scales.view(np.uint32))
+    _, ob, le, amb = run_emu(inp, mx, block, causal, exact)
     res = compare_outputs(o, lse, ob, le, ties=amb)
     assert res["ok"], res
 
