@@ -32,6 +32,10 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 E4M3_TOKBLOCK, MX_ROW32, MX_COL32, MX_TOKEN = 0, 1, 2, 3
 MX_RULE_NOSAT, MX_RULE_OCP_FLOOR = 0, 1
 QUANTIZE_P = 1
+# the probabilities' exponential (emulation flags): 2^x, Schraudolph's, log-domain P (Mitchell)
+EXP_HW, EXP_SCHRAUDOLPH, EXP_MITCHELL_P = 0, 1, 2
+_EXP_FLAGS = {EXP_HW: 0, EXP_SCHRAUDOLPH: 2, EXP_MITCHELL_P: 4}
+SCHRAUDOLPH_DELTA = 0.057984814725439975
 
 _lock = threading.Lock()
 _lib = None
@@ -87,8 +91,13 @@ def lib():
                 i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
             L.or_attention_emulate_given_p.argtypes = [ctypes.POINTER(_QT)] * 3 + [
-                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, vp, i32, vp, vp, vp, vp, ctypes.c_long, vp]
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp,
+                ctypes.c_long, vp]
             L.or_attention_emulate_given_p.restype = i32
+            L.or_exp2_schraudolph.argtypes = [dbl]
+            L.or_exp2_schraudolph.restype = ctypes.c_float
+            L.or_exp2_mitchell_code.argtypes = [dbl]
+            L.or_exp2_mitchell_code.restype = ctypes.c_uint8
             _lib = L
     return _lib
 
@@ -283,13 +292,29 @@ def attention_fp64_backward(q, k, v, dout, cu_seqlens=None, causal=False, softma
 
 
 # ---- O-3 -------------------------------------------------------------------
+def exp2_schraudolph(x) -> np.ndarray:
+    """Schraudolph's exponential of each x (float32 values; scalar path, small arrays)."""
+    xs = np.asarray(x, dtype=np.float64)
+    L = lib()
+    return np.array([L.or_exp2_schraudolph(float(v)) for v in xs.ravel()], dtype=np.float32).reshape(xs.shape)
+
+
+def exp2_mitchell_code(x) -> np.ndarray:
+    """The log-domain E4M3 code of 2^x for each x (uint8; scalar path, small arrays)."""
+    xs = np.asarray(x, dtype=np.float64)
+    L = lib()
+    return np.array([L.or_exp2_mitchell_code(float(v)) for v in xs.ravel()], dtype=np.uint8).reshape(xs.shape)
+
+
 def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causal=False,
-                      exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False, rescale_tau=0.0):
+                      exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False, rescale_tau=0.0,
+                      exp_mode=EXP_HW):
     """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R]),
     and with ties=True a fourth array [R,H,d]: the tie allowance (how far E4M3
     probability codes that sit within rounding of a code boundary can move each
     output element). rescale_tau: a row's reference maximum moves only when a
-    key tile's maximum exceeds it by more than this (log2 units; 0 = exact)."""
+    key tile's maximum exceeds it by more than this (log2 units; 0 = exact).
+    exp_mode: EXP_HW (2^x), EXP_SCHRAUDOLPH or EXP_MITCHELL_P."""
     T, H, d = q.codes.shape
     if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
         raise ValueError("Q and K must carry the same rotation")
@@ -305,7 +330,7 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
     st = lib().or_attention_emulate(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
                                     _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
                                     int(bool(q.rotated)), scale, float(rescale_tau),
-                                    QUANTIZE_P if quantize_p else 0,
+                                    (QUANTIZE_P if quantize_p else 0) | _EXP_FLAGS[exp_mode],
                                     _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data,
                                     None if amb is None else amb.ctypes.data)
     if st != 0:
@@ -314,7 +339,8 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
 
 
 def attention_emulate_given_p(q: QTensor, k: QTensor, v: QTensor, p_codes: np.ndarray, cu_seqlens=None,
-                              causal=False, exact=False, softmax_scale=None, rows=None, rescale_tau=0.0):
+                              causal=False, exact=False, softmax_scale=None, rows=None, rescale_tau=0.0,
+                              exp_mode=EXP_HW):
     """The emulation with a device's E4M3 probability codes checked and used in
     place of its own. p_codes: uint8 [H, T, stride], the code row t of head h
     gave document-local key k at [h, t, k] (0 where the row sees no key).
@@ -339,7 +365,8 @@ def attention_emulate_given_p(q: QTensor, k: QTensor, v: QTensor, p_codes: np.nd
     qq, kk, vv = q._qt(), k._qt(), v._qt()
     st = lib().or_attention_emulate_given_p(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
                                             _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
-                                            int(bool(q.rotated)), scale, float(rescale_tau), _ptr(r), R, o.ctypes.data,
+                                            int(bool(q.rotated)), scale, float(rescale_tau), _EXP_FLAGS[exp_mode],
+                                            _ptr(r), R, o.ctypes.data,
                                             ob.ctypes.data, lse.ctypes.data, pc.ctypes.data, pc.shape[2],
                                             counts.ctypes.data)
     if st != 0:

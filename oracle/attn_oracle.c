@@ -481,6 +481,44 @@ void or_attention_fp64_bwd(const double* q, const double* k, const double* v, co
 }
 
 /* ------------------------------------------------------------------------- */
+/* Bit-level exponentials for inference (FLAMIA section 1: two bit-level      */
+/* exponential approximations; section 4.3: log-domain probability            */
+/* quantisation; section 4.4: Schraudolph's approximation, Mitchell-P).       */
+/*                                                                           */
+/* A binary floating-point number's bit pattern, read as a fixed-point        */
+/* number, is its log2 plus the exponent bias, interpolated linearly between  */
+/* powers of two (Mitchell's logarithm). Read backwards, writing 2^23 (u+127) */
+/* into an fp32's bits gives 2^floor(u) (1 + frac(u)) ~ 2^u (Schraudolph);    */
+/* an E4M3 code (3 mantissa bits, bias 7) of 2^u is round(8 (u + 7)).         */
+/* Relative to 2^u that interpolation is (1 + f) 2^-f, f = frac(u), too large */
+/* by up to 6.2%; evaluating it at u = x - delta scales it by 2^-delta, and   */
+/* delta = log2(1/2 + 3 / (8 ln 2)) minimises the mean square relative error  */
+/* over f uniform on [0, 1) (the minimiser of the quadratic in K = 2^-delta   */
+/* is K = E[g] / E[g^2], g = (1 + f) 2^-f, E[g] = 1 / (2 ln^2 2),             */
+/* E[g^2] = (2 ln 2 + 3/2) / (8 ln^3 2)).                                     */
+/* Readings: u resolved to 2^-14 in the fp32 form (its bits carry 23          */
+/* fractional bits; the reading keeps the whole fp32 range at 2^-14, well     */
+/* below E4M3's 2^-3); ties to even at both roundings; the lower limits keep  */
+/* -inf and tiny probabilities at the smallest normal fp32 (E4M3 code 0) and  */
+/* at code 0.                                                                 */
+/* ------------------------------------------------------------------------- */
+float or_exp2_schraudolph(double x) {
+    double u = x - OR_SCHRAUDOLPH_DELTA;
+    if (!(u > -126.0)) u = -126.0;                        /* also -inf, NaN */
+    double n = nearbyint(ldexp(u + 126.0, 14));          /* to nearest even */
+    double fl = floor(n / 16384.0);
+    double frac = (n - fl * 16384.0) / 16384.0;
+    return (float)ldexp(1.0 + frac, (int)fl - 126);
+}
+
+uint8_t or_exp2_mitchell_code(double x) {
+    double y = 8.0 * (x - OR_SCHRAUDOLPH_DELTA) + 56.0;
+    if (!(y > 0.0)) return 0;                             /* also -inf, NaN */
+    if (y > 126.0) y = 126.0;
+    return (uint8_t)nearbyint(y);
+}
+
+/* ------------------------------------------------------------------------- */
 /* O-3: the running-softmax loop over quantised operands, the way the kernel */
 /* tiles it ("Fused attention kernel", Implementation sketch: running max m, */
 /* rescale alpha = exp(m_old - m_new) applied to the old output, every key   */
@@ -504,6 +542,15 @@ void or_attention_fp64_bwd(const double* q, const double* k, const double* v, co
 /*   l     = fl32(alpha l + fl32(sum_t pt_t))                                 */
 /*   O_c   = fl32(alpha O_c + fl32(sum_t Phat_t vhat_tc))                     */
 /* End: O = fl32(O * fl32(ref / l)), lse = ln2 * (m + log2 l - 8), O -> bf16. */
+/* Bit-level exponentials (E4M3 tile or MX col32, not exact): with            */
+/* x_t = s'_t - m' + 8 + log2 r_t (the V ratio folded into the exponent),     */
+/*   Schraudolph: p_t = or_exp2_schraudolph(x_t), Phat = E4M3(p_t),           */
+/*                l adds p_t / r_t;                                           */
+/*   Mitchell-P:  Phat = the value of or_exp2_mitchell_code(x_t),             */
+/*                l adds Phat / r_t.                                          */
+/* Their tie band adds 2^-15 to dx (the device rounds u + 126 or 8 u + 56,    */
+/* scaled into [0, 1], to fp32 before the final rounding, and forms log2 r    */
+/* with an fp32 approximation).                                               */
 /* vhat = V code (E4M3 layouts; its scale enters through r_t and ref) or     */
 /* code * 2^X (MX col32: the block-scaled MMA applies V's exponents).        */
 /* ref = max over the document's V blocks (default), or, in the causal-exact */
@@ -530,6 +577,7 @@ typedef struct {
     int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse; float* amb;
     double dec[256];
     float tau;                   /* rescale threshold of the running max, log2 units */
+    int expm;                    /* 0: 2^x; OR_EMU_EXP_SCHRAUDOLPH or OR_EMU_EXP_MITCHELL_P */
     const uint8_t* pg;           /* device probability codes [H][T][pstride], or NULL */
     long pstride;
     long counts[4];              /* given codes: same, other tie code, violation, masked non-zero */
@@ -565,6 +613,44 @@ static void emu_decode_unit(void* vc, long t) {
     if (c->v->layout == OR_MX_TOKEN) {
         int b = c->v->scales_u8[(long)c->h * c->T + t];
         c->vtok[t] = b ? ldexpf(1.0f, b - 127) : 0.0f;
+    }
+}
+
+/* One key under a bit-level exponential: x is the exponent with the V ratio
+ * r folded in, dx its error band. Sets ph[a] (the probability P V uses, the
+ * device's code where given) and tie[a], and adds the key's share to rowsum. */
+static void emu_bitexp_key(const emu_ctx* c, int a, double x, double r, double dx, const uint8_t* gcodes,
+                           double* ph, double* tie, double* rowsum, long* n_same, long* n_tie, long* n_bad) {
+    const int schr = c->expm == OR_EMU_EXP_SCHRAUDOLPH;
+    float pf = 0.0f;
+    uint8_t own, lo, hi;
+    if (schr) {
+        pf = or_exp2_schraudolph(x);
+        own = or_e4m3_encode(pf);
+        lo = or_e4m3_encode(or_exp2_schraudolph(x - dx));
+        hi = or_e4m3_encode(or_exp2_schraudolph(x + dx));
+    } else {
+        own = or_exp2_mitchell_code(x);
+        lo = or_exp2_mitchell_code(x - dx);
+        hi = or_exp2_mitchell_code(x + dx);
+    }
+    uint8_t use = own;
+    tie[a] = 0.0;
+    if (gcodes) {
+        uint8_t gc = gcodes[a];
+        if (gc == own) (*n_same)++;
+        else if (lo != hi && (gc == lo || gc == hi)) (*n_tie)++;
+        else (*n_bad)++;
+        use = gc;
+    } else if (lo != hi && (c->flags & OR_EMU_QUANTIZE_P)) {
+        tie[a] = fabs(c->dec[hi] - c->dec[lo]);
+    }
+    if (schr) {
+        ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[use] : (double)pf;
+        *rowsum += (double)pf / r;
+    } else {
+        ph[a] = c->dec[use];
+        *rowsum += c->dec[use] / r;
     }
 }
 
@@ -652,13 +738,20 @@ static void emu_unit(void* vc, long ri) {
         float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
         double rowsum = 0.0;
         for (int a = 0; a < kn; a++) {
-            double pt = exp2((double)sp[a] - (double)mnew + 8.0);
-            rowsum += pt;
             double r = 1.0;
             if (!vmx) {
                 float sv = vs_row[(k0 + a) / vb];
                 r = (sv > 0.0f && ref > 0.0f) ? (double)(sv * inv_ref) : 1.0;
             }
+            if (c->expm) {
+                emu_bitexp_key(c, a, (double)sp[a] - (double)mnew + 8.0 + log2(r), r,
+                               ldexp(at[a] + amax, -20) +
+                                   ldexp(fabs((double)sp[a]) + fabs((double)mnew) + 8.0, -21) + ldexp(1.0, -15),
+                               prow ? prow + k0 : NULL, ph, tie, &rowsum, &n_same, &n_tie, &n_bad);
+                continue;
+            }
+            double pt = exp2((double)sp[a] - (double)mnew + 8.0);
+            rowsum += pt;
             float pr = (float)(pt * r);
             uint8_t own = or_e4m3_encode(pr);
             ph[a] = (c->flags & OR_EMU_QUANTIZE_P) ? c->dec[own] : (double)pr;
@@ -725,6 +818,11 @@ static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v
     if (d < 1 || d > 256) return OR_ERR_ARG;
     if (pg && (!(flags & OR_EMU_QUANTIZE_P) || pstride < 1 || amb)) return OR_ERR_ARG;
     if (!(tau >= 0.0f && tau < 1.0f)) return OR_ERR_ARG;
+    int expm = flags & (OR_EMU_EXP_SCHRAUDOLPH | OR_EMU_EXP_MITCHELL_P);
+    if (expm == (OR_EMU_EXP_SCHRAUDOLPH | OR_EMU_EXP_MITCHELL_P)) return OR_ERR_ARG;
+    /* the bit-level forms: E4M3 with one V scale per key tile, or MX with col32 V; not exact */
+    if (expm && (exact || v->layout == OR_MX_TOKEN || (v->layout == OR_E4M3_TOKBLOCK && v->block != 128)))
+        return OR_ERR_ARG;
     int mxq = q->layout == OR_MX_ROW32, mxk = k->layout == OR_MX_ROW32;
     if (mxq != mxk) return OR_ERR_ARG;
     if (q->layout == OR_MX_COL32 || k->layout == OR_MX_COL32 || v->layout == OR_MX_ROW32) return OR_ERR_ARG;
@@ -736,7 +834,7 @@ static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v
     c.q = q; c.k = k; c.v = v; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
     c.causal = causal; c.exact = exact; c.rotated = rotated; c.scale = scale; c.flags = flags;
     c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse; c.amb = amb;
-    c.pg = pg; c.pstride = pstride; c.tau = tau;
+    c.pg = pg; c.pstride = pstride; c.tau = tau; c.expm = expm;
     for (int i = 0; i < 256; i++) c.dec[i] = or_e4m3_decode((uint8_t)i);
     if (!mxq) { c.nbq = block_offset(&c.D, c.D.nd, q->block); c.nbk = block_offset(&c.D, c.D.nd, k->block); }
     if (v->layout == OR_E4M3_TOKBLOCK) c.nbv = block_offset(&c.D, c.D.nd, v->block);
@@ -776,10 +874,10 @@ int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qten
  * codes, so that they can be compared without any tie allowance. */
 int or_attention_emulate_given_p(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                                  int T, int H, int d, const int32_t* cu, int nd,
-                                 int causal, int exact, int rotated, double scale, float rescale_tau,
+                                 int causal, int exact, int rotated, double scale, float rescale_tau, int flags,
                                  const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse,
                                  const uint8_t* p_codes, long p_stride, long* counts) {
     if (!p_codes || !counts) return OR_ERR_ARG;
-    return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, OR_EMU_QUANTIZE_P, rows,
-                   nrows, o, ob, lse, NULL, p_codes, p_stride, counts);
+    return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, flags | OR_EMU_QUANTIZE_P,
+                   rows, nrows, o, ob, lse, NULL, p_codes, p_stride, counts);
 }

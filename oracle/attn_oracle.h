@@ -94,8 +94,22 @@ typedef struct {
     const uint8_t* scales_u8;   /* MX layouts */
 } or_qtensor;
 
-/* flags */
-enum { OR_EMU_QUANTIZE_P = 1 };
+/* flags. The exponential of the probabilities (default: 2^x itself, the
+ * hardware exp2's target): OR_EMU_EXP_SCHRAUDOLPH or OR_EMU_EXP_MITCHELL_P
+ * select the bit-level forms below (with E4M3 P; E4M3 block-128 or MX col32
+ * V; not causal-exact). */
+enum { OR_EMU_QUANTIZE_P = 1, OR_EMU_EXP_SCHRAUDOLPH = 2, OR_EMU_EXP_MITCHELL_P = 4 };
+
+/* ---- bit-level exponentials (FLAMIA sections 1, 4.3, 4.4) ----
+ * Both take u = x - OR_SCHRAUDOLPH_DELTA, delta = log2(1/2 + 3 / (8 ln 2)).
+ * or_exp2_schraudolph: 2^floor(u) (1 + frac(u)), u resolved to 2^-14 (to
+ *   nearest, ties to even) and limited to u >= -126: the fp32 value whose
+ *   bit pattern is 2^23 (u + 127) (Schraudolph's exponential).
+ * or_exp2_mitchell_code: the E4M3 code round(8 u + 56) (ties to even),
+ *   limited to [0, 126]: the code read as a fixed-point log2 (Mitchell). */
+#define OR_SCHRAUDOLPH_DELTA 0.057984814725439975
+float   or_exp2_schraudolph(double x);
+uint8_t or_exp2_mitchell_code(double x);
 
 /* rows as for O-1; o, o_bf16: [nrows][H][d]; lse: [H][nrows].
  * amb (NULL to skip): [nrows][H][d], the part of each output element that
@@ -116,7 +130,7 @@ int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qten
 int or_attention_emulate_given_p(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                                  int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
                                  int causal, int exact, int rotated, double softmax_scale, float rescale_tau,
-                                 const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
+                                 int flags, const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
                                  const uint8_t* p_codes, long p_stride, long* counts);
 
 #ifdef __cplusplus
