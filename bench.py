@@ -190,7 +190,7 @@ def measure_fp8_peak(torch, dev):
         return None
 
 
-def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=None, keep=False):
+def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=None, keep=False, exp_mode=0):
     """Time `steps` whole steps (quantise Q, K, V, then the FP8 forward) of one
     workload after `warmup` untimed ones; inputs resident in HBM. Returns the
     timings (and, with keep, the device tensors for the end-to-end leg)."""
@@ -237,7 +237,7 @@ def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=No
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0, ws=ws, out=o, lse=lse, stream=stream)
+        pa.attn_fp8_fwd_ex(Q, K, V, cu, causal, exact, 0.0, exp_mode, ws=ws, out=o, lse=lse, stream=stream)
         if record:
             e1.record(stream)
             attn_ev.append((e0, e1))
@@ -403,6 +403,24 @@ def gpu_arm(args, rank, world, local_rank):
             rr = time_workload(args, pa, torch, dev, wid, ex, min(args.steps, 30), 3, clocks_idx=local_rank)
             per[f"{workloads.WORKLOADS[wid].name}{' causal-exact' if ex else ''}"] = summarize(rr, wid, ex)
         r["per_workload"] = per
+        # the bit-level exponentials (inference options) on the four non-exact configurations
+        hw = {w_: (r["attn_ms"], r["acc"]) if w_ == args.workload and not args.exact else None for w_ in (2, 3, 4, 5)}
+        for w_ in hw:
+            if hw[w_] is None:
+                e_ = per[workloads.WORKLOADS[w_].name]
+                hw[w_] = (e_["attn_ms"], e_["accuracy"])
+        bx = {}
+        for w_ in (2, 3, 4, 5):
+            for name, em in (("schraudolph", pa.ATTN_EXP_SCHRAUDOLPH), ("mitchell_p", pa.ATTN_EXP_MITCHELL_P)):
+                rr = time_workload(args, pa, torch, dev, w_, False, min(args.steps, 30), 3, clocks_idx=local_rank,
+                                   exp_mode=em)
+                e_ = summarize(rr, w_, False)
+                e_["exp_mode"] = name
+                e_["attn_speedup_vs_hw_exp2"] = hw[w_][0] / rr["attn_ms"]
+                if rr.get("acc") and hw[w_][1]:
+                    e_["cosine_change_vs_hw_exp2"] = rr["acc"]["cosine_fp8_vs_fp64"] - hw[w_][1]["cosine_fp8_vs_fp64"]
+                bx[f"{workloads.WORKLOADS[w_].name} {name}"] = e_
+        r["bit_level_exp"] = bx
     r["fp8_peak_measured"] = measure_fp8_peak(torch, dev) if rank == 0 else None
     return r
 
@@ -624,7 +642,7 @@ def main():
                                "bytes_per_step": qbytes, "peak_basis": hbm_basis},
             "attn_ms": r["attn_ms"], "quant_ms": r["quant_ms"], "timing_stats": r["stats"],
             "clocks": r["clocks"], "accuracy": r["acc"], "bf16_path": r.get("bf16"),
-            "per_workload": r.get("per_workload")}
+            "per_workload": r.get("per_workload"), "bit_level_exp": r.get("bit_level_exp")}
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_sample(args, r.get("inp"))
         line["cpu_baseline"].pop("seconds", None)

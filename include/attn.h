@@ -62,6 +62,31 @@ extern "C" {
  * running maximum (the head_dim 64 and BF16 paths use that). */
 #define ATTN_RESCALE_THRESHOLD 0.75f
 
+/* How the FP8 forward at head_dim 128 forms each probability p = 2^x of the
+ * softmax, x = s - m + 8 in log2 units (attn_fp8_fwd_ex; attn_fp8_fwd always
+ * uses ATTN_EXP_HW). Source: FLAMIA section 1 (two bit-level exponentials for
+ * inference), section 4.3 (log-domain probability quantisation) and section
+ * 4.4 "Bit-Level Exponentials at Inference".
+ *  ATTN_EXP_HW           the hardware exp2 (fp32, about 2 ulp), then E4M3 with
+ *                        round to nearest even.
+ *  ATTN_EXP_SCHRAUDOLPH  Schraudolph's exponential: the fp32 value whose bit
+ *                        pattern is 2^23 (u + 127), u = x - ATTN_SCHRAUDOLPH_DELTA,
+ *                        i.e. 2^floor(u) (1 + frac(u)), with u resolved to 2^-14
+ *                        (round to nearest even) and limited to u >= -126; then
+ *                        E4M3 with round to nearest even. The row sum adds the
+ *                        fp32 values.
+ *  ATTN_EXP_MITCHELL_P   log-domain P: the E4M3 code itself is the fixed-point
+ *                        log2 of the probability (Mitchell: the code c of a
+ *                        normal E4M3 value is 8 (log2 of its value + 7) where
+ *                        the value is a power of two, linear in between), so
+ *                        c = round(8 u + 56), limited to [0, 126]; the row sum
+ *                        adds the exact E4M3 values of the codes.
+ * Both bit-level modes shift x by ATTN_SCHRAUDOLPH_DELTA = log2(1/2 + 3 / (8 ln 2)),
+ * the shift that minimises the root-mean-square relative error of the linear
+ * interpolation between powers of two (1.77%, within -3.9% / +2.0%). */
+typedef enum { ATTN_EXP_HW = 0, ATTN_EXP_SCHRAUDOLPH = 1, ATTN_EXP_MITCHELL_P = 2 } attn_exp_mode;
+#define ATTN_SCHRAUDOLPH_DELTA 0.057984814725439975
+
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,     /* bad pointer, size, stride, alignment or combination */
@@ -201,6 +226,20 @@ attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const att
                          const attn_shape* shape, int32_t causal, int32_t causal_exact,
                          float softmax_scale, void* o, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_fp8_fwd with a choice of the probabilities' exponential (attn_exp_mode;
+ * ATTN_EXP_HW is attn_fp8_fwd itself). The bit-level modes are inference
+ * options: they need head_dim 128 and causal_exact = 0, and q, k, v either
+ * all ATTN_E4M3_TOKBLOCK with block 128 or ATTN_MX_ROW32 q, k with an
+ * ATTN_MX_COL32 v (else ATTN_ERR_UNSUPPORTED); an exp_mode outside the enum
+ * is ATTN_ERR_INVALID_ARG. Every other argument, check and result is that of
+ * attn_fp8_fwd; lse is the log of the row sum the mode forms.
+ * Source: as attn_fp8_fwd, and FLAMIA sections 1, 4.3 and 4.4 (bit-level
+ * exponentials at inference, log-domain probability quantisation). */
+attn_status attn_fp8_fwd_ex(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                            const attn_shape* shape, int32_t causal, int32_t causal_exact,
+                            float softmax_scale, int32_t exp_mode, void* o, float* lse,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* BF16 attention forward: the same loop with bf16 q, k, v [T][H][d]
  * (contiguous), P in bf16, fp32 accumulation. Same o and lse as above.

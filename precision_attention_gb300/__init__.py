@@ -8,7 +8,7 @@ missing or fails to load, every call raises.
 The functions keep the C names:
 
     attn_quantize_sizes, attn_workspace_size, attn_fwd_workspace_size,
-    attn_quantize, attn_fp8_fwd,
+    attn_quantize, attn_fp8_fwd, attn_fp8_fwd_ex,
     attn_bf16_fwd, attn_read_device_status, attn_status_string,
     attn_device_sm_count
 """
@@ -41,14 +41,16 @@ ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 # include/attn.h: the FP8 forward at head_dim 128 moves a row's reference maximum
 # only by more than this (log2 units); the other paths use the exact running max
 ATTN_RESCALE_THRESHOLD = 0.75
+# include/attn.h attn_exp_mode: the probabilities' exponential of the FP8 forward
+ATTN_EXP_HW, ATTN_EXP_SCHRAUDOLPH, ATTN_EXP_MITCHELL_P = 0, 1, 2
 
 
 def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
     """The reference-maximum threshold the forward uses for this head_dim."""
     return ATTN_RESCALE_THRESHOLD if (fp8 and head_dim == 128) else 0.0
 
-EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd", "attn_bf16_fwd",
-           "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
+EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd",
+           "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
            "attn_set_wait_limit")
 
 
@@ -84,6 +86,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_fwd_workspace_size.argtypes = [S, i32, ctypes.POINTER(sz)]
     L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
     L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    L.attn_fp8_fwd_ex.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, i32, vp, vp, vp, sz, vp]
     L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.attn_fp8_fwd_noalloc.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, vp]
@@ -93,8 +96,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_device_sm_count.argtypes = []
     L.attn_set_wait_limit.argtypes = [i64]
     for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
-              "attn_fp8_fwd", "attn_bf16_fwd", "attn_read_device_status", "attn_device_sm_count",
-              "attn_set_wait_limit"):
+              "attn_fp8_fwd", "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status",
+              "attn_device_sm_count", "attn_set_wait_limit"):
         getattr(L, f).restype = ctypes.c_int32
     if hasattr(L, "attn_pdump_set"):
         L.attn_pdump_set.argtypes = [vp, i64]
@@ -239,6 +242,17 @@ def attn_fp8_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | 
                  causal_exact: bool = False, softmax_scale: float = 0.0, ws: torch.Tensor | None = None,
                  out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
     """FP8 attention forward. Returns (o bf16 [T, H, d], lse fp32 [H, T])."""
+    return attn_fp8_fwd_ex(q, k, v, cu_seqlens, causal, causal_exact, softmax_scale, ATTN_EXP_HW, ws, out, lse,
+                           stream)
+
+
+def attn_fp8_fwd_ex(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None, causal: bool = False,
+                    causal_exact: bool = False, softmax_scale: float = 0.0, exp_mode: int = ATTN_EXP_HW,
+                    ws: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None, stream=None):
+    """FP8 attention forward with a choice of the probabilities' exponential
+    (ATTN_EXP_HW: attn_fp8_fwd itself; ATTN_EXP_SCHRAUDOLPH, ATTN_EXP_MITCHELL_P:
+    the bit-level inference forms). Returns (o bf16 [T, H, d], lse fp32 [H, T])."""
     T, H, d = q.codes.shape
     nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     dev = q.codes.device
@@ -250,9 +264,15 @@ def attn_fp8_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | 
         lse = torch.empty((H, T), dtype=torch.float32, device=dev)
     shape = make_shape(T, H, d, cu_seqlens)
     cq, ck, cv = q._c(), k._c(), v._c()
-    _check(lib().attn_fp8_fwd(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
-                              int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), out.data_ptr(),
-                              lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)), "attn_fp8_fwd")
+    if exp_mode == ATTN_EXP_HW:
+        _check(lib().attn_fp8_fwd(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                                  int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), out.data_ptr(),
+                                  lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)), "attn_fp8_fwd")
+    else:
+        _check(lib().attn_fp8_fwd_ex(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                                     int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), int(exp_mode),
+                                     out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)),
+               "attn_fp8_fwd_ex")
     return out, lse
 
 
@@ -302,7 +322,8 @@ def attn_fp8_fwd_noalloc(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.T
 
 
 def attn_fp8_fwd_pdump(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None, key_stride: int,
-                       causal: bool = False, causal_exact: bool = False, softmax_scale: float = 0.0):
+                       causal: bool = False, causal_exact: bool = False, softmax_scale: float = 0.0,
+                       exp_mode: int = ATTN_EXP_HW):
     """attn_fp8_fwd through the test build, which also writes every E4M3
     probability code it hands to the P V MMA. Returns (o, lse, codes) with
     codes uint8 [H, T, key_stride]: codes[h, t, k] is what row t of head h gave
@@ -319,9 +340,10 @@ def attn_fp8_fwd_pdump(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Ten
     cq, ck, cv = q._c(), k._c(), v._c()
     _check(L.attn_pdump_set(codes.data_ptr(), key_stride), "attn_pdump_set")
     try:
-        _check(L.attn_fp8_fwd(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
-                              int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), out.data_ptr(),
-                              lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(None)), "attn_fp8_fwd (test build)")
+        _check(L.attn_fp8_fwd_ex(ctypes.byref(cq), ctypes.byref(ck), ctypes.byref(cv), ctypes.byref(shape),
+                                 int(bool(causal)), int(bool(causal_exact)), float(softmax_scale), int(exp_mode),
+                                 out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream(None)),
+               "attn_fp8_fwd_ex (test build)")
         flags = ctypes.c_uint32()
         st = L.attn_read_device_status(ws.data_ptr(), _stream(None), ctypes.byref(flags))
         if st != ATTN_OK:

@@ -659,7 +659,7 @@ struct PairBars {
 };
 static_assert(sizeof(PairBars) <= 1024, "pair kernel barrier block exceeds its reserved space");
 
-template <int MODE>
+template <int MODE, int EXPM>
 __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 const float bias = 8.0f - m_use + lr;
                 uint32_t pk[32];
                 float rowsum;
-                if constexpr (!PC::COLS) {
+                if constexpr (!PC::COLS && EXPM == ATTN_EXP_HW) {
                     const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
                     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                      make_float2(0.f, 0.f)};
@@ -1067,6 +1067,61 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     }
                     const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
                     rowsum = a.x + a.y;
+                } else if constexpr (!PC::COLS && EXPM == ATTN_EXP_SCHRAUDOLPH) {
+                    // Schraudolph: p = the fp32 value with bits 2^23 (u + 127), u = x - delta.
+                    // y = sat((u + 126) / 256) in [0, 1) (-inf and u < -126 give 0), then
+                    // n = round(2^22 y) = round(2^14 (u + 126)) lands in the low mantissa bits of
+                    // y 2^22 + 1.5 2^23; shifted left by 9 that word is 2^31 + 2^9 n, so adding
+                    // 2^31 + 2^23 leaves p's bits 2^9 n + 2^23 (n < 2^22: no carry anywhere)
+                    constexpr float kOff = (float)(126.0 - ATTN_SCHRAUDOLPH_DELTA);
+                    const float c1 = c * 0.00390625f, b1 = (bias + kOff) * 0.00390625f;
+                    const float2 r2 = make_float2(4194304.0f, 4194304.0f), k2 = make_float2(12582912.0f, 12582912.0f);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int t = 0; t < 128; t += 8) {
+                        float e[8];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            const float2 yy = make_float2(fma_sat(s[t + u], c1, b1), fma_sat(s[t + u + 1], c1, b1));
+                            const float2 tt = __ffma2_rn(yy, r2, k2);
+                            e[u] = __uint_as_float((__float_as_uint(tt.x) << 9) + 0x80800000u);
+                            e[u + 1] = __uint_as_float((__float_as_uint(tt.y) << 9) + 0x80800000u);
+                            acc[u >> 1] = __fadd2_rn(acc[u >> 1], make_float2(e[u], e[u + 1]));
+                        }
+                        pk[t / 4] = pack_e4m3x4(e[0], e[1], e[2], e[3]);
+                        pk[t / 4 + 1] = pack_e4m3x4(e[4], e[5], e[6], e[7]);
+                    }
+                    const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                    rowsum = a.x + a.y;
+                } else if constexpr (!PC::COLS && EXPM == ATTN_EXP_MITCHELL_P) {
+                    // log-domain P: code = round(8 u + 56) in [0, 126]. y = sat((8 u + 56) / 128),
+                    // then the code lands in the low byte of y 128 + 1.5 2^23 (x <= 8.75 keeps
+                    // 128 y <= 126). Word << 20 = code << 20: the fp32 whose value is 2^-120 times
+                    // the code's E4M3 value (normal and subnormal codes alike); the row sum adds
+                    // those and takes the 2^120 back once.
+                    constexpr float kOff = (float)(0.4375 - ATTN_SCHRAUDOLPH_DELTA / 16.0);
+                    const float c1 = c * 0.0625f, b1 = fmaf(bias, 0.0625f, kOff);
+                    const float2 r2 = make_float2(128.0f, 128.0f), k2 = make_float2(12582912.0f, 12582912.0f);
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int t = 0; t < 128; t += 8) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            const float2 yy = make_float2(fma_sat(s[t + u], c1, b1), fma_sat(s[t + u + 1], c1, b1));
+                            const float2 tt = __ffma2_rn(yy, r2, k2);
+                            w[u] = __float_as_uint(tt.x);
+                            w[u + 1] = __float_as_uint(tt.y);
+                            acc[u >> 1] = __fadd2_rn(acc[u >> 1],
+                                                     make_float2(__uint_as_float(w[u] << 20), __uint_as_float(w[u + 1] << 20)));
+                        }
+                        pk[t / 4] = __byte_perm(__byte_perm(w[0], w[1], 0x0040), __byte_perm(w[2], w[3], 0x0040), 0x5410);
+                        pk[t / 4 + 1] = __byte_perm(__byte_perm(w[4], w[5], 0x0040), __byte_perm(w[6], w[7], 0x0040), 0x5410);
+                    }
+                    const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+                    rowsum = (a.x + a.y) * 1.329227995784916e36f;   // 2^120
                 } else {
                     // p = 2^(s' + bias), row sum of the unquantised p, then each key's V
                     // ratio r = s_v x (1 / ref) folded in. A key whose V scale is 0 has
@@ -1212,7 +1267,7 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
     return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, int EXPM = ATTN_EXP_HW>
 static cudaError_t launch_pair(const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                                cudaStream_t st) {
     CUtensorMap mq, mk, mv;
@@ -1220,7 +1275,7 @@ static cudaError_t launch_pair(const void* q, const void* k, const void* v, cons
         !make_map(&mv, v, 1, p.T, p.H, 128, 128, true))
         return cudaErrorInvalidValue;
     using PC = PairCfgT<MODE>;
-    auto kern = attn_pair_kernel<MODE>;
+    auto kern = attn_pair_kernel<MODE, EXPM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, PC::THREADS, PC::SMEM, st>>>(mq, mk, mv, p);
@@ -1228,8 +1283,18 @@ static cudaError_t launch_pair(const void* q, const void* k, const void* v, cons
 }
 
 // mode: 0 bf16, 1 E4M3 tile scales, 2 E4M3 per-column scales, 3 MX, 4 MX with per-token V (causal-exact)
-cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
-                        cudaStream_t st) {
+cudaError_t launch_attn(int mode, int expm, int D, const void* q, const void* k, const void* v, const FwdParams& p,
+                        int grid, cudaStream_t st) {
+    if (expm != ATTN_EXP_HW) {
+        if (D != 128) return cudaErrorInvalidValue;
+        if (mode == MODE_E4M3_TILE)
+            return expm == ATTN_EXP_SCHRAUDOLPH ? launch_pair<MODE_E4M3_TILE, ATTN_EXP_SCHRAUDOLPH>(q, k, v, p, grid, st)
+                                                : launch_pair<MODE_E4M3_TILE, ATTN_EXP_MITCHELL_P>(q, k, v, p, grid, st);
+        if (mode == MODE_MX)
+            return expm == ATTN_EXP_SCHRAUDOLPH ? launch_pair<MODE_MX, ATTN_EXP_SCHRAUDOLPH>(q, k, v, p, grid, st)
+                                                : launch_pair<MODE_MX, ATTN_EXP_MITCHELL_P>(q, k, v, p, grid, st);
+        return cudaErrorInvalidValue;
+    }
     if (mode == MODE_BF16) return D == 128 ? launch_t<2, 128, MODE_BF16>(q, k, v, p, grid, st)
                                            : launch_t<2, 64, MODE_BF16>(q, k, v, p, grid, st);
     // E4M3 and MX at d = 128: two query tiles per CTA (the work list is built in pair mode)

@@ -198,7 +198,7 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     return st;
 }
 
-static attn_status forward(int mode, const void* q, const void* k, const void* v, const attn_qtensor* qq,
+static attn_status forward(int mode, int expm, const void* q, const void* k, const void* v, const attn_qtensor* qq,
                            const attn_qtensor* qk, const attn_qtensor* qv, const attn_shape* shape, int causal,
                            int exact, float softmax_scale, int rotated, void* o, float* lse, void* workspace,
                            cudaStream_t stream) {
@@ -309,7 +309,7 @@ static attn_status forward(int mode, const void* q, const void* k, const void* v
     }
     const int grid = attn_device_sm_count();
     if (grid < 1) return ATTN_ERR_CUDA;
-    e = launch_attn(mode, d, q, k, v, fp, grid, stream);
+    e = launch_attn(mode, expm, d, q, k, v, fp, grid, stream);
     return e == cudaSuccess ? ATTN_OK : (e == cudaErrorInvalidValue ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA);
 }
 
@@ -320,7 +320,23 @@ attn_status attn_fp8_fwd(const attn_qtensor* q, const attn_qtensor* k, const att
     attn_status st = pa::fp8_fwd_check(q, k, v, shape, causal, causal_exact, softmax_scale, o, lse, true, workspace,
                                        workspace_bytes, &mode);
     if (st != ATTN_OK) return st;
-    return forward(mode, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
+    return forward(mode, ATTN_EXP_HW, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
+                   softmax_scale, q->rotated, o, lse, workspace, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fp8_fwd_ex(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
+                            const attn_shape* shape, int32_t causal, int32_t causal_exact, float softmax_scale,
+                            int32_t exp_mode, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    int mode = 0;
+    attn_status st = pa::fp8_fwd_check(q, k, v, shape, causal, causal_exact, softmax_scale, o, lse, true, workspace,
+                                       workspace_bytes, &mode);
+    if (st != ATTN_OK) return st;
+    if (exp_mode < ATTN_EXP_HW || exp_mode > ATTN_EXP_MITCHELL_P) return ATTN_ERR_INVALID_ARG;
+    // the bit-level exponentials: the pair kernel's E4M3 tile and MX paths (inference)
+    if (exp_mode != ATTN_EXP_HW && (shape->head_dim != 128 || (mode != 1 && mode != 3)))
+        return ATTN_ERR_UNSUPPORTED;
+    return forward(mode, exp_mode, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
                    softmax_scale, q->rotated, o, lse, workspace, static_cast<cudaStream_t>(stream));
 }
 
@@ -334,7 +350,7 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
         return ATTN_ERR_INVALID_ARG;
     if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
     if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
-    return forward(0, q, k, v, nullptr, nullptr, nullptr, shape, causal != 0, 0, softmax_scale, 0, o, lse,
+    return forward(0, ATTN_EXP_HW, q, k, v, nullptr, nullptr, nullptr, shape, causal != 0, 0, softmax_scale, 0, o, lse,
                    workspace, static_cast<cudaStream_t>(stream));
 }
 

@@ -91,8 +91,9 @@ cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t st);
 cudaError_t launch_vref(const VrefParams& p, cudaStream_t st);
 // mode: 0 bf16, 1 E4M3 with one scale per tile, 2 E4M3 per-column scales, 3 MXFP8,
-// 4 MXFP8 Q and K with one V exponent per token (the causal-exact MX mode)
-cudaError_t launch_attn(int mode, int D, const void* q, const void* k, const void* v, const FwdParams& p, int grid,
-                        cudaStream_t st);
+// 4 MXFP8 Q and K with one V exponent per token (the causal-exact MX mode); expm: the
+// probabilities' exponential (attn_exp_mode; the bit-level ones with modes 1 and 3 at D = 128)
+cudaError_t launch_attn(int mode, int expm, int D, const void* q, const void* k, const void* v, const FwdParams& p,
+                        int grid, cudaStream_t st);
 
 }  // namespace pa

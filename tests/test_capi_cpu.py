@@ -151,6 +151,41 @@ def test_seed_mismatch_and_layout_rules_on_host(pa):
                           fake, fake, fake, big, None) == pa.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses placeholder device pointers; only run where no GPU could be reached")
+def test_exp_mode_rules_on_host(pa):
+    """attn_fp8_fwd_ex: an exp_mode outside the enum is an invalid argument; the
+    bit-level modes are refused (unsupported) with causal-exact, per-column E4M3
+    blocks, per-token MX V or head_dim 64 -- all before any device call."""
+    L = pa.lib()
+    fake = 1 << 20
+
+    def call(q, k, v, shape, causal, exact, mode):
+        ws = pa.attn_workspace_size(shape.total_tokens, shape.heads, shape.head_dim, 1)
+        return L.attn_fp8_fwd_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shape), causal,
+                                 exact, 0.0, mode, fake, fake, fake, ws, None)
+
+    s128 = pa._Shape(256, 2, 128, 1, None)
+    e = pa._QT(fake, fake, 0, 128, 0, 1, 7)
+    ev = pa._QT(fake, fake, 0, 128, 0, 0, 0)
+    assert call(e, e, ev, s128, 0, 0, 3) == pa.ATTN_ERR_INVALID_ARG
+    assert call(e, e, ev, s128, 0, 0, -1) == pa.ATTN_ERR_INVALID_ARG
+    e1 = pa._QT(fake, fake, 0, 1, 0, 1, 7)
+    e1v = pa._QT(fake, fake, 0, 1, 0, 0, 0)
+    assert call(e1, e1, e1v, s128, 1, 1, pa.ATTN_EXP_SCHRAUDOLPH) == pa.ATTN_ERR_UNSUPPORTED   # causal-exact
+    e64 = pa._QT(fake, fake, 0, 64, 0, 1, 7)
+    e64v = pa._QT(fake, fake, 0, 64, 0, 0, 0)
+    assert call(e64, e64, e64v, s128, 0, 0, pa.ATTN_EXP_MITCHELL_P) == pa.ATTN_ERR_UNSUPPORTED  # blocks < tile
+    s64 = pa._Shape(256, 2, 64, 1, None)
+    assert call(e, e, ev, s64, 0, 0, pa.ATTN_EXP_SCHRAUDOLPH) == pa.ATTN_ERR_UNSUPPORTED        # head_dim 64
+    m = pa._QT(fake, fake, 1, 32, 0, 1, 7)
+    mtok = pa._QT(fake, fake, 3, 1, 0, 0, 0)
+    assert call(m, m, mtok, s128, 1, 0, pa.ATTN_EXP_MITCHELL_P) == pa.ATTN_ERR_UNSUPPORTED      # per-token V
+    # the other checks keep their order: a small workspace is still reported first
+    assert L.attn_fp8_fwd_ex(ctypes.byref(e), ctypes.byref(e), ctypes.byref(ev), ctypes.byref(s128), 0, 0, 0.0,
+                             pa.ATTN_EXP_SCHRAUDOLPH, fake, fake, fake, 16, None) == pa.ATTN_ERR_WORKSPACE
+
+
 def test_test_build_exports_the_probability_dump_and_the_timed_library_does_not(pa):
     """libpa_gb300_pdump.so (include/attn_pdump.h) is the parity tests' build: it
     exports every call of include/attn.h plus attn_pdump_set; the library that

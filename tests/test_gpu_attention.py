@@ -149,17 +149,31 @@ def test_mx_causal_exact_rows_unchanged_by_later_tokens():
     assert not torch.equal(a[cut + 1:].view(torch.int16), b[cut + 1:].view(torch.int16))
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bf16_forward_against_fp64(oracle_mod, causal):
+def test_bf16_forward_against_fp64(oracle_mod, causal, d):
+    """The BF16 comparator against O-1, element by element, at the bound its two
+    roundings give: each probability rounds to bf16 (relative error <= 2^-8 with
+    7 stored mantissa bits) while the row sum keeps the fp32 values, so
+    |dO_c| <= 2^-8 sum_k w_k |v_kc| (w the exact softmax weights); the output
+    rounds to bf16, another 2^-8 |O_c|. Everything else (fp32 scores and
+    accumulation, the fp32 exp2's ~2^-22) stays below 1e-5 here. lse is formed
+    in fp32 from the unrounded sum: within 2e-5 + 2^-20 |lse|."""
     inp = workloads.make(2, heads=2, lengths=[300, 77, 129])
+    if d == 64:
+        inp.q, inp.k, inp.v = (np.ascontiguousarray(x[..., :64]) for x in (inp.q, inp.k, inp.v))
     q, k, v, cu = to_device(inp)
     o, lse = pa.attn_bf16_fwd(q, k, v, cu, causal)
     o1, l1 = oracle.attention_fp64(inp.q, inp.k, inp.v, inp.cu_seqlens, causal)
+    oabs, _ = oracle.attention_fp64(inp.q, inp.k, np.abs(inp.v), inp.cu_seqlens, causal)
     og = o.float().cpu().numpy()
-    rel = np.linalg.norm(og - o1) / np.linalg.norm(o1)
-    # BF16 P and BF16 output rounding: a few 2^-9 relative
-    assert rel < 6e-3, rel
-    assert np.abs(lse.cpu().numpy() - l1).max() < 2e-3
+    bound = 2.0 ** -8 * (oabs + np.abs(o1)) + 1e-5
+    err = np.abs(og - o1)
+    assert np.all(err <= bound), float(np.max(err / bound))
+    # the bound is not loose by orders of magnitude: the worst element uses a fair share of it
+    assert np.max(err / bound) > 0.05
+    lg = lse.cpu().numpy()
+    assert np.all(np.abs(lg - l1) <= 2e-5 + 2.0 ** -20 * np.abs(l1)), float(np.max(np.abs(lg - l1)))
 
 
 def test_fp8_rmse_against_fp64_reported(oracle_mod):

@@ -11,6 +11,8 @@ code on the other side of that boundary; keys a row does not see must hold 0
 -- and the output is then compared with the emulation recomputed from the
 device's codes under the plain bounds, with no tie allowance: relative RMSE
 <= 1e-3, per element |diff| <= max(2e-3, one BF16 ulp), lse within 1e-3.
+The same check covers the bit-level exponentials (Schraudolph's form and the
+log-domain P codes), whose emulation mirrors the codes they define.
 
 Sources: "Fused attention kernel", Implementation sketch (the running softmax)
 and 8-bit forward pass (P cast to e4m3 before the P V product);
@@ -59,17 +61,18 @@ def key_stride(cu):
     return max(128, (L + 127) // 128 * 128)
 
 
-def check_given_codes(inp, mx, block, causal, exact=False, rows=None):
+def check_given_codes(inp, mx, block, causal, exact=False, rows=None, exp_mode=0):
     (Q, K, V), (Qo, Ko, Vo), cu = quantise_both(inp, mx, block)
-    o_ref, l_ref = pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0)
+    o_ref, l_ref = pa.attn_fp8_fwd_ex(Q, K, V, cu, causal, exact, 0.0, exp_mode)
     ks = key_stride(inp.cu_seqlens)
-    o, lse, codes = pa.attn_fp8_fwd_pdump(Q, K, V, cu, ks, causal, exact)
+    o, lse, codes = pa.attn_fp8_fwd_pdump(Q, K, V, cu, ks, causal, exact, exp_mode=exp_mode)
     torch.cuda.synchronize()
     # the test build computes the same output bit for bit
     assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(lse, l_ref)
     _, ob, le, counts = oracle.attention_emulate_given_p(Qo, Ko, Vo, codes.cpu().numpy(), inp.cu_seqlens, causal,
                                                          exact, None, rows=rows,
-                                                         rescale_tau=pa.rescale_threshold(inp.q.shape[2]))
+                                                         rescale_tau=pa.rescale_threshold(inp.q.shape[2]),
+                                                         exp_mode=exp_mode)
     assert counts["wrong"] == 0 and counts["masked_nonzero"] == 0, counts
     res = compare_outputs(o, lse, ob, le, rows=rows)
     assert res["ok"], (res, counts)
@@ -111,3 +114,32 @@ def test_long_documents_with_causal_first_rows(oracle_mod, wid, mx, causal, exac
                                      rng.choice(T, 160, replace=False)])).astype(np.int32)
     block = (1 if exact else 32) if mx else (1 if exact else 128)
     check_given_codes(inp, mx, block, causal, exact, rows=rows)
+
+
+# the bit-level exponentials (FLAMIA sections 1, 4.3, 4.4): Schraudolph's fp32
+# form and the log-domain P codes, on the E4M3 tile and MX paths
+BITEXP_CASES = [
+    (2, [300, 77, 129], False, 128, False),
+    (3, [300, 77, 129], False, 128, True),
+    (4, [300, 77, 129], True, 32, False),
+    (5, [300, 77, 129, 1], True, 32, True),
+]
+
+
+@pytest.mark.parametrize("exp_mode", [1, 2], ids=["schraudolph", "mitchell_p"])
+@pytest.mark.parametrize("wid,lengths,mx,block,causal", BITEXP_CASES)
+def test_bit_level_exponentials_codes_and_output(oracle_mod, wid, lengths, mx, block, causal, exp_mode):
+    inp = workloads.make(wid, heads=2, lengths=lengths)
+    res, counts = check_given_codes(inp, mx, block, causal, exp_mode=exp_mode)
+    assert counts["same"] > 0.99 * (counts["same"] + counts["tie_other"])
+
+
+@pytest.mark.parametrize("exp_mode", [1, 2], ids=["schraudolph", "mitchell_p"])
+@pytest.mark.parametrize("wid,mx,causal", [(2, False, False), (5, True, True)])
+def test_bit_level_exponentials_long_documents(oracle_mod, wid, mx, causal, exp_mode):
+    inp = workloads.make(wid, heads=4, lengths=[2048, 2048])
+    rng = np.random.default_rng(200 + wid)
+    T = inp.T
+    rows = np.unique(np.concatenate([np.arange(0, 96), np.arange(2048, 2144), np.array([127, 128, 2047, T - 1]),
+                                     rng.choice(T, 160, replace=False)])).astype(np.int32)
+    check_given_codes(inp, mx, 32 if mx else 128, causal, rows=rows, exp_mode=exp_mode)
