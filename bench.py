@@ -298,7 +298,7 @@ def gpu_arm(args, rank, world, local_rank):
     args.world = world
     w = workloads.WORKLOADS[args.workload]
     r = time_workload(args, pa, torch, dev, args.workload, bool(args.exact), args.steps, args.warmup,
-                      clocks_idx=local_rank, keep=True)
+                      clocks_idx=local_rank, keep=True, exp_mode=EXP_MODES[args.exp_mode])
     T, H, d, nd = r["T"], r["H"], r["d"], r["nd"]
     q_h, k_h, v_h, cu, ws, Q, K, V = (r[x] for x in ("q_h", "k_h", "v_h", "cu", "ws", "Q", "K", "V"))
     lq, lk, lv, blk, rot, seed, stream = (r[x] for x in ("lq", "lk", "lv", "blk", "rot", "seed", "stream"))
@@ -347,7 +347,8 @@ def gpu_arm(args, rank, world, local_rank):
             pa.attn_quantize(qi, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
             pa.attn_quantize(ki, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
             pa.attn_quantize(vi, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
-            pa.attn_fp8_fwd(Q, K, V, cu, causal, exact, 0.0, ws=ws, out=oi, lse=li, stream=stream)
+            pa.attn_fp8_fwd_ex(Q, K, V, cu, causal, exact, 0.0, EXP_MODES[args.exp_mode], ws=ws, out=oi, lse=li,
+                               stream=stream)
             comp_done[b].record(stream)
             used[b] = True
             d2h_s.wait_event(comp_done[b])
@@ -395,7 +396,8 @@ def gpu_arm(args, rank, world, local_rank):
     r.update({"ms_step": ms_step, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "acc": acc, "bf16": bf16})
     # the other benchmark configurations, timed in this process (rank 0, N = 1 only)
     r["per_workload"] = None
-    if rank == 0 and world == 1 and not args.no_per_workload and args.heads is None and args.seqlen is None:
+    if (rank == 0 and world == 1 and not args.no_per_workload and args.heads is None and args.seqlen is None
+            and args.exp_mode == "hw"):
         per = {}
         for wid, ex in ((2, False), (3, False), (3, True), (4, False), (5, False), (5, True)):
             if wid == args.workload and ex == bool(args.exact):
@@ -510,7 +512,7 @@ def cpu_sample(args, inp=None, budget_s=15.0, rows=None):
             K = oracle.quantize_tensor(k, c1, E4M3, b, not args.no_rotate, w.hadamard_seed)
             V = oracle.quantize_tensor(v, c1, E4M3, b, False, 0)
         oracle.attention_emulate(Q, K, V, c1, w.causal, bool(args.exact), None, rows=row_idx,
-                                 rescale_tau=0.75 if d == 128 else 0.0)
+                                 rescale_tau=0.75 if d == 128 else 0.0, exp_mode=EXP_MODES[args.exp_mode])
         t_total += time.perf_counter() - t0
         nkeys = np.arange(1, R + 1) if w.causal else np.full(R, L0)
         flops += float(4.0 * d * nkeys.sum())
@@ -546,10 +548,14 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# the probabilities' exponential (include/attn.h attn_exp_mode)
+EXP_MODES = {"hw": 0, "schraudolph": 1, "mitchell_p": 2}
+
+
 def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
-            "causal": w.causal, "causal_exact": bool(args.exact),
+            "causal": w.causal, "causal_exact": bool(args.exact), "exp_mode": args.exp_mode,
             "quant": (("MXFP8 (E8M0 per 32; V one E8M0 per token, causal-exact)" if args.exact else "MXFP8 (E8M0 per 32)")
                       if w.mx else
                       ("E4M3 one scale per token (causal-exact)" if args.exact else f"E4M3 blocks of {w.block} tokens")) +
@@ -572,6 +578,8 @@ def main():
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
     ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")
+    ap.add_argument("--exp-mode", default="hw", choices=sorted(EXP_MODES),
+                    help="the probabilities' exponential: the hardware exp2 (default), Schraudolph's, or log-domain P")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip timing the other benchmark configurations in the same process")
     args = ap.parse_args()
