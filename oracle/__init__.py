@@ -29,7 +29,7 @@ _HDR = os.path.join(_HERE, "attn_oracle.h")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-E4M3_TOKBLOCK, MX_ROW32, MX_COL32, MX_TOKEN = 0, 1, 2, 3
+E4M3_TOKBLOCK, MX_ROW32, MX_COL32, MX_TOKEN, NVFP4 = 0, 1, 2, 3, 4
 MX_RULE_NOSAT, MX_RULE_OCP_FLOOR = 0, 1
 QUANTIZE_P = 1
 # the probabilities' exponential (emulation flags): 2^x, Schraudolph's, log-domain P (Mitchell)
@@ -72,6 +72,10 @@ def lib():
             L.or_e4m3_decode.restype = dbl
             L.or_e4m3_encode.argtypes = [ctypes.c_float]
             L.or_e4m3_encode.restype = ctypes.c_uint8
+            L.or_e2m1_decode.argtypes = [ctypes.c_uint8]
+            L.or_e2m1_decode.restype = dbl
+            L.or_e2m1_encode.argtypes = [ctypes.c_float]
+            L.or_e2m1_encode.restype = ctypes.c_uint8
             L.or_e8m0_exponent.argtypes = [ctypes.c_float, i32]
             L.or_e8m0_exponent.restype = i32
             L.or_bf16_rne.argtypes = [ctypes.c_float]
@@ -126,6 +130,18 @@ def threads() -> int:
 def e4m3_decode_table() -> np.ndarray:
     L = lib()
     return np.array([L.or_e4m3_decode(i) for i in range(256)], dtype=np.float64)
+
+
+def e2m1_decode_table() -> np.ndarray:
+    L = lib()
+    return np.array([L.or_e2m1_decode(i) for i in range(16)], dtype=np.float64)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    L = lib()
+    out = np.array([L.or_e2m1_encode(ctypes.c_float(v)) for v in x.ravel()], dtype=np.uint8)
+    return out.reshape(x.shape)
 
 
 def e4m3_encode(x) -> np.ndarray:
@@ -185,12 +201,14 @@ def quantize(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, 
 
     scales: E4M3 token blocks -> fp32 [H, NB]; MX row32 -> u8 [T, H, d/32];
     MX col32 -> u8 [H, NG, d] (NG = document-local 32-token groups); MX token ->
-    u8 [H, T] (one exponent per token and head over all d).
+    u8 [H, T] (one exponent per token and head over all d); NVFP4 -> the pair
+    (fp32 [H, NB] per 128-token block, u8 [T, H, d/16] E4M3 scales), codes
+    u8 [T, H, d/2] with two E2M1 codes per byte (even channel low).
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     T, H, d = x.shape
     cu, nd = _cu(cu_seqlens, T)
-    codes = np.zeros((T, H, d), dtype=np.uint8)
+    codes = np.zeros((T, H, d // 2 if layout == NVFP4 else d), dtype=np.uint8)
     sf = su = None
     if layout == E4M3_TOKBLOCK:
         sf = np.zeros((H, num_blocks(cu, T, block)), dtype=np.float32)
@@ -200,10 +218,15 @@ def quantize(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, 
         su = np.zeros((H, num_blocks(cu, T, 32), d), dtype=np.uint8)
     elif layout == MX_TOKEN:
         su = np.zeros((H, T), dtype=np.uint8)
+    elif layout == NVFP4:
+        sf = np.zeros((H, num_blocks(cu, T, 128)), dtype=np.float32)
+        su = np.zeros((T, H, d // 16), dtype=np.uint8)
     else:
         raise ValueError(layout)
     st = lib().or_quantize(x.ctypes.data, T, H, d, _ptr(cu), nd, layout, block, int(bool(rotate)),
                            seed & (2**64 - 1), mx_rule, codes.ctypes.data, _ptr(sf), _ptr(su))
+    if layout == NVFP4:
+        return codes, (sf, su), st
     return codes, (sf if sf is not None else su), st
 
 
@@ -215,14 +238,19 @@ class QTensor:
         self.rotated, self.seed = rotated, seed
 
     def _qt(self):
-        sf = self.scales if self.layout == E4M3_TOKBLOCK else None
-        su = self.scales if self.layout != E4M3_TOKBLOCK else None
+        if self.layout == NVFP4:
+            sf, su = self.scales
+        else:
+            sf = self.scales if self.layout == E4M3_TOKBLOCK else None
+            su = self.scales if self.layout != E4M3_TOKBLOCK else None
         return _QT(self.codes.ctypes.data, self.layout, self.block, _ptr(sf), _ptr(su))
 
 
 def quantize_tensor(x, cu_seqlens=None, layout=E4M3_TOKBLOCK, block=128, rotate=False, seed=0,
                     mx_rule=MX_RULE_NOSAT) -> QTensor:
     codes, scales, st = quantize(x, cu_seqlens, layout, block, rotate, seed, mx_rule)
+    if st == 1:
+        raise ValueError("oracle quantiser rejected its arguments")
     if st != 0:
         raise FloatingPointError(f"oracle quantiser status {st}")
     return QTensor(codes, scales, layout, block, rotate, seed)
@@ -232,7 +260,14 @@ def dequantize(qt: QTensor, cu_seqlens=None) -> np.ndarray:
     """Decoded values code * scale in fp64 (rotation not undone)."""
     dec = e4m3_decode_table()
     T, H, d = qt.codes.shape
-    v = dec[qt.codes]
+    if qt.layout == NVFP4:
+        d = 2 * d
+        e2 = e2m1_decode_table()
+        lo, hi = e2[qt.codes & 15], e2[qt.codes >> 4]
+        v = np.stack([lo, hi], axis=-1).reshape(T, H, d) * np.repeat(dec[qt.scales[1]], 16, axis=2)
+        qt = QTensor(qt.codes, qt.scales[0], E4M3_TOKBLOCK, 128)
+    else:
+        v = dec[qt.codes]
     cu, nd = _cu(cu_seqlens, T)
     starts = np.zeros(T, dtype=np.int64)
     docs = np.zeros(T, dtype=np.int64)
@@ -316,6 +351,8 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
     key tile's maximum exceeds it by more than this (log2 units; 0 = exact).
     exp_mode: EXP_HW (2^x), EXP_SCHRAUDOLPH or EXP_MITCHELL_P."""
     T, H, d = q.codes.shape
+    if q.layout == NVFP4:
+        d *= 2                                         # two E2M1 codes per byte
     if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
         raise ValueError("Q and K must carry the same rotation")
     cu, nd = _cu(cu_seqlens, T)
@@ -349,6 +386,8 @@ def attention_emulate_given_p(q: QTensor, k: QTensor, v: QTensor, p_codes: np.nd
     the emulation's own, keys whose device code is the other faithful code of a
     tie, keys with any other code, and unseen keys with a non-zero code."""
     T, H, d = q.codes.shape
+    if q.layout == NVFP4:
+        d *= 2                                         # two E2M1 codes per byte
     if q.rotated != k.rotated or (q.rotated and q.seed != k.seed):
         raise ValueError("Q and K must carry the same rotation")
     pc = np.ascontiguousarray(p_codes, dtype=np.uint8)

@@ -101,6 +101,33 @@ uint8_t or_e4m3_encode(float x) {
     return sign | (uint8_t)code;
 }
 
+/* E2M1, the element format of NVFP4 (FLAMIA section 2: NVFP4 blocks of 16
+ * elements; the OCP 4-bit floating point definition is taken): sign, 2
+ * exponent bits with bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6; no infinities or NaN. */
+double or_e2m1_decode(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* Nearest magnitude, ties to the even code (mantissa bit 0); beyond 6 and
+ * infinities saturate to 6 (satfinite); the sign is kept, zero included;
+ * NaN -> 0x7 (the format has none; a quantiser block holding one is reported). */
+uint8_t or_e2m1_encode(float x) {
+    if (isnan(x)) return 0x7;
+    uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    double a = fabs((double)x);
+    if (a >= 6.0) return sign | 0x7;
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (uint8_t c = 0; c < 8; c++) {
+        double dd = fabs(a - or_e2m1_decode(c));
+        if (dd < bd || (dd == bd && (c & 1) == 0)) { bd = dd; best = c; }
+    }
+    return sign | best;
+}
+
 void or_e4m3_encode_range(uint64_t start, uint64_t count, uint8_t* out) {
     for (uint64_t i = 0; i < count; i++) {
         uint32_t bits = (uint32_t)(start + i);
@@ -331,6 +358,63 @@ static void quant_mxtok_unit(void* vc, long t) {
     }
 }
 
+/* NVFP4 (Q and K of the mixed NVFP4/FP8 path; FLAMIA sections 1 and 2:
+ * 16-element blocks with a shared scale plus a tensor-level scale, NVFP4 for
+ * Q K^T and 8-bit operands elsewhere). Readings: the tensor-level scale is
+ * kept per document-local 128-token block and head (the token-block scaling
+ * the pages reuse, document-local like every other scale here), fp32
+ * s_t = amax / (448 * 6); each 16-channel group of a row takes the E4M3 scale
+ * sf = E4M3(max |z|) with z = fl32(y * fl32(448 / amax)) (the same form as the
+ * E4M3 token-block codes), and its codes e = E2M1(fl32(z * fl32(6 / dec(sf)))),
+ * zero when sf decodes to 0. Value = e2m1(e) * dec(sf) * s_t. Unit =
+ * (document, head). */
+static void quant_nvfp4_unit(void* vc, long u) {
+    quant_ctx* c = (quant_ctx*)vc;
+    int doc = (int)(u / c->H), h = (int)(u % c->H);
+    int s = c->D.cu[doc], L = c->D.cu[doc + 1] - s, d = c->d;
+    long boff = block_offset(&c->D, doc, 128);
+    long NB = block_offset(&c->D, c->D.nd, 128);
+    float* y = (float*)malloc(sizeof(float) * 128 * (size_t)d);
+    for (int blk = 0; blk * 128 < L; blk++) {
+        int n = L - blk * 128 < 128 ? L - blk * 128 : 128;
+        float amax = 0.0f;
+        for (int r = 0; r < n; r++) {
+            rotated_row(c, s + blk * 128 + r, h, y + (long)r * d);
+            for (int j = 0; j < d; j++) {
+                float a = fabsf(y[(long)r * d + j]);
+                if (!(a <= amax)) amax = a;
+            }
+        }
+        float st, inv;
+        if (!isfinite(amax)) { __atomic_store_n(&c->err, OR_ERR_NONFINITE, __ATOMIC_RELAXED); st = NAN; inv = 0.0f; }
+        else if (amax == 0.0f) { st = 0.0f; inv = 0.0f; }
+        else { inv = 448.0f / amax; st = amax / 2688.0f; }
+        c->sf[(long)h * NB + boff + blk] = st;
+        for (int r = 0; r < n; r++) {
+            long t = s + blk * 128 + r;
+            uint8_t* dst = c->codes + (t * c->H + h) * (d / 2);
+            for (int g = 0; g < d / 16; g++) {
+                float z[16], gmax = 0.0f;
+                for (int i = 0; i < 16; i++) {
+                    z[i] = y[(long)r * d + 16 * g + i] * inv;
+                    float a = fabsf(z[i]);
+                    if (!(a <= gmax)) gmax = a;
+                }
+                uint8_t sf = or_e4m3_encode(gmax);
+                c->su[(t * c->H + h) * (d / 16) + g] = sf;
+                double sv = or_e4m3_decode(sf);
+                float rr = sv > 0.0 ? 6.0f / (float)sv : 0.0f;
+                for (int i = 0; i < 16; i += 2) {
+                    uint8_t lo = sv > 0.0 ? or_e2m1_encode(z[i] * rr) : 0;
+                    uint8_t hi = sv > 0.0 ? or_e2m1_encode(z[i + 1] * rr) : 0;
+                    dst[8 * g + i / 2] = (uint8_t)(lo | (hi << 4));
+                }
+            }
+        }
+    }
+    free(y);
+}
+
 int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
                 int layout, int block, int rotate, uint64_t seed, int mx_rule,
                 uint8_t* codes, float* scales_f32, uint8_t* scales_u8) {
@@ -338,6 +422,7 @@ int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
     if (layout == OR_E4M3_TOKBLOCK && (block < 1 || !scales_f32)) return OR_ERR_ARG;
     if ((layout == OR_MX_ROW32 || layout == OR_MX_COL32) && (d % 32 || !scales_u8)) return OR_ERR_ARG;
     if (layout == OR_MX_TOKEN && !scales_u8) return OR_ERR_ARG;
+    if (layout == OR_NVFP4 && (d % 16 || block != 128 || !scales_f32 || !scales_u8)) return OR_ERR_ARG;
     quant_ctx c;
     memset(&c, 0, sizeof(c));
     c.x = x; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
@@ -348,6 +433,7 @@ int or_quantize(const float* x, int T, int H, int d, const int32_t* cu, int nd,
     else if (layout == OR_MX_ROW32) parallel_for(T, quant_mxrow_unit, &c);
     else if (layout == OR_MX_COL32) parallel_for((long)c.D.nd * H, quant_mxcol_unit, &c);
     else if (layout == OR_MX_TOKEN) parallel_for(T, quant_mxtok_unit, &c);
+    else if (layout == OR_NVFP4) parallel_for((long)c.D.nd * H, quant_nvfp4_unit, &c);
     else { free(c.D.cu); return OR_ERR_ARG; }
     free(c.D.cu);
     return c.err;
@@ -590,6 +676,11 @@ typedef struct {
 /* dequantised element: code value, times 2^X for the MX layouts (the E4M3
  * layouts return the bare code value; their scale is applied per block) */
 static double hat(const emu_ctx* c, const or_qtensor* x, int t, int h, int j, long ng) {
+    if (x->layout == OR_NVFP4) {   /* e2m1 code times its 16-channel E4M3 scale (s_t enters with cf) */
+        uint8_t b = x->codes[((long)t * c->H + h) * (c->d / 2) + j / 2];
+        uint8_t e = (j & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 15);
+        return or_e2m1_decode(e) * c->dec[x->scales_u8[((long)t * c->H + h) * (c->d / 16) + j / 16]];
+    }
     uint8_t code = x->codes[((long)t * c->H + h) * c->d + j];
     double v = c->dec[code];
     if (x->layout == OR_MX_ROW32) {
@@ -825,6 +916,11 @@ static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v
         return OR_ERR_ARG;
     int mxq = q->layout == OR_MX_ROW32, mxk = k->layout == OR_MX_ROW32;
     if (mxq != mxk) return OR_ERR_ARG;
+    /* NVFP4 Q K^T (the mixed path): both NVFP4 with 128-token s_t blocks, an E4M3 V, not exact */
+    int nvq = q->layout == OR_NVFP4, nvk = k->layout == OR_NVFP4;
+    if (nvq != nvk || v->layout == OR_NVFP4) return OR_ERR_ARG;
+    if (nvq && (q->block != 128 || k->block != 128 || v->layout != OR_E4M3_TOKBLOCK || exact || d % 16))
+        return OR_ERR_ARG;
     if (q->layout == OR_MX_COL32 || k->layout == OR_MX_COL32 || v->layout == OR_MX_ROW32) return OR_ERR_ARG;
     if (exact && (!causal || !((v->layout == OR_E4M3_TOKBLOCK && v->block == 1) || v->layout == OR_MX_TOKEN)))
         return OR_ERR_ARG;

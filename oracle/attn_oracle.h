@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-enum { OR_E4M3_TOKBLOCK = 0, OR_MX_ROW32 = 1, OR_MX_COL32 = 2, OR_MX_TOKEN = 3 };
+enum { OR_E4M3_TOKBLOCK = 0, OR_MX_ROW32 = 1, OR_MX_COL32 = 2, OR_MX_TOKEN = 3, OR_NVFP4 = 4 };
 enum { OR_MX_RULE_NOSAT = 0, OR_MX_RULE_OCP_FLOOR = 1 };
 enum { OR_OK = 0, OR_ERR_ARG = 1, OR_ERR_NONFINITE = 5 };
 
@@ -46,6 +46,8 @@ int or_threads(void);
 /* ---- number formats ---- */
 double   or_e4m3_decode(uint8_t code);
 uint8_t  or_e4m3_encode(float x);
+double   or_e2m1_decode(uint8_t code);   /* low 4 bits: sign, 2 exponent bits (bias 1), 1 mantissa bit */
+uint8_t  or_e2m1_encode(float x);        /* nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to even, beyond 6 -> 6 */
 int      or_e8m0_exponent(float amax, int rule);   /* unbiased X; byte = X + 127 */
 uint16_t or_bf16_rne(float x);
 void     or_e4m3_encode_range(uint64_t start, uint64_t count, uint8_t* out); /* bit patterns start.. */
@@ -65,6 +67,10 @@ long     or_num_blocks(const int32_t* cu_seqlens, int num_docs, int total_tokens
  * E4M3 token blocks : scales_f32 [H][NB], NB = or_num_blocks(.., block)
  * MX row32 (Q, K)   : scales_u8  [T][H][d/32] (biased E8M0 bytes)
  * MX col32 (V)      : scales_u8  [H][NG][d], NG = or_num_blocks(.., 32)
+ * NVFP4 (Q, K)      : codes [T][H][d/2] (two E2M1 codes per byte, the even
+ *                     channel in the low nibble); scales_f32 [H][NB] (fp32
+ *                     scale per document-local 128-token block, block = 128);
+ *                     scales_u8 [T][H][d/16] (E4M3 scale per 16 channels)
  */
 int or_quantize(const float* x, int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
                 int layout, int block, int rotate, uint64_t seed, int mx_rule,
