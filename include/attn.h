@@ -127,8 +127,23 @@ typedef enum { ATTN_IN_F32 = 0, ATTN_IN_BF16 = 1 } attn_in_dtype;
  * ATTN_MX_TOKEN (V of the causal-exact MX mode): MXFP8 codes with one E8M0
  *   exponent per (token, head) over all head_dim channels, so that no scale
  *   depends on another token; code = E4M3(x * 2^-X). Scales array: bytes
- *   [heads][T + num_docs], the token t (global index) at column t. */
-typedef enum { ATTN_E4M3_TOKBLOCK = 0, ATTN_MX_ROW32 = 1, ATTN_MX_COL32 = 2, ATTN_MX_TOKEN = 3 } attn_layout;
+ *   [heads][T + num_docs], the token t (global index) at column t.
+ * ATTN_NVFP4 (Q, K of the mixed NVFP4/FP8 path; head_dim 128, block 128):
+ *   E2M1 codes, two per byte (the even channel in the low nibble), codes
+ *   array [T][H][head_dim / 2]; an fp32 scale s_t = amax / (448 * 6) per
+ *   (document, head, 128-token block) and an E4M3 scale per (token, head, 16
+ *   consecutive channels): sf = E4M3(max |z|) with z = x * (448 / amax) over
+ *   the 16 channels, code = E2M1(z * (6 / sf)) (0 where sf is 0); value =
+ *   code * sf * s_t. Scales array: fp32 [heads][nt_cap] (block t of document
+ *   i at toff_i + t, as the MX tiles), then, from byte offset
+ *   ceil(heads * nt_cap * 4 / 1024) * 1024, bytes [heads][nt_cap][1024]: two
+ *   512-byte tiles per 128-token block (channels 0..63, 64..127) in the MX
+ *   tile order, row r (the token 128 t + r) and group g (16 channels) at
+ *   byte (r % 32) * 16 + (r / 32) * 4 + g; rows past the document end hold 0.
+ *   (FLAMIA sections 1 and 2: NVFP4 = 16-element blocks plus a tensor-level
+ *   scale, here kept per document-local 128-token block.) */
+typedef enum { ATTN_E4M3_TOKBLOCK = 0, ATTN_MX_ROW32 = 1, ATTN_MX_COL32 = 2, ATTN_MX_TOKEN = 3,
+               ATTN_NVFP4 = 4 } attn_layout;
 
 /* E8M0 exponent rule: NOSAT = smallest X with amax <= 448 * 2^X (nothing
  * saturates; default); OCP_FLOOR = floor(log2 amax) - 8 (values above

@@ -36,7 +36,7 @@ ATTN_ERR_BAD_SEQLENS = 7
 ATTN_ERR_WORKSPACE = 8
 
 ATTN_IN_F32, ATTN_IN_BF16 = 0, 1
-ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32, ATTN_MX_TOKEN = 0, 1, 2, 3
+ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32, ATTN_MX_COL32, ATTN_MX_TOKEN, ATTN_NVFP4 = 0, 1, 2, 3, 4
 ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 # include/attn.h: the FP8 forward at head_dim 128 moves a row's reference maximum
 # only by more than this (log2 units); the other paths use the exact running max
@@ -206,6 +206,9 @@ class QTensor:
 def empty_qtensor(T: int, H: int, d: int, num_docs: int, layout: int, block: int,
                   mx_rule: int = ATTN_MX_RULE_NOSAT, device="cuda") -> QTensor:
     cb, sb = attn_quantize_sizes(T, H, d, num_docs, layout, block)
+    if layout == ATTN_NVFP4:   # two E2M1 codes per byte; scales: one byte buffer (see nvfp4_scales)
+        return QTensor(torch.empty((T, H, d // 2), dtype=torch.uint8, device=device),
+                       torch.empty((sb,), dtype=torch.uint8, device=device), layout, block, mx_rule)
     codes = torch.empty((T, H, d), dtype=torch.uint8, device=device)
     if layout == ATTN_E4M3_TOKBLOCK:
         scales = torch.empty((H, sb // (4 * H)), dtype=torch.float32, device=device)
@@ -214,6 +217,17 @@ def empty_qtensor(T: int, H: int, d: int, num_docs: int, layout: int, block: int
     else:
         scales = torch.empty((H, sb // (512 * H), 512), dtype=torch.uint8, device=device)
     return QTensor(codes, scales, layout, block, mx_rule)
+
+
+def nvfp4_scales(qt: QTensor, num_docs: int):
+    """Views of an ATTN_NVFP4 scales buffer (include/attn.h): the fp32 block scales
+    [H, nt_cap] and the 1024-byte scale-factor tiles [H, nt_cap, 1024]."""
+    T, H = qt.codes.shape[0], qt.codes.shape[1]
+    ntcap = (T + 127) // 128 + num_docs
+    off = (H * ntcap * 4 + 1023) // 1024 * 1024
+    st = qt.scales[:H * ntcap * 4].view(torch.float32).view(H, ntcap)
+    sf = qt.scales[off:off + H * ntcap * 1024].view(H, ntcap, 1024)
+    return st, sf
 
 
 def attn_quantize(x: torch.Tensor, cu_seqlens: torch.Tensor | None, layout: int, block: int = 128,

@@ -49,6 +49,7 @@ attn_status check_ws(const attn_shape* s, void* ws, size_t bytes) {
 
 bool valid_block(int layout, int block) {
     if (layout == ATTN_E4M3_TOKBLOCK) return block == 1 || block == 32 || block == 64 || block == 128;
+    if (layout == ATTN_NVFP4) return block == 128;
     return layout == ATTN_MX_ROW32 || layout == ATTN_MX_COL32 || layout == ATTN_MX_TOKEN;
 }
 
@@ -123,11 +124,13 @@ attn_status attn_quantize_sizes(const attn_shape* shape, int32_t layout, int32_t
     attn_status st = check_shape(shape);
     if (st != ATTN_OK) return st;
     if (!codes_bytes || !scales_bytes) return ATTN_ERR_INVALID_ARG;
-    if (layout < 0 || layout > 3 || !valid_block(layout, block)) return ATTN_ERR_INVALID_ARG;
+    if (layout < 0 || layout > 4 || !valid_block(layout, block)) return ATTN_ERR_INVALID_ARG;
     if (layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     const long long T = shape->total_tokens, H = shape->heads, d = shape->head_dim;
-    *codes_bytes = static_cast<size_t>(T * H * d);
-    if (layout == ATTN_E4M3_TOKBLOCK)
+    *codes_bytes = static_cast<size_t>(T * H * (layout == ATTN_NVFP4 ? d / 2 : d));
+    if (layout == ATTN_NVFP4)
+        *scales_bytes = nvfp4_sf_offset(H, tiles_cap(shape)) + static_cast<size_t>(H * tiles_cap(shape)) * 1024;
+    else if (layout == ATTN_E4M3_TOKBLOCK)
         *scales_bytes = static_cast<size_t>(H * blocks_cap(shape, block)) * sizeof(float);
     else if (layout == ATTN_MX_TOKEN)
         *scales_bytes = static_cast<size_t>(H * blocks_cap(shape, 1));
@@ -156,7 +159,7 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     if (st != ATTN_OK) return st;
     if (!x || !out || !out->codes || !out->scales) return ATTN_ERR_INVALID_ARG;
     if (in_dtype != ATTN_IN_F32 && in_dtype != ATTN_IN_BF16) return ATTN_ERR_INVALID_ARG;
-    if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 3) return ATTN_ERR_INVALID_ARG;
+    if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 4) return ATTN_ERR_INVALID_ARG;
     if (out->layout != ATTN_E4M3_TOKBLOCK && shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (out->mx_rule != ATTN_MX_RULE_NOSAT && out->mx_rule != ATTN_MX_RULE_OCP_FLOOR) return ATTN_ERR_INVALID_ARG;
     const int elt = in_dtype == ATTN_IN_BF16 ? 2 : 4;
@@ -165,6 +168,7 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
         return ATTN_ERR_INVALID_ARG;
     if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
     QuantParams p;
+    std::memset(&p, 0, sizeof(p));
     p.x = x;
     p.in_bf16 = in_dtype == ATTN_IN_BF16;
     p.tstride = token_stride;
@@ -178,10 +182,15 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     p.scales = out->scales;
     // MX layouts have fixed blocks (32 channels or tokens; one token): the caller's
     // `block` field does not reach the kernel's block arithmetic for them
-    p.block = out->layout == ATTN_E4M3_TOKBLOCK ? out->block : (out->layout == ATTN_MX_TOKEN ? 1 : 32);
+    p.block = out->layout == ATTN_E4M3_TOKBLOCK ? out->block
+              : out->layout == ATTN_NVFP4        ? 128
+              : (out->layout == ATTN_MX_TOKEN ? 1 : 32);
     p.scale_cap = out->layout == ATTN_E4M3_TOKBLOCK ? blocks_cap(shape, out->block)
                   : out->layout == ATTN_MX_TOKEN     ? blocks_cap(shape, 1)
                                                      : tiles_cap(shape);
+    p.sf16 = out->layout == ATTN_NVFP4
+                 ? static_cast<uint8_t*>(out->scales) + nvfp4_sf_offset(shape->heads, tiles_cap(shape))
+                 : nullptr;
     p.rotate = rotate != 0;
     p.seed = hadamard_seed;
     p.mx_rule = out->mx_rule;

@@ -59,6 +59,10 @@ inline WsLayout ws_layout(int64_t T, int64_t H, int64_t nd) {
     return w;
 }
 
+// NVFP4 scales array: fp32 block scales [H][nt_cap], then the 1024-byte scale-factor
+// tiles [H][nt_cap] from this byte offset
+inline size_t nvfp4_sf_offset(int64_t H, int64_t nt_cap) { return align_up(static_cast<size_t>(H * nt_cap) * 4, 1024); }
+
 // Header at the start of the workspace.
 struct WsHeader {
     uint32_t status;

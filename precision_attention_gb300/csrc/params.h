@@ -22,6 +22,7 @@ struct QuantParams {
     unsigned long long seed;
     int mx_rule;
     uint32_t* status;
+    uint8_t* sf16;                // NVFP4: the 1024-byte scale-factor tiles [H][scale_cap]
     int32_t* gtab;                // device document table [3][nd + 1] (start, tile prefix, block
                                   // prefix) written by doc_table_kernel, or null: each CTA builds
                                   // its own in shared memory (nd <= MAX_DOCS)

@@ -145,6 +145,21 @@ __device__ __forceinline__ float pow2_neg(int X) {   // 2^-X for X in [-127, 126
     return __uint_as_float((uint32_t)(127 - X) << 23);
 }
 
+// two fp32 -> two E2M1 codes in one byte (round to nearest even, beyond 6 saturates):
+// `lo` in the low nibble
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+// value of a non-negative E4M3 code (0x00..0x7E): exponent field e, mantissa m
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const uint32_t e = b >> 3, m = b & 7u;
+    return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+}
+
 template <int EPL>
 __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&y)[EPL], float mul) {
     uint32_t w[EPL / 4];
@@ -266,7 +281,7 @@ __device__ __forceinline__ int find_doc(const int32_t* off, int nd, int u) {
     return lo;
 }
 
-enum { QM_E4M3_BLOCK = 0, QM_E4M3_ROW = 1, QM_MX_ROW = 2, QM_MX_COL = 3, QM_MX_TOK = 4 };
+enum { QM_E4M3_BLOCK = 0, QM_E4M3_ROW = 1, QM_MX_ROW = 2, QM_MX_COL = 3, QM_MX_TOK = 4, QM_NVFP4 = 5 };
 
 constexpr int QUANT_THREADS = 256;
 
@@ -403,6 +418,81 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                     if (t0 + row < L)
                         store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y[hp], inv);
                 }
+            }
+        } else if constexpr (QM == QM_NVFP4) {
+            // the 128-token tile is the fp32 block: amax over the tile gives s_t = amax / 2688
+            // and inv = 448 / amax; each thread's 16 channels of a row are one group: its
+            // E4M3 scale sf = E4M3(max |y inv|) and E2M1 codes of y inv (6 / sf), the scale
+            // byte at its place in the MMA-ready tile (groups 4 kk .. 4 kk + 3 in tile kk)
+            static_assert(EPL == 16, "NVFP4 groups are one thread's 16 channels");
+            float y[4][EPL];
+            float amax = 0.0f;
+#pragma unroll
+            for (int hp = 0; hp < 4; hp++) {
+                const int row = hp * 32 + warp * 4 + rw;
+                smem_row<EPL, ELT>(tile, row, sl, y[hp]);
+                if (t0 + row >= L) {
+#pragma unroll
+                    for (int i = 0; i < EPL; i++) y[hp][i] = 0.0f;
+                }
+                if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
+#pragma unroll
+                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
+            }
+            if (!finite_abs(amax)) {
+                nonfin = true;
+                amax = 0.0f;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
+            if (lane == 0) {
+                red[warp] = amax;
+                if (wbad) flag[0] = 1;
+            }
+            __syncthreads();
+            amax = red[0];
+#pragma unroll
+            for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
+            const bool bad = flag[0] != 0;
+            __syncthreads();
+            if (tid == 0) flag[0] = 0;
+            float inv = 0.0f, st_scale = 0.0f;
+            if (bad) st_scale = __int_as_float(0x7FC00000);
+            else if (amax > 0.0f) {
+                inv = __fdiv_rn(448.0f, amax);
+                st_scale = __fdiv_rn(amax, 2688.0f);
+            }
+            if (tid == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + g] = st_scale;
+            uint8_t* sft = p.sf16 + ((long long)h * p.scale_cap + g) * 1024 + (sl >> 2) * 512;
+#pragma unroll
+            for (int hp = 0; hp < 4; hp++) {
+                const int row = hp * 32 + warp * 4 + rw;
+                float z[EPL];
+                float gmax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < EPL; i++) {
+                    z[i] = __fmul_rn(y[hp][i], inv);
+                    gmax = fmaxf(gmax, fabsf(z[i]));
+                }
+                const uint32_t sfb = cvt_e4m3x2(gmax, 0.0f) & 0xFFu;
+                const float sfv = e4m3_value(sfb);
+                const float r6 = sfv > 0.0f ? __fdiv_rn(6.0f, sfv) : 0.0f;
+                uint32_t w[2] = {0u, 0u};
+                if (sfv > 0.0f) {
+#pragma unroll
+                    for (int i = 0; i < EPL; i += 2)
+                        w[i >> 3] |= cvt_e2m1x2(__fmul_rn(z[i], r6), __fmul_rn(z[i + 1], r6)) << (4 * (i & 7));
+                }
+                const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfb, 1);
+                const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfb, 2);
+                const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfb, 3);
+                if ((sl & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(sft + (row % 32) * 16 + (row / 32) * 4) =
+                        sfb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                if (t0 + row < L)
+                    *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * (D / 2) + sl * 8) =
+                        make_uint2(w[0], w[1]);
             }
         } else if constexpr (QM == QM_E4M3_ROW) {
 #pragma unroll 1
@@ -589,6 +679,7 @@ static cudaError_t launch_layout(const CUtensorMap& m, const QuantParams& p, int
         if (layout == 1) return launch_q<EPL, ELT, QM_MX_ROW, 1>(m, p, grid, st);
         if (layout == 2) return launch_q<EPL, ELT, QM_MX_COL, 1>(m, p, grid, st);
         if (layout == 3) return launch_q<EPL, ELT, QM_MX_TOK, 1>(m, p, grid, st);
+        if (layout == 4) return launch_q<EPL, ELT, QM_NVFP4, 4>(m, p, grid, st);
     } else {
         if (layout != 0) return cudaErrorInvalidValue;
     }

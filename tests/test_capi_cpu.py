@@ -100,7 +100,15 @@ def test_shape_rules_on_host(pa):
     assert sizes(pa._Shape(50000, 2, 128, 20000, placeholder_cu)) == pa.ATTN_OK   # no cap on the document count
     assert sizes(pa._Shape(1 << 26, 64, 128, 1, None)) == pa.ATTN_ERR_UNSUPPORTED          # T x H beyond int32
     assert sizes(pa._Shape(1024, 2, 128, 1024, placeholder_cu)) == pa.ATTN_OK              # one token per document
-    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=4, block=32) == pa.ATTN_ERR_INVALID_ARG   # no such layout
+    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=5, block=32) == pa.ATTN_ERR_INVALID_ARG   # no such layout
+    assert sizes(pa._Shape(100, 2, 128, 1, None), layout=4, block=32) == pa.ATTN_ERR_INVALID_ARG   # NVFP4: block 128
+    assert sizes(pa._Shape(100, 2, 64, 1, None), layout=4, block=128) == pa.ATTN_ERR_UNSUPPORTED   # NVFP4: d = 128
+    cb4, sb4 = ctypes.c_size_t(), ctypes.c_size_t()
+    shape4 = pa._Shape(1000, 2, 128, 3, placeholder_cu)
+    assert L.attn_quantize_sizes(ctypes.byref(shape4), 4, 128, ctypes.byref(cb4), ctypes.byref(sb4)) == pa.ATTN_OK
+    ntcap = (1000 + 127) // 128 + 3
+    assert cb4.value == 1000 * 2 * 64                                      # two E2M1 codes per byte
+    assert sb4.value == (2 * ntcap * 4 + 1023) // 1024 * 1024 + 2 * ntcap * 1024
     assert sizes(pa._Shape(100, 2, 64, 1, None), layout=3, block=1) == pa.ATTN_ERR_UNSUPPORTED     # MX: d = 128
     cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     shape = pa._Shape(100, 2, 128, 3, placeholder_cu)

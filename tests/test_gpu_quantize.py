@@ -117,3 +117,32 @@ def test_mx_token_bit_exact(oracle_mod, lengths, H, rule):
     assert ost == 0
     assert np.array_equal(qt.codes.cpu().numpy(), codes)
     assert np.array_equal(qt.scales.cpu().numpy()[:, :inp.T], su)
+
+
+@pytest.mark.parametrize("wid,lengths,H,rotate", [
+    (2, [300, 77, 129], 2, True),       # outlier recipe, ragged documents, rotated
+    (4, [256, 1, 130], 2, True),        # outlier channels, a one-token document
+    (2, [384], 1, False),
+])
+def test_nvfp4_bit_exact(oracle_mod, wid, lengths, H, rotate):
+    """NVFP4 Q/K operands (FLAMIA sections 1 and 2): E2M1 codes, the fp32 scale of
+    each 128-token block and every 16-channel E4M3 scale in the MMA-ready tiles
+    equal the oracle's; scale bytes of rows past a document end are 0."""
+    inp = workloads.make(wid, heads=H, lengths=lengths)
+    q, k, v, cu = to_device(inp)
+    T = inp.T
+    nd = len(inp.cu_seqlens) - 1
+    for x_np, x_dev in ((inp.q, q), (inp.k, k)):
+        qt, st = gpu_quant(x_dev, cu, pa.ATTN_NVFP4, 128, rotate)
+        assert st == 0
+        codes, (sf32, su), ost = oracle_mod.quantize(x_np, inp.cu_seqlens, oracle_mod.NVFP4, 128, rotate, SEED)
+        assert ost == 0
+        g_st, g_sf = (t.cpu().numpy() for t in pa.nvfp4_scales(qt, nd))
+        assert np.array_equal(qt.codes.cpu().numpy(), codes), f"{np.sum(qt.codes.cpu().numpy() != codes)} code bytes differ"
+        nb = sf32.shape[1]
+        assert np.array_equal(g_st[:, :nb].view(np.uint32), sf32.view(np.uint32))
+        lo = mx_row_tiles_to_logical(g_sf[:, :, :512], inp.cu_seqlens, T, H)
+        hi = mx_row_tiles_to_logical(g_sf[:, :, 512:], inp.cu_seqlens, T, H)
+        assert np.array_equal(np.concatenate([lo, hi], axis=2), su)
+        assert np.all(mx_row_pad_bytes(g_sf[:, :, :512], inp.cu_seqlens, T) == 0)
+        assert np.all(mx_row_pad_bytes(g_sf[:, :, 512:], inp.cu_seqlens, T) == 0)
