@@ -154,10 +154,13 @@ def job_throughput(world, flops_per_rank, ms_per_step):
 
 
 # ---------------------------------------------------------------------------
-def quant_bytes(T, H, d, in_elt, mx, block, nd):
+def quant_bytes(T, H, d, in_elt, mx, block, nd, nv=False):
     """Algorithmic HBM bytes of one step's quantisation (Q, K, V): inputs read,
     codes written, scales written."""
     n = T * H * d
+    if nv:   # NVFP4 Q, K: half a byte per element, an E4M3 scale per 16, fp32 per 128 tokens; E4M3 V
+        blocks = H * ((T + 127) // 128 + nd) * 4
+        return 3 * n * in_elt + 2 * (n // 2 + n // 16 + blocks) + n + blocks
     scales = (3 * H * (T + 127) // 128 * 512 / 4) if mx else 3 * H * ((T + block - 1) // block + nd) * 4
     return 3 * n * (in_elt + 1) + scales
 
@@ -190,7 +193,8 @@ def measure_fp8_peak(torch, dev):
         return None
 
 
-def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=None, keep=False, exp_mode=0):
+def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=None, keep=False, exp_mode=0,
+                  nv=False):
     """Time `steps` whole steps (quantise Q, K, V, then the FP8 forward) of one
     workload after `warmup` untimed ones; inputs resident in HBM. Returns the
     timings (and, with keep, the device tensors for the end-to-end leg)."""
@@ -212,7 +216,11 @@ def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=No
     q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
     cu = torch.from_numpy(cu_np.astype(np.int32)).to(dev)
     ws = pa.workspace(T, H, d, nd, dev)
-    if mx:   # causal-exact: one V exponent per token
+    if nv:   # mixed NVFP4 / FP8: NVFP4 Q and K, E4M3 V in 128-token blocks
+        if mx or exact:
+            raise SystemExit("--nvfp4 takes an E4M3 workload without --exact")
+        lq, lk, lv, blk = pa.ATTN_NVFP4, pa.ATTN_NVFP4, E4M3, 128
+    elif mx:   # causal-exact: one V exponent per token
         lq, lk, lv, blk = ROW, ROW, (pa.ATTN_MX_TOKEN if exact else COL), 32
     else:
         lq = lk = lv = E4M3
@@ -277,7 +285,7 @@ def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=No
          "stats": {name: {"median": float(np.median(x)), "min": float(np.min(x)), "p90": float(np.percentile(x, 90))}
                    for name, x in (("step_ms", step_ms), ("attn_ms", attn_ms))},
          "clocks": clk, "T": T, "H": H, "d": d, "nd": nd, "mx": mx, "causal": causal, "exact": exact,
-         "quant_bytes": quant_bytes(T, H, d, 4 if w.in_dtype == "f32" else 2, mx, blk, nd)}
+         "quant_bytes": quant_bytes(T, H, d, 4 if w.in_dtype == "f32" else 2, mx, blk, nd, nv)}
     r["quant_ms"] = r["ms_step"] - r["attn_ms"]
     if keep:
         r.update(dict(q=q, k=k, v=v, q_h=q_h, k_h=k_h, v_h=v_h, cu=cu, ws=ws, Q=Q, K=K, V=V, o=o, lse=lse,
@@ -298,7 +306,7 @@ def gpu_arm(args, rank, world, local_rank):
     args.world = world
     w = workloads.WORKLOADS[args.workload]
     r = time_workload(args, pa, torch, dev, args.workload, bool(args.exact), args.steps, args.warmup,
-                      clocks_idx=local_rank, keep=True, exp_mode=EXP_MODES[args.exp_mode])
+                      clocks_idx=local_rank, keep=True, exp_mode=EXP_MODES[args.exp_mode], nv=args.nvfp4)
     T, H, d, nd = r["T"], r["H"], r["d"], r["nd"]
     q_h, k_h, v_h, cu, ws, Q, K, V = (r[x] for x in ("q_h", "k_h", "v_h", "cu", "ws", "Q", "K", "V"))
     lq, lk, lv, blk, rot, seed, stream = (r[x] for x in ("lq", "lk", "lv", "blk", "rot", "seed", "stream"))
@@ -397,13 +405,19 @@ def gpu_arm(args, rank, world, local_rank):
     # the other benchmark configurations, timed in this process (rank 0, N = 1 only)
     r["per_workload"] = None
     if (rank == 0 and world == 1 and not args.no_per_workload and args.heads is None and args.seqlen is None
-            and args.exp_mode == "hw"):
+            and args.exp_mode == "hw" and not args.nvfp4):
         per = {}
         for wid, ex in ((2, False), (3, False), (3, True), (4, False), (5, False), (5, True)):
             if wid == args.workload and ex == bool(args.exact):
                 continue
             rr = time_workload(args, pa, torch, dev, wid, ex, min(args.steps, 30), 3, clocks_idx=local_rank)
             per[f"{workloads.WORKLOADS[wid].name}{' causal-exact' if ex else ''}"] = summarize(rr, wid, ex)
+        # the mixed NVFP4/FP8 path (NVFP4 Q K^T) on the two E4M3 configurations
+        for wid in (2, 3):
+            rr = time_workload(args, pa, torch, dev, wid, False, min(args.steps, 30), 3, clocks_idx=local_rank, nv=True)
+            e_ = summarize(rr, wid, False)
+            e_["qk"] = "NVFP4"
+            per[f"{workloads.WORKLOADS[wid].name} nvfp4-qk"] = e_
         r["per_workload"] = per
         # the bit-level exponentials (inference options) on the four non-exact configurations
         hw = {w_: (r["attn_ms"], r["acc"]) if w_ == args.workload and not args.exact else None for w_ in (2, 3, 4, 5)}
@@ -556,7 +570,9 @@ def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
             "causal": w.causal, "causal_exact": bool(args.exact), "exp_mode": args.exp_mode,
-            "quant": (("MXFP8 (E8M0 per 32; V one E8M0 per token, causal-exact)" if args.exact else "MXFP8 (E8M0 per 32)")
+            "quant": ("NVFP4 Q, K (E2M1, E4M3 per 16 channels, fp32 per 128 tokens); V E4M3 blocks of 128 tokens"
+                      if args.nvfp4 else
+                      ("MXFP8 (E8M0 per 32; V one E8M0 per token, causal-exact)" if args.exact else "MXFP8 (E8M0 per 32)")
                       if w.mx else
                       ("E4M3 one scale per token (causal-exact)" if args.exact else f"E4M3 blocks of {w.block} tokens")) +
             (" + Hadamard rotation of Q, K" if not args.no_rotate else ", no rotation"), "input_dtype": w.in_dtype,
@@ -578,6 +594,8 @@ def main():
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
     ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="the mixed NVFP4/FP8 path: NVFP4 Q and K (Q K^T on the FP4 tensor cores), E4M3 V")
     ap.add_argument("--exp-mode", default="hw", choices=sorted(EXP_MODES),
                     help="the probabilities' exponential: the hardware exp2 (default), Schraudolph's, or log-domain P")
     ap.add_argument("--no-per-workload", action="store_true",

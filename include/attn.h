@@ -223,10 +223,12 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
  * section 4.3 (score scales folded into one multiplier, longest-first causal
  * work), sections 1 and 4.5 (exact scaling against causal leakage), section
  * 4.1 (packed documents).
- * q, k: ATTN_E4M3_TOKBLOCK or ATTN_MX_ROW32 (both the same; both rotated with
- *    the same seed or both not -> else ATTN_ERR_SEED_MISMATCH).
+ * q, k: ATTN_E4M3_TOKBLOCK, ATTN_MX_ROW32 or ATTN_NVFP4 (both the same; both
+ *    rotated with the same seed or both not -> else ATTN_ERR_SEED_MISMATCH).
  * v: ATTN_E4M3_TOKBLOCK (with E4M3 q, k), or ATTN_MX_COL32 or ATTN_MX_TOKEN
- *    (with MX q, k).
+ *    (with MX q, k), or ATTN_E4M3_TOKBLOCK with block 128 (with NVFP4 q, k:
+ *    the mixed NVFP4/FP8 path of FLAMIA section 1, S from the block-scaled
+ *    FP4 MMA, P V in E4M3; head_dim 128; causal_exact -> ATTN_ERR_UNSUPPORTED).
  * causal: key j > query i masked, positions local to each document.
  * causal_exact: requires causal, and block 1 for q, k and v (E4M3) or a v in
  *    ATTN_MX_TOKEN (MX: q and k rows are per token already); every scale then

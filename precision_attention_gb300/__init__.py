@@ -198,6 +198,11 @@ class QTensor:
     rotated: int = 0
     hadamard_seed: int = 0
 
+    def dims(self):
+        """(T, H, head_dim) of the operand (NVFP4 codes hold two channels per byte)."""
+        T, H, w = self.codes.shape
+        return T, H, 2 * w if self.layout == ATTN_NVFP4 else w
+
     def _c(self) -> _QT:
         return _QT(self.codes.data_ptr(), self.scales.data_ptr(), self.layout, self.block, self.mx_rule,
                    self.rotated, self.hadamard_seed)
@@ -267,7 +272,7 @@ def attn_fp8_fwd_ex(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor
     """FP8 attention forward with a choice of the probabilities' exponential
     (ATTN_EXP_HW: attn_fp8_fwd itself; ATTN_EXP_SCHRAUDOLPH, ATTN_EXP_MITCHELL_P:
     the bit-level inference forms). Returns (o bf16 [T, H, d], lse fp32 [H, T])."""
-    T, H, d = q.codes.shape
+    T, H, d = q.dims()
     nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     dev = q.codes.device
     if ws is None:
@@ -319,7 +324,7 @@ def attn_fp8_fwd_noalloc(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.T
     16 MiB device array (for callers that cannot allocate; see include/attn.h).
     `status`, if given, is a 1-element int32 device tensor that receives the
     call's device status word. Returns (o, lse)."""
-    T, H, d = q.codes.shape
+    T, H, d = q.dims()
     dev = q.codes.device
     if out is None:
         out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
@@ -343,7 +348,7 @@ def attn_fp8_fwd_pdump(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Ten
     codes uint8 [H, T, key_stride]: codes[h, t, k] is what row t of head h gave
     document-local key k (0 where nothing was written)."""
     L = pdump_lib()
-    T, H, d = q.codes.shape
+    T, H, d = q.dims()
     nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     dev = q.codes.device
     ws = workspace(T, H, d, nd, dev)

@@ -12,7 +12,7 @@
 
 namespace pa {
 
-enum { MODE_BF16 = 0, MODE_E4M3_TILE = 1, MODE_E4M3_COL = 2, MODE_MX = 3, MODE_MX_EXACT = 4 };
+enum { MODE_BF16 = 0, MODE_E4M3_TILE = 1, MODE_E4M3_COL = 2, MODE_MX = 3, MODE_MX_EXACT = 4, MODE_NVFP4 = 5 };
 
 template <int ELT, int D, int MODE>
 struct Cfg {

@@ -613,16 +613,24 @@ struct PairCfgT {
     // per-token exponent into P instead (as the E4M3 per-column mode folds V scales).
     static constexpr bool MX = MODE == MODE_MX || MODE == MODE_MX_EXACT;
     static constexpr bool MXPV = MODE == MODE_MX;
+    // NV: Q K^T on NVFP4 operands (E2M1, E4M3 scales per 16 channels in TMEM, fp32
+    // 128-token block scales folded into the score multiplier as in the E4M3 tile
+    // mode), P V on E4M3 as there
+    static constexpr bool NV = MODE == MODE_NVFP4;
+    static constexpr bool SFT = MX || NV;             // scale factors in TMEM
     // P lives in TMEM, the A operand of P V read from there: two buffers per query
-    // tile, one in MX mode (TMEM also holds the scale factors)
-    static constexpr int PBUF = MX ? 1 : 2;
-    static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile
+    // tile, one when TMEM also holds scale factors
+    static constexpr int PBUF = SFT ? 1 : 2;
+    static constexpr int TILE = 128 * 128;           // bytes of a 128 x 128 E4M3 tile (one ring slot)
+    static constexpr int QKB = NV ? TILE / 2 : TILE;  // bytes of a Q or K tile (NVFP4: 64-byte rows)
+    static constexpr int QD = NV ? 64 : 128;          // Q / K row bytes (descriptor geometry)
     static constexpr int NS = MX ? 3 : 4;             // K/V ring depth
     static constexpr int OFF_Q = 0;                   // Q0, Q1
     static constexpr int OFF_KV = 2 * TILE;           // stage s: K at +2s TILE, V at +(2s + 1) TILE
     // MX scale tiles, 512 bytes each: Q0, Q1, P (all 2^0), K per stage, V per stage
     static constexpr int OFF_SF = OFF_KV + NS * 2 * TILE;
-    static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : 0;
+    // NV: 1024 bytes (two K = 64 steps) each: Q0, Q1, K per stage
+    static constexpr int SF_BYTES = MX ? 512 * (3 + 2 * NS) : NV ? 1024 * (2 + NS) : 0;
     // per-key scales of key tile g, staged per stage: float [NS][2][128]. E4M3 per-column
     // mode (blocks shorter than a tile, causal-exact): K and V scales; MX exact mode: V's
     // 2^X only (K's exponents are inside the block-scaled MMA)
@@ -640,11 +648,14 @@ struct PairCfgT {
     static constexpr bool SHARED_S = true;
     static constexpr uint32_t T_S1 = SHARED_S ? 0 : 128;
     static constexpr uint32_t T_SFQ = 128, T_SFP = 136, T_SFK = 144, T_SFV = 160;
-    static constexpr uint32_t T_P = MX ? 176 : 128;   // P of query tile q, buffer b at T_P + 32 (PBUF q + b)
+    static constexpr uint32_t T_P = SFT ? 176 : 128;  // P of query tile q, buffer b at T_P + 32 (PBUF q + b)
+    // NV: Q_q's scale factors at T_NQ + 8q, K of key tile g (issuer q) at T_NK + 16q + 8 (g % 2)
+    static constexpr uint32_t T_NQ = 128, T_NK = 144;
 };
 static_assert(PairCfgT<MODE_E4M3_TILE>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_MX>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_MX_EXACT>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
+static_assert(PairCfgT<MODE_NVFP4>::SMEM <= 227 * 1024, "pair kernel shared memory exceeds the per-CTA limit");
 static_assert(PairCfgT<MODE_E4M3_TILE>::NS <= 8 && PairCfgT<MODE_MX>::NS <= 8, "K/V ring deeper than its barriers");
 
 struct PairBars {
@@ -747,7 +758,8 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             q_issued = qi & 1;
             // MX: the second query tile's scale tile exists only inside the document
             const bool q1_in = 2 * w.qtile + 1 < (d.len + 127) / 128;
-            const uint32_t qbytes = 2 * PC::TILE + (PC::MX ? (q1_in ? 1024 : 512) : 0);
+            const uint32_t qbytes =
+                2 * PC::QKB + (PC::MX ? (q1_in ? 1024 : 512) : PC::NV ? (q1_in ? 2048 : 1024) : 0);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&B->q_full, qbytes);
                 tma_load_3d(sm + PC::OFF_Q, &tmq, &B->q_full, 0, w.head, d.start + 256 * w.qtile);
@@ -756,6 +768,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     const long long t0 = (long long)w.head * p.ntcap + d.toff + 2 * w.qtile;
                     bulk_load(sm + PC::OFF_SF, p.mq + t0 * 512, 512, &B->q_full);
                     if (q1_in) bulk_load(sm + PC::OFF_SF + 512, p.mq + (t0 + 1) * 512, 512, &B->q_full);
+                } else if constexpr (PC::NV) {
+                    const long long t0 = (long long)w.head * p.ntcap + d.toff + 2 * w.qtile;
+                    bulk_load(sm + PC::OFF_SF, p.mq + t0 * 1024, 1024, &B->q_full);
+                    if (q1_in) bulk_load(sm + PC::OFF_SF + 1024, p.mq + (t0 + 1) * 1024, 1024, &B->q_full);
                 }
             }
             for (int j = 0; j < w.ntiles; j++, g++) {
@@ -766,12 +782,15 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 }
                 issued[st] = (g / PC::NS) & 1;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&B->k_full[st], PC::TILE + (PC::MX ? 512 : 0));
+                    mbar_arrive_expect_tx(&B->k_full[st], PC::QKB + (PC::MX ? 512 : PC::NV ? 1024 : 0));
                     tma_load_3d(sm + PC::OFF_KV + st * 2 * PC::TILE, &tmk, &B->k_full[st], 0, w.head,
                                 d.start + 128 * j);
                     if constexpr (PC::MX)
                         bulk_load(sm + PC::OFF_SF + 1536 + st * 512,
                                   p.mk + ((long long)w.head * p.ntcap + d.toff + j) * 512, 512, &B->k_full[st]);
+                    if constexpr (PC::NV)
+                        bulk_load(sm + PC::OFF_SF + 2048 + st * 1024,
+                                  p.mk + ((long long)w.head * p.ntcap + d.toff + j) * 1024, 1024, &B->k_full[st]);
                 }
                 if (!__all_sync(FULL, mbar_wait(&B->v_empty[st], ((g / PC::NS) & 1) ^ 1, abort, lim))) {
                     ok = false;
@@ -835,8 +854,8 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             constexpr uint32_t id_pv = idesc(0, 0, false, true, 128, 128);
             constexpr uint64_t TILE16 = (uint64_t)PC::TILE >> 4;
             constexpr uint64_t STAGE16 = (uint64_t)(2 * PC::TILE) >> 4;
-            const uint64_t dq = desc_kmajor<1, 128, MODE>(sQ, 0) + q * TILE16;
-            const uint64_t dk0 = desc_kmajor<1, 128, MODE>(sKV, 0);
+            const uint64_t dq = desc_kmajor<1, PC::QD, MODE>(sQ, 0) + q * TILE16;
+            const uint64_t dk0 = desc_kmajor<1, PC::QD, MODE>(sKV, 0);
             const uint64_t dv0 = desc_v<1, 128, MODE>(sKV + PC::TILE, 0);
             const uint32_t tS = tmem + q * PC::T_S1, tO = tmem + PC::T_O + q * 128;
             // MX: this query tile's Q, P, K and V scale-factor columns
@@ -849,6 +868,20 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             int kP = 0, itP = itS, jP = 0;
             uint32_t gP = 0;
             WorkItem wP = wS;
+            // NVFP4: the K scale factors of key tile gS are already in their TMEM slot,
+            // copied right after the previous S (off the hand-over between S buffers) when
+            // the tile had landed by then
+            bool sf_pre = false;
+            auto copy_k_sf = [&](uint32_t gx) {
+                const int sx = gx % PC::NS;
+                if constexpr (PC::NV) {
+                    const uint32_t nk = tmem + PC::T_NK + 16 * q + 8 * (gx & 1);
+                    tc_cp_sf(nk, desc_sf(sSF + 2048 + sx * 1024));
+                    tc_cp_sf(nk + 4, desc_sf(sSF + 2048 + sx * 1024 + 512));
+                } else if constexpr (PC::MX) {
+                    tc_cp_sf(sfk0 + 4 * (gx & 1), desc_sf(sSF + 1536 + sx * 512));
+                }
+            };
             auto issue_s = [&]() -> bool {   // S_q of key tile gS
                 const int st = gS % PC::NS;
                 if (jS == 0 && !mbar_wait(&B->q_full, qiS & 1, abort, lim)) return false;
@@ -864,10 +897,23 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint64_t dk = dk0 + st * STAGE16;
-                if constexpr (PC::MX) {
+                if constexpr (PC::NV) {
+                    // E4M3 scale factors of Q_q (once per item) and of this key tile, two
+                    // 512-byte tiles each (K = 64 per MMA), then two block-scaled MMAs
+                    const uint32_t nq = tmem + PC::T_NQ + 8 * q, nk = tmem + PC::T_NK + 16 * q + 8 * (gS & 1);
+                    if (jS == 0) {
+                        tc_cp_sf(nq, desc_sf(sSF + 1024 * q));
+                        tc_cp_sf(nq + 4, desc_sf(sSF + 1024 * q + 512));
+                    }
+                    if (!sf_pre) copy_k_sf(gS);
+#pragma unroll
+                    for (int kk = 0; kk < 2; kk++)
+                        mma_nvf4(tS, dq + koff<1, 64, MODE>(kk), dk + koff<1, 64, MODE>(kk), idesc_nvf4(128, 128),
+                                 nq + 4 * kk, nk + 4 * kk, kk ? 1u : 0u);
+                } else if constexpr (PC::MX) {
                     if (jS == 0) tc_cp_sf(sfq, desc_sf(sSF + 512 * q));
                     const uint32_t sfk = sfk0 + 4 * (gS & 1);
-                    tc_cp_sf(sfk, desc_sf(sSF + 1536 + st * 512));
+                    copy_k_sf(gS);
 #pragma unroll
                     for (int kk = 0; kk < C::KSTEPS_S; kk++)
                         mma_mxf8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk),
@@ -886,6 +932,19 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     qiS++;
                     itS = item_of(++kS);
                     if (itS < n_items) wS = p.items[itS];
+                }
+                sf_pre = false;
+                if constexpr (PC::NV) {
+                    // the next key tile's scale factors into the other slot, if it has landed
+                    // (tcgen05 copies and MMAs of this thread run in issue order, so the S two
+                    // tiles back has read that slot before the copy writes it). NVFP4 only: its
+                    // two copies per tile moved off the hand-over save 2.5% there, while moving
+                    // the MX layouts' single copy measured 1.2% slower
+                    if (itS < n_items && mbar_test(&B->k_full[gS % PC::NS], (gS / PC::NS) & 1)) {
+                        tc_fence_after();
+                        copy_k_sf(gS);
+                        sf_pre = true;
+                    }
                 }
                 return true;
             };
@@ -952,7 +1011,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             const int rloc = 128 * qt + r;                        // row position in the document
             const int rcl = rloc < L ? rloc : L - 1;
             float qs = 1.0f, ref = 1.0f;   // MX: the scales are inside the MMAs
-            if constexpr (MODE == MODE_E4M3_TILE) {
+            if constexpr (MODE == MODE_E4M3_TILE || MODE == MODE_NVFP4) {
                 qs = p.sq[h * p.capq + d.boff_q + (128 * qtc) / p.bq];
                 ref = p.vref[(long long)h * p.nd + w.doc];
             } else if constexpr (MODE == MODE_E4M3_COL) {
@@ -967,11 +1026,11 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             // tile ahead of use (written by the V-reference pass before this launch)
             const float4* tsc = p.tsc + (long long)h * p.tsc_cap + d.toff;
             float4 tnext = make_float4(0.0f, 0.0f, 1.0f, 0.0f);
-            if constexpr (MODE == MODE_E4M3_TILE) tnext = tsc[0];
+            if constexpr (MODE == MODE_E4M3_TILE || MODE == MODE_NVFP4) tnext = tsc[0];
             for (int j = 0; j < nt; j++) {
                 const uint32_t gj = g + j;
                 float c = p.C, lr = 0.0f, invr = 1.0f;
-                if constexpr (MODE == MODE_E4M3_TILE) {
+                if constexpr (MODE == MODE_E4M3_TILE || MODE == MODE_NVFP4) {
                     c = qs * tnext.x;
                     lr = tnext.y;
                     invr = tnext.z;
@@ -1270,11 +1329,12 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
 template <int MODE, int EXPM = ATTN_EXP_HW>
 static cudaError_t launch_pair(const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                                cudaStream_t st) {
+    using PC = PairCfgT<MODE>;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, 1, p.T, p.H, 128, 128, true) || !make_map(&mk, k, 1, p.T, p.H, 128, 128, true) ||
+    // Q, K rows: 128 E4M3 bytes (128-byte swizzle), or 64 NVFP4 bytes (64-byte swizzle)
+    if (!make_map(&mq, q, 1, p.T, p.H, PC::QD, PC::QD, !PC::NV) || !make_map(&mk, k, 1, p.T, p.H, PC::QD, PC::QD, !PC::NV) ||
         !make_map(&mv, v, 1, p.T, p.H, 128, 128, true))
         return cudaErrorInvalidValue;
-    using PC = PairCfgT<MODE>;
     auto kern = attn_pair_kernel<MODE, EXPM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM);
     if (e != cudaSuccess) return e;
@@ -1293,6 +1353,9 @@ cudaError_t launch_attn(int mode, int expm, int D, const void* q, const void* k,
         if (mode == MODE_MX)
             return expm == ATTN_EXP_SCHRAUDOLPH ? launch_pair<MODE_MX, ATTN_EXP_SCHRAUDOLPH>(q, k, v, p, grid, st)
                                                 : launch_pair<MODE_MX, ATTN_EXP_MITCHELL_P>(q, k, v, p, grid, st);
+        if (mode == MODE_NVFP4)
+            return expm == ATTN_EXP_SCHRAUDOLPH ? launch_pair<MODE_NVFP4, ATTN_EXP_SCHRAUDOLPH>(q, k, v, p, grid, st)
+                                                : launch_pair<MODE_NVFP4, ATTN_EXP_MITCHELL_P>(q, k, v, p, grid, st);
         return cudaErrorInvalidValue;
     }
     if (mode == MODE_BF16) return D == 128 ? launch_t<2, 128, MODE_BF16>(q, k, v, p, grid, st)
@@ -1304,6 +1367,7 @@ cudaError_t launch_attn(int mode, int expm, int D, const void* q, const void* k,
                                                : launch_t<1, 64, MODE_E4M3_COL>(q, k, v, p, grid, st);
     if (mode == MODE_MX && D == 128) return launch_pair<MODE_MX>(q, k, v, p, grid, st);
     if (mode == MODE_MX_EXACT && D == 128) return launch_pair<MODE_MX_EXACT>(q, k, v, p, grid, st);
+    if (mode == MODE_NVFP4 && D == 128) return launch_pair<MODE_NVFP4>(q, k, v, p, grid, st);
     return cudaErrorInvalidValue;
 }
 

@@ -62,7 +62,7 @@ namespace pa {
 // Every synchronous check of attn_fp8_fwd, in its order; the workspace is checked
 // only when check_workspace is set (the no-allocation entry point has none).
 // *mode receives the kernel mode (1 E4M3 one scale per tile, 2 E4M3 per-column
-// scales, 3 MX).
+// scales, 3 MX, 4 MX with per-token V, 5 NVFP4 Q K^T with E4M3 V).
 attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const attn_qtensor* v,
                           const attn_shape* shape, int causal, int causal_exact, float softmax_scale, const void* o,
                           const float* lse, bool check_workspace, void* workspace, size_t workspace_bytes,
@@ -77,7 +77,14 @@ attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const at
     if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
     if (check_workspace && (st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
     const bool mx = q->layout == ATTN_MX_ROW32;
-    if (mx) {
+    const bool nv = q->layout == ATTN_NVFP4;
+    if (nv) {
+        // mixed NVFP4/FP8: NVFP4 Q and K, E4M3 V with one scale per 128-token block
+        if (k->layout != ATTN_NVFP4 || v->layout != ATTN_E4M3_TOKBLOCK) return ATTN_ERR_INVALID_ARG;
+        if (q->block != 128 || k->block != 128 || v->block != 128) return ATTN_ERR_INVALID_ARG;
+        if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+        if (causal_exact) return ATTN_ERR_UNSUPPORTED;   // the 128-token block scales span later tokens
+    } else if (mx) {
         if (k->layout != ATTN_MX_ROW32 || (v->layout != ATTN_MX_COL32 && v->layout != ATTN_MX_TOKEN))
             return ATTN_ERR_INVALID_ARG;
         if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
@@ -97,6 +104,7 @@ attn_status fp8_fwd_check(const attn_qtensor* q, const attn_qtensor* k, const at
         return ATTN_ERR_INVALID_ARG;
     *mode = v->layout == ATTN_MX_TOKEN ? 4 : 3;
     if (!mx) *mode = (q->block == 128 && k->block == 128 && v->block == 128 && !causal_exact) ? 1 : 2;
+    if (nv) *mode = 5;
     return ATTN_OK;
 }
 
@@ -219,7 +227,7 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
     WorkItem* items = reinterpret_cast<WorkItem*>(ws + L.items_off);
     float* vref = reinterpret_cast<float*>(ws + L.vref_off);
     float4* tsc = reinterpret_cast<float4*>(ws + L.tsc_off);
-    const bool e4m3 = mode == 1 || mode == 2;
+    const bool e4m3 = mode == 1 || mode == 2 || mode == 5;   // fp32 block scales (NVFP4: Q, K's 128-token ones)
 
     SchedParams sp;
     sp.cu = shape->cu_seqlens;
@@ -281,7 +289,7 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
         vp.T = T;
         vp.exact = exact;
         vp.bv = qv->block;
-        vp.tiles = (mode == 1 && !exact) ? 1 : 0;
+        vp.tiles = ((mode == 1 || mode == 5) && !exact) ? 1 : 0;
         vp.bk = qk->block;
         vp.sk = fp.sk;
         vp.sk_cap = fp.capk;
@@ -290,6 +298,12 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
         vp.tsc_cap = L.tsc_cap;
         fp.tsc = tsc;
         fp.tsc_cap = L.tsc_cap;
+        if (mode == 5) {   // NVFP4: the 16-channel scale tiles after the fp32 block scales
+            const size_t off = nvfp4_sf_offset(H, tiles_cap(shape));
+            fp.mq = static_cast<const uint8_t*>(qq->scales) + off;
+            fp.mk = static_cast<const uint8_t*>(qk->scales) + off;
+            fp.ntcap = tiles_cap(shape);
+        }
         if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     } else if (mode == 3 || mode == 4) {
         fp.mq = static_cast<const uint8_t*>(qq->scales);
@@ -343,7 +357,7 @@ attn_status attn_fp8_fwd_ex(const attn_qtensor* q, const attn_qtensor* k, const 
     if (st != ATTN_OK) return st;
     if (exp_mode < ATTN_EXP_HW || exp_mode > ATTN_EXP_MITCHELL_P) return ATTN_ERR_INVALID_ARG;
     // the bit-level exponentials: the pair kernel's E4M3 tile and MX paths (inference)
-    if (exp_mode != ATTN_EXP_HW && (shape->head_dim != 128 || (mode != 1 && mode != 3)))
+    if (exp_mode != ATTN_EXP_HW && (shape->head_dim != 128 || (mode != 1 && mode != 3 && mode != 5)))
         return ATTN_ERR_UNSUPPORTED;
     return forward(mode, exp_mode, q->codes, k->codes, v->codes, q, k, v, shape, causal != 0, causal_exact != 0,
                    softmax_scale, q->rotated, o, lse, workspace, static_cast<cudaStream_t>(stream));

@@ -151,6 +151,11 @@ constexpr uint32_t idesc_mx(uint32_t afmt, uint32_t bfmt, bool a_mn, bool b_mn, 
            (a_sf << 29);
 }
 
+// kind::mxf4nvf4: A and B E2M1 (format 1), K-major, scale factors UE4M3 (scale type 0)
+constexpr uint32_t idesc_nvf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -185,6 +190,17 @@ __device__ __forceinline__ void mma_mxf8_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d_tmem),
         "r"(a_tmem), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc));
+}
+// NVFP4 (kind::mxf4nvf4, scale_vec::4X): E2M1 A and B, K = 64 per MMA, an E4M3 scale
+// per 16 elements, the four of a row's K step in one 32-bit TMEM column (row r at lane
+// r % 32, column r / 32 of the step's four)
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t sfa,
+                                         uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc));
 }
 // 32 lanes x 128 bits from shared memory, replicated into the four 32-lane
 // quarters of TMEM (the scale-factor copy of block-scaled MMAs)

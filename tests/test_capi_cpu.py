@@ -194,6 +194,33 @@ def test_exp_mode_rules_on_host(pa):
                              pa.ATTN_EXP_SCHRAUDOLPH, fake, fake, fake, 16, None) == pa.ATTN_ERR_WORKSPACE
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses placeholder device pointers; only run where no GPU could be reached")
+def test_nvfp4_forward_rules_on_host(pa):
+    """The mixed NVFP4/FP8 forward: NVFP4 Q needs NVFP4 K and an E4M3 V in 128-token
+    blocks (else invalid), head_dim 128 and no causal-exact mode (else unsupported)."""
+    L = pa.lib()
+    fake = 1 << 20
+    shape = pa._Shape(256, 2, 128, 1, None)
+    big = pa.attn_workspace_size(256, 2, 128, 1)
+
+    def call(q, k, v, shp=shape, causal=0, exact=0):
+        return L.attn_fp8_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(shp), causal, exact,
+                              0.0, fake, fake, fake, big, None)
+
+    nq = pa._QT(fake, fake, pa.ATTN_NVFP4, 128, 0, 1, 7)
+    e = pa._QT(fake, fake, 0, 128, 0, 1, 7)
+    ev = pa._QT(fake, fake, 0, 128, 0, 0, 0)
+    ev64 = pa._QT(fake, fake, 0, 64, 0, 0, 0)
+    mcol = pa._QT(fake, fake, pa.ATTN_MX_COL32, 32, 0, 0, 0)
+    assert call(nq, e, ev) == pa.ATTN_ERR_INVALID_ARG            # K must be NVFP4 too
+    assert call(nq, nq, ev64) == pa.ATTN_ERR_INVALID_ARG         # V blocks of 128 tokens
+    assert call(nq, nq, mcol) == pa.ATTN_ERR_INVALID_ARG         # V in E4M3
+    assert call(nq, nq, ev, causal=1, exact=1) == pa.ATTN_ERR_UNSUPPORTED
+    nk8 = pa._QT(fake, fake, pa.ATTN_NVFP4, 128, 0, 1, 8)
+    assert call(nq, nk8, ev) == pa.ATTN_ERR_SEED_MISMATCH
+
+
 def test_test_build_exports_the_probability_dump_and_the_timed_library_does_not(pa):
     """libpa_gb300_pdump.so (include/attn_pdump.h) is the parity tests' build: it
     exports every call of include/attn.h plus attn_pdump_set; the library that

@@ -34,13 +34,16 @@ pytestmark = pytest.mark.gpu
 E4M3, ROW, COL = 0, 1, 2
 
 
-def quantise_both(inp, mx, block, rotate=True):
+def quantise_both(inp, mx, block, rotate=True, nv=False):
     seed = 0x5EED0000 + inp.wid
     q, k, v, cu = to_device(inp)
     T, H, d = q.shape
     ws = pa.workspace(T, H, d, cu.numel() - 1)
     ocu = inp.cu_seqlens
-    if mx:
+    if nv:    # mixed NVFP4 / FP8: NVFP4 Q, K; E4M3 V in 128-token blocks
+        lay = (pa.ATTN_NVFP4, pa.ATTN_NVFP4, E4M3)
+        blk = 128
+    elif mx:
         lay = (ROW, ROW, pa.ATTN_MX_TOKEN if block == 1 else COL)
         blk = 32
     else:
@@ -49,7 +52,8 @@ def quantise_both(inp, mx, block, rotate=True):
     rot = (rotate, rotate, False)
     sd = (seed, seed, 0)
     G = [pa.attn_quantize(x, cu, L, blk, r, s_, ws=ws) for x, L, r, s_ in zip((q, k, v), lay, rot, sd)]
-    olay = tuple(oracle.MX_TOKEN if L == pa.ATTN_MX_TOKEN else L for L in lay)
+    olay = tuple(oracle.MX_TOKEN if L == pa.ATTN_MX_TOKEN else oracle.NVFP4 if L == pa.ATTN_NVFP4 else L
+                 for L in lay)
     O = [oracle.quantize_tensor(x, ocu, L, blk, r, s_) for x, L, r, s_ in zip((inp.q, inp.k, inp.v), olay, rot, sd)]
     for g_, o_ in zip(G, O):
         assert np.array_equal(g_.codes.cpu().numpy(), o_.codes)
@@ -61,8 +65,8 @@ def key_stride(cu):
     return max(128, (L + 127) // 128 * 128)
 
 
-def check_given_codes(inp, mx, block, causal, exact=False, rows=None, exp_mode=0):
-    (Q, K, V), (Qo, Ko, Vo), cu = quantise_both(inp, mx, block)
+def check_given_codes(inp, mx, block, causal, exact=False, rows=None, exp_mode=0, nv=False):
+    (Q, K, V), (Qo, Ko, Vo), cu = quantise_both(inp, mx, block, nv=nv)
     o_ref, l_ref = pa.attn_fp8_fwd_ex(Q, K, V, cu, causal, exact, 0.0, exp_mode)
     ks = key_stride(inp.cu_seqlens)
     o, lse, codes = pa.attn_fp8_fwd_pdump(Q, K, V, cu, ks, causal, exact, exp_mode=exp_mode)
@@ -143,3 +147,31 @@ def test_bit_level_exponentials_long_documents(oracle_mod, wid, mx, causal, exp_
     rows = np.unique(np.concatenate([np.arange(0, 96), np.arange(2048, 2144), np.array([127, 128, 2047, T - 1]),
                                      rng.choice(T, 160, replace=False)])).astype(np.int32)
     check_given_codes(inp, mx, 32 if mx else 128, causal, rows=rows, exp_mode=exp_mode)
+
+
+# mixed NVFP4 / FP8 (FLAMIA sections 1 and 2): S from NVFP4 Q and K through the
+# block-scaled FP4 MMA, P V in E4M3
+NV_CASES = [
+    (2, [300, 77, 129], False, 0),
+    (3, [300, 77, 129], True, 0),
+    (4, [256, 1, 130], False, 0),
+    (5, [300, 77, 129, 1], True, 0),
+    (2, [300, 77, 129], False, 1),     # with Schraudolph's exponential
+    (3, [300, 77, 129], True, 2),      # with log-domain P (Mitchell-P over NVFP4)
+]
+
+
+@pytest.mark.parametrize("wid,lengths,causal,exp_mode", NV_CASES)
+def test_nvfp4_qk_codes_and_output(oracle_mod, wid, lengths, causal, exp_mode):
+    inp = workloads.make(wid, heads=2, lengths=lengths)
+    check_given_codes(inp, False, 128, causal, exp_mode=exp_mode, nv=True)
+
+
+@pytest.mark.parametrize("wid,causal", [(2, False), (3, True)])
+def test_nvfp4_qk_long_documents(oracle_mod, wid, causal):
+    inp = workloads.make(wid, heads=4, lengths=[2048, 2048])
+    rng = np.random.default_rng(300 + wid)
+    T = inp.T
+    rows = np.unique(np.concatenate([np.arange(0, 96), np.arange(2048, 2144), np.array([127, 128, 2047, T - 1]),
+                                     rng.choice(T, 160, replace=False)])).astype(np.int32)
+    check_given_codes(inp, False, 128, causal, rows=rows, nv=True)
