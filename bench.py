@@ -55,12 +55,14 @@ def fp8_peak():
     return 2.0 * 1900.0, "fallback 1.9 PFLOP/s bf16 x2"
 
 
-def attn_traffic(args):
-    """DRAM bytes per attention launch from the committed ncu summary, or None
-    when the kernel source changed since the capture or the workload differs."""
+def recorded_traffic(args, name, sources, key="bytes_per_launch"):
+    """DRAM bytes from a committed ncu summary (profiles/<name>), or None when the
+    kernel source changed since the capture or the workload differs (the
+    captures are of workload 2 at full size, hardware exp2, E4M3)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.txt")
-    if args.workload != 2 or args.heads or args.seqlen or args.batch or not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", name)
+    if (args.workload != 2 or args.heads or args.seqlen or args.batch or args.exact or args.nvfp4
+            or args.exp_mode != "hw" or args.no_rotate or not os.path.exists(path)):
         return None
     kv = {}
     for line in open(path):
@@ -68,11 +70,20 @@ def attn_traffic(args):
             a, b = line.split(":", 1)
             kv[a.strip()] = b.strip()
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "ptx.cuh", "params.h"):
+    for f in sources:
         h.update(open(os.path.join(ROOT, "precision_attention_gb300", "csrc", f), "rb").read())
     if h.hexdigest()[:16] != kv.get("source_sha256_prefix"):
         return None
-    return float(kv["bytes_per_launch"])
+    return float(kv[key])
+
+
+def attn_traffic(args):
+    return recorded_traffic(args, "attn_fwd_traffic.txt", ("attn_fwd.cu", "ptx.cuh", "params.h"))
+
+
+def quant_traffic(args):
+    """DRAM bytes of one step's three quantiser launches (Q, K, V)."""
+    return recorded_traffic(args, "quant_traffic.txt", ("quant.cu", "ptx.cuh", "params.h"), "bytes_per_step")
 
 
 def hbm_peak():
@@ -665,7 +676,7 @@ def main():
                          "frac_vs_mma_rate": (achieved / mma_rate) if mma_rate else None},
             "quant_roofline": {"bound": "hbm", "kernel": "quant_tile_kernel (three launches: Q, K, V)",
                                "achieved": quant_gbs, "peak": hbm, "unit": "GB/s", "frac": quant_gbs / hbm,
-                               "bytes_per_step": qbytes, "peak_basis": hbm_basis},
+                               "bytes_per_step": qbytes, "peak_basis": hbm_basis, "traffic": quant_traffic(args)},
             "attn_ms": r["attn_ms"], "quant_ms": r["quant_ms"], "timing_stats": r["stats"],
             "clocks": r["clocks"], "accuracy": r["acc"], "bf16_path": r.get("bf16"),
             "per_workload": r.get("per_workload"), "bit_level_exp": r.get("bit_level_exp")}
