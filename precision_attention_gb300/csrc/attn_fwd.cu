@@ -605,7 +605,8 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
 // buffers per query tile at 128 + 32 (2q + b), so the softmax of tile j writes P
 // while P V of tile j - 1 may still read the other one; MX one buffer per query
 // tile at 176 + 32q, beside the block-scaled MMAs' scale factors at [128,176).
-// A K slot is released after both S_0j and S_1j, a V slot after both P V of tile j.
+// A K slot is released by S_1j's completion (S_1j is issued after S_0j completed), a V
+// slot after both P V of tile j.
 template <int MODE>
 struct PairCfgT {
     // MX: Q K^T block-scaled (scale factors of Q and K in TMEM); MXPV: P V block-scaled
@@ -686,7 +687,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&B->q_full, 1);
-        mbar_init(&B->q_empty, 2);
+        mbar_init(&B->q_empty, 1);   // S_1 of an item's last key tile (after S_0's)
         for (int q = 0; q < 2; q++) {
             mbar_init(&B->s_full[q], 1);
             mbar_init(&B->s_empty[q], 128);
@@ -698,7 +699,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         for (int i = 0; i < PC::NS; i++) {
             mbar_init(&B->k_full[i], 1);
             mbar_init(&B->v_full[i], 1);
-            mbar_init(&B->k_empty[i], 2);
+            mbar_init(&B->k_empty[i], 1);   // S_1 of the key tile (after S_0's)
             mbar_init(&B->v_empty[i], 2);
         }
         mbar_init(&B->drain[0], 1);
@@ -846,8 +847,9 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         // neither chain S_q -> softmax_q -> P_q V waits behind the other's. Each issues
         // in a fixed order with S one key tile ahead of P V (across item boundaries):
         //   S_0 | S_1 P V_0 | S_2 P V_1 | ...
-        // and parks on the one barrier it needs (mbarrier.try_wait). A K, V or Q slot
-        // is released once both issuers have committed their MMAs that read it.
+        // and parks on the one barrier it needs (mbarrier.try_wait). A V slot is released
+        // once both issuers have committed their P V that read it, a K slot (and the Q
+        // tiles) by issuer 1's S commit.
         if (lane == 0) {
             const int q = warp == 1 ? 0 : 1;
             constexpr uint32_t id_s = idesc(0, 0, false, false, 128, 128);
@@ -924,10 +926,13 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                         mma_f8(tS, dq + koff<1, 128, MODE>(kk), dk + koff<1, 128, MODE>(kk), id_s, kk ? 1u : 0u);
                 }
                 tc_commit(&B->s_full[q]);
-                tc_commit(&B->k_empty[st]);
+                // S_1(g) is issued only once S_0(g) has completed (its row loads freed the
+                // buffer), so S_1's completion alone releases the K slot and, after an
+                // item's last key tile, the Q tiles
+                if (q == 1) tc_commit(&B->k_empty[st]);
                 gS++;
                 if (++jS == wS.ntiles) {   // last S of the item: Q may be replaced
-                    tc_commit(&B->q_empty);
+                    if (q == 1) tc_commit(&B->q_empty);
                     jS = 0;
                     qiS++;
                     itS = item_of(++kS);

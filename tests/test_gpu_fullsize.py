@@ -76,3 +76,42 @@ def test_full_size_codes_and_sampled_rows(oracle_mod, wid, exact):
     res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
     print(f"workload {wid}{' exact' if exact else ''}: {len(rows)} rows x {H} heads:", res)
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("wid,exp_mode", [(2, 0), (3, 0), (2, 1), (3, 2)])
+def test_full_size_nvfp4_qk_and_bit_level_exponentials(oracle_mod, wid, exp_mode):
+    """The mixed NVFP4/FP8 path at the fa3 configurations' full size (NVFP4 Q, K codes
+    and both scale levels bit-exact, sampled rows within the parity bounds), with the
+    hardware exp2 and with the bit-level exponentials (Schraudolph, log-domain P)."""
+    w = workloads.WORKLOADS[wid]
+    inp = workloads.make(wid)
+    T, H, d = inp.q.shape
+    cu = inp.cu_seqlens
+    nd = len(cu) - 1
+    q, k, v, cu_d = to_device(inp)
+    ws = pa.workspace(T, H, d, nd)
+    seed = w.hadamard_seed
+    Q = pa.attn_quantize(q, cu_d, pa.ATTN_NVFP4, 128, True, seed, ws=ws)
+    K = pa.attn_quantize(k, cu_d, pa.ATTN_NVFP4, 128, True, seed, ws=ws)
+    V = pa.attn_quantize(v, cu_d, E4M3, 128, False, 0, ws=ws)
+    o, lse = pa.attn_fp8_fwd_ex(Q, K, V, cu_d, w.causal, False, 0.0, exp_mode, ws=ws)
+    st, flags = pa.attn_read_device_status(ws)
+    assert st == 0, (st, flags)
+    Qo = oracle.quantize_tensor(inp.q, cu, oracle.NVFP4, 128, True, seed)
+    Ko = oracle.quantize_tensor(inp.k, cu, oracle.NVFP4, 128, True, seed)
+    Vo = oracle.quantize_tensor(inp.v, cu, E4M3, 128, False, 0)
+    for name, g, c in (("Q", Q, Qo), ("K", K, Ko)):
+        assert np.array_equal(g.codes.cpu().numpy(), c.codes), name
+        g_st, g_sf = (t.cpu().numpy() for t in pa.nvfp4_scales(g, nd))
+        nb = c.scales[0].shape[1]
+        assert np.array_equal(g_st[:, :nb].view(np.uint32), c.scales[0].view(np.uint32)), name
+        both = np.concatenate([mx_row_tiles_to_logical(g_sf[:, :, :512], cu, T, H),
+                               mx_row_tiles_to_logical(g_sf[:, :, 512:], cu, T, H)], axis=2)
+        assert np.array_equal(both, c.scales[1]), name
+    assert np.array_equal(V.codes.cpu().numpy(), Vo.codes)
+    rows = sample_rows(cu, T, seed=100 + wid)
+    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, False, None, rows=rows, ties=True,
+                                              rescale_tau=pa.rescale_threshold(d), exp_mode=exp_mode)
+    res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
+    print(f"workload {wid} NVFP4 Q K^T, exp mode {exp_mode}: {len(rows)} rows x {H} heads:", res)
+    assert res["ok"], res
