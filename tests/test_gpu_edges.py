@@ -124,3 +124,37 @@ def test_valid_forward_after_bad_seqlens_on_same_workspace(oracle_mod, block):
     assert res["ok"], res
     st, flags = pa.attn_read_device_status(ws)
     assert st == pa.ATTN_ERR_BAD_SEQLENS and flags == (1 << pa.ATTN_ERR_BAD_SEQLENS)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_nvfp4_empty_and_many_documents(oracle_mod, causal):
+    """The mixed NVFP4/FP8 path on zero-length documents inside the batch and on
+    1,500 documents of 1 .. 40 tokens: every device probability code checked
+    against the emulation, the output under the plain bounds."""
+    from test_gpu_ties import check_given_codes
+    wid = 3 if causal else 2
+    check_given_codes(workloads.make(wid, heads=2, lengths=EMPTY_DOCS), False, 128, causal, nv=True)
+    lengths = np.random.default_rng(77 + wid).integers(1, 41, size=1500).tolist()
+    check_given_codes(workloads.make(wid, heads=2, lengths=lengths), False, 128, causal, nv=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_nvfp4_all_zero_inputs_closed_form(causal):
+    """Q = K = V = 0 through NVFP4 Q, K: zero block scales and codes, every score 0:
+    O = 0 exactly and lse = ln(visible keys)."""
+    inp = workloads.make(2, heads=2, lengths=[200, 77, 129])
+    q, k, v, cu = to_device(inp)
+    q.zero_()
+    k.zero_()
+    v.zero_()
+    T, H, d = q.shape
+    ws = pa.workspace(T, H, d, cu.numel() - 1)
+    Q = pa.attn_quantize(q, cu, pa.ATTN_NVFP4, 128, True, 5, ws=ws)
+    K = pa.attn_quantize(k, cu, pa.ATTN_NVFP4, 128, True, 5, ws=ws)
+    V = pa.attn_quantize(v, cu, pa.ATTN_E4M3_TOKBLOCK, 128, False, 0, ws=ws)
+    o, lse = pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws)
+    st, _ = pa.attn_read_device_status(ws)
+    assert st == 0
+    assert int(torch.count_nonzero(o.float())) == 0
+    want = np.log(visible_keys(inp.cu_seqlens, causal))
+    assert np.abs(lse.double().cpu().numpy() - want[None, :]).max() <= 1e-5 * np.maximum(1.0, want).max()
