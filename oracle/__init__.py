@@ -83,6 +83,8 @@ def lib():
             L.or_e4m3_encode_range.argtypes = [u64, u64, vp]
             L.or_signs.argtypes = [u64, i32, vp]
             L.or_fwht_f32.argtypes = [vp, i32]
+            L.or_rotation_channel.argtypes = [i32, i32]
+            L.or_rotation_channel.restype = i32
             L.or_splitmix64_next.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
             L.or_splitmix64_next.restype = u64
             L.or_num_blocks.argtypes = [vp, i32, i32, i32]
@@ -92,7 +94,7 @@ def lib():
             L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
             L.or_attention_fp64_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, vp, vp]
             L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
-                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp]
+                i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
             L.or_attention_emulate_given_p.argtypes = [ctypes.POINTER(_QT)] * 3 + [
                 i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp,
@@ -187,6 +189,18 @@ def fwht(x) -> np.ndarray:
         lib().or_fwht_f32(row.ctypes.data, row.size)
         flat[r] = row
     return flat.reshape(y.shape)
+
+
+def rotation_channels(d: int) -> np.ndarray:
+    """pi: the rotation stores the transform's output channel pi[p] at channel p."""
+    return np.array([lib().or_rotation_channel(p, d) for p in range(d)], dtype=np.int64)
+
+
+def rotate(x, seed: int) -> np.ndarray:
+    """The quantiser's rotation of x [..., d] in fp32: sign flip, transform, stored order."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    return fwht(x * signs(seed, d))[..., rotation_channels(d)]
 
 
 def num_blocks(cu_seqlens, T: int, block: int) -> int:
@@ -343,12 +357,14 @@ def exp2_mitchell_code(x) -> np.ndarray:
 
 def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causal=False,
                       exact=False, softmax_scale=None, rows=None, quantize_p=True, ties=False, rescale_tau=0.0,
-                      exp_mode=EXP_HW):
+                      exp_mode=EXP_HW, lse_ties=False):
     """Quantised-operand emulation. Returns (o fp32 [R,H,d], o_bf16 u16 [R,H,d], lse fp32 [H,R]),
     and with ties=True a fourth array [R,H,d]: the tie allowance (how far E4M3
     probability codes that sit within rounding of a code boundary can move each
-    output element). rescale_tau: a row's reference maximum moves only when a
-    key tile's maximum exceeds it by more than this (log2 units; 0 = exact).
+    output element); with lse_ties=True as well a fifth [H,R], the same for lse
+    (non-zero under the log-domain P only, whose row sum adds the codes' values).
+    rescale_tau: a row's reference maximum moves only when a key tile's maximum
+    exceeds it by more than this (log2 units; 0 = exact).
     exp_mode: EXP_HW (2^x), EXP_SCHRAUDOLPH or EXP_MITCHELL_P."""
     T, H, d = q.codes.shape
     if q.layout == NVFP4:
@@ -363,15 +379,19 @@ def attention_emulate(q: QTensor, k: QTensor, v: QTensor, cu_seqlens=None, causa
     ob = np.zeros((R, H, d), dtype=np.uint16)
     lse = np.zeros((H, R), dtype=np.float32)
     amb = np.zeros((R, H, d), dtype=np.float32) if ties else None
+    lamb = np.zeros((H, R), dtype=np.float32) if (ties and lse_ties) else None
     qq, kk, vv = q._qt(), k._qt(), v._qt()
     st = lib().or_attention_emulate(ctypes.byref(qq), ctypes.byref(kk), ctypes.byref(vv), T, H, d,
                                     _ptr(cu), nd, int(bool(causal)), int(bool(exact)),
                                     int(bool(q.rotated)), scale, float(rescale_tau),
                                     (QUANTIZE_P if quantize_p else 0) | _EXP_FLAGS[exp_mode],
                                     _ptr(r), R, o.ctypes.data, ob.ctypes.data, lse.ctypes.data,
-                                    None if amb is None else amb.ctypes.data)
+                                    None if amb is None else amb.ctypes.data,
+                                    None if lamb is None else lamb.ctypes.data)
     if st != 0:
         raise ValueError(f"oracle emulation rejected its arguments (status {st})")
+    if lamb is not None:
+        return o, ob, lse, amb, lamb
     return (o, ob, lse, amb) if ties else (o, ob, lse)
 
 

@@ -174,7 +174,12 @@ uint16_t or_bf16_rne(float x) {
 /* Sylvester one (H H^T = d I), applied as a fast Walsh-Hadamard transform   */
 /* with stages h = 1, 2, 4, ..., d/2 in that order, each butterfly           */
 /* (a, b) -> (a + b, a - b) rounded to fp32. The 1/d is left to the score    */
-/* scale.                                                                    */
+/* scale. The pages ask for a Hadamard matrix, not for a row order: at       */
+/* d = 128 the rotation stores the transform's output channel pi(p) at      */
+/* channel p, pi swapping the 3-bit fields at bits 1-3 and 4-6 of the index  */
+/* (rows of the Sylvester matrix permuted: still a Hadamard matrix, R R^T =  */
+/* d I, so the rotation still cancels in Q K^T); at d = 64 pi is the         */
+/* identity.                                                                 */
 /* ------------------------------------------------------------------------- */
 uint64_t or_splitmix64_next(uint64_t* state) {
     uint64_t z = (*state += 0x9E3779B97F4A7C15ULL);
@@ -196,6 +201,11 @@ void or_fwht_f32(float* x, int d) {
                 x[i] = a + b;
                 x[i + h] = a - b;
             }
+}
+
+int or_rotation_channel(int p, int d) {
+    if (d != 128) return p;
+    return (p & 1) | (((p >> 4) & 7) << 1) | (((p >> 1) & 7) << 4);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -251,7 +261,12 @@ typedef struct {
 static void rotated_row(const quant_ctx* c, int t, int h, float* y) {
     const float* src = c->x + ((long)t * c->H + h) * c->d;
     for (int j = 0; j < c->d; j++) y[j] = c->rotate ? c->signs[j] * src[j] : src[j];
-    if (c->rotate) or_fwht_f32(y, c->d);
+    if (c->rotate) {
+        float t[256];
+        or_fwht_f32(y, c->d);
+        for (int p = 0; p < c->d; p++) t[p] = y[or_rotation_channel(p, c->d)];
+        for (int p = 0; p < c->d; p++) y[p] = t[p];
+    }
 }
 
 /* E4M3 token block (reading: scale = amax / 448 with IEEE division, codes from
@@ -660,7 +675,7 @@ uint8_t or_exp2_mitchell_code(double x) {
 /* ------------------------------------------------------------------------- */
 typedef struct {
     const or_qtensor *q, *k, *v; int T, H, d; docs_t D; int causal, exact, rotated; double scale;
-    int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse; float* amb;
+    int flags; const int32_t* rows; int nrows; float* o; uint16_t* ob; float* lse; float* amb; float* lamb;
     double dec[256];
     float tau;                   /* rescale threshold of the running max, log2 units */
     int expm;                    /* 0: 2^x; OR_EMU_EXP_SCHRAUDOLPH or OR_EMU_EXP_MITCHELL_P */
@@ -709,9 +724,11 @@ static void emu_decode_unit(void* vc, long t) {
 
 /* One key under a bit-level exponential: x is the exponent with the V ratio
  * r folded in, dx its error band. Sets ph[a] (the probability P V uses, the
- * device's code where given) and tie[a], and adds the key's share to rowsum. */
+ * device's code where given) and tie[a], and adds the key's share to rowsum
+ * (and, log-domain P, its tie band to rowtie). */
 static void emu_bitexp_key(const emu_ctx* c, int a, double x, double r, double dx, const uint8_t* gcodes,
-                           double* ph, double* tie, double* rowsum, long* n_same, long* n_tie, long* n_bad) {
+                           double* ph, double* tie, double* rowsum, double* rowtie, long* n_same, long* n_tie,
+                           long* n_bad) {
     const int schr = c->expm == OR_EMU_EXP_SCHRAUDOLPH;
     float pf = 0.0f;
     uint8_t own, lo, hi;
@@ -742,6 +759,7 @@ static void emu_bitexp_key(const emu_ctx* c, int a, double x, double r, double d
     } else {
         ph[a] = c->dec[use];
         *rowsum += c->dec[use] / r;
+        *rowtie += tie[a] / r;
     }
 }
 
@@ -787,6 +805,7 @@ static void emu_unit(void* vc, long ri) {
     const float inv_ref = ref > 0.0f ? 1.0f / ref : 0.0f;   /* rounded once per row */
 
     float m = -INFINITY, l = 0.0f;
+    double lt = 0.0;             /* tie band of l (log-domain P) */
     float O[256];
     double Am[256];
     for (int x = 0; x < d; x++) O[x] = 0.0f, Am[x] = 0.0;
@@ -827,7 +846,7 @@ static void emu_unit(void* vc, long ri) {
         float mcand = mt > m ? mt : m;
         float mnew = (m == -INFINITY || mcand > m + c->tau) ? mcand : m;
         float alpha = (m == -INFINITY) ? 0.0f : (float)exp2((double)m - (double)mnew);
-        double rowsum = 0.0;
+        double rowsum = 0.0, rowtie = 0.0;
         for (int a = 0; a < kn; a++) {
             double r = 1.0;
             if (!vmx) {
@@ -838,7 +857,7 @@ static void emu_unit(void* vc, long ri) {
                 emu_bitexp_key(c, a, (double)sp[a] - (double)mnew + 8.0 + log2(r), r,
                                ldexp(at[a] + amax, -20) +
                                    ldexp(fabs((double)sp[a]) + fabs((double)mnew) + 8.0, -21) + ldexp(1.0, -15),
-                               prow ? prow + k0 : NULL, ph, tie, &rowsum, &n_same, &n_tie, &n_bad);
+                               prow ? prow + k0 : NULL, ph, tie, &rowsum, &rowtie, &n_same, &n_tie, &n_bad);
                 continue;
             }
             double pt = exp2((double)sp[a] - (double)mnew + 8.0);
@@ -869,6 +888,7 @@ static void emu_unit(void* vc, long ri) {
             }
         }
         l = alpha * l + (float)rowsum;
+        lt = (double)alpha * lt + rowtie;
         for (int x = 0; x < d; x++) {
             double acc = 0.0, ta = 0.0;
             for (int a = 0; a < kn; a++) {
@@ -899,15 +919,18 @@ static void emu_unit(void* vc, long ri) {
     }
     c->lse[(long)h * c->nrows + ri] =
         (l > 0.0f) ? (float)(0.6931471805599453 * ((double)m + log2((double)l) - 8.0)) : -INFINITY;
+    if (c->lamb)
+        c->lamb[(long)h * c->nrows + ri] =
+            (lt <= 0.0 || !(l > 0.0f)) ? 0.0f : (lt < (double)l ? (float)(-log1p(-lt / (double)l)) : INFINITY);
 }
 
 static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                    int T, int H, int d, const int32_t* cu, int nd,
                    int causal, int exact, int rotated, double scale, float tau, int flags,
                    const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb,
-                   const uint8_t* pg, long pstride, long* counts) {
+                   float* lamb, const uint8_t* pg, long pstride, long* counts) {
     if (d < 1 || d > 256) return OR_ERR_ARG;
-    if (pg && (!(flags & OR_EMU_QUANTIZE_P) || pstride < 1 || amb)) return OR_ERR_ARG;
+    if (pg && (!(flags & OR_EMU_QUANTIZE_P) || pstride < 1 || amb || lamb)) return OR_ERR_ARG;
     if (!(tau >= 0.0f && tau < 1.0f)) return OR_ERR_ARG;
     int expm = flags & (OR_EMU_EXP_SCHRAUDOLPH | OR_EMU_EXP_MITCHELL_P);
     if (expm == (OR_EMU_EXP_SCHRAUDOLPH | OR_EMU_EXP_MITCHELL_P)) return OR_ERR_ARG;
@@ -929,7 +952,7 @@ static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v
     memset(&c, 0, sizeof(c));
     c.q = q; c.k = k; c.v = v; c.T = T; c.H = H; c.d = d; c.D = docs_make(cu, nd, T);
     c.causal = causal; c.exact = exact; c.rotated = rotated; c.scale = scale; c.flags = flags;
-    c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse; c.amb = amb;
+    c.rows = rows; c.nrows = rows ? nrows : T; c.o = o; c.ob = ob; c.lse = lse; c.amb = amb; c.lamb = lamb;
     c.pg = pg; c.pstride = pstride; c.tau = tau; c.expm = expm;
     for (int i = 0; i < 256; i++) c.dec[i] = or_e4m3_decode((uint8_t)i);
     if (!mxq) { c.nbq = block_offset(&c.D, c.D.nd, q->block); c.nbk = block_offset(&c.D, c.D.nd, k->block); }
@@ -952,9 +975,10 @@ static int emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v
 int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                          int T, int H, int d, const int32_t* cu, int nd,
                          int causal, int exact, int rotated, double scale, float rescale_tau, int flags,
-                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb) {
+                         const int32_t* rows, int nrows, float* o, uint16_t* ob, float* lse, float* amb,
+                         float* lse_amb) {
     return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, flags, rows, nrows, o, ob,
-                   lse, amb, NULL, 0, NULL);
+                   lse, amb, lse_amb, NULL, 0, NULL);
 }
 
 /* The same emulation with a device's probability codes in place of its own
@@ -975,5 +999,5 @@ int or_attention_emulate_given_p(const or_qtensor* q, const or_qtensor* k, const
                                  const uint8_t* p_codes, long p_stride, long* counts) {
     if (!p_codes || !counts) return OR_ERR_ARG;
     return emulate(q, k, v, T, H, d, cu, nd, causal, exact, rotated, scale, rescale_tau, flags | OR_EMU_QUANTIZE_P,
-                   rows, nrows, o, ob, lse, NULL, p_codes, p_stride, counts);
+                   rows, nrows, o, ob, lse, NULL, NULL, p_codes, p_stride, counts);
 }

@@ -56,6 +56,9 @@ void     or_e4m3_encode_range(uint64_t start, uint64_t count, uint8_t* out); /* 
 uint64_t or_splitmix64_next(uint64_t* state);
 void     or_signs(uint64_t seed, int d, float* s);
 void     or_fwht_f32(float* x, int d);
+/* the transform output channel the rotation stores at channel p (d = 128: the
+ * 3-bit fields at bits 1-3 and 4-6 of p swapped; else p) */
+int      or_rotation_channel(int p, int d);
 
 /* ---- document bookkeeping ---- */
 /* number of document-local blocks of `block` tokens: sum over documents of ceil(L/block) */
@@ -120,13 +123,17 @@ uint8_t or_exp2_mitchell_code(double x);
 /* rows as for O-1; o, o_bf16: [nrows][H][d]; lse: [H][nrows].
  * amb (NULL to skip): [nrows][H][d], the part of each output element that
  * E4M3 probability codes within rounding of a code boundary could move (the
- * tie allowance described beside the implementation). */
+ * tie allowance described beside the implementation).
+ * lse_amb (NULL to skip): [H][nrows], the same for lse (natural log units):
+ * non-zero only under the log-domain P, whose row sum adds the codes' values,
+ * so that a tie there moves l as well: -ln(1 - Lt / l), Lt the sum over tied
+ * keys of |code_hi - code_lo| / r, rescaled like l. */
 
 int or_attention_emulate(const or_qtensor* q, const or_qtensor* k, const or_qtensor* v,
                          int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
                          int causal, int exact, int rotated, double softmax_scale, float rescale_tau, int flags,
                          const int32_t* rows, int nrows, float* o, uint16_t* o_bf16, float* lse,
-                         float* amb);
+                         float* amb, float* lse_amb);
 
 /* The emulation with a device's E4M3 probability codes checked and substituted
  * for its own: p_codes[(h * T + t) * p_stride + k] is the code row t of head h

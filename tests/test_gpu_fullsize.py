@@ -110,8 +110,10 @@ def test_full_size_nvfp4_qk_and_bit_level_exponentials(oracle_mod, wid, exp_mode
         assert np.array_equal(both, c.scales[1]), name
     assert np.array_equal(V.codes.cpu().numpy(), Vo.codes)
     rows = sample_rows(cu, T, seed=100 + wid)
-    _, ob, le, amb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, False, None, rows=rows, ties=True,
-                                              rescale_tau=pa.rescale_threshold(d), exp_mode=exp_mode)
-    res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb)
+    _, ob, le, amb, lamb = oracle.attention_emulate(Qo, Ko, Vo, cu, w.causal, False, None, rows=rows, ties=True,
+                                                    rescale_tau=pa.rescale_threshold(d), exp_mode=exp_mode,
+                                                    lse_ties=True)
+    res = compare_outputs(o, lse, ob, le, rows=rows, ties=amb, lse_ties=lamb)
+    res["lse_tie_max"] = float(lamb.max())
     print(f"workload {wid} NVFP4 Q K^T, exp mode {exp_mode}: {len(rows)} rows x {H} heads:", res)
     assert res["ok"], res

@@ -226,3 +226,31 @@ def test_bit_level_modes_reject_exact_and_per_token_v(oracle_mod):
         oracle_mod.attention_emulate(Q, K, V, cu, True, True, None, exp_mode=oracle_mod.EXP_SCHRAUDOLPH)
     with pytest.raises(ValueError):   # V blocks shorter than a key tile
         oracle_mod.attention_emulate(Q, K, V, cu, True, False, None, exp_mode=oracle_mod.EXP_MITCHELL_P)
+
+
+def test_log_domain_lse_tie_allowance_explains_score_rounding(oracle_mod):
+    """Under the log-domain P the row sum adds the codes' values, so a code that
+    sits within fp32 rounding of a boundary moves lse too. A relative change of
+    2^-21 in the score scale (the size of an fp32 rounding difference) flips some
+    codes; every lse change it causes lies within the emulation's lse allowance
+    (plus the continuous part, the running maximum's own shift), which is zero
+    under the hardware and Schraudolph exponentials (their row sums add
+    unquantised probabilities)."""
+    inp = workloads.make(2, heads=2, lengths=[1024, 300])
+    cu = inp.cu_seqlens
+    Q, K, V = _quant(oracle_mod, inp, False)
+    scale = 1 / math.sqrt(128)
+    mode = oracle_mod.EXP_MITCHELL_P
+    _, _, la, _, lt = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale, ties=True, exp_mode=mode,
+                                                   rescale_tau=0.75, lse_ties=True)
+    _, _, lb = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale * (1 + 2.0 ** -21), exp_mode=mode,
+                                            rescale_tau=0.75)
+    diff = np.abs(la.astype(np.float64) - lb)
+    cont = 2.0 ** -19 * (np.abs(la.astype(np.float64)) + 16.0)
+    assert np.all(lt >= 0) and np.count_nonzero(lt) > 0
+    assert np.all(diff <= lt + cont)
+    assert np.count_nonzero(diff > cont) > 0                  # some row sums did move by a flip
+    for other in (oracle_mod.EXP_HW, oracle_mod.EXP_SCHRAUDOLPH):
+        _, _, _, _, l0 = oracle_mod.attention_emulate(Q, K, V, cu, False, False, scale, ties=True,
+                                                      exp_mode=other, rescale_tau=0.75, lse_ties=True)
+        assert not l0.any()

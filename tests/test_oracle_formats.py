@@ -113,6 +113,41 @@ def sylvester(d):
     return H
 
 
+def stored_order(d):
+    """The channel order the rotation stores at head_dim 128, bit by bit: stored
+    channel p (bits p6..p0) holds the transform's output channel with bits
+    (p3 p2 p1 p6 p5 p4 p0)."""
+    if d != 128:
+        return np.arange(d)
+    out = []
+    for p in range(d):
+        bit = [(p >> i) & 1 for i in range(7)]
+        out.append(bit[0] | bit[4] << 1 | bit[5] << 2 | bit[6] << 3 | bit[1] << 4 | bit[2] << 5 | bit[3] << 6)
+    return np.array(out)
+
+
+def rotation_matrix(oracle_mod, d, seed):
+    """R = P H D: the Sylvester rows in the stored order times the sign diagonal."""
+    return sylvester(d)[stored_order(d)] * oracle_mod.signs(seed, d)[None, :]
+
+
+def test_rotation_stored_order(oracle_mod):
+    """At head_dim 128 the rotation stores the transform's outputs with the 3-bit
+    fields at bits 1-3 and 4-6 of the channel index swapped (the order the device
+    transform leaves them in); R = P H is still a Hadamard matrix, so the rotation
+    still cancels in Q K^T. At 64 the order is the natural one."""
+    pi = oracle_mod.rotation_channels(128)
+    assert np.array_equal(pi, stored_order(128))
+    assert sorted(pi) == list(range(128)) and np.array_equal(pi[pi], np.arange(128))   # an involution
+    assert [pi[p] for p in (0, 1, 2, 16, 0x0E, 0x70, 0x7F, 0x55)] == [0, 1, 16, 2, 0x70, 0x0E, 0x7F, 0x2B]
+    assert np.array_equal(oracle_mod.rotation_channels(64), np.arange(64))
+    R = rotation_matrix(oracle_mod, 128, 3)
+    assert np.array_equal(R @ R.T, 128 * np.eye(128))
+    rng = np.random.default_rng(3)
+    xi = rng.integers(-50, 50, size=(6, 128)).astype(np.float32)    # exact in fp32
+    assert np.array_equal(oracle_mod.rotate(xi, 3).astype(np.float64), xi.astype(np.float64) @ R.T)
+
+
 @pytest.mark.parametrize("d", [2, 8, 32, 64, 128])
 def test_fwht_equals_dense_hadamard(oracle_mod, d):
     H = sylvester(d)

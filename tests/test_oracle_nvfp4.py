@@ -56,9 +56,9 @@ def test_e2m1_values_are_e4m3_values_and_round_trip(oracle_mod):
 
 
 def _dense_rot(x, seed, oracle_mod):
-    from test_oracle_formats import sylvester
+    from test_oracle_formats import rotation_matrix
     d = x.shape[-1]
-    R = sylvester(d) * oracle_mod.signs(seed, d)[None, :]
+    R = rotation_matrix(oracle_mod, d, seed)
     return (x.astype(np.float64) @ R.T)
 
 

@@ -9,14 +9,14 @@ import numpy as np
 import pytest
 
 import workloads
-from test_oracle_formats import sylvester
+from test_oracle_formats import rotation_matrix
 
 E4M3, ROW, COL = 0, 1, 2
 
 
 def rotate_ref(oracle_mod, x, seed):
     d = x.shape[-1]
-    return (x.astype(np.float64) * oracle_mod.signs(seed, d)) @ sylvester(d).T
+    return x.astype(np.float64) @ rotation_matrix(oracle_mod, d, seed).T
 
 
 def e4m3_err_bound(y, unit):
@@ -46,7 +46,7 @@ def test_tokblock_scale_rule_and_error_bound(oracle_mod, rotate, block):
     assert st == 0
     y = rotate_ref(oracle_mod, x, seed) if rotate else x.astype(np.float64)
     # the fp32 transform (pinned against the dense matrix elsewhere) fixes the exact scales
-    y32 = oracle_mod.fwht(x * oracle_mod.signs(seed, d)) if rotate else x
+    y32 = oracle_mod.rotate(x, seed) if rotate else x
     qt = oracle_mod.QTensor(codes, sc, E4M3, block, rotate, seed)
     deq = oracle_mod.dequantize(qt, cu)
     # blocks are document-local and start at the document start
@@ -107,7 +107,7 @@ def test_mx_row32_rule_and_error_bound(oracle_mod, rotate):
     assert st == 0 and su.shape == (T, H, d // 32)
     y = rotate_ref(oracle_mod, x, 55) if rotate else x.astype(np.float64)
     X = su.astype(np.int64) - 127
-    y32 = oracle_mod.fwht(x * oracle_mod.signs(55, d)) if rotate else x
+    y32 = oracle_mod.rotate(x, 55) if rotate else x
     yg = y32.astype(np.float64).reshape(T, H, d // 32, 32)
     amax = np.abs(yg).max(-1)
     assert np.all(amax <= 448.0 * 2.0 ** X)                   # nothing saturates
