@@ -1,7 +1,7 @@
 """Benchmark: FP8 attention forward TFLOP/s including quantisation.
 
 One step = the whole hot path over one batch of synthetic input resident in
-HBM: rotate-and-quantise Q, K and V (three launches), then the FP8 forward
+HBM: rotate-and-quantise Q, K and V (one launch), then the FP8 forward
 (work-list, V-reference and attention launches). FLOPs = 4 B H N^2 d, halved
 for causal workloads. The default workload is the FlashAttention-3 headline
 shape: batch 2, 32 heads, sequence 8192, head_dim 128, non-causal, 0.1%
@@ -244,14 +244,21 @@ def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=No
     stream = torch.cuda.current_stream(dev)
     attn_ev, step_ev = [], []
 
+    def quantise(qi, ki, vi):
+        # one launch for the three operands (FLAMIA section 4.3); --quant-split: one per tensor
+        if args.quant_split:
+            pa.attn_quantize(qi, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
+            pa.attn_quantize(ki, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
+            pa.attn_quantize(vi, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
+        else:
+            pa.attn_quantize_qkv(qi, ki, vi, cu, lq, blk, lv, blk, rot, seed, ws=ws, outs=(Q, K, V), stream=stream)
+
     def step(record=False):
         if record:
             es = torch.cuda.Event(enable_timing=True)
             es.record(stream)
             step_ev.append(es)
-        pa.attn_quantize(q, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
-        pa.attn_quantize(k, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
-        pa.attn_quantize(v, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
+        quantise(q, k, v)
         if record:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -300,7 +307,7 @@ def time_workload(args, pa, torch, dev, wid, exact, steps, warmup, clocks_idx=No
     r["quant_ms"] = r["ms_step"] - r["attn_ms"]
     if keep:
         r.update(dict(q=q, k=k, v=v, q_h=q_h, k_h=k_h, v_h=v_h, cu=cu, ws=ws, Q=Q, K=K, V=V, o=o, lse=lse,
-                      lq=lq, lk=lk, lv=lv, blk=blk, rot=rot, seed=seed, stream=stream))
+                      lq=lq, lk=lk, lv=lv, blk=blk, rot=rot, seed=seed, stream=stream, quantise=quantise))
     else:
         r["acc"] = None if args.no_accuracy else accuracy_sample(inp, wid, q, k, v, cu, o, pa, torch)
         del q, k, v, Q, K, V, o, lse, ws
@@ -363,9 +370,7 @@ def gpu_arm(args, rank, world, local_rank):
                 stream.wait_event(d2h_done[b])      # step i - 2's output has been read back
             qi, ki, vi = sets_in[b]
             oi, li = sets_out[b]
-            pa.attn_quantize(qi, cu, lq, blk, rot, seed, ws=ws, out=Q, stream=stream)
-            pa.attn_quantize(ki, cu, lk, blk, rot, seed, ws=ws, out=K, stream=stream)
-            pa.attn_quantize(vi, cu, lv, blk, False, 0, ws=ws, out=V, stream=stream)
+            r["quantise"](qi, ki, vi)
             pa.attn_fp8_fwd_ex(Q, K, V, cu, causal, exact, 0.0, EXP_MODES[args.exp_mode], ws=ws, out=oi, lse=li,
                                stream=stream)
             comp_done[b].record(stream)
@@ -604,6 +609,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
+    ap.add_argument("--quant-split", action="store_true",
+                    help="quantise Q, K and V in three launches instead of one")
     ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")
     ap.add_argument("--nvfp4", action="store_true",
                     help="the mixed NVFP4/FP8 path: NVFP4 Q and K (Q K^T on the FP4 tensor cores), E4M3 V")
@@ -662,9 +669,11 @@ def main():
             "vs_baseline": None, "dtype": "e4m3" if not w.mx else "mxfp8 (e4m3 + e8m0)", "data": "synthetic",
             "config": config_of(args, w),
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            # per step: three quantiser launches, the work list, (E4M3 only) the V
-            # references, the attention kernel
-            "gpu_launches": (5 if w.mx else 6) * args.steps,
+            # per step: the quantiser (one launch, or three with --quant-split; each
+            # after the document-table kernel above 1,024 documents), the work list,
+            # the V references (E4M3, NVFP4 and causal-exact MX), the attention kernel
+            "gpu_launches": ((3 if args.quant_split else 1) * (2 if r["nd"] > 1024 else 1) +
+                             (2 if (w.mx and not args.exact) else 3)) * args.steps,
             "roofline": {"bound": "tensor", "kernel": kernel + " (FP8 forward call)", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": attn_traffic(args),
                          "peak_basis": peak_basis + " (of measured)",
@@ -674,7 +683,8 @@ def main():
                                                     "8192^3, best of 10, this process",
                          "mma_rate_at_clock": mma_rate,
                          "frac_vs_mma_rate": (achieved / mma_rate) if mma_rate else None},
-            "quant_roofline": {"bound": "hbm", "kernel": "quant_tile_kernel (three launches: Q, K, V)",
+            "quant_roofline": {"bound": "hbm", "kernel": ("quant_tile_kernel (three launches: Q, K, V)" if args.quant_split
+                                                      else "quant_tile_kernel (one launch: Q, K, V)"),
                                "achieved": quant_gbs, "peak": hbm, "unit": "GB/s", "frac": quant_gbs / hbm,
                                "bytes_per_step": qbytes, "peak_basis": hbm_basis, "traffic": quant_traffic(args)},
             "attn_ms": r["attn_ms"], "quant_ms": r["quant_ms"], "timing_stats": r["stats"],

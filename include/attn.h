@@ -6,6 +6,7 @@
  *
  *   attn_quantize  rotate (Q, K) and encode Q, K, V as E4M3 with per-block
  *                  scales or as MXFP8 with 32-element E8M0 scales
+ *                  (attn_quantize_qkv: the three tensors in one launch)
  *   attn_fp8_fwd   S = Q K^T per key block, running row max and row sum,
  *                  P V accumulation, final normalisation and logsumexp;
  *                  FP32 softmax statistics, BF16 output
@@ -204,13 +205,37 @@ attn_status attn_fwd_workspace_size(const attn_shape* shape, int32_t causal, siz
  *    (strides in elements; channels contiguous; 16-byte aligned rows).
  * rotate != 0: codes of H_d * diag(s) * x, s_j = -1 if bit 63 of the j-th
  *    SplitMix64 output from `hadamard_seed` is set, else +1; H_d the
- *    unnormalised Sylvester Hadamard matrix (Q and K only; V is not rotated).
+ *    unnormalised Sylvester Hadamard matrix, at d = 128 with its rows in the
+ *    order the device transform leaves them: output channel p is Sylvester
+ *    row pi(p), pi swapping the 3-bit fields at bits 1-3 and 4-6 of p (a
+ *    Hadamard matrix still: H_d H_d^T = d I); at d = 64 the natural order.
+ *    Q and K only; V is not rotated.
  * Writes out->codes and out->scales; sets out->rotated and out->hadamard_seed.
  * A scale block holding Inf or NaN raises ATTN_ERR_NONFINITE in the status word;
  * the codes and scale of such a block are then unspecified. */
 attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
                           const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed,
                           attn_qtensor* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Q, K and V in one launch: the same work as attn_quantize on each (Q and K
+ * rotated with one seed when rotate != 0, V never), the three tensors' tiles
+ * spread over one grid, so that the quantisation of a forward is a single
+ * kernel (plus, above 64 documents, the document-table kernel once).
+ * Source: FLAMIA section 4.3 (the quantisation of the forward's operands
+ * fused into one launch); the operations as for attn_quantize.
+ * q, k, v: device inputs of one dtype, one stride pair and the shape `shape`.
+ * q_out, k_out, v_out: as attn_quantize's `out`; the layouts must be a set
+ *    the forward takes: all ATTN_E4M3_TOKBLOCK with one block; ATTN_MX_ROW32
+ *    for q and k with ATTN_MX_COL32 or ATTN_MX_TOKEN for v; ATTN_NVFP4 for q
+ *    and k with ATTN_E4M3_TOKBLOCK block 128 for v. Any other set ->
+ *    ATTN_ERR_INVALID_ARG; argument errors as attn_quantize, nothing launched.
+ * Codes and scales are byte-identical to three attn_quantize calls with the
+ * same arguments; device errors go to the one status word. */
+attn_status attn_quantize_qkv(const void* q, const void* k, const void* v, int32_t in_dtype,
+                              int64_t token_stride, int64_t head_stride, const attn_shape* shape,
+                              int32_t rotate, uint64_t hadamard_seed, attn_qtensor* q_out,
+                              attn_qtensor* k_out, attn_qtensor* v_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /* FP8 attention forward over quantised operands.
  * Source: "Fused attention kernel", Implementation sketch (per key block:

@@ -8,7 +8,7 @@ missing or fails to load, every call raises.
 The functions keep the C names:
 
     attn_quantize_sizes, attn_workspace_size, attn_fwd_workspace_size,
-    attn_quantize, attn_fp8_fwd, attn_fp8_fwd_ex,
+    attn_quantize, attn_quantize_qkv, attn_fp8_fwd, attn_fp8_fwd_ex,
     attn_bf16_fwd, attn_read_device_status, attn_status_string,
     attn_device_sm_count
 """
@@ -49,7 +49,8 @@ def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
     """The reference-maximum threshold the forward uses for this head_dim."""
     return ATTN_RESCALE_THRESHOLD if (fp8 and head_dim == 128) else 0.0
 
-EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize", "attn_fp8_fwd",
+EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
+           "attn_quantize_qkv", "attn_fp8_fwd",
            "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
            "attn_set_wait_limit")
 
@@ -85,6 +86,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
     L.attn_fwd_workspace_size.argtypes = [S, i32, ctypes.POINTER(sz)]
     L.attn_quantize.argtypes = [vp, i32, i64, i64, S, i32, u64, Q, vp, sz, vp]
+    L.attn_quantize_qkv.argtypes = [vp, vp, vp, i32, i64, i64, S, i32, u64, Q, Q, Q, vp, sz, vp]
     L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     L.attn_fp8_fwd_ex.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, i32, vp, vp, vp, sz, vp]
     L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
@@ -96,7 +98,7 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_device_sm_count.argtypes = []
     L.attn_set_wait_limit.argtypes = [i64]
     for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
-              "attn_fp8_fwd", "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status",
+              "attn_quantize_qkv",              "attn_fp8_fwd", "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status",
               "attn_device_sm_count", "attn_set_wait_limit"):
         getattr(L, f).restype = ctypes.c_int32
     if hasattr(L, "attn_pdump_set"):
@@ -255,6 +257,39 @@ def attn_quantize(x: torch.Tensor, cu_seqlens: torch.Tensor | None, layout: int,
                                _stream(stream)), "attn_quantize")
     out.rotated, out.hadamard_seed = c.rotated, c.hadamard_seed
     return out
+
+
+def attn_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor | None,
+                      layout: int, block: int = 128, layout_v: int | None = None, block_v: int | None = None,
+                      rotate: bool = False, hadamard_seed: int = 0, mx_rule: int = ATTN_MX_RULE_NOSAT,
+                      ws: torch.Tensor | None = None, outs: tuple | None = None, stream=None):
+    """Quantise Q, K (layout, block; rotated when `rotate`) and V (layout_v, block_v;
+    by default the same as Q and K) in one launch. q, k, v: [T, H, d], one dtype and
+    one stride pair. Returns (q8, k8, v8) as three attn_quantize calls would."""
+    assert q.is_cuda and q.dim() == 3 and q.stride(2) == 1
+    assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
+    assert k.stride() == q.stride() and v.stride() == q.stride()
+    assert q.dtype in (torch.bfloat16, torch.float32)
+    T, H, d = q.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    layout_v = layout if layout_v is None else layout_v
+    block_v = block if block_v is None else block_v
+    if ws is None:
+        ws = workspace(T, H, d, nd, q.device)
+    if outs is None:
+        outs = (empty_qtensor(T, H, d, nd, layout, block, mx_rule, q.device),
+                empty_qtensor(T, H, d, nd, layout, block, mx_rule, q.device),
+                empty_qtensor(T, H, d, nd, layout_v, block_v, mx_rule, q.device))
+    dt = ATTN_IN_BF16 if q.dtype == torch.bfloat16 else ATTN_IN_F32
+    shape = make_shape(T, H, d, cu_seqlens)
+    cs = [o._c() for o in outs]
+    _check(lib().attn_quantize_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), dt, q.stride(0), q.stride(1),
+                                   ctypes.byref(shape), int(bool(rotate)), hadamard_seed & (2 ** 64 - 1),
+                                   ctypes.byref(cs[0]), ctypes.byref(cs[1]), ctypes.byref(cs[2]), ws.data_ptr(),
+                                   ws.numel(), _stream(stream)), "attn_quantize_qkv")
+    for o, c in zip(outs, cs):
+        o.rotated, o.hadamard_seed = c.rotated, c.hadamard_seed
+    return tuple(outs)
 
 
 def attn_fp8_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None, causal: bool = False,

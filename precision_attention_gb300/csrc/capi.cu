@@ -160,11 +160,10 @@ attn_status attn_fwd_workspace_size(const attn_shape* shape, int32_t causal, siz
     return attn_workspace_size(shape, bytes);
 }
 
-attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
-                          const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed, attn_qtensor* out,
-                          void* workspace, size_t workspace_bytes, void* stream) {
-    attn_status st = check_shape(shape);
-    if (st != ATTN_OK) return st;
+// Checks one output operand and its input against the shape and fills its kernel parameters.
+static attn_status quant_params(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
+                                const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed,
+                                const attn_qtensor* out, void* workspace, QuantParams* pp) {
     if (!x || !out || !out->codes || !out->scales) return ATTN_ERR_INVALID_ARG;
     if (in_dtype != ATTN_IN_F32 && in_dtype != ATTN_IN_BF16) return ATTN_ERR_INVALID_ARG;
     if (!valid_block(out->layout, out->block) || out->layout < 0 || out->layout > 4) return ATTN_ERR_INVALID_ARG;
@@ -174,8 +173,7 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
     if (!aligned16(x) || !aligned16(out->codes) || !aligned16(out->scales)) return ATTN_ERR_INVALID_ARG;
     if (token_stride < 1 || head_stride < 1 || (token_stride * elt) % 16 || (head_stride * elt) % 16)
         return ATTN_ERR_INVALID_ARG;
-    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
-    QuantParams p;
+    QuantParams& p = *pp;
     std::memset(&p, 0, sizeof(p));
     p.x = x;
     p.in_bf16 = in_dtype == ATTN_IN_BF16;
@@ -207,10 +205,61 @@ attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride,
                  ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
                                               ws_layout(shape->total_tokens, shape->heads, shape->num_docs).qtab_off)
                  : nullptr;
+    return ATTN_OK;
+}
+
+static void mark_rotation(attn_qtensor* out, int32_t rotate, uint64_t hadamard_seed) {
+    out->rotated = rotate != 0;
+    out->hadamard_seed = rotate ? hadamard_seed : 0;
+}
+
+attn_status attn_quantize(const void* x, int32_t in_dtype, int64_t token_stride, int64_t head_stride,
+                          const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed, attn_qtensor* out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    QuantParams p;
+    if ((st = quant_params(x, in_dtype, token_stride, head_stride, shape, rotate, hadamard_seed, out, workspace, &p)) !=
+        ATTN_OK)
+        return st;
+    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
     st = cuda_status(launch_quantize(p, out->layout, static_cast<cudaStream_t>(stream)));
+    if (st == ATTN_OK) mark_rotation(out, rotate, hadamard_seed);
+    return st;
+}
+
+attn_status attn_quantize_qkv(const void* q, const void* k, const void* v, int32_t in_dtype, int64_t token_stride,
+                              int64_t head_stride, const attn_shape* shape, int32_t rotate, uint64_t hadamard_seed,
+                              attn_qtensor* q_out, attn_qtensor* k_out, attn_qtensor* v_out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!q_out || !k_out || !v_out) return ATTN_ERR_INVALID_ARG;
+    QuantParams ps[3];
+    const void* xs[3] = {q, k, v};
+    attn_qtensor* outs[3] = {q_out, k_out, v_out};
+    for (int t = 0; t < 3; t++)
+        if ((st = quant_params(xs[t], in_dtype, token_stride, head_stride, shape, t < 2 ? rotate : 0, hadamard_seed,
+                               outs[t], workspace, &ps[t])) != ATTN_OK)
+            return st;
+    // the pairs one launch serves: Q and K alike, V in the layout the forward takes with them
+    const int lq = q_out->layout, lv = v_out->layout;
+    bool ok = k_out->layout == lq;
+    if (lq == ATTN_E4M3_TOKBLOCK)
+        ok = ok && lv == ATTN_E4M3_TOKBLOCK && k_out->block == q_out->block && v_out->block == q_out->block;
+    else if (lq == ATTN_MX_ROW32)
+        ok = ok && (lv == ATTN_MX_COL32 || lv == ATTN_MX_TOKEN);
+    else if (lq == ATTN_NVFP4)
+        ok = ok && lv == ATTN_E4M3_TOKBLOCK && v_out->block == 128;
+    else
+        ok = false;
+    if (!ok) return ATTN_ERR_INVALID_ARG;
+    if ((st = check_ws(shape, workspace, workspace_bytes)) != ATTN_OK) return st;
+    st = cuda_status(launch_quantize_qkv(ps, lq, lv, static_cast<cudaStream_t>(stream)));
     if (st == ATTN_OK) {
-        out->rotated = rotate != 0;
-        out->hadamard_seed = rotate ? hadamard_seed : 0;
+        mark_rotation(q_out, rotate, hadamard_seed);
+        mark_rotation(k_out, rotate, hadamard_seed);
+        mark_rotation(v_out, 0, 0);
     }
     return st;
 }

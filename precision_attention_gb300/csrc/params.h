@@ -89,6 +89,8 @@ bool make_tensor_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt
 int sm_count();
 
 cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st);
+// Q, K (ps[0], ps[1], layout_qk) and V (ps[2], layout_v) in one launch: same shape, dtype and strides
+cudaError_t launch_quantize_qkv(const QuantParams* ps, int layout_qk, int layout_v, cudaStream_t st);
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t st);
 cudaError_t launch_vref(const VrefParams& p, cudaStream_t st);
 // mode: 0 bf16, 1 E4M3 with one scale per tile, 2 E4M3 per-column scales, 3 MXFP8,

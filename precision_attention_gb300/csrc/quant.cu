@@ -76,9 +76,27 @@ __device__ __forceinline__ void smem_row(const uint8_t* tile, int row, int sl, f
 
 // sign flip then the Walsh-Hadamard stages (see the file comment). Stage h = 1
 // pairs neighbours held in one register pair; stages 2 .. EPL/2 run two
-// butterflies per packed f32x2 add and fused multiply-add (fma(b, -1, a) is a - b
-// rounded once, so every butterfly is the same IEEE operation as before); the
-// cross-lane stages compute o + s v with s = +-1, i.e. v + o or o - v.
+// butterflies per packed f32x2 add and fused multiply-add (fma(b, +-1, a) is
+// a +- b rounded once, so every butterfly is the same IEEE operation as before).
+//
+// head_dim 64 (EPL 8): the three cross-lane stages compute o + s v with s = +-1
+// from a full shuffle of the partner's values, leaving channel 8 l + r in lane l,
+// register r.
+//
+// head_dim 128 (EPL 16): each cross-lane stage is a half exchange. Lane bit j
+// (stage h = 16 << j) swaps places with register bit j + 1, whose stage (h = 2 << j)
+// is done: a lane sends the value at register bit j + 1 = 1, keeps the one at 0,
+// and the butterfly then runs in registers. For the kept and sent values to be the
+// right ones, lanes with bit j set store stage 2 << j's outputs swapped ((a - b,
+// a + b) into registers (r, r + 2^(j+1))), which is the same two operations with
+// the sign operand exchanged. After the exchange a lane with bit j clear holds
+// a = kept, b = received, one with bit j set a = received, b = kept: a + b is
+// kept + received in both (IEEE addition commutes, signed zeros included), and
+// a - b = fma(received, -s, s * kept) with s = +1 or -1, the product exact. Half
+// as many shuffles as the full form; the values are bit-identical to the
+// transform's, and lane l, register r ends holding Hadamard output channel
+// (r & 1) | (l << 1) | ((r >> 1) << 4) (stored channel 16 l + r: the two 3-bit
+// fields of the channel index at bits 1-3 and 4-6 swapped).
 template <int EPL>
 __device__ __forceinline__ void rotate_row(float (&v)[EPL], uint32_t smask, int lane) {
 #pragma unroll
@@ -89,32 +107,70 @@ __device__ __forceinline__ void rotate_row(float (&v)[EPL], uint32_t smask, int 
         v[i] = __fadd_rn(a, b);
         v[i + 1] = __fsub_rn(a, b);
     }
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    if constexpr (EPL == 16) {
 #pragma unroll
-    for (int h = 2; h < EPL; h <<= 1) {
+        for (int h = 2; h < 16; h <<= 1) {
+            const float sg = (lane & (h >> 1)) ? -1.0f : 1.0f;   // lane bit j for h = 2 << j
+            const float2 s2 = make_float2(sg, sg), n2 = make_float2(-sg, -sg);
 #pragma unroll
-        for (int i = 0; i < EPL; i += 2) {
-            if (!(i & h)) {
-                const float2 a = make_float2(v[i], v[i + 1]), b = make_float2(v[i + h], v[i + h + 1]);
-                const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, neg1, a);
-                v[i] = sum.x;
-                v[i + 1] = sum.y;
-                v[i + h] = dif.x;
-                v[i + h + 1] = dif.y;
+            for (int i = 0; i < 16; i += 2) {
+                if (!(i & h)) {
+                    const float2 a = make_float2(v[i], v[i + 1]), b = make_float2(v[i + h], v[i + h + 1]);
+                    const float2 lo = __ffma2_rn(b, s2, a), hi = __ffma2_rn(b, n2, a);
+                    v[i] = lo.x;
+                    v[i + 1] = lo.y;
+                    v[i + h] = hi.x;
+                    v[i + h + 1] = hi.y;
+                }
             }
         }
-    }
 #pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
-        const float sg = (lane & m) ? -1.0f : 1.0f;
-        const float2 s2 = make_float2(sg, sg);
+        for (int m = 1, K = 2; m < 8; m <<= 1, K <<= 1) {
+            const float sg = (lane & m) ? -1.0f : 1.0f;
+            const float2 s2 = make_float2(sg, sg), n2 = make_float2(-sg, -sg);
 #pragma unroll
-        for (int i = 0; i < EPL; i += 2) {
-            const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v[i], m);
-            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v[i + 1], m);
-            const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), s2, make_float2(o0, o1));
-            v[i] = r.x;
-            v[i + 1] = r.y;
+            for (int i = 0; i < 16; i += 2) {
+                if (!(i & K)) {
+                    const float r0 = __shfl_xor_sync(0xFFFFFFFFu, v[i + K], m);
+                    const float r1 = __shfl_xor_sync(0xFFFFFFFFu, v[i + K + 1], m);
+                    const float2 keep = make_float2(v[i], v[i + 1]), recv = make_float2(r0, r1);
+                    const float2 sum = __fadd2_rn(keep, recv);
+                    const float2 dif = __ffma2_rn(recv, n2, __fmul2_rn(keep, s2));
+                    v[i] = sum.x;
+                    v[i + 1] = sum.y;
+                    v[i + K] = dif.x;
+                    v[i + K + 1] = dif.y;
+                }
+            }
+        }
+    } else {
+        const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+        for (int h = 2; h < EPL; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < EPL; i += 2) {
+                if (!(i & h)) {
+                    const float2 a = make_float2(v[i], v[i + 1]), b = make_float2(v[i + h], v[i + h + 1]);
+                    const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, neg1, a);
+                    v[i] = sum.x;
+                    v[i + 1] = sum.y;
+                    v[i + h] = dif.x;
+                    v[i + h + 1] = dif.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+            const float sg = (lane & m) ? -1.0f : 1.0f;
+            const float2 s2 = make_float2(sg, sg);
+#pragma unroll
+            for (int i = 0; i < EPL; i += 2) {
+                const float o0 = __shfl_xor_sync(0xFFFFFFFFu, v[i], m);
+                const float o1 = __shfl_xor_sync(0xFFFFFFFFu, v[i + 1], m);
+                const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), s2, make_float2(o0, o1));
+                v[i] = r.x;
+                v[i + 1] = r.y;
+            }
         }
     }
 }
@@ -301,135 +357,27 @@ struct QuantSmem {
     static_assert(OFF_BAR % 8 == 0, "mbarriers need 8-byte alignment");
 };
 
-// One kernel for every layout. QM_E4M3_BLOCK: blocks of HOLD*32 tokens (32,
-// 64 or 128), amax over the block's rows, scale = amax / 448, codes of
-// y * (448 / amax). QM_E4M3_ROW: the same per (token, head). QM_MX_ROW: E8M0
-// per (token, 32 channels). QM_MX_COL: E8M0 per (32 tokens, channel). MX scale
-// bytes go to the unit's 512-byte tile at (r % 32) * 16 + (r / 32) * 4 + g;
-// rows or groups past the document end get 127. QM_MX_TOK: E8M0 per (token,
-// head) over all channels, one byte per token.
+// One 128-token tile (unit g of head h) of one tensor, staged in shared memory at
+// `tile`: the body every layout's kernel runs per unit.
 template <int EPL, int ELT, int QM, int HOLD>
-__global__ void __launch_bounds__(QUANT_THREADS, 2)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
-    using S = QuantSmem<EPL, ELT>;
+__device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTablePtrs& tab, const uint8_t* tile,
+                                           float* red, int* xs, int* flag, uint32_t smask, bool& nonfin, int g,
+                                           int h, int doc, int s0, int L, int t0) {
     constexpr int D = EPL * 8;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    DocTable& stab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
-    int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 65 ints
-    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [4][8][128]
-    int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
-    int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
-    volatile int* abort = flag + 1;
-
-    DocTablePtrs tab{stab.start, stab.off_tile, stab.off_blk};
-    if (p.gtab) {   // written by doc_table_kernel (a malformed batch has no tiles)
-        tab = DocTablePtrs{p.gtab, p.gtab + (p.nd + 1), p.gtab + 2 * (p.nd + 1)};
-    } else if (!build_doc_table(p, tab, misc)) {
-        return;
-    }
-    const int H = p.H, nd = p.nd;
-    const int n_units = tab.off_tile[nd] * H;
+    const int H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sl = lane & 7, rw = lane >> 3;
-    if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        flag[0] = 0;
-        flag[1] = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-    int issued[2] = {0, 0};   // loads issued per stage (thread 0 only)
-    auto issue = [&](int u, int st) {
-        issued[st]++;
-        const int g = u / H, h = u % H;
-        const int doc = find_doc(tab.off_tile, nd, g);
-        const int t0 = tab.start[doc] + (g - tab.off_tile[doc]) * 128;
-        mbar_arrive_expect_tx(&full[st], S::STAGE);
-        tma_load_3d(sm + st * S::STAGE, &tmx, &full[st], 0, h, t0);
-    };
-    if (tid == 0) {
-        if (blockIdx.x < n_units) issue(blockIdx.x, 0);
-        if (blockIdx.x + gridDim.x < n_units) issue(blockIdx.x + gridDim.x, 1);
-    }
-    const uint32_t smask = sign_mask<EPL>(p, sl);
-    bool nonfin = false;
-    int k = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, k++) {
-        const int st = k & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (k >> 1) & 1, abort, 4000000000LL))) break;
-        const uint8_t* tile = sm + st * S::STAGE;
-        const int g = u / H, h = u % H;
-        const int doc = find_doc(tab.off_tile, nd, g);
-        const int s0 = tab.start[doc], L = tab.start[doc + 1] - s0;
-        const int t0 = (g - tab.off_tile[doc]) * 128;      // first local token of the tile
-
-        if constexpr (QM == QM_E4M3_BLOCK) {
-            constexpr int NBLK = 4 / HOLD;
+    (void)xs;
+    (void)doc;
+    if constexpr (QM == QM_E4M3_BLOCK) {
+        constexpr int NBLK = 4 / HOLD;
 #pragma unroll 1
-            for (int blk = 0; blk < NBLK; blk++) {
-                if (t0 + blk * HOLD * 32 >= L) break;          // block past the document end (uniform)
-                float y[HOLD][EPL];
-                float amax = 0.0f;
-#pragma unroll
-                for (int hp = 0; hp < HOLD; hp++) {
-                    const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
-                    smem_row<EPL, ELT>(tile, row, sl, y[hp]);
-                    if (t0 + row >= L) {
-#pragma unroll
-                        for (int i = 0; i < EPL; i++) y[hp][i] = 0.0f;
-                    }
-                    if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
-#pragma unroll
-                    for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
-                }
-                if (!finite_abs(amax)) {   // NaN or infinity in this thread's rows
-                    nonfin = true;
-                    amax = 0.0f;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
-                if (lane == 0) {
-                    red[warp] = amax;
-                    if (wbad) flag[0] = 1;
-                }
-                __syncthreads();
-                amax = red[0];
-#pragma unroll
-                for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
-                const bool bad = flag[0] != 0;
-                __syncthreads();                                 // red[] and flag[0] reused by the next block
-                if (tid == 0) flag[0] = 0;
-                float inv = 0.0f, scale = 0.0f;
-                if (bad) scale = __int_as_float(0x7FC00000);
-                else if (amax > 0.0f) {
-                    inv = __fdiv_rn(448.0f, amax);
-                    scale = __fdiv_rn(amax, 448.0f);
-                }
-                if (tid == 0) {
-                    const int b = tab.off_blk[doc] + (t0 + blk * HOLD * 32) / (HOLD * 32);
-                    static_cast<float*>(p.scales)[(long long)h * p.scale_cap + b] = scale;
-                }
-#pragma unroll
-                for (int hp = 0; hp < HOLD; hp++) {
-                    const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
-                    if (t0 + row < L)
-                        store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y[hp], inv);
-                }
-            }
-        } else if constexpr (QM == QM_NVFP4) {
-            // the 128-token tile is the fp32 block: amax over the tile gives s_t = amax / 2688
-            // and inv = 448 / amax; each thread's 16 channels of a row are one group: its
-            // E4M3 scale sf = E4M3(max |y inv|) and E2M1 codes of y inv (6 / sf), the scale
-            // byte at its place in the MMA-ready tile (groups 4 kk .. 4 kk + 3 in tile kk)
-            static_assert(EPL == 16, "NVFP4 groups are one thread's 16 channels");
-            float y[4][EPL];
+        for (int blk = 0; blk < NBLK; blk++) {
+            if (t0 + blk * HOLD * 32 >= L) break;          // block past the document end (uniform)
+            float y[HOLD][EPL];
             float amax = 0.0f;
 #pragma unroll
-            for (int hp = 0; hp < 4; hp++) {
-                const int row = hp * 32 + warp * 4 + rw;
+            for (int hp = 0; hp < HOLD; hp++) {
+                const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
                 smem_row<EPL, ELT>(tile, row, sl, y[hp]);
                 if (t0 + row >= L) {
 #pragma unroll
@@ -439,7 +387,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
 #pragma unroll
                 for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
             }
-            if (!finite_abs(amax)) {
+            if (!finite_abs(amax)) {   // NaN or infinity in this thread's rows
                 nonfin = true;
                 amax = 0.0f;
             }
@@ -455,198 +403,358 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
 #pragma unroll
             for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
             const bool bad = flag[0] != 0;
-            __syncthreads();
+            __syncthreads();                                 // red[] and flag[0] reused by the next block
             if (tid == 0) flag[0] = 0;
-            float inv = 0.0f, st_scale = 0.0f;
-            if (bad) st_scale = __int_as_float(0x7FC00000);
+            float inv = 0.0f, scale = 0.0f;
+            if (bad) scale = __int_as_float(0x7FC00000);
             else if (amax > 0.0f) {
                 inv = __fdiv_rn(448.0f, amax);
-                st_scale = __fdiv_rn(amax, 2688.0f);
+                scale = __fdiv_rn(amax, 448.0f);
             }
-            if (tid == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + g] = st_scale;
-            uint8_t* sft = p.sf16 + ((long long)h * p.scale_cap + g) * 1024 + (sl >> 2) * 512;
+            if (tid == 0) {
+                const int b = tab.off_blk[doc] + (t0 + blk * HOLD * 32) / (HOLD * 32);
+                static_cast<float*>(p.scales)[(long long)h * p.scale_cap + b] = scale;
+            }
 #pragma unroll
-            for (int hp = 0; hp < 4; hp++) {
-                const int row = hp * 32 + warp * 4 + rw;
-                float z[EPL];
-                float gmax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    z[i] = __fmul_rn(y[hp][i], inv);
-                    gmax = fmaxf(gmax, fabsf(z[i]));
-                }
-                const uint32_t sfb = cvt_e4m3x2(gmax, 0.0f) & 0xFFu;
-                const float sfv = e4m3_value(sfb);
-                const float r6 = sfv > 0.0f ? __fdiv_rn(6.0f, sfv) : 0.0f;
-                uint32_t w[2] = {0u, 0u};
-                if (sfv > 0.0f) {
-#pragma unroll
-                    for (int i = 0; i < EPL; i += 2)
-                        w[i >> 3] |= cvt_e2m1x2(__fmul_rn(z[i], r6), __fmul_rn(z[i + 1], r6)) << (4 * (i & 7));
-                }
-                const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfb, 1);
-                const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfb, 2);
-                const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfb, 3);
-                if ((sl & 3) == 0)
-                    *reinterpret_cast<uint32_t*>(sft + (row % 32) * 16 + (row / 32) * 4) =
-                        sfb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            for (int hp = 0; hp < HOLD; hp++) {
+                const int row = (blk * HOLD + hp) * 32 + warp * 4 + rw;
                 if (t0 + row < L)
-                    *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * (D / 2) + sl * 8) =
-                        make_uint2(w[0], w[1]);
+                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y[hp], inv);
             }
-        } else if constexpr (QM == QM_E4M3_ROW) {
-#pragma unroll 1
-            for (int ps = 0; ps < 4; ps++) {
-                const int row = ps * 32 + warp * 4 + rw;
-                const bool valid = t0 + row < L;
-                float y[EPL];
-                smem_row<EPL, ELT>(tile, row, sl, y);
-                if (p.rotate) rotate_row<EPL>(y, smask, lane);
-                float amax = 0.0f;
+        }
+    } else if constexpr (QM == QM_NVFP4) {
+        // the 128-token tile is the fp32 block: amax over the tile gives s_t = amax / 2688
+        // and inv = 448 / amax; each thread's 16 channels of a row are one group: its
+        // E4M3 scale sf = E4M3(max |y inv|) and E2M1 codes of y inv (6 / sf), the scale
+        // byte at its place in the MMA-ready tile (groups 4 kk .. 4 kk + 3 in tile kk)
+        static_assert(EPL == 16, "NVFP4 groups are one thread's 16 channels");
+        float y[4][EPL];
+        float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
-                bool bad = !finite_abs(amax);
-                if (bad) amax = 0.0f;
+        for (int hp = 0; hp < 4; hp++) {
+            const int row = hp * 32 + warp * 4 + rw;
+            smem_row<EPL, ELT>(tile, row, sl, y[hp]);
+            if (t0 + row >= L) {
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                    bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
-                }
-                if (valid) {
-                    float inv = 0.0f, scale = 0.0f;
-                    if (bad) {
-                        scale = __int_as_float(0x7FC00000);
-                        nonfin = true;
-                    } else if (amax > 0.0f) {
-                        inv = __fdiv_rn(448.0f, amax);
-                        scale = __fdiv_rn(amax, 448.0f);
-                    }
-                    // block 1: the block index of a token is the token itself
-                    if (sl == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = scale;
-                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, inv);
-                }
+                for (int i = 0; i < EPL; i++) y[hp][i] = 0.0f;
             }
-        } else if constexpr (QM == QM_MX_TOK) {
-            // one E8M0 exponent per (token, head) over all d channels (the causal-exact
-            // MX mode's V): scale byte at the token's own column
-#pragma unroll 1
-            for (int ps = 0; ps < 4; ps++) {
-                const int row = ps * 32 + warp * 4 + rw;
-                const bool valid = t0 + row < L;
-                float y[EPL];
-                smem_row<EPL, ELT>(tile, row, sl, y);
-                if (p.rotate) rotate_row<EPL>(y, smask, lane);
-                float amax = 0.0f;
+            if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
 #pragma unroll
-                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
-                bool bad = !finite_abs(amax);
-                if (bad) amax = 0.0f;
+            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
+        }
+        if (!finite_abs(amax)) {
+            nonfin = true;
+            amax = 0.0f;
+        }
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                    bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
-                }
-                if (valid) {
-                    if (bad) nonfin = true;
-                    const int X = e8m0_exponent(amax, p.mx_rule);
-                    if (sl == 0)
-                        static_cast<uint8_t*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = (uint8_t)(X + 127);
-                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, pow2_neg(X));
-                }
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
+        if (lane == 0) {
+            red[warp] = amax;
+            if (wbad) flag[0] = 1;
+        }
+        __syncthreads();
+        amax = red[0];
+#pragma unroll
+        for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
+        const bool bad = flag[0] != 0;
+        __syncthreads();
+        if (tid == 0) flag[0] = 0;
+        float inv = 0.0f, st_scale = 0.0f;
+        if (bad) st_scale = __int_as_float(0x7FC00000);
+        else if (amax > 0.0f) {
+            inv = __fdiv_rn(448.0f, amax);
+            st_scale = __fdiv_rn(amax, 2688.0f);
+        }
+        if (tid == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + g] = st_scale;
+        uint8_t* sft = p.sf16 + ((long long)h * p.scale_cap + g) * 1024 + (sl >> 2) * 512;
+#pragma unroll
+        for (int hp = 0; hp < 4; hp++) {
+            const int row = hp * 32 + warp * 4 + rw;
+            float z[EPL];
+            float gmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; i++) {
+                z[i] = __fmul_rn(y[hp][i], inv);
+                gmax = fmaxf(gmax, fabsf(z[i]));
             }
-        } else if constexpr (QM == QM_MX_ROW) {
-            uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-#pragma unroll 1
-            for (int ps = 0; ps < 4; ps++) {
-                const int r = ps * 32 + warp * 4 + rw;
-                const bool valid = t0 + r < L;
-                float y[EPL];
-                smem_row<EPL, ELT>(tile, r, sl, y);
-                if (p.rotate) rotate_row<EPL>(y, smask, lane);
-                float amax = 0.0f;
+            const uint32_t sfb = cvt_e4m3x2(gmax, 0.0f) & 0xFFu;
+            const float sfv = e4m3_value(sfb);
+            const float r6 = sfv > 0.0f ? __fdiv_rn(6.0f, sfv) : 0.0f;
+            uint32_t w[2] = {0u, 0u};
+            if (sfv > 0.0f) {
 #pragma unroll
-                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
-                bool bad = !finite_abs(amax);
-                if (bad) amax = 0.0f;
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
-                if (bad && valid) nonfin = true;
-                const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
-                const uint32_t byte = (uint32_t)(X + 127);
-                const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-                const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-                const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+                for (int i = 0; i < EPL; i += 2)
+                    w[i >> 3] |= cvt_e2m1x2(__fmul_rn(z[i], r6), __fmul_rn(z[i + 1], r6)) << (4 * (i & 7));
+            }
+            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfb, 1);
+            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfb, 2);
+            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfb, 3);
+            if ((sl & 3) == 0)
+                *reinterpret_cast<uint32_t*>(sft + (row % 32) * 16 + (row / 32) * 4) =
+                    sfb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            if (t0 + row < L)
+                *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * (D / 2) + sl * 8) =
+                    make_uint2(w[0], w[1]);
+        }
+    } else if constexpr (QM == QM_E4M3_ROW) {
+#pragma unroll 1
+        for (int ps = 0; ps < 4; ps++) {
+            const int row = ps * 32 + warp * 4 + rw;
+            const bool valid = t0 + row < L;
+            float y[EPL];
+            smem_row<EPL, ELT>(tile, row, sl, y);
+            if (p.rotate) rotate_row<EPL>(y, smask, lane);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            bool bad = !finite_abs(amax);
+            if (bad) amax = 0.0f;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
+            }
+            if (valid) {
+                float inv = 0.0f, scale = 0.0f;
+                if (bad) {
+                    scale = __int_as_float(0x7FC00000);
+                    nonfin = true;
+                } else if (amax > 0.0f) {
+                    inv = __fdiv_rn(448.0f, amax);
+                    scale = __fdiv_rn(amax, 448.0f);
+                }
+                // block 1: the block index of a token is the token itself
+                if (sl == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = scale;
+                store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, inv);
+            }
+        }
+    } else if constexpr (QM == QM_MX_TOK) {
+        // one E8M0 exponent per (token, head) over all d channels (the causal-exact
+        // MX mode's V): scale byte at the token's own column
+#pragma unroll 1
+        for (int ps = 0; ps < 4; ps++) {
+            const int row = ps * 32 + warp * 4 + rw;
+            const bool valid = t0 + row < L;
+            float y[EPL];
+            smem_row<EPL, ELT>(tile, row, sl, y);
+            if (p.rotate) rotate_row<EPL>(y, smask, lane);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            bool bad = !finite_abs(amax);
+            if (bad) amax = 0.0f;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
+            }
+            if (valid) {
+                if (bad) nonfin = true;
+                const int X = e8m0_exponent(amax, p.mx_rule);
                 if (sl == 0)
-                    *reinterpret_cast<uint32_t*>(sct + (r % 32) * 16 + (r / 32) * 4) =
-                        byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                if (valid)
-                    store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
+                    static_cast<uint8_t*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = (uint8_t)(X + 127);
+                store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, pow2_neg(X));
             }
-        } else {   // QM_MX_COL
-            // Column maxima straight from the staged tile: warp w takes group w / 2 and
-            // channel pairs 32 (w % 2) .. + 31, one pair per lane, and scans the group's
-            // 32 rows (one 32-bit bf16 pair or 64-bit fp32 pair per row: consecutive
-            // words across the warp). No shuffles and one barrier; the codes are then
-            // written row-parallel as in the other layouts.
-            uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-            {
-                const int gi = warp >> 1, c = 2 * (32 * (warp & 1) + lane);   // first channel of the pair
-                const int nrow = min(32, L - t0 - gi * 32);                     // rows inside the document
-                float m0 = 0.0f, m1 = 0.0f;
-                for (int r = 0; r < nrow; r++) {
-                    float v0, v1;
-                    const int row = gi * 32 + r;
-                    if constexpr (ELT == 2) {
-                        const uint32_t w2 = *reinterpret_cast<const uint32_t*>(tile + (row * D + c) * 2);
-                        v0 = __uint_as_float(w2 << 16);
-                        v1 = __uint_as_float(w2 & 0xFFFF0000u);
-                    } else {
-                        const float2 f2 = *reinterpret_cast<const float2*>(tile + (row * D + c) * 4);
-                        v0 = f2.x;
-                        v1 = f2.y;
-                    }
-                    m0 = amax_nan(m0, v0);
-                    m1 = amax_nan(m1, v1);
-                }
-                if (!finite_abs(m0)) { nonfin = true; m0 = 0.0f; }
-                if (!finite_abs(m1)) { nonfin = true; m1 = 0.0f; }
-                const bool inside = nrow > 0;                    // groups past the document end: 127
-                const int X0 = inside ? e8m0_exponent(m0, p.mx_rule) : 0;
-                const int X1 = inside ? e8m0_exponent(m1, p.mx_rule) : 0;
-                xs[gi * 128 + c] = X0;
-                xs[gi * 128 + c + 1] = X1;
-                sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X0 + 127);
-                sct[((c + 1) % 32) * 16 + ((c + 1) / 32) * 4 + gi] = (uint8_t)(X1 + 127);
-            }
-            __syncthreads();
+        }
+    } else if constexpr (QM == QM_MX_ROW) {
+        uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
 #pragma unroll 1
-            for (int gi = 0; gi < 4; gi++) {
-                const int row = gi * 32 + warp * 4 + rw;
-                if (t0 + row < L) {
-                    float y[EPL];
-                    smem_row<EPL, ELT>(tile, row, sl, y);
-                    uint32_t w4[EPL / 4];
+        for (int ps = 0; ps < 4; ps++) {
+            const int r = ps * 32 + warp * 4 + rw;
+            const bool valid = t0 + r < L;
+            float y[EPL];
+            smem_row<EPL, ELT>(tile, r, sl, y);
+            if (p.rotate) rotate_row<EPL>(y, smask, lane);
+            float amax = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < EPL / 4; i++) {
-                        const int c = sl * EPL + 4 * i;
-                        const int4 x4 = *reinterpret_cast<const int4*>(xs + gi * 128 + c);
-                        w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(x4.x)),
-                                            __fmul_rn(y[4 * i + 1], pow2_neg(x4.y)),
-                                            __fmul_rn(y[4 * i + 2], pow2_neg(x4.z)),
-                                            __fmul_rn(y[4 * i + 3], pow2_neg(x4.w)));
-                    }
-                    if constexpr (EPL == 16) {
-                        *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
-                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    } else {
-                        *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
-                            make_uint2(w4[0], w4[1]);
-                    }
+            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            bool bad = !finite_abs(amax);
+            if (bad) amax = 0.0f;
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
+            if (bad && valid) nonfin = true;
+            const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
+            const uint32_t byte = (uint32_t)(X + 127);
+            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
+            if (sl == 0)
+                *reinterpret_cast<uint32_t*>(sct + (r % 32) * 16 + (r / 32) * 4) =
+                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            if (valid)
+                store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
+        }
+    } else {   // QM_MX_COL
+        // Column maxima straight from the staged tile: warp w takes group w / 2 and
+        // channel pairs 32 (w % 2) .. + 31, one pair per lane, and scans the group's
+        // 32 rows (one 32-bit bf16 pair or 64-bit fp32 pair per row: consecutive
+        // words across the warp). No shuffles and one barrier; the codes are then
+        // written row-parallel as in the other layouts.
+        uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
+        {
+            const int gi = warp >> 1, c = 2 * (32 * (warp & 1) + lane);   // first channel of the pair
+            const int nrow = min(32, L - t0 - gi * 32);                     // rows inside the document
+            float m0 = 0.0f, m1 = 0.0f;
+            for (int r = 0; r < nrow; r++) {
+                float v0, v1;
+                const int row = gi * 32 + r;
+                if constexpr (ELT == 2) {
+                    const uint32_t w2 = *reinterpret_cast<const uint32_t*>(tile + (row * D + c) * 2);
+                    v0 = __uint_as_float(w2 << 16);
+                    v1 = __uint_as_float(w2 & 0xFFFF0000u);
+                } else {
+                    const float2 f2 = *reinterpret_cast<const float2*>(tile + (row * D + c) * 4);
+                    v0 = f2.x;
+                    v1 = f2.y;
+                }
+                m0 = amax_nan(m0, v0);
+                m1 = amax_nan(m1, v1);
+            }
+            if (!finite_abs(m0)) { nonfin = true; m0 = 0.0f; }
+            if (!finite_abs(m1)) { nonfin = true; m1 = 0.0f; }
+            const bool inside = nrow > 0;                    // groups past the document end: 127
+            const int X0 = inside ? e8m0_exponent(m0, p.mx_rule) : 0;
+            const int X1 = inside ? e8m0_exponent(m1, p.mx_rule) : 0;
+            xs[gi * 128 + c] = X0;
+            xs[gi * 128 + c + 1] = X1;
+            sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X0 + 127);
+            sct[((c + 1) % 32) * 16 + ((c + 1) / 32) * 4 + gi] = (uint8_t)(X1 + 127);
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int gi = 0; gi < 4; gi++) {
+            const int row = gi * 32 + warp * 4 + rw;
+            if (t0 + row < L) {
+                float y[EPL];
+                smem_row<EPL, ELT>(tile, row, sl, y);
+                uint32_t w4[EPL / 4];
+#pragma unroll
+                for (int i = 0; i < EPL / 4; i++) {
+                    const int c = sl * EPL + 4 * i;
+                    const int4 x4 = *reinterpret_cast<const int4*>(xs + gi * 128 + c);
+                    w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(x4.x)),
+                                        __fmul_rn(y[4 * i + 1], pow2_neg(x4.y)),
+                                        __fmul_rn(y[4 * i + 2], pow2_neg(x4.z)),
+                                        __fmul_rn(y[4 * i + 3], pow2_neg(x4.w)));
+                }
+                if constexpr (EPL == 16) {
+                    *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                } else {
+                    *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
+                        make_uint2(w4[0], w4[1]);
                 }
             }
         }
+    }}
+
+// Units [ubeg, uend) of one tensor, stride gridDim.x, through the two-stage copy
+// pipeline (stage k & 1); unit u is unit u - base of the tensor `p` describes.
+// `issue` starts the copy of a later unit (of any tensor) into a freed stage.
+// Returns false when a copy wait ran out.
+template <int EPL, int ELT, int QM, int HOLD, class Issue>
+__device__ __forceinline__ bool quant_range(const QuantParams& p, const DocTablePtrs& tab, uint8_t* sm,
+                                            uint64_t* full, float* red, int* xs, int* flag, volatile int* abort,
+                                            uint32_t smask, bool& nonfin, int ubeg, int uend, int base, int n_units,
+                                            int& k, Issue& issue) {
+    using S = QuantSmem<EPL, ELT>;
+    const int H = p.H, nd = p.nd;
+    for (int u = ubeg; u < uend; u += gridDim.x, k++) {
+        const int st = k & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (k >> 1) & 1, abort, 4000000000LL))) return false;
+        const uint8_t* tile = sm + st * S::STAGE;
+        const int uu = u - base;
+        const int g = uu / H, h = uu % H;
+        const int doc = find_doc(tab.off_tile, nd, g);
+        const int s0 = tab.start[doc], L = tab.start[doc + 1] - s0;
+        const int t0 = (g - tab.off_tile[doc]) * 128;      // first local token of the tile
+        quant_unit<EPL, ELT, QM, HOLD>(p, tab, tile, red, xs, flag, smask, nonfin, g, h, doc, s0, L, t0);
         __syncthreads();                                       // every read of this stage is done
-        if (tid == 0 && u + 2 * (int)gridDim.x < n_units) issue(u + 2 * gridDim.x, st);
+        if (threadIdx.x == 0 && u + 2 * (int)gridDim.x < n_units) issue(u + 2 * gridDim.x, st);
+    }
+    return true;
+}
+
+// One kernel for every layout. QM_E4M3_BLOCK: blocks of HOLD*32 tokens (32,
+// 64 or 128), amax over the block's rows, scale = amax / 448, codes of
+// y * (448 / amax). QM_E4M3_ROW: the same per (token, head). QM_MX_ROW: E8M0
+// per (token, 32 channels). QM_MX_COL: E8M0 per (32 tokens, channel). MX scale
+// bytes go to the unit's 512-byte tile at (r % 32) * 16 + (r / 32) * 4 + g;
+// rows or groups past the document end get 127. QM_MX_TOK: E8M0 per (token,
+// head) over all channels, one byte per token.
+template <int EPL, int ELT, int QM, int HOLD, int QMV, int HOLDV, int NT>
+__global__ void __launch_bounds__(QUANT_THREADS, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                      const __grid_constant__ CUtensorMap tm2, const __grid_constant__ QuantParams p0,
+                      const __grid_constant__ QuantParams p1, const __grid_constant__ QuantParams p2) {
+    // NT = 1: one tensor (p0, layout QM); 3: Q, K (p0, p1, layout QM) and V (p2, layout
+    // QMV) in one launch, the units of the three tensors one after another
+    constexpr int ntens = NT;
+    using S = QuantSmem<EPL, ELT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    DocTable& stab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
+    int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 65 ints
+    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [4][8][128]
+    int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
+    int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
+    volatile int* abort = flag + 1;
+
+    // the document table is the same for the three tensors (one shape)
+    DocTablePtrs tab{stab.start, stab.off_tile, stab.off_blk};
+    if (p0.gtab) {   // written by doc_table_kernel (a malformed batch has no tiles)
+        tab = DocTablePtrs{p0.gtab, p0.gtab + (p0.nd + 1), p0.gtab + 2 * (p0.nd + 1)};
+    } else if (!build_doc_table(p0, tab, misc)) {
+        return;
+    }
+    const int H = p0.H, nd = p0.nd;
+    const int n_units_t = tab.off_tile[nd] * H;   // units of one tensor
+    const int n_units = n_units_t * ntens;
+    const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        flag[0] = 0;
+        flag[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int issued[2] = {0, 0};   // loads issued per stage (thread 0 only)
+    auto issue = [&](int u, int st) {
+        issued[st]++;
+        const int t = u / n_units_t, uu = u % n_units_t;
+        const int g = uu / H, h = uu % H;
+        const int doc = find_doc(tab.off_tile, nd, g);
+        const int t0 = tab.start[doc] + (g - tab.off_tile[doc]) * 128;
+        mbar_arrive_expect_tx(&full[st], S::STAGE);
+        tma_load_3d(sm + st * S::STAGE, t == 0 ? &tm0 : (t == 1 ? &tm1 : &tm2), &full[st], 0, h, t0);
+    };
+    if (tid == 0) {
+        if (blockIdx.x < n_units) issue(blockIdx.x, 0);
+        if (blockIdx.x + gridDim.x < n_units) issue(blockIdx.x + gridDim.x, 1);
+    }
+    const uint32_t smask = sign_mask<EPL>(p0, sl);                      // Q and K: one rotation
+    uint32_t smask_v = smask;
+    if constexpr (NT == 3) smask_v = sign_mask<EPL>(p2, sl);
+    bool nonfin = false;
+    int k = 0;
+    if constexpr (NT == 1) {
+        quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, blockIdx.x, n_units,
+                                        0, n_units, k, issue);
+    } else {
+        // the three tensors one after another, each loop with its own parameters;
+        // first(lo): this CTA's first unit at or after lo
+        const int G = gridDim.x, b = blockIdx.x;
+        auto first = [&](int lo) { return lo + ((b - lo % G) % G + G) % G; };
+        const int n = n_units_t;
+        if (quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(0), n, 0,
+                                            n_units, k, issue) &&
+            quant_range<EPL, ELT, QM, HOLD>(p1, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(n), 2 * n,
+                                            n, n_units, k, issue))
+            quant_range<EPL, ELT, QMV, HOLDV>(p2, tab, sm, full, red, xs, flag, abort, smask_v, nonfin, first(2 * n),
+                                              3 * n, 2 * n, n_units, k, issue);
     }
     if (tid == 0) {
         // every issued copy must have landed before the CTA's shared memory goes away
@@ -658,60 +766,90 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
                 }
             }
     }
-    if (nonfin) atomicOr(p.status, ST_NONFINITE);
-    if (*abort && tid == 0) atomicOr(p.status, ST_TIMEOUT);
+    if (nonfin) atomicOr(p0.status, ST_NONFINITE);
+    if (*abort && tid == 0) atomicOr(p0.status, ST_TIMEOUT);
 }
 
 // ---------------------------------------------------------------------------
-template <int EPL, int ELT, int QM, int HOLD>
-static cudaError_t launch_q(const CUtensorMap& m, const QuantParams& p, int grid, cudaStream_t st) {
+// maps[t] / ps[t] for the ntens tensors of the launch (1, or 3: Q, K with layout QM, V with QMV)
+template <int EPL, int ELT, int QM, int HOLD, int NT, int QMV = QM, int HOLDV = HOLD>
+static cudaError_t launch_q(const CUtensorMap* maps, const QuantParams* ps, int grid, cudaStream_t st) {
     using S = QuantSmem<EPL, ELT>;
-    auto kern = quant_tile_kernel<EPL, ELT, QM, HOLD>;
+    auto kern = quant_tile_kernel<EPL, ELT, QM, HOLD, QMV, HOLDV, NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, QUANT_THREADS, S::BYTES, st>>>(m, p);
+    const int t1 = NT == 3 ? 1 : 0, t2 = NT == 3 ? 2 : 0;
+    kern<<<grid, QUANT_THREADS, S::BYTES, st>>>(maps[0], maps[t1], maps[t2], ps[0], ps[t1], ps[t2]);
     return cudaGetLastError();
 }
 
+// one tensor of any layout, or (layout_v >= 0) Q, K in `layout` and V in `layout_v`
 template <int EPL, int ELT>
-static cudaError_t launch_layout(const CUtensorMap& m, const QuantParams& p, int layout, int grid, cudaStream_t st) {
-    if constexpr (EPL == 16) {   // MX layouts: d = 128 only
-        if (layout == 1) return launch_q<EPL, ELT, QM_MX_ROW, 1>(m, p, grid, st);
-        if (layout == 2) return launch_q<EPL, ELT, QM_MX_COL, 1>(m, p, grid, st);
-        if (layout == 3) return launch_q<EPL, ELT, QM_MX_TOK, 1>(m, p, grid, st);
-        if (layout == 4) return launch_q<EPL, ELT, QM_NVFP4, 4>(m, p, grid, st);
-    } else {
-        if (layout != 0) return cudaErrorInvalidValue;
+static cudaError_t launch_layout(const CUtensorMap* m, const QuantParams* ps, int layout, int layout_v, int grid,
+                                 cudaStream_t st) {
+    const int nt = layout_v >= 0 ? 3 : 1;
+    if constexpr (EPL == 16) {   // MX and NVFP4 layouts: d = 128 only
+        if (nt == 3) {
+            if (layout == 1 && layout_v == 2) return launch_q<EPL, ELT, QM_MX_ROW, 1, 3, QM_MX_COL, 1>(m, ps, grid, st);
+            if (layout == 1 && layout_v == 3) return launch_q<EPL, ELT, QM_MX_ROW, 1, 3, QM_MX_TOK, 1>(m, ps, grid, st);
+            if (layout == 4 && layout_v == 0)
+                return launch_q<EPL, ELT, QM_NVFP4, 4, 3, QM_E4M3_BLOCK, 4>(m, ps, grid, st);
+        } else {
+            if (layout == 1) return launch_q<EPL, ELT, QM_MX_ROW, 1, 1>(m, ps, grid, st);
+            if (layout == 2) return launch_q<EPL, ELT, QM_MX_COL, 1, 1>(m, ps, grid, st);
+            if (layout == 3) return launch_q<EPL, ELT, QM_MX_TOK, 1, 1>(m, ps, grid, st);
+            if (layout == 4) return launch_q<EPL, ELT, QM_NVFP4, 4, 1>(m, ps, grid, st);
+        }
     }
-    switch (p.block) {
-        case 1: return launch_q<EPL, ELT, QM_E4M3_ROW, 1>(m, p, grid, st);
-        case 32: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 1>(m, p, grid, st);
-        case 64: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 2>(m, p, grid, st);
-        default: return launch_q<EPL, ELT, QM_E4M3_BLOCK, 4>(m, p, grid, st);
+    if (layout != 0 || (nt == 3 && layout_v != 0)) return cudaErrorInvalidValue;
+    switch (ps[0].block) {
+        case 1: return nt == 3 ? launch_q<EPL, ELT, QM_E4M3_ROW, 1, 3>(m, ps, grid, st)
+                               : launch_q<EPL, ELT, QM_E4M3_ROW, 1, 1>(m, ps, grid, st);
+        case 32: return nt == 3 ? launch_q<EPL, ELT, QM_E4M3_BLOCK, 1, 3>(m, ps, grid, st)
+                                : launch_q<EPL, ELT, QM_E4M3_BLOCK, 1, 1>(m, ps, grid, st);
+        case 64: return nt == 3 ? launch_q<EPL, ELT, QM_E4M3_BLOCK, 2, 3>(m, ps, grid, st)
+                                : launch_q<EPL, ELT, QM_E4M3_BLOCK, 2, 1>(m, ps, grid, st);
+        default: return nt == 3 ? launch_q<EPL, ELT, QM_E4M3_BLOCK, 4, 3>(m, ps, grid, st)
+                                : launch_q<EPL, ELT, QM_E4M3_BLOCK, 4, 1>(m, ps, grid, st);
     }
 }
 
-cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st) {
+static bool input_map(CUtensorMap* m, const QuantParams& p) {
+    const int elt = p.in_bf16 ? 2 : 4;
+    return make_tensor_map_3d(m, p.x, p.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              p.d, p.H, p.T, (uint64_t)p.hstride * elt, (uint64_t)p.tstride * elt, p.d, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// ps[0..ntens): one tensor, or Q, K, V (same shape, dtype and strides)
+static cudaError_t launch_tensors(const QuantParams* ps, int ntens, int layout, int layout_v, cudaStream_t st) {
+    const QuantParams& p = ps[0];
     if (p.gtab) {
         doc_table_kernel<<<1, 1024, 0, st>>>(p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const int elt = p.in_bf16 ? 2 : 4;
-    CUtensorMap m;
-    if (!make_tensor_map_3d(&m, p.x, p.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                            p.d, p.H, p.T, (uint64_t)p.hstride * elt, (uint64_t)p.tstride * elt, p.d, 128,
-                            CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    const long long units = (long long)p.H * (((long long)p.T + 127) / 128 + p.nd);
+    CUtensorMap m[3];
+    for (int t = 0; t < ntens; t++)
+        if (!input_map(&m[t], ps[t])) return cudaErrorInvalidValue;
+    const long long units = (long long)ntens * p.H * (((long long)p.T + 127) / 128 + p.nd);
     const int sms = sm_count();
     if (sms < 1) return cudaErrorInvalidDevice;
     // two CTAs per SM except fp32 rows of 128 channels (128 KB of stages per CTA)
     const int per_sm = (p.d == 128 && !p.in_bf16) ? 1 : 2;
     const int grid = (int)(units < (long long)per_sm * sms ? units : (long long)per_sm * sms);
-    if (p.d == 128) return p.in_bf16 ? launch_layout<16, 2>(m, p, layout, grid, st)
-                                     : launch_layout<16, 4>(m, p, layout, grid, st);
-    return p.in_bf16 ? launch_layout<8, 2>(m, p, layout, grid, st) : launch_layout<8, 4>(m, p, layout, grid, st);
+    if (p.d == 128) return p.in_bf16 ? launch_layout<16, 2>(m, ps, layout, layout_v, grid, st)
+                                     : launch_layout<16, 4>(m, ps, layout, layout_v, grid, st);
+    return p.in_bf16 ? launch_layout<8, 2>(m, ps, layout, layout_v, grid, st)
+                     : launch_layout<8, 4>(m, ps, layout, layout_v, grid, st);
+}
+
+cudaError_t launch_quantize(const QuantParams& p, int layout, cudaStream_t st) {
+    return launch_tensors(&p, 1, layout, -1, st);
+}
+
+cudaError_t launch_quantize_qkv(const QuantParams* ps, int layout_qk, int layout_v, cudaStream_t st) {
+    return launch_tensors(ps, 3, layout_qk, layout_v, st);
 }
 
 }  // namespace pa

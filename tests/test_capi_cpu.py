@@ -221,6 +221,47 @@ def test_nvfp4_forward_rules_on_host(pa):
     assert call(nq, nk8, ev) == pa.ATTN_ERR_SEED_MISMATCH
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses placeholder device pointers; only run where no GPU could be reached")
+def test_quantize_qkv_layout_sets_on_host(pa):
+    """attn_quantize_qkv takes only the operand sets the forward accepts (E4M3 with one
+    block for all three; MX rows with MX columns or per-token V; NVFP4 with E4M3 V in
+    128-token blocks): any other set is an invalid argument, refused before the
+    workspace check, which every accepted set reaches (here a 16-byte workspace)."""
+    L = pa.lib()
+    fake = 1 << 20
+    shape = pa._Shape(256, 2, 128, 1, None)
+
+    def call(q, k, v, ws=16, dt=1, stride=256):
+        return L.attn_quantize_qkv(fake, fake, fake, dt, stride, 128, ctypes.byref(shape), 1, 7, ctypes.byref(q),
+                                   ctypes.byref(k), ctypes.byref(v), fake, ws, None)
+
+    def qt(layout, block):
+        return pa._QT(fake, fake, layout, block, 0, 0, 0)
+
+    E, R, C, TOK, NV = (pa.ATTN_E4M3_TOKBLOCK, pa.ATTN_MX_ROW32, pa.ATTN_MX_COL32, pa.ATTN_MX_TOKEN,
+                        pa.ATTN_NVFP4)
+    accepted = [(qt(E, 128), qt(E, 128), qt(E, 128)), (qt(E, 1), qt(E, 1), qt(E, 1)),
+                (qt(E, 64), qt(E, 64), qt(E, 64)), (qt(R, 32), qt(R, 32), qt(C, 32)),
+                (qt(R, 32), qt(R, 32), qt(TOK, 1)), (qt(NV, 128), qt(NV, 128), qt(E, 128))]
+    refused = [(qt(E, 128), qt(E, 64), qt(E, 128)), (qt(E, 128), qt(E, 128), qt(E, 64)),
+               (qt(R, 32), qt(E, 128), qt(C, 32)), (qt(R, 32), qt(R, 32), qt(R, 32)),
+               (qt(R, 32), qt(R, 32), qt(E, 128)), (qt(C, 32), qt(C, 32), qt(C, 32)),
+               (qt(NV, 128), qt(NV, 128), qt(E, 64)), (qt(NV, 128), qt(E, 128), qt(E, 128)),
+               (qt(E, 128), qt(E, 128), qt(NV, 128))]
+    for q, k, v in accepted:
+        assert call(q, k, v) == pa.ATTN_ERR_WORKSPACE, (q.layout, k.layout, v.layout, q.block, v.block)
+    for q, k, v in refused:
+        assert call(q, k, v) == pa.ATTN_ERR_INVALID_ARG, (q.layout, k.layout, v.layout, q.block, v.block)
+    assert call(qt(E, 128), qt(E, 128), qt(E, 128), dt=2) == pa.ATTN_ERR_INVALID_ARG      # no such dtype
+    assert call(qt(E, 128), qt(E, 128), qt(E, 128), stride=100) == pa.ATTN_ERR_INVALID_ARG  # 200-byte rows
+    assert L.attn_quantize_qkv(fake, None, fake, 1, 256, 128, ctypes.byref(shape), 1, 7,
+                               ctypes.byref(qt(E, 128)), ctypes.byref(qt(E, 128)), ctypes.byref(qt(E, 128)),
+                               fake, 16, None) == pa.ATTN_ERR_INVALID_ARG                 # null K input
+    assert L.attn_quantize_qkv(fake, fake, fake, 1, 256, 128, ctypes.byref(shape), 1, 7, ctypes.byref(qt(E, 128)),
+                               None, ctypes.byref(qt(E, 128)), fake, 16, None) == pa.ATTN_ERR_INVALID_ARG
+
+
 def test_test_build_exports_the_probability_dump_and_the_timed_library_does_not(pa):
     """libpa_gb300_pdump.so (include/attn_pdump.h) is the parity tests' build: it
     exports every call of include/attn.h plus attn_pdump_set; the library that
