@@ -183,6 +183,13 @@ __device__ __forceinline__ float amax_nan(float m, float a) {
     return r;
 }
 
+// max(m, |a|, |b|), NaN-propagating
+__device__ __forceinline__ float amax_nan2(float m, float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+    return r;
+}
+
 __device__ __forceinline__ bool finite_abs(float a) { return a <= 3.402823466e38f; }
 
 // E8M0 exponent X of a block amax (NOSAT = smallest X with amax <= 448 * 2^X;
@@ -343,36 +350,50 @@ constexpr int QUANT_THREADS = 256;
 
 // shared memory of the quantise kernel (dynamic; the two input stages first),
 // every offset aligned for what it holds (TMA destinations 128 B, mbarriers 8 B)
+// NST input stages: one tile in flight while the other is processed (a third stage
+// of 32 KB, with two CTAs per SM, measured slower)
 template <int EPL, int ELT>
 struct QuantSmem {
     static constexpr int STAGE = 128 * EPL * 8 * ELT;   // 128 rows x d elements
-    static constexpr int OFF_TAB = 2 * STAGE;
+    static constexpr int NST = 2;
+    static constexpr int OFF_TAB = NST * STAGE;
     static constexpr int OFF_SCRATCH = (OFF_TAB + (int)sizeof(DocTable) + 127) / 128 * 128;   // 96 ints
-    static constexpr int OFF_RED = OFF_SCRATCH + 96 * 4;                                     // float[4][8][128]
+    static constexpr int OFF_RED = OFF_SCRATCH + 96 * 4;                                     // float[2][8] + spare
     static constexpr int OFF_XS = OFF_RED + 4 * 8 * 128 * 4;                                 // int[4][128]
-    static constexpr int OFF_BAR = OFF_XS + 4 * 128 * 4;                                     // uint64[2]
-    static constexpr int OFF_FLAG = OFF_BAR + 2 * 8;                                         // int[2]
+    static constexpr int OFF_BAR = OFF_XS + 4 * 128 * 4;                                     // uint64[NST]
+    static constexpr int OFF_FLAG = OFF_BAR + NST * 8;                                       // int[2]
     static constexpr int BYTES = OFF_FLAG + 2 * 4 + 128;                                     // + base alignment
     static_assert(STAGE % 128 == 0 && OFF_SCRATCH % 128 == 0, "TMA destinations need 128-byte alignment");
-    static_assert(OFF_BAR % 8 == 0, "mbarriers need 8-byte alignment");
+    static_assert(OFF_XS % 16 == 0 && OFF_BAR % 8 == 0, "int4 reads and mbarriers need alignment");
 };
 
+// Layouts whose unit holds the whole tile in registers before its one barrier:
+// the tile's stage is free after that barrier (quant_unit calls `release` there).
+template <int QM, int HOLD>
+constexpr bool quant_early_release() {
+    return (QM == QM_E4M3_BLOCK && HOLD == 4) || QM == QM_NVFP4;
+}
+
 // One 128-token tile (unit g of head h) of one tensor, staged in shared memory at
-// `tile`: the body every layout's kernel runs per unit.
-template <int EPL, int ELT, int QM, int HOLD>
+// `tile`. rc counts the CTA's block reductions (red[] alternates between two
+// eight-float slots, so one barrier per reduction suffices); `release()` is called
+// by every thread once no thread reads the tile any more, in the layouts of
+// quant_early_release().
+template <int EPL, int ELT, int QM, int HOLD, class Rel>
 __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTablePtrs& tab, const uint8_t* tile,
                                            float* red, int* xs, int* flag, uint32_t smask, bool& nonfin, int g,
-                                           int h, int doc, int s0, int L, int t0) {
+                                           int h, int doc, int s0, int L, int t0, int& rc, Rel& release) {
     constexpr int D = EPL * 8;
     const int H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sl = lane & 7, rw = lane >> 3;
     (void)xs;
     (void)doc;
+    (void)flag;
     if constexpr (QM == QM_E4M3_BLOCK) {
         constexpr int NBLK = 4 / HOLD;
 #pragma unroll 1
         for (int blk = 0; blk < NBLK; blk++) {
-            if (t0 + blk * HOLD * 32 >= L) break;          // block past the document end (uniform)
+            if (NBLK > 1 && t0 + blk * HOLD * 32 >= L) break;   // block past the document end (uniform)
             float y[HOLD][EPL];
             float amax = 0.0f;
 #pragma unroll
@@ -385,26 +406,22 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
                 }
                 if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
 #pragma unroll
-                for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
+                for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[hp][i], y[hp][i + 1]);
             }
-            if (!finite_abs(amax)) {   // NaN or infinity in this thread's rows
+            const bool tbad = !finite_abs(amax);   // NaN or infinity in this thread's rows
+            if (tbad) {
                 nonfin = true;
                 amax = 0.0f;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
-            if (lane == 0) {
-                red[warp] = amax;
-                if (wbad) flag[0] = 1;
-            }
-            __syncthreads();
-            amax = red[0];
+            float* rb = red + 8 * (rc++ & 1);
+            if (lane == 0) rb[warp] = amax;
+            const bool bad = __syncthreads_or(tbad) != 0;
+            if constexpr (quant_early_release<QM, HOLD>()) release();
+            amax = rb[0];
 #pragma unroll
-            for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
-            const bool bad = flag[0] != 0;
-            __syncthreads();                                 // red[] and flag[0] reused by the next block
-            if (tid == 0) flag[0] = 0;
+            for (int w = 1; w < 8; w++) amax = fmaxf(amax, rb[w]);
             float inv = 0.0f, scale = 0.0f;
             if (bad) scale = __int_as_float(0x7FC00000);
             else if (amax > 0.0f) {
@@ -440,26 +457,23 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             }
             if (p.rotate) rotate_row<EPL>(y[hp], smask, lane);
 #pragma unroll
-            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[hp][i]);
+            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[hp][i], y[hp][i + 1]);
         }
-        if (!finite_abs(amax)) {
+        const bool tbad = !finite_abs(amax);
+        if (tbad) {
             nonfin = true;
             amax = 0.0f;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const bool wbad = __any_sync(0xFFFFFFFFu, nonfin);
-        if (lane == 0) {
-            red[warp] = amax;
-            if (wbad) flag[0] = 1;
-        }
-        __syncthreads();
-        amax = red[0];
+        float* rb = red + 8 * (rc++ & 1);
+        if (lane == 0) rb[warp] = amax;
+        const bool bad = __syncthreads_or(tbad) != 0;
+        static_assert(quant_early_release<QM, HOLD>(), "the NVFP4 unit frees its stage itself");
+        release();
+        amax = rb[0];
 #pragma unroll
-        for (int w = 1; w < 8; w++) amax = fmaxf(amax, red[w]);
-        const bool bad = flag[0] != 0;
-        __syncthreads();
-        if (tid == 0) flag[0] = 0;
+        for (int w = 1; w < 8; w++) amax = fmaxf(amax, rb[w]);
         float inv = 0.0f, st_scale = 0.0f;
         if (bad) st_scale = __int_as_float(0x7FC00000);
         else if (amax > 0.0f) {
@@ -507,7 +521,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             if (p.rotate) rotate_row<EPL>(y, smask, lane);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
             bool bad = !finite_abs(amax);
             if (bad) amax = 0.0f;
 #pragma unroll
@@ -541,7 +555,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             if (p.rotate) rotate_row<EPL>(y, smask, lane);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
             bool bad = !finite_abs(amax);
             if (bad) amax = 0.0f;
 #pragma unroll
@@ -568,7 +582,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             if (p.rotate) rotate_row<EPL>(y, smask, lane);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i++) amax = amax_nan(amax, y[i]);
+            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
             bool bad = !finite_abs(amax);
             if (bad) amax = 0.0f;
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
@@ -657,21 +671,29 @@ template <int EPL, int ELT, int QM, int HOLD, class Issue>
 __device__ __forceinline__ bool quant_range(const QuantParams& p, const DocTablePtrs& tab, uint8_t* sm,
                                             uint64_t* full, float* red, int* xs, int* flag, volatile int* abort,
                                             uint32_t smask, bool& nonfin, int ubeg, int uend, int base, int n_units,
-                                            int& k, Issue& issue) {
+                                            int& k, int& rc, Issue& issue) {
     using S = QuantSmem<EPL, ELT>;
     const int H = p.H, nd = p.nd;
+    constexpr int NST = S::NST;
     for (int u = ubeg; u < uend; u += gridDim.x, k++) {
-        const int st = k & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (k >> 1) & 1, abort, 4000000000LL))) return false;
+        const int st = k % NST;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (k / NST) & 1, abort, 4000000000LL))) return false;
         const uint8_t* tile = sm + st * S::STAGE;
         const int uu = u - base;
         const int g = uu / H, h = uu % H;
         const int doc = find_doc(tab.off_tile, nd, g);
         const int s0 = tab.start[doc], L = tab.start[doc + 1] - s0;
         const int t0 = (g - tab.off_tile[doc]) * 128;      // first local token of the tile
-        quant_unit<EPL, ELT, QM, HOLD>(p, tab, tile, red, xs, flag, smask, nonfin, g, h, doc, s0, L, t0);
-        __syncthreads();                                       // every read of this stage is done
-        if (threadIdx.x == 0 && u + 2 * (int)gridDim.x < n_units) issue(u + 2 * gridDim.x, st);
+        // the stage takes unit u + NST G once no thread reads it any more
+        auto release = [&]() {
+            if (threadIdx.x == 0 && u + NST * (int)gridDim.x < n_units) issue(u + NST * gridDim.x, st);
+        };
+        quant_unit<EPL, ELT, QM, HOLD>(p, tab, tile, red, xs, flag, smask, nonfin, g, h, doc, s0, L, t0, rc,
+                                       release);
+        if constexpr (!quant_early_release<QM, HOLD>()) {
+            __syncthreads();                                   // every read of this stage is done
+            release();
+        }
     }
     return true;
 }
@@ -696,9 +718,10 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     DocTable& stab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);
     int* misc = reinterpret_cast<int*>(sm + S::OFF_SCRATCH);   // doc-table scratch, 65 ints
-    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [4][8][128]
+    float* red = reinterpret_cast<float*>(sm + S::OFF_RED);     // [2][8] used
     int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [NST]
+    constexpr int NST = S::NST;
     int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
     volatile int* abort = flag + 1;
 
@@ -714,14 +737,13 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     const int n_units = n_units_t * ntens;
     const int tid = threadIdx.x, lane = tid & 31, sl = lane & 7;
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        for (int st = 0; st < NST; st++) mbar_init(&full[st], 1);
         flag[0] = 0;
         flag[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    int issued[2] = {0, 0};   // loads issued per stage (thread 0 only)
+    int issued[NST] = {};   // loads issued per stage (thread 0 only)
     auto issue = [&](int u, int st) {
         issued[st]++;
         const int t = u / n_units_t, uu = u % n_units_t;
@@ -732,17 +754,17 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
         tma_load_3d(sm + st * S::STAGE, t == 0 ? &tm0 : (t == 1 ? &tm1 : &tm2), &full[st], 0, h, t0);
     };
     if (tid == 0) {
-        if (blockIdx.x < n_units) issue(blockIdx.x, 0);
-        if (blockIdx.x + gridDim.x < n_units) issue(blockIdx.x + gridDim.x, 1);
+        for (int st = 0; st < NST; st++)
+            if (blockIdx.x + st * gridDim.x < n_units) issue(blockIdx.x + st * gridDim.x, st);
     }
     const uint32_t smask = sign_mask<EPL>(p0, sl);                      // Q and K: one rotation
     uint32_t smask_v = smask;
     if constexpr (NT == 3) smask_v = sign_mask<EPL>(p2, sl);
     bool nonfin = false;
-    int k = 0;
+    int k = 0, rc = 0;
     if constexpr (NT == 1) {
         quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, blockIdx.x, n_units,
-                                        0, n_units, k, issue);
+                                        0, n_units, k, rc, issue);
     } else {
         // the three tensors one after another, each loop with its own parameters;
         // first(lo): this CTA's first unit at or after lo
@@ -750,16 +772,16 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
         auto first = [&](int lo) { return lo + ((b - lo % G) % G + G) % G; };
         const int n = n_units_t;
         if (quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(0), n, 0,
-                                            n_units, k, issue) &&
+                                            n_units, k, rc, issue) &&
             quant_range<EPL, ELT, QM, HOLD>(p1, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(n), 2 * n,
-                                            n, n_units, k, issue))
+                                            n, n_units, k, rc, issue))
             quant_range<EPL, ELT, QMV, HOLDV>(p2, tab, sm, full, red, xs, flag, abort, smask_v, nonfin, first(2 * n),
-                                              3 * n, 2 * n, n_units, k, issue);
+                                              3 * n, 2 * n, n_units, k, rc, issue);
     }
     if (tid == 0) {
         // every issued copy must have landed before the CTA's shared memory goes away
         // (immediate on the normal path, where each issued unit was consumed)
-        for (int st = 0; st < 2; st++)
+        for (int st = 0; st < NST; st++)
             if (issued[st]) {
                 const long long t0 = clock64();
                 while (!mbar_try_wait(&full[st], (issued[st] - 1) & 1) && clock64() - t0 < 4000000000LL) {
