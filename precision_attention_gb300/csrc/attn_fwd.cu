@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
+#include "pdl.cuh"
 
 namespace pa {
 
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(Cfg<ELT, D, MODE>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B->tmem_base;
+    pdl_wait();   // the work list, the scales and the codes of the kernels before this one
     const int n_items = p.hdr->n_items;
 
     const uint32_t sQ = smem_u32(sm + C::OFF_Q);
@@ -746,6 +748,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B->tmem_base;
+    pdl_wait();   // the work list, the scales and the codes of the kernels before this one
     const int n_items = p.hdr->n_items;
     const uint32_t sQ = smem_u32(sm + PC::OFF_Q);
     const uint32_t sKV = smem_u32(sm + PC::OFF_KV);
@@ -1355,8 +1358,7 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
     auto kern = attn_fwd_kernel<ELT, D, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::THREADS, C::SMEM, st>>>(mq, mk, mv, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, mq, mk, mv, p);
 }
 
 template <int MODE, int EXPM = ATTN_EXP_HW>
@@ -1371,8 +1373,7 @@ static cudaError_t launch_pair(const void* q, const void* k, const void* v, cons
     auto kern = attn_pair_kernel<MODE, EXPM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, PC::THREADS, PC::SMEM, st>>>(mq, mk, mv, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(PC::THREADS), PC::SMEM, st, mq, mk, mv, p);
 }
 
 // mode: 0 bf16, 1 E4M3 tile scales, 2 E4M3 per-column scales, 3 MX, 4 MX with per-token V (causal-exact)

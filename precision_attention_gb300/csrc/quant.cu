@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "params.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace pa {
@@ -714,6 +715,9 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     // QMV) in one launch, the units of the three tensors one after another
     constexpr int ntens = NT;
     using S = QuantSmem<EPL, ELT>;
+    // the forward's work-list kernel, if it comes next, touches nothing this one
+    // reads or writes: it may run beside this kernel's last tiles
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     DocTable& stab = *reinterpret_cast<DocTable*>(sm + S::OFF_TAB);

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "params.h"
+#include "pdl.cuh"
 
 namespace pa {
 
@@ -41,6 +42,10 @@ __device__ int block_exclusive_scan4(int (&v)[4], int* wsum) {
 __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
     __shared__ int wsum[32];
     __shared__ int bad;
+    // reads only cu_seqlens and writes only the work list and the header's counts,
+    // which the quantiser before it neither reads nor writes: it runs beside the
+    // quantiser's last tiles; the V-reference pass may be scheduled meanwhile
+    pdl_trigger();
     const int tid = threadIdx.x, nd = p.nd;
     if (tid == 0) bad = 0;
     __syncthreads();
@@ -105,6 +110,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
             p.hdr->n_items = 0;
             p.hdr->n_tiles = 0;
         }
+        pdl_wait();   // this kernel's completion implies the previous one's
         return;
     }
     // pass 2: work items
@@ -165,6 +171,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
         p.hdr->n_items = (int)total;
         p.hdr->n_tiles = units;
     }
+    pdl_wait();   // this kernel's completion implies the previous one's
 }
 
 // V reference scales (E4M3 layouts): the scale every row's V ratios r = s_v / ref
@@ -175,6 +182,8 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
 __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
     __shared__ float wmax[8];
     __shared__ float carry;
+    pdl_trigger();   // the attention kernel may set up; it waits for this one before its reads
+    pdl_wait();      // the work list and (through it) the quantiser's scales
     // this call's schedule: the work-list pass wrote no items when its cu_seqlens
     // were malformed (the status word's bits may be older than this call)
     if (p.hdr->n_items <= 0) return;
@@ -241,13 +250,11 @@ __global__ void __launch_bounds__(256) vref_kernel(VrefParams p) {
 }
 
 cudaError_t launch_sched(const SchedParams& p, cudaStream_t st) {
-    sched_kernel<<<1, 1024, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, st, p);
 }
 
 cudaError_t launch_vref(const VrefParams& p, cudaStream_t st) {
-    vref_kernel<<<(unsigned)(p.H * p.nd), 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(vref_kernel, dim3((unsigned)(p.H * p.nd)), dim3(256), 0, st, p);
 }
 
 }  // namespace pa
