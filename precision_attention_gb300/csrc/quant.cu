@@ -604,15 +604,20 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
         // Column maxima straight from the staged tile: warp w takes group w / 2 and
         // channel pairs 32 (w % 2) .. + 31, one pair per lane, and scans the group's
         // 32 rows (one 32-bit bf16 pair or 64-bit fp32 pair per row: consecutive
-        // words across the warp). No shuffles and one barrier; the codes are then
-        // written row-parallel as in the other layouts.
+        // words across the warp). No shuffles and one barrier. Each column's
+        // multiplier 2^-X goes to shared memory as a float, four channels per
+        // 16-byte slot ordered [group][slot of the lane's channels][lane of the
+        // row], so that the row pass reads it conflict-free, one float4 per four
+        // codes; the codes are then written row-parallel as in the other layouts.
+        constexpr int NI = EPL / 4;                                  // float4 slots per lane and row
+        float* xf = reinterpret_cast<float*>(xs);                    // [4][NI][8][4]
+        auto xf_at = [&](int gi, int c) { return ((gi * NI + (c % EPL) / 4) * 8 + c / EPL) * 4 + (c & 3); };
         uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
         {
             const int gi = warp >> 1, c = 2 * (32 * (warp & 1) + lane);   // first channel of the pair
             const int nrow = min(32, L - t0 - gi * 32);                     // rows inside the document
             float m0 = 0.0f, m1 = 0.0f;
-            for (int r = 0; r < nrow; r++) {
-                float v0, v1;
+            auto pair_at = [&](int r, float& v0, float& v1) {
                 const int row = gi * 32 + r;
                 if constexpr (ELT == 2) {
                     const uint32_t w2 = *reinterpret_cast<const uint32_t*>(tile + (row * D + c) * 2);
@@ -623,16 +628,28 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
                     v0 = f2.x;
                     v1 = f2.y;
                 }
-                m0 = amax_nan(m0, v0);
-                m1 = amax_nan(m1, v1);
+            };
+            int r = 0;
+#pragma unroll 4
+            for (; r + 1 < nrow; r += 2) {
+                float a0, a1, b0, b1;
+                pair_at(r, a0, a1);
+                pair_at(r + 1, b0, b1);
+                m0 = amax_nan2(m0, a0, b0);
+                m1 = amax_nan2(m1, a1, b1);
+            }
+            if (r < nrow) {
+                float a0, a1;
+                pair_at(r, a0, a1);
+                m0 = amax_nan(m0, a0);
+                m1 = amax_nan(m1, a1);
             }
             if (!finite_abs(m0)) { nonfin = true; m0 = 0.0f; }
             if (!finite_abs(m1)) { nonfin = true; m1 = 0.0f; }
             const bool inside = nrow > 0;                    // groups past the document end: 127
             const int X0 = inside ? e8m0_exponent(m0, p.mx_rule) : 0;
             const int X1 = inside ? e8m0_exponent(m1, p.mx_rule) : 0;
-            xs[gi * 128 + c] = X0;
-            xs[gi * 128 + c + 1] = X1;
+            *reinterpret_cast<float2*>(xf + xf_at(gi, c)) = make_float2(pow2_neg(X0), pow2_neg(X1));
             sct[(c % 32) * 16 + (c / 32) * 4 + gi] = (uint8_t)(X0 + 127);
             sct[((c + 1) % 32) * 16 + ((c + 1) / 32) * 4 + gi] = (uint8_t)(X1 + 127);
         }
@@ -645,13 +662,11 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
                 smem_row<EPL, ELT>(tile, row, sl, y);
                 uint32_t w4[EPL / 4];
 #pragma unroll
-                for (int i = 0; i < EPL / 4; i++) {
-                    const int c = sl * EPL + 4 * i;
-                    const int4 x4 = *reinterpret_cast<const int4*>(xs + gi * 128 + c);
-                    w4[i] = pack_e4m3x4(__fmul_rn(y[4 * i], pow2_neg(x4.x)),
-                                        __fmul_rn(y[4 * i + 1], pow2_neg(x4.y)),
-                                        __fmul_rn(y[4 * i + 2], pow2_neg(x4.z)),
-                                        __fmul_rn(y[4 * i + 3], pow2_neg(x4.w)));
+                for (int i = 0; i < NI; i++) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(xf + ((gi * NI + i) * 8 + sl) * 4);
+                    const float2 a = __fmul2_rn(make_float2(y[4 * i], y[4 * i + 1]), make_float2(m4.x, m4.y));
+                    const float2 b = __fmul2_rn(make_float2(y[4 * i + 2], y[4 * i + 3]), make_float2(m4.z, m4.w));
+                    w4[i] = pack_e4m3x4(a.x, a.y, b.x, b.y);
                 }
                 if constexpr (EPL == 16) {
                     *reinterpret_cast<uint4*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL) =
