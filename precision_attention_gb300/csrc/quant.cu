@@ -184,6 +184,13 @@ __device__ __forceinline__ float amax_nan(float m, float a) {
     return r;
 }
 
+// max(a, b), NaN-propagating (an infinity or NaN on either side survives)
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // max(m, |a|, |b|), NaN-propagating
 __device__ __forceinline__ float amax_nan2(float m, float a, float b) {
     float r;
@@ -486,21 +493,23 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
 #pragma unroll
         for (int hp = 0; hp < 4; hp++) {
             const int row = hp * 32 + warp * 4 + rw;
-            float z[EPL];
-            float gmax = 0.0f;
+            // the group's largest |y inv| is fl(max |y| x inv): rounding is monotone
+            float gy = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i++) {
-                z[i] = __fmul_rn(y[hp][i], inv);
-                gmax = fmaxf(gmax, fabsf(z[i]));
-            }
+            for (int i = 0; i < EPL; i += 2) gy = amax_nan2(gy, y[hp][i], y[hp][i + 1]);
+            const float gmax = __fmul_rn(gy, inv);
             const uint32_t sfb = cvt_e4m3x2(gmax, 0.0f) & 0xFFu;
             const float sfv = e4m3_value(sfb);
             const float r6 = sfv > 0.0f ? __fdiv_rn(6.0f, sfv) : 0.0f;
             uint32_t w[2] = {0u, 0u};
             if (sfv > 0.0f) {
+                const float2 inv2 = make_float2(inv, inv), r62 = make_float2(r6, r6);
 #pragma unroll
-                for (int i = 0; i < EPL; i += 2)
-                    w[i >> 3] |= cvt_e2m1x2(__fmul_rn(z[i], r6), __fmul_rn(z[i + 1], r6)) << (4 * (i & 7));
+                for (int i = 0; i < EPL; i += 2) {
+                    const float2 z = __fmul2_rn(make_float2(y[hp][i], y[hp][i + 1]), inv2);   // y x inv
+                    const float2 c = __fmul2_rn(z, r62);                                      // then x 6 / sf
+                    w[i >> 3] |= cvt_e2m1x2(c.x, c.y) << (4 * (i & 7));
+                }
             }
             const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfb, 1);
             const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfb, 2);
@@ -523,13 +532,12 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
-            bool bad = !finite_abs(amax);
-            if (bad) amax = 0.0f;
+            // the row's maximum over its 8 lanes; a NaN or infinity in any lane survives
+            // the NaN-propagating reduction and marks the row
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
-            }
+            for (int o = 1; o < 8; o <<= 1) amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            const bool bad = !finite_abs(amax);
+            if (bad) amax = 0.0f;
             if (valid) {
                 float inv = 0.0f, scale = 0.0f;
                 if (bad) {
@@ -557,13 +565,12 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
-            bool bad = !finite_abs(amax);
-            if (bad) amax = 0.0f;
+            // the row's maximum over its 8 lanes; a NaN or infinity in any lane survives
+            // the NaN-propagating reduction and marks the row
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, o) != 0);
-            }
+            for (int o = 1; o < 8; o <<= 1) amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            const bool bad = !finite_abs(amax);
+            if (bad) amax = 0.0f;
             if (valid) {
                 if (bad) nonfin = true;
                 const int X = e8m0_exponent(amax, p.mx_rule);
@@ -584,10 +591,9 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             float amax = 0.0f;
 #pragma unroll
             for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
-            bool bad = !finite_abs(amax);
+            amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));   // the 32-channel group's two lanes
+            const bool bad = !finite_abs(amax);
             if (bad) amax = 0.0f;
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            bad = bad | (__shfl_xor_sync(0xFFFFFFFFu, (int)bad, 1) != 0);
             if (bad && valid) nonfin = true;
             const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
             const uint32_t byte = (uint32_t)(X + 127);
