@@ -322,6 +322,7 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     args.world = world
+    pa.attn_set_schedule(pa.ATTN_SCHED_TICKET if args.sched == "ticket" else pa.ATTN_SCHED_STATIC)
     w = workloads.WORKLOADS[args.workload]
     r = time_workload(args, pa, torch, dev, args.workload, bool(args.exact), args.steps, args.warmup,
                       clocks_idx=local_rank, keep=True, exp_mode=EXP_MODES[args.exp_mode], nv=args.nvfp4)
@@ -591,7 +592,7 @@ EXP_MODES = {"hw": 0, "schraudolph": 1, "mitchell_p": 2}
 def config_of(args, w):
     return {"workload": f"{w.name} (workload {w.wid})", "batch": args.batch or w.batch,
             "heads": args.heads or w.heads, "seq_len": args.seqlen or w.seqlen or None, "head_dim": w.head_dim,
-            "causal": w.causal, "causal_exact": bool(args.exact), "exp_mode": args.exp_mode,
+            "causal": w.causal, "causal_exact": bool(args.exact), "exp_mode": args.exp_mode, "schedule": args.sched,
             "quant": ("NVFP4 Q, K (E2M1, E4M3 per 16 channels, fp32 per 128 tokens); V E4M3 blocks of 128 tokens"
                       if args.nvfp4 else
                       ("MXFP8 (E8M0 per 32; V one E8M0 per token, causal-exact)" if args.exact else "MXFP8 (E8M0 per 32)")
@@ -615,6 +616,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-accuracy", action="store_true")
     ap.add_argument("--no-rotate", action="store_true", help="quantise Q and K without the Hadamard rotation")
+    ap.add_argument("--sched", default="static", choices=["static", "ticket"],
+                    help="the pair kernel's work order: static longest-first rounds or just-in-time tickets")
     ap.add_argument("--quant-split", action="store_true",
                     help="quantise Q, K and V in three launches instead of one")
     ap.add_argument("--exact", action="store_true", help="causal-exact mode (one E4M3 scale per token)")

@@ -332,6 +332,18 @@ attn_status attn_read_device_status(void* workspace, void* stream, uint32_t* fla
  * pages: the bounded waits are this library's failure detection. */
 attn_status attn_set_wait_limit(int64_t cycles);
 
+/* Work order of the FP8 forward's pair kernel (head_dim 128) for the calls
+ * made after this one. ATTN_SCHED_STATIC (default): each CTA takes rounds of
+ * the longest-first work list, in alternating directions for causal work.
+ * ATTN_SCHED_TICKET: each CTA takes its next item just in time from a global
+ * counter in the workspace, the items in list order (longest first for causal
+ * work). The results are bitwise the same; only which CTA computes which item
+ * changes. Process-wide; host only. Returns ATTN_ERR_INVALID_ARG for any
+ * other value. Source: FLAMIA section 4.3 (just-in-time work acquisition by
+ * cluster launch control, against a static longest-first order). */
+typedef enum { ATTN_SCHED_STATIC = 0, ATTN_SCHED_TICKET = 1 } attn_schedule;
+attn_status attn_set_schedule(int32_t schedule);
+
 /* Static description of a status code (no counterpart on the pages). */
 const char* attn_status_string(int32_t status);
 

@@ -9,7 +9,7 @@ The functions keep the C names:
 
     attn_quantize_sizes, attn_workspace_size, attn_fwd_workspace_size,
     attn_quantize, attn_quantize_qkv, attn_fp8_fwd, attn_fp8_fwd_ex,
-    attn_bf16_fwd, attn_read_device_status, attn_status_string,
+    attn_bf16_fwd, attn_read_device_status, attn_status_string, attn_set_schedule,
     attn_device_sm_count
 """
 from __future__ import annotations
@@ -43,6 +43,8 @@ ATTN_MX_RULE_NOSAT, ATTN_MX_RULE_OCP_FLOOR = 0, 1
 ATTN_RESCALE_THRESHOLD = 0.75
 # include/attn.h attn_exp_mode: the probabilities' exponential of the FP8 forward
 ATTN_EXP_HW, ATTN_EXP_SCHRAUDOLPH, ATTN_EXP_MITCHELL_P = 0, 1, 2
+# include/attn.h attn_schedule: the pair kernel's work order
+ATTN_SCHED_STATIC, ATTN_SCHED_TICKET = 0, 1
 
 
 def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
@@ -52,7 +54,7 @@ def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
            "attn_quantize_qkv", "attn_fp8_fwd",
            "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
-           "attn_set_wait_limit")
+           "attn_set_wait_limit", "attn_set_schedule")
 
 
 class AttnError(RuntimeError):
@@ -97,9 +99,10 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_device_sm_count.argtypes = []
     L.attn_set_wait_limit.argtypes = [i64]
+    L.attn_set_schedule.argtypes = [i32]
     for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
               "attn_quantize_qkv",              "attn_fp8_fwd", "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status",
-              "attn_device_sm_count", "attn_set_wait_limit"):
+              "attn_device_sm_count", "attn_set_wait_limit", "attn_set_schedule"):
         getattr(L, f).restype = ctypes.c_int32
     if hasattr(L, "attn_pdump_set"):
         L.attn_pdump_set.argtypes = [vp, i64]
@@ -137,6 +140,12 @@ def attn_status_string(status: int) -> str:
 
 def attn_device_sm_count() -> int:
     return int(lib().attn_device_sm_count())
+
+
+def attn_set_schedule(schedule: int) -> None:
+    """ATTN_SCHED_STATIC (default) or ATTN_SCHED_TICKET (items taken just in time) for
+    later forward calls; process-wide."""
+    _check(lib().attn_set_schedule(int(schedule)), "attn_set_schedule")
 
 
 def attn_set_wait_limit(cycles: int) -> None:

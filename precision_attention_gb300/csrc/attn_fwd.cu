@@ -683,12 +683,14 @@ struct PairBars {
     uint64_t drain[2];
     uint64_t ksc_full[8], ksc_empty[8];   // per-column mode: key scales of a stage written / read
     uint64_t q_full1, q_empty1;           // Q buffer 1 (the double buffer of the non-MX modes)
+    uint64_t ring_full[8], ring_empty[8];   // just-in-time schedule: item k in slot k % 8
+    int ring[8];
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(PairBars) <= 1024, "pair kernel barrier block exceeds its reserved space");
 
-template <int MODE, int EXPM>
+template <int MODE, int EXPM, bool DYN>
 __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
@@ -727,6 +729,10 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             mbar_init(&B->ksc_full[i], 32);    // every producer lane, after its stores
             mbar_init(&B->ksc_empty[i], 256);  // every softmax thread of both query tiles
         }
+        for (int i = 0; i < 8; i++) {
+            mbar_init(&B->ring_full[i], 1);    // the producer, after writing the slot
+            mbar_init(&B->ring_empty[i], 12);  // 8 softmax warps + 2 issuers x (S, P cursor)
+        }
         B->abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmq);
@@ -764,6 +770,43 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         const int g = (int)gridDim.x, b = (int)blockIdx.x;
         return k * g + ((snake && (k & 1)) ? g - 1 - b : b);
     };
+    // Just-in-time schedule (DYN): the producer takes item k by ticket when it starts
+    // the item's loads (CTA b's first item is b; then an atomic counter the work-list
+    // pass set to the grid size) and hands it through slot k % 8 of a ring to the
+    // issuers' S and P cursors and the softmax warps, in the same order. An index past
+    // the list ends every role.
+    constexpr int kEnd = 0x7FFFFFFF;
+    auto seq_producer = [&](int k) -> int {   // warp 0, all lanes
+        if constexpr (!DYN) return item_of(k);
+        int it = kEnd;
+        if (lane == 0) {
+            const int sl = k & 7;
+            if (mbar_wait(&B->ring_empty[sl], ((k >> 3) & 1) ^ 1, abort, lim)) {
+                const int t = k == 0 ? (int)blockIdx.x : atomicAdd(&p.hdr->ticket, 1);
+                it = t < n_items ? t : kEnd;
+                B->ring[sl] = it;
+                mbar_arrive(&B->ring_full[sl]);   // releases the slot's write to the readers
+            }
+        }
+        return __shfl_sync(FULL, it, 0);
+    };
+    auto seq_issuer = [&](int k, int cursors) -> int {   // one issuing thread; cursors freeing the slot
+        if constexpr (!DYN) return item_of(k);
+        const int sl = k & 7;
+        if (!mbar_wait(&B->ring_full[sl], (k >> 3) & 1, abort, lim)) return kEnd;
+        const int it = *reinterpret_cast<volatile int*>(&B->ring[sl]);
+        for (int c = 0; c < cursors; c++) mbar_arrive(&B->ring_empty[sl]);
+        return it;
+    };
+    auto seq_softmax = [&](int k) -> int {   // a softmax warp, all lanes
+        if constexpr (!DYN) return item_of(k);
+        const int sl = k & 7;
+        if (!__all_sync(FULL, mbar_wait(&B->ring_full[sl], (k >> 3) & 1, abort, lim))) return kEnd;
+        const int it = *reinterpret_cast<volatile int*>(&B->ring[sl]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B->ring_empty[sl]);
+        return it;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -772,7 +815,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         uint32_t g = 0;
         int qi = 0;
         bool ok = true;
-        for (int k = 0, it = item_of(0); it < n_items && ok; it = item_of(++k), qi++) {
+        for (int k = 0, it = seq_producer(0); it < n_items && ok; it = seq_producer(++k), qi++) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
             const int qb = PC::q_buf(qi);   // Q buffer of this item
@@ -892,7 +935,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
             const uint32_t sfq = tmem + PC::T_SFQ + 4 * q, sfp = tmem + PC::T_SFP + 4 * q;
             const uint32_t sfk0 = tmem + PC::T_SFK + 8 * q, sfv0 = tmem + PC::T_SFV + 8 * q;
             if constexpr (PC::MXPV) tc_cp_sf(sfp, desc_sf(sSF + 1024));
-            int kS = 0, itS = item_of(0), jS = 0, qiS = 0;
+            int kS = 0, itS = seq_issuer(0, 2), jS = 0, qiS = 0;   // the P cursor starts on the same item
             uint32_t gS = 0;
             WorkItem wS = itS < n_items ? p.items[itS] : WorkItem{};
             int kP = 0, itP = itS, jP = 0;
@@ -966,7 +1009,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                     if (q == 1) tc_commit(PC::q_buf(qiS) ? &B->q_empty1 : &B->q_empty);
                     jS = 0;
                     qiS++;
-                    itS = item_of(++kS);
+                    itS = seq_issuer(++kS, 1);
                     if (itS < n_items) wS = p.items[itS];
                 }
                 sf_pre = false;
@@ -1009,7 +1052,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
                 gP++;
                 if (++jP == wP.ntiles) {
                     jP = 0;
-                    itP = item_of(++kP);
+                    itP = seq_issuer(++kP, 1);
                     if (itP < n_items) wP = p.items[itP];
                 }
                 return true;
@@ -1037,7 +1080,7 @@ __global__ void __launch_bounds__(PairCfgT<MODE>::THREADS, 1)
         auto wait_pv = [&](uint32_t gx) -> bool {
             return __all_sync(FULL, mbar_wait(&B->pv_done[q][gx & 1], (gx >> 1) & 1, abort, lim));
         };
-        for (int k = 0, it = item_of(0); it < n_items && ok; it = item_of(++k)) {
+        for (int k = 0, it = seq_softmax(0); it < n_items && ok; it = seq_softmax(++k)) {
             const WorkItem w = p.items[it];
             const DocEntry d = p.docs[w.doc];
             const int h = w.head, L = d.len, nt = w.ntiles;
@@ -1361,16 +1404,20 @@ static cudaError_t launch_t(const void* q, const void* k, const void* v, const F
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, mq, mk, mv, p);
 }
 
-template <int MODE, int EXPM = ATTN_EXP_HW>
+// DYN: the just-in-time (ticket) work order, instantiated with the hardware exp2 only
+template <int MODE, int EXPM = ATTN_EXP_HW, bool DYN = false>
 static cudaError_t launch_pair(const void* q, const void* k, const void* v, const FwdParams& p, int grid,
                                cudaStream_t st) {
+    if constexpr (EXPM == ATTN_EXP_HW && !DYN) {
+        if (p.dyn) return launch_pair<MODE, EXPM, true>(q, k, v, p, grid, st);
+    }
     using PC = PairCfgT<MODE>;
     CUtensorMap mq, mk, mv;
     // Q, K rows: 128 E4M3 bytes (128-byte swizzle), or 64 NVFP4 bytes (64-byte swizzle)
     if (!make_map(&mq, q, 1, p.T, p.H, PC::QD, PC::QD, !PC::NV) || !make_map(&mk, k, 1, p.T, p.H, PC::QD, PC::QD, !PC::NV) ||
         !make_map(&mv, v, 1, p.T, p.H, 128, 128, true))
         return cudaErrorInvalidValue;
-    auto kern = attn_pair_kernel<MODE, EXPM>;
+    auto kern = attn_pair_kernel<MODE, EXPM, DYN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(PC::THREADS), PC::SMEM, st, mq, mk, mv, p);

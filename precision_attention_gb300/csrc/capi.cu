@@ -19,6 +19,7 @@ namespace {
 
 constexpr long long kWaitLimit = 4000000000LL;   // SM cycles (about 2 s) before a wait gives up
 std::atomic<long long> g_wait_limit{kWaitLimit};   // attn_set_wait_limit
+std::atomic<int> g_schedule{ATTN_SCHED_STATIC};     // attn_set_schedule
 #ifdef PA_PDUMP
 uint8_t* g_pdump = nullptr;                        // attn_pdump_set (test build)
 long long g_pdump_stride = 0;
@@ -292,6 +293,9 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
     sp.items = items;
     sp.items_cap = L.items_cap;
     sp.qpair = mode >= 1 && d == 128;   // FP8, d = 128: two query tiles per item
+    const int grid = attn_device_sm_count();
+    if (grid < 1) return ATTN_ERR_CUDA;
+    sp.ticket0 = grid;
     cudaError_t e = launch_sched(sp, stream);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
 
@@ -310,6 +314,7 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
     const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt((double)d);
     fp.C = static_cast<float>(sc * 1.4426950408889634 / (rotated ? static_cast<double>(d) : 1.0));
     fp.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+    fp.dyn = g_schedule.load(std::memory_order_relaxed) == ATTN_SCHED_TICKET;
 #ifdef PA_PDUMP
     fp.pdump = g_pdump;
     fp.pdump_stride = g_pdump_stride;
@@ -379,8 +384,6 @@ static attn_status forward(int mode, int expm, const void* q, const void* k, con
             if ((e = launch_vref(vp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
         }
     }
-    const int grid = attn_device_sm_count();
-    if (grid < 1) return ATTN_ERR_CUDA;
     e = launch_attn(mode, expm, d, q, k, v, fp, grid, stream);
     return e == cudaSuccess ? ATTN_OK : (e == cudaErrorInvalidValue ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA);
 }
@@ -435,6 +438,12 @@ attn_status attn_pdump_set(void* buf, int64_t key_stride) {
     return ATTN_OK;
 }
 #endif
+
+attn_status attn_set_schedule(int32_t schedule) {
+    if (schedule != ATTN_SCHED_STATIC && schedule != ATTN_SCHED_TICKET) return ATTN_ERR_INVALID_ARG;
+    g_schedule.store(schedule, std::memory_order_relaxed);
+    return ATTN_OK;
+}
 
 attn_status attn_set_wait_limit(int64_t cycles) {
     g_wait_limit.store(cycles > 0 ? static_cast<long long>(cycles) : kWaitLimit, std::memory_order_relaxed);

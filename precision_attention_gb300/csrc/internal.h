@@ -68,7 +68,8 @@ struct WsHeader {
     uint32_t status;
     int32_t n_items;
     int32_t n_tiles;
-    int32_t pad[61];
+    int32_t ticket;      // next item of the just-in-time schedule (written by the work-list pass)
+    int32_t pad[60];
 };
 
 }  // namespace pa

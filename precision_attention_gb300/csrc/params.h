@@ -37,6 +37,7 @@ struct SchedParams {
     WorkItem* items;
     long long items_cap;
     int qpair;             // 1: an item covers the query tiles 2p and 2p + 1 of a document
+    int ticket0;           // first ticket of the forward's just-in-time schedule (its grid size)
 };
 
 struct VrefParams {
@@ -75,6 +76,7 @@ struct FwdParams {
     const float4* tsc;    // per (head, key tile) multipliers (E4M3 tile mode), see VrefParams
     long long tsc_cap;
     long long wait_limit;
+    int dyn;              // 1: items taken just in time by ticket (pair kernel), else static rounds
     // test build only (PA_PDUMP): every E4M3 probability code handed to the P V MMA,
     // byte [(h * T + t) * pdump_stride + k] for row t, document-local key k
     uint8_t* pdump;

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(1024) sched_kernel(SchedParams p) {
     if (tid == 0) {
         p.hdr->n_items = (int)total;
         p.hdr->n_tiles = units;
+        p.hdr->ticket = p.ticket0;   // the forward's CTAs take items 0 .. grid - 1 first
     }
     pdl_wait();   // this kernel's completion implies the previous one's
 }

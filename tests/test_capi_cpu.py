@@ -80,6 +80,14 @@ def test_wait_limit_setting_is_host_only(pa):
     assert pa.lib().attn_set_wait_limit(0) == pa.ATTN_OK     # back to the default
 
 
+def test_schedule_setting_is_host_only(pa):
+    L = pa.lib()
+    assert L.attn_set_schedule(pa.ATTN_SCHED_TICKET) == pa.ATTN_OK
+    assert L.attn_set_schedule(2) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_set_schedule(-1) == pa.ATTN_ERR_INVALID_ARG
+    assert L.attn_set_schedule(pa.ATTN_SCHED_STATIC) == pa.ATTN_OK     # back to the default
+
+
 def test_shape_rules_on_host(pa):
     """The shape checks every call starts with, through the two size queries (pure
     host functions: there cu_seqlens is only tested for presence, never read)."""
