@@ -78,11 +78,15 @@ def recorded_traffic(args, name, sources, key="bytes_per_launch"):
 
 
 def attn_traffic(args):
+    if args.sched != "static":   # the record is of the static-order kernel
+        return None
     return recorded_traffic(args, "attn_fwd_traffic.txt", ("attn_fwd.cu", "ptx.cuh", "params.h"))
 
 
 def quant_traffic(args):
-    """DRAM bytes of one step's three quantiser launches (Q, K, V)."""
+    """DRAM bytes of one step's quantisation (the one launch for Q, K and V)."""
+    if args.quant_split:
+        return None
     return recorded_traffic(args, "quant_traffic.txt", ("quant.cu", "ptx.cuh", "params.h"), "bytes_per_step")
 
 

@@ -389,14 +389,13 @@ constexpr bool quant_early_release() {
 // quant_early_release().
 template <int EPL, int ELT, int QM, int HOLD, class Rel>
 __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTablePtrs& tab, const uint8_t* tile,
-                                           float* red, int* xs, int* flag, uint32_t smask, bool& nonfin, int g,
+                                           float* red, int* xs, uint32_t smask, bool& nonfin, int g,
                                            int h, int doc, int s0, int L, int t0, int& rc, Rel& release) {
     constexpr int D = EPL * 8;
     const int H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, sl = lane & 7, rw = lane >> 3;
     (void)xs;
     (void)doc;
-    (void)flag;
     if constexpr (QM == QM_E4M3_BLOCK) {
         constexpr int NBLK = 4 / HOLD;
 #pragma unroll 1
@@ -691,7 +690,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
 // Returns false when a copy wait ran out.
 template <int EPL, int ELT, int QM, int HOLD, class Issue>
 __device__ __forceinline__ bool quant_range(const QuantParams& p, const DocTablePtrs& tab, uint8_t* sm,
-                                            uint64_t* full, float* red, int* xs, int* flag, volatile int* abort,
+                                            uint64_t* full, float* red, int* xs, volatile int* abort,
                                             uint32_t smask, bool& nonfin, int ubeg, int uend, int base, int n_units,
                                             int& k, int& rc, Issue& issue) {
     using S = QuantSmem<EPL, ELT>;
@@ -710,8 +709,7 @@ __device__ __forceinline__ bool quant_range(const QuantParams& p, const DocTable
         auto release = [&]() {
             if (threadIdx.x == 0 && u + NST * (int)gridDim.x < n_units) issue(u + NST * gridDim.x, st);
         };
-        quant_unit<EPL, ELT, QM, HOLD>(p, tab, tile, red, xs, flag, smask, nonfin, g, h, doc, s0, L, t0, rc,
-                                       release);
+        quant_unit<EPL, ELT, QM, HOLD>(p, tab, tile, red, xs, smask, nonfin, g, h, doc, s0, L, t0, rc, release);
         if constexpr (!quant_early_release<QM, HOLD>()) {
             __syncthreads();                                   // every read of this stage is done
             release();
@@ -747,7 +745,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     int* xs = reinterpret_cast<int*>(sm + S::OFF_XS);           // [4][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);   // [NST]
     constexpr int NST = S::NST;
-    int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [0] non-finite seen, [1] abort
+    int* flag = reinterpret_cast<int*>(sm + S::OFF_FLAG);       // [1] abort ([0] spare)
     volatile int* abort = flag + 1;
 
     // the document table is the same for the three tensors (one shape)
@@ -788,7 +786,7 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
     bool nonfin = false;
     int k = 0, rc = 0;
     if constexpr (NT == 1) {
-        quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, blockIdx.x, n_units,
+        quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, abort, smask, nonfin, blockIdx.x, n_units,
                                         0, n_units, k, rc, issue);
     } else {
         // the three tensors one after another, each loop with its own parameters;
@@ -796,11 +794,11 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
         const int G = gridDim.x, b = blockIdx.x;
         auto first = [&](int lo) { return lo + ((b - lo % G) % G + G) % G; };
         const int n = n_units_t;
-        if (quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(0), n, 0,
+        if (quant_range<EPL, ELT, QM, HOLD>(p0, tab, sm, full, red, xs, abort, smask, nonfin, first(0), n, 0,
                                             n_units, k, rc, issue) &&
-            quant_range<EPL, ELT, QM, HOLD>(p1, tab, sm, full, red, xs, flag, abort, smask, nonfin, first(n), 2 * n,
+            quant_range<EPL, ELT, QM, HOLD>(p1, tab, sm, full, red, xs, abort, smask, nonfin, first(n), 2 * n,
                                             n, n_units, k, rc, issue))
-            quant_range<EPL, ELT, QMV, HOLDV>(p2, tab, sm, full, red, xs, flag, abort, smask_v, nonfin, first(2 * n),
+            quant_range<EPL, ELT, QMV, HOLDV>(p2, tab, sm, full, red, xs, abort, smask_v, nonfin, first(2 * n),
                                               3 * n, 2 * n, n_units, k, rc, issue);
     }
     if (tid == 0) {
