@@ -69,6 +69,17 @@ def test_fused_equals_three_launches(wid, lengths, H, lq, bq, lv, bv, rotate, ru
     assert fus[2].rotated == 0 and fus[0].rotated == int(rotate)
 
 
+@pytest.mark.parametrize("lq,bq,lv,bv", [(E4M3, 128, E4M3, 128), (ROW, 32, COL, 32), (NV, 128, E4M3, 128)])
+def test_fused_fp32_input_head_dim_128(lq, bq, lv, bv):
+    """fp32 rows of 128 channels: 64 KB stages, one CTA per SM (the bf16 cases run two)."""
+    inp = workloads.make(2, heads=2, lengths=[300, 77, 129])
+    q, k, v, cu = to_device(inp, dtype=torch.float32)
+    sep, fus, st_sep, st_fus = _separate_and_fused(q, k, v, cu, lq, bq, lv, bv, True)
+    assert st_sep == 0 and st_fus == 0
+    for name, a, b in zip("QKV", sep, fus):
+        assert _bytes(a) == _bytes(b), name
+
+
 def test_fused_matches_oracle(oracle_mod):
     """Q, K and V of one fused launch against the oracle directly (E4M3, 128-token blocks)."""
     inp = workloads.make(2, heads=2, lengths=[300, 77, 129])
