@@ -521,34 +521,50 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
                     make_uint2(w[0], w[1]);
         }
     } else if constexpr (QM == QM_E4M3_ROW) {
-#pragma unroll 1
+        // The thread's four rows (one per pass) are held, so that the warp's 16 rows take
+        // their two IEEE divisions in one step: lane l serves row (pass (l & 15) / 4,
+        // group l & 3), lanes 0-15 forming 448 / amax and lanes 16-31 amax / 448 (one
+        // division with lane-chosen operands), instead of all 8 lanes of a row
+        // repeating both, pass after pass.
+        float y[4][EPL];
+        float am[4];   // each held row's maximum over its 8 lanes (NaN-propagating)
+#pragma unroll
         for (int ps = 0; ps < 4; ps++) {
             const int row = ps * 32 + warp * 4 + rw;
-            const bool valid = t0 + row < L;
-            float y[EPL];
-            smem_row<EPL, ELT>(tile, row, sl, y);
-            if (p.rotate) rotate_row<EPL>(y, smask, lane);
+            smem_row<EPL, ELT>(tile, row, sl, y[ps]);
+            if (p.rotate) rotate_row<EPL>(y[ps], smask, lane);
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[i], y[i + 1]);
-            // the row's maximum over its 8 lanes; a NaN or infinity in any lane survives
-            // the NaN-propagating reduction and marks the row
+            for (int i = 0; i < EPL; i += 2) amax = amax_nan2(amax, y[ps][i], y[ps][i + 1]);
 #pragma unroll
             for (int o = 1; o < 8; o <<= 1) amax = max_nan(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            const bool bad = !finite_abs(amax);
-            if (bad) amax = 0.0f;
-            if (valid) {
-                float inv = 0.0f, scale = 0.0f;
-                if (bad) {
-                    scale = __int_as_float(0x7FC00000);
-                    nonfin = true;
-                } else if (amax > 0.0f) {
-                    inv = __fdiv_rn(448.0f, amax);
-                    scale = __fdiv_rn(amax, 448.0f);
-                }
-                // block 1: the block index of a token is the token itself
-                if (sl == 0) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = scale;
-                store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y, inv);
+            am[ps] = amax;
+        }
+        const int ri = lane & 15, pr = ri >> 2, gr = ri & 3;
+        float a = 0.0f;
+#pragma unroll
+        for (int ps = 0; ps < 4; ps++) {
+            const float t = __shfl_sync(0xFFFFFFFFu, am[ps], gr * 8);
+            if (ps == pr) a = t;
+        }
+        const bool first = lane < 16;
+        float dv = 0.0f;   // 448 / amax (the codes' multiplier) or amax / 448 (the scale)
+        if (!finite_abs(a)) {
+            if (!first) dv = __int_as_float(0x7FC00000);
+        } else if (a > 0.0f) {
+            dv = __fdiv_rn(first ? 448.0f : a, first ? a : 448.0f);
+        }
+        {   // block 1: the block index of a token is the token itself
+            const int row = pr * 32 + warp * 4 + gr;
+            if (!first && t0 + row < L) static_cast<float*>(p.scales)[(long long)h * p.scale_cap + s0 + t0 + row] = dv;
+        }
+#pragma unroll
+        for (int ps = 0; ps < 4; ps++) {
+            const float inv = __shfl_sync(0xFFFFFFFFu, dv, ps * 4 + rw);   // this thread's row, pass ps
+            const int row = ps * 32 + warp * 4 + rw;
+            if (t0 + row < L) {
+                if (!finite_abs(am[ps])) nonfin = true;
+                store_codes<EPL>(p.codes + ((long long)(s0 + t0 + row) * H + h) * D + sl * EPL, y[ps], inv);
             }
         }
     } else if constexpr (QM == QM_MX_TOK) {
