@@ -570,7 +570,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
     } else if constexpr (QM == QM_MX_TOK) {
         // one E8M0 exponent per (token, head) over all d channels (the causal-exact
         // MX mode's V): scale byte at the token's own column
-#pragma unroll 1
+#pragma unroll
         for (int ps = 0; ps < 4; ps++) {
             const int row = ps * 32 + warp * 4 + rw;
             const bool valid = t0 + row < L;
@@ -596,7 +596,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
         }
     } else if constexpr (QM == QM_MX_ROW) {
         uint8_t* sct = static_cast<uint8_t*>(p.scales) + ((long long)h * p.scale_cap + g) * 512;
-#pragma unroll 1
+#pragma unroll
         for (int ps = 0; ps < 4; ps++) {
             const int r = ps * 32 + warp * 4 + rw;
             const bool valid = t0 + r < L;
