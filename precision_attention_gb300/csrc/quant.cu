@@ -611,13 +611,8 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             if (bad) amax = 0.0f;
             if (bad && valid) nonfin = true;
             const int X = valid ? e8m0_exponent(amax, p.mx_rule) : 0;
-            const uint32_t byte = (uint32_t)(X + 127);
-            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 6);
-            if (sl == 0)
-                *reinterpret_cast<uint32_t*>(sct + (r % 32) * 16 + (r / 32) * 4) =
-                    byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            // the group's scale byte, written by its first lane (group sl / 2 of the row)
+            if ((sl & 1) == 0) sct[(r % 32) * 16 + (r / 32) * 4 + (sl >> 1)] = (uint8_t)(X + 127);
             if (valid)
                 store_codes<EPL>(p.codes + ((long long)(s0 + t0 + r) * H + h) * D + sl * EPL, y, pow2_neg(X));
         }
