@@ -510,12 +510,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
                     w[i >> 3] |= cvt_e2m1x2(c.x, c.y) << (4 * (i & 7));
                 }
             }
-            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sfb, 1);
-            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sfb, 2);
-            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sfb, 3);
-            if ((sl & 3) == 0)
-                *reinterpret_cast<uint32_t*>(sft + (row % 32) * 16 + (row / 32) * 4) =
-                    sfb | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            sft[(row % 32) * 16 + (row / 32) * 4 + (sl & 3)] = (uint8_t)sfb;   // this group's scale byte
             if (t0 + row < L)
                 *reinterpret_cast<uint2*>(p.codes + ((long long)(s0 + t0 + row) * H + h) * (D / 2) + sl * 8) =
                     make_uint2(w[0], w[1]);
