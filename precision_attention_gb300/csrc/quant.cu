@@ -499,7 +499,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             const float gmax = __fmul_rn(gy, inv);
             const uint32_t sfb = cvt_e4m3x2(gmax, 0.0f) & 0xFFu;
             const float sfv = e4m3_value(sfb);
-            const float r6 = sfv > 0.0f ? __fdiv_rn(6.0f, sfv) : 0.0f;
+            const float r6 = red[16 + sfb];   // 6 / sf (table built at the kernel's start)
             uint32_t w[2] = {0u, 0u};
             if (sfv > 0.0f) {
                 const float2 inv2 = make_float2(inv, inv), r62 = make_float2(r6, r6);
@@ -770,6 +770,14 @@ __global__ void __launch_bounds__(QUANT_THREADS, 2)
         flag[0] = 0;
         flag[1] = 0;
         fence_mbar_init();
+    }
+    if constexpr (QM == QM_NVFP4) {
+        // 6 / sf for every non-negative E4M3 scale code (0 for the zero code), the IEEE
+        // division each NVFP4 group would otherwise repeat, after the reduction slots
+        if (tid < 128) {
+            const float v = e4m3_value((uint32_t)tid);
+            red[16 + tid] = v > 0.0f ? __fdiv_rn(6.0f, v) : 0.0f;
+        }
     }
     __syncthreads();
     int issued[NST] = {};   // loads issued per stage (thread 0 only)
