@@ -429,15 +429,16 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, const DocTableP
             amax = rb[0];
 #pragma unroll
             for (int w = 1; w < 8; w++) amax = fmaxf(amax, rb[w]);
-            float inv = 0.0f, scale = 0.0f;
-            if (bad) scale = __int_as_float(0x7FC00000);
-            else if (amax > 0.0f) {
-                inv = __fdiv_rn(448.0f, amax);
-                scale = __fdiv_rn(amax, 448.0f);
-            }
-            if (tid == 0) {
+            // one IEEE division per thread: even lanes 448 / amax (the codes' multiplier),
+            // odd lanes amax / 448 (the scale), the multiplier then shared from lane 0
+            const bool odd = lane & 1;
+            float dv = 0.0f;
+            if (bad) dv = odd ? __int_as_float(0x7FC00000) : 0.0f;
+            else if (amax > 0.0f) dv = __fdiv_rn(odd ? amax : 448.0f, odd ? 448.0f : amax);
+            const float inv = __shfl_sync(0xFFFFFFFFu, dv, 0);
+            if (tid == 1) {
                 const int b = tab.off_blk[doc] + (t0 + blk * HOLD * 32) / (HOLD * 32);
-                static_cast<float*>(p.scales)[(long long)h * p.scale_cap + b] = scale;
+                static_cast<float*>(p.scales)[(long long)h * p.scale_cap + b] = dv;
             }
 #pragma unroll
             for (int hp = 0; hp < HOLD; hp++) {
