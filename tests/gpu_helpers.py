@@ -101,7 +101,7 @@ def compare_outputs(o_gpu_bf16: torch.Tensor, lse_gpu: torch.Tensor, o_emu_bf16_
                     lse_emu: np.ndarray, rows=None, ties=None, lse_ties=None):
     """Parity of the GPU output with the oracle's quantised-operand emulation.
 
-    Criteria (the benchmark spec's bounds, read for a BF16 output): relative RMSE of
+    Criteria (the stated accuracy bounds, read for a BF16 output): relative RMSE of
     the BF16 outputs <= 1e-3; per element |diff| <= max(2e-3, one BF16 ulp of
     the emulated value) -- one ulp is what a rounding flip of nearly equal fp32
     values costs, and it exceeds 2e-3 wherever |O| >= 0.5; lse within 1e-3
