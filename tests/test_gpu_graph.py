@@ -3,7 +3,8 @@ lists stay on the GPU, no host synchronisation, graph capture, replay bitwise
 equal to eager). The quantiser launch and the forward's work-list, V-reference
 and attention kernels (the last three launched as programmatic dependents)
 are captured on one stream; replays on new inputs copied into the captured
-buffers give O and lse bit for bit equal to eager calls on the same inputs.
+buffers give O and lse bit for bit equal to eager calls on the same inputs,
+under the static and the ticket work order.
 """
 import pytest
 import torch
@@ -24,13 +25,22 @@ def _forward(q, k, v, cu, outs, o, lse, ws, layouts, causal, seed, stream=None):
     pa.attn_fp8_fwd(Q, K, V, cu, causal, False, 0.0, ws=ws, out=o, lse=lse, stream=stream)
 
 
+@pytest.mark.parametrize("schedule", [0, 1])   # static rounds; tickets (the counter restarts with every replay)
 @pytest.mark.parametrize("wid,layouts,causal", [
     (2, (E4M3, 128, E4M3), False),   # E4M3 tile scales (with the V-reference pass)
     (3, (E4M3, 128, E4M3), True),
     (4, (ROW, 32, COL), False),      # MXFP8 (no V-reference pass)
     (2, (NV, 128, E4M3), True),      # NVFP4 Q K^T
 ])
-def test_forward_graph_replay_bitwise(wid, layouts, causal):
+def test_forward_graph_replay_bitwise(wid, layouts, causal, schedule):
+    pa.attn_set_schedule(schedule)
+    try:
+        _graph_replay(wid, layouts, causal)
+    finally:
+        pa.attn_set_schedule(pa.ATTN_SCHED_STATIC)
+
+
+def _graph_replay(wid, layouts, causal):
     lengths = [700, 129, 1000]
     inp = workloads.make(wid, heads=4, lengths=lengths)
     q, k, v, cu = to_device(inp)
