@@ -293,6 +293,34 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
                           int32_t causal, float softmax_scale, void* o, float* lse,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes that attn_bf16_bwd needs for this shape: the forward's
+ * workspace plus two fp32 vectors per row (lse log2(e) and rowsum(dO o O)),
+ * kept per (head, 128-token tile). 256-byte aligned; host-only.
+ * Source: FLAMIA appendix F (scales and work lists on the GPU). */
+attn_status attn_bwd_workspace_size(const attn_shape* shape, size_t* bytes);
+
+/* BF16 attention backward: the gradients dq, dk, dv of o = softmax(scale q k^T) v
+ * (causal mask and packed documents as in the forward) for an upstream
+ * gradient dout. P is formed again from q, k and the forward's lse;
+ * D = rowsum(dout o o) uses the forward's bf16 o. fp32 accumulation in the
+ * tensor memory, P and dS rounded to bf16 as the operands of the dV, dK and dQ
+ * products, bf16 outputs. Deterministic: every output element has one fixed
+ * summation order, so repeated calls give the same bits.
+ * q, k, v, o, dout: device bf16 [T][H][d], contiguous, 16-byte aligned;
+ * lse: device fp32 [H][T] as attn_bf16_fwd writes it (natural log of the
+ * scaled scores). dq, dk, dv: device bf16 [T][H][d], written for every token
+ * of every document. head_dim must be 128 (else ATTN_ERR_UNSUPPORTED).
+ * softmax_scale <= 0 selects 1 / sqrt(d). Malformed cu_seqlens is reported
+ * through the status word (ATTN_ERR_BAD_SEQLENS) and writes no gradient.
+ * Source: FLAMIA section 1 (the forward and backward of the training call
+ * over the same document-local token blocks), section 4.5 (the causal
+ * backward); the gradients are the plain derivative of the forward's
+ * definition ("Fused attention kernel", Overview). */
+attn_status attn_bf16_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, const attn_shape* shape, int32_t causal, float softmax_scale,
+                          void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* FP8 forward without a caller workspace (the pages have no counterpart to
  * this call). For callers that cannot allocate device memory where they run
  * attention -- a host that owns all device memory and forbids extra

@@ -9,8 +9,8 @@ The functions keep the C names:
 
     attn_quantize_sizes, attn_workspace_size, attn_fwd_workspace_size,
     attn_quantize, attn_quantize_qkv, attn_fp8_fwd, attn_fp8_fwd_ex,
-    attn_bf16_fwd, attn_read_device_status, attn_status_string, attn_set_schedule,
-    attn_device_sm_count
+    attn_bf16_fwd, attn_bwd_workspace_size, attn_bf16_bwd, attn_read_device_status,
+    attn_status_string, attn_set_schedule, attn_device_sm_count
 """
 from __future__ import annotations
 
@@ -54,7 +54,7 @@ def rescale_threshold(head_dim: int, fp8: bool = True) -> float:
 EXPORTS = ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
            "attn_quantize_qkv", "attn_fp8_fwd",
            "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status", "attn_status_string", "attn_device_sm_count", "attn_fp8_fwd_noalloc",
-           "attn_set_wait_limit", "attn_set_schedule")
+           "attn_set_wait_limit", "attn_set_schedule", "attn_bwd_workspace_size", "attn_bf16_bwd")
 
 
 class AttnError(RuntimeError):
@@ -92,6 +92,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_fp8_fwd.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
     L.attn_fp8_fwd_ex.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, i32, vp, vp, vp, sz, vp]
     L.attn_bf16_fwd.argtypes = [vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    L.attn_bwd_workspace_size.argtypes = [S, ctypes.POINTER(sz)]
+    L.attn_bf16_bwd.argtypes = [vp, vp, vp, vp, vp, vp, S, i32, ctypes.c_float, vp, vp, vp, vp, sz, vp]
     L.attn_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.attn_fp8_fwd_noalloc.argtypes = [Q, Q, Q, S, i32, i32, ctypes.c_float, vp, vp, vp, vp]
     L.attn_fp8_fwd_noalloc.restype = ctypes.c_int32
@@ -102,7 +104,8 @@ def _load(path: str) -> ctypes.CDLL:
     L.attn_set_schedule.argtypes = [i32]
     for f in ("attn_quantize_sizes", "attn_workspace_size", "attn_fwd_workspace_size", "attn_quantize",
               "attn_quantize_qkv",              "attn_fp8_fwd", "attn_fp8_fwd_ex", "attn_bf16_fwd", "attn_read_device_status",
-              "attn_device_sm_count", "attn_set_wait_limit", "attn_set_schedule"):
+              "attn_device_sm_count", "attn_set_wait_limit", "attn_set_schedule", "attn_bwd_workspace_size",
+              "attn_bf16_bwd"):
         getattr(L, f).restype = ctypes.c_int32
     if hasattr(L, "attn_pdump_set"):
         L.attn_pdump_set.argtypes = [vp, i64]
@@ -191,6 +194,18 @@ def attn_fwd_workspace_size(T: int, H: int, d: int, num_docs: int, causal: bool)
     b = ctypes.c_size_t()
     _check(lib().attn_fwd_workspace_size(ctypes.byref(s), int(causal), ctypes.byref(b)), "attn_fwd_workspace_size")
     return b.value
+
+
+def attn_bwd_workspace_size(T: int, H: int, d: int, num_docs: int) -> int:
+    s = _Shape(T, H, d, num_docs, None if num_docs == 1 else 1)
+    b = ctypes.c_size_t()
+    _check(lib().attn_bwd_workspace_size(ctypes.byref(s), ctypes.byref(b)), "attn_bwd_workspace_size")
+    return b.value
+
+
+def bwd_workspace(T: int, H: int, d: int, num_docs: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace buffer for attn_bf16_bwd."""
+    return torch.zeros(attn_bwd_workspace_size(T, H, d, num_docs), dtype=torch.uint8, device=device)
 
 
 def workspace(T: int, H: int, d: int, num_docs: int, device="cuda") -> torch.Tensor:
@@ -358,6 +373,29 @@ def attn_bf16_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens:
                                float(softmax_scale), out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream(stream)), "attn_bf16_fwd")
     return out, lse
+
+
+def attn_bf16_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+                  lse: torch.Tensor, cu_seqlens: torch.Tensor | None, causal: bool = False,
+                  softmax_scale: float = 0.0, ws: torch.Tensor | None = None, outs=None, stream=None):
+    """BF16 attention backward: (dq, dk, dv) for the upstream gradient dout, from
+    the forward's inputs, its bf16 output o and its lse (attn_bf16_fwd)."""
+    ts = (q, k, v, o, dout)
+    assert all(t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts)
+    assert lse.dtype == torch.float32 and lse.is_contiguous()
+    T, H, d = q.shape
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if ws is None:
+        ws = bwd_workspace(T, H, d, nd, q.device)
+    if outs is None:
+        outs = tuple(torch.empty_like(q) for _ in range(3))
+    dq, dk, dv = outs
+    shape = make_shape(T, H, d, cu_seqlens)
+    _check(lib().attn_bf16_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                               lse.data_ptr(), ctypes.byref(shape), int(bool(causal)), float(softmax_scale),
+                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream(stream)), "attn_bf16_bwd")
+    return dq, dk, dv
 
 
 def attn_fp8_fwd_noalloc(q: QTensor, k: QTensor, v: QTensor, cu_seqlens: torch.Tensor | None,

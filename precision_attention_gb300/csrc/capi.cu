@@ -429,6 +429,82 @@ attn_status attn_bf16_fwd(const void* q, const void* k, const void* v, const att
                    workspace, static_cast<cudaStream_t>(stream));
 }
 
+static size_t bwd_vec_off(const attn_shape* s) { return ws_layout(s->total_tokens, s->heads, s->num_docs).total; }
+
+attn_status attn_bwd_workspace_size(const attn_shape* shape, size_t* bytes) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!bytes) return ATTN_ERR_INVALID_ARG;
+    *bytes = align_up(bwd_vec_off(shape) + 2 * sizeof(float) * 128 * static_cast<size_t>(shape->heads) *
+                                               static_cast<size_t>(tiles_cap(shape)),
+                      256);
+    return ATTN_OK;
+}
+
+attn_status attn_bf16_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, const attn_shape* shape, int32_t causal, float softmax_scale, void* dq,
+                          void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    attn_status st = check_shape(shape);
+    if (st != ATTN_OK) return st;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
+    if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    size_t need = 0;
+    attn_bwd_workspace_size(shape, &need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return ATTN_ERR_WORKSPACE;
+    const int T = shape->total_tokens, H = shape->heads, nd = shape->num_docs;
+    const WsLayout L = ws_layout(T, H, nd);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int grid = attn_device_sm_count();
+    if (grid < 2) return ATTN_ERR_CUDA;
+    grid &= ~1;   // even: each CTA alternates between the two roles (see attn_bwd.cu)
+
+    SchedParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.cu = shape->cu_seqlens;
+    sp.nd = nd;
+    sp.T = T;
+    sp.H = H;
+    sp.causal = causal != 0;
+    sp.bq = sp.bk = sp.bv = 1;
+    sp.hdr = reinterpret_cast<WsHeader*>(ws);
+    sp.docs = reinterpret_cast<DocEntry*>(ws + L.docs_off);
+    sp.items = reinterpret_cast<WorkItem*>(ws + L.items_off);
+    sp.items_cap = L.items_cap;
+    sp.qpair = 0;
+    sp.ticket0 = grid;
+    if (launch_sched(sp, s) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    bp.docs = sp.docs;
+    bp.items = sp.items;
+    bp.hdr = sp.hdr;
+    bp.o = static_cast<const uint16_t*>(o);
+    bp.dout = static_cast<const uint16_t*>(dout);
+    bp.lse = lse;
+    bp.vec = reinterpret_cast<float*>(ws + bwd_vec_off(shape));
+    bp.tiles_cap = tiles_cap(shape);
+    bp.dq = static_cast<uint16_t*>(dq);
+    bp.dk = static_cast<uint16_t*>(dk);
+    bp.dv = static_cast<uint16_t*>(dv);
+    bp.T = T;
+    bp.H = H;
+    bp.nd = nd;
+    bp.causal = causal != 0;
+    const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(128.0);
+    bp.scale = static_cast<float>(sc);
+    bp.C = static_cast<float>(sc * 1.4426950408889634);
+    bp.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+    const cudaError_t e = launch_bwd(q, k, v, dout, bp, grid, s);
+    return e == cudaSuccess ? ATTN_OK : (e == cudaErrorInvalidValue ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA);
+}
+
 #ifdef PA_PDUMP
 attn_status attn_pdump_set(void* buf, int64_t key_stride) {
     if (buf && (key_stride < 128 || key_stride % 128 || (reinterpret_cast<uintptr_t>(buf) & 15u)))

@@ -287,3 +287,36 @@ def test_test_build_exports_the_probability_dump_and_the_timed_library_does_not(
     L = pa.pdump_lib()
     assert L.attn_pdump_set(None, 0) == pa.ATTN_OK
     assert L.attn_pdump_set(16, 100) == pa.ATTN_ERR_INVALID_ARG      # stride not a multiple of 128
+
+
+def test_backward_arguments_rejected_on_host(pa):
+    """attn_bf16_bwd: every synchronous check returns before any CUDA call."""
+    L = pa.lib()
+    T, H = 1000, 4
+    fwd = pa.attn_workspace_size(T, H, 128, 3)
+    bwd = pa.attn_bwd_workspace_size(T, H, 128, 3)
+    # the forward's workspace plus lse log2(e) and D per (head, tile, row)
+    assert bwd % 256 == 0 and bwd >= fwd + 2 * 4 * 128 * H * ((T + 127) // 128 + 3)
+    fake = ctypes.c_void_p(1 << 20)                     # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    ws = ctypes.c_void_p(1 << 24)
+    cu = ctypes.c_void_p(1 << 21)
+
+    def call(shape, ptrs=None, wsp=ws, nbytes=bwd, scale=0.0):
+        p = ptrs or [fake] * 9
+        return L.attn_bf16_bwd(p[0], p[1], p[2], p[3], p[4], p[5], ctypes.byref(shape), 1, scale,
+                               p[6], p[7], p[8], wsp, nbytes, None)
+
+    shape = pa._Shape(T, H, 128, 3, cu)
+    for i in range(9):
+        ptrs = [fake] * 9
+        ptrs[i] = None
+        assert call(shape, ptrs) == pa.ATTN_ERR_INVALID_ARG, i
+        ptrs[i] = odd
+        assert call(shape, ptrs) == pa.ATTN_ERR_INVALID_ARG, i
+    assert call(shape, scale=float("nan")) == pa.ATTN_ERR_INVALID_ARG
+    assert call(pa._Shape(T, H, 64, 3, cu)) == pa.ATTN_ERR_UNSUPPORTED       # d = 128 only
+    assert call(shape, nbytes=bwd - 256) == pa.ATTN_ERR_WORKSPACE
+    assert call(shape, nbytes=fwd) == pa.ATTN_ERR_WORKSPACE                  # the forward's is too small
+    assert call(shape, wsp=ctypes.c_void_p((1 << 24) + 128)) == pa.ATTN_ERR_WORKSPACE
+    assert call(pa._Shape(T, H, 128, 3, None)) == pa.ATTN_ERR_INVALID_ARG    # 3 documents need cu_seqlens
