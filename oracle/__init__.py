@@ -93,6 +93,7 @@ def lib():
             L.or_quantize.restype = i32
             L.or_attention_fp64.argtypes = [vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, i32, vp, vp]
             L.or_attention_fp64_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, vp, vp]
+            L.or_attention_fp64_bwd_o.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp, i32, i32, dbl, vp, vp, vp]
             L.or_attention_emulate.argtypes = [ctypes.POINTER(_QT)] * 3 + [
                 i32, i32, i32, vp, i32, i32, i32, i32, dbl, ctypes.c_float, i32, vp, i32, vp, vp, vp, vp, vp]
             L.or_attention_emulate.restype = i32
@@ -326,17 +327,25 @@ def attention_fp64(q, k, v, cu_seqlens=None, causal=False, softmax_scale=None, r
     return o, lse
 
 
-def attention_fp64_backward(q, k, v, dout, cu_seqlens=None, causal=False, softmax_scale=None):
+def attention_fp64_backward(q, k, v, dout, cu_seqlens=None, causal=False, softmax_scale=None, o=None):
     """Gradients of the FP64 attention for an upstream gradient dout.
-    Returns (dq, dk, dv), each fp64 [T, H, d]."""
+    With `o` given ([T, H, d], the forward's stored output), D_i = dout_i . o_i
+    comes from it. Returns (dq, dk, dv), each fp64 [T, H, d]."""
     q, k, v, dout = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, dout))
     T, H, d = q.shape
     cu, nd = _cu(cu_seqlens, T)
     scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
     dq, dk, dv = (np.zeros((T, H, d), dtype=np.float64) for _ in range(3))
-    lib().or_attention_fp64_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, T, H, d,
-                                _ptr(cu), nd, int(bool(causal)), scale, dq.ctypes.data, dk.ctypes.data,
-                                dv.ctypes.data)
+    if o is None:
+        lib().or_attention_fp64_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, T, H, d,
+                                    _ptr(cu), nd, int(bool(causal)), scale, dq.ctypes.data, dk.ctypes.data,
+                                    dv.ctypes.data)
+    else:
+        o = np.ascontiguousarray(o, dtype=np.float64)
+        assert o.shape == q.shape
+        lib().or_attention_fp64_bwd_o(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, o.ctypes.data,
+                                      T, H, d, _ptr(cu), nd, int(bool(causal)), scale, dq.ctypes.data,
+                                      dk.ctypes.data, dv.ctypes.data)
     return dq, dk, dv
 
 

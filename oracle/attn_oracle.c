@@ -511,10 +511,14 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 /*   dV = P^T dO;  dP = dO V^T;  D_i = sum_j P_ij dP_ij  (= dO_i . O_i);       */
 /*   dS = P o (dP - D);  dQ = scale dS K;  dK = scale dS^T Q.                  */
 /* One (document, head) per unit, so a thread owns that unit's dK, dV rows.  */
+/* With a given output o (the forward's stored output, as a training step    */
+/* keeps it), D_i = dO_i . o_i is taken from that o instead; everything else */
+/* is unchanged.                                                             */
 /* ------------------------------------------------------------------------- */
 typedef struct {
     const double *q, *k, *v, *dout; int T, H, d; docs_t D; int causal; double scale;
     double *dq, *dk, *dv;
+    const double* o;   /* NULL: D from P and dP */
 } bwd_ctx;
 
 static void bwd_unit(void* vc, long u) {
@@ -555,6 +559,11 @@ static void bwd_unit(void* vc, long u) {
             dp[j] = acc;
             D += p[j] * dp[j];
         }
+        if (c->o) {
+            const double* orow = c->o + ((long)(s0 + i) * H + h) * d;
+            D = 0.0;
+            for (int x = 0; x < d; x++) D += gr[x] * orow[x];
+        }
         double* dqr = c->dq + ((long)(s0 + i) * H + h) * d;
         for (int x = 0; x < d; x++) dqr[x] = 0.0;
         for (int j = 0; j < nk; j++) {
@@ -576,7 +585,13 @@ static void bwd_unit(void* vc, long u) {
 void or_attention_fp64_bwd(const double* q, const double* k, const double* v, const double* dout, int T, int H,
                            int d, const int32_t* cu, int nd, int causal, double scale, double* dq, double* dk,
                            double* dv) {
-    bwd_ctx c = {q, k, v, dout, T, H, d, docs_make(cu, nd, T), causal, scale, dq, dk, dv};
+    or_attention_fp64_bwd_o(q, k, v, dout, NULL, T, H, d, cu, nd, causal, scale, dq, dk, dv);
+}
+
+void or_attention_fp64_bwd_o(const double* q, const double* k, const double* v, const double* dout,
+                             const double* o, int T, int H, int d, const int32_t* cu, int nd, int causal,
+                             double scale, double* dq, double* dk, double* dv) {
+    bwd_ctx c = {q, k, v, dout, T, H, d, docs_make(cu, nd, T), causal, scale, dq, dk, dv, o};
     parallel_for((long)c.D.nd * H, bwd_unit, &c);
     free(c.D.cu);
 }

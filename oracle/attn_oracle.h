@@ -93,6 +93,11 @@ void or_attention_fp64(const double* q, const double* k, const double* v, int T,
 void or_attention_fp64_bwd(const double* q, const double* k, const double* v, const double* dout, int T, int H,
                            int d, const int32_t* cu_seqlens, int num_docs, int causal, double softmax_scale,
                            double* dq, double* dk, double* dv);
+/* The same with D_i = dout_i . o_i taken from a given output o [T][H][d] (the
+ * forward's stored output; NULL = or_attention_fp64_bwd). */
+void or_attention_fp64_bwd_o(const double* q, const double* k, const double* v, const double* dout,
+                             const double* o, int T, int H, int d, const int32_t* cu_seqlens, int num_docs,
+                             int causal, double softmax_scale, double* dq, double* dk, double* dv);
 
 /* ---- O-3 quantised-operand emulation ---- */
 typedef struct {

@@ -75,3 +75,28 @@ def test_backward_packed_equals_per_document(oracle_mod):
             single = oracle.attention_fp64_backward(q[a:b], k[a:b], v[a:b], do[a:b], None, causal, 0.3)
             for g, s in zip(grads, single):
                 assert np.array_equal(g[a:b], s)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_with_stored_output(oracle_mod, causal):
+    """D taken from a given output o. With the exact forward output it is the
+    default backward (pinned above by finite differences). With o + delta, only
+    D_i moves, by c_i = dO_i . delta_i, so dV is unchanged and, from
+    dS = P o (dP - D): dQ moves by -scale c_i (P K)_i, which is attention with K
+    in place of V, and dK by -scale P^T (c o Q), which is the dV that the
+    upstream gradient c_i Q_i would get."""
+    q, k, v, do, cu = _inputs([6, 1, 9], H=2, d=8, seed=21)
+    scale = 0.45
+    o, _ = oracle.attention_fp64(q, k, v, cu, causal, scale)
+    ref = oracle.attention_fp64_backward(q, k, v, do, cu, causal, scale)
+    same = oracle.attention_fp64_backward(q, k, v, do, cu, causal, scale, o=o)
+    for a, b in zip(ref, same):
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-13)
+    delta = np.random.default_rng(4).standard_normal(o.shape) * 1e-2
+    dq, dk, dv = oracle.attention_fp64_backward(q, k, v, do, cu, causal, scale, o=o + delta)
+    c = np.sum(do * delta, axis=2, keepdims=True)                      # [T, H, 1]
+    pk, _ = oracle.attention_fp64(q, k, k, cu, causal, scale)          # (P K)_i
+    assert np.allclose(dq - ref[0], -scale * c * pk, rtol=1e-10, atol=1e-13)
+    _, _, ptcq = oracle.attention_fp64_backward(q, k, v, c * q, cu, causal, scale)
+    assert np.allclose(dk - ref[1], -scale * ptcq, rtol=1e-10, atol=1e-13)
+    assert np.array_equal(dv, ref[2])
