@@ -464,6 +464,7 @@ def gpu_arm(args, rank, world, local_rank):
                     e_["cosine_change_vs_hw_exp2"] = rr["acc"]["cosine_fp8_vs_fp64"] - hw[w_][1]["cosine_fp8_vs_fp64"]
                 bx[f"{workloads.WORKLOADS[w_].name} {name}"] = e_
         r["bit_level_exp"] = bx
+        r["backward"] = time_bwd(pa, torch, dev)
     r["fp8_peak_measured"] = measure_fp8_peak(torch, dev) if rank == 0 else None
     return r
 
@@ -486,6 +487,48 @@ def time_bf16(pa, torch, q, k, v, cu, causal, flops, ws, n=10):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n
     return {"attn_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "kernel": "attn_fwd_kernel (BF16 operands)"}
+
+
+def time_bwd(pa, torch, dev, n=10):
+    """The BF16 backward (attn_bf16_bwd: dQ, dK, dV) on the headline shape, non-causal
+    and causal: seeded bf16 inputs of that shape, o and lse from attn_bf16_fwd, then
+    n timed calls (CUDA events on the launching stream; the five [T, H, d] inputs are
+    over 600 MB, larger than L2). FLOPs: 2.5 x the forward's (five matrix products of
+    the forward's size; the kernel performs seven, as dQ forms S and dP again)."""
+    pk = load_peaks()
+    bf16_peak = float(pk["bf16_tflops"]) if pk and pk.get("bf16_tflops") else 1900.0
+    out = {}
+    B, H, N, d = 2, 32, 8192, 128
+    T = B * N
+    g = torch.Generator(device=dev).manual_seed(1234)
+    q, k, v, do = (torch.randn((T, H, d), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    cu = torch.arange(0, T + 1, N, dtype=torch.int32, device=dev)
+    ws = pa.bwd_workspace(T, H, d, B, dev)
+    outs = tuple(torch.empty_like(q) for _ in range(3))
+    for causal in (False, True):
+        o, lse = pa.attn_bf16_fwd(q, k, v, cu, causal)
+        for _ in range(3):
+            pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, causal, ws=ws, outs=outs)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, causal, ws=ws, outs=outs)
+        e1.record()
+        torch.cuda.synchronize()
+        st, _ = pa.attn_read_device_status(ws)
+        ms = e0.elapsed_time(e1) / n
+        fl = 2.5 * workloads.attention_flops(cu.cpu().numpy(), H, d, causal)
+        tf = fl / (ms * 1e-3) / 1e12
+        out["causal" if causal else "non-causal"] = {
+            "ms": ms, "tflops": tf, "frac_vs_bf16_measured": tf / bf16_peak, "status": st}
+        del o, lse
+    out.update({"config": {"batch": B, "heads": H, "seq_len": N, "head_dim": d, "dtype": "bf16"},
+                "kernels": "sched_kernel, bwd_prep_kernel, attn_bwd_kernel (three launches per call)",
+                "flops": "2.5 x forward FLOPs (causal halved)", "bf16_peak": bf16_peak,
+                "bf16_peak_basis": "MEASURED_PEAKS.json bf16_tflops (burst)" if pk else "fallback"})
+    return out
 
 
 def summarize(rr, wid, exact):
@@ -704,7 +747,8 @@ def main():
                                "bytes_per_step": qbytes, "peak_basis": hbm_basis, "traffic": quant_traffic(args)},
             "attn_ms": r["attn_ms"], "quant_ms": r["quant_ms"], "timing_stats": r["stats"],
             "clocks": r["clocks"], "accuracy": r["acc"], "bf16_path": r.get("bf16"),
-            "per_workload": r.get("per_workload"), "bit_level_exp": r.get("bit_level_exp")}
+            "per_workload": r.get("per_workload"), "bit_level_exp": r.get("bit_level_exp"),
+            "backward": r.get("backward")}
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_sample(args, r.get("inp"))
         line["cpu_baseline"].pop("seconds", None)

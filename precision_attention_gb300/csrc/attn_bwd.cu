@@ -12,35 +12,40 @@
 //
 // Two launches after the work-list pass (the forward's one-query-tile list):
 //   bwd_prep_kernel  D and lse log2(e) per row, stored per (head, 128-token
-//                    tile) so the gradient kernel fetches a tile's 128 values
-//                    with one bulk copy
+//                    tile) so the gradient kernel fetches the values of a run
+//                    of rows with one bulk copy
 //   attn_bwd_kernel  persistent; the work items alternate between two roles,
-//                    both for one (document, head, 128-token tile):
-//     dK/dV role   key tile j: K_j and V_j once, then each query tile i that
+//                    both for one (document, head, 128-token row tile), each a
+//                    loop over 64-row stream tiles:
+//     dK/dV role   key tile j: K_j and V_j once, then each 64-query tile i that
 //                  sees it: S^T = K_j Q_i^T and dP^T = V_j dO_i^T into TMEM,
-//                  P^T and dS^T in registers, written back into TMEM as bf16
-//                  over S^T and dP^T, then dV += P^T dO_i and dK += dS^T Q_i
-//                  with the A operand read from TMEM
-//     dQ role      query tile i: Q_i and dO_i once, then each key tile j it
-//                  sees: S = Q_i K_j^T, dP = dO_i V_j^T, dS into TMEM over dP,
+//                  P^T and dS^T in registers, stored as bf16 into shared
+//                  memory, then dV += P^T dO_i and dK += dS^T Q_i
+//     dQ role      query tile i: Q_i and dO_i once, then each 64-key tile j it
+//                  sees: S = Q_i K_j^T, dP = dO_i V_j^T, dS into shared memory,
 //                  dQ += dS K_j
 //   dQ is formed in its own role (S and dP computed a second time) rather than
 //   accumulated across key tiles with atomics, so the gradients are
 //   deterministic: one fixed summation order per output element.
 // Warp roles: warp 0 TMA producer (the item's two row tiles, then the two
-// stream tiles of each step, and in the dK/dV role the step's 128 lse and D
-// values, into a 2-stage ring); warp 1 TMEM owner and MMA issuer; warps 2-9
-// elementwise: two warps per 32-row TMEM lane quarter, each taking 64 of the
-// 128 columns, and the epilogue.
-// TMEM (512 columns): S [0,128), dP [128,256), dV or dQ [256,384), dK
-// [384,512). P^T of column half hh goes to [64 hh, 64 hh + 32) and dS to
-// [128 + 64 hh, ...): inside the columns that half itself loaded, so neither
-// warp overwrites S or dP values its partner has yet to read.
+// stream tiles of each step, and in the dK/dV role the step's 64 lse and D
+// values, into a 3-stage ring); warp 1 TMEM owner and MMA issuer; warps 2-9
+// elementwise in two groups of four that take the steps in turn (one thread
+// per row, all 64 columns), and together the epilogue.
+// TMEM (512 columns): two step buffers, buffer b = {S [128 b, 128 b + 64),
+// dP [128 b + 64, 128 b + 128)}, then dV or dQ [256,384), dK [384,512).
+// Shared memory holds two P/dS buffers. A step's TMEM buffer is free as soon
+// as the elementwise warps have loaded it, so the issuer keeps S and dP of the
+// next step queued ahead of the output MMAs, and the tensor pipe runs
+// S(g + 1), out(g), S(g + 2), out(g + 1), ... while the elementwise warps work
+// on the step between.
 // Every wait is bounded; on a timeout the CTA raises its flag, drains, frees
 // TMEM and returns, and the host reads ATTN_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "attn_common.cuh"
 #include "pdl.cuh"
@@ -49,15 +54,19 @@ namespace pa {
 
 namespace bwd {
 constexpr int D = 128;
-constexpr int TILE = 128 * D * 2;          // one bf16 tile of 128 rows: two 16 KB 128-byte-swizzled atoms
-constexpr int NS = 2;                      // stream-tile stages
+constexpr int TILE = 128 * D * 2;          // a bf16 row tile of 128 rows: two 16 KB 128-byte-swizzled atoms
+constexpr int SR = 64;                     // rows of a stream tile
+constexpr int XTILE = SR * D * 2;          // a stream tile: two 8 KB atoms
+constexpr int NS = 3;                      // stream-tile stages
+constexpr int PT = 128 * SR * 2;           // a P or dS operand: 128 rows x 64 bf16, one 128-byte swizzle atom
 constexpr int OFF_R = 0;                   // row tiles R0, R1
 constexpr int OFF_X = 2 * TILE;            // NS stages of the stream tiles X0, X1
-constexpr int OFF_VEC = OFF_X + NS * 2 * TILE;   // NS x {lse log2(e) [128], D [128]}
-constexpr int OFF_BAR = OFF_VEC + NS * 1024;
+constexpr int OFF_P = OFF_X + NS * 2 * XTILE;     // two buffers of {P, dS}
+constexpr int OFF_VEC = OFF_P + 2 * 2 * PT;       // NS x {lse log2(e) [64], D [64]}
+constexpr int OFF_BAR = OFF_VEC + NS * 512;
 constexpr int SMEM = OFF_BAR + 512 + 1024;
 constexpr int THREADS = 64 + 256;
-constexpr uint32_t T_S = 0, T_DP = 128, T_O0 = 256, T_O1 = 384;
+constexpr uint32_t T_O0 = 256, T_O1 = 384;
 using C = Cfg<2, D, MODE_BF16>;
 static_assert(C::TILE == TILE && C::ATOMS == 2, "bf16 d = 128 tiles are two 128-byte swizzle atoms");
 static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
@@ -65,15 +74,30 @@ static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA li
 struct Bars {
     uint64_t r_full, r_empty;
     uint64_t x_full[NS], x_empty[NS];
-    uint64_t s_full;     // S and dP of the step are in TMEM
-    uint64_t p_full;     // the step's P and dS are back in TMEM (256 arrivals)
-    uint64_t o_done;     // the step's output MMAs completed
-    uint64_t epi_done;   // the item's accumulators were read (256 arrivals)
+    uint64_t s_full[2];   // S and dP of a step are in TMEM buffer b
+    uint64_t s_free[2];   // the step group b has loaded them (128 arrivals)
+    uint64_t p_full[2];   // P and dS of the step are in shared-memory buffer b (128 arrivals)
+    uint64_t o_done[2];   // the step's output MMAs, readers of P/dS buffer b, completed
+    uint64_t epi_done;    // the item's accumulators were read (256 arrivals)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(Bars) <= 512, "backward barrier block exceeds its reserved space");
+
+// K-major B operand of S = R X^T: a 64-row stream tile, K step kk (32 bytes of channels)
+__device__ __forceinline__ uint64_t desc_x_kmajor(uint32_t base, int kk) {
+    return sdesc(base + (uint32_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32), 16, 1024, SWZ_128B);
+}
+// MN-major B operand of the output products: the stream tile's rows are the K
+// dimension (16 per step), its channels the N dimension (two atoms SR * 128 bytes apart)
+__device__ __forceinline__ uint64_t desc_x_mn(uint32_t base, int kk) {
+    return sdesc(base + (uint32_t)(kk * 16 * 128), SR * 128, 1024, SWZ_128B);
+}
+// K-major A operand of the output products: P or dS, 128 rows x 64 columns, K step kk
+__device__ __forceinline__ uint64_t desc_p64(uint32_t base, int kk) {
+    return sdesc(base + (uint32_t)(kk * 32), 16, 1024, SWZ_128B);
+}
 
 // One work item of the gradient kernel. Position `it` of the combined list holds
 // work item it / 2 of the forward's list in one of the two roles; with an even
@@ -82,28 +106,29 @@ static_assert(sizeof(Bars) <= 512, "backward barrier block exceeds its reserved 
 struct Item {
     int kv;          // 1: dK/dV of key tile rt; 0: dQ of query tile rt
     int head, start, len, toff;
-    int rt;          // the row tile (keys or queries), document-local
-    int s0, n;       // stream tiles s0 .. s0 + n - 1
+    int rt;          // the 128-row tile (keys or queries), document-local
+    int s0, n;       // 64-row stream tiles s0 .. s0 + n - 1
 };
 __device__ __forceinline__ Item decode(const BwdParams& p, int it) {
     Item x;
     x.kv = ((it & 1) ^ ((it / (int)gridDim.x) & 1)) == 0;
     const WorkItem w = p.items[it >> 1];
     const DocEntry d = p.docs[w.doc];
-    const int nt = (d.len + 127) >> 7;
+    const int nt = (d.len + 127) >> 7, n64 = (d.len + 63) >> 6;
     x.head = w.head;
     x.start = d.start;
     x.len = d.len;
     x.toff = d.toff;
-    x.n = w.ntiles;
     if (x.kv) {
         // causal: query tile qtile of the list sees qtile + 1 key tiles; key tile
         // nt - 1 - qtile is seen by as many query tiles (from itself to the last)
         x.rt = p.causal ? nt - 1 - w.qtile : w.qtile;
-        x.s0 = p.causal ? x.rt : 0;
+        x.s0 = p.causal ? 2 * x.rt : 0;
+        x.n = n64 - x.s0;
     } else {
         x.rt = w.qtile;
         x.s0 = 0;
+        x.n = p.causal ? min(2 * x.rt + 2, n64) : n64;
     }
     return x;
 }
@@ -153,7 +178,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
 __global__ void __launch_bounds__(bwd::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                    const __grid_constant__ CUtensorMap sxq, const __grid_constant__ CUtensorMap sxk,
+                    const __grid_constant__ CUtensorMap sxv, const __grid_constant__ CUtensorMap sxdo,
                     const BwdParams p) {
+    // tm*: 128-row boxes (the row tiles); sx*: 64-row boxes (the stream tiles)
     using namespace bwd;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,9 +197,12 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             mbar_init(&B->x_full[i], 1);
             mbar_init(&B->x_empty[i], 1);
         }
-        mbar_init(&B->s_full, 1);
-        mbar_init(&B->p_full, 256);
-        mbar_init(&B->o_done, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&B->s_full[i], 1);
+            mbar_init(&B->s_free[i], 128);
+            mbar_init(&B->p_full[i], 128);
+            mbar_init(&B->o_done[i], 1);
+        }
         mbar_init(&B->epi_done, 256);
         mbar_init(&B->drain, 1);
         B->abort = 0;
@@ -180,6 +211,10 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
         prefetch_tensormap(&tmdo);
+        prefetch_tensormap(&sxq);
+        prefetch_tensormap(&sxk);
+        prefetch_tensormap(&sxv);
+        prefetch_tensormap(&sxdo);
     }
     if (warp == 1) {
         tmem_alloc(&B->tmem_base, 512);
@@ -205,8 +240,8 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             const Item x = decode(p, it);
             const CUtensorMap* r0 = x.kv ? &tmk : &tmq;
             const CUtensorMap* r1 = x.kv ? &tmv : &tmdo;
-            const CUtensorMap* x0 = x.kv ? &tmq : &tmk;
-            const CUtensorMap* x1 = x.kv ? &tmdo : &tmv;
+            const CUtensorMap* x0 = x.kv ? &sxq : &sxk;
+            const CUtensorMap* x1 = x.kv ? &sxdo : &sxv;
             if (!__all_sync(FULL, mbar_wait(&B->r_empty, (qi & 1) ^ 1, abort, lim))) break;
             r_issued = qi & 1;
             if (lane == 0) {
@@ -225,19 +260,20 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 }
                 issued[st] = (g / NS) & 1;
                 if (lane == 0) {
-                    const int tile = x.s0 + t;
-                    const int row = x.start + 128 * tile;
-                    uint8_t* xs = sm + OFF_X + st * 2 * TILE;
-                    mbar_arrive_expect_tx(&B->x_full[st], 2 * TILE + (x.kv ? 1024 : 0));
+                    const int s64 = x.s0 + t;
+                    const int row = x.start + SR * s64;
+                    uint8_t* xs = sm + OFF_X + st * 2 * XTILE;
+                    mbar_arrive_expect_tx(&B->x_full[st], 2 * XTILE + (x.kv ? 512 : 0));
                     for (int a = 0; a < 2; a++) {
-                        tma_load_3d(xs + a * 16384, x0, &B->x_full[st], a * 64, x.head, row);
-                        tma_load_3d(xs + TILE + a * 16384, x1, &B->x_full[st], a * 64, x.head, row);
+                        tma_load_3d(xs + a * (SR * 128), x0, &B->x_full[st], a * 64, x.head, row);
+                        tma_load_3d(xs + XTILE + a * (SR * 128), x1, &B->x_full[st], a * 64, x.head, row);
                     }
-                    if (x.kv) {   // the query tile's lse log2(e) and D
-                        const float* vl = p.vec + ((long long)x.head * p.tiles_cap + x.toff + tile) * 128;
-                        uint8_t* dst = sm + OFF_VEC + st * 1024;
-                        bulk_load(dst, vl, 512, &B->x_full[st]);
-                        bulk_load(dst + 512, vl + (long long)p.H * p.tiles_cap * 128, 512, &B->x_full[st]);
+                    if (x.kv) {   // the 64 queries' lse log2(e) and D
+                        const float* vl = p.vec + ((long long)x.head * p.tiles_cap + x.toff + (s64 >> 1)) * 128 +
+                                          64 * (s64 & 1);
+                        uint8_t* dst = sm + OFF_VEC + st * 512;
+                        bulk_load(dst, vl, 256, &B->x_full[st]);
+                        bulk_load(dst + 256, vl + (long long)p.H * p.tiles_cap * 128, 256, &B->x_full[st]);
                     }
                 }
             }
@@ -250,91 +286,123 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t id_s = idesc(1, 1, false, false, 128, 128);   // K-major A and B
-            constexpr uint32_t id_o = idesc(1, 1, false, true, 128, 128);    // A from TMEM, MN-major B
+        // The whole warp runs the loop, so the descriptors are computed in converged
+        // code from values every lane shares; lane 0 alone executes the MMAs and
+        // their commits.
+        {
+            constexpr unsigned FULL = 0xFFFFFFFFu;
+            const bool leader = lane == 0;
+            constexpr uint32_t id_s = idesc(1, 1, false, false, 128, SR);    // K-major A and B, N = 64
+            constexpr uint32_t id_o = idesc(1, 1, false, true, 128, D);      // K-major A, MN-major B
             const uint32_t sR = smem_u32(sm + OFF_R), sX = smem_u32(sm + OFF_X);
             const uint64_t dr0 = desc_kmajor<2, D, MODE_BF16>(sR, 0);
             const uint64_t dr1 = desc_kmajor<2, D, MODE_BF16>(sR + TILE, 0);
-            const uint64_t dx0 = desc_kmajor<2, D, MODE_BF16>(sX, 0);
-            const uint64_t dx1 = desc_kmajor<2, D, MODE_BF16>(sX + TILE, 0);
-            const uint64_t vx0 = desc_v<2, D, MODE_BF16>(sX, 0);          // the stream tiles as MN-major B
-            const uint64_t vx1 = desc_v<2, D, MODE_BF16>(sX + TILE, 0);
-            constexpr uint64_t STAGE16 = (uint64_t)(2 * TILE) >> 4;
-            // TMEM column of K step kk of a P or dS operand (16 columns of keys or queries
-            // per step; column halves at 0 and 64)
-            auto acol = [](int kk) -> uint32_t { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); };
-            uint32_t g = 0;
+            // Descriptors are built once: every operand sits at a fixed shared-memory
+            // address, so a stage, buffer or K step only adds a constant to the
+            // start-address field (addresses stay below 256 KB, the field never carries).
+            const uint32_t sP0 = smem_u32(sm + OFF_P);
+            const uint64_t dxk = desc_x_kmajor(sX, 0), dxm = desc_x_mn(sX, 0), dpa = desc_p64(sP0, 0);
+            constexpr uint64_t XST16 = (uint64_t)(2 * XTILE) >> 4, X1_16 = (uint64_t)XTILE >> 4;
+            constexpr uint64_t PB16 = (uint64_t)(2 * PT) >> 4, DS16 = (uint64_t)PT >> 4;
+            constexpr uint64_t KP16 = 32 >> 4, KX16 = (16 * 128) >> 4;   // out K step: 16 columns of P, 16 rows of X
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+                return __all_sync(FULL, mbar_wait(bar, parity, abort, lim));
+            };
+            // step gs: S and dP of its stream stage into TMEM buffer gs & 1
+            auto issue_s = [&](uint32_t gs) {
+                const uint64_t x0 = dxk + (gs % NS) * XST16, x1 = x0 + X1_16;
+                const uint32_t tb = tmem + (gs & 1) * 128;
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {
+                        const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
+                        mma_f16(tb, dr0 + koff<2, D, MODE_BF16>(kk), x0 + xo, id_s, kk ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {
+                        const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
+                        mma_f16(tb + 64, dr1 + koff<2, D, MODE_BF16>(kk), x1 + xo, id_s, kk ? 1u : 0u);
+                    }
+                    tc_commit(&B->s_full[gs & 1]);
+                }
+                __syncwarp();
+            };
+            uint32_t g = 0;     // steps whose output MMAs are issued
+            uint32_t gs = 0;    // steps whose S and dP are issued
             int qi = 0;
             bool ok = true;
+            // S and dP of step gs, once its stream tiles have landed and the elementwise
+            // warps have loaded step gs - 2 out of the same TMEM buffer
+            auto try_issue_s = [&]() -> bool {
+                if (!wait_all(&B->x_full[gs % NS], (gs / NS) & 1)) return false;
+                if (gs >= 2 && !wait_all(&B->s_free[gs & 1], ((gs - 2) >> 1) & 1)) return false;
+                tc_fence_after();
+                issue_s(gs);
+                gs++;
+                return true;
+            };
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
                 const Item x = decode(p, it);
-                if (!mbar_wait(&B->r_full, qi & 1, abort, lim)) break;
-                for (int t = 0; t < x.n; t++, g++) {
-                    const int st = g % NS;
-                    if (!mbar_wait(&B->x_full[st], (g / NS) & 1, abort, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t so = st * STAGE16;
-#pragma unroll
-                    for (int kk = 0; kk < 8; kk++)
-                        mma_f16(tmem + T_S, dr0 + koff<2, D, MODE_BF16>(kk), dx0 + so + koff<2, D, MODE_BF16>(kk),
-                                id_s, kk ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 8; kk++)
-                        mma_f16(tmem + T_DP, dr1 + koff<2, D, MODE_BF16>(kk), dx1 + so + koff<2, D, MODE_BF16>(kk),
-                                id_s, kk ? 1u : 0u);
-                    tc_commit(&B->s_full);
-                    if (!mbar_wait(&B->p_full, g & 1, abort, lim)) {
+                if (!wait_all(&B->r_full, qi & 1)) break;
+                const uint32_t g_end = g + x.n;   // this item's steps: g .. g_end - 1
+                for (int t = 0; t < x.n && ok; t++, g++) {
+                    // S and dP one step ahead of the output MMAs, within the item: the pipe
+                    // runs S(g + 1), out(g), S(g + 2), out(g + 1), ... (S(g + 2) waits for the
+                    // stream stage that out(g - 1) frees, so it is issued after out(g))
+                    while (ok && gs < g_end && gs <= g + 1) ok = try_issue_s();
+                    if (!ok) break;
+                    if (!wait_all(&B->p_full[g & 1], (g >> 1) & 1)) {
                         ok = false;
                         break;
                     }
                     // the previous item's epilogue has read the accumulators
-                    if (t == 0 && qi > 0 && !mbar_wait(&B->epi_done, (qi - 1) & 1, abort, lim)) {
+                    if (t == 0 && qi > 0 && !wait_all(&B->epi_done, (qi - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (x.kv) {
+                    const uint64_t x0 = dxm + (g % NS) * XST16, x1 = x0 + X1_16;
+                    const uint64_t pb = dpa + (g & 1) * PB16, db = pb + DS16;
+                    const uint32_t acc0 = t ? 1u : 0u;
+                    if (leader) {
+                        if (x.kv) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; kk++)   // dV += P^T dO
-                            mma_f16_ta(tmem + T_O0, tmem + T_S + acol(kk), vx1 + so + voff<2, D, MODE_BF16>(kk), id_o,
-                                       (t | kk) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; kk++)   // dV += P^T dO
+                                mma_f16(tmem + T_O0, pb + kk * KP16, x1 + kk * KX16, id_o, kk ? 1u : acc0);
 #pragma unroll
-                        for (int kk = 0; kk < 8; kk++)   // dK += dS^T Q
-                            mma_f16_ta(tmem + T_O1, tmem + T_DP + acol(kk), vx0 + so + voff<2, D, MODE_BF16>(kk), id_o,
-                                       (t | kk) ? 1u : 0u);
-                    } else {
+                            for (int kk = 0; kk < 4; kk++)   // dK += dS^T Q
+                                mma_f16(tmem + T_O1, db + kk * KP16, x0 + kk * KX16, id_o, kk ? 1u : acc0);
+                        } else {
 #pragma unroll
-                        for (int kk = 0; kk < 8; kk++)   // dQ += dS K
-                            mma_f16_ta(tmem + T_O0, tmem + T_DP + acol(kk), vx0 + so + voff<2, D, MODE_BF16>(kk), id_o,
-                                       (t | kk) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; kk++)   // dQ += dS K
+                                mma_f16(tmem + T_O0, db + kk * KP16, x0 + kk * KX16, id_o, kk ? 1u : acc0);
+                        }
+                        tc_commit(&B->x_empty[g % NS]);
+                        tc_commit(&B->o_done[g & 1]);
+                        if (t == x.n - 1) tc_commit(&B->r_empty);
                     }
-                    tc_commit(&B->x_empty[st]);
-                    if (t == x.n - 1) tc_commit(&B->r_empty);
-                    tc_commit(&B->o_done);
-                    // P and dS sit over S and dP: the next step's S waits for their readers
-                    if (!mbar_wait(&B->o_done, g & 1, abort, lim)) {
-                        ok = false;
-                        break;
-                    }
+                    __syncwarp();
                 }
             }
-            // every MMA this thread issued has completed before TMEM is released
-            tc_commit(&B->drain);
-            wait_drain(&B->drain, 0, kDrainLimit);
+            // every MMA lane 0 issued has completed before TMEM is released
+            if (leader) {
+                tc_commit(&B->drain);
+                wait_drain(&B->drain, 0, kDrainLimit);
+            }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ elementwise + epilogue
+        // Two groups of four warps take the steps in turn (group gr: the steps g with
+        // g % 2 == gr, TMEM and P/dS buffer gr), so one group's chain (S from TMEM, P and
+        // dS, stores) overlaps the other's; within a group, warp w covers TMEM lane
+        // quarter w % 4 and one thread a row, all 64 columns.
         constexpr unsigned FULL = 0xFFFFFFFFu;
-        const int hh = (warp - 2) >> 2;                      // column half
+        const int gr = (warp - 2) >> 2;                      // step group
         const int quarter = warp & 3;                        // TMEM lane quarter
         const int r = quarter * 32 + lane;                   // row of the row tile
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const float c = p.C;
+        const float2 c2 = make_float2(p.C, p.C);
         uint32_t g = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -348,79 +416,138 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 row_d = p.vec[vi + (long long)p.H * p.tiles_cap * 128];
             }
             for (int t = 0; t < x.n; t++, g++) {
-                const int st = g % NS;
-                if (!__all_sync(FULL, mbar_wait(&B->s_full, g & 1, abort, lim))) {
+                const int st = g % NS, b = g & 1;
+                if (b != gr) continue;
+                if (!__all_sync(FULL, mbar_wait(&B->s_full[b], (g >> 1) & 1, abort, lim))) {
                     ok = false;
                     break;
                 }
                 // the bulk-copied vectors: observe their barrier as well (its phase cannot
-                // advance past this step before these threads arrive on p_full)
+                // advance past this step before this group arrives on p_full)
                 if (x.kv && !__all_sync(FULL, mbar_wait(&B->x_full[st], (g / NS) & 1, abort, lim))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int tile = x.s0 + t;
-                const int cbase = 128 * tile + 64 * hh;       // document-local position of column 0 of this half
-                // masked: the causal diagonal tile or a tile reaching past the document's end
-                const bool need_mask = (p.causal && tile == x.rt) || (128 * tile + 128 > x.len);
-                const float* vl = reinterpret_cast<const float*>(sm + OFF_VEC + st * 1024) + 64 * hh;
-                const float* vd = vl + 128;
-#pragma unroll
-                for (int ch = 0; ch < 2; ch++) {
-                    uint32_t us[32], ud[32];
-                    tmem_ld32(tmem + lane_off + T_S + 64 * hh + 32 * ch, us);
-                    tmem_ld32(tmem + lane_off + T_DP + 64 * hh + 32 * ch, ud);
-                    tmem_wait_ld();
-                    uint32_t pk[16], dk[16];
+                const int s64 = x.s0 + t;
+                const int cbase = SR * s64;                   // document-local position of column 0
+                // masked: a stream tile inside the causal diagonal tile, or one reaching
+                // past the document's end
+                const bool need_mask = (p.causal && (s64 >> 1) == x.rt) || (SR * s64 + SR > x.len);
+                const float* vl = reinterpret_cast<const float*>(sm + OFF_VEC + st * 512);
+                const float* vd = vl + 64;
+                const uint32_t tb = tmem + lane_off + b * 128;
+                uint32_t pk[32], dk[32];
+                // P = 2^(S c - lse log2 e), dS = P (dP - D), in pairs, 32 columns at a time;
+                // one branch-free unrolled loop per (role, masked) case
+                auto compute = [&](auto kv_c, auto mask_c, int h, const uint32_t (&us)[32], const uint32_t (&ud)[32]) {
+                    constexpr bool KV = decltype(kv_c)::value, MASK = decltype(mask_c)::value;
 #pragma unroll
                     for (int u = 0; u < 32; u += 4) {
-                        float l4[4], d4[4];
-                        if (x.kv) {
-                            const float4 a = *reinterpret_cast<const float4*>(vl + 32 * ch + u);
-                            const float4 b = *reinterpret_cast<const float4*>(vd + 32 * ch + u);
-                            l4[0] = a.x; l4[1] = a.y; l4[2] = a.z; l4[3] = a.w;
-                            d4[0] = b.x; d4[1] = b.y; d4[2] = b.z; d4[3] = b.w;
+                        const int col = 32 * h + u;
+                        float2 l01, l23, d01, d23;
+                        if constexpr (KV) {
+                            const float4 a = *reinterpret_cast<const float4*>(vl + col);
+                            const float4 bb = *reinterpret_cast<const float4*>(vd + col);
+                            l01 = make_float2(-a.x, -a.y);
+                            l23 = make_float2(-a.z, -a.w);
+                            d01 = make_float2(-bb.x, -bb.y);
+                            d23 = make_float2(-bb.z, -bb.w);
                         } else {
+                            l01 = l23 = make_float2(-row_l2, -row_l2);
+                            d01 = d23 = make_float2(-row_d, -row_d);
+                        }
+                        const float2 x01 =
+                            __ffma2_rn(make_float2(__uint_as_float(us[u]), __uint_as_float(us[u + 1])), c2, l01);
+                        const float2 x23 =
+                            __ffma2_rn(make_float2(__uint_as_float(us[u + 2]), __uint_as_float(us[u + 3])), c2, l23);
+                        float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+                        float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+                        const float2 g01 =
+                            __fadd2_rn(make_float2(__uint_as_float(ud[u]), __uint_as_float(ud[u + 1])), d01);
+                        const float2 g23 =
+                            __fadd2_rn(make_float2(__uint_as_float(ud[u + 2]), __uint_as_float(ud[u + 3])), d23);
+                        float2 s01 = __fmul2_rn(p01, g01);
+                        float2 s23 = __fmul2_rn(p23, g23);
+                        if constexpr (MASK) {
+                            float* pp[4] = {&p01.x, &p01.y, &p23.x, &p23.y};
+                            float* ss[4] = {&s01.x, &s01.y, &s23.x, &s23.y};
 #pragma unroll
                             for (int e = 0; e < 4; e++) {
-                                l4[e] = row_l2;
-                                d4[e] = row_d;
-                            }
-                        }
-                        float pe[4], ds[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            pe[e] = ex2(fmaf(__uint_as_float(us[u + e]), c, -l4[e]));
-                            ds[e] = pe[e] * (__uint_as_float(ud[u + e]) - d4[e]);
-                            if (need_mask) {
-                                const int cpos = cbase + 32 * ch + u + e;
+                                const int cpos = cbase + col + e;
                                 // dK/dV role: column = query, row = key; dQ role: the reverse
-                                const bool vis = cpos < x.len &&
-                                                 (!p.causal || (x.kv ? cpos >= rpos : cpos <= rpos));
-                                pe[e] = vis ? pe[e] : 0.0f;
-                                ds[e] = vis ? ds[e] : 0.0f;
+                                const bool vis = cpos < x.len && (!p.causal || (KV ? cpos >= rpos : cpos <= rpos));
+                                *pp[e] = vis ? *pp[e] : 0.0f;
+                                *ss[e] = vis ? *ss[e] : 0.0f;
                             }
                         }
-                        pk[u / 2] = pack_bf16x2(pe[0], pe[1]);
-                        pk[u / 2 + 1] = pack_bf16x2(pe[2], pe[3]);
-                        dk[u / 2] = pack_bf16x2(ds[0], ds[1]);
-                        dk[u / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+                        if constexpr (KV) {
+                            pk[col / 2] = pack_bf16x2(p01.x, p01.y);
+                            pk[col / 2 + 1] = pack_bf16x2(p23.x, p23.y);
+                        }
+                        dk[col / 2] = pack_bf16x2(s01.x, s01.y);
+                        dk[col / 2 + 1] = pack_bf16x2(s23.x, s23.y);
                     }
-                    if (x.kv) tmem_st16(tmem + lane_off + T_S + 64 * hh + 16 * ch, pk);
-                    tmem_st16(tmem + lane_off + T_DP + 64 * hh + 16 * ch, dk);
+                };
+                auto dispatch = [&](int h, const uint32_t (&us)[32], const uint32_t (&ud)[32]) {
+                    if (x.kv) {
+                        if (need_mask) compute(std::true_type{}, std::true_type{}, h, us, ud);
+                        else compute(std::true_type{}, std::false_type{}, h, us, ud);
+                    } else {
+                        if (need_mask) compute(std::false_type{}, std::true_type{}, h, us, ud);
+                        else compute(std::false_type{}, std::false_type{}, h, us, ud);
+                    }
+                };
+                {
+                    uint32_t us[32], ud[32];
+                    tmem_ld32(tb, us);
+                    tmem_ld32(tb + 64, ud);
+                    tmem_wait_ld();
+                    dispatch(0, us, ud);
                 }
-                tmem_wait_st();
+                {
+                    uint32_t us[32], ud[32];
+                    tmem_ld32(tb + 32, us);
+                    tmem_ld32(tb + 96, ud);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&B->s_free[b]);   // the TMEM buffer may take step g + 2
+                    dispatch(1, us, ud);
+                }
+                // the P/dS buffer was last read by the output MMAs of step g - 2
+                if (g >= 2 && !__all_sync(FULL, mbar_wait(&B->o_done[b], ((g - 2) >> 1) & 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                // the row -> shared memory (128-byte swizzled K-major rows of 64 columns)
+                uint8_t* pbuf = sm + OFF_P + b * 2 * PT;
+#pragma unroll
+                for (int cc = 0; cc < 8; cc++) {
+                    const int off = r * 128 + ((cc ^ (r & 7)) << 4);
+                    if (x.kv)
+                        *reinterpret_cast<uint4*>(pbuf + off) =
+                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+                    *reinterpret_cast<uint4*>(pbuf + PT + off) =
+                        make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
+                }
+                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&B->p_full);
+                mbar_arrive(&B->p_full[b]);
             }
-            if (!ok) break;
-            // epilogue: the accumulators of this half of the channels -> bf16 rows
-            if (!__all_sync(FULL, mbar_wait(&B->o_done, (g - 1) & 1, abort, lim))) {
+            // epilogue: the group that ran the item's last step waits for its output MMAs
+            // (it has waited on every earlier phase of that barrier), then both groups
+            // store: warp w the rows of lane quarter w % 4, channel half hh. Every
+            // elementwise thread reaches this barrier once per item, stopped or not, and
+            // all take the same exit decision from it.
+            if (ok && ((g - 1) & 1) == (uint32_t)gr &&
+                !__all_sync(FULL, mbar_wait(&B->o_done[gr], ((g - 1) >> 1) & 1, abort, lim)))
+                ok = false;
+            if (named_bar_or(1, 256, !ok || *abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const int hh = gr;
             const bool store = rpos < x.len;
             const long long row = ((long long)(x.start + (store ? rpos : 0)) * p.H + x.head) * D + 64 * hh;
             for (int which = 0; which < (x.kv ? 2 : 1); which++) {
@@ -467,15 +594,18 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        cudaStream_t st) {
     using namespace bwd;
     if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mdo;
-    if (!make_map(&mq, q, 2, p.T, p.H, D, 64, true) || !make_map(&mk, k, 2, p.T, p.H, D, 64, true) ||
-        !make_map(&mv, v, 2, p.T, p.H, D, 64, true) || !make_map(&mdo, dout, 2, p.T, p.H, D, 64, true))
-        return cudaErrorInvalidValue;
+    CUtensorMap m[8];
+    const void* base[4] = {q, k, v, dout};
+    for (int i = 0; i < 8; i++)
+        if (!make_tensor_map_3d(&m[i], base[i & 3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H, p.T, (uint64_t)D * 2,
+                                (uint64_t)p.H * D * 2, 64, i < 4 ? 128 : SR, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(bwd_prep_kernel, dim3((unsigned)p.tiles_cap, (unsigned)p.H), dim3(256), 0, st, p);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_bwd_kernel, dim3(grid), dim3(THREADS), SMEM, st, mq, mk, mv, mdo, p);
+    return launch_pdl(attn_bwd_kernel, dim3(grid), dim3(THREADS), SMEM, st, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+                      m[7], p);
 }
 
 }  // namespace pa
