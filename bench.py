@@ -489,7 +489,7 @@ def time_bf16(pa, torch, q, k, v, cu, causal, flops, ws, n=10):
     return {"attn_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "kernel": "attn_fwd_kernel (BF16 operands)"}
 
 
-def time_bwd(pa, torch, dev, n=10):
+def time_bwd(pa, torch, dev, n=10, B=2, H=32, N=8192, causals=(False, True), warmup=3):
     """The BF16 backward (attn_bf16_bwd: dQ, dK, dV) on the headline shape, non-causal
     and causal: seeded bf16 inputs of that shape, o and lse from attn_bf16_fwd, then
     n timed calls (CUDA events on the launching stream; the five [T, H, d] inputs are
@@ -498,16 +498,16 @@ def time_bwd(pa, torch, dev, n=10):
     pk = load_peaks()
     bf16_peak = float(pk["bf16_tflops"]) if pk and pk.get("bf16_tflops") else 1900.0
     out = {}
-    B, H, N, d = 2, 32, 8192, 128
+    d = 128
     T = B * N
     g = torch.Generator(device=dev).manual_seed(1234)
     q, k, v, do = (torch.randn((T, H, d), device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
     cu = torch.arange(0, T + 1, N, dtype=torch.int32, device=dev)
     ws = pa.bwd_workspace(T, H, d, B, dev)
     outs = tuple(torch.empty_like(q) for _ in range(3))
-    for causal in (False, True):
+    for causal in causals:
         o, lse = pa.attn_bf16_fwd(q, k, v, cu, causal)
-        for _ in range(3):
+        for _ in range(warmup):
             pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, causal, ws=ws, outs=outs)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -672,6 +672,10 @@ def main():
                     help="the mixed NVFP4/FP8 path: NVFP4 Q and K (Q K^T on the FP4 tensor cores), E4M3 V")
     ap.add_argument("--exp-mode", default="hw", choices=sorted(EXP_MODES),
                     help="the probabilities' exponential: the hardware exp2 (default), Schraudolph's, or log-domain P")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the BF16 backward (attn_bf16_bwd) on --batch/--heads/--seqlen "
+                         "(default B2 H32 N8192), --steps calls after --warmup, and print its JSON")
+    ap.add_argument("--causal", action="store_true", help="with --backward-only: the causal backward only")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip timing the other benchmark configurations in the same process")
     args = ap.parse_args()
@@ -683,6 +687,17 @@ def main():
 
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        return
+
+    if args.backward_only:
+        import torch
+        from precision_attention_gb300 import build as pbuild
+        pbuild.build()
+        import precision_attention_gb300 as pa
+        torch.cuda.set_device(0)
+        res = time_bwd(pa, torch, torch.device("cuda"), n=args.steps, B=args.batch or 2, H=args.heads or 32,
+                       N=args.seqlen or 8192, causals=(True,) if args.causal else (False,), warmup=args.warmup)
+        print(json.dumps({"backward": res}), flush=True)
         return
 
     if world > 1:
