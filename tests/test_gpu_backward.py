@@ -165,3 +165,44 @@ def test_backward_malformed_seqlens_writes_status():
     ws = pa.bwd_workspace(T, H, d, 3)
     pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, False, ws=ws)
     assert pa.attn_read_device_status(ws)[0] == pa.ATTN_ERR_BAD_SEQLENS
+
+
+def test_backward_short_wait_limit_then_context_usable():
+    """Failure detection without a fault: under a 100-cycle wait limit the
+    gradient kernel either completes or gives up with ATTN_ERR_DEVICE_TIMEOUT
+    (letting its copies and MMAs finish and freeing TMEM first); either way the
+    next call in the same context, default limit, gives the bits of a clean call.
+    Each bounded wait starts with mbarrier.try_wait, which suspends until the
+    phase completes or a hardware window passes, so a limit is reached only by a
+    wait longer than two such windows; the backward's steps are shorter, and the
+    forward's failure test (test_gpu_failure.py) is the one whose wait runs out."""
+    inp = workloads.make(2, heads=2, lengths=[300, 77, 129])
+    q, k, v, cu = to_device(inp)
+    T, H, d = q.shape
+    do = torch.from_numpy(_dout(T, H, d)).to(torch.bfloat16).cuda()
+    o, lse = pa.attn_bf16_fwd(q, k, v, cu, True)
+    clean = pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, True)
+    ws = pa.bwd_workspace(T, H, d, 3)
+    try:
+        pa.attn_set_wait_limit(100)   # SM cycles: no copy or MMA completes that fast
+        pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, True, ws=ws)
+        st, flags = pa.attn_read_device_status(ws)
+    finally:
+        pa.attn_set_wait_limit(0)
+    assert st in (pa.ATTN_OK, pa.ATTN_ERR_DEVICE_TIMEOUT), (st, flags)
+    again = pa.attn_bf16_bwd(q, k, v, o, do, lse, cu, True, ws=ws)
+    assert pa.attn_read_device_status(ws)[0] == 0
+    for a, b in zip(clean, again):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_backward_many_small_documents():
+    """About a thousand documents of 1 to 12 tokens (one partial tile each, the
+    prep kernel's document search over a long table), causal, against FP64."""
+    lens = workloads.doc_lengths(6000, 1, 12, seed=21)
+    assert len(lens) > 800
+    inp = workloads.make(2, heads=2, lengths=list(lens))
+    T, H, d = inp.q.shape
+    do = _dout(T, H, d, seed=80)
+    got, o_used = _run(inp, True, do)
+    _check_all(inp, do, True, 0.0, got, o_used)
