@@ -32,13 +32,14 @@
 // values, into a 3-stage ring); warp 1 TMEM owner and MMA issuer; warps 2-9
 // elementwise in two groups of four that take the steps in turn (one thread
 // per row, all 64 columns), and together the epilogue.
-// TMEM (512 columns): two step buffers, buffer b = {S [128 b, 128 b + 64),
-// dP [128 b + 64, 128 b + 128)}, then dV or dQ [256,384), dK [384,512).
-// Shared memory holds two P/dS buffers. A step's TMEM buffer is free as soon
-// as the elementwise warps have loaded it, so the issuer keeps S and dP of the
-// next step queued ahead of the output MMAs, and the tensor pipe runs
-// S(g + 1), out(g), S(g + 2), out(g + 1), ... while the elementwise warps work
-// on the step between.
+// TMEM (512 columns): the item's two row tiles [0,128) as the A operand of S
+// and dP (the elementwise warps copy them in from the TMA-loaded tiles once per
+// item), so those MMAs read only their B slice from shared memory; S [128,192)
+// and dP [192,256); dV or dQ [256,384), dK [384,512). Shared memory holds two
+// P/dS buffers. The S/dP columns are free as soon as a group has loaded them,
+// so the issuer keeps S and dP of the next step queued ahead of the output
+// MMAs, and the tensor pipe runs S(g + 1), out(g), S(g + 2), out(g + 1), ...
+// while the elementwise warps work on the step between.
 // Every wait is bounded; on a timeout the CTA raises its flag, drains, frees
 // TMEM and returns, and the host reads ATTN_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
@@ -66,16 +67,19 @@ constexpr int OFF_VEC = OFF_P + 2 * 2 * PT;       // NS x {lse log2(e) [64], D [
 constexpr int OFF_BAR = OFF_VEC + NS * 512;
 constexpr int SMEM = OFF_BAR + 512 + 1024;
 constexpr int THREADS = 64 + 256;
-constexpr uint32_t T_O0 = 256, T_O1 = 384;
+// TMEM columns: the row tiles as the A operand of S and dP (bf16 pairs, column c of
+// a row holding channels 2c, 2c + 1), the one S/dP buffer, the accumulators
+constexpr uint32_t T_R0 = 0, T_R1 = 64, T_S = 128, T_DP = 192, T_O0 = 256, T_O1 = 384;
 using C = Cfg<2, D, MODE_BF16>;
 static_assert(C::TILE == TILE && C::ATOMS == 2, "bf16 d = 128 tiles are two 128-byte swizzle atoms");
 static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
 
 struct Bars {
     uint64_t r_full, r_empty;
+    uint64_t r_tmem;      // the item's row tiles copied into TMEM (256 arrivals)
     uint64_t x_full[NS], x_empty[NS];
-    uint64_t s_full[2];   // S and dP of a step are in TMEM buffer b
-    uint64_t s_free[2];   // the step group b has loaded them (128 arrivals)
+    uint64_t s_full[2];   // S and dP of a step of group b are in TMEM
+    uint64_t s_free[2];   // group b has loaded them (128 arrivals)
     uint64_t p_full[2];   // P and dS of the step are in shared-memory buffer b (128 arrivals)
     uint64_t o_done[2];   // the step's output MMAs, readers of P/dS buffer b, completed
     uint64_t epi_done;    // the item's accumulators were read (256 arrivals)
@@ -192,6 +196,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&B->r_full, 1);
+        mbar_init(&B->r_tmem, 256);
         mbar_init(&B->r_empty, 1);
         for (int i = 0; i < NS; i++) {
             mbar_init(&B->x_full[i], 1);
@@ -294,9 +299,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             const bool leader = lane == 0;
             constexpr uint32_t id_s = idesc(1, 1, false, false, 128, SR);    // K-major A and B, N = 64
             constexpr uint32_t id_o = idesc(1, 1, false, true, 128, D);      // K-major A, MN-major B
-            const uint32_t sR = smem_u32(sm + OFF_R), sX = smem_u32(sm + OFF_X);
-            const uint64_t dr0 = desc_kmajor<2, D, MODE_BF16>(sR, 0);
-            const uint64_t dr1 = desc_kmajor<2, D, MODE_BF16>(sR + TILE, 0);
+            const uint32_t sX = smem_u32(sm + OFF_X);
             // Descriptors are built once: every operand sits at a fixed shared-memory
             // address, so a stage, buffer or K step only adds a constant to the
             // start-address field (addresses stay below 256 KB, the field never carries).
@@ -309,19 +312,20 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 return __all_sync(FULL, mbar_wait(bar, parity, abort, lim));
             };
             // step gs: S and dP of its stream stage into TMEM buffer gs & 1
+            // (A, the row tiles, from TMEM: each MMA reads only its 2 KB B slice from
+            // shared memory, so the N = 64 products run at the tensor rate)
             auto issue_s = [&](uint32_t gs) {
                 const uint64_t x0 = dxk + (gs % NS) * XST16, x1 = x0 + X1_16;
-                const uint32_t tb = tmem + (gs & 1) * 128;
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < 8; kk++) {
                         const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
-                        mma_f16(tb, dr0 + koff<2, D, MODE_BF16>(kk), x0 + xo, id_s, kk ? 1u : 0u);
+                        mma_f16_ta(tmem + T_S, tmem + T_R0 + 8 * kk, x0 + xo, id_s, kk ? 1u : 0u);
                     }
 #pragma unroll
                     for (int kk = 0; kk < 8; kk++) {
                         const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
-                        mma_f16(tb + 64, dr1 + koff<2, D, MODE_BF16>(kk), x1 + xo, id_s, kk ? 1u : 0u);
+                        mma_f16_ta(tmem + T_DP, tmem + T_R1 + 8 * kk, x1 + xo, id_s, kk ? 1u : 0u);
                     }
                     tc_commit(&B->s_full[gs & 1]);
                 }
@@ -332,10 +336,10 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             int qi = 0;
             bool ok = true;
             // S and dP of step gs, once its stream tiles have landed and the elementwise
-            // warps have loaded step gs - 2 out of the same TMEM buffer
+            // warps have loaded step gs - 1 out of the S/dP columns
             auto try_issue_s = [&]() -> bool {
                 if (!wait_all(&B->x_full[gs % NS], (gs / NS) & 1)) return false;
-                if (gs >= 2 && !wait_all(&B->s_free[gs & 1], ((gs - 2) >> 1) & 1)) return false;
+                if (gs >= 1 && !wait_all(&B->s_free[(gs - 1) & 1], ((gs - 1) >> 1) & 1)) return false;
                 tc_fence_after();
                 issue_s(gs);
                 gs++;
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             };
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
                 const Item x = decode(p, it);
-                if (!wait_all(&B->r_full, qi & 1)) break;
+                if (!wait_all(&B->r_tmem, qi & 1)) break;   // the row tiles, in TMEM
                 const uint32_t g_end = g + x.n;   // this item's steps: g .. g_end - 1
                 for (int t = 0; t < x.n && ok; t++, g++) {
                     // S and dP one step ahead of the output MMAs, within the item: the pipe
@@ -404,8 +408,9 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float2 c2 = make_float2(p.C, p.C);
         uint32_t g = 0;
+        int qi = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
             const Item x = decode(p, it);
             const int rpos = 128 * x.rt + r;                 // document-local position of this row
             // dQ role: this row's lse log2(e) and D
@@ -415,7 +420,29 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 row_l2 = p.vec[vi];
                 row_d = p.vec[vi + (long long)p.H * p.tiles_cap * 128];
             }
-            for (int t = 0; t < x.n; t++, g++) {
+            // the item's row tiles into TMEM (group 0: R0, group 1: R1; a thread its row).
+            // Every MMA of the previous item has completed: its epilogue waited for them.
+            if (ok && !__all_sync(FULL, mbar_wait(&B->r_full, qi & 1, abort, lim))) ok = false;
+            if (ok) {
+                const uint8_t* rt = sm + OFF_R + gr * TILE + r * 128;
+#pragma unroll
+                for (int a = 0; a < 2; a++) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; c8++) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(rt + a * 16384 + ((c8 ^ (r & 7)) << 4));
+                        w[4 * c8] = v4.x;
+                        w[4 * c8 + 1] = v4.y;
+                        w[4 * c8 + 2] = v4.z;
+                        w[4 * c8 + 3] = v4.w;
+                    }
+                    tmem_st32(tmem + lane_off + (gr ? T_R1 : T_R0) + 32 * a, w);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&B->r_tmem);
+            }
+            for (int t = 0; t < x.n && ok; t++, g++) {
                 const int st = g % NS, b = g & 1;
                 if (b != gr) continue;
                 if (!__all_sync(FULL, mbar_wait(&B->s_full[b], (g >> 1) & 1, abort, lim))) {
@@ -436,7 +463,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 const bool need_mask = (p.causal && (s64 >> 1) == x.rt) || (SR * s64 + SR > x.len);
                 const float* vl = reinterpret_cast<const float*>(sm + OFF_VEC + st * 512);
                 const float* vd = vl + 64;
-                const uint32_t tb = tmem + lane_off + b * 128;
+                const uint32_t tb = tmem + lane_off + T_S;
                 uint32_t pk[32], dk[32];
                 // P = 2^(S c - lse log2 e), dS = P (dP - D), in pairs, 32 columns at a time;
                 // one branch-free unrolled loop per (role, masked) case
@@ -511,7 +538,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                     tmem_ld32(tb + 96, ud);
                     tmem_wait_ld();
                     tc_fence_before();
-                    mbar_arrive(&B->s_free[b]);   // the TMEM buffer may take step g + 2
+                    mbar_arrive(&B->s_free[b]);   // the S/dP columns may take step g + 1
                     dispatch(1, us, ud);
                 }
                 // the P/dS buffer was last read by the output MMAs of step g - 2
