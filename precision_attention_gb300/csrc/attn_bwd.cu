@@ -75,7 +75,7 @@ static_assert(C::TILE == TILE && C::ATOMS == 2, "bf16 d = 128 tiles are two 128-
 static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
 
 struct Bars {
-    uint64_t r_full, r_empty;
+    uint64_t r_full, r_empty;   // the item's row tiles landed in shared memory / may be replaced
     uint64_t r_tmem;      // the item's row tiles copied into TMEM (256 arrivals)
     uint64_t x_full[NS], x_empty[NS];
     uint64_t s_full[2];   // S and dP of a step of group b are in TMEM
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
         {
             constexpr unsigned FULL = 0xFFFFFFFFu;
             const bool leader = lane == 0;
-            constexpr uint32_t id_s = idesc(1, 1, false, false, 128, SR);    // K-major A and B, N = 64
+            constexpr uint32_t id_s = idesc(1, 1, false, false, 128, SR);    // A from TMEM, K-major B, N = 64
             constexpr uint32_t id_o = idesc(1, 1, false, true, 128, D);      // K-major A, MN-major B
             const uint32_t sX = smem_u32(sm + OFF_X);
             // Descriptors are built once: every operand sits at a fixed shared-memory
