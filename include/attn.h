@@ -309,7 +309,7 @@ attn_status attn_bwd_workspace_size(const attn_shape* shape, size_t* bytes);
  * q, k, v, o, dout: device bf16 [T][H][d], contiguous, 16-byte aligned;
  * lse: device fp32 [H][T] as attn_bf16_fwd writes it (natural log of the
  * scaled scores). dq, dk, dv: device bf16 [T][H][d], written for every token
- * of every document. head_dim must be 128 (else ATTN_ERR_UNSUPPORTED).
+ * of every document. head_dim 64 or 128.
  * softmax_scale <= 0 selects 1 / sqrt(d). Malformed cu_seqlens is reported
  * through the status word (ATTN_ERR_BAD_SEQLENS) and writes no gradient.
  * Source: FLAMIA section 1 (the forward and backward of the training call

@@ -1,5 +1,5 @@
-// attn_bwd.cu -- attention backward (dQ, dK, dV) for BF16 operands, d = 128, on
-// sm_103a (tcgen05 + TMEM + TMA).
+// attn_bwd.cu -- attention backward (dQ, dK, dV) for BF16 operands, d = 64 or
+// 128, on sm_103a (tcgen05 + TMEM + TMA).
 //
 // The gradients of softmax attention for an upstream gradient dO (FLAMIA
 // section 1: the training call is the forward plus a backward over the same
@@ -54,25 +54,35 @@
 namespace pa {
 
 namespace bwd {
-constexpr int D = 128;
-constexpr int TILE = 128 * D * 2;          // a bf16 row tile of 128 rows: two 16 KB 128-byte-swizzled atoms
 constexpr int SR = 64;                     // rows of a stream tile
-constexpr int XTILE = SR * D * 2;          // a stream tile: two 8 KB atoms
 constexpr int NS = 3;                      // stream-tile stages
 constexpr int PT = 128 * SR * 2;           // a P or dS operand: 128 rows x 64 bf16, one 128-byte swizzle atom
-constexpr int OFF_R = 0;                   // row tiles R0, R1
-constexpr int OFF_X = 2 * TILE;            // NS stages of the stream tiles X0, X1
-constexpr int OFF_P = OFF_X + NS * 2 * XTILE;     // two buffers of {P, dS}
-constexpr int OFF_VEC = OFF_P + 2 * 2 * PT;       // NS x {lse log2(e) [64], D [64]}
-constexpr int OFF_BAR = OFF_VEC + NS * 512;
-constexpr int SMEM = OFF_BAR + 512 + 1024;
 constexpr int THREADS = 64 + 256;
-// TMEM columns: the row tiles as the A operand of S and dP (bf16 pairs, column c of
-// a row holding channels 2c, 2c + 1), the one S/dP buffer, the accumulators
-constexpr uint32_t T_R0 = 0, T_R1 = 64, T_S = 128, T_DP = 192, T_O0 = 256, T_O1 = 384;
-using C = Cfg<2, D, MODE_BF16>;
-static_assert(C::TILE == TILE && C::ATOMS == 2, "bf16 d = 128 tiles are two 128-byte swizzle atoms");
-static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
+// TMEM columns: the one S/dP buffer and the accumulators (the row tiles: Lay)
+constexpr uint32_t T_R0 = 0, T_S = 128, T_DP = 192, T_O0 = 256, T_O1 = 384;
+
+// shared-memory layout and shapes for head dimension D (64 or 128); a row of D
+// bf16 channels is D / 64 atoms of the 128-byte swizzle
+template <int D>
+struct Lay {
+    static constexpr int ATOMS = D / 64;
+    static constexpr int TILE = 128 * D * 2;       // a row tile of 128 rows
+    static constexpr int XTILE = SR * D * 2;       // a stream tile
+    static constexpr int OFF_R = 0;                // row tiles R0, R1
+    static constexpr int OFF_X = 2 * TILE;         // NS stages of the stream tiles X0, X1
+    static constexpr int OFF_P = OFF_X + NS * 2 * XTILE;   // two buffers of {P, dS}
+    static constexpr int OFF_VEC = OFF_P + 2 * 2 * PT;     // NS x {lse log2(e) [64], D [64]}
+    static constexpr int OFF_BAR = OFF_VEC + NS * 512;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;
+    static constexpr int KS = D / 16;              // K steps of S and dP (16 channels each)
+    static constexpr int HD = D / 2;               // channels per warp half in the epilogue
+    // the row tiles in TMEM as the A operand of S and dP: bf16 pairs, column c of a
+    // row holding channels 2c, 2c + 1
+    static constexpr uint32_t T_R1 = D / 2;
+    static_assert(Cfg<2, D, MODE_BF16>::TILE == TILE && Cfg<2, D, MODE_BF16>::ATOMS == ATOMS,
+                  "row tiles as the forward's bf16 tiles");
+    static_assert(SMEM <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
+};
 
 struct Bars {
     uint64_t r_full, r_empty;   // the item's row tiles landed in shared memory / may be replaced
@@ -140,6 +150,7 @@ __device__ __forceinline__ Item decode(const BwdParams& p, int it) {
 
 // D = rowsum(dO o O) and lse log2(e) of every row, per (head, 128-token tile).
 // Grid (tiles_cap, H); eight warps, one row per warp at a time.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     pdl_trigger();
     pdl_wait();   // the document table
@@ -160,14 +171,22 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
         const int loc = 128 * lt + r;
         float dsum = 0.0f, l2 = 0.0f;
         if (loc < d.len) {
-            const long long base = ((long long)(d.start + loc) * p.H + h) * bwd::D + 4 * lane;
-            const uint2 a = *reinterpret_cast<const uint2*>(p.o + base);
-            const uint2 b = *reinterpret_cast<const uint2*>(p.dout + base);
-            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-            const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
-            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
-            dsum = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+            const long long base = ((long long)(d.start + loc) * p.H + h) * D + (D / 32) * lane;
+            if constexpr (D == 128) {
+                const uint2 a = *reinterpret_cast<const uint2*>(p.o + base);
+                const uint2 b = *reinterpret_cast<const uint2*>(p.dout + base);
+                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+                const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+                const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+                const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+                dsum = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+            } else {
+                const uint32_t a = *reinterpret_cast<const uint32_t*>(p.o + base);
+                const uint32_t b = *reinterpret_cast<const uint32_t*>(p.dout + base);
+                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+                const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
+                dsum = a0.x * b0.x + a0.y * b0.y;
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
             l2 = p.lse[(long long)h * p.T + d.start + loc] * 1.4426950408889634f;
@@ -179,6 +198,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdParams p) {
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(bwd::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -187,6 +207,10 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                     const BwdParams p) {
     // tm*: 128-row boxes (the row tiles); sx*: 64-row boxes (the stream tiles)
     using namespace bwd;
+    using L = Lay<D>;
+    constexpr int TILE = L::TILE, XTILE = L::XTILE, ATOMS = L::ATOMS;
+    constexpr int OFF_R = L::OFF_R, OFF_X = L::OFF_X, OFF_P = L::OFF_P, OFF_VEC = L::OFF_VEC, OFF_BAR = L::OFF_BAR;
+    constexpr uint32_t T_R1 = L::T_R1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* B = reinterpret_cast<Bars*>(sm + OFF_BAR);
@@ -252,7 +276,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(&B->r_full, 2 * TILE);
                 const int row = x.start + 128 * x.rt;
-                for (int a = 0; a < 2; a++) {
+                for (int a = 0; a < ATOMS; a++) {
                     tma_load_3d(sm + OFF_R + a * 16384, r0, &B->r_full, a * 64, x.head, row);
                     tma_load_3d(sm + OFF_R + TILE + a * 16384, r1, &B->r_full, a * 64, x.head, row);
                 }
@@ -269,7 +293,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                     const int row = x.start + SR * s64;
                     uint8_t* xs = sm + OFF_X + st * 2 * XTILE;
                     mbar_arrive_expect_tx(&B->x_full[st], 2 * XTILE + (x.kv ? 512 : 0));
-                    for (int a = 0; a < 2; a++) {
+                    for (int a = 0; a < ATOMS; a++) {
                         tma_load_3d(xs + a * (SR * 128), x0, &B->x_full[st], a * 64, x.head, row);
                         tma_load_3d(xs + XTILE + a * (SR * 128), x1, &B->x_full[st], a * 64, x.head, row);
                     }
@@ -318,12 +342,12 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 const uint64_t x0 = dxk + (gs % NS) * XST16, x1 = x0 + X1_16;
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; kk++) {
+                    for (int kk = 0; kk < L::KS; kk++) {
                         const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
                         mma_f16_ta(tmem + T_S, tmem + T_R0 + 8 * kk, x0 + xo, id_s, kk ? 1u : 0u);
                     }
 #pragma unroll
-                    for (int kk = 0; kk < 8; kk++) {
+                    for (int kk = 0; kk < L::KS; kk++) {
                         const uint64_t xo = (uint64_t)((kk >> 2) * (SR * 128) + (kk & 3) * 32) >> 4;
                         mma_f16_ta(tmem + T_DP, tmem + T_R1 + 8 * kk, x1 + xo, id_s, kk ? 1u : 0u);
                     }
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             if (ok) {
                 const uint8_t* rt = sm + OFF_R + gr * TILE + r * 128;
 #pragma unroll
-                for (int a = 0; a < 2; a++) {
+                for (int a = 0; a < ATOMS; a++) {
                     uint32_t w[32];
 #pragma unroll
                     for (int c8 = 0; c8 < 8; c8++) {
@@ -576,15 +600,15 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
             tc_fence_after();
             const int hh = gr;
             const bool store = rpos < x.len;
-            const long long row = ((long long)(x.start + (store ? rpos : 0)) * p.H + x.head) * D + 64 * hh;
+            const long long row = ((long long)(x.start + (store ? rpos : 0)) * p.H + x.head) * D + L::HD * hh;
             for (int which = 0; which < (x.kv ? 2 : 1); which++) {
                 // dK/dV role: dV (unscaled), then dK; dQ role: dQ
-                const uint32_t col = (which ? T_O1 : T_O0) + 64 * hh;
+                const uint32_t col = (which ? T_O1 : T_O0) + L::HD * hh;
                 const float f = (x.kv && which == 0) ? 1.0f : p.scale;
                 uint16_t* out = x.kv ? (which ? p.dk : p.dv) : p.dq;
                 const float2 f2 = make_float2(f, f);
 #pragma unroll
-                for (int cc = 0; cc < 2; cc++) {
+                for (int cc = 0; cc < L::HD / 32; cc++) {
                     uint32_t u[32];
                     tmem_ld32(tmem + lane_off + col + 32 * cc, u);
                     tmem_wait_ld();
@@ -617,22 +641,31 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
     if (threadIdx.x == 0 && *abort) atomicOr(&p.hdr->status, ST_TIMEOUT);
 }
 
-cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* dout, const BwdParams& p, int grid,
-                       cudaStream_t st) {
+template <int D>
+static cudaError_t launch_bwd_t(const void* q, const void* k, const void* v, const void* dout, const BwdParams& p,
+                                int grid, cudaStream_t st) {
     using namespace bwd;
-    if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
-    CUtensorMap m[8];
+    using L = Lay<D>;
+    CUtensorMap m[8];   // q, k, v, dO with 128-row boxes (the row tiles), then with 64-row boxes
     const void* base[4] = {q, k, v, dout};
     for (int i = 0; i < 8; i++)
         if (!make_tensor_map_3d(&m[i], base[i & 3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H, p.T, (uint64_t)D * 2,
                                 (uint64_t)p.H * D * 2, 64, i < 4 ? 128 : SR, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(bwd_prep_kernel, dim3((unsigned)p.tiles_cap, (unsigned)p.H), dim3(256), 0, st, p);
+    cudaError_t e = launch_pdl(bwd_prep_kernel<D>, dim3((unsigned)p.tiles_cap, (unsigned)p.H), dim3(256), 0, st, p);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_bwd_kernel, dim3(grid), dim3(THREADS), SMEM, st, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
-                      m[7], p);
+    return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(THREADS), L::SMEM, st, m[0], m[1], m[2], m[3], m[4], m[5],
+                      m[6], m[7], p);
+}
+
+cudaError_t launch_bwd(int D, const void* q, const void* k, const void* v, const void* dout, const BwdParams& p,
+                       int grid, cudaStream_t st) {
+    if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
+    if (D == 128) return launch_bwd_t<128>(q, k, v, dout, p, grid, st);
+    if (D == 64) return launch_bwd_t<64>(q, k, v, dout, p, grid, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

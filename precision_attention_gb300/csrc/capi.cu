@@ -451,7 +451,6 @@ attn_status attn_bf16_bwd(const void* q, const void* k, const void* v, const voi
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return ATTN_ERR_INVALID_ARG;
     if (!(softmax_scale <= 0.0f || std::isfinite(softmax_scale))) return ATTN_ERR_INVALID_ARG;
-    if (shape->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     size_t need = 0;
     attn_bwd_workspace_size(shape, &need);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
@@ -497,11 +496,12 @@ attn_status attn_bf16_bwd(const void* q, const void* k, const void* v, const voi
     bp.H = H;
     bp.nd = nd;
     bp.causal = causal != 0;
-    const double sc = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(128.0);
+    const double sc =
+        softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(static_cast<double>(shape->head_dim));
     bp.scale = static_cast<float>(sc);
     bp.C = static_cast<float>(sc * 1.4426950408889634);
     bp.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
-    const cudaError_t e = launch_bwd(q, k, v, dout, bp, grid, s);
+    const cudaError_t e = launch_bwd(shape->head_dim, q, k, v, dout, bp, grid, s);
     return e == cudaSuccess ? ATTN_OK : (e == cudaErrorInvalidValue ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_CUDA);
 }
 

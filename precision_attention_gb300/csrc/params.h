@@ -83,7 +83,7 @@ struct FwdParams {
     long long pdump_stride;
 };
 
-// The backward (BF16 operands, d = 128). Per-row vectors are kept per (head,
+// The backward (BF16 operands, d = 64 or 128). Per-row vectors are kept per (head,
 // 128-token tile) so that one tile's 128 values are one aligned 512-byte copy:
 // vec[0][h][tile][r] = lse log2(e), vec[1][h][tile][r] = rowsum(dO o O), tile =
 // DocEntry::toff + local tile, rows past the document's end 0.
@@ -91,12 +91,12 @@ struct BwdParams {
     const DocEntry* docs;
     const WorkItem* items;
     WsHeader* hdr;
-    const uint16_t* o;       // bf16 [T][H][128] (prep)
-    const uint16_t* dout;    // bf16 [T][H][128] (prep)
+    const uint16_t* o;       // bf16 [T][H][D] (prep)
+    const uint16_t* dout;    // bf16 [T][H][D] (prep)
     const float* lse;        // [H][T] natural log (prep)
     float* vec;              // [2][H][tiles_cap][128]
     long long tiles_cap;
-    uint16_t *dq, *dk, *dv;  // bf16 [T][H][128]
+    uint16_t *dq, *dk, *dv;  // bf16 [T][H][D]
     int T, H, nd, causal;
     float C;                 // softmax_scale * log2(e)
     float scale;             // softmax_scale
@@ -119,9 +119,10 @@ cudaError_t launch_vref(const VrefParams& p, cudaStream_t st);
 // 4 MXFP8 Q and K with one V exponent per token (the causal-exact MX mode); expm: the
 // probabilities' exponential (attn_exp_mode; the bit-level ones with modes 1 and 3 at D = 128)
 // the backward after its work list: the per-row vectors, then the gradient kernel
-// (q, k, v, dout: bf16 [T][H][128]; grid: CTAs of the persistent gradient kernel, even)
-cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* dout, const BwdParams& p, int grid,
-                       cudaStream_t st);
+// (q, k, v, dout: bf16 [T][H][D], D = 64 or 128; grid: CTAs of the persistent
+// gradient kernel, even)
+cudaError_t launch_bwd(int D, const void* q, const void* k, const void* v, const void* dout, const BwdParams& p,
+                       int grid, cudaStream_t st);
 cudaError_t launch_attn(int mode, int expm, int D, const void* q, const void* k, const void* v, const FwdParams& p,
                         int grid, cudaStream_t st);
 

@@ -315,7 +315,7 @@ def test_backward_arguments_rejected_on_host(pa):
         ptrs[i] = odd
         assert call(shape, ptrs) == pa.ATTN_ERR_INVALID_ARG, i
     assert call(shape, scale=float("nan")) == pa.ATTN_ERR_INVALID_ARG
-    assert call(pa._Shape(T, H, 64, 3, cu)) == pa.ATTN_ERR_UNSUPPORTED       # d = 128 only
+    assert call(pa._Shape(T, H, 96, 3, cu)) == pa.ATTN_ERR_UNSUPPORTED       # d = 64 or 128 only
     assert call(shape, nbytes=bwd - 256) == pa.ATTN_ERR_WORKSPACE
     assert call(shape, nbytes=fwd) == pa.ATTN_ERR_WORKSPACE                  # the forward's is too small
     assert call(shape, wsp=ctypes.c_void_p((1 << 24) + 128)) == pa.ATTN_ERR_WORKSPACE

@@ -23,6 +23,8 @@ and dK that no relative bound on that row can hold.
      a few rows, such as a wrong causal diagonal or a document boundary, that
      an RMSE over the whole tensor would dilute.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -38,6 +40,16 @@ pytestmark = pytest.mark.gpu
 REL_RMSE = 1e-2
 ROW_REL = 2e-2
 ROW_ABS_OF_RMS = 1e-2
+
+
+def _make(wid, heads, lengths):
+    """Seeded inputs of workload `wid` as bf16 values (workload 1, head_dim 64, is
+    fp32 in the forward's tests; the backward takes bf16)."""
+    inp = workloads.make(wid, heads=heads, lengths=lengths)
+    if inp.in_dtype != "bf16":
+        inp = dataclasses.replace(inp, q=workloads.bf16_round(inp.q), k=workloads.bf16_round(inp.k),
+                                  v=workloads.bf16_round(inp.v), in_dtype="bf16")
+    return inp
 
 
 def _dout(T, H, d, seed=77):
@@ -81,10 +93,12 @@ def _check_all(inp, do, causal, scale, got, o_used):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("lengths", [[700, 129, 1000], [1, 128, 129, 255]])
-def test_backward_against_fp64(causal, lengths):
-    """The chain a caller runs: attn_bf16_fwd, then attn_bf16_bwd on its o and lse."""
-    inp = workloads.make(2, heads=2, lengths=lengths)
+@pytest.mark.parametrize("wid,lengths", [(2, [700, 129, 1000]), (2, [1, 128, 129, 255]),
+                                         (1, [700, 129, 1000]), (1, [1, 64, 65, 255])])
+def test_backward_against_fp64(causal, wid, lengths):
+    """The chain a caller runs: attn_bf16_fwd, then attn_bf16_bwd on its o and lse
+    (head_dim 128: workload 2's normal inputs; head_dim 64: workload 1's)."""
+    inp = _make(wid, 2, lengths)
     T, H, d = inp.q.shape
     do = _dout(T, H, d)
     got, o_used = _run(inp, causal, do)
@@ -107,11 +121,12 @@ def test_backward_on_oracle_forward(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_deterministic_and_packed_equals_documents(causal):
+@pytest.mark.parametrize("wid", [2, 1])
+def test_backward_deterministic_and_packed_equals_documents(causal, wid):
     """Two calls give the same bits; each document of a packed batch gets the
     bits it gets alone (every tile is document-local, every sum has one order)."""
     lengths = [300, 0, 77, 129]
-    inp = workloads.make(2, heads=2, lengths=lengths)
+    inp = _make(wid, 2, lengths)
     q, k, v, cu = to_device(inp)
     T, H, d = q.shape
     do = torch.from_numpy(_dout(T, H, d)).to(torch.bfloat16).cuda()
