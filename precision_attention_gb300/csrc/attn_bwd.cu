@@ -488,98 +488,93 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
                 const float* vl = reinterpret_cast<const float*>(sm + OFF_VEC + st * 512);
                 const float* vd = vl + 64;
                 const uint32_t tb = tmem + lane_off + T_S;
-                uint32_t pk[32], dk[32];
-                // P = 2^(S c - lse log2 e), dS = P (dP - D), in pairs, 32 columns at a time;
-                // one branch-free unrolled loop per (role, masked) case
-                auto compute = [&](auto kv_c, auto mask_c, int h, const uint32_t (&us)[32], const uint32_t (&ud)[32]) {
-                    constexpr bool KV = decltype(kv_c)::value, MASK = decltype(mask_c)::value;
-#pragma unroll
-                    for (int u = 0; u < 32; u += 4) {
-                        const int col = 32 * h + u;
-                        float2 l01, l23, d01, d23;
-                        if constexpr (KV) {
-                            const float4 a = *reinterpret_cast<const float4*>(vl + col);
-                            const float4 bb = *reinterpret_cast<const float4*>(vd + col);
-                            l01 = make_float2(-a.x, -a.y);
-                            l23 = make_float2(-a.z, -a.w);
-                            d01 = make_float2(-bb.x, -bb.y);
-                            d23 = make_float2(-bb.z, -bb.w);
-                        } else {
-                            l01 = l23 = make_float2(-row_l2, -row_l2);
-                            d01 = d23 = make_float2(-row_d, -row_d);
-                        }
-                        const float2 x01 =
-                            __ffma2_rn(make_float2(__uint_as_float(us[u]), __uint_as_float(us[u + 1])), c2, l01);
-                        const float2 x23 =
-                            __ffma2_rn(make_float2(__uint_as_float(us[u + 2]), __uint_as_float(us[u + 3])), c2, l23);
-                        float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-                        float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-                        const float2 g01 =
-                            __fadd2_rn(make_float2(__uint_as_float(ud[u]), __uint_as_float(ud[u + 1])), d01);
-                        const float2 g23 =
-                            __fadd2_rn(make_float2(__uint_as_float(ud[u + 2]), __uint_as_float(ud[u + 3])), d23);
-                        float2 s01 = __fmul2_rn(p01, g01);
-                        float2 s23 = __fmul2_rn(p23, g23);
-                        if constexpr (MASK) {
-                            float* pp[4] = {&p01.x, &p01.y, &p23.x, &p23.y};
-                            float* ss[4] = {&s01.x, &s01.y, &s23.x, &s23.y};
-#pragma unroll
-                            for (int e = 0; e < 4; e++) {
-                                const int cpos = cbase + col + e;
-                                // dK/dV role: column = query, row = key; dQ role: the reverse
-                                const bool vis = cpos < x.len && (!p.causal || (KV ? cpos >= rpos : cpos <= rpos));
-                                *pp[e] = vis ? *pp[e] : 0.0f;
-                                *ss[e] = vis ? *ss[e] : 0.0f;
-                            }
-                        }
-                        if constexpr (KV) {
-                            pk[col / 2] = pack_bf16x2(p01.x, p01.y);
-                            pk[col / 2 + 1] = pack_bf16x2(p23.x, p23.y);
-                        }
-                        dk[col / 2] = pack_bf16x2(s01.x, s01.y);
-                        dk[col / 2 + 1] = pack_bf16x2(s23.x, s23.y);
-                    }
-                };
-                auto dispatch = [&](int h, const uint32_t (&us)[32], const uint32_t (&ud)[32]) {
-                    if (x.kv) {
-                        if (need_mask) compute(std::true_type{}, std::true_type{}, h, us, ud);
-                        else compute(std::true_type{}, std::false_type{}, h, us, ud);
-                    } else {
-                        if (need_mask) compute(std::false_type{}, std::true_type{}, h, us, ud);
-                        else compute(std::false_type{}, std::false_type{}, h, us, ud);
-                    }
-                };
+                // S and dP of all 64 columns first: the S/dP columns go back to the issuer
+                // before any arithmetic, so S and dP of step g + 1 can start at once
+                uint32_t us[64], ud[64];
                 {
-                    uint32_t us[32], ud[32];
-                    tmem_ld32(tb, us);
-                    tmem_ld32(tb + 64, ud);
-                    tmem_wait_ld();
-                    dispatch(0, us, ud);
+                    uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&us[0]);
+                    uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&us[32]);
+                    uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ud[0]);
+                    uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ud[32]);
+                    tmem_ld32(tb, s0);
+                    tmem_ld32(tb + 32, s1);
+                    tmem_ld32(tb + 64, d0);
+                    tmem_ld32(tb + 96, d1);
                 }
-                {
-                    uint32_t us[32], ud[32];
-                    tmem_ld32(tb + 32, us);
-                    tmem_ld32(tb + 96, ud);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&B->s_free[b]);   // the S/dP columns may take step g + 1
-                    dispatch(1, us, ud);
-                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&B->s_free[b]);   // the S/dP columns may take step g + 1
                 // the P/dS buffer was last read by the output MMAs of step g - 2
                 if (g >= 2 && !__all_sync(FULL, mbar_wait(&B->o_done[b], ((g - 2) >> 1) & 1, abort, lim))) {
                     ok = false;
                     break;
                 }
-                // the row -> shared memory (128-byte swizzled K-major rows of 64 columns)
                 uint8_t* pbuf = sm + OFF_P + b * 2 * PT;
+                // P = 2^(S c - lse log2 e), dS = P (dP - D), in pairs, 8 columns (one 16-byte
+                // chunk of each row) at a time, stored as they are formed into the 128-byte
+                // swizzled K-major rows; one branch-free unrolled loop per (role, masked) case
+                auto compute = [&](auto kv_c, auto mask_c) {
+                    constexpr bool KV = decltype(kv_c)::value, MASK = decltype(mask_c)::value;
 #pragma unroll
-                for (int cc = 0; cc < 8; cc++) {
-                    const int off = r * 128 + ((cc ^ (r & 7)) << 4);
-                    if (x.kv)
-                        *reinterpret_cast<uint4*>(pbuf + off) =
-                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-                    *reinterpret_cast<uint4*>(pbuf + PT + off) =
-                        make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
+                    for (int cc = 0; cc < 8; cc++) {
+                        uint32_t pw[4], dw[4];
+#pragma unroll
+                        for (int v = 0; v < 8; v += 4) {
+                            const int col = 8 * cc + v;
+                            float2 l01, l23, d01, d23;
+                            if constexpr (KV) {
+                                const float4 a = *reinterpret_cast<const float4*>(vl + col);
+                                const float4 bb = *reinterpret_cast<const float4*>(vd + col);
+                                l01 = make_float2(-a.x, -a.y);
+                                l23 = make_float2(-a.z, -a.w);
+                                d01 = make_float2(-bb.x, -bb.y);
+                                d23 = make_float2(-bb.z, -bb.w);
+                            } else {
+                                l01 = l23 = make_float2(-row_l2, -row_l2);
+                                d01 = d23 = make_float2(-row_d, -row_d);
+                            }
+                            const float2 x01 = __ffma2_rn(
+                                make_float2(__uint_as_float(us[col]), __uint_as_float(us[col + 1])), c2, l01);
+                            const float2 x23 = __ffma2_rn(
+                                make_float2(__uint_as_float(us[col + 2]), __uint_as_float(us[col + 3])), c2, l23);
+                            float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+                            float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+                            const float2 g01 = __fadd2_rn(
+                                make_float2(__uint_as_float(ud[col]), __uint_as_float(ud[col + 1])), d01);
+                            const float2 g23 = __fadd2_rn(
+                                make_float2(__uint_as_float(ud[col + 2]), __uint_as_float(ud[col + 3])), d23);
+                            float2 s01 = __fmul2_rn(p01, g01);
+                            float2 s23 = __fmul2_rn(p23, g23);
+                            if constexpr (MASK) {
+                                float* pp[4] = {&p01.x, &p01.y, &p23.x, &p23.y};
+                                float* ss[4] = {&s01.x, &s01.y, &s23.x, &s23.y};
+#pragma unroll
+                                for (int e = 0; e < 4; e++) {
+                                    const int cpos = cbase + col + e;
+                                    // dK/dV role: column = query, row = key; dQ role: the reverse
+                                    const bool vis =
+                                        cpos < x.len && (!p.causal || (KV ? cpos >= rpos : cpos <= rpos));
+                                    *pp[e] = vis ? *pp[e] : 0.0f;
+                                    *ss[e] = vis ? *ss[e] : 0.0f;
+                                }
+                            }
+                            pw[v / 2] = pack_bf16x2(p01.x, p01.y);
+                            pw[v / 2 + 1] = pack_bf16x2(p23.x, p23.y);
+                            dw[v / 2] = pack_bf16x2(s01.x, s01.y);
+                            dw[v / 2 + 1] = pack_bf16x2(s23.x, s23.y);
+                        }
+                        const int off = r * 128 + ((cc ^ (r & 7)) << 4);
+                        if constexpr (KV)
+                            *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        *reinterpret_cast<uint4*>(pbuf + PT + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+                    }
+                };
+                if (x.kv) {
+                    if (need_mask) compute(std::true_type{}, std::true_type{});
+                    else compute(std::true_type{}, std::false_type{});
+                } else {
+                    if (need_mask) compute(std::false_type{}, std::true_type{});
+                    else compute(std::false_type{}, std::false_type{});
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
