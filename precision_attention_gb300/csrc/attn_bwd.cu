@@ -125,8 +125,8 @@ struct Item {
 };
 __device__ __forceinline__ Item decode(const BwdParams& p, int it) {
     Item x;
-    x.kv = ((it & 1) ^ ((it / (int)gridDim.x) & 1)) == 0;
-    const WorkItem w = p.items[it >> 1];
+    x.kv = p.kv_only || ((it & 1) ^ ((it / (int)gridDim.x) & 1)) == 0;
+    const WorkItem w = p.items[p.kv_only ? it : it >> 1];
     const DocEntry d = p.docs[w.doc];
     const int nt = (d.len + 127) >> 7, n64 = (d.len + 63) >> 6;
     x.head = w.head;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = B->tmem_base;
     pdl_wait();   // the work list and the per-row vectors
-    const int n_items = 2 * p.hdr->n_items;
+    const int n_items = (p.kv_only ? 1 : 2) * p.hdr->n_items;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -636,6 +636,337 @@ __global__ void __launch_bounds__(bwd::THREADS, 1)
     if (threadIdx.x == 0 && *abort) atomicOr(&p.hdr->status, ST_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// dQ in its own kernel, 128 keys per step. With only one accumulator (dQ), TMEM
+// holds the item's Q and dO tiles as the A operand [0, D), S [128,256) and dP
+// [256,384) at N = 128, and dQ [384, 384 + D): S and dP take half the MMA
+// instructions per FLOP of the 64-row steps above, which the issuing thread is
+// bound by. Warp 0 streams the K and V tiles of each key tile (2 stages), warp 1
+// issues (S and dP of the next step ahead of dQ += dS K of this one), warps 2-9
+// form dS for 64 of the 128 keys each (two warps per TMEM lane quarter) into one
+// of two shared-memory dS buffers, and together the epilogue.
+namespace bwdq {
+constexpr int NS = 2;
+constexpr int DST = 128 * 128 * 2;   // dS: 128 query rows x 128 keys, two 128-byte swizzle atoms
+template <int D>
+struct Lay {
+    static constexpr int ATOMS = D / 64;
+    static constexpr int XT = 128 * D * 2;               // a 128-row K or V tile
+    static constexpr int OFF_X = 0;                      // NS stages of {K, V}
+    static constexpr int OFF_DS = OFF_X + NS * 2 * XT;   // two dS buffers
+    static constexpr int OFF_BAR = OFF_DS + 2 * DST;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;
+    static constexpr int KS = D / 16;                    // K steps of S and dP
+    static constexpr int HD = D / 2;                     // dQ channels per warp half
+    static constexpr uint32_t T_Q = 0, T_DO = D / 2, T_S = 128, T_DP = 256, T_DQ = 384;
+    static_assert(SMEM <= 227 * 1024, "dQ kernel shared memory exceeds the per-CTA limit");
+};
+struct Bars {
+    uint64_t r_tmem;                 // Q and dO of the item in TMEM (256 arrivals)
+    uint64_t x_full[NS], x_empty[NS];
+    uint64_t s_full;                 // S and dP of a step in TMEM
+    uint64_t s_free;                 // loaded by the elementwise warps (256 arrivals)
+    uint64_t p_full[2];              // dS of the step in shared-memory buffer b (256 arrivals)
+    uint64_t o_done[2];              // the step's dQ MMAs, readers of dS buffer b, completed
+    uint64_t epi_done;               // the item's dQ was read (256 arrivals)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Bars) <= 512, "dQ kernel barrier block exceeds its reserved space");
+}  // namespace bwdq
+
+template <int D>
+__global__ void __launch_bounds__(bwd::THREADS, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       const BwdParams p) {
+    using namespace bwdq;
+    using L = Lay<D>;
+    constexpr unsigned FULL = 0xFFFFFFFFu;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* B = reinterpret_cast<Bars*>(sm + L::OFF_BAR);
+    volatile int* abort = &B->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long lim = p.wait_limit;
+    if (threadIdx.x == 0) {
+        mbar_init(&B->r_tmem, 256);
+        for (int i = 0; i < NS; i++) {
+            mbar_init(&B->x_full[i], 1);
+            mbar_init(&B->x_empty[i], 1);
+        }
+        mbar_init(&B->s_full, 1);
+        mbar_init(&B->s_free, 256);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&B->p_full[i], 256);
+            mbar_init(&B->o_done[i], 1);
+        }
+        mbar_init(&B->epi_done, 256);
+        mbar_init(&B->drain, 1);
+        B->abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&B->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem_base;
+    pdl_wait();   // the work list and the per-row vectors
+    const int n_items = p.hdr->n_items;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int issued[NS];
+        for (int i = 0; i < NS; i++) issued[i] = -1;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const WorkItem w = p.items[it];
+            const DocEntry d = p.docs[w.doc];
+            for (int t = 0; t < w.ntiles; t++, g++) {
+                const int st = g % NS;
+                if (!__all_sync(FULL, mbar_wait(&B->x_empty[st], ((g / NS) & 1) ^ 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                issued[st] = (g / NS) & 1;
+                if (lane == 0) {
+                    uint8_t* xs = sm + L::OFF_X + st * 2 * L::XT;
+                    mbar_arrive_expect_tx(&B->x_full[st], 2 * L::XT);
+                    for (int a = 0; a < L::ATOMS; a++) {
+                        tma_load_3d(xs + a * 16384, &tmk, &B->x_full[st], a * 64, w.head, d.start + 128 * t);
+                        tma_load_3d(xs + L::XT + a * 16384, &tmv, &B->x_full[st], a * 64, w.head, d.start + 128 * t);
+                    }
+                }
+            }
+        }
+        if (*abort && lane == 0)
+            for (int s2 = 0; s2 < NS; s2++)
+                if (issued[s2] >= 0) wait_drain(&B->x_full[s2], (uint32_t)issued[s2], kDrainLimit);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (warp-wide loop)
+        const bool leader = lane == 0;
+        constexpr uint32_t id_s = idesc(1, 1, false, false, 128, 128);   // A from TMEM, K-major B, N = 128
+        constexpr uint32_t id_o = idesc(1, 1, false, true, 128, D);      // K-major A (dS), MN-major B (K)
+        const uint32_t sX = smem_u32(sm + L::OFF_X), sD = smem_u32(sm + L::OFF_DS);
+        const uint64_t dk0 = desc_kmajor<2, D, MODE_BF16>(sX, 0);        // K (and V) as the K-major B of S, dP
+        const uint64_t dkm = desc_v<2, D, MODE_BF16>(sX, 0);             // K as the MN-major B of dQ
+        const uint64_t dsa = desc_p<2>(sD, 0);                            // dS as the K-major A of dQ
+        constexpr uint64_t XST16 = (uint64_t)(2 * L::XT) >> 4, V16 = (uint64_t)L::XT >> 4, DS16 = (uint64_t)DST >> 4;
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(FULL, mbar_wait(bar, parity, abort, lim));
+        };
+        uint32_t g = 0, gs = 0;
+        int qi = 0;
+        bool ok = true;
+        auto try_issue_s = [&]() -> bool {
+            if (!wait_all(&B->x_full[gs % NS], (gs / NS) & 1)) return false;
+            if (gs >= 1 && !wait_all(&B->s_free, (gs - 1) & 1)) return false;   // S, dP of gs - 1 loaded
+            tc_fence_after();
+            const uint64_t bk = dk0 + (gs % NS) * XST16, bv = bk + V16;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < L::KS; kk++)
+                    mma_f16_ta(tmem + L::T_S, tmem + L::T_Q + 8 * kk, bk + koff<2, D, MODE_BF16>(kk), id_s, kk ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < L::KS; kk++)
+                    mma_f16_ta(tmem + L::T_DP, tmem + L::T_DO + 8 * kk, bv + koff<2, D, MODE_BF16>(kk), id_s,
+                               kk ? 1u : 0u);
+                tc_commit(&B->s_full);
+            }
+            __syncwarp();
+            gs++;
+            return true;
+        };
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
+            const WorkItem w = p.items[it];
+            if (!wait_all(&B->r_tmem, qi & 1)) break;
+            const uint32_t g_end = g + w.ntiles;
+            for (int t = 0; t < w.ntiles && ok; t++, g++) {
+                while (ok && gs < g_end && gs <= g + 1) ok = try_issue_s();
+                if (!ok) break;
+                if (!wait_all(&B->p_full[g & 1], (g >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (t == 0 && qi > 0 && !wait_all(&B->epi_done, (qi - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t a0 = dsa + (g & 1) * DS16, bk = dkm + (g % NS) * XST16;
+                const uint32_t acc0 = t ? 1u : 0u;
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++)   // dQ += dS K, 16 keys per step
+                        mma_f16(tmem + L::T_DQ, a0 + poff(kk), bk + voff<2, D, MODE_BF16>(kk), id_o, kk ? 1u : acc0);
+                    tc_commit(&B->x_empty[g % NS]);
+                    tc_commit(&B->o_done[g & 1]);
+                }
+                __syncwarp();
+            }
+        }
+        if (leader) {
+            tc_commit(&B->drain);
+            wait_drain(&B->drain, 0, kDrainLimit);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ elementwise + epilogue
+        const int hh = (warp - 2) >> 2;                  // key half (64 of the 128 keys)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;               // query row of the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float2 c2 = make_float2(p.C, p.C);
+        uint32_t g = 0;
+        int qi = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, qi++) {
+            const WorkItem w = p.items[it];
+            const DocEntry d = p.docs[w.doc];
+            const int rt = w.qtile, len = d.len;
+            const int rpos = 128 * rt + r;
+            const long long vi = ((long long)w.head * p.tiles_cap + d.toff + rt) * 128 + r;
+            const float row_l2 = p.vec[vi];
+            const float row_d = p.vec[vi + (long long)p.H * p.tiles_cap * 128];
+            // Q (half 0) or dO (half 1) of this row into TMEM; rows past the document's end
+            // are zero. Every MMA of the previous item has completed (its epilogue waited).
+            {
+                const uint16_t* src = hh ? p.dout : p.q;
+                const bool in_doc = rpos < len;
+                const uint4* row4 =
+                    reinterpret_cast<const uint4*>(src + ((long long)(d.start + (in_doc ? rpos : 0)) * p.H + w.head) * D);
+#pragma unroll
+                for (int a = 0; a < L::ATOMS; a++) {
+                    uint32_t wv[32];
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; c8++) {
+                        const uint4 v4 = in_doc ? __ldg(row4 + 8 * a + c8) : make_uint4(0, 0, 0, 0);
+                        wv[4 * c8] = v4.x;
+                        wv[4 * c8 + 1] = v4.y;
+                        wv[4 * c8 + 2] = v4.z;
+                        wv[4 * c8 + 3] = v4.w;
+                    }
+                    tmem_st32(tmem + lane_off + (hh ? L::T_DO : L::T_Q) + 32 * a, wv);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&B->r_tmem);
+            }
+            for (int t = 0; t < w.ntiles && ok; t++, g++) {
+                const int b = g & 1;
+                if (!__all_sync(FULL, mbar_wait(&B->s_full, g & 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t us[64], ud[64];
+                {
+                    uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&us[0]);
+                    uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&us[32]);
+                    uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ud[0]);
+                    uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&ud[32]);
+                    tmem_ld32(tmem + lane_off + L::T_S + 64 * hh, s0);
+                    tmem_ld32(tmem + lane_off + L::T_S + 64 * hh + 32, s1);
+                    tmem_ld32(tmem + lane_off + L::T_DP + 64 * hh, d0);
+                    tmem_ld32(tmem + lane_off + L::T_DP + 64 * hh + 32, d1);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&B->s_free);
+                if (g >= 2 && !__all_sync(FULL, mbar_wait(&B->o_done[b], ((g - 2) >> 1) & 1, abort, lim))) {
+                    ok = false;
+                    break;
+                }
+                const int kbase = 128 * t + 64 * hh;            // document-local key of column 0 of this half
+                const bool need_mask = (p.causal && t == rt) || (128 * t + 128 > len);
+                uint8_t* dsb = sm + L::OFF_DS + b * DST + hh * 16384;
+                // dS = 2^(S c - lse log2 e) (dP - D), 8 keys (one 16-byte chunk) at a time
+                auto compute = [&](auto mask_c) {
+                    constexpr bool MASK = decltype(mask_c)::value;
+                    const float2 l2 = make_float2(-row_l2, -row_l2), dd = make_float2(-row_d, -row_d);
+#pragma unroll
+                    for (int cc = 0; cc < 8; cc++) {
+                        uint32_t dw[4];
+#pragma unroll
+                        for (int v = 0; v < 8; v += 2) {
+                            const int col = 8 * cc + v;
+                            const float2 x2 = __ffma2_rn(
+                                make_float2(__uint_as_float(us[col]), __uint_as_float(us[col + 1])), c2, l2);
+                            float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                            const float2 g2 = __fadd2_rn(
+                                make_float2(__uint_as_float(ud[col]), __uint_as_float(ud[col + 1])), dd);
+                            float2 s2 = __fmul2_rn(p2, g2);
+                            if constexpr (MASK) {
+                                const int k0 = kbase + col;
+                                const bool v0 = k0 < len && (!p.causal || k0 <= rpos);
+                                const bool v1 = k0 + 1 < len && (!p.causal || k0 + 1 <= rpos);
+                                s2.x = v0 ? s2.x : 0.0f;
+                                s2.y = v1 ? s2.y : 0.0f;
+                            }
+                            dw[v / 2] = pack_bf16x2(s2.x, s2.y);
+                        }
+                        *reinterpret_cast<uint4*>(dsb + r * 128 + ((cc ^ (r & 7)) << 4)) =
+                            make_uint4(dw[0], dw[1], dw[2], dw[3]);
+                    }
+                };
+                if (need_mask) compute(std::true_type{});
+                else compute(std::false_type{});
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&B->p_full[b]);
+            }
+            // epilogue: every thread has waited on each earlier phase of the last step's
+            // o_done barrier; the barrier below gives all threads one exit decision
+            if (ok && !__all_sync(FULL, mbar_wait(&B->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, lim)))
+                ok = false;
+            if (named_bar_or(1, 256, !ok || *abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool store = rpos < len;
+            const long long row = ((long long)(d.start + (store ? rpos : 0)) * p.H + w.head) * D + L::HD * hh;
+            const float2 f2 = make_float2(p.scale, p.scale);
+#pragma unroll
+            for (int cc = 0; cc < L::HD / 32; cc++) {
+                uint32_t u[32];
+                tmem_ld32(tmem + lane_off + L::T_DQ + L::HD * hh + 32 * cc, u);
+                tmem_wait_ld();
+                uint32_t pkd[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; i2++) {
+                    const float2 v2 =
+                        __fmul2_rn(make_float2(__uint_as_float(u[2 * i2]), __uint_as_float(u[2 * i2 + 1])), f2);
+                    pkd[i2] = pack_bf16x2(v2.x, v2.y);
+                }
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.dq + row + 32 * cc);
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; i2++)
+                        dst[i2] = make_uint4(pkd[4 * i2], pkd[4 * i2 + 1], pkd[4 * i2 + 2], pkd[4 * i2 + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&B->epi_done);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && *abort) atomicOr(&p.hdr->status, ST_TIMEOUT);
+}
+
 template <int D>
 static cudaError_t launch_bwd_t(const void* q, const void* k, const void* v, const void* dout, const BwdParams& p,
                                 int grid, cudaStream_t st) {
@@ -651,8 +982,14 @@ static cudaError_t launch_bwd_t(const void* q, const void* k, const void* v, con
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(THREADS), L::SMEM, st, m[0], m[1], m[2], m[3], m[4], m[5],
-                      m[6], m[7], p);
+    BwdParams pk = p;
+    pk.kv_only = 1;   // dK, dV here; dQ in the kernel after it
+    e = launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(THREADS), L::SMEM, st, m[0], m[1], m[2], m[3], m[4], m[5],
+                   m[6], m[7], pk);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bwdq::Lay<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_bwd_dq_kernel<D>, dim3(grid), dim3(THREADS), bwdq::Lay<D>::SMEM, st, m[1], m[2], p);
 }
 
 cudaError_t launch_bwd(int D, const void* q, const void* k, const void* v, const void* dout, const BwdParams& p,

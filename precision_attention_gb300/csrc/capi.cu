@@ -484,6 +484,7 @@ attn_status attn_bf16_bwd(const void* q, const void* k, const void* v, const voi
     bp.docs = sp.docs;
     bp.items = sp.items;
     bp.hdr = sp.hdr;
+    bp.q = static_cast<const uint16_t*>(q);
     bp.o = static_cast<const uint16_t*>(o);
     bp.dout = static_cast<const uint16_t*>(dout);
     bp.lse = lse;

@@ -91,6 +91,7 @@ struct BwdParams {
     const DocEntry* docs;
     const WorkItem* items;
     WsHeader* hdr;
+    const uint16_t* q;       // bf16 [T][H][D] (the dQ kernel's row tiles)
     const uint16_t* o;       // bf16 [T][H][D] (prep)
     const uint16_t* dout;    // bf16 [T][H][D] (prep)
     const float* lse;        // [H][T] natural log (prep)
@@ -101,6 +102,7 @@ struct BwdParams {
     float C;                 // softmax_scale * log2(e)
     float scale;             // softmax_scale
     long long wait_limit;
+    int kv_only;             // 1: the gradient kernel takes only the dK/dV role (dQ has its own kernel)
 };
 
 // host: a 3-D tiled tensor map over [d2][d1][d0] (d0 contiguous), box (box0, 1, box2)
