@@ -525,7 +525,7 @@ def time_bwd(pa, torch, dev, n=10, B=2, H=32, N=8192, causals=(False, True), war
             "ms": ms, "tflops": tf, "frac_vs_bf16_measured": tf / bf16_peak, "status": st}
         del o, lse
     out.update({"config": {"batch": B, "heads": H, "seq_len": N, "head_dim": d, "dtype": "bf16"},
-                "kernels": "sched_kernel, bwd_prep_kernel, attn_bwd_kernel (three launches per call)",
+                "kernels": "sched_kernel, bwd_prep_kernel, attn_bwd_kernel (dK, dV), attn_bwd_dq_kernel (dQ): four launches per call",
                 "flops": "2.5 x forward FLOPs (causal halved)", "bf16_peak": bf16_peak,
                 "bf16_peak_basis": "MEASURED_PEAKS.json bf16_tflops (burst)" if pk else "fallback"})
     return out
