@@ -10,13 +10,15 @@
 // Causal masks and packed documents follow the forward: keys after the query
 // and tokens of other documents get P = 0; every tile is document-local.
 //
-// Two launches after the work-list pass (the forward's one-query-tile list):
+// Three launches after the work-list pass (the forward's one-query-tile list),
+// each a programmatic dependent of the one before:
 //   bwd_prep_kernel  D and lse log2(e) per row, stored per (head, 128-token
-//                    tile) so the gradient kernel fetches the values of a run
+//                    tile) so the gradient kernels fetch the values of a run
 //                    of rows with one bulk copy
-//   attn_bwd_kernel  persistent; the work items alternate between two roles,
-//                    both for one (document, head, 128-token row tile), each a
-//                    loop over 64-row stream tiles:
+//   attn_bwd_kernel  persistent, in its dK/dV role (kv_only = 1; with
+//                    kv_only = 0 its work items alternate between the two
+//                    roles below), both for one (document, head, 128-token row
+//                    tile), each a loop over 64-row stream tiles:
 //     dK/dV role   key tile j: K_j and V_j once, then each 64-query tile i that
 //                  sees it: S^T = K_j Q_i^T and dP^T = V_j dO_i^T into TMEM,
 //                  P^T and dS^T in registers, stored as bf16 into shared
@@ -27,6 +29,8 @@
 //   dQ is formed in its own role (S and dP computed a second time) rather than
 //   accumulated across key tiles with atomics, so the gradients are
 //   deterministic: one fixed summation order per output element.
+//   attn_bwd_dq_kernel  the dQ role with 128-key steps (below), the form the
+//                    library launches after the dK/dV pass
 // Warp roles: warp 0 TMA producer (the item's two row tiles, then the two
 // stream tiles of each step, and in the dK/dV role the step's 64 lse and D
 // values, into a 3-stage ring); warp 1 TMEM owner and MMA issuer; warps 2-9
